@@ -1,0 +1,298 @@
+/*
+ * Plain float64 CPU oracle for the block-sparse FlexAttention forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file: only the tests, the package's smoke check and the bench's
+ * CPU-baseline leg do.  It shares no code, header or constant table with the
+ * CUDA library; the mask and score kinds are numbered like the C-ABI enums so
+ * that the same integers can be passed to both.
+ *
+ * What it computes, written out as the plain definition (no tiling, no
+ * online softmax, no reordering):
+ *
+ *   mask_mod (b,h,q,kv)  -> bool        "Performance for templated attention
+ *       strangely bad for a combination of causal + upper square mask"
+ *       (PyTorch issue #124369), the mask written with torch.where: a masked
+ *       score becomes -inf; the causal + upper-square predicate is
+ *       (q <= P and kv <= P) or (q >= kv) with inclusive bounds.
+ *   score_mod(t,b,h,q,kv) -> t'         "[Inductor][Flex Attention] Add
+ *       Subtiling Option for Alpha Scaling" (PyTorch PR #167356), the
+ *       flex_attention higher-order op: scale is its own argument and the
+ *       score_mod graph acts on the scaled score QK^T*scale.
+ *   attention            -> out, lse    softmax over kv of the masked,
+ *       modified scores, times V, plus the per-row log-sum-exp
+ *       (OUTPUT_LOGSUMEXP in the same op's options); a row with no
+ *       unmasked score gives out = 0 and lse = -inf (the guard that the
+ *       ROWS_GUARANTEED_SAFE option lets a caller skip).
+ *   block mask           -> kv_num_blocks, kv_indices, full_kv_num_blocks,
+ *       full_kv_indices   (the BlockMask tuple passed to the same op): each
+ *       BLOCK x BLOCK tile of the dense mask is full (all true), partial
+ *       (some true) or empty; each row of an index tensor lists the selected
+ *       kv blocks in ascending order followed by the unselected ones, also
+ *       ascending (a stable descending sort of the 0/1 tile row).
+ *
+ * Inputs are float32 arrays holding the exact values the device reads
+ * (bf16 values are exact in float32); every product and sum is taken in
+ * double.
+ *
+ * Parity pins: see the tests (textbook attention through a library routine,
+ * closed-form block counts, ALiBi and softcap closed forms, brute force on
+ * tiny shapes).  No function here is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define OR_MASK_CAUSAL 0
+#define OR_MASK_SLIDING_WINDOW 1
+#define OR_MASK_CAUSAL_PREFIX 2
+#define OR_MASK_DOCUMENT 3
+#define OR_MASK_ALL 4
+
+#define OR_SCORE_IDENTITY 0
+#define OR_SCORE_SOFTCAP 1
+#define OR_SCORE_ALIBI 2
+
+#define OR_OK 0
+#define OR_ERR_ARG -1
+#define OR_ERR_NOMEM -2
+
+typedef struct {
+    int kind;
+    int window;            /* sliding window W: keep 0 <= q - kv < W      */
+    int prefix;            /* prefix P: (q <= P and kv <= P) or q >= kv    */
+    const int32_t *doc;    /* [B, len] document id of every position      */
+    int64_t doc_len;
+} or_mask;
+
+/* mask_mod(b, h, q, kv): the enumerated predicates. */
+static int or_mask_mod(const or_mask *m, int64_t b, int64_t h, int64_t q, int64_t kv)
+{
+    (void)h;
+    switch (m->kind) {
+    case OR_MASK_CAUSAL:
+        return q >= kv;
+    case OR_MASK_SLIDING_WINDOW:
+        return q >= kv && (q - kv) < (int64_t)m->window;
+    case OR_MASK_CAUSAL_PREFIX:
+        return (q <= (int64_t)m->prefix && kv <= (int64_t)m->prefix) || q >= kv;
+    case OR_MASK_DOCUMENT:
+        return m->doc[b * m->doc_len + q] == m->doc[b * m->doc_len + kv] && q >= kv;
+    case OR_MASK_ALL:
+        return 1;
+    default:
+        return 0;
+    }
+}
+
+/* score_mod(t, b, h, q, kv) applied to the scaled score t = scale * q.k */
+static double or_score_mod(int kind, double param, double t, int64_t h, int64_t H,
+                           int64_t q, int64_t kv)
+{
+    switch (kind) {
+    case OR_SCORE_SOFTCAP:
+        return param * tanh(t / param);
+    case OR_SCORE_ALIBI: {
+        /* slope_h = 2^(-8 (h+1) / H), h counted from 0 */
+        double slope = pow(2.0, -8.0 * (double)(h + 1) / (double)H);
+        return t - slope * (double)(q - kv);
+    }
+    default:
+        return t;
+    }
+}
+
+static int or_mask_ok(int kind)
+{
+    return kind >= OR_MASK_CAUSAL && kind <= OR_MASK_ALL;
+}
+
+/*
+ * Dense mask evaluated tile by tile; one BLOCK-row band of the mask is
+ * materialised at a time to bound memory.  Output layouts:
+ *   kv_num, full_num : [B, H, NQB]
+ *   kv_idx, full_idx : [B, H, NQB, NKVB]
+ */
+int oracle_block_mask(int kind, int window, int prefix, const int32_t *doc,
+                      int B, int H, int q_len, int kv_len, int block,
+                      int32_t *kv_num, int32_t *kv_idx,
+                      int32_t *full_num, int32_t *full_idx)
+{
+    if (!or_mask_ok(kind) || B <= 0 || H <= 0 || q_len <= 0 || kv_len <= 0 || block <= 0)
+        return OR_ERR_ARG;
+    if (q_len % block || kv_len % block)
+        return OR_ERR_ARG;
+    if (kind == OR_MASK_DOCUMENT && (doc == NULL || q_len != kv_len))
+        return OR_ERR_ARG;
+    const int64_t nqb = q_len / block, nkvb = kv_len / block;
+    or_mask m = {kind, window, prefix, doc, (int64_t)q_len};
+    int err = OR_OK;
+
+#pragma omp parallel for collapse(2) schedule(dynamic)
+    for (int64_t bh = 0; bh < (int64_t)B * H; ++bh) {
+        for (int64_t qb = 0; qb < nqb; ++qb) {
+            int64_t b = bh / H, h = bh % H;
+            /* the dense mask of rows [qb*block, (qb+1)*block) */
+            unsigned char *band = (unsigned char *)malloc((size_t)block * (size_t)kv_len);
+            int64_t *count = (int64_t *)calloc((size_t)nkvb, sizeof(int64_t));
+            if (!band || !count) {
+                free(band);
+                free(count);
+#pragma omp atomic write
+                err = OR_ERR_NOMEM;
+                continue;
+            }
+            for (int64_t r = 0; r < block; ++r)
+                for (int64_t kv = 0; kv < kv_len; ++kv)
+                    band[r * kv_len + kv] = (unsigned char)or_mask_mod(&m, b, h, qb * block + r, kv);
+            for (int64_t r = 0; r < block; ++r)
+                for (int64_t kv = 0; kv < kv_len; ++kv)
+                    count[kv / block] += band[r * kv_len + kv];
+
+            const int64_t all = (int64_t)block * block;
+            const int64_t row = bh * nqb + qb;
+            int32_t *pi = kv_idx + row * nkvb, *fi = full_idx + row * nkvb;
+            int32_t np = 0, nf = 0;
+            /* selected blocks first, ascending */
+            for (int64_t j = 0; j < nkvb; ++j) {
+                if (count[j] > 0 && count[j] < all) pi[np++] = (int32_t)j;
+                if (count[j] == all) fi[nf++] = (int32_t)j;
+            }
+            kv_num[row] = np;
+            full_num[row] = nf;
+            /* then the unselected ones, ascending */
+            int32_t tp = np, tf = nf;
+            for (int64_t j = 0; j < nkvb; ++j) {
+                if (!(count[j] > 0 && count[j] < all)) pi[tp++] = (int32_t)j;
+                if (count[j] != all) fi[tf++] = (int32_t)j;
+            }
+            free(band);
+            free(count);
+        }
+    }
+    return err;
+}
+
+/*
+ * One output row (b, h, i):
+ *   S[j] = mask_mod(b,h,i,j) ? score_mod(scale * sum_d q[i,d] k[j,d]) : -inf
+ *   no unmasked j          -> out = 0, lse = -inf
+ *   else  mx = max_j S[j], Z = sum_j exp(S[j] - mx), lse = mx + ln Z,
+ *         out[d] = sum_j exp(S[j] - lse) v[j,d]
+ */
+static void or_row(const float *q, const float *k, const float *v,
+                   int64_t H, int64_t s_kv, int64_t D, const or_mask *m,
+                   int score_kind, double score_param, double scale,
+                   int64_t b, int64_t h, int64_t i,
+                   double *srow, unsigned char *mrow, double *out, double *lse)
+{
+    const float *qi = q + i * D;
+    int any = 0;
+    for (int64_t j = 0; j < s_kv; ++j) {
+        mrow[j] = (unsigned char)or_mask_mod(m, b, h, i, j);
+        any |= mrow[j];
+        double dot = 0.0;
+        const float *kj = k + j * D;
+        for (int64_t d = 0; d < D; ++d)
+            dot += (double)qi[d] * (double)kj[d];
+        double t = or_score_mod(score_kind, score_param, scale * dot, h, H, i, j);
+        srow[j] = mrow[j] ? t : -INFINITY;
+    }
+    if (!any) {
+        for (int64_t d = 0; d < D; ++d)
+            out[d] = 0.0;
+        *lse = -INFINITY;
+        return;
+    }
+    double mx = -INFINITY;
+    for (int64_t j = 0; j < s_kv; ++j)
+        if (mrow[j] && srow[j] > mx) mx = srow[j];
+    double Z = 0.0;
+    for (int64_t j = 0; j < s_kv; ++j)
+        if (mrow[j]) Z += exp(srow[j] - mx);
+    const double L = mx + log(Z);
+    for (int64_t d = 0; d < D; ++d)
+        out[d] = 0.0;
+    for (int64_t j = 0; j < s_kv; ++j) {
+        if (!mrow[j]) continue;
+        const double p = exp(srow[j] - L);
+        const float *vj = v + j * D;
+        for (int64_t d = 0; d < D; ++d)
+            out[d] += p * (double)vj[d];
+    }
+    *lse = L;
+}
+
+/*
+ * q: [B, H, s_q, D], k, v: [B, H, s_kv, D], contiguous float32.
+ * rows == NULL: every row; out [B, H, s_q, D], lse [B, H, s_q].
+ * rows != NULL: nrows flat row ids ((b*H + h)*s_q + i); out [nrows, D], lse [nrows].
+ */
+int oracle_attention(const float *q, const float *k, const float *v,
+                     int B, int H, int s_q, int s_kv, int D,
+                     int mask_kind, int window, int prefix, const int32_t *doc,
+                     int score_kind, double score_param, double scale,
+                     const int64_t *rows, int64_t nrows,
+                     double *out, double *lse)
+{
+    if (!or_mask_ok(mask_kind) || B <= 0 || H <= 0 || s_q <= 0 || s_kv <= 0 || D <= 0)
+        return OR_ERR_ARG;
+    if (score_kind < OR_SCORE_IDENTITY || score_kind > OR_SCORE_ALIBI)
+        return OR_ERR_ARG;
+    if (mask_kind == OR_MASK_DOCUMENT && (doc == NULL || s_q != s_kv))
+        return OR_ERR_ARG;
+    if (score_kind == OR_SCORE_SOFTCAP && !(score_param > 0.0))
+        return OR_ERR_ARG;
+    or_mask m = {mask_kind, window, prefix, doc, (int64_t)s_q};
+    const int64_t total = rows ? nrows : (int64_t)B * H * s_q;
+    int err = OR_OK;
+
+#pragma omp parallel
+    {
+        double *srow = (double *)malloc((size_t)s_kv * sizeof(double));
+        unsigned char *mrow = (unsigned char *)malloc((size_t)s_kv);
+        if (!srow || !mrow) {
+#pragma omp atomic write
+            err = OR_ERR_NOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t r = 0; r < total; ++r) {
+                const int64_t flat = rows ? rows[r] : r;
+                const int64_t i = flat % s_q, bh = flat / s_q;
+                const int64_t b = bh / H, h = bh % H;
+                if (b >= B) continue;
+                or_row(q + bh * (int64_t)s_q * D, k + bh * (int64_t)s_kv * D,
+                       v + bh * (int64_t)s_kv * D, H, s_kv, D, &m, score_kind,
+                       score_param, scale, b, h, i, srow, mrow, out + r * D, lse + r);
+            }
+        }
+        free(srow);
+        free(mrow);
+    }
+    return err;
+}
+
+/* the single predicate, exposed so tests can check it against the pages' examples */
+int oracle_mask_value(int kind, int window, int prefix, const int32_t *doc, int64_t doc_len,
+                      int64_t b, int64_t h, int64_t q, int64_t kv)
+{
+    or_mask m = {kind, window, prefix, doc, doc_len};
+    return or_mask_ok(kind) ? or_mask_mod(&m, b, h, q, kv) : -1;
+}
+
+int oracle_num_threads(void)
+{
+    int n = 1;
+#ifdef _OPENMP
+#pragma omp parallel
+    {
+#pragma omp single
+        n = omp_get_num_threads();
+    }
+#endif
+    return n;
+}

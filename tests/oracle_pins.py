@@ -1,0 +1,423 @@
+"""Pins that tie the float64 oracle to something other than itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+when the oracle disagrees with:
+  * a library routine (PyTorch's CPU scaled-dot-product attention, which also
+    returns the log-sum-exp) on cases that reduce to it: the all-true mask,
+    the causal mask, the causal + bidirectional prefix mask (prefix rows are
+    plain attention over keys 0..P, the rest causal), the document mask
+    (causal attention inside each document slice), the sliding window (each
+    row is plain attention over its window slice);
+  * closed forms (ALiBi with zero scores is a truncated geometric series;
+    softcap scores built through atanh; block counts of causal, sliding
+    window and prefix masks; document tiles from the document intervals);
+  * special cases (constant V, W = 1, W = 0, first causal row, a huge cap);
+  * a pure-Python brute force on tiny shapes (math.exp, plain loops).
+
+The mutation test compiles deliberately broken copies of oracle.c and checks
+that at least one pin fails for each.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+from block_sparse_masked_blockmask_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _sdpa(q, k, v, scale, causal=False):
+    """(out, lse) from PyTorch's CPU flash attention in float64."""
+    tq, tk, tv = (torch.from_numpy(np.asarray(x, np.float64)) for x in (q, k, v))
+    out, lse = torch.ops.aten._scaled_dot_product_flash_attention_for_cpu(
+        tq, tk, tv, 0.0, causal, scale=scale)
+    return out.numpy(), lse.numpy()
+
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape).astype(np.float32)
+
+
+def _close(a, b, tol, what):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    assert a.shape == b.shape, (what, a.shape, b.shape)
+    fin = np.isfinite(b)
+    assert np.array_equal(np.isfinite(a), fin), f"{what}: finiteness differs"
+    assert np.array_equal(a[~fin], b[~fin]), f"{what}: infinities differ"
+    err = float(np.max(np.abs(a[fin] - b[fin]))) if fin.any() else 0.0
+    assert err <= tol, f"{what}: max abs err {err:.3e} > {tol:.1e}"
+
+
+# --------------------------------------------------------------- library pins
+def pin_all_true_mask_is_textbook_attention(orc):
+    for (B, H, sq, skv, D, scale, seed) in [(2, 3, 40, 56, 8, 0.37, 1), (1, 2, 33, 33, 16, 0.25, 2)]:
+        q, k, v = _rand((B, H, sq, D), seed), _rand((B, H, skv, D), seed + 1), _rand((B, H, skv, D), seed + 2)
+        out, lse = orc.attention(q, k, v, W.MASK_ALL, W.SCORE_IDENTITY, scale)
+        ro, rl = _sdpa(q, k, v, scale)
+        _close(out, ro, 1e-12, "all-true out")
+        _close(lse, rl, 1e-12, "all-true lse")
+
+
+def pin_causal_mask_is_library_causal(orc):
+    B, H, S, D, scale = 2, 2, 48, 8, 0.5
+    q, k, v = _rand((B, H, S, D), 3), _rand((B, H, S, D), 4), _rand((B, H, S, D), 5)
+    out, lse = orc.attention(q, k, v, W.MASK_CAUSAL, W.SCORE_IDENTITY, scale)
+    ro, rl = _sdpa(q, k, v, scale, causal=True)
+    _close(out, ro, 1e-12, "causal out")
+    _close(lse, rl, 1e-12, "causal lse")
+
+
+def pin_causal_prefix_splits_into_library_calls(orc):
+    # rows q <= P attend to keys 0..P (both bounds inclusive); rows q > P are causal.
+    B, H, S, D, P, scale = 1, 2, 40, 4, 13, 0.5
+    q, k, v = _rand((B, H, S, D), 6), _rand((B, H, S, D), 7), _rand((B, H, S, D), 8)
+    out, lse = orc.attention(q, k, v, W.MASK_CAUSAL_PREFIX, W.SCORE_IDENTITY, scale, prefix=P)
+    po, pl = _sdpa(q[:, :, :P + 1], k[:, :, :P + 1], v[:, :, :P + 1], scale)
+    co, cl = _sdpa(q, k, v, scale, causal=True)
+    _close(out[:, :, :P + 1], po, 1e-12, "prefix rows out")
+    _close(lse[:, :, :P + 1], pl, 1e-12, "prefix rows lse")
+    _close(out[:, :, P + 1:], co[:, :, P + 1:], 1e-12, "causal rows out")
+    _close(lse[:, :, P + 1:], cl[:, :, P + 1:], 1e-12, "causal rows lse")
+
+
+def pin_document_mask_is_per_document_causal(orc):
+    lengths = [5, 11, 3, 9]
+    S, B, H, D, scale = sum(lengths), 1, 2, 4, 0.6
+    doc = np.repeat(np.arange(len(lengths), dtype=np.int32), lengths)[None, :]
+    q, k, v = _rand((B, H, S, D), 9), _rand((B, H, S, D), 10), _rand((B, H, S, D), 11)
+    out, lse = orc.attention(q, k, v, W.MASK_DOCUMENT, W.SCORE_IDENTITY, scale, doc_ids=doc)
+    s0 = 0
+    for L in lengths:
+        sl = slice(s0, s0 + L)
+        ro, rl = _sdpa(q[:, :, sl], k[:, :, sl], v[:, :, sl], scale, causal=True)
+        _close(out[:, :, sl], ro, 1e-12, "document out")
+        _close(lse[:, :, sl], rl, 1e-12, "document lse")
+        s0 += L
+
+
+def pin_sliding_window_rows_are_window_slices(orc):
+    B, H, S, D, Wd, scale = 1, 2, 24, 4, 5, 0.5
+    q, k, v = _rand((B, H, S, D), 12), _rand((B, H, S, D), 13), _rand((B, H, S, D), 14)
+    out, lse = orc.attention(q, k, v, W.MASK_SLIDING_WINDOW, W.SCORE_IDENTITY, scale, window=Wd)
+    for i in range(S):
+        lo = max(0, i - Wd + 1)
+        ro, rl = _sdpa(q[:, :, i:i + 1], k[:, :, lo:i + 1], v[:, :, lo:i + 1], scale)
+        _close(out[:, :, i:i + 1], ro, 1e-12, f"window row {i} out")
+        _close(lse[:, :, i:i + 1], rl, 1e-12, f"window row {i} lse")
+
+
+def pin_huge_softcap_is_identity(orc):
+    B, H, S, D, scale = 1, 2, 20, 8, 0.35
+    q, k, v = _rand((B, H, S, D), 15), _rand((B, H, S, D), 16), _rand((B, H, S, D), 17)
+    out, lse = orc.attention(q, k, v, W.MASK_CAUSAL, W.SCORE_SOFTCAP, scale, score_param=1e30)
+    ro, rl = _sdpa(q, k, v, scale, causal=True)
+    _close(out, ro, 1e-12, "softcap 1e30 out")
+    _close(lse, rl, 1e-12, "softcap 1e30 lse")
+
+
+# ------------------------------------------------------------- closed forms
+def pin_softcap_through_atanh(orc):
+    # q = [1, 0], k_j = [c_j, 0], scale = 1: the scaled score of key j is c_j.  With
+    # c_j = cap * atanh(x_j), cap * tanh(c_j / cap) = cap * x_j (up to the
+    # float32 rounding of c_j), so the softcapped scores are known.
+    cap = 50.0
+    x = np.linspace(-0.06, 0.05, 17)
+    kj = (cap * np.arctanh(x)).astype(np.float32)
+    q = np.array([1.0, 0.0], np.float32).reshape(1, 1, 1, 2)
+    k = np.stack([kj, np.zeros_like(kj)], -1)[None, None]
+    v = np.stack([np.arange(x.size, dtype=np.float32), np.ones(x.size, np.float32)], -1)[None, None]
+    out, lse = orc.attention(q, k, v, W.MASK_ALL, W.SCORE_SOFTCAP, 1.0, score_param=cap)
+    s = cap * x
+    p = np.exp(s - s.max())
+    ref_lse = s.max() + math.log(p.sum())
+    ref_out = (p / p.sum()) @ np.asarray(v[0, 0], np.float64)
+    # float32 rounding of k_j moves each score by < 1e-5
+    _close(lse[0, 0], [ref_lse], 1e-5, "softcap lse")
+    _close(out[0, 0, 0], ref_out, 1e-4, "softcap out")
+
+
+def pin_alibi_zero_scores_geometric(orc):
+    # q = k = 0: scores are the bias -slope_h (i - j), slope_h = 2^(-8(h+1)/H).
+    # Causal row i: weights r^d over d = i - j in 0..i with r = exp(-slope_h):
+    #   lse_i = ln((1 - r^(i+1)) / (1 - r)),  E[d] = sum d r^d / sum r^d,
+    #   out_i = [i - E[d], 1] for v_j = [j, 1].
+    B, H, S = 1, 4, 20
+    q = np.zeros((B, H, S, 2), np.float32)
+    k = np.zeros((B, H, S, 2), np.float32)
+    v = np.zeros((B, H, S, 2), np.float32)
+    v[..., 0] = np.arange(S, dtype=np.float32)
+    v[..., 1] = 1.0
+    out, lse = orc.attention(q, k, v, W.MASK_CAUSAL, W.SCORE_ALIBI, 0.125)
+    for h in range(H):
+        r = math.exp(-(2.0 ** (-8.0 * (h + 1) / H)))
+        for i in range(S):
+            n = i
+            zsum = (1 - r ** (n + 1)) / (1 - r)
+            dsum = r * (1 - (n + 1) * r ** n + n * r ** (n + 1)) / (1 - r) ** 2
+            _close([lse[0, h, i]], [math.log(zsum)], 1e-12, f"alibi lse h{h} i{i}")
+            # the closed form cancels in (1 - r)^2 for small slopes: 1e-9
+            _close(out[0, h, i], [i - dsum / zsum, 1.0], 1e-9, f"alibi out h{h} i{i}")
+
+
+# ----------------------------------------------------------- special cases
+def pin_constant_v_gives_constant_out(orc):
+    B, H, S, D = 2, 2, 32, 4
+    q, k = _rand((B, H, S, D), 18), _rand((B, H, S, D), 19)
+    v = np.full((B, H, S, D), 0.75, np.float32)
+    doc = np.repeat(np.arange(4, dtype=np.int32), 8)[None, :].repeat(B, 0)
+    for mask, kw in [(W.MASK_CAUSAL, {}), (W.MASK_SLIDING_WINDOW, {"window": 3}),
+                     (W.MASK_CAUSAL_PREFIX, {"prefix": 9}), (W.MASK_DOCUMENT, {"doc_ids": doc}),
+                     (W.MASK_ALL, {})]:
+        for score, sp in [(W.SCORE_IDENTITY, 0.0), (W.SCORE_SOFTCAP, 2.0), (W.SCORE_ALIBI, 0.0)]:
+            out, lse = orc.attention(q, k, v, mask, score, 0.5, score_param=sp, **kw)
+            assert np.all(np.isfinite(lse))
+            # the weights sum to 1 up to a few double roundings per key
+            assert np.max(np.abs(out - 0.75)) <= 1e-13, (mask, score)
+
+
+def pin_window_one_and_zero(orc):
+    B, H, S, D, scale = 1, 2, 16, 4, 0.5
+    q, k, v = _rand((B, H, S, D), 20), _rand((B, H, S, D), 21), _rand((B, H, S, D), 22)
+    out, lse = orc.attention(q, k, v, W.MASK_SLIDING_WINDOW, W.SCORE_IDENTITY, scale, window=1)
+    _close(out, v, 1e-15, "W=1 out = v")
+    diag = scale * np.einsum("bhsd,bhsd->bhs", q.astype(np.float64), k.astype(np.float64))
+    _close(lse, diag, 1e-12, "W=1 lse = diagonal score")
+    out0, lse0 = orc.attention(q, k, v, W.MASK_SLIDING_WINDOW, W.SCORE_IDENTITY, scale, window=0)
+    assert np.all(out0 == 0.0) and np.all(np.isneginf(lse0)), "W=0 rows must be empty"
+
+
+def pin_first_causal_row_is_v0(orc):
+    B, H, S, D = 2, 2, 12, 4
+    q, k, v = _rand((B, H, S, D), 23), _rand((B, H, S, D), 24), _rand((B, H, S, D), 25)
+    for score, sp in [(W.SCORE_IDENTITY, 0.0), (W.SCORE_SOFTCAP, 3.0), (W.SCORE_ALIBI, 0.0)]:
+        out, _ = orc.attention(q, k, v, W.MASK_CAUSAL, score, 0.5, score_param=sp)
+        _close(out[:, :, 0], v[:, :, 0], 1e-15, "causal row 0")
+
+
+def pin_alibi_diagonal_has_no_bias(orc):
+    # Sliding window W=1 keeps only the diagonal, where the ALiBi bias is 0.
+    B, H, S, D = 1, 4, 10, 4
+    q, k, v = _rand((B, H, S, D), 26), _rand((B, H, S, D), 27), _rand((B, H, S, D), 28)
+    _, la = orc.attention(q, k, v, W.MASK_SLIDING_WINDOW, W.SCORE_ALIBI, 0.5, window=1)
+    _, li = orc.attention(q, k, v, W.MASK_SLIDING_WINDOW, W.SCORE_IDENTITY, 0.5, window=1)
+    _close(la, li, 0.0, "alibi diagonal")
+
+
+# -------------------------------------------------------- block-mask forms
+def _rows_are_permutations(bm):
+    for key in ("kv_indices", "full_kv_indices"):
+        idx = bm[key]
+        n = idx.shape[-1]
+        assert np.array_equal(np.sort(idx, axis=-1), np.broadcast_to(np.arange(n), idx.shape)), key
+
+
+def _expected_lists(status_rows):
+    """status_rows [NQB, NKVB] in {0 empty, 1 partial, 2 full} -> the four tensors (one (b,h))."""
+    nq, nk = status_rows.shape
+    out = {k: [] for k in ("kv_num_blocks", "kv_indices", "full_kv_num_blocks", "full_kv_indices")}
+    for r in range(nq):
+        part = [j for j in range(nk) if status_rows[r, j] == 1]
+        full = [j for j in range(nk) if status_rows[r, j] == 2]
+        out["kv_num_blocks"].append(len(part))
+        out["kv_indices"].append(part + [j for j in range(nk) if j not in part])
+        out["full_kv_num_blocks"].append(len(full))
+        out["full_kv_indices"].append(full + [j for j in range(nk) if j not in full])
+    return {k: np.asarray(v, np.int32) for k, v in out.items()}
+
+
+def _check_lists(bm, status, what):
+    """status: [B, H, NQB, NKVB] expected tile classes."""
+    _rows_are_permutations(bm)
+    B, H = status.shape[:2]
+    for b in range(B):
+        for h in range(H):
+            exp = _expected_lists(status[b, h])
+            for key, val in exp.items():
+                assert np.array_equal(bm[key][b, h], val), f"{what}: {key} (b={b}, h={h})"
+
+
+def pin_causal_block_counts_closed_form(orc):
+    for nb in (1, 2, 5, 16):
+        S = nb * 128
+        bm = orc.block_mask(W.MASK_CAUSAL, 1, 2, S, S, 128)
+        assert bm["full_kv_num_blocks"].sum() == 2 * nb * (nb - 1) // 2
+        assert bm["kv_num_blocks"].sum() == 2 * nb
+        qb = np.arange(nb)[:, None]
+        kb = np.arange(nb)[None, :]
+        status = np.where(kb < qb, 2, np.where(kb == qb, 1, 0))
+        _check_lists(bm, np.broadcast_to(status, (1, 2, nb, nb)), f"causal nb={nb}")
+
+
+def pin_sliding_window_block_counts_closed_form(orc):
+    # W = 256 = 2 blocks: row qb has kv block qb-1 full, qb-2 and qb partial.
+    nb, S = 16, 2048
+    bm = orc.block_mask(W.MASK_SLIDING_WINDOW, 2, 1, S, S, 128, window=256)
+    assert np.all(bm["kv_num_blocks"].sum(-1) == nb + (nb - 2))
+    assert np.all(bm["full_kv_num_blocks"].sum(-1) == nb - 1)
+    qb = np.arange(nb)[:, None]
+    kb = np.arange(nb)[None, :]
+    status = np.where(kb == qb - 1, 2, np.where((kb == qb) | (kb == qb - 2), 1, 0))
+    _check_lists(bm, np.broadcast_to(status, (2, 1, nb, nb)), "window 256")
+
+
+def pin_causal_prefix_block_counts_closed_form(orc):
+    # P = 1024 (inclusive): q blocks 0..8 see kv blocks 0..7 in full and kv
+    # block 8 (which holds only kv = 1024 for rows < 1024, and is the diagonal
+    # for q block 8) as partial; q blocks >= 9 are causal.
+    nb, S, P = 32, 4096, 1024
+    bm = orc.block_mask(W.MASK_CAUSAL_PREFIX, 1, 2, S, S, 128, prefix=P)
+    assert np.all(bm["full_kv_num_blocks"].sum(-1) == 532)
+    assert np.all(bm["kv_num_blocks"].sum(-1) == 32)
+    status = np.zeros((nb, nb), np.int64)
+    for r in range(nb):
+        if r <= 8:
+            status[r, :8] = 2
+            status[r, 8] = 1
+        else:
+            status[r, :r] = 2
+            status[r, r] = 1
+    _check_lists(bm, np.broadcast_to(status, (1, 2, nb, nb)), "prefix 1024")
+
+
+def pin_document_blocks_from_intervals(orc):
+    # Contiguous documents: a tile below the diagonal is full when its rows and
+    # columns lie in one document, partial when the last column's document is
+    # the first row's document, empty otherwise; the diagonal tile is partial.
+    B, S, blk = 2, 2048, 128
+    doc = W.document_ids(B, S, seed=3, lo=100, hi=700)
+    bm = orc.block_mask(W.MASK_DOCUMENT, B, 1, S, S, blk, doc_ids=doc)
+    nb = S // blk
+    status = np.zeros((B, 1, nb, nb), np.int64)
+    for b in range(B):
+        d = doc[b]
+        for qb in range(nb):
+            r0, r1 = d[qb * blk], d[qb * blk + blk - 1]
+            for kb in range(qb + 1):
+                c0, c1 = d[kb * blk], d[kb * blk + blk - 1]
+                if kb == qb:
+                    status[b, 0, qb, kb] = 1
+                elif r0 == r1 == c0 == c1:
+                    status[b, 0, qb, kb] = 2
+                elif c1 == r0:
+                    status[b, 0, qb, kb] = 1
+    _check_lists(bm, status, "document")
+
+
+def pin_golden_causal_prefix_predicate(orc):
+    path = os.path.join(GOLDEN, "causal_prefix_predicate.txt")
+    n = 0
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            P, qi, kv, expect = (int(x) for x in line.split())
+            got = orc.mask_value(W.MASK_CAUSAL_PREFIX, qi, kv, prefix=P)
+            assert got == bool(expect), (P, qi, kv, expect)
+            n += 1
+    assert n >= 8
+
+
+# ------------------------------------------------------------ brute force
+def _bf_mask(kind, b, h, i, j, window, prefix, doc):
+    if kind == W.MASK_CAUSAL:
+        return i >= j
+    if kind == W.MASK_SLIDING_WINDOW:
+        return i >= j and i - j < window
+    if kind == W.MASK_CAUSAL_PREFIX:
+        return (i <= prefix and j <= prefix) or i >= j
+    if kind == W.MASK_DOCUMENT:
+        return doc[b][i] == doc[b][j] and i >= j
+    return True
+
+
+def _bf_score(kind, param, t, h, H, i, j):
+    if kind == W.SCORE_SOFTCAP:
+        return param * math.tanh(t / param)
+    if kind == W.SCORE_ALIBI:
+        return t - 2.0 ** (-8.0 * (h + 1) / H) * (i - j)
+    return t
+
+
+def brute_force(q, k, v, mask, score, scale, window=0, prefix=0, doc=None, param=0.0, block=2):
+    """Plain Python loops: (out, lse, block-mask dict) for tiny shapes."""
+    B, H, S, D = q.shape
+    out = [[[[0.0] * D for _ in range(S)] for _ in range(H)] for _ in range(B)]
+    lse = [[[0.0] * S for _ in range(H)] for _ in range(B)]
+    for b in range(B):
+        for h in range(H):
+            for i in range(S):
+                row = []
+                for j in range(S):
+                    if _bf_mask(mask, b, h, i, j, window, prefix, doc):
+                        t = scale * math.fsum(float(q[b, h, i, d]) * float(k[b, h, j, d]) for d in range(D))
+                        row.append((j, _bf_score(score, param, t, h, H, i, j)))
+                if not row:
+                    lse[b][h][i] = -math.inf
+                    continue
+                mx = max(s for _, s in row)
+                L = mx + math.log(math.fsum(math.exp(s - mx) for _, s in row))
+                lse[b][h][i] = L
+                for d in range(D):
+                    out[b][h][i][d] = math.fsum(math.exp(s - L) * float(v[b, h, j, d]) for j, s in row)
+    nb = S // block
+    status = np.zeros((B, H, nb, nb), np.int64)
+    for b in range(B):
+        for h in range(H):
+            for qb in range(nb):
+                for kb in range(nb):
+                    c = sum(_bf_mask(mask, b, h, i, j, window, prefix, doc)
+                            for i in range(qb * block, qb * block + block)
+                            for j in range(kb * block, kb * block + block))
+                    status[b, h, qb, kb] = 2 if c == block * block else (1 if c else 0)
+    return np.asarray(out), np.asarray(lse), status
+
+
+def pin_brute_force_tiny(orc):
+    B, H, D = 2, 2, 3
+    for S, block in [(8, 2), (12, 4), (16, 4)]:
+        q, k, v = _rand((B, H, S, D), S), _rand((B, H, S, D), S + 1), _rand((B, H, S, D), S + 2)
+        doc = np.zeros((B, S), np.int32)
+        doc[0, S // 3:] = 1
+        doc[1, S // 2:] = 1
+        doc[1, S - 2:] = 2
+        for mask, kw in [(W.MASK_CAUSAL, {}), (W.MASK_SLIDING_WINDOW, {"window": 3}),
+                         (W.MASK_CAUSAL_PREFIX, {"prefix": 5}), (W.MASK_DOCUMENT, {"doc": doc}),
+                         (W.MASK_ALL, {})]:
+            for score, sp in [(W.SCORE_IDENTITY, 0.0), (W.SCORE_SOFTCAP, 0.9), (W.SCORE_ALIBI, 0.0)]:
+                bo, bl, bs = brute_force(q, k, v, mask, score, 0.7, param=sp, block=block,
+                                         window=kw.get("window", 0), prefix=kw.get("prefix", 0),
+                                         doc=kw.get("doc"))
+                okw = {"window": kw.get("window", 0), "prefix": kw.get("prefix", 0),
+                       "doc_ids": kw.get("doc")}
+                oo, ol = orc.attention(q, k, v, mask, score, 0.7, score_param=sp, **okw)
+                _close(oo, bo, 1e-12, f"brute out S{S} m{mask} s{score}")
+                _close(ol, bl, 1e-12, f"brute lse S{S} m{mask} s{score}")
+                bm = orc.block_mask(mask, B, H, S, S, block, **okw)
+                _check_lists(bm, bs, f"brute block mask S{S} m{mask}")
+
+
+ALL_PINS = [
+    pin_all_true_mask_is_textbook_attention,
+    pin_causal_mask_is_library_causal,
+    pin_causal_prefix_splits_into_library_calls,
+    pin_document_mask_is_per_document_causal,
+    pin_sliding_window_rows_are_window_slices,
+    pin_huge_softcap_is_identity,
+    pin_softcap_through_atanh,
+    pin_alibi_zero_scores_geometric,
+    pin_constant_v_gives_constant_out,
+    pin_window_one_and_zero,
+    pin_first_causal_row_is_v0,
+    pin_alibi_diagonal_has_no_bias,
+    pin_causal_block_counts_closed_form,
+    pin_sliding_window_block_counts_closed_form,
+    pin_causal_prefix_block_counts_closed_form,
+    pin_document_blocks_from_intervals,
+    pin_golden_causal_prefix_predicate,
+    pin_brute_force_tiny,
+]

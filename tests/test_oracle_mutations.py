@@ -1,0 +1,55 @@
+"""Plant plausible mistakes in copies of the oracle and check the pins catch each.
+
+Every mutant is built from a temporary copy of oracle.c with one textual
+change (a wrong sign, bound, index, dropped term or misplaced operand); at
+least one pin must fail on it.  CPU only; the real oracle is untouched.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+MUTATIONS = [
+    ("alibi sign", "t - slope * (double)(q - kv)", "t + slope * (double)(q - kv)"),
+    ("alibi head index", "-8.0 * (double)(h + 1)", "-8.0 * (double)(h)"),
+    ("alibi slope uses H-1", "/ (double)H);", "/ (double)(H + 1));"),
+    ("causal strict", "        return q >= kv;\n    case OR_MASK_SLIDING", "        return q > kv;\n    case OR_MASK_SLIDING"),
+    ("window bound", "(q - kv) < (int64_t)m->window", "(q - kv) <= (int64_t)m->window"),
+    ("prefix bound", "q <= (int64_t)m->prefix && kv <= (int64_t)m->prefix",
+     "q < (int64_t)m->prefix && kv < (int64_t)m->prefix"),
+    ("prefix and/or", "(q <= (int64_t)m->prefix && kv <= (int64_t)m->prefix) || q >= kv",
+     "(q <= (int64_t)m->prefix || kv <= (int64_t)m->prefix) && q >= kv"),
+    ("document drops causality", "== m->doc[b * m->doc_len + kv] && q >= kv", "== m->doc[b * m->doc_len + kv]"),
+    ("softcap drops cap", "return param * tanh(t / param);", "return tanh(t / param);"),
+    ("softcap scale inside", "return param * tanh(t / param);", "return param * tanh(t);"),
+    ("lse drops max", "const double L = mx + log(Z);", "const double L = log(Z);"),
+    ("out unnormalised", "const double p = exp(srow[j] - L);", "const double p = exp(srow[j] - mx);"),
+    ("scale dropped", "or_score_mod(score_kind, score_param, scale * dot, h, H, i, j)",
+     "or_score_mod(score_kind, score_param, dot, h, H, i, j)"),
+    ("v row index", "const float *vj = v + j * D;", "const float *vj = v + i * D;"),
+    ("full tiles classed as partial", "const int64_t all = (int64_t)block * block;",
+     "const int64_t all = (int64_t)block * block + 1;"),
+    ("padding order", "if (!(count[j] > 0 && count[j] < all)) pi[tp++] = (int32_t)j;",
+     "if (!(count[j] > 0 && count[j] < all)) pi[tp++] = (int32_t)(nkvb - 1 - j);"),
+    ("empty row guard", "        *lse = -INFINITY;\n        return;", "        *lse = 0.0;\n        return;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_mutation(tmp_path, name, old, new):
+    src = open(oracle.oracle.SOURCE).read()
+    assert src.count(old) == 1, f"mutation anchor not unique: {name}"
+    path = os.path.join(tmp_path, "mutant.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    lib = oracle.compile_oracle(path, os.path.join(tmp_path, "libmutant.so"))
+    mutant = oracle.Oracle(lib)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(mutant)
+        except (AssertionError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught the mutation '{name}'"
