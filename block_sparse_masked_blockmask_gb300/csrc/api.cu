@@ -1,0 +1,212 @@
+// C-ABI layer (include/flexattn.h): argument validation on the host, the
+// per-device status word, and dispatch to the kernels.  Nothing here computes
+// attention or block classes; every step of the path runs in the kernels.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "flex_internal.h"
+
+namespace flex {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_ws_mutex;
+int *g_status[kMaxDevices] = {nullptr};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_mask_kind(int k) { return k >= FLEX_MASK_CAUSAL && k <= FLEX_MASK_ALL; }
+
+int check_sizes(int32_t B, int32_t H, int32_t q_len, int32_t kv_len, int32_t block) {
+    if (B <= 0 || H <= 0 || q_len <= 0 || kv_len <= 0 || block <= 0) return FLEX_ERR_INVALID_ARG;
+    if (block != kBlock) return FLEX_ERR_UNSUPPORTED;
+    if (q_len % block != 0 || kv_len % block != 0) return FLEX_ERR_SHAPE;
+    if (kv_len / block > kMaxKvBlocks) return FLEX_ERR_UNSUPPORTED;
+    if (B > 65535 || H > 65535) return FLEX_ERR_UNSUPPORTED;
+    return FLEX_OK;
+}
+
+int check_tensor(const flex_tensor *t, int dtype, int64_t B, int64_t H, int64_t S, int64_t D) {
+    if (!t || !t->data) return FLEX_ERR_INVALID_ARG;
+    if (t->dtype != dtype) return FLEX_ERR_INVALID_ARG;
+    if (t->shape[0] != B || t->shape[1] != H || t->shape[2] != S || t->shape[3] != D) return FLEX_ERR_SHAPE;
+    if (t->stride[3] != 1) return FLEX_ERR_ALIGNMENT;
+    const int64_t elem = dtype == FLEX_DTYPE_BF16 ? 2 : 4;
+    for (int i = 0; i < 3; ++i)
+        if (t->stride[i] <= 0 || (t->stride[i] * elem) % 16 != 0 || t->stride[i] * elem >= (int64_t(1) << 40))
+            return FLEX_ERR_ALIGNMENT;
+    if (!aligned16(t->data)) return FLEX_ERR_ALIGNMENT;
+    return FLEX_OK;
+}
+
+}  // namespace
+
+int *device_status_word(int *err) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *err = FLEX_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    if (!g_status[dev]) {
+        int *p = nullptr;
+        if (cudaMalloc(&p, 256) != cudaSuccess || cudaMemset(p, 0, 256) != cudaSuccess) {
+            *err = FLEX_ERR_CUDA;
+            return nullptr;
+        }
+        g_status[dev] = p;
+    }
+    *err = FLEX_OK;
+    return g_status[dev];
+}
+
+}  // namespace flex
+
+using namespace flex;
+
+extern "C" {
+
+int flex_block_mask_sizes(int32_t B, int32_t H, int32_t q_len, int32_t kv_len, int32_t block, int64_t *num_elems,
+                          int64_t *idx_elems) {
+    if (!num_elems || !idx_elems) return FLEX_ERR_INVALID_ARG;
+    const int rc = check_sizes(B, H, q_len, kv_len, block);
+    if (rc != FLEX_OK) return rc;
+    const int64_t nqb = q_len / block, nkvb = kv_len / block;
+    *num_elems = (int64_t)B * H * nqb;
+    *idx_elems = (int64_t)B * H * nqb * nkvb;
+    return FLEX_OK;
+}
+
+int flex_block_mask_create(int32_t mask_kind, const flex_mask_params *params, int32_t B, int32_t H, int32_t q_len,
+                           int32_t kv_len, int32_t block, flex_block_mask *bm, void *stream) {
+    if (!bm || !valid_mask_kind(mask_kind)) return FLEX_ERR_INVALID_ARG;
+    const int rc = check_sizes(B, H, q_len, kv_len, block);
+    if (rc != FLEX_OK) return rc;
+    if (!bm->kv_num_blocks || !bm->kv_indices || !bm->full_kv_num_blocks || !bm->full_kv_indices)
+        return FLEX_ERR_INVALID_ARG;
+    flex_mask_params prm = {0, 0, nullptr};
+    if (params) prm = *params;
+    if (mask_kind == FLEX_MASK_SLIDING_WINDOW && (!params || prm.window < 0)) return FLEX_ERR_INVALID_ARG;
+    if (mask_kind == FLEX_MASK_CAUSAL_PREFIX && !params) return FLEX_ERR_INVALID_ARG;
+    if (mask_kind == FLEX_MASK_DOCUMENT) {
+        if (!params || !prm.doc_ids) return FLEX_ERR_INVALID_ARG;
+        if (q_len != kv_len) return FLEX_ERR_SHAPE;
+        if (!aligned16(prm.doc_ids)) return FLEX_ERR_ALIGNMENT;
+    }
+    bm->B = B;
+    bm->H = H;
+    bm->q_len = q_len;
+    bm->kv_len = kv_len;
+    bm->block = block;
+    bm->nqb = q_len / block;
+    bm->nkvb = kv_len / block;
+    bm->mask_kind = mask_kind;
+    bm->params = prm;
+    MaskDesc md{mask_kind, prm.window, prm.prefix, q_len, prm.doc_ids};
+    const cudaError_t e = launch_block_mask(md, B, H, q_len, kv_len, bm->kv_num_blocks, bm->kv_indices,
+                                            bm->full_kv_num_blocks, bm->full_kv_indices,
+                                            static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FLEX_OK : FLEX_ERR_CUDA;
+}
+
+int flex_attention_fwd(const flex_tensor *q, const flex_tensor *k, const flex_tensor *v, const flex_block_mask *bm,
+                       int32_t score_kind, float score_param, float scale, void *out, float *lse, void *stream) {
+    if (!q || !k || !v || !bm || !out || !lse) return FLEX_ERR_INVALID_ARG;
+    const int dtype = q->dtype;
+    if (dtype != FLEX_DTYPE_BF16 && dtype != FLEX_DTYPE_FP32) return FLEX_ERR_INVALID_ARG;
+    if (score_kind < FLEX_SCORE_IDENTITY || score_kind > FLEX_SCORE_ALIBI) return FLEX_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return FLEX_ERR_INVALID_ARG;
+    if (score_kind == FLEX_SCORE_SOFTCAP && !(score_param > 0.f && std::isfinite(score_param)))
+        return FLEX_ERR_INVALID_ARG;
+    const int64_t B = q->shape[0], H = q->shape[1], Sq = q->shape[2], D = q->shape[3], Skv = k->shape[2];
+    if (B <= 0 || H <= 0 || Sq <= 0 || Skv <= 0 || D <= 0) return FLEX_ERR_SHAPE;
+    if (D != 64 && D != 128) return FLEX_ERR_UNSUPPORTED;
+    if (Sq > INT32_MAX || Skv > INT32_MAX) return FLEX_ERR_UNSUPPORTED;
+    int rc = check_tensor(q, dtype, B, H, Sq, D);
+    if (rc == FLEX_OK) rc = check_tensor(k, dtype, B, H, Skv, D);
+    if (rc == FLEX_OK) rc = check_tensor(v, dtype, B, H, Skv, D);
+    if (rc != FLEX_OK) return rc;
+    if (!aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return FLEX_ERR_ALIGNMENT;
+    // BlockMask consistency
+    if (!valid_mask_kind(bm->mask_kind)) return FLEX_ERR_INVALID_ARG;
+    rc = check_sizes(bm->B, bm->H, bm->q_len, bm->kv_len, bm->block);
+    if (rc != FLEX_OK) return rc;
+    if (bm->B != B || bm->H != H || bm->q_len != Sq || bm->kv_len != Skv) return FLEX_ERR_SHAPE;
+    if (bm->nqb != bm->q_len / bm->block || bm->nkvb != bm->kv_len / bm->block) return FLEX_ERR_SHAPE;
+    if (!bm->kv_num_blocks || !bm->kv_indices || !bm->full_kv_num_blocks || !bm->full_kv_indices)
+        return FLEX_ERR_INVALID_ARG;
+    if (bm->mask_kind == FLEX_MASK_DOCUMENT && (!bm->params.doc_ids || !aligned16(bm->params.doc_ids)))
+        return FLEX_ERR_INVALID_ARG;
+    if (bm->mask_kind == FLEX_MASK_SLIDING_WINDOW && bm->params.window < 0) return FLEX_ERR_INVALID_ARG;
+    if (B * H * ((bm->nqb + 1) / 2) > INT32_MAX) return FLEX_ERR_UNSUPPORTED;
+
+    int err = FLEX_OK;
+    int *status = device_status_word(&err);
+    if (!status) return err;
+
+    AttnProblem p;
+    p.B = (int)B;
+    p.H = (int)H;
+    p.q_len = (int)Sq;
+    p.kv_len = (int)Skv;
+    p.D = (int)D;
+    p.nqb = bm->nqb;
+    p.nkvb = bm->nkvb;
+    for (int i = 0; i < 4; ++i) {
+        p.q_stride[i] = q->stride[i];
+        p.k_stride[i] = k->stride[i];
+        p.v_stride[i] = v->stride[i];
+    }
+    p.q = q->data;
+    p.k = k->data;
+    p.v = v->data;
+    p.out = out;
+    p.lse = lse;
+    p.kv_num = bm->kv_num_blocks;
+    p.kv_idx = bm->kv_indices;
+    p.full_num = bm->full_kv_num_blocks;
+    p.full_idx = bm->full_kv_indices;
+    p.mask = MaskDesc{bm->mask_kind, bm->params.window, bm->params.prefix, bm->q_len, bm->params.doc_ids};
+    p.score_kind = score_kind;
+    p.score_param = score_param;
+    p.scale = scale;
+    p.status = status;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = dtype == FLEX_DTYPE_BF16 ? launch_attn_bf16(p, s) : launch_attn_fp32(p, s);
+    return e == cudaSuccess ? FLEX_OK : FLEX_ERR_CUDA;
+}
+
+int flex_device_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FLEX_ERR_CUDA;
+    int err = FLEX_OK;
+    int *status = device_status_word(&err);
+    if (!status) return err;
+    int host = 0;
+    if (cudaMemcpy(&host, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FLEX_ERR_CUDA;
+    if (host != 0 && cudaMemset(status, 0, sizeof(int)) != cudaSuccess) return FLEX_ERR_CUDA;
+    return host == 0 ? FLEX_OK : FLEX_ERR_DEVICE_TIMEOUT;
+}
+
+const char *flex_status_string(int status) {
+    switch (status) {
+        case FLEX_OK:
+            return "ok";
+        case FLEX_ERR_INVALID_ARG:
+            return "invalid argument";
+        case FLEX_ERR_UNSUPPORTED:
+            return "unsupported configuration";
+        case FLEX_ERR_SHAPE:
+            return "shape mismatch or length not a multiple of the block size";
+        case FLEX_ERR_ALIGNMENT:
+            return "pointer or stride not 16-byte aligned, or inner stride is not 1";
+        case FLEX_ERR_CUDA:
+            return "CUDA error";
+        case FLEX_ERR_DEVICE_TIMEOUT:
+            return "a kernel gave up on a device-side wait";
+        default:
+            return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// Host side of the bf16 tensor-core attention: TMA tensor maps for Q, K, V
+// (4-D [B, H, S, D] views with 64 x 128 boxes and 128-byte swizzle) and
+// dispatch on head dim and score kind.
+#include <mutex>
+
+#include "attn_bf16_launch.cuh"
+
+namespace flex {
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// [B, H, S, D] bf16 with element strides st (st[3] == 1) as a 4-D tensor map
+// whose box is 64 (D) x 128 (S) x 1 x 1.
+bool make_map(CUtensorMap *map, const void *base, int B, int H, int S, int D, const int64_t st[4]) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)kBlock, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bf16(const AttnProblem &p, cudaStream_t stream) {
+    CUtensorMap tq, tk, tv;
+    if (!make_map(&tq, p.q, p.B, p.H, p.q_len, p.D, p.q_stride) ||
+        !make_map(&tk, p.k, p.B, p.H, p.kv_len, p.D, p.k_stride) ||
+        !make_map(&tv, p.v, p.B, p.H, p.kv_len, p.D, p.v_stride))
+        return cudaErrorInvalidValue;
+    Bf16Params kp;
+    kp.B = p.B;
+    kp.H = p.H;
+    kp.q_len = p.q_len;
+    kp.kv_len = p.kv_len;
+    kp.nqb = p.nqb;
+    kp.nkvb = p.nkvb;
+    kp.npairs = (p.nqb + 1) / 2;
+    kp.kv_num = p.kv_num;
+    kp.kv_idx = p.kv_idx;
+    kp.full_num = p.full_num;
+    kp.full_idx = p.full_idx;
+    kp.mask = p.mask;
+    kp.scale = p.scale;
+    kp.score_param = p.score_param;
+    kp.out = static_cast<uint16_t *>(p.out);
+    kp.lse = p.lse;
+    kp.status = p.status;
+    return p.D == 64 ? launch_bf16_d64(tq, tk, tv, kp, p.score_kind, stream)
+                     : launch_bf16_d128(tq, tk, tv, kp, p.score_kind, stream);
+}
+
+}  // namespace flex

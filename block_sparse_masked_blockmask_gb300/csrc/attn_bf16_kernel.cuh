@@ -1,0 +1,558 @@
+// Block-sparse FlexAttention forward for bf16 inputs on sm_103a tensor cores.
+//
+// What it computes (the flex_attention op with OUTPUT_LOGSUMEXP, from
+// "[Inductor][Flex Attention] Add Subtiling Option for Alpha Scaling",
+// PyTorch PR #167356): for each query row, over the kv tiles its BlockMask
+// lists, s = score_mod(scale * q.k) with s = -inf where mask_mod is false
+// (mask_mod evaluated on partial tiles only), out = softmax(s) V and
+// lse = ln sum exp(s).  The online-softmax step is the page's forward_block_mn
+// (l = l * alpha + sum(p); acc = acc * alpha; acc += p V) carried out with
+// the running max in base-2 units.
+//
+// Design for one GB300 SM (one CTA per SM, 384 threads):
+//   * A CTA owns two consecutive q blocks (two 128-row Q tiles) of one
+//     (batch, head) and walks the union of their kv-tile lists in descending
+//     kv order, so the K/V tile staged in shared memory serves both Q tiles.
+//   * warp 8  (TMA)     : loads Q0/Q1 once, then K and V tiles of each union
+//                         step into a ring of shared-memory stages (128-byte
+//                         swizzle, the layout tcgen05 descriptors read).
+//   * warp 9  (MMA)     : one thread issues tcgen05.mma: S_i = Q_i K^T into
+//                         tensor memory (TMEM) and O_i += P_i V with P_i read
+//                         from TMEM; order per step PV0, S0(next), PV1,
+//                         S1(next), so each softmax group has two MMAs of
+//                         slack while the tensor core works for the other.
+//   * warps 0-3 / 4-7   : softmax of Q tile 0 / 1, one thread per row (TMEM
+//                         lane = row).  Score_mod on every listed tile,
+//                         mask_mod only on partial tiles (the row's kept
+//                         interval or document id is hoisted out of the
+//                         column loop).  P goes back to TMEM over the S
+//                         columns as bf16.
+//   * O rescale: the running max is only raised when a tile's max exceeds it
+//     by more than 2^8, so exp2(s - m) <= 256 stays exact in fp32/bf16 and
+//     the O rescale (a TMEM read-modify-write by the softmax warp, between
+//     the S load and the next PV) is rare; the result is the same softmax.
+//     This replaces the page's subtiled alpha scaling of the register
+//     accumulator: with O in TMEM the rescale leaves the register file and
+//     the PV critical path entirely on most steps.
+//   * Every wait is bounded (globaltimer); on timeout the CTA records
+//     FLEX_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees TMEM, exits.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "flex_internal.h"
+#include "ptx.cuh"
+
+namespace flex {
+
+constexpr int kAttnThreads = 384;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // raise the running max only beyond 2^8
+
+struct Bf16Params {
+    int B, H, q_len, kv_len, nqb, nkvb, npairs;
+    const int32_t *kv_num, *kv_idx, *full_num, *full_idx;
+    MaskDesc mask;
+    float scale, score_param;
+    uint16_t *out;  // bf16 bits, contiguous [B, H, q_len, D]
+    float *lse;     // [B, H, q_len]
+    int *status;
+};
+
+// Shared-memory bookkeeping that follows the Q/K/V tiles.
+struct AttnMisc {
+    uint64_t q_full;
+    uint64_t k_full[4], v_full[4], kv_empty[4];
+    uint64_t s_full[2], p_full[2];
+    uint64_t o_full, drain;
+    uint32_t tmem_base;
+    int abort;
+    int n_union;
+    int pad;
+    uint32_t flags[kMaxKvBlocks];  // bit0 present in tile 0, bit1 full in tile 0, bit2/bit3 same for tile 1
+    uint32_t ulist[kMaxKvBlocks];  // union, descending kv: kv block | flags << 16
+};
+
+template <int D>
+struct Bf16Cfg {
+    static_assert(D == 64 || D == 128, "head dim");
+    static constexpr int kAtoms = D / 64;                  // 128-byte swizzle atoms along D
+    static constexpr uint32_t kAtomBytes = 128 * 128;      // 128 rows x 128 bytes
+    static constexpr uint32_t kTileBytes = 128 * D * 2;    // one 128 x D bf16 tile
+    static constexpr int kStages = D == 128 ? 2 : 4;
+    static constexpr uint32_t kQOff = 0;
+    static constexpr uint32_t kKvOff = 2 * kTileBytes;
+    static constexpr uint32_t kStageBytes = 2 * kTileBytes;  // K then V
+    static constexpr uint32_t kMiscOff = kKvOff + kStages * kStageBytes;
+    static constexpr uint32_t kSmemBytes = kMiscOff + sizeof(AttnMisc) + 1024;
+    // TMEM columns: S0 | S1 | O0 | O1 (P_i overwrites the first 64 columns of S_i)
+    __host__ __device__ static constexpr uint32_t s_col(int i) { return i ? 128u : 0u; }
+    __host__ __device__ static constexpr uint32_t o_col(int i) { return i ? 256u + D : 256u; }
+};
+
+__device__ __forceinline__ void record_failure(AttnMisc &ms, int *status) {
+    *reinterpret_cast<volatile int *>(&ms.abort) = 1;
+    atomicCAS(status, 0, kDeviceTimeout);
+}
+
+// A wait taken by all 32 lanes of a warp with one outcome for the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        if ((it & 15u) == 0) {
+            const int stop = (*abort != 0) || (global_timer_ns() - t0 > kWaitLimitNs);
+            if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight work).
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+    int never = 0;
+    (void)mbar_wait(bar, parity, &never);
+}
+
+// TMEM read of 64 columns of this thread's lane, completed before returning.
+__device__ __forceinline__ void tmem_ld64_sync(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+        "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]),
+          "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
+          "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]),
+          "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
+}
+
+// TMEM read of 32 columns of this thread's lane, completed before returning.
+__device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// score_mod in base-2 units: x = log2(e) * score_mod(scale * s).
+template <int SCORE>
+struct ScoreLog2 {
+    float k0, k1, k2;  // per-kind constants
+    float base;        // ALiBi: log2(e) * slope_h * (kv0 - q), per tile
+    float slope2;      // ALiBi: log2(e) * slope_h
+    __device__ __forceinline__ void init(const Bf16Params &p, int h) {
+        if constexpr (SCORE == FLEX_SCORE_SOFTCAP) {
+            // cap * tanh(y) = cap - 2 cap / (exp(2y) + 1),  y = scale * s / cap
+            k0 = 2.f * p.scale * kLog2e / p.score_param;
+            k1 = -2.f * p.score_param * kLog2e;
+            k2 = p.score_param * kLog2e;
+        } else {
+            k0 = p.scale * kLog2e;
+            k1 = k2 = 0.f;
+        }
+        slope2 = SCORE == FLEX_SCORE_ALIBI ? kLog2e * exp2f(-8.f * (float)(h + 1) / (float)p.H) : 0.f;
+        base = 0.f;
+    }
+    __device__ __forceinline__ void tile(int kv0, int q) {
+        if constexpr (SCORE == FLEX_SCORE_ALIBI) base = slope2 * (float)(kv0 - q);
+    }
+    __device__ __forceinline__ float operator()(float s, int c) const {
+        if constexpr (SCORE == FLEX_SCORE_SOFTCAP) {
+            const float t = ex2_approx(s * k0);
+            return fmaf(k1, rcp_approx(t + 1.f), k2);
+        } else if constexpr (SCORE == FLEX_SCORE_ALIBI) {
+            return fmaf(s, k0, fmaf((float)c, slope2, base));
+        } else {
+            return s * k0;
+        }
+    }
+};
+
+// mask_mod on a partial tile for row q (columns kv0 .. kv0 + 127).
+__device__ __forceinline__ void apply_partial_mask(const MaskDesc &m, int b, int q, int kv0, float (&x)[128]) {
+    int lo, hi;
+    if (mask_row_interval(m, q, lo, hi)) {
+        const int clo = lo - kv0, chi = hi - kv0;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) x[c] = (c >= clo && c <= chi) ? x[c] : -INFINITY;
+    } else {  // document: same document id and kv <= q
+        const int32_t *dr = m.doc_ids + (int64_t)b * m.doc_len;
+        const int dq = __ldg(dr + q);
+        const int lim = q - kv0;
+        const int4 *dk = reinterpret_cast<const int4 *>(dr + kv0);
+#pragma unroll
+        for (int c4 = 0; c4 < 32; ++c4) {
+            const int4 d = __ldg(dk + c4);
+            const int c = 4 * c4;
+            x[c + 0] = (c + 0 <= lim && d.x == dq) ? x[c + 0] : -INFINITY;
+            x[c + 1] = (c + 1 <= lim && d.y == dq) ? x[c + 1] : -INFINITY;
+            x[c + 2] = (c + 2 <= lim && d.z == dq) ? x[c + 2] : -INFINITY;
+            x[c + 3] = (c + 3 <= lim && d.w == dq) ? x[c + 3] : -INFINITY;
+        }
+    }
+}
+
+template <int D, int SCORE>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, const Bf16Params p) {
+    using C = Bf16Cfg<D>;
+    constexpr int NS = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    AttnMisc &ms = *reinterpret_cast<AttnMisc *>(smem + C::kMiscOff);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+    // Work item: heads outermost (their K/V stay in L2 while in flight),
+    // q-block pairs from the last (the longest kv lists for causal-like
+    // masks) to the first.
+    const int item = blockIdx.x;
+    const int bh = item / p.npairs;
+    const int pair = p.npairs - 1 - item % p.npairs;
+    const int b = bh / p.H, h = bh % p.H;
+    const int qb0 = 2 * pair;
+    const bool has1 = qb0 + 1 < p.nqb;
+    const int64_t row0 = (int64_t)bh * p.nqb + qb0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&ms.q_full, 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&ms.k_full[s], 1);
+            mbar_init(&ms.v_full[s], 1);
+            mbar_init(&ms.kv_empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ms.s_full[i], 1);
+            mbar_init(&ms.p_full[i], 128);
+        }
+        mbar_init(&ms.o_full, 1);
+        mbar_init(&ms.drain, 1);
+        ms.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&ms.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    for (int i = threadIdx.x; i < p.nkvb; i += kAttnThreads) ms.flags[i] = 0u;
+    __syncthreads();
+
+    // Mark every kv tile of both q blocks (bounds-checked: a malformed
+    // BlockMask cannot write outside the flag array).
+    {
+        const int nkvb = p.nkvb;
+        const int32_t *pidx = p.kv_idx + row0 * nkvb, *fidx = p.full_idx + row0 * nkvb;
+        const int np0 = min(max(p.kv_num[row0], 0), nkvb), nf0 = min(max(p.full_num[row0], 0), nkvb);
+        const int np1 = has1 ? min(max(p.kv_num[row0 + 1], 0), nkvb) : 0;
+        const int nf1 = has1 ? min(max(p.full_num[row0 + 1], 0), nkvb) : 0;
+        for (int i = threadIdx.x; i < np0; i += kAttnThreads) {
+            const int j = pidx[i];
+            if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 1u);
+        }
+        for (int i = threadIdx.x; i < nf0; i += kAttnThreads) {
+            const int j = fidx[i];
+            if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 3u);
+        }
+        for (int i = threadIdx.x; i < np1; i += kAttnThreads) {
+            const int j = pidx[nkvb + i];
+            if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 4u);
+        }
+        for (int i = threadIdx.x; i < nf1; i += kAttnThreads) {
+            const int j = fidx[nkvb + i];
+            if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 12u);
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {  // union of the two lists, descending kv order
+        int count = 0;
+        const unsigned lt = (1u << lane) - 1u;
+        for (int base = 0; base < p.nkvb; base += 32) {
+            const int c = p.nkvb - 1 - (base + lane);
+            const uint32_t f = c >= 0 ? ms.flags[c] : 0u;
+            const unsigned bal = __ballot_sync(0xffffffffu, f != 0u);
+            if (f != 0u) ms.ulist[count + __popc(bal & lt)] = (uint32_t)c | (f << 16);
+            count += __popc(bal);
+        }
+        if (lane == 0) ms.n_union = count;
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = ms.tmem_base;
+    const int nu = ms.n_union;
+    volatile int *abort_flag = &ms.abort;
+
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0 && nu > 0) {
+            prefetch_tensormap(&tmap_q);
+            prefetch_tensormap(&tmap_k);
+            prefetch_tensormap(&tmap_v);
+            mbar_arrive_expect_tx(&ms.q_full, (has1 ? 2u : 1u) * C::kTileBytes);
+            for (int a = 0; a < C::kAtoms; ++a) {
+                tma_load_4d(smem + C::kQOff + a * C::kAtomBytes, &tmap_q, &ms.q_full, 64 * a, qb0 * kBlock, h, b);
+                if (has1)
+                    tma_load_4d(smem + C::kQOff + C::kTileBytes + a * C::kAtomBytes, &tmap_q, &ms.q_full, 64 * a,
+                                (qb0 + 1) * kBlock, h, b);
+            }
+            int issued = 0;
+            for (int u = 0; u < nu; ++u) {
+                const int s = u % NS;
+                const uint32_t use = (uint32_t)(u / NS);
+                if (use > 0 && !mbar_wait(&ms.kv_empty[s], (use - 1) & 1u, abort_flag)) {
+                    record_failure(ms, p.status);
+                    break;
+                }
+                const int kv0 = (int)(ms.ulist[u] & 0xFFFFu) * kBlock;
+                uint8_t *kd = smem + C::kKvOff + s * C::kStageBytes;
+                uint8_t *vd = kd + C::kTileBytes;
+                mbar_arrive_expect_tx(&ms.k_full[s], C::kTileBytes);
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_4d(kd + a * C::kAtomBytes, &tmap_k, &ms.k_full[s], 64 * a, kv0, h, b);
+                mbar_arrive_expect_tx(&ms.v_full[s], C::kTileBytes);
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_4d(vd + a * C::kAtomBytes, &tmap_v, &ms.v_full[s], 64 * a, kv0, h, b);
+                issued = u + 1;
+            }
+            // Drain: every copy issued above must land before the CTA exits.
+            drain_wait(&ms.q_full, 0);
+            for (int s = 0; s < NS && s < issued; ++s) {
+                const int last = s + ((issued - 1 - s) / NS) * NS;
+                const uint32_t par = (uint32_t)(last / NS) & 1u;
+                drain_wait(&ms.k_full[s], par);
+                drain_wait(&ms.v_full[s], par);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0 && nu > 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
+            const uint32_t q_addr0 = smem_u32(smem + C::kQOff);
+            uint32_t pv_done[2] = {0u, 0u};
+            auto issue_s = [&](int i, int s) {
+                const uint32_t qa = q_addr0 + i * C::kTileBytes;
+                const uint32_t ka = smem_u32(smem + C::kKvOff + s * C::kStageBytes);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k / 4) * C::kAtomBytes + (k % 4) * 32;
+                    mma_ss(tmem + C::s_col(i), smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                           idesc_s, k > 0 ? 1u : 0u);
+                }
+                mma_commit(&ms.s_full[i]);
+            };
+            auto issue_pv = [&](int i, int s) {
+                const uint32_t va = smem_u32(smem + C::kKvOff + s * C::kStageBytes + C::kTileBytes);
+                const uint32_t acc = pv_done[i] > 0 ? 1u : 0u;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mma_ts(tmem + C::o_col(i), tmem + C::s_col(i) + k * 8, smem_desc_sw128(va + k * 2048, C::kAtomBytes, 1024),
+                           idesc_o, (k > 0 || acc) ? 1u : 0u);
+                ++pv_done[i];
+            };
+            bool ok = mbar_wait(&ms.q_full, 0, abort_flag) && mbar_wait(&ms.k_full[0], 0, abort_flag);
+            tc_fence_after_sync();
+            if (ok) {
+                const uint32_t f = ms.ulist[0] >> 16;
+                if (f & 1u) issue_s(0, 0);
+                if (f & 4u) issue_s(1, 0);
+            }
+            for (int u = 0; ok && u < nu; ++u) {
+                const int s = u % NS;
+                const uint32_t f = ms.ulist[u] >> 16;
+                const bool nxt = u + 1 < nu;
+                const int s1 = (u + 1) % NS;
+                const uint32_t f1 = nxt ? (ms.ulist[u + 1] >> 16) : 0u;
+                if (!mbar_wait(&ms.v_full[s], (uint32_t)(u / NS) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (f & 1u) {
+                    if (!mbar_wait(&ms.p_full[0], pv_done[0] & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    issue_pv(0, s);
+                }
+                if (nxt) {
+                    if (!mbar_wait(&ms.k_full[s1], (uint32_t)((u + 1) / NS) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    if (f1 & 1u) issue_s(0, s1);
+                }
+                if (f & 4u) {
+                    if (!mbar_wait(&ms.p_full[1], pv_done[1] & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    issue_pv(1, s);
+                }
+                mma_commit(&ms.kv_empty[s]);
+                if (f1 & 4u) issue_s(1, s1);
+            }
+            if (ok)
+                mma_commit(&ms.o_full);
+            else
+                record_failure(ms, p.status);
+            mma_commit(&ms.drain);  // every MMA issued above completes before TMEM is freed
+            drain_wait(&ms.drain, 0);
+        }
+        __syncwarp();
+    } else if (warp < 8) {
+        // ----------------------------------------------------------- softmax
+        const int i = warp / 4;
+        const int t = threadIdx.x % 128;
+        const bool valid = i == 0 || has1;
+        const int q = (qb0 + i) * kBlock + t;
+        const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
+        const uint32_t s_addr = tmem + lane_base + C::s_col(i);
+        const uint32_t o_addr = tmem + lane_base + C::o_col(i);
+        const uint32_t present = i ? 4u : 1u, fullbit = i ? 8u : 2u;
+        ScoreLog2<SCORE> score;
+        score.init(p, h);
+        float m_run = -INFINITY, l_run = 0.f;
+        uint32_t cnt = 0;
+        bool ok = true;
+        if (valid) {
+            for (int u = 0; u < nu; ++u) {
+                const uint32_t e = ms.ulist[u];
+                const uint32_t f = e >> 16;
+                if (!(f & present)) continue;
+                const int kv0 = (int)(e & 0xFFFFu) * kBlock;
+                if (!warp_wait(&ms.s_full[i], cnt & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                float x[128];
+                {
+                    uint32_t r[64];
+                    tmem_ld64_sync(s_addr, r);
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(r[c]);
+                    tmem_ld64_sync(s_addr + 64, r);
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) x[64 + c] = __uint_as_float(r[c]);
+                }
+                score.tile(kv0, q);
+#pragma unroll
+                for (int c = 0; c < 128; ++c) x[c] = score(x[c], c);
+                if (!(f & fullbit)) apply_partial_mask(p.mask, b, q, kv0, x);
+
+                float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+#pragma unroll
+                for (int c = 4; c < 128; c += 4) {
+                    mx0 = fmaxf(mx0, x[c]);
+                    mx1 = fmaxf(mx1, x[c + 1]);
+                    mx2 = fmaxf(mx2, x[c + 2]);
+                    mx3 = fmaxf(mx3, x[c + 3]);
+                }
+                const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+                float alpha = 1.f;
+                if (m_tile > m_run + kRescaleThreshold) {  // also taken when m_run = -inf
+                    alpha = ex2_approx(m_run - m_tile);
+                    m_run = m_tile;
+                }
+                const float m_use = m_run == -INFINITY ? 0.f : m_run;
+                float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float p0 = ex2_approx(x[c0 + 2 * j] - m_use);
+                        const float p1 = ex2_approx(x[c0 + 2 * j + 1] - m_use);
+                        rs0 += p0;
+                        rs1 += p1;
+                        pk[j] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st16(s_addr + c0 / 2, pk);
+                }
+                l_run = fmaf(l_run, alpha, rs0 + rs1);
+                if (cnt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32_sync(o_addr + c0, o);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                        tmem_st32(o_addr + c0, o);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                mbar_arrive(&ms.p_full[i]);
+                ++cnt;
+            }
+            // ---------------------------------------------------- epilogue
+            bool have = ok && cnt > 0;
+            if (have && !warp_wait(&ms.o_full, 0, abort_flag)) {
+                have = false;
+                ok = false;
+            }
+            if (!ok) record_failure(ms, p.status);
+            if (ok) {
+                tc_fence_after_sync();
+                const int64_t orow = ((int64_t)bh * p.q_len + q);
+                uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D);
+                const bool live = have && l_run > 0.f;
+                const float inv = live ? 1.f / l_run : 0.f;
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {
+                    uint32_t o[32];
+                    if (have) {
+                        tmem_ld32_sync(o_addr + c0, o);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = 0u;
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        pk[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        dst[c0 / 8 + j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                }
+                p.lse[orow] = live ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+            }
+        }
+    }
+
+    // ---------------------------------------------------------- teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace flex

@@ -1,0 +1,39 @@
+// Launch of the bf16 tensor-core attention kernel for one head dim; included
+// by one translation unit per head dim so the instantiations compile in parallel.
+#pragma once
+
+#include "attn_bf16_kernel.cuh"
+
+namespace flex {
+
+template <int D, int SCORE>
+cudaError_t launch_bf16_kernel(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                               const Bf16Params &kp, cudaStream_t stream) {
+    using C = Bf16Cfg<D>;
+    auto kernel = attn_bf16_kernel<D, SCORE>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)((int64_t)kp.B * kp.H * kp.npairs);
+    kernel<<<grid, kAttnThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_bf16_dim(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            const Bf16Params &kp, int score_kind, cudaStream_t stream) {
+    switch (score_kind) {
+        case FLEX_SCORE_SOFTCAP:
+            return launch_bf16_kernel<D, FLEX_SCORE_SOFTCAP>(tq, tk, tv, kp, stream);
+        case FLEX_SCORE_ALIBI:
+            return launch_bf16_kernel<D, FLEX_SCORE_ALIBI>(tq, tk, tv, kp, stream);
+        default:
+            return launch_bf16_kernel<D, FLEX_SCORE_IDENTITY>(tq, tk, tv, kp, stream);
+    }
+}
+
+cudaError_t launch_bf16_d64(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                            const Bf16Params &kp, int score_kind, cudaStream_t stream);
+cudaError_t launch_bf16_d128(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                             const Bf16Params &kp, int score_kind, cudaStream_t stream);
+
+}  // namespace flex

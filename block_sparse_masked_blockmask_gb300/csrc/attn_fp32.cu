@@ -1,0 +1,139 @@
+// Block-sparse attention forward for float32 inputs on the CUDA cores.
+//
+// The same computation as the tensor-core path (the flex_attention op of
+// "[Inductor][Flex Attention] Add Subtiling Option for Alpha Scaling",
+// PyTorch PR #167356): for every tile listed in the BlockMask, scores
+// s = score_mod(scale * q.k), masked to -inf by mask_mod on partial tiles,
+// folded into an online softmax (running max m, running sum l, output rescaled
+// by alpha = exp(m_old - m_new): the forward_block_mn step), then out = acc / l
+// and lse = m + ln l.  All arithmetic is fp32 FFMA; no tensor cores, so the
+// 1e-4 tolerance of fp32 inputs holds (a single TF32 pass would not).
+//
+// One CTA per (q block, head, batch); D/64 threads per query row, each owning
+// 64 dims of q and of the accumulator.  K and V tiles are staged in shared
+// memory and read as broadcasts.
+#include "flex_internal.h"
+
+namespace flex {
+namespace {
+
+constexpr int kDimsPerThread = 64;
+constexpr int kChunk = 16;   // columns per online-softmax update
+
+template <int D>
+struct Fp32Cfg {
+    static constexpr int kTpr = D / kDimsPerThread;      // threads per row
+    static constexpr int kThreads = kBlock * kTpr;
+    static constexpr size_t kSmem = 2ull * kBlock * D * sizeof(float);
+};
+
+__device__ __forceinline__ float score_mod_f32(int kind, float param, float s, float slope, int q, int kv) {
+    if (kind == FLEX_SCORE_SOFTCAP) return param * tanhf(s / param);
+    if (kind == FLEX_SCORE_ALIBI) return s - slope * (float)(q - kv);
+    return s;
+}
+
+template <int D>
+__global__ void __launch_bounds__(Fp32Cfg<D>::kThreads) attn_fp32_kernel(AttnProblem p) {
+    using C = Fp32Cfg<D>;
+    extern __shared__ float4 smem4[];
+    float *ks = reinterpret_cast<float *>(smem4);
+    float *vs = ks + kBlock * D;
+
+    const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int row = threadIdx.x / C::kTpr, part = threadIdx.x % C::kTpr;
+    const int q = qb * kBlock + row;
+    const int64_t bhq = ((int64_t)b * p.H + h) * p.nqb + qb;
+
+    const float *qp = static_cast<const float *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1] +
+                      (int64_t)q * p.q_stride[2] + part * kDimsPerThread;
+    float qr[kDimsPerThread], acc[kDimsPerThread];
+#pragma unroll
+    for (int d = 0; d < kDimsPerThread; ++d) {
+        qr[d] = qp[d];
+        acc[d] = 0.f;
+    }
+    const float slope = exp2f(-8.f * (float)(h + 1) / (float)p.H);
+    float m = -INFINITY, l = 0.f;
+
+    const int nfull = p.full_num[bhq], npart = p.kv_num[bhq];
+    const int32_t *fidx = p.full_idx + bhq * p.nkvb;
+    const int32_t *pidx = p.kv_idx + bhq * p.nkvb;
+    const float *kbase = static_cast<const float *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
+    const float *vbase = static_cast<const float *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1];
+
+    for (int t = 0; t < nfull + npart; ++t) {
+        const bool full = t < nfull;
+        const int kvb = full ? fidx[t] : pidx[t - nfull];
+        const int kv0 = kvb * kBlock;
+        __syncthreads();  // previous tile fully consumed
+        for (int i = threadIdx.x; i < kBlock * D / 4; i += C::kThreads) {
+            const int r = (i * 4) / D, c = (i * 4) % D;
+            const int64_t ko = (int64_t)(kv0 + r) * p.k_stride[2] + c;
+            const int64_t vo = (int64_t)(kv0 + r) * p.v_stride[2] + c;
+            reinterpret_cast<float4 *>(ks)[i] = *reinterpret_cast<const float4 *>(kbase + ko);
+            reinterpret_cast<float4 *>(vs)[i] = *reinterpret_cast<const float4 *>(vbase + vo);
+        }
+        __syncthreads();
+
+        for (int c0 = 0; c0 < kBlock; c0 += kChunk) {
+            float s[kChunk];
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) {
+                const float *kr = ks + (c0 + j) * D + part * kDimsPerThread;
+                float dot = 0.f;
+#pragma unroll
+                for (int d = 0; d < kDimsPerThread; ++d) dot = fmaf(qr[d], kr[d], dot);
+                if constexpr (C::kTpr == 2) dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+                const int kv = kv0 + c0 + j;
+                float x = score_mod_f32(p.score_kind, p.score_param, dot * p.scale, slope, q, kv);
+                if (!full && !mask_mod(p.mask, b, q, kv)) x = -INFINITY;
+                s[j] = x;
+            }
+            float cmax = s[0];
+#pragma unroll
+            for (int j = 1; j < kChunk; ++j) cmax = fmaxf(cmax, s[j]);
+            const float m_new = fmaxf(m, cmax);
+            if (m_new == -INFINITY) continue;  // nothing unmasked in this row yet
+            const float alpha = expf(m - m_new);  // 0 when m was -inf
+            l *= alpha;
+#pragma unroll
+            for (int d = 0; d < kDimsPerThread; ++d) acc[d] *= alpha;
+            m = m_new;
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) {
+                const float pj = expf(s[j] - m);
+                l += pj;
+                const float *vr = vs + (c0 + j) * D + part * kDimsPerThread;
+#pragma unroll
+                for (int d = 0; d < kDimsPerThread; ++d) acc[d] = fmaf(pj, vr[d], acc[d]);
+            }
+        }
+    }
+
+    float *op = static_cast<float *>(p.out) + (((int64_t)b * p.H + h) * p.q_len + q) * D + part * kDimsPerThread;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int d = 0; d < kDimsPerThread; d += 4)
+        *reinterpret_cast<float4 *>(op + d) = make_float4(acc[d] * inv, acc[d + 1] * inv, acc[d + 2] * inv,
+                                                          acc[d + 3] * inv);
+    if (part == 0) p.lse[((int64_t)b * p.H + h) * p.q_len + q] = l > 0.f ? m + logf(l) : -INFINITY;
+}
+
+template <int D>
+cudaError_t launch_d(const AttnProblem &p, cudaStream_t stream) {
+    using C = Fp32Cfg<D>;
+    cudaError_t e = cudaFuncSetAttribute(attn_fp32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    attn_fp32_kernel<D><<<dim3(p.nqb, p.H, p.B), C::kThreads, C::kSmem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fp32(const AttnProblem &p, cudaStream_t stream) {
+    return p.D == 64 ? launch_d<64>(p, stream) : launch_d<128>(p, stream);
+}
+
+}  // namespace flex

@@ -1,0 +1,94 @@
+// Internal declarations shared by the CUDA translation units of the library:
+// the device-side mask description, the mask_mod predicate, the kernel
+// launchers called by the C-ABI layer, and the per-device workspace.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda.h>
+
+#include "../../include/flexattn.h"
+
+namespace flex {
+
+constexpr int kBlock = 128;       // BlockMask granularity (Q_BLOCK = KV_BLOCK = 128)
+constexpr int kMaxKvBlocks = 1024;  // kv blocks per BlockMask row the kernels stage on chip
+
+// mask_mod as the kernels see it.
+struct MaskDesc {
+    int32_t kind;
+    int32_t window;
+    int32_t prefix;
+    int32_t doc_len;            // row length of doc_ids (== q_len == kv_len)
+    const int32_t *doc_ids;     // [B, doc_len]
+};
+
+// mask_mod(b, h, q, kv) for the enumerated kinds.  No kind depends on h.
+__host__ __device__ __forceinline__ bool mask_mod(const MaskDesc &m, int b, int q, int kv) {
+    switch (m.kind) {
+        case FLEX_MASK_CAUSAL:
+            return q >= kv;
+        case FLEX_MASK_SLIDING_WINDOW:
+            return q >= kv && q - kv < m.window;
+        case FLEX_MASK_CAUSAL_PREFIX:
+            return (q <= m.prefix && kv <= m.prefix) || q >= kv;
+        case FLEX_MASK_DOCUMENT:
+            return q >= kv && m.doc_ids[(int64_t)b * m.doc_len + q] == m.doc_ids[(int64_t)b * m.doc_len + kv];
+        default:
+            return true;
+    }
+}
+
+// The interval kinds keep, for a fixed row q, exactly the kv in [lo, hi].
+// Returns false for kinds whose kept set is not an interval (document).
+__host__ __device__ __forceinline__ bool mask_row_interval(const MaskDesc &m, int q, int &lo, int &hi) {
+    switch (m.kind) {
+        case FLEX_MASK_CAUSAL:
+            lo = 0;
+            hi = q;
+            return true;
+        case FLEX_MASK_SLIDING_WINDOW:
+            lo = q - m.window + 1;
+            hi = q;
+            return true;
+        case FLEX_MASK_CAUSAL_PREFIX:
+            lo = 0;
+            hi = q <= m.prefix ? m.prefix : q;
+            return true;
+        case FLEX_MASK_ALL:
+            lo = 0;
+            hi = 0x7fffffff;
+            return true;
+        default:
+            return false;
+    }
+}
+
+// Problem description handed from the C-ABI layer to the attention launchers.
+struct AttnProblem {
+    int B, H, q_len, kv_len, D, nqb, nkvb;
+    int64_t q_stride[4], k_stride[4], v_stride[4];  // elements
+    const void *q, *k, *v;
+    void *out;                                       // contiguous [B,H,q_len,D]
+    float *lse;                                      // contiguous [B,H,q_len]
+    const int32_t *kv_num, *kv_idx, *full_num, *full_idx;
+    MaskDesc mask;
+    int score_kind;
+    float score_param;
+    float scale;
+    int *status;                                     // device status word
+};
+
+// Launchers (return a cudaError_t from the launch).
+cudaError_t launch_block_mask(const MaskDesc &mask, int B, int H, int q_len, int kv_len, int32_t *kv_num,
+                              int32_t *kv_idx, int32_t *full_num, int32_t *full_idx, cudaStream_t stream);
+cudaError_t launch_attn_fp32(const AttnProblem &p, cudaStream_t stream);
+cudaError_t launch_attn_bf16(const AttnProblem &p, cudaStream_t stream);
+
+// The per-device workspace holding the status word (allocated once per device).
+int *device_status_word(int *err);
+
+// Status codes a kernel writes into the status word.
+constexpr int kDeviceTimeout = 1;
+
+}  // namespace flex

@@ -1,0 +1,214 @@
+"""Thin Python binding of the C-ABI in include/flexattn.h.
+
+Argument marshalling only: torch tensors supply device memory and
+torch.cuda streams supply the cudaStream_t; every step of the path runs in
+the CUDA kernels of libflexattn.so.  There is no fallback: if the library is
+missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import _build
+
+FLEX_OK = 0
+FLEX_ERR_INVALID_ARG = -1
+FLEX_ERR_UNSUPPORTED = -2
+FLEX_ERR_SHAPE = -3
+FLEX_ERR_ALIGNMENT = -4
+FLEX_ERR_CUDA = -5
+FLEX_ERR_DEVICE_TIMEOUT = -6
+
+FLEX_MASK_CAUSAL = 0
+FLEX_MASK_SLIDING_WINDOW = 1
+FLEX_MASK_CAUSAL_PREFIX = 2
+FLEX_MASK_DOCUMENT = 3
+FLEX_MASK_ALL = 4
+
+FLEX_SCORE_IDENTITY = 0
+FLEX_SCORE_SOFTCAP = 1
+FLEX_SCORE_ALIBI = 2
+
+FLEX_DTYPE_BF16 = 0
+FLEX_DTYPE_FP32 = 1
+
+EXPORTED = ("flex_block_mask_sizes", "flex_block_mask_create", "flex_attention_fwd",
+            "flex_device_status", "flex_status_string")
+
+
+class FlexError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {flex_status_string(code)} ({code})")
+
+
+class flex_mask_params(ctypes.Structure):
+    _fields_ = [("window", ctypes.c_int32), ("prefix", ctypes.c_int32), ("doc_ids", ctypes.c_void_p)]
+
+
+class flex_block_mask(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("q_len", ctypes.c_int32),
+                ("kv_len", ctypes.c_int32), ("block", ctypes.c_int32), ("nqb", ctypes.c_int32),
+                ("nkvb", ctypes.c_int32), ("mask_kind", ctypes.c_int32), ("params", flex_mask_params),
+                ("kv_num_blocks", ctypes.c_void_p), ("kv_indices", ctypes.c_void_p),
+                ("full_kv_num_blocks", ctypes.c_void_p), ("full_kv_indices", ctypes.c_void_p)]
+
+
+class flex_tensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIBRARY
+
+
+def load_library():
+    """Load libflexattn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; "
+                                   "g.build()')")
+            lib = ctypes.CDLL(path)
+            i32, i64p, vp = ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), ctypes.c_void_p
+            lib.flex_block_mask_sizes.argtypes = [i32, i32, i32, i32, i32, i64p, i64p]
+            lib.flex_block_mask_sizes.restype = ctypes.c_int
+            lib.flex_block_mask_create.argtypes = [i32, ctypes.POINTER(flex_mask_params), i32, i32, i32, i32, i32,
+                                                   ctypes.POINTER(flex_block_mask), vp]
+            lib.flex_block_mask_create.restype = ctypes.c_int
+            tp = ctypes.POINTER(flex_tensor)
+            lib.flex_attention_fwd.argtypes = [tp, tp, tp, ctypes.POINTER(flex_block_mask), i32, ctypes.c_float,
+                                               ctypes.c_float, vp, vp, vp]
+            lib.flex_attention_fwd.restype = ctypes.c_int
+            lib.flex_device_status.argtypes = [vp]
+            lib.flex_device_status.restype = ctypes.c_int
+            lib.flex_status_string.argtypes = [ctypes.c_int]
+            lib.flex_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def _stream_handle(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def flex_status_string(code: int) -> str:
+    return load_library().flex_status_string(int(code)).decode()
+
+
+def flex_block_mask_sizes(B: int, H: int, q_len: int, kv_len: int, block: int = 128) -> tuple[int, int]:
+    n_num, n_idx = ctypes.c_int64(), ctypes.c_int64()
+    rc = load_library().flex_block_mask_sizes(B, H, q_len, kv_len, block, ctypes.byref(n_num), ctypes.byref(n_idx))
+    if rc != FLEX_OK:
+        raise FlexError(rc, "flex_block_mask_sizes")
+    return n_num.value, n_idx.value
+
+
+class BlockMask:
+    """Device BlockMask: the C struct plus the torch tensors that own its buffers."""
+
+    def __init__(self, struct: flex_block_mask, tensors: dict, doc_ids):
+        self.struct = struct
+        self.kv_num_blocks = tensors["kv_num_blocks"]
+        self.kv_indices = tensors["kv_indices"]
+        self.full_kv_num_blocks = tensors["full_kv_num_blocks"]
+        self.full_kv_indices = tensors["full_kv_indices"]
+        self.doc_ids = doc_ids  # keeps the document ids alive while the mask is in use
+
+    def as_numpy(self) -> dict:
+        return {k: getattr(self, k).cpu().numpy() for k in
+                ("kv_num_blocks", "kv_indices", "full_kv_num_blocks", "full_kv_indices")}
+
+
+def flex_block_mask_create(mask_kind: int, B: int, H: int, q_len: int, kv_len: int, block: int = 128,
+                           window: int = 0, prefix: int = 0, doc_ids: torch.Tensor | None = None,
+                           device=None, stream=None) -> BlockMask:
+    """Build a BlockMask on the device (asynchronous on `stream`)."""
+    device = torch.device(device) if device is not None else (
+        doc_ids.device if doc_ids is not None else torch.device("cuda", torch.cuda.current_device()))
+    n_num, n_idx = flex_block_mask_sizes(B, H, q_len, kv_len, block)
+    nqb, nkvb = q_len // block, kv_len // block
+    t = {
+        "kv_num_blocks": torch.empty((B, H, nqb), dtype=torch.int32, device=device),
+        "kv_indices": torch.empty((B, H, nqb, nkvb), dtype=torch.int32, device=device),
+        "full_kv_num_blocks": torch.empty((B, H, nqb), dtype=torch.int32, device=device),
+        "full_kv_indices": torch.empty((B, H, nqb, nkvb), dtype=torch.int32, device=device),
+    }
+    assert t["kv_num_blocks"].numel() == n_num and t["kv_indices"].numel() == n_idx
+    if doc_ids is not None:
+        doc_ids = doc_ids.to(device=device, dtype=torch.int32).contiguous()
+    params = flex_mask_params(window, prefix, doc_ids.data_ptr() if doc_ids is not None else None)
+    bm = flex_block_mask()
+    bm.kv_num_blocks = t["kv_num_blocks"].data_ptr()
+    bm.kv_indices = t["kv_indices"].data_ptr()
+    bm.full_kv_num_blocks = t["full_kv_num_blocks"].data_ptr()
+    bm.full_kv_indices = t["full_kv_indices"].data_ptr()
+    with torch.cuda.device(device):
+        rc = load_library().flex_block_mask_create(mask_kind, ctypes.byref(params), B, H, q_len, kv_len, block,
+                                                   ctypes.byref(bm), _stream_handle(stream, device))
+    if rc != FLEX_OK:
+        raise FlexError(rc, "flex_block_mask_create")
+    return BlockMask(bm, t, doc_ids)
+
+
+_DTYPES = {torch.bfloat16: FLEX_DTYPE_BF16, torch.float32: FLEX_DTYPE_FP32}
+
+
+def _tensor(x: torch.Tensor) -> flex_tensor:
+    if x.dim() != 4:
+        raise ValueError("expected a [B, H, S, D] tensor")
+    if x.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {x.dtype}")
+    t = flex_tensor()
+    t.data = x.data_ptr()
+    t.dtype = _DTYPES[x.dtype]
+    for i in range(4):
+        t.shape[i] = x.shape[i]
+        t.stride[i] = x.stride(i)
+    return t
+
+
+def flex_attention_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_mask: BlockMask,
+                       score_kind: int = FLEX_SCORE_IDENTITY, score_param: float = 0.0,
+                       scale: float | None = None, out: torch.Tensor | None = None,
+                       lse: torch.Tensor | None = None, stream=None):
+    """Block-sparse attention forward; returns (out, lse).  Asynchronous on `stream`."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    B, H, Sq, D = q.shape
+    if out is None:
+        out = torch.empty((B, H, Sq, D), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if not out.is_contiguous() or not lse.is_contiguous() or lse.dtype != torch.float32:
+        raise ValueError("out and lse must be contiguous; lse float32")
+    tq, tk, tv = _tensor(q), _tensor(k), _tensor(v)
+    with torch.cuda.device(q.device):
+        rc = load_library().flex_attention_fwd(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                               ctypes.byref(block_mask.struct), score_kind, float(score_param),
+                                               float(scale), ctypes.c_void_p(out.data_ptr()),
+                                               ctypes.c_void_p(lse.data_ptr()), _stream_handle(stream, q.device))
+    if rc != FLEX_OK:
+        raise FlexError(rc, "flex_attention_fwd")
+    return out, lse
+
+
+def flex_device_status(stream=None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the device status word."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(device):
+        return int(load_library().flex_device_status(_stream_handle(stream, device)))

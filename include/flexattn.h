@@ -1,0 +1,191 @@
+/*
+ * flexattn.h -- C-ABI of the GB300 (sm_103a) block-sparse FlexAttention forward.
+ *
+ * Two calls do the work:
+ *   flex_block_mask_create  builds a BlockMask from an enumerated mask_mod;
+ *   flex_attention_fwd      runs softmax(mask(score_mod(Q K^T * scale))) V
+ *                           block-sparsely from that BlockMask and returns the
+ *                           output and the per-row log-sum-exp.
+ * Helpers size the BlockMask buffers, name status codes and read the device
+ * status word.
+ *
+ * Sources of the semantics (web pages on PyTorch FlexAttention):
+ *  - "[Inductor][Flex Attention] Add Subtiling Option for Alpha Scaling"
+ *    (PyTorch PR #167356): the flex_attention higher-order op signature
+ *    flex_attention(q, k, v, score_mod, block_mask, scale, kernel_options),
+ *    the BlockMask tuple (kv_num_blocks, kv_indices, full_kv_num_blocks,
+ *    full_kv_indices, ..., Q_BLOCK = KV_BLOCK = 128, mask_mod), the
+ *    OUTPUT_LOGSUMEXP option, and the online-softmax step forward_block_mn
+ *    (l_i = l_i * alpha + sum(p); acc = acc * alpha; acc += p @ v).
+ *  - "Performance for templated attention strangely bad for a combination of
+ *    causal + upper square mask" (PyTorch issue #124369): masked scores become
+ *    -inf (torch.where); the causal + upper-square predicate
+ *    (q <= 1024 and kv <= 1024) or (q >= kv).
+ *
+ * Conventions shared by every call:
+ *  - Every pointer named "device" is CUDA device memory owned by the caller;
+ *    the library never frees caller memory and keeps no per-call state.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Work is enqueued asynchronously on it; the calls do not
+ *    synchronise the host except where stated.
+ *  - Return value: FLEX_OK (0) or a negative flex_status.  Argument errors
+ *    are detected on the host before anything is enqueued.  A CUDA launch
+ *    error returns FLEX_ERR_CUDA.  A device-side wait that exceeds its time
+ *    limit does not hang: the kernel records FLEX_ERR_DEVICE_TIMEOUT in the
+ *    device status word and returns; read it with flex_device_status().
+ *  - The library allocates one small per-device workspace (the status word)
+ *    with cudaMalloc the first time a device is used; call any entry point
+ *    once before capturing a stream into a CUDA graph.
+ *  - Indices and counts are int32.  Lengths must be multiples of BLOCK = 128.
+ */
+#ifndef FLEXATTN_H
+#define FLEXATTN_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FLEX_API __attribute__((visibility("default")))
+#else
+#define FLEX_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FLEX_OK = 0,
+    FLEX_ERR_INVALID_ARG = -1,     /* null pointer, bad enum, bad scale/parameter            */
+    FLEX_ERR_UNSUPPORTED = -2,     /* head dim, dtype or size outside what the kernels cover  */
+    FLEX_ERR_SHAPE = -3,           /* shapes disagree or lengths are not multiples of BLOCK   */
+    FLEX_ERR_ALIGNMENT = -4,       /* pointer or stride not 16-byte aligned / inner stride!=1 */
+    FLEX_ERR_CUDA = -5,            /* a CUDA runtime/driver call failed                       */
+    FLEX_ERR_DEVICE_TIMEOUT = -6   /* a kernel gave up on a wait (reported by status word)    */
+} flex_status;
+
+/* The enumerated mask_mods (b = batch, h = head, q = query row, kv = key row). */
+typedef enum {
+    FLEX_MASK_CAUSAL = 0,          /* q >= kv                                               */
+    FLEX_MASK_SLIDING_WINDOW = 1,  /* q >= kv and q - kv < window                           */
+    FLEX_MASK_CAUSAL_PREFIX = 2,   /* (q <= prefix and kv <= prefix) or q >= kv (inclusive) */
+    FLEX_MASK_DOCUMENT = 3,        /* doc_ids[b][q] == doc_ids[b][kv] and q >= kv           */
+    FLEX_MASK_ALL = 4              /* every pair (dense attention; for checks and timing)   */
+} flex_mask_kind;
+
+/* The enumerated score_mods, applied to the scaled score s = scale * q.k. */
+typedef enum {
+    FLEX_SCORE_IDENTITY = 0,       /* s                                                     */
+    FLEX_SCORE_SOFTCAP = 1,        /* cap * tanh(s / cap), cap = score_param > 0            */
+    FLEX_SCORE_ALIBI = 2           /* s - slope_h * (q - kv), slope_h = 2^(-8 (h+1) / H)    */
+} flex_score_kind;
+
+typedef enum {
+    FLEX_DTYPE_BF16 = 0,           /* bfloat16 storage; tensor-core path, fp32 accumulation */
+    FLEX_DTYPE_FP32 = 1            /* float32 storage; CUDA-core fp32 path                  */
+} flex_dtype;
+
+/* Parameters of a mask_mod.  Unused fields are ignored for kinds that do not need them. */
+typedef struct {
+    int32_t window;                /* FLEX_MASK_SLIDING_WINDOW: W >= 0 (W = 0 masks everything) */
+    int32_t prefix;                /* FLEX_MASK_CAUSAL_PREFIX: P, inclusive bound                */
+    const int32_t *doc_ids;        /* FLEX_MASK_DOCUMENT: device, [B, Q_LEN] int32, contiguous   */
+} flex_mask_params;
+
+/*
+ * A BlockMask at BLOCK x BLOCK granularity (the BlockMask tuple of the
+ * flex_attention op, kv side).  For every (b, h, q-block qb) and kv block:
+ *   full     the mask_mod is true on the whole tile  -> listed in full_kv_*
+ *   partial  true on some of the tile                -> listed in kv_*
+ *   empty    true nowhere                            -> listed in neither
+ * kv_num_blocks[b,h,qb] counts the partial tiles; kv_indices[b,h,qb,:] holds
+ * their kv-block indices in ascending order followed by all other kv-block
+ * indices in ascending order, so each row is a permutation of 0..NKVB-1.
+ * full_kv_num_blocks / full_kv_indices follow the same layout for full tiles.
+ * The mask kind and parameters are kept because the attention kernel
+ * evaluates the mask_mod on partial tiles only.
+ */
+typedef struct {
+    int32_t B, H, q_len, kv_len, block, nqb, nkvb;
+    int32_t mask_kind;             /* flex_mask_kind the mask was built from      */
+    flex_mask_params params;       /* its parameters (doc_ids stays caller-owned) */
+    int32_t *kv_num_blocks;        /* device, [B, H, NQB]        int32            */
+    int32_t *kv_indices;           /* device, [B, H, NQB, NKVB]  int32            */
+    int32_t *full_kv_num_blocks;   /* device, [B, H, NQB]        int32            */
+    int32_t *full_kv_indices;      /* device, [B, H, NQB, NKVB]  int32            */
+} flex_block_mask;
+
+/* A strided 4-D tensor [B, H, S, D] (strides in elements; stride[3] must be 1). */
+typedef struct {
+    const void *data;              /* device */
+    int32_t dtype;                 /* flex_dtype */
+    int32_t reserved;
+    int64_t shape[4];
+    int64_t stride[4];
+} flex_tensor;
+
+/*
+ * Element counts of the BlockMask buffers for the given sizes:
+ * *num_elems = B*H*NQB (each of kv_num_blocks, full_kv_num_blocks),
+ * *idx_elems = B*H*NQB*NKVB (each of kv_indices, full_kv_indices).
+ * Errors: FLEX_ERR_INVALID_ARG (null outputs, non-positive sizes),
+ * FLEX_ERR_SHAPE (lengths not multiples of block), FLEX_ERR_UNSUPPORTED
+ * (block != 128).
+ */
+FLEX_API int flex_block_mask_sizes(int32_t B, int32_t H, int32_t q_len, int32_t kv_len, int32_t block,
+                          int64_t *num_elems, int64_t *idx_elems);
+
+/*
+ * Build the BlockMask of an enumerated mask_mod on the device (the block
+ * mask that create_block_mask produces for the flex_attention op, see the
+ * BlockMask tuple in PyTorch PR #167356; predicate of the causal + prefix
+ * kind from PyTorch issue #124369).
+ *   in : bm->kv_num_blocks, kv_indices, full_kv_num_blocks, full_kv_indices
+ *        point to caller-allocated device buffers sized by flex_block_mask_sizes.
+ *   out: every other field of *bm is filled (sizes, mask kind, parameters), and
+ *        the four buffers are written by a kernel enqueued on `stream`.
+ * params may be NULL for kinds without parameters.  doc_ids must stay valid
+ * while the BlockMask is used by flex_attention_fwd.
+ * Errors: FLEX_ERR_INVALID_ARG, FLEX_ERR_SHAPE, FLEX_ERR_UNSUPPORTED
+ * (block != 128, or NKVB > 1024), FLEX_ERR_CUDA.
+ */
+FLEX_API int flex_block_mask_create(int32_t mask_kind, const flex_mask_params *params, int32_t B, int32_t H,
+                           int32_t q_len, int32_t kv_len, int32_t block, flex_block_mask *bm,
+                           void *stream);
+
+/*
+ * Block-sparse attention forward (the flex_attention op of PyTorch PR
+ * #167356 with OUTPUT_LOGSUMEXP): for every (b, h, q)
+ *   s[kv]   = score_mod(scale * q.k[kv])   on every tile listed in bm
+ *   s[kv]   = -inf where mask_mod is false (evaluated on partial tiles only;
+ *             tiles in neither list are skipped entirely)
+ *   out[q]  = sum_kv exp(s[kv] - lse[q]) v[kv],  lse[q] = ln sum_kv exp(s[kv])
+ * and a row with no unmasked score gets out = 0, lse = -inf.
+ *   q    : [B, H, q_len, D];  k, v : [B, H, kv_len, D]; same dtype, B, H, D.
+ *          D in {64, 128}.  bf16 needs 16-byte-aligned base and strides.
+ *   bm   : a BlockMask for (B, H, q_len, kv_len) from flex_block_mask_create.
+ *   score_kind, score_param : flex_score_kind and the softcap value.
+ *   scale: multiplies q.k before score_mod (finite).
+ *   out  : device, contiguous [B, H, q_len, D] in q's dtype, 16-byte aligned.
+ *   lse  : device, contiguous [B, H, q_len] float32, natural logarithm.
+ * Errors: FLEX_ERR_INVALID_ARG, FLEX_ERR_SHAPE, FLEX_ERR_ALIGNMENT,
+ * FLEX_ERR_UNSUPPORTED, FLEX_ERR_CUDA.  Asynchronous on `stream`.
+ */
+FLEX_API int flex_attention_fwd(const flex_tensor *q, const flex_tensor *k, const flex_tensor *v,
+                       const flex_block_mask *bm, int32_t score_kind, float score_param,
+                       float scale, void *out, float *lse, void *stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of
+ * the current device: FLEX_OK, or FLEX_ERR_DEVICE_TIMEOUT if a kernel gave up
+ * on a wait since the last call.  FLEX_ERR_CUDA if the synchronisation failed.
+ */
+FLEX_API int flex_device_status(void *stream);
+
+/* A static, human-readable name for a flex_status value. */
+FLEX_API const char *flex_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLEXATTN_H */

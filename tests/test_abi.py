@@ -1,0 +1,140 @@
+"""The C-ABI library builds for sm_103a, loads, exports every symbol the
+header declares, and rejects bad arguments on the host (no GPU needed: every
+call here fails validation before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_sparse_masked_blockmask_gb300 import _build, flexattn as fa
+
+HEADER = os.path.join(_build.INCLUDE, "flexattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return fa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"FLEX_API\s+[\w\s\*]+?\b(flex_\w+)\s*\(", text)
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    assert sorted(names) == sorted(fa.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in (fa.FLEX_OK, fa.FLEX_ERR_INVALID_ARG, fa.FLEX_ERR_UNSUPPORTED, fa.FLEX_ERR_SHAPE,
+                 fa.FLEX_ERR_ALIGNMENT, fa.FLEX_ERR_CUDA, fa.FLEX_ERR_DEVICE_TIMEOUT):
+        s = fa.flex_status_string(code)
+        assert s and s != "unknown status"
+    assert fa.flex_status_string(12345) == "unknown status"
+
+
+def test_block_mask_sizes(lib):
+    assert fa.flex_block_mask_sizes(2, 32, 16384, 16384) == (2 * 32 * 128, 2 * 32 * 128 * 128)
+    assert fa.flex_block_mask_sizes(1, 1, 128, 384) == (1, 3)
+    for args, code in [((0, 1, 128, 128), fa.FLEX_ERR_INVALID_ARG),
+                       ((1, 1, 100, 128), fa.FLEX_ERR_SHAPE),
+                       ((1, 1, 128, 130), fa.FLEX_ERR_SHAPE),
+                       ((1, 1, 128, 128, 64), fa.FLEX_ERR_UNSUPPORTED),
+                       ((1, 1, 128, 128 * 1025), fa.FLEX_ERR_UNSUPPORTED)]:
+        with pytest.raises(fa.FlexError) as e:
+            fa.flex_block_mask_sizes(*args)
+        assert e.value.code == code, args
+
+
+def _call_create(lib, kind, params, B=1, H=1, q=256, kv=256, block=128, buffers=True):
+    bm = fa.flex_block_mask()
+    if buffers:  # non-null dummies: validation must fail before they are touched
+        bm.kv_num_blocks = bm.kv_indices = bm.full_kv_num_blocks = bm.full_kv_indices = 0x1000
+    p = None if params is None else ctypes.byref(params)
+    return lib.flex_block_mask_create(kind, p, B, H, q, kv, block, ctypes.byref(bm), None)
+
+
+def test_block_mask_create_rejects_bad_arguments(lib):
+    assert _call_create(lib, 7, None) == fa.FLEX_ERR_INVALID_ARG
+    assert _call_create(lib, fa.FLEX_MASK_CAUSAL, None, buffers=False) == fa.FLEX_ERR_INVALID_ARG
+    assert _call_create(lib, fa.FLEX_MASK_CAUSAL, None, q=200) == fa.FLEX_ERR_SHAPE
+    assert _call_create(lib, fa.FLEX_MASK_CAUSAL, None, block=64) == fa.FLEX_ERR_UNSUPPORTED
+    assert _call_create(lib, fa.FLEX_MASK_SLIDING_WINDOW, None) == fa.FLEX_ERR_INVALID_ARG
+    assert _call_create(lib, fa.FLEX_MASK_SLIDING_WINDOW, fa.flex_mask_params(-1, 0, None)) == \
+        fa.FLEX_ERR_INVALID_ARG
+    assert _call_create(lib, fa.FLEX_MASK_DOCUMENT, fa.flex_mask_params(0, 0, None)) == fa.FLEX_ERR_INVALID_ARG
+    assert _call_create(lib, fa.FLEX_MASK_DOCUMENT, fa.flex_mask_params(0, 0, 0x1000), kv=384) == \
+        fa.FLEX_ERR_SHAPE
+    assert _call_create(lib, fa.FLEX_MASK_DOCUMENT, fa.flex_mask_params(0, 0, 0x1004)) == fa.FLEX_ERR_ALIGNMENT
+
+
+def _tensor(dtype, shape, stride=None, data=0x10000):
+    t = fa.flex_tensor()
+    t.data = data
+    t.dtype = dtype
+    if stride is None:
+        stride = [shape[1] * shape[2] * shape[3], shape[2] * shape[3], shape[3], 1]
+    for i in range(4):
+        t.shape[i] = shape[i]
+        t.stride[i] = stride[i]
+    return t
+
+
+def _mask_struct(B=1, H=2, q=256, kv=256, kind=fa.FLEX_MASK_CAUSAL):
+    bm = fa.flex_block_mask()
+    bm.B, bm.H, bm.q_len, bm.kv_len, bm.block = B, H, q, kv, 128
+    bm.nqb, bm.nkvb, bm.mask_kind = q // 128, kv // 128, kind
+    bm.kv_num_blocks = bm.kv_indices = bm.full_kv_num_blocks = bm.full_kv_indices = 0x1000
+    return bm
+
+
+def _fwd(lib, q, k, v, bm, score=fa.FLEX_SCORE_IDENTITY, param=0.0, scale=0.125, out=0x20000, lse=0x30000):
+    return lib.flex_attention_fwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(bm), score,
+                                  param, scale, ctypes.c_void_p(out), ctypes.c_void_p(lse), None)
+
+
+def test_attention_rejects_bad_arguments(lib):
+    bf = fa.FLEX_DTYPE_BF16
+    q = _tensor(bf, [1, 2, 256, 64])
+    bm = _mask_struct()
+    cases = [
+        (dict(q=_tensor(bf, [1, 2, 256, 96]), k=_tensor(bf, [1, 2, 256, 96]), v=_tensor(bf, [1, 2, 256, 96])),
+         fa.FLEX_ERR_UNSUPPORTED),
+        (dict(k=_tensor(fa.FLEX_DTYPE_FP32, [1, 2, 256, 64])), fa.FLEX_ERR_INVALID_ARG),
+        (dict(k=_tensor(bf, [1, 3, 256, 64])), fa.FLEX_ERR_SHAPE),
+        (dict(v=_tensor(bf, [1, 2, 256, 64], stride=[32768, 16384, 64, 2])), fa.FLEX_ERR_ALIGNMENT),
+        (dict(v=_tensor(bf, [1, 2, 256, 64], stride=[32768, 16384, 68, 1])), fa.FLEX_ERR_ALIGNMENT),
+        (dict(k=_tensor(bf, [1, 2, 256, 64], data=0x10002)), fa.FLEX_ERR_ALIGNMENT),
+        (dict(out=0x20008), fa.FLEX_ERR_ALIGNMENT),
+        (dict(lse=0), fa.FLEX_ERR_INVALID_ARG),
+        (dict(score=3), fa.FLEX_ERR_INVALID_ARG),
+        (dict(score=fa.FLEX_SCORE_SOFTCAP, param=0.0), fa.FLEX_ERR_INVALID_ARG),
+        (dict(scale=float("nan")), fa.FLEX_ERR_INVALID_ARG),
+        (dict(bm=_mask_struct(H=3)), fa.FLEX_ERR_SHAPE),
+        (dict(bm=_mask_struct(q=384, kv=384)), fa.FLEX_ERR_SHAPE),
+        (dict(bm=_mask_struct(kind=9)), fa.FLEX_ERR_INVALID_ARG),
+        (dict(q=_tensor(bf, [1, 2, 200, 64]), bm=_mask_struct(q=200)), fa.FLEX_ERR_SHAPE),
+    ]
+    for change, code in cases:
+        args = dict(q=q, k=_tensor(bf, [1, 2, 256, 64]), v=_tensor(bf, [1, 2, 256, 64]), bm=bm)
+        args.update(change)
+        rc = _fwd(lib, args.pop("q"), args.pop("k"), args.pop("v"), args.pop("bm"), **args)
+        assert rc == code, (change, rc)
+
+
+def test_product_path_has_no_oracle_dependency():
+    pkg = os.path.dirname(_build.__file__)
+    for root, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(root, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "liboracle" not in text, f

@@ -1,0 +1,154 @@
+"""Attention forward (bf16 tensor-core and fp32 paths) vs the float64 oracle.
+
+Tolerances: bf16 out max-abs 1e-2, LSE 5e-3; fp32 1e-4 on both.  The five
+synthetic configurations run in the launch configuration the bench times;
+the large ones are checked on sampled rows (the oracle computes rows one by
+one) plus properties over every row.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_masked_blockmask_gb300 import flexattn as fa
+from block_sparse_masked_blockmask_gb300 import workloads as W
+from gpu_harness import TOL, compare, device_tensor, run_attention, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle(w, q, k, v, docs, rows=None):
+    return oracle.workload_attention(w, q, k, v, docs, rows=rows)
+
+
+@pytest.mark.parametrize("w", W.CONFIGS, ids=lambda w: w.name)
+def test_configs(w):
+    q, k, v, docs = W.workload_inputs(w)
+    out, lse, _ = run_attention(q, k, v, w.mask, w.score, w.scale, w.dtype, w.window, w.prefix, docs,
+                                w.score_param)
+    # every row of these masks sees its diagonal: no empty rows anywhere
+    assert np.all(np.isfinite(lse)) and np.all(np.isfinite(out))
+    if w.B * w.H * w.S <= 2 * 8 * 2048:
+        ref_out, ref_lse = _oracle(w, q, k, v, docs)
+        compare(out, lse, ref_out, ref_lse, w.dtype, w.name)
+    else:
+        rows = sample_rows(w.B, w.H, w.S, 512)
+        ref_out, ref_lse = _oracle(w, q, k, v, docs, rows)
+        D = w.D
+        compare(out.reshape(-1, D)[rows], lse.reshape(-1)[rows], ref_out, ref_lse, w.dtype, w.name)
+
+
+MASKS = [
+    (W.MASK_CAUSAL, {}),
+    (W.MASK_SLIDING_WINDOW, {"window": 100}),
+    (W.MASK_SLIDING_WINDOW, {"window": 129}),
+    (W.MASK_CAUSAL_PREFIX, {"prefix": 200}),
+    (W.MASK_DOCUMENT, {}),
+    (W.MASK_ALL, {}),
+]
+SCORES = [(W.SCORE_IDENTITY, 0.0), (W.SCORE_SOFTCAP, 50.0), (W.SCORE_SOFTCAP, 2.0), (W.SCORE_ALIBI, 0.0)]
+
+
+def _docs(B, S, seed):
+    rng = np.random.default_rng(seed)
+    d = np.zeros((B, S), np.int32)
+    for b in range(B):
+        cuts = np.sort(rng.choice(np.arange(1, S), size=3, replace=False))
+        for c in cuts:
+            d[b, c:] += 1
+    return d
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("mask,mkw", MASKS, ids=lambda x: str(x))
+@pytest.mark.parametrize("score,param", SCORES, ids=lambda x: str(x))
+def test_kinds_small(dtype, D, mask, mkw, score, param):
+    # S = 384: three q blocks, so one CTA pair is ragged (a single Q tile)
+    B, H, S = 2, 3, 384
+    q, k, v = W.draw_qkv(B, H, S, D, seed=7, dtype=dtype)
+    docs = _docs(B, S, 3) if mask == W.MASK_DOCUMENT else None
+    scale = 1.0 / np.sqrt(D)
+    out, lse, _ = run_attention(q, k, v, mask, score, scale, dtype, doc_ids=docs, score_param=param, **mkw)
+    ref_out, ref_lse = oracle.attention(q, k, v, mask, score, scale, doc_ids=docs, score_param=param, **mkw)
+    compare(out, lse, ref_out, ref_lse, dtype, f"{dtype} D{D} m{mask} s{score}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_fully_masked_rows(dtype):
+    B, H, S, D = 1, 2, 256, 64
+    q, k, v = W.draw_qkv(B, H, S, D, seed=9, dtype=dtype)
+    out, lse, _ = run_attention(q, k, v, W.MASK_SLIDING_WINDOW, W.SCORE_IDENTITY, 0.125, dtype, window=0)
+    assert np.all(out == 0.0) and np.all(np.isneginf(lse))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("score", [W.SCORE_IDENTITY, W.SCORE_ALIBI])
+def test_single_key_rows_return_v(dtype, score):
+    B, H, S, D = 1, 2, 384, 128
+    q, k, v = W.draw_qkv(B, H, S, D, seed=10, dtype=dtype)
+    out, lse, _ = run_attention(q, k, v, W.MASK_SLIDING_WINDOW, score, 0.1, dtype, window=1)
+    tol = TOL[dtype][0]
+    assert np.max(np.abs(out - v)) <= (0.0 if dtype == "bf16" else tol)
+    diag = 0.1 * np.einsum("bhsd,bhsd->bhs", q.astype(np.float64), k.astype(np.float64))
+    assert np.max(np.abs(lse - diag)) <= TOL[dtype][1]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("q_len,kv_len", [(256, 640), (640, 256)])
+@pytest.mark.parametrize("mask", [W.MASK_CAUSAL, W.MASK_ALL])
+def test_rectangular(dtype, q_len, kv_len, mask):
+    B, H, D = 1, 2, 64
+    rng = np.random.default_rng(11)
+    q = rng.standard_normal((B, H, q_len, D), dtype=np.float32)
+    k = rng.standard_normal((B, H, kv_len, D), dtype=np.float32)
+    v = rng.standard_normal((B, H, kv_len, D), dtype=np.float32)
+    if dtype == "bf16":
+        q, k, v = W.round_to_bf16(q), W.round_to_bf16(k), W.round_to_bf16(v)
+    out, lse, _ = run_attention(q, k, v, mask, W.SCORE_IDENTITY, 0.125, dtype)
+    ref_out, ref_lse = oracle.attention(q, k, v, mask, W.SCORE_IDENTITY, 0.125)
+    compare(out, lse, ref_out, ref_lse, dtype, "rect")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_strided_inputs(dtype):
+    # q, k, v as [B, S, H, D] buffers viewed as [B, H, S, D]
+    B, H, S, D = 2, 4, 512, 128
+    q, k, v = W.draw_qkv(B, H, S, D, seed=12, dtype=dtype)
+    dev = [device_tensor(np.ascontiguousarray(x.transpose(0, 2, 1, 3)), dtype).permute(0, 2, 1, 3)
+           for x in (q, k, v)]
+    assert not dev[0].is_contiguous()
+    out, lse, _ = run_attention(q, k, v, W.MASK_CAUSAL, W.SCORE_SOFTCAP, 1 / np.sqrt(D), dtype,
+                                score_param=30.0, device_inputs=dev)
+    ref_out, ref_lse = oracle.attention(q, k, v, W.MASK_CAUSAL, W.SCORE_SOFTCAP, 1 / np.sqrt(D), score_param=30.0)
+    compare(out, lse, ref_out, ref_lse, dtype, "strided")
+
+
+def test_deterministic_and_status_clean():
+    w = W.scaled(W.BF16_DOC_SOFTCAP_S8192, B=2, H=2, S=2048)
+    q, k, v, docs = W.workload_inputs(w)
+    a = run_attention(q, k, v, w.mask, w.score, w.scale, w.dtype, doc_ids=docs, score_param=w.score_param)
+    b = run_attention(q, k, v, w.mask, w.score, w.scale, w.dtype, doc_ids=docs, score_param=w.score_param)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert fa.flex_device_status() == fa.FLEX_OK
+
+
+def test_slice_invariance():
+    # a (b, h) slice of a batched run equals a standalone B = H = 1 run
+    B, H, S, D = 2, 3, 512, 64
+    q, k, v = W.draw_qkv(B, H, S, D, seed=13)
+    out, lse, _ = run_attention(q, k, v, W.MASK_CAUSAL, W.SCORE_IDENTITY, 0.125, "bf16")
+    for b, h in [(0, 0), (1, 2)]:
+        o1, l1, _ = run_attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1],
+                                  W.MASK_CAUSAL, W.SCORE_IDENTITY, 0.125, "bf16")
+        assert np.array_equal(o1[0, 0], out[b, h]) and np.array_equal(l1[0, 0], lse[b, h])
+
+
+def test_inputs_not_modified():
+    B, H, S, D = 1, 2, 256, 128
+    q, k, v = W.draw_qkv(B, H, S, D, seed=14)
+    dev = [device_tensor(x, "bf16") for x in (q, k, v)]
+    before = [t.clone() for t in dev]
+    run_attention(q, k, v, W.MASK_CAUSAL, W.SCORE_ALIBI, 0.125, "bf16", device_inputs=dev)
+    for a, b in zip(dev, before):
+        assert torch.equal(a, b)
