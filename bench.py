@@ -1,0 +1,379 @@
+"""Benchmark of the block-sparse FlexAttention forward on one GB300.
+
+A step is one pass of the hot path over the workload already resident in
+HBM: the BlockMask build (flex_block_mask_create) and the attention forward
+(flex_attention_fwd), both through the C-ABI.  The metric is forward TFLOP/s
+counted over unmasked blocks only (4 * 128 * 128 * D per full or partial
+tile), also given as a fraction of the dense bf16 tensor peak.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the float64 CPU
+oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_sparse_masked_blockmask_gb300 import workloads as W  # noqa: E402
+
+METRIC = "flex-attn fwd TFLOP/s (unmasked blocks) and % of GB300 bf16 tensor peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_bf16_traffic.txt")
+KERNEL_SOURCES = ["attn_bf16_kernel.cuh", "attn_bf16_launch.cuh", "attn_bf16.cu", "attn_bf16_d64.cu",
+                  "attn_bf16_d128.cu", "ptx.cuh", "flex_internal.h"]
+
+
+def workload_by_name(name: str) -> W.Workload:
+    for w in W.CONFIGS:
+        if w.name == name:
+            return w
+    raise SystemExit(f"unknown workload {name}; choose from {[w.name for w in W.CONFIGS]}")
+
+
+def tile_counts(bm: dict) -> np.ndarray:
+    """Computed tiles (full + partial) per (b, h, q block)."""
+    return bm["kv_num_blocks"].astype(np.int64) + bm["full_kv_num_blocks"].astype(np.int64)
+
+
+def unmasked_block_flops(w: W.Workload, bm: dict) -> float:
+    return float(tile_counts(bm).sum()) * 4.0 * 128 * 128 * w.D
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16": float(d["bf16_tflops"]), "bf16_sustained": float(d.get("bf16_tflops_sustained", 0.0)),
+                "hbm": float(d["hbm_gbs"]), "source": "measured"}
+    return {"bf16": FALLBACK_BF16_TFLOPS, "bf16_sustained": 0.0, "hbm": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def kernel_sources_digest() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "block_sparse_masked_blockmask_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel sources."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    rec = {}
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if "=" in line and not line.startswith("#"):
+                k, v = line.strip().split("=", 1)
+                rec[k.strip()] = v.strip()
+    if rec.get("workload") != workload or rec.get("sources_sha256_16") != kernel_sources_digest():
+        return None
+    try:
+        return float(rec["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.15)
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_rows_baseline(w: W.Workload, q, k, v, docs, bm: dict, budget_s: float) -> dict:
+    """The float64 oracle timed on a bounded sample of the workload's rows (host cores)."""
+    import oracle
+    tiles = tile_counts(bm)  # [B, H, NQB]
+    total_rows = w.B * w.H * w.S
+    rng = np.random.default_rng(5)
+
+    def run(n):
+        rows = np.sort(rng.choice(total_rows, size=min(n, total_rows), replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.workload_attention(w, q, k, v, docs, rows=rows)
+        dt = time.perf_counter() - t0
+        i = rows % w.S
+        bh = rows // w.S
+        flops = float((tiles.reshape(-1, tiles.shape[-1])[bh, i // 128] * 4.0 * 128 * w.D).sum())
+        return rows.size, dt, flops
+
+    n0, t0, _ = run(256)
+    n = int(min(total_rows, max(256, n0 * budget_s / max(t0, 1e-3))))
+    n, dt, flops = run(n)
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} of {total_rows} query rows of {w.name} (all keys of each row, float64), "
+                      f"{dt:.1f} s; TFLOP/s credits each row its share of unmasked-block FLOPs"}
+
+
+def run_reference(args, w: W.Workload) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    q, k, v, docs = W.workload_inputs(w)
+    import oracle
+    bm = oracle.workload_block_mask(w, docs)
+    # each step is a bounded sample; the whole run stays within a few minutes
+    per_step = args.ref_seconds if args.ref_seconds > 0 else min(6.0, 150.0 / (args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_rows_baseline(w, q, k, v, docs, bm, budget_s=min(per_step, 0.5))
+    vals, secs = [], []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        r = oracle_rows_baseline(w, q, k, v, docs, bm, budget_s=per_step)
+        secs.append(time.perf_counter() - t0)
+        vals.append(r["value"])
+    value = float(np.median(vals))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * float(np.median(secs)),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+                             "sample": r["sample"]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w: W.Workload) -> dict:
+    c = {"workload": w.name, "B": w.B, "H": w.H, "S": w.S, "D": w.D, "block": 128,
+         "mask": W.MASK_NAMES[w.mask], "score": W.SCORE_NAMES[w.score], "scale": w.scale,
+         "input_dtype": w.dtype}
+    if w.mask == W.MASK_SLIDING_WINDOW:
+        c["window"] = w.window
+    if w.mask == W.MASK_CAUSAL_PREFIX:
+        c["prefix"] = w.prefix
+    if w.score == W.SCORE_SOFTCAP:
+        c["softcap"] = w.softcap
+    qkv_bytes = 3 * w.B * w.H * w.S * w.D * (2 if w.dtype == "bf16" else 4)
+    c["l2"] = (f"inputs larger than L2 ({qkv_bytes / 2**20:.0f} MiB of Q/K/V vs 129 MiB), no flush"
+               if qkv_bytes > L2_BYTES else "L2 flushed between steps (256 MiB write)")
+    return c
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=W.BF16_CAUSAL_ALIBI_S16384.name)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget (cpu_baseline)")
+    ap.add_argument("--ref-seconds", type=float, default=0.0,
+                    help="oracle sample budget per reference step (0: fit the run in ~150 s)")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None, help="override B (profiling a smaller case)")
+    ap.add_argument("--heads", type=int, default=None, help="override H (profiling a smaller case)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = workload_by_name(args.workload)
+    if args.batch or args.heads:
+        w = W.scaled(w, B=args.batch or w.B, H=args.heads or w.H, name=w.name + "_profiling_subset")
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+    run_ours(args, w)
+
+
+def run_ours(args, w: W.Workload) -> None:
+    import torch
+    from block_sparse_masked_blockmask_gb300 import flexattn as fa
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    q, k, v, docs = W.workload_inputs(w)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+
+    def to_dev(x):
+        if w.dtype == "bf16":
+            return torch.from_numpy(W.bf16_bits(x).view(np.int16)).cuda().view(torch.bfloat16)
+        return torch.from_numpy(x).cuda()
+
+    dq, dk, dv = to_dev(q), to_dev(k), to_dev(v)
+    dd = torch.from_numpy(docs).cuda() if docs is not None else None
+    out = torch.empty_like(dq)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    flush = None
+    if 3 * dq.numel() * dq.element_size() <= L2_BYTES:
+        flush = torch.empty(256 * 2**20, dtype=torch.uint8, device="cuda")
+
+    def step():
+        bm = fa.flex_block_mask_create(w.mask, w.B, w.H, w.S, w.S, 128, window=w.window, prefix=w.prefix,
+                                       doc_ids=dd, stream=stream)
+        fa.flex_attention_fwd(dq, dk, dv, bm, w.score, w.score_param, w.scale, out=out, lse=lse, stream=stream)
+        return bm
+
+    bm = None
+    for _ in range(args.warmup):
+        bm = step()
+    torch.cuda.synchronize()
+    if fa.flex_device_status() != fa.FLEX_OK:
+        raise SystemExit("device status reported a timeout during warm-up")
+    bm_host = bm.as_numpy()
+    flops = unmasked_block_flops(w, bm_host)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            bmi = fa.flex_block_mask_create(w.mask, w.B, w.H, w.S, w.S, 128, window=w.window, prefix=w.prefix,
+                                            doc_ids=dd, stream=stream)
+            e1.record(stream)
+            fa.flex_attention_fwd(dq, dk, dv, bmi, w.score, w.score_param, w.scale, out=out, lse=lse,
+                                  stream=stream)
+            e2.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    if fa.flex_device_status() != fa.FLEX_OK:
+        raise SystemExit("device status reported a timeout during the timed region")
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    attn_ms = [b.elapsed_time(c) for _, b, c in ev]
+    total_ms = float(np.sum(step_ms))
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the public API: host inputs in, host outputs back, every step
+    hq, hk, hv = (x.cpu().pin_memory() for x in (dq, dk, dv))
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    hdoc = torch.from_numpy(docs).pin_memory() if docs is not None else None
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv)) + (hdoc.numel() * 4 if hdoc is not None else 0)
+    d2h = hout.numel() * hout.element_size() + hlse.numel() * 4
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        if hdoc is not None:
+            dd.copy_(hdoc, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    e2e = None
+    if args.e2e_steps > 0:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / args.e2e_steps
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        return
+    peaks = measured_peaks()
+    attn_mean_ms = float(np.mean(attn_ms))
+    achieved = flops / (attn_mean_ms * 1e-3) / 1e12
+    traffic = recorded_traffic(w.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16"], "traffic": traffic,
+                "kernel": "attn_bf16_kernel" if w.dtype == "bf16" else "attn_fp32_kernel",
+                "peak_source": f"{peaks['source']} bf16 burst (dense cuBLAS)",
+                "achieved_hbm_gbs": None if traffic is None else traffic / (attn_mean_ms * 1e-3) / 1e9,
+                "algorithmic_flops_per_launch": flops, "mean_launch_ms": attn_mean_ms}
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = oracle_rows_baseline(w, q, k, v, docs, bm_host, budget_s=args.cpu_seconds)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": config_dict(w), "pct_of_bf16_peak": 100.0 * value / peaks["bf16"],
+            "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 2 * args.steps, "clocks": clocks.summary(),
+            "attn_ms_per_launch": {"mean": attn_mean_ms, "median": float(np.median(attn_ms)),
+                                   "min": float(np.min(attn_ms))},
+            "block_mask_ms_per_launch": float(np.mean(np.asarray(step_ms) - np.asarray(attn_ms)))}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
