@@ -52,6 +52,16 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // raise the running max only beyond 2^8
+// Register split.  Three warps share each SM sub-partition's 64 KB register
+// file, so the kernel is compiled to kRegsAtLaunch (168) registers per thread.
+// The softmax warpgroups then raise their budget to kRegsSoftmax while the
+// TMA/MMA warpgroup lowers its own to kRegsControl; per sub-partition this is
+// 2 * 224 + 56 = 3 * 168 registers per lane, so the increase never waits on
+// registers that are not released.  The launcher checks the compiled count.
+constexpr uint32_t kRegsAtLaunch = 168;
+constexpr uint32_t kRegsSoftmax = 224;
+constexpr uint32_t kRegsControl = 56;
+static_assert(2 * kRegsSoftmax + kRegsControl == 3 * kRegsAtLaunch, "register split");
 
 struct Bf16Params {
     int B, H, q_len, kv_len, nqb, nkvb, npairs;
@@ -66,13 +76,14 @@ struct Bf16Params {
 // Shared-memory bookkeeping that follows the Q/K/V tiles.
 struct AttnMisc {
     uint64_t q_full;
-    uint64_t k_full[4], v_full[4], kv_empty[4];
+    uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];
     uint64_t s_full[2], p_full[2];
     uint64_t o_full, drain;
     uint32_t tmem_base;
     int abort;
     int n_union;
     int pad;
+    float alibi_tbl[128];          // log2(e) slope_h c, c = 0..127 (ALiBi score_mod)
     uint32_t flags[kMaxKvBlocks];  // bit0 present in tile 0, bit1 full in tile 0, bit2/bit3 same for tile 1
     uint32_t ulist[kMaxKvBlocks];  // union, descending kv: kv block | flags << 16
 };
@@ -140,6 +151,32 @@ __device__ __forceinline__ void tmem_ld64_sync(uint32_t taddr, uint32_t (&r)[64]
         : "memory");
 }
 
+// TMEM read of 128 columns of this thread's lane as four 32-column loads
+// (smaller register vectors than one x128) with a single wait.
+__device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t (&r)[128]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%129];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64, %65, %66, %67, %68, %69, %70, %71, %72, %73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, %90, %91, %92, %93, %94, %95}, [%130];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%96, %97, %98, %99, %100, %101, %102, %103, %104, %105, %106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, %120, %121, %122, %123, %124, %125, %126, %127}, [%131];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+        : "r"(taddr), "r"(taddr + 32), "r"(taddr + 64), "r"(taddr + 96)
+        : "memory");
+}
+
+// Each thread of the warp writes 64 consecutive 32-bit columns of its own lane.
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, "
+        "%33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, "
+        "%49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63, %64};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]), "r"(r[32]), "r"(r[33]), "r"(r[34]), "r"(r[35]), "r"(r[36]), "r"(r[37]), "r"(r[38]), "r"(r[39]), "r"(r[40]), "r"(r[41]), "r"(r[42]), "r"(r[43]), "r"(r[44]), "r"(r[45]), "r"(r[46]), "r"(r[47]), "r"(r[48]), "r"(r[49]), "r"(r[50]), "r"(r[51]), "r"(r[52]), "r"(r[53]), "r"(r[54]), "r"(r[55]), "r"(r[56]), "r"(r[57]), "r"(r[58]), "r"(r[59]), "r"(r[60]), "r"(r[61]), "r"(r[62]), "r"(r[63])
+        : "memory");
+}
+
 // TMEM read of 32 columns of this thread's lane, completed before returning.
 __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -156,61 +193,95 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]
         : "memory");
 }
 
-// score_mod in base-2 units: x = log2(e) * score_mod(scale * s).
+// score_mod in base-2 units, two columns (c, c+1) at a time on packed fp32x2:
+//   identity : x = k0 s                              k0 = scale log2(e)
+//   softcap  : x = k2 + k1 / (2^(k0 s) + 1)          = log2(e) cap tanh(scale s / cap)
+//   ALiBi    : x = k0 s + slope2 c                   slope2 = log2(e) slope_h
+// For ALiBi the per-tile term slope2 (kv0 - q) is kept out of x as `offset`:
+// it shifts the whole row, so it is added to the row max and subtracted in
+// the exponent instead of being added to every element.
 template <int SCORE>
 struct ScoreLog2 {
-    float k0, k1, k2;  // per-kind constants
-    float base;        // ALiBi: log2(e) * slope_h * (kv0 - q), per tile
-    float slope2;      // ALiBi: log2(e) * slope_h
-    __device__ __forceinline__ void init(const Bf16Params &p, int h) {
+    uint64_t k0, k1, k2, one;
+    float slope2, offset;
+    const float *tbl;  // ALiBi: slope2 * c for c = 0..127, in shared memory
+    __device__ __forceinline__ void init(const Bf16Params &p, int h, const float *table) {
+        float a0, a1 = 0.f, a2 = 0.f;
         if constexpr (SCORE == FLEX_SCORE_SOFTCAP) {
-            // cap * tanh(y) = cap - 2 cap / (exp(2y) + 1),  y = scale * s / cap
-            k0 = 2.f * p.scale * kLog2e / p.score_param;
-            k1 = -2.f * p.score_param * kLog2e;
-            k2 = p.score_param * kLog2e;
+            // cap tanh(y) = cap - 2 cap / (exp(2y) + 1),  y = scale s / cap
+            a0 = 2.f * p.scale * kLog2e / p.score_param;
+            a1 = -2.f * p.score_param * kLog2e;
+            a2 = p.score_param * kLog2e;
         } else {
-            k0 = p.scale * kLog2e;
-            k1 = k2 = 0.f;
+            a0 = p.scale * kLog2e;
         }
+        k0 = f2_pack(a0, a0);
+        k1 = f2_pack(a1, a1);
+        k2 = f2_pack(a2, a2);
+        one = f2_pack(1.f, 1.f);
         slope2 = SCORE == FLEX_SCORE_ALIBI ? kLog2e * exp2f(-8.f * (float)(h + 1) / (float)p.H) : 0.f;
-        base = 0.f;
+        offset = 0.f;
+        tbl = table;
     }
     __device__ __forceinline__ void tile(int kv0, int q) {
-        if constexpr (SCORE == FLEX_SCORE_ALIBI) base = slope2 * (float)(kv0 - q);
+        if constexpr (SCORE == FLEX_SCORE_ALIBI) offset = slope2 * (float)(kv0 - q);
     }
-    __device__ __forceinline__ float operator()(float s, int c) const {
+    // columns 2j, 2j+1
+    __device__ __forceinline__ uint64_t pair(uint64_t s2, int j) const {
         if constexpr (SCORE == FLEX_SCORE_SOFTCAP) {
-            const float t = ex2_approx(s * k0);
-            return fmaf(k1, rcp_approx(t + 1.f), k2);
+            float t0, t1;
+            f2_unpack(f2_mul(s2, k0), t0, t1);
+            float u0, u1;
+            f2_unpack(f2_add(f2_pack(ex2_approx(t0), ex2_approx(t1)), one), u0, u1);
+            return f2_fma(k1, f2_pack(rcp_approx(u0), rcp_approx(u1)), k2);
         } else if constexpr (SCORE == FLEX_SCORE_ALIBI) {
-            return fmaf(s, k0, fmaf((float)c, slope2, base));
+            return f2_fma(s2, k0, reinterpret_cast<const uint64_t *>(tbl)[j]);
         } else {
-            return s * k0;
+            return f2_mul(s2, k0);
         }
     }
 };
 
-// mask_mod on a partial tile for row q (columns kv0 .. kv0 + 127).
-__device__ __forceinline__ void apply_partial_mask(const MaskDesc &m, int b, int q, int kv0, float (&x)[128]) {
+// mask_mod on a partial tile for row q (columns kv0 .. kv0 + 127), on the
+// packed score pairs.
+__device__ __forceinline__ uint64_t keep_pair(uint64_t v, bool k0, bool k1) {
+    float a, b;
+    f2_unpack(v, a, b);
+    return f2_pack(k0 ? a : -INFINITY, k1 ? b : -INFINITY);
+}
+
+__device__ __forceinline__ void apply_partial_mask(const MaskDesc &m, int b, int q, int kv0, uint64_t (&x2)[64]) {
     int lo, hi;
     if (mask_row_interval(m, q, lo, hi)) {
         const int clo = lo - kv0, chi = hi - kv0;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = (c >= clo && c <= chi) ? x[c] : -INFINITY;
+        for (int j = 0; j < 64; ++j)
+            x2[j] = keep_pair(x2[j], 2 * j >= clo && 2 * j <= chi, 2 * j + 1 >= clo && 2 * j + 1 <= chi);
     } else {  // document: same document id and kv <= q
         const int32_t *dr = m.doc_ids + (int64_t)b * m.doc_len;
         const int dq = __ldg(dr + q);
         const int lim = q - kv0;
         const int4 *dk = reinterpret_cast<const int4 *>(dr + kv0);
+        // keep-bits of the 128 columns in four words (rolled loads), then one
+        // fully unrolled pass so the scores stay in registers
+        uint32_t keep[4];
 #pragma unroll
-        for (int c4 = 0; c4 < 32; ++c4) {
-            const int4 d = __ldg(dk + c4);
-            const int c = 4 * c4;
-            x[c + 0] = (c + 0 <= lim && d.x == dq) ? x[c + 0] : -INFINITY;
-            x[c + 1] = (c + 1 <= lim && d.y == dq) ? x[c + 1] : -INFINITY;
-            x[c + 2] = (c + 2 <= lim && d.z == dq) ? x[c + 2] : -INFINITY;
-            x[c + 3] = (c + 3 <= lim && d.w == dq) ? x[c + 3] : -INFINITY;
+        for (int w = 0; w < 4; ++w) {
+            uint32_t bits = 0u;
+#pragma unroll 2
+            for (int j = 0; j < 8; ++j) {
+                const int4 d = __ldg(dk + w * 8 + j);
+                const int c = w * 32 + j * 4;
+                const uint32_t nib = (uint32_t)(d.x == dq && c + 0 <= lim) | ((uint32_t)(d.y == dq && c + 1 <= lim) << 1) |
+                                     ((uint32_t)(d.z == dq && c + 2 <= lim) << 2) |
+                                     ((uint32_t)(d.w == dq && c + 3 <= lim) << 3);
+                bits |= nib << (4 * j);
+            }
+            keep[w] = bits;
         }
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+            x2[j] = keep_pair(x2[j], (keep[j / 16] >> ((2 * j) % 32)) & 1u, (keep[j / 16] >> ((2 * j + 1) % 32)) & 1u);
     }
 }
 
@@ -241,7 +312,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int s = 0; s < NS; ++s) {
             mbar_init(&ms.k_full[s], 1);
             mbar_init(&ms.v_full[s], 1);
-            mbar_init(&ms.kv_empty[s], 1);
+            mbar_init(&ms.k_empty[s], 1);
+            mbar_init(&ms.v_empty[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ms.s_full[i], 1);
@@ -257,6 +329,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tmem_relinquish();
     }
     for (int i = threadIdx.x; i < p.nkvb; i += kAttnThreads) ms.flags[i] = 0u;
+    if (threadIdx.x < 128)
+        ms.alibi_tbl[threadIdx.x] = kLog2e * exp2f(-8.f * (float)(h + 1) / (float)p.H) * (float)threadIdx.x;
     __syncthreads();
 
     // Mark every kv tile of both q blocks (bounds-checked: a malformed
@@ -304,6 +378,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int nu = ms.n_union;
     volatile int *abort_flag = &ms.abort;
 
+    if (warp >= 8) {
+        regs_decrease<kRegsControl>();
+    }
     if (warp == kTmaWarp) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0 && nu > 0) {
@@ -321,16 +398,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int u = 0; u < nu; ++u) {
                 const int s = u % NS;
                 const uint32_t use = (uint32_t)(u / NS);
-                if (use > 0 && !mbar_wait(&ms.kv_empty[s], (use - 1) & 1u, abort_flag)) {
-                    record_failure(ms, p.status);
-                    break;
-                }
                 const int kv0 = (int)(ms.ulist[u] & 0xFFFFu) * kBlock;
                 uint8_t *kd = smem + C::kKvOff + s * C::kStageBytes;
                 uint8_t *vd = kd + C::kTileBytes;
+                // K of this stage is free once the S MMAs of its previous step are done,
+                // V once the PV MMAs are: the two are released separately.
+                if (use > 0 && !mbar_wait(&ms.k_empty[s], (use - 1) & 1u, abort_flag)) {
+                    record_failure(ms, p.status);
+                    break;
+                }
                 mbar_arrive_expect_tx(&ms.k_full[s], C::kTileBytes);
                 for (int a = 0; a < C::kAtoms; ++a)
                     tma_load_4d(kd + a * C::kAtomBytes, &tmap_k, &ms.k_full[s], 64 * a, kv0, h, b);
+                if (use > 0 && !mbar_wait(&ms.v_empty[s], (use - 1) & 1u, abort_flag)) {
+                    record_failure(ms, p.status);
+                    drain_wait(&ms.k_full[s], use & 1u);
+                    break;
+                }
                 mbar_arrive_expect_tx(&ms.v_full[s], C::kTileBytes);
                 for (int a = 0; a < C::kAtoms; ++a)
                     tma_load_4d(vd + a * C::kAtomBytes, &tmap_v, &ms.v_full[s], 64 * a, kv0, h, b);
@@ -353,24 +437,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
             const uint32_t q_addr0 = smem_u32(smem + C::kQOff);
             uint32_t pv_done[2] = {0u, 0u};
+            // Q and K are K-major (rows of 64 elements per 128-byte swizzle
+            // atom, 8-row groups 1024 bytes apart); V is MN-major (kv rows of
+            // 64 head-dim elements, the two 64-wide halves 16 KB apart).
+            constexpr uint32_t kHi = smem_desc_hi_sw128(1024);
+            const uint32_t kv_lo0 = smem_desc_lo(smem_u32(smem + C::kKvOff), 16);
+            const uint32_t v_lo0 = smem_desc_lo(smem_u32(smem + C::kKvOff + C::kTileBytes), C::kAtomBytes);
+            const uint32_t q_lo0 = smem_desc_lo(q_addr0, 16);
             auto issue_s = [&](int i, int s) {
-                const uint32_t qa = q_addr0 + i * C::kTileBytes;
-                const uint32_t ka = smem_u32(smem + C::kKvOff + s * C::kStageBytes);
+                const uint32_t qa = q_lo0 + ((i * C::kTileBytes) >> 4);
+                const uint32_t ka = kv_lo0 + ((s * C::kStageBytes) >> 4);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k / 4) * C::kAtomBytes + (k % 4) * 32;
-                    mma_ss(tmem + C::s_col(i), smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-                           idesc_s, k > 0 ? 1u : 0u);
+                    const uint32_t off = ((k / 4) * C::kAtomBytes + (k % 4) * 32) >> 4;
+                    mma_ss_lo<kHi, kHi>(tmem + C::s_col(i), qa + off, ka + off, idesc_s, k > 0 ? 1u : 0u);
                 }
                 mma_commit(&ms.s_full[i]);
             };
             auto issue_pv = [&](int i, int s) {
-                const uint32_t va = smem_u32(smem + C::kKvOff + s * C::kStageBytes + C::kTileBytes);
+                const uint32_t va = v_lo0 + ((s * C::kStageBytes) >> 4);
                 const uint32_t acc = pv_done[i] > 0 ? 1u : 0u;
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mma_ts(tmem + C::o_col(i), tmem + C::s_col(i) + k * 8, smem_desc_sw128(va + k * 2048, C::kAtomBytes, 1024),
-                           idesc_o, (k > 0 || acc) ? 1u : 0u);
+                    mma_ts_lo<kHi>(tmem + C::o_col(i), tmem + C::s_col(i) + k * 8, va + ((k * 2048) >> 4), idesc_o,
+                                   (k > 0 || acc) ? 1u : 0u);
                 ++pv_done[i];
             };
             bool ok = mbar_wait(&ms.q_full, 0, abort_flag) && mbar_wait(&ms.k_full[0], 0, abort_flag);
@@ -379,6 +469,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const uint32_t f = ms.ulist[0] >> 16;
                 if (f & 1u) issue_s(0, 0);
                 if (f & 4u) issue_s(1, 0);
+                mma_commit(&ms.k_empty[0]);
             }
             for (int u = 0; ok && u < nu; ++u) {
                 const int s = u % NS;
@@ -414,8 +505,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     tc_fence_after_sync();
                     issue_pv(1, s);
                 }
-                mma_commit(&ms.kv_empty[s]);
-                if (f1 & 4u) issue_s(1, s1);
+                mma_commit(&ms.v_empty[s]);
+                if (nxt) {
+                    if (f1 & 4u) issue_s(1, s1);
+                    mma_commit(&ms.k_empty[s1]);
+                }
             }
             if (ok)
                 mma_commit(&ms.o_full);
@@ -427,6 +521,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         __syncwarp();
     } else if (warp < 8) {
         // ----------------------------------------------------------- softmax
+        regs_increase<kRegsSoftmax>();
         const int i = warp / 4;
         const int t = threadIdx.x % 128;
         const bool valid = i == 0 || has1;
@@ -436,7 +531,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t o_addr = tmem + lane_base + C::o_col(i);
         const uint32_t present = i ? 4u : 1u, fullbit = i ? 8u : 2u;
         ScoreLog2<SCORE> score;
-        score.init(p, h);
+        score.init(p, h, ms.alibi_tbl);
         float m_run = -INFINITY, l_run = 0.f;
         uint32_t cnt = 0;
         bool ok = true;
@@ -451,58 +546,83 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                float x[128];
+                uint64_t x2[64];
                 {
-                    uint32_t r[64];
-                    tmem_ld64_sync(s_addr, r);
+                    uint32_t r[128];
+                    tmem_ld128_sync(s_addr, r);
+                    score.tile(kv0, q);
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(r[c]);
-                    tmem_ld64_sync(s_addr + 64, r);
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) x[64 + c] = __uint_as_float(r[c]);
+                    for (int j = 0; j < 64; ++j)
+                        x2[j] = score.pair(f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), j);
                 }
-                score.tile(kv0, q);
-#pragma unroll
-                for (int c = 0; c < 128; ++c) x[c] = score(x[c], c);
-                if (!(f & fullbit)) apply_partial_mask(p.mask, b, q, kv0, x);
+                if (!(f & fullbit)) apply_partial_mask(p.mask, b, q, kv0, x2);
 
-                float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+                float mx[8];
 #pragma unroll
-                for (int c = 4; c < 128; c += 4) {
-                    mx0 = fmaxf(mx0, x[c]);
-                    mx1 = fmaxf(mx1, x[c + 1]);
-                    mx2 = fmaxf(mx2, x[c + 2]);
-                    mx3 = fmaxf(mx3, x[c + 3]);
+                for (int k = 0; k < 8; ++k) {
+                    float lo, hi;
+                    f2_unpack(x2[k], lo, hi);
+                    mx[k] = fmaxf(lo, hi);
                 }
-                const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+#pragma unroll
+                for (int j = 8; j < 64; ++j) {
+                    float lo, hi;
+                    f2_unpack(x2[j], lo, hi);
+                    mx[j & 7] = fmax3(mx[j & 7], lo, hi);
+                }
+                const float m_tile = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) +
+                                     score.offset;
                 float alpha = 1.f;
                 if (m_tile > m_run + kRescaleThreshold) {  // also taken when m_run = -inf
                     alpha = ex2_approx(m_run - m_tile);
                     m_run = m_tile;
                 }
                 const float m_use = m_run == -INFINITY ? 0.f : m_run;
-                float rs0 = 0.f, rs1 = 0.f;
+                const float sub = score.offset - m_use;
+                const uint64_t sub2 = f2_pack(sub, sub);
+                uint64_t rs2[4];
 #pragma unroll
-                for (int c0 = 0; c0 < 128; c0 += 32) {
-                    uint32_t pk[16];
+                for (int k = 0; k < 4; ++k) rs2[k] = 0ull;
+                {
+                    uint32_t pk[64];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float p0 = ex2_approx(x[c0 + 2 * j] - m_use);
-                        const float p1 = ex2_approx(x[c0 + 2 * j + 1] - m_use);
-                        rs0 += p0;
-                        rs1 += p1;
+                    for (int j = 0; j < 64; ++j) {
+                        float d0, d1;
+                        f2_unpack(f2_add(x2[j], sub2), d0, d1);
+                        const float p0 = ex2_approx(d0);
+                        const float p1 = ex2_approx(d1);
+                        rs2[j & 3] = f2_add(rs2[j & 3], f2_pack(p0, p1));
                         pk[j] = pack_bf16x2(p0, p1);
                     }
-                    tmem_st16(s_addr + c0 / 2, pk);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t q16[16];
+#pragma unroll
+                        for (int t2 = 0; t2 < 16; ++t2) q16[t2] = pk[16 * j + t2];
+                        tmem_st16(s_addr + 16 * j, q16);
+                    }
                 }
-                l_run = fmaf(l_run, alpha, rs0 + rs1);
+                float rsum;
+                {
+                    float a0, a1;
+                    f2_unpack(f2_add(f2_add(rs2[0], rs2[1]), f2_add(rs2[2], rs2[3])), a0, a1);
+                    rsum = a0 + a1;
+                }
+                l_run = fmaf(l_run, alpha, rsum);
                 if (cnt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
                     for (int c0 = 0; c0 < D; c0 += 32) {
                         uint32_t o[32];
                         tmem_ld32_sync(o_addr + c0, o);
+                        const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                        for (int j = 0; j < 16; ++j) {
+                            float lo, hi;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * j]), __uint_as_float(o[2 * j + 1])), a2), lo,
+                                      hi);
+                            o[2 * j] = __float_as_uint(lo);
+                            o[2 * j + 1] = __float_as_uint(hi);
+                        }
                         tmem_st32(o_addr + c0, o);
                     }
                 }

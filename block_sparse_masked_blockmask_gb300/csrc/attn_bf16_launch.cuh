@@ -11,7 +11,13 @@ cudaError_t launch_bf16_kernel(const CUtensorMap &tq, const CUtensorMap &tk, con
                                const Bf16Params &kp, cudaStream_t stream) {
     using C = Bf16Cfg<D>;
     auto kernel = attn_bf16_kernel<D, SCORE>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+    // The in-kernel register split assumes exactly kRegsAtLaunch registers per
+    // thread at launch; any other count could stall the increase, so refuse.
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, kernel);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs != (int)kRegsAtLaunch) return cudaErrorInvalidDeviceFunction;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((int64_t)kp.B * kp.H * kp.npairs);
     kernel<<<grid, kAttnThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
