@@ -61,6 +61,44 @@ int *device_status_word(int *err) {
     return g_status[dev];
 }
 
+// ----------------------------------------------------------------------------
+// Scratch for flex_attention_fwd_noalloc.  Some callers cannot let a library
+// call cudaMalloc: code that enqueues work while a stream is being captured,
+// plug-ins whose host framework owns every device allocation, and processes
+// that must not grow device memory after start-up.  For them the status word
+// that the attention kernel writes on a timed-out wait lives in this
+// file-scope device array instead of the cudaMalloc'd per-device workspace.
+// Every GPU that loads the library holds these bytes until the process exits.
+constexpr size_t kNoAllocScratchBytes = 256;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_noalloc_mutex;
+int *g_noalloc_word[kMaxDevices] = {nullptr};
+
+// Device address of the static scratch on the current device.  Looked up once
+// per device (cudaGetSymbolAddress, checked) with that device current; the
+// host-side name of the array is not a device address.
+int *noalloc_scratch_address(int *err) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *err = FLEX_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_word[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+            *err = FLEX_ERR_CUDA;
+            return nullptr;
+        }
+        g_noalloc_word[dev] = static_cast<int *>(ptr);
+    }
+    *err = FLEX_OK;
+    return g_noalloc_word[dev];
+}
+}  // namespace
+
 }  // namespace flex
 
 using namespace flex;
@@ -207,6 +245,83 @@ const char *flex_status_string(int status) {
         default:
             return "unknown status";
     }
+}
+
+int flex_attention_fwd_noalloc(const flex_tensor *q, const flex_tensor *k, const flex_tensor *v,
+                               const flex_block_mask *bm, int32_t score_kind, float score_param, float scale,
+                               void *out, float *lse, void *stream, const int **device_status) {
+    if (device_status) *device_status = nullptr;
+    // the same argument checks as flex_attention_fwd
+    if (!q || !k || !v || !bm || !out || !lse) return FLEX_ERR_INVALID_ARG;
+    const int dtype = q->dtype;
+    if (dtype != FLEX_DTYPE_BF16 && dtype != FLEX_DTYPE_FP32) return FLEX_ERR_INVALID_ARG;
+    if (score_kind < FLEX_SCORE_IDENTITY || score_kind > FLEX_SCORE_ALIBI) return FLEX_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return FLEX_ERR_INVALID_ARG;
+    if (score_kind == FLEX_SCORE_SOFTCAP && !(score_param > 0.f && std::isfinite(score_param)))
+        return FLEX_ERR_INVALID_ARG;
+    const int64_t B = q->shape[0], H = q->shape[1], Sq = q->shape[2], D = q->shape[3], Skv = k->shape[2];
+    if (B <= 0 || H <= 0 || Sq <= 0 || Skv <= 0 || D <= 0) return FLEX_ERR_SHAPE;
+    if (D != 64 && D != 128) return FLEX_ERR_UNSUPPORTED;
+    if (Sq > INT32_MAX || Skv > INT32_MAX) return FLEX_ERR_UNSUPPORTED;
+    int rc = check_tensor(q, dtype, B, H, Sq, D);
+    if (rc == FLEX_OK) rc = check_tensor(k, dtype, B, H, Skv, D);
+    if (rc == FLEX_OK) rc = check_tensor(v, dtype, B, H, Skv, D);
+    if (rc != FLEX_OK) return rc;
+    if (!aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return FLEX_ERR_ALIGNMENT;
+    if (!valid_mask_kind(bm->mask_kind)) return FLEX_ERR_INVALID_ARG;
+    rc = check_sizes(bm->B, bm->H, bm->q_len, bm->kv_len, bm->block);
+    if (rc != FLEX_OK) return rc;
+    if (bm->B != B || bm->H != H || bm->q_len != Sq || bm->kv_len != Skv) return FLEX_ERR_SHAPE;
+    if (bm->nqb != bm->q_len / bm->block || bm->nkvb != bm->kv_len / bm->block) return FLEX_ERR_SHAPE;
+    if (!bm->kv_num_blocks || !bm->kv_indices || !bm->full_kv_num_blocks || !bm->full_kv_indices)
+        return FLEX_ERR_INVALID_ARG;
+    if (bm->mask_kind == FLEX_MASK_DOCUMENT && (!bm->params.doc_ids || !aligned16(bm->params.doc_ids)))
+        return FLEX_ERR_INVALID_ARG;
+    if (bm->mask_kind == FLEX_MASK_SLIDING_WINDOW && bm->params.window < 0) return FLEX_ERR_INVALID_ARG;
+    if (B * H * ((bm->nqb + 1) / 2) > INT32_MAX) return FLEX_ERR_UNSUPPORTED;
+
+    // The kernel's scratch is one int status word whatever the problem size;
+    // anything larger than the static array is refused.
+    constexpr size_t kScratchNeeded = sizeof(int);
+    if (kScratchNeeded > kNoAllocScratchBytes) return FLEX_ERR_UNSUPPORTED;
+    int err = FLEX_OK;
+    int *status = noalloc_scratch_address(&err);
+    if (!status) return err;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the kernel only ever sets the word, so every call starts it at zero
+    if (cudaMemsetAsync(status, 0, kScratchNeeded, s) != cudaSuccess) return FLEX_ERR_CUDA;
+
+    AttnProblem p;
+    p.B = (int)B;
+    p.H = (int)H;
+    p.q_len = (int)Sq;
+    p.kv_len = (int)Skv;
+    p.D = (int)D;
+    p.nqb = bm->nqb;
+    p.nkvb = bm->nkvb;
+    for (int i = 0; i < 4; ++i) {
+        p.q_stride[i] = q->stride[i];
+        p.k_stride[i] = k->stride[i];
+        p.v_stride[i] = v->stride[i];
+    }
+    p.q = q->data;
+    p.k = k->data;
+    p.v = v->data;
+    p.out = out;
+    p.lse = lse;
+    p.kv_num = bm->kv_num_blocks;
+    p.kv_idx = bm->kv_indices;
+    p.full_num = bm->full_kv_num_blocks;
+    p.full_idx = bm->full_kv_indices;
+    p.mask = MaskDesc{bm->mask_kind, bm->params.window, bm->params.prefix, bm->q_len, bm->params.doc_ids};
+    p.score_kind = score_kind;
+    p.score_param = score_param;
+    p.scale = scale;
+    p.status = status;
+    const cudaError_t e = dtype == FLEX_DTYPE_BF16 ? launch_attn_bf16(p, s) : launch_attn_fp32(p, s);
+    if (e != cudaSuccess) return FLEX_ERR_CUDA;
+    if (device_status) *device_status = status;
+    return FLEX_OK;
 }
 
 }  // extern "C"

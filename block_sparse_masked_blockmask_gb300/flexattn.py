@@ -38,7 +38,7 @@ FLEX_DTYPE_BF16 = 0
 FLEX_DTYPE_FP32 = 1
 
 EXPORTED = ("flex_block_mask_sizes", "flex_block_mask_create", "flex_attention_fwd",
-            "flex_device_status", "flex_status_string")
+            "flex_attention_fwd_noalloc", "flex_device_status", "flex_status_string")
 
 
 class FlexError(RuntimeError):
@@ -92,6 +92,10 @@ def load_library():
             lib.flex_attention_fwd.argtypes = [tp, tp, tp, ctypes.POINTER(flex_block_mask), i32, ctypes.c_float,
                                                ctypes.c_float, vp, vp, vp]
             lib.flex_attention_fwd.restype = ctypes.c_int
+            lib.flex_attention_fwd_noalloc.argtypes = [tp, tp, tp, ctypes.POINTER(flex_block_mask), i32,
+                                                       ctypes.c_float, ctypes.c_float, vp, vp, vp,
+                                                       ctypes.POINTER(ctypes.POINTER(ctypes.c_int))]
+            lib.flex_attention_fwd_noalloc.restype = ctypes.c_int
             lib.flex_device_status.argtypes = [vp]
             lib.flex_device_status.restype = ctypes.c_int
             lib.flex_status_string.argtypes = [ctypes.c_int]
@@ -205,6 +209,30 @@ def flex_attention_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_
     if rc != FLEX_OK:
         raise FlexError(rc, "flex_attention_fwd")
     return out, lse
+
+
+def flex_attention_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_mask: BlockMask,
+                               out: torch.Tensor, lse: torch.Tensor, score_kind: int = FLEX_SCORE_IDENTITY,
+                               score_param: float = 0.0, scale: float | None = None, stream=None):
+    """flex_attention_fwd into caller-provided out/lse without any device allocation by the library.
+
+    Returns the device address (int) of the status word the call uses; after the
+    stream finishes, a nonzero word means a kernel gave up on a wait.
+    """
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    tq, tk, tv = _tensor(q), _tensor(k), _tensor(v)
+    status = ctypes.POINTER(ctypes.c_int)()
+    with torch.cuda.device(q.device):
+        rc = load_library().flex_attention_fwd_noalloc(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                                       ctypes.byref(block_mask.struct), score_kind,
+                                                       float(score_param), float(scale),
+                                                       ctypes.c_void_p(out.data_ptr()),
+                                                       ctypes.c_void_p(lse.data_ptr()),
+                                                       _stream_handle(stream, q.device), ctypes.byref(status))
+    if rc != FLEX_OK:
+        raise FlexError(rc, "flex_attention_fwd_noalloc")
+    return ctypes.cast(status, ctypes.c_void_p).value
 
 
 def flex_device_status(stream=None, device=None) -> int:

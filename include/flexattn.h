@@ -175,6 +175,40 @@ FLEX_API int flex_attention_fwd(const flex_tensor *q, const flex_tensor *k, cons
                        float scale, void *out, float *lse, void *stream);
 
 /*
+ * flex_attention_fwd for callers that cannot allocate device memory.  (No
+ * counterpart in the pages: it exists for how the library is called, not for
+ * what it computes.)
+ *
+ * flex_attention_fwd keeps the status word its kernels write on a timed-out
+ * wait in a small workspace that it cudaMalloc's the first time a device is
+ * used.  Some callers cannot allow that: code that enqueues work while a
+ * stream is being captured, plug-ins whose host framework owns every device
+ * allocation, processes that must not grow device memory after start-up.
+ * This entry point computes exactly what flex_attention_fwd computes, with the
+ * same arguments, checks and errors, and allocates nothing: the status word
+ * lives in a static 256-byte device array inside the library, which every GPU
+ * that loads the library holds until the process exits.  The status word is
+ * 4 bytes whatever the problem size; a request for more scratch than the
+ * array holds is refused with FLEX_ERR_UNSUPPORTED.
+ *   - The first call on a device looks up that array's device address (once
+ *     per device, with the device current); make that first call before any
+ *     stream capture.
+ *   - Each call clears the status word on `stream` (cudaMemsetAsync) before
+ *     launching.  All calls share the one array and it keeps the last call's
+ *     contents, so calls whose work overlaps on the GPU (other streams, other
+ *     threads) race on it.
+ *   - device_status (may be NULL): set to the device address of the status
+ *     word.  After `stream` has finished, 0 means every wait completed and a
+ *     nonzero value means a kernel gave up on a wait (outputs unspecified).
+ *     Read it with a device-to-host copy; flex_device_status() does not see it.
+ * Errors: as flex_attention_fwd.
+ */
+FLEX_API int flex_attention_fwd_noalloc(const flex_tensor *q, const flex_tensor *k, const flex_tensor *v,
+                                        const flex_block_mask *bm, int32_t score_kind, float score_param,
+                                        float scale, void *out, float *lse, void *stream,
+                                        const int **device_status);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: FLEX_OK, or FLEX_ERR_DEVICE_TIMEOUT if a kernel gave up
  * on a wait since the last call.  FLEX_ERR_CUDA if the synchronisation failed.
