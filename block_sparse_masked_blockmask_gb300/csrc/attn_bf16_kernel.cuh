@@ -38,6 +38,8 @@
 //     FLEX_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees TMEM, exits.
 #pragma once
 
+#include <cstddef>
+
 #include <cuda_bf16.h>
 
 #include "flex_internal.h"
@@ -83,10 +85,14 @@ struct AttnMisc {
     int abort;
     int n_union;
     int pad;
-    float alibi_tbl[128];          // log2(e) slope_h c, c = 0..127 (ALiBi score_mod)
-    uint32_t flags[kMaxKvBlocks];  // bit0 present in tile 0, bit1 full in tile 0, bit2/bit3 same for tile 1
-    uint32_t ulist[kMaxKvBlocks];  // union, descending kv: kv block | flags << 16
+    alignas(16) float alibi_tbl[128];          // log2(e) slope_h c, c = 0..127 (ALiBi score_mod)
+    alignas(16) int32_t stage_doc[4][128];     // document ids of each stage's kv tile (bulk-copy target)
+    alignas(16) uint32_t flags[kMaxKvBlocks];  // bit0/bit1 present/full in tile 0, bit2/bit3 in tile 1
+    alignas(16) uint32_t ulist[kMaxKvBlocks];  // union, descending kv: kv block | flags << 16
 };
+// bulk copies need 16-byte aligned shared-memory destinations
+static_assert(offsetof(AttnMisc, stage_doc) % 16 == 0, "stage_doc alignment");
+static_assert(sizeof(AttnMisc::stage_doc[0]) % 16 == 0, "stage_doc row size");
 
 template <int D>
 struct Bf16Cfg {
@@ -250,42 +256,48 @@ __device__ __forceinline__ uint64_t keep_pair(uint64_t v, bool k0, bool k1) {
     return f2_pack(k0 ? a : -INFINITY, k1 ? b : -INFINITY);
 }
 
-__device__ __forceinline__ void apply_partial_mask(const MaskDesc &m, int b, int q, int kv0, uint64_t (&x2)[64]) {
+// Interval mask_mods (causal, sliding window, causal + prefix, all): the row
+// keeps exactly the kv in [lo, hi].
+__device__ __forceinline__ void apply_interval_mask(const MaskDesc &m, int q, int kv0, uint64_t (&x2)[64]) {
     int lo, hi;
-    if (mask_row_interval(m, q, lo, hi)) {
-        const int clo = lo - kv0, chi = hi - kv0;
+    mask_row_interval(m, q, lo, hi);
+    const int clo = lo - kv0, chi = hi - kv0;
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
-            x2[j] = keep_pair(x2[j], 2 * j >= clo && 2 * j <= chi, 2 * j + 1 >= clo && 2 * j + 1 <= chi);
-    } else {  // document: same document id and kv <= q
-        const int32_t *dr = m.doc_ids + (int64_t)b * m.doc_len;
-        const int dq = __ldg(dr + q);
-        const int lim = q - kv0;
-        const int4 *dk = reinterpret_cast<const int4 *>(dr + kv0);
-        // keep-bits of the 128 columns in four words (rolled loads), then one
-        // fully unrolled pass so the scores stay in registers
-        uint32_t keep[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            uint32_t bits = 0u;
-#pragma unroll 2
-            for (int j = 0; j < 8; ++j) {
-                const int4 d = __ldg(dk + w * 8 + j);
-                const int c = w * 32 + j * 4;
-                const uint32_t nib = (uint32_t)(d.x == dq && c + 0 <= lim) | ((uint32_t)(d.y == dq && c + 1 <= lim) << 1) |
-                                     ((uint32_t)(d.z == dq && c + 2 <= lim) << 2) |
-                                     ((uint32_t)(d.w == dq && c + 3 <= lim) << 3);
-                bits |= nib << (4 * j);
-            }
-            keep[w] = bits;
-        }
-#pragma unroll
-        for (int j = 0; j < 64; ++j)
-            x2[j] = keep_pair(x2[j], (keep[j / 16] >> ((2 * j) % 32)) & 1u, (keep[j / 16] >> ((2 * j + 1) % 32)) & 1u);
-    }
+    for (int j = 0; j < 64; ++j)
+        x2[j] = keep_pair(x2[j], 2 * j >= clo && 2 * j <= chi, 2 * j + 1 >= clo && 2 * j + 1 <= chi);
 }
 
-template <int D, int SCORE>
+// Document mask_mod: same document id (the tile's ids staged in shared
+// memory) and kv <= q.
+__device__ __forceinline__ void apply_document_mask(int q, int kv0, int doc_q, const int32_t *tile_doc,
+                                                    uint64_t (&x2)[64]) {
+    const int lim = q - kv0;
+    const int4 *dk = reinterpret_cast<const int4 *>(tile_doc);
+    // keep-bits of the 128 columns in four words, then one fully unrolled
+    // pass so the scores stay in registers
+    uint32_t keep[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        uint32_t bits = 0u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int4 d = dk[w * 8 + j];
+            const int c = w * 32 + j * 4;
+            const uint32_t nib = (uint32_t)(d.x == doc_q && c + 0 <= lim) | ((uint32_t)(d.y == doc_q && c + 1 <= lim) << 1) |
+                                 ((uint32_t)(d.z == doc_q && c + 2 <= lim) << 2) |
+                                 ((uint32_t)(d.w == doc_q && c + 3 <= lim) << 3);
+            bits |= nib << (4 * j);
+        }
+        keep[w] = bits;
+    }
+#pragma unroll
+    for (int j = 0; j < 64; ++j)
+        x2[j] = keep_pair(x2[j], (keep[j / 16] >> ((2 * j) % 32)) & 1u, (keep[j / 16] >> ((2 * j + 1) % 32)) & 1u);
+}
+
+// DOC: the BlockMask's mask_mod is the document mask (its partial tiles read
+// per-tile document ids staged next to V); other kinds are interval masks.
+template <int D, int SCORE, bool DOC>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const Bf16Params p) {
@@ -384,6 +396,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp == kTmaWarp) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0 && nu > 0) {
+            constexpr bool is_doc = DOC;
+            const int32_t *doc_row = DOC ? p.mask.doc_ids + (int64_t)b * p.mask.doc_len : nullptr;
             prefetch_tensormap(&tmap_q);
             prefetch_tensormap(&tmap_k);
             prefetch_tensormap(&tmap_v);
@@ -415,9 +429,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     drain_wait(&ms.k_full[s], use & 1u);
                     break;
                 }
-                mbar_arrive_expect_tx(&ms.v_full[s], C::kTileBytes);
+                // the kv tile's document ids travel with V: V's stage is released
+                // only after both softmax groups are done with the tile
+                mbar_arrive_expect_tx(&ms.v_full[s], C::kTileBytes + (is_doc ? 512u : 0u));
                 for (int a = 0; a < C::kAtoms; ++a)
                     tma_load_4d(vd + a * C::kAtomBytes, &tmap_v, &ms.v_full[s], 64 * a, kv0, h, b);
+                if (is_doc) bulk_load(ms.stage_doc[s], doc_row + kv0, 512u, &ms.v_full[s]);
                 issued = u + 1;
             }
             // Drain: every copy issued above must land before the CTA exits.
@@ -532,6 +549,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t present = i ? 4u : 1u, fullbit = i ? 8u : 2u;
         ScoreLog2<SCORE> score;
         score.init(p, h, ms.alibi_tbl);
+        int doc_q = 0;
+        if constexpr (DOC) {
+            if (valid) doc_q = __ldg(p.mask.doc_ids + (int64_t)b * p.mask.doc_len + q);
+        }
         float m_run = -INFINITY, l_run = 0.f;
         uint32_t cnt = 0;
         bool ok = true;
@@ -555,7 +576,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int j = 0; j < 64; ++j)
                         x2[j] = score.pair(f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), j);
                 }
-                if (!(f & fullbit)) apply_partial_mask(p.mask, b, q, kv0, x2);
+                if (!(f & fullbit)) {
+                    if constexpr (DOC) {
+                        const int stage = u % NS;
+                        if (!warp_wait(&ms.v_full[stage], (uint32_t)(u / NS) & 1u, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        apply_document_mask(q, kv0, doc_q, ms.stage_doc[stage], x2);
+                    } else {
+                        apply_interval_mask(p.mask, q, kv0, x2);
+                    }
+                }
 
                 float mx[8];
 #pragma unroll

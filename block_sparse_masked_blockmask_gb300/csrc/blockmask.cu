@@ -4,12 +4,21 @@
 // PyTorch PR #167356, the BlockMask tuple: kv_num_blocks, kv_indices,
 // full_kv_num_blocks, full_kv_indices at Q_BLOCK = KV_BLOCK = 128).
 //
-// One CTA per (batch b, q block qb).  Each warp classifies whole tiles by
-// evaluating mask_mod on all 16384 (q, kv) pairs of the tile (no closed-form
-// shortcut, so document masks with arbitrary ids are exact).  None of the
-// enumerated mask_mods depends on the head, so a row is classified once and
-// written for every head.  Index rows hold the selected kv blocks in
-// ascending order followed by the remaining kv blocks in ascending order.
+// One CTA per (batch b, q block qb); each warp classifies whole tiles.
+//  * causal, sliding window, causal + prefix, all: for a fixed row q the kept
+//    kv form exactly the interval [lo(q), hi(q)] (mask_row_interval), so a
+//    tile is full when every row's interval covers the tile's 128 columns and
+//    empty when no row's interval meets them: 128 row tests instead of 16384
+//    predicate evaluations.
+//  * document: exact quick decisions first (a tile above the diagonal is
+//    empty; a tile below it whose 256 row and column ids are one id is full;
+//    disjoint id ranges are empty), otherwise mask_mod is evaluated on all
+//    16384 pairs, so arbitrary ids stay exact.
+// None of the enumerated mask_mods depends on the head, so a row is
+// classified once and written for every head.  Index rows hold the selected kv
+// blocks in ascending order followed by the remaining kv blocks ascending.
+#include <climits>
+
 #include "flex_internal.h"
 
 namespace flex {
@@ -20,34 +29,49 @@ constexpr int kBmWarps = kBmThreads / 32;
 
 enum : uint8_t { kEmpty = 0, kPartial = 1, kFull = 2 };
 
-// Lane `lane` tests the four columns lane + 32 j of the tile against all 128
-// rows; the warp then reduces "any true" and "all true".
-template <int KIND>
-__device__ __forceinline__ uint8_t classify_tile(const MaskDesc &m, int b, int q0, int kv0, int lane,
-                                                 const int32_t *row_doc) {
+// Interval kinds: lane `lane` tests rows lane + 32 j of the tile.
+__device__ __forceinline__ uint8_t classify_interval_tile(const MaskDesc &m, int q0, int kv0, int lane) {
     bool any = false, all = true;
-    int col_doc[4];
-    if constexpr (KIND == FLEX_MASK_DOCUMENT) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) col_doc[j] = m.doc_ids[(int64_t)b * m.doc_len + kv0 + lane + 32 * j];
+    for (int j = 0; j < 4; ++j) {
+        int lo, hi;
+        mask_row_interval(m, q0 + lane + 32 * j, lo, hi);
+        const int a = max(lo, kv0), e = min(hi, kv0 + kBlock - 1);
+        any |= a <= e;
+        all &= lo <= kv0 && hi >= kv0 + kBlock - 1;
     }
+    any = __any_sync(0xffffffffu, any);
+    all = __all_sync(0xffffffffu, all);
+    return all ? kFull : (any ? kPartial : kEmpty);
+}
+
+// Document kind: quick exact decisions, else every (q, kv) pair of the tile.
+__device__ __forceinline__ uint8_t classify_document_tile(const MaskDesc &m, int b, int qb, int kvb, int lane,
+                                                          const int32_t *row_doc, int row_min, int row_max) {
+    if (kvb > qb) return kEmpty;  // every kv of the tile is above every q: kv > q
+    const int kv0 = kvb * kBlock;
+    int col_doc[4];
+    int cmin = INT_MAX, cmax = INT_MIN;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        col_doc[j] = m.doc_ids[(int64_t)b * m.doc_len + kv0 + lane + 32 * j];
+        cmin = min(cmin, col_doc[j]);
+        cmax = max(cmax, col_doc[j]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        cmin = min(cmin, __shfl_xor_sync(0xffffffffu, cmin, o));
+        cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
+    }
+    if (cmax < row_min || cmin > row_max) return kEmpty;  // no id in common
+    if (kvb < qb && cmin == cmax && row_min == row_max && cmin == row_min) return kFull;
+    const int q0 = qb * kBlock;
+    bool any = false, all = true;
     for (int r = 0; r < kBlock; ++r) {
         const int q = q0 + r;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int kv = kv0 + lane + 32 * j;
-            bool keep;
-            if constexpr (KIND == FLEX_MASK_CAUSAL) {
-                keep = q >= kv;
-            } else if constexpr (KIND == FLEX_MASK_SLIDING_WINDOW) {
-                keep = q >= kv && q - kv < m.window;
-            } else if constexpr (KIND == FLEX_MASK_CAUSAL_PREFIX) {
-                keep = (q <= m.prefix && kv <= m.prefix) || q >= kv;
-            } else if constexpr (KIND == FLEX_MASK_DOCUMENT) {
-                keep = q >= kv && row_doc[r] == col_doc[j];
-            } else {
-                keep = true;
-            }
+            const bool keep = q >= kv0 + lane + 32 * j && row_doc[r] == col_doc[j];
             any |= keep;
             all &= keep;
         }
@@ -88,6 +112,7 @@ __global__ void __launch_bounds__(kBmThreads) block_mask_kernel(MaskDesc m, int 
     __shared__ int32_t part_list[kMaxKvBlocks];
     __shared__ int32_t full_list[kMaxKvBlocks];
     __shared__ int32_t row_doc[kBlock];
+    __shared__ int32_t row_range[2];
     __shared__ int32_t counts[2];
 
     const int qb = blockIdx.x, b = blockIdx.y;
@@ -95,11 +120,25 @@ __global__ void __launch_bounds__(kBmThreads) block_mask_kernel(MaskDesc m, int 
     const int q0 = qb * kBlock;
 
     if constexpr (KIND == FLEX_MASK_DOCUMENT) {
-        for (int r = threadIdx.x; r < kBlock; r += kBmThreads) row_doc[r] = m.doc_ids[(int64_t)b * m.doc_len + q0 + r];
+        if (threadIdx.x == 0) {
+            row_range[0] = INT_MAX;
+            row_range[1] = INT_MIN;
+        }
+        __syncthreads();
+        for (int r = threadIdx.x; r < kBlock; r += kBmThreads) {
+            const int d = m.doc_ids[(int64_t)b * m.doc_len + q0 + r];
+            row_doc[r] = d;
+            atomicMin(&row_range[0], d);
+            atomicMax(&row_range[1], d);
+        }
         __syncthreads();
     }
     for (int kvb = warp; kvb < nkvb; kvb += kBmWarps) {
-        const uint8_t st = classify_tile<KIND>(m, b, q0, kvb * kBlock, lane, row_doc);
+        uint8_t st;
+        if constexpr (KIND == FLEX_MASK_DOCUMENT)
+            st = classify_document_tile(m, b, qb, kvb, lane, row_doc, row_range[0], row_range[1]);
+        else
+            st = classify_interval_tile(m, q0, kvb * kBlock, lane);
         if (lane == 0) status[kvb] = st;
     }
     __syncthreads();
