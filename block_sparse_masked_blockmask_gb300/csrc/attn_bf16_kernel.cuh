@@ -79,13 +79,12 @@ struct Bf16Params {
 struct AttnMisc {
     uint64_t q_full;
     uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];
-    uint64_t s_full[2], p_full[2];
+    uint64_t s_full[2], p_half[2], p_full[2];
     uint64_t o_full, drain;
     uint32_t tmem_base;
     int abort;
     int n_union;
     int pad;
-    alignas(16) float alibi_tbl[128];          // log2(e) slope_h c, c = 0..127 (ALiBi score_mod)
     alignas(16) int32_t stage_doc[4][128];     // document ids of each stage's kv tile (bulk-copy target)
     alignas(16) uint32_t flags[kMaxKvBlocks];  // bit0/bit1 present/full in tile 0, bit2/bit3 in tile 1
     alignas(16) uint32_t ulist[kMaxKvBlocks];  // union, descending kv: kv block | flags << 16
@@ -120,12 +119,10 @@ __device__ __forceinline__ void record_failure(AttnMisc &ms, int *status) {
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
     if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
+    for (;;) {
         if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
-        if ((it & 15u) == 0) {
-            const int stop = (*abort != 0) || (global_timer_ns() - t0 > kWaitLimitNs);
-            if (__shfl_sync(0xffffffffu, stop, 0)) return false;
-        }
+        const int stop = (*abort != 0) || (global_timer_ns() - t0 > kWaitLimitNs);
+        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
     }
 }
 
@@ -205,13 +202,16 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]
 //   ALiBi    : x = k0 s + slope2 c                   slope2 = log2(e) slope_h
 // For ALiBi the per-tile term slope2 (kv0 - q) is kept out of x as `offset`:
 // it shifts the whole row, so it is added to the row max and subtracted in
-// the exponent instead of being added to every element.
+// the exponent instead of being added to every element.  The column term
+// slope2 c comes from eight interleaved add chains (step 16 slope2, at most
+// seven adds each, error below 1e-4 in base-2 units on the tile's columns).
 template <int SCORE>
 struct ScoreLog2 {
     uint64_t k0, k1, k2, one;
     float slope2, offset;
-    const float *tbl;  // ALiBi: slope2 * c for c = 0..127, in shared memory
-    __device__ __forceinline__ void init(const Bf16Params &p, int h, const float *table) {
+    uint64_t bias[8];  // ALiBi: slope2 * (2j, 2j+1) for the next pair j of each of 8 chains
+    uint64_t step;     // ALiBi: 16 slope2 in both lanes (8 pairs further on)
+    __device__ __forceinline__ void init(const Bf16Params &p, int h) {
         float a0, a1 = 0.f, a2 = 0.f;
         if constexpr (SCORE == FLEX_SCORE_SOFTCAP) {
             // cap tanh(y) = cap - 2 cap / (exp(2y) + 1),  y = scale s / cap
@@ -226,14 +226,19 @@ struct ScoreLog2 {
         k2 = f2_pack(a2, a2);
         one = f2_pack(1.f, 1.f);
         slope2 = SCORE == FLEX_SCORE_ALIBI ? kLog2e * exp2f(-8.f * (float)(h + 1) / (float)p.H) : 0.f;
+        step = f2_pack(16.f * slope2, 16.f * slope2);
         offset = 0.f;
-        tbl = table;
     }
+    // start of a tile: per-tile row offset and the eight bias chains
     __device__ __forceinline__ void tile(int kv0, int q) {
-        if constexpr (SCORE == FLEX_SCORE_ALIBI) offset = slope2 * (float)(kv0 - q);
+        if constexpr (SCORE == FLEX_SCORE_ALIBI) {
+            offset = slope2 * (float)(kv0 - q);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) bias[t] = f2_pack(slope2 * (float)(2 * t), slope2 * (float)(2 * t + 1));
+        }
     }
-    // columns 2j, 2j+1
-    __device__ __forceinline__ uint64_t pair(uint64_t s2, int j) const {
+    // columns 2j, 2j+1 (called for j = 0, 1, ..., 63 in order)
+    __device__ __forceinline__ uint64_t pair(uint64_t s2, int j) {
         if constexpr (SCORE == FLEX_SCORE_SOFTCAP) {
             float t0, t1;
             f2_unpack(f2_mul(s2, k0), t0, t1);
@@ -241,7 +246,9 @@ struct ScoreLog2 {
             f2_unpack(f2_add(f2_pack(ex2_approx(t0), ex2_approx(t1)), one), u0, u1);
             return f2_fma(k1, f2_pack(rcp_approx(u0), rcp_approx(u1)), k2);
         } else if constexpr (SCORE == FLEX_SCORE_ALIBI) {
-            return f2_fma(s2, k0, reinterpret_cast<const uint64_t *>(tbl)[j]);
+            const uint64_t x = f2_fma(s2, k0, bias[j & 7]);
+            bias[j & 7] = f2_add(bias[j & 7], step);
+            return x;
         } else {
             return f2_mul(s2, k0);
         }
@@ -329,6 +336,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ms.s_full[i], 1);
+            mbar_init(&ms.p_half[i], 128);
             mbar_init(&ms.p_full[i], 128);
         }
         mbar_init(&ms.o_full, 1);
@@ -341,8 +349,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tmem_relinquish();
     }
     for (int i = threadIdx.x; i < p.nkvb; i += kAttnThreads) ms.flags[i] = 0u;
-    if (threadIdx.x < 128)
-        ms.alibi_tbl[threadIdx.x] = kLog2e * exp2f(-8.f * (float)(h + 1) / (float)p.H) * (float)threadIdx.x;
     __syncthreads();
 
     // Mark every kv tile of both q blocks (bounds-checked: a malformed
@@ -471,14 +477,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 mma_commit(&ms.s_full[i]);
             };
-            auto issue_pv = [&](int i, int s) {
+            // O_i += P_i V for kv rows 64 * half .. 64 * half + 63 (four K = 16 steps)
+            auto issue_pv_half = [&](int i, int s, int half) {
                 const uint32_t va = v_lo0 + ((s * C::kStageBytes) >> 4);
                 const uint32_t acc = pv_done[i] > 0 ? 1u : 0u;
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int k = 4 * half + kk;
                     mma_ts_lo<kHi>(tmem + C::o_col(i), tmem + C::s_col(i) + k * 8, va + ((k * 2048) >> 4), idesc_o,
                                    (k > 0 || acc) ? 1u : 0u);
+                }
+            };
+            // wait for each half of P_i, then its PV MMAs
+            auto issue_pv = [&](int i, int s) -> bool {
+                if (!mbar_wait(&ms.p_half[i], pv_done[i] & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+                issue_pv_half(i, s, 0);
+                if (!mbar_wait(&ms.p_full[i], pv_done[i] & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+                issue_pv_half(i, s, 1);
                 ++pv_done[i];
+                return true;
             };
             bool ok = mbar_wait(&ms.q_full, 0, abort_flag) && mbar_wait(&ms.k_full[0], 0, abort_flag);
             tc_fence_after_sync();
@@ -498,29 +517,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     ok = false;
                     break;
                 }
-                if (f & 1u) {
-                    if (!mbar_wait(&ms.p_full[0], pv_done[0] & 1u, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    issue_pv(0, s);
+                if ((f & 1u) && !issue_pv(0, s)) {
+                    ok = false;
+                    break;
                 }
                 if (nxt) {
+                    // K arrives by TMA: the mbarrier alone orders it for the MMA
                     if (!mbar_wait(&ms.k_full[s1], (uint32_t)((u + 1) / NS) & 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after_sync();
                     if (f1 & 1u) issue_s(0, s1);
                 }
-                if (f & 4u) {
-                    if (!mbar_wait(&ms.p_full[1], pv_done[1] & 1u, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    issue_pv(1, s);
+                if ((f & 4u) && !issue_pv(1, s)) {
+                    ok = false;
+                    break;
                 }
                 mma_commit(&ms.v_empty[s]);
                 if (nxt) {
@@ -548,7 +559,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t o_addr = tmem + lane_base + C::o_col(i);
         const uint32_t present = i ? 4u : 1u, fullbit = i ? 8u : 2u;
         ScoreLog2<SCORE> score;
-        score.init(p, h, ms.alibi_tbl);
+        score.init(p, h);
         int doc_q = 0;
         if constexpr (DOC) {
             if (valid) doc_q = __ldg(p.mask.doc_ids + (int64_t)b * p.mask.doc_len + q);
@@ -612,35 +623,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const float m_use = m_run == -INFINITY ? 0.f : m_run;
                 const float sub = score.offset - m_use;
                 const uint64_t sub2 = f2_pack(sub, sub);
-                uint64_t rs2[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) rs2[k] = 0ull;
-                {
-                    uint32_t pk[64];
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) {
-                        float d0, d1;
-                        f2_unpack(f2_add(x2[j], sub2), d0, d1);
-                        const float p0 = ex2_approx(d0);
-                        const float p1 = ex2_approx(d1);
-                        rs2[j & 3] = f2_add(rs2[j & 3], f2_pack(p0, p1));
-                        pk[j] = pack_bf16x2(p0, p1);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t q16[16];
-#pragma unroll
-                        for (int t2 = 0; t2 < 16; ++t2) q16[t2] = pk[16 * j + t2];
-                        tmem_st16(s_addr + 16 * j, q16);
-                    }
-                }
-                float rsum;
-                {
-                    float a0, a1;
-                    f2_unpack(f2_add(f2_add(rs2[0], rs2[1]), f2_add(rs2[2], rs2[3])), a0, a1);
-                    rsum = a0 + a1;
-                }
-                l_run = fmaf(l_run, alpha, rsum);
+                // O rescale (rare) before the first half of P is handed over:
+                // the PV MMA of this step accumulates into the rescaled O
                 if (cnt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
                     for (int c0 = 0; c0 < D; c0 += 32) {
@@ -658,9 +642,39 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         tmem_st32(o_addr + c0, o);
                     }
                 }
-                tmem_wait_st();
-                tc_fence_before_sync();
-                mbar_arrive(&ms.p_full[i]);
+                uint64_t rs2[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) rs2[k] = 0ull;
+                // P in two halves (kv columns 0..63, then 64..127): the MMA warp
+                // starts the first half of PV while the second half is computed
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                    for (int g = 2 * half; g < 2 * half + 2; ++g) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int t2 = 0; t2 < 16; ++t2) {
+                            const int j = 16 * g + t2;
+                            float d0, d1;
+                            f2_unpack(f2_add(x2[j], sub2), d0, d1);
+                            const float p0 = ex2_approx(d0);
+                            const float p1 = ex2_approx(d1);
+                            rs2[j & 3] = f2_add(rs2[j & 3], f2_pack(p0, p1));
+                            pk[t2] = pack_bf16x2(p0, p1);
+                        }
+                        tmem_st16(s_addr + 16 * g, pk);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before_sync();
+                    mbar_arrive(half == 0 ? &ms.p_half[i] : &ms.p_full[i]);
+                }
+                float rsum;
+                {
+                    float a0, a1;
+                    f2_unpack(f2_add(f2_add(rs2[0], rs2[1]), f2_add(rs2[2], rs2[3])), a0, a1);
+                    rsum = a0 + a1;
+                }
+                l_run = fmaf(l_run, alpha, rsum);
                 ++cnt;
             }
             // ---------------------------------------------------- epilogue
