@@ -54,6 +54,10 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // raise the running max only beyond 2^8
+// P_i is handed to the MMA warp in this many column chunks (each with its own
+// mbarrier), so the PV MMAs of the first chunks run while later chunks of P
+// are still being computed.
+constexpr int kPChunks = 2;
 // Register split.  Three warps share each SM sub-partition's 64 KB register
 // file, so the kernel is compiled to kRegsAtLaunch (168) registers per thread.
 // The softmax warpgroups then raise their budget to kRegsSoftmax while the
@@ -79,7 +83,7 @@ struct Bf16Params {
 struct AttnMisc {
     uint64_t q_full;
     uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];
-    uint64_t s_full[2], p_half[2], p_full[2];
+    uint64_t s_full[2], p_part[2][4];  // p_part[i][c]: chunk c of P_i is in TMEM
     uint64_t o_full, drain;
     uint32_t tmem_base;
     int abort;
@@ -336,8 +340,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ms.s_full[i], 1);
-            mbar_init(&ms.p_half[i], 128);
-            mbar_init(&ms.p_full[i], 128);
+            for (int c = 0; c < kPChunks; ++c) mbar_init(&ms.p_part[i][c], 128);
         }
         mbar_init(&ms.o_full, 1);
         mbar_init(&ms.drain, 1);
@@ -477,25 +480,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 mma_commit(&ms.s_full[i]);
             };
-            // O_i += P_i V for kv rows 64 * half .. 64 * half + 63 (four K = 16 steps)
-            auto issue_pv_half = [&](int i, int s, int half) {
+            // O_i += P_i V, chunk by chunk of P_i (8 / kPChunks K = 16 steps each)
+            auto issue_pv = [&](int i, int s) -> bool {
                 const uint32_t va = v_lo0 + ((s * C::kStageBytes) >> 4);
                 const uint32_t acc = pv_done[i] > 0 ? 1u : 0u;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const int k = 4 * half + kk;
-                    mma_ts_lo<kHi>(tmem + C::o_col(i), tmem + C::s_col(i) + k * 8, va + ((k * 2048) >> 4), idesc_o,
-                                   (k > 0 || acc) ? 1u : 0u);
+                for (int c = 0; c < kPChunks; ++c) {
+                    if (!mbar_wait(&ms.p_part[i][c], pv_done[i] & 1u, abort_flag)) return false;
+                    tc_fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < 8 / kPChunks; ++kk) {
+                        const int k = c * (8 / kPChunks) + kk;
+                        mma_ts_lo<kHi>(tmem + C::o_col(i), tmem + C::s_col(i) + k * 8, va + ((k * 2048) >> 4), idesc_o,
+                                       (k > 0 || acc) ? 1u : 0u);
+                    }
                 }
-            };
-            // wait for each half of P_i, then its PV MMAs
-            auto issue_pv = [&](int i, int s) -> bool {
-                if (!mbar_wait(&ms.p_half[i], pv_done[i] & 1u, abort_flag)) return false;
-                tc_fence_after_sync();
-                issue_pv_half(i, s, 0);
-                if (!mbar_wait(&ms.p_full[i], pv_done[i] & 1u, abort_flag)) return false;
-                tc_fence_after_sync();
-                issue_pv_half(i, s, 1);
                 ++pv_done[i];
                 return true;
             };
@@ -645,12 +644,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 uint64_t rs2[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) rs2[k] = 0ull;
-                // P in two halves (kv columns 0..63, then 64..127): the MMA warp
-                // starts the first half of PV while the second half is computed
+                // P in kPChunks column chunks: the MMA warp starts the PV of the
+                // first chunks while the later ones are computed
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                for (int chunk = 0; chunk < kPChunks; ++chunk) {
 #pragma unroll
-                    for (int g = 2 * half; g < 2 * half + 2; ++g) {
+                    for (int g = chunk * (4 / kPChunks); g < (chunk + 1) * (4 / kPChunks); ++g) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int t2 = 0; t2 < 16; ++t2) {
@@ -666,7 +665,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                     tmem_wait_st();
                     tc_fence_before_sync();
-                    mbar_arrive(half == 0 ? &ms.p_half[i] : &ms.p_full[i]);
+                    mbar_arrive(&ms.p_part[i][chunk]);
                 }
                 float rsum;
                 {
