@@ -226,6 +226,16 @@ int flex_device_status(void *stream) {
     return host == 0 ? FLEX_OK : FLEX_ERR_DEVICE_TIMEOUT;
 }
 
+int flex_selftest_wait_timeout(uint32_t limit_ms, void *stream) {
+    if (limit_ms == 0 || limit_ms > 60000) return FLEX_ERR_INVALID_ARG;
+    int err = FLEX_OK;
+    int *status = device_status_word(&err);
+    if (!status) return err;
+    const cudaError_t e =
+        launch_wait_timeout_selftest(status, (uint64_t)limit_ms * 1000000ull, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FLEX_OK : FLEX_ERR_CUDA;
+}
+
 const char *flex_status_string(int status) {
     switch (status) {
         case FLEX_OK:

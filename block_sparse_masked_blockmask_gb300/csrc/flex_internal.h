@@ -85,6 +85,8 @@ cudaError_t launch_block_mask(const MaskDesc &mask, int B, int H, int q_len, int
 cudaError_t launch_attn_fp32(const AttnProblem &p, cudaStream_t stream);
 cudaError_t launch_attn_bf16(const AttnProblem &p, cudaStream_t stream);
 
+cudaError_t launch_wait_timeout_selftest(int *status, uint64_t limit_ns, cudaStream_t stream);
+
 // The per-device workspace holding the status word (allocated once per device).
 int *device_status_word(int *err);
 

@@ -38,7 +38,8 @@ FLEX_DTYPE_BF16 = 0
 FLEX_DTYPE_FP32 = 1
 
 EXPORTED = ("flex_block_mask_sizes", "flex_block_mask_create", "flex_attention_fwd",
-            "flex_attention_fwd_noalloc", "flex_device_status", "flex_status_string")
+            "flex_attention_fwd_noalloc", "flex_device_status", "flex_selftest_wait_timeout",
+            "flex_status_string")
 
 
 class FlexError(RuntimeError):
@@ -98,6 +99,8 @@ def load_library():
             lib.flex_attention_fwd_noalloc.restype = ctypes.c_int
             lib.flex_device_status.argtypes = [vp]
             lib.flex_device_status.restype = ctypes.c_int
+            lib.flex_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
+            lib.flex_selftest_wait_timeout.restype = ctypes.c_int
             lib.flex_status_string.argtypes = [ctypes.c_int]
             lib.flex_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -233,6 +236,15 @@ def flex_attention_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor
     if rc != FLEX_OK:
         raise FlexError(rc, "flex_attention_fwd_noalloc")
     return ctypes.cast(status, ctypes.c_void_p).value
+
+
+def flex_selftest_wait_timeout(limit_ms: int = 50, stream=None, device=None) -> None:
+    """Enqueue the bounded-wait failure check (see include/flexattn.h)."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(device):
+        rc = load_library().flex_selftest_wait_timeout(int(limit_ms), _stream_handle(stream, device))
+    if rc != FLEX_OK:
+        raise FlexError(rc, "flex_selftest_wait_timeout")
 
 
 def flex_device_status(stream=None, device=None) -> int:

@@ -215,6 +215,17 @@ FLEX_API int flex_attention_fwd_noalloc(const flex_tensor *q, const flex_tensor 
  */
 FLEX_API int flex_device_status(void *stream);
 
+/*
+ * Diagnostic of the failure path: enqueues on `stream` a one-warp kernel that
+ * waits on an mbarrier no thread arrives at, using the same bounded wait as the
+ * attention kernel but with a limit of `limit_ms` milliseconds (1..60000).
+ * The wait gives up, the kernel records FLEX_ERR_DEVICE_TIMEOUT in the device
+ * status word and returns; flex_device_status() then reports it and clears
+ * it.  The GPU context stays usable.  Errors: FLEX_ERR_INVALID_ARG,
+ * FLEX_ERR_CUDA.
+ */
+FLEX_API int flex_selftest_wait_timeout(uint32_t limit_ms, void *stream);
+
 /* A static, human-readable name for a flex_status value. */
 FLEX_API const char *flex_status_string(int status);
 
