@@ -13,9 +13,10 @@
 //   * A CTA owns two consecutive q blocks (two 128-row Q tiles) of one
 //     (batch, head) and walks the union of their kv-tile lists in descending
 //     kv order, so the K/V tile staged in shared memory serves both Q tiles.
-//   * warp 8  (TMA)     : loads Q0/Q1 once, then K and V tiles of each union
-//                         step into a ring of shared-memory stages (128-byte
-//                         swizzle, the layout tcgen05 descriptors read).
+//   * warps 8 / 10 (TMA): load the K tiles / the V tiles of each union step
+//                         into a ring of shared-memory stages (128-byte
+//                         swizzle, the layout tcgen05 descriptors read); Q0/Q1
+//                         are loaded by thread 0 at the start of the prologue.
 //   * warp 9  (MMA)     : one thread issues tcgen05.mma: S_i = Q_i K^T into
 //                         tensor memory (TMEM) and O_i += P_i V with P_i read
 //                         from TMEM; order per step PV0, S0(next), PV1,
@@ -48,11 +49,13 @@
 namespace flex {
 
 constexpr int kAttnThreads = 384;
-constexpr int kTmaWarp = 8;
+constexpr int kTmaWarp = 8;   // Q and K loads
+constexpr int kTmaVWarp = 10; // V loads
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kHeadGroup = 4;              // (batch, head) pairs scheduled together
 constexpr float kRescaleThreshold = 8.0f;  // raise the running max only beyond 2^8
 // P_i is handed to the MMA warp in this many column chunks (each with its own
 // mbarrier), so the PV MMAs of the first chunks run while later chunks of P
@@ -319,12 +322,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     AttnMisc &ms = *reinterpret_cast<AttnMisc *>(smem + C::kMiscOff);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    // Work item: heads outermost (their K/V stay in L2 while in flight),
-    // q-block pairs from the last (the longest kv lists for causal-like
-    // masks) to the first.
+    // Work item: heads in groups of kHeadGroup (their K/V stay in L2 while in
+    // flight); inside a group, q-block pairs from the last (the longest kv
+    // lists for causal-like masks) to the first, the group's heads innermost,
+    // so the heaviest items of each group start first and the final wave is
+    // made of light items.
     const int item = blockIdx.x;
-    const int bh = item / p.npairs;
-    const int pair = p.npairs - 1 - item % p.npairs;
+    const int nbh = p.B * p.H;
+    const int group_items = kHeadGroup * p.npairs;
+    const int g0 = (item / group_items) * kHeadGroup;
+    const int gsize = min(kHeadGroup, nbh - g0);
+    const int r = item - (item / group_items) * group_items;
+    const int pair = p.npairs - 1 - r / gsize;
+    const int bh = g0 + r % gsize;
     const int b = bh / p.H, h = bh % p.H;
     const int qb0 = 2 * pair;
     const bool has1 = qb0 + 1 < p.nqb;
@@ -346,6 +356,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_init(&ms.drain, 1);
         ms.abort = 0;
         fence_barrier_init();
+        // Q tiles first: their load latency overlaps the union build below
+        prefetch_tensormap(&tmap_q);
+        mbar_arrive_expect_tx(&ms.q_full, (has1 ? 2u : 1u) * C::kTileBytes);
+        for (int a = 0; a < C::kAtoms; ++a) {
+            tma_load_4d(smem + C::kQOff + a * C::kAtomBytes, &tmap_q, &ms.q_full, 64 * a, qb0 * kBlock, h, b);
+            if (has1)
+                tma_load_4d(smem + C::kQOff + C::kTileBytes + a * C::kAtomBytes, &tmap_q, &ms.q_full, 64 * a,
+                            (qb0 + 1) * kBlock, h, b);
+        }
     }
     if (warp == kMmaWarp) {
         tmem_alloc(&ms.tmem_base, kTmemCols);
@@ -402,57 +421,41 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp >= 8) {
         regs_decrease<kRegsControl>();
     }
-    if (warp == kTmaWarp) {
-        // ------------------------------------------------------ TMA producer
+    if (warp == kTmaWarp || warp == kTmaVWarp) {
+        // ----------------------------------------------------- TMA producers
+        // warp 8 loads Q and the K tiles, warp 10 the V tiles.  K of a stage is
+        // free once its step's S MMAs are done, V once its PV MMAs are; with
+        // one producer each, a late V release never holds back the next K.
         if (lane == 0 && nu > 0) {
-            constexpr bool is_doc = DOC;
+            const bool is_k = warp == kTmaWarp;
+            const CUtensorMap *map = is_k ? &tmap_k : &tmap_v;
+            uint64_t *full = is_k ? ms.k_full : ms.v_full;
+            uint64_t *empty = is_k ? ms.k_empty : ms.v_empty;
+            const uint32_t half = is_k ? 0u : C::kTileBytes;
+            // the kv tile's document ids travel with V: V's stage is released
+            // only after both softmax groups are done with the tile
+            const bool with_doc = DOC && !is_k;
             const int32_t *doc_row = DOC ? p.mask.doc_ids + (int64_t)b * p.mask.doc_len : nullptr;
-            prefetch_tensormap(&tmap_q);
-            prefetch_tensormap(&tmap_k);
-            prefetch_tensormap(&tmap_v);
-            mbar_arrive_expect_tx(&ms.q_full, (has1 ? 2u : 1u) * C::kTileBytes);
-            for (int a = 0; a < C::kAtoms; ++a) {
-                tma_load_4d(smem + C::kQOff + a * C::kAtomBytes, &tmap_q, &ms.q_full, 64 * a, qb0 * kBlock, h, b);
-                if (has1)
-                    tma_load_4d(smem + C::kQOff + C::kTileBytes + a * C::kAtomBytes, &tmap_q, &ms.q_full, 64 * a,
-                                (qb0 + 1) * kBlock, h, b);
-            }
+            prefetch_tensormap(map);
             int issued = 0;
             for (int u = 0; u < nu; ++u) {
                 const int s = u % NS;
                 const uint32_t use = (uint32_t)(u / NS);
                 const int kv0 = (int)(ms.ulist[u] & 0xFFFFu) * kBlock;
-                uint8_t *kd = smem + C::kKvOff + s * C::kStageBytes;
-                uint8_t *vd = kd + C::kTileBytes;
-                // K of this stage is free once the S MMAs of its previous step are done,
-                // V once the PV MMAs are: the two are released separately.
-                if (use > 0 && !mbar_wait(&ms.k_empty[s], (use - 1) & 1u, abort_flag)) {
+                uint8_t *dst = smem + C::kKvOff + s * C::kStageBytes + half;
+                if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, abort_flag)) {
                     record_failure(ms, p.status);
                     break;
                 }
-                mbar_arrive_expect_tx(&ms.k_full[s], C::kTileBytes);
-                for (int a = 0; a < C::kAtoms; ++a)
-                    tma_load_4d(kd + a * C::kAtomBytes, &tmap_k, &ms.k_full[s], 64 * a, kv0, h, b);
-                if (use > 0 && !mbar_wait(&ms.v_empty[s], (use - 1) & 1u, abort_flag)) {
-                    record_failure(ms, p.status);
-                    drain_wait(&ms.k_full[s], use & 1u);
-                    break;
-                }
-                // the kv tile's document ids travel with V: V's stage is released
-                // only after both softmax groups are done with the tile
-                mbar_arrive_expect_tx(&ms.v_full[s], C::kTileBytes + (is_doc ? 512u : 0u));
-                for (int a = 0; a < C::kAtoms; ++a)
-                    tma_load_4d(vd + a * C::kAtomBytes, &tmap_v, &ms.v_full[s], 64 * a, kv0, h, b);
-                if (is_doc) bulk_load(ms.stage_doc[s], doc_row + kv0, 512u, &ms.v_full[s]);
+                mbar_arrive_expect_tx(&full[s], C::kTileBytes + (with_doc ? 512u : 0u));
+                for (int a = 0; a < C::kAtoms; ++a) tma_load_4d(dst + a * C::kAtomBytes, map, &full[s], 64 * a, kv0, h, b);
+                if (with_doc) bulk_load(ms.stage_doc[s], doc_row + kv0, 512u, &full[s]);
                 issued = u + 1;
             }
             // Drain: every copy issued above must land before the CTA exits.
-            drain_wait(&ms.q_full, 0);
             for (int s = 0; s < NS && s < issued; ++s) {
                 const int last = s + ((issued - 1 - s) / NS) * NS;
-                const uint32_t par = (uint32_t)(last / NS) & 1u;
-                drain_wait(&ms.k_full[s], par);
-                drain_wait(&ms.v_full[s], par);
+                drain_wait(&full[s], (uint32_t)(last / NS) & 1u);
             }
         }
         __syncwarp();
@@ -712,6 +715,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
 
     // ---------------------------------------------------------- teardown
+    if (threadIdx.x == 0) drain_wait(&ms.q_full, 0);  // the Q copies issued in the prologue have landed
     tc_fence_before_sync();
     __syncthreads();
     if (warp == kMmaWarp) {
