@@ -58,9 +58,12 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kHeadGroup = 4;              // (batch, head) pairs scheduled together
 constexpr float kRescaleThreshold = 8.0f;  // raise the running max only beyond 2^8
 // P_i is handed to the MMA warp in this many column chunks (each with its own
-// mbarrier), so the PV MMAs of the first chunks run while later chunks of P
-// are still being computed.
-constexpr int kPChunks = 2;
+// mbarrier); with more than one, the PV MMAs of the first chunks can run while
+// later chunks of P are still being computed.  One chunk measures fastest: the
+// thread that issues the MMAs spends ~46 cycles issuing each 64-cycle MMA, so
+// the extra wait and fence per chunk cost more tensor-core time than the
+// earlier start gains.
+constexpr int kPChunks = 1;
 // Register split.  Three warps share each SM sub-partition's 64 KB register
 // file, so the kernel is compiled to kRegsAtLaunch (168) registers per thread.
 // The softmax warpgroups then raise their budget to kRegsSoftmax while the
