@@ -9,14 +9,20 @@
 // (l = l * alpha + sum(p); acc = acc * alpha; acc += p V) carried out with
 // the running max in base-2 units.
 //
-// Design for one GB300 SM (one CTA per SM, 384 threads):
-//   * A CTA owns two consecutive q blocks (two 128-row Q tiles) of one
-//     (batch, head) and walks the union of their kv-tile lists in descending
-//     kv order, so the K/V tile staged in shared memory serves both Q tiles.
+// Design for one GB300 SM (one persistent CTA per SM, 384 threads):
+//   * A work item is two consecutive q blocks (two 128-row Q tiles) of one
+//     (batch, head); the CTA walks the union of their kv-tile lists in
+//     descending kv order, so the K/V tile staged in shared memory serves
+//     both Q tiles.  After its first item (its own index) a CTA takes the
+//     items of CTAs that have not started yet (cluster launch control).
+//   * warp 11 (scheduler): builds each item's union list into one of two
+//                         shared-memory slots, loads its Q tiles once the
+//                         previous item's S MMAs are done, and fetches the
+//                         next item while the current one computes.
 //   * warps 8 / 10 (TMA): load the K tiles / the V tiles of each union step
 //                         into a ring of shared-memory stages (128-byte
-//                         swizzle, the layout tcgen05 descriptors read); Q0/Q1
-//                         are loaded by thread 0 at the start of the prologue.
+//                         swizzle, the layout tcgen05 descriptors read) that
+//                         runs on across items.
 //   * warp 9  (MMA)     : one thread issues tcgen05.mma: S_i = Q_i K^T into
 //                         tensor memory (TMEM) and O_i += P_i V with P_i read
 //                         from TMEM; order per step PV0, S0(next), PV1,
@@ -52,27 +58,27 @@ constexpr int kAttnThreads = 384;
 constexpr int kTmaWarp = 8;   // Q and K loads
 constexpr int kTmaVWarp = 10; // V loads
 constexpr int kMmaWarp = 9;
+constexpr int kSchedWarp = 11; // work items: union lists, Q loads, next item by launch control
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kHeadGroup = 4;              // (batch, head) pairs scheduled together
 constexpr float kRescaleThreshold = 8.0f;  // raise the running max only beyond 2^8
-// P_i is handed to the MMA warp in this many column chunks (each with its own
-// mbarrier); with more than one, the PV MMAs of the first chunks can run while
-// later chunks of P are still being computed.  One chunk measures fastest: the
-// thread that issues the MMAs spends ~46 cycles issuing each 64-cycle MMA, so
-// the extra wait and fence per chunk cost more tensor-core time than the
-// earlier start gains.
-constexpr int kPChunks = 1;
+// P_i is handed to the MMA warp whole (one mbarrier per tile), not in column
+// chunks: the thread that issues the MMAs spends ~46 cycles issuing each
+// 64-cycle 128x128x16 MMA, so an extra wait and fence per chunk costs more
+// tensor-core time than starting the PV on the first chunk early gains.
 // Register split.  Three warps share each SM sub-partition's 64 KB register
 // file, so the kernel is compiled to kRegsAtLaunch (168) registers per thread.
 // The softmax warpgroups then raise their budget to kRegsSoftmax while the
-// TMA/MMA warpgroup lowers its own to kRegsControl; per sub-partition this is
-// 2 * 224 + 56 = 3 * 168 registers per lane, so the increase never waits on
-// registers that are not released.  The launcher checks the compiled count.
+// scheduler/TMA/MMA warpgroup lowers its own to kRegsControl (enough for its
+// loop state without spilling); per sub-partition this is 2 * 216 + 72 =
+// 3 * 168 registers per lane, the registers the CTA was launched with, so the
+// increase never waits on registers that are not released.  The launcher
+// checks the compiled count.
 constexpr uint32_t kRegsAtLaunch = 168;
-constexpr uint32_t kRegsSoftmax = 224;
-constexpr uint32_t kRegsControl = 56;
+constexpr uint32_t kRegsSoftmax = 216;
+constexpr uint32_t kRegsControl = 72;
 static_assert(2 * kRegsSoftmax + kRegsControl == 3 * kRegsAtLaunch, "register split");
 
 struct Bf16Params {
@@ -85,23 +91,38 @@ struct Bf16Params {
     int *status;
 };
 
-// Shared-memory bookkeeping that follows the Q/K/V tiles.
-struct AttnMisc {
-    uint64_t q_full;
-    uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];
-    uint64_t s_full[2], p_part[2][4];  // p_part[i][c]: chunk c of P_i is in TMEM
-    uint64_t o_full, drain;
-    uint32_t tmem_base;
-    int abort;
-    int n_union;
-    int pad;
-    alignas(16) int32_t stage_doc[4][128];     // document ids of each stage's kv tile (bulk-copy target)
-    alignas(16) uint32_t flags[kMaxKvBlocks];  // bit0/bit1 present/full in tile 0, bit2/bit3 in tile 1
+// One work item (two consecutive q blocks of one (batch, head)) as the
+// scheduler warp publishes it.
+struct ItemSlot {
+    int nu;                                    // union length; -1: no more work for this CTA
+    int b, h, qb0, has1;
+    int pad[3];
     alignas(16) uint32_t ulist[kMaxKvBlocks];  // union, descending kv: kv block | flags << 16
 };
-// bulk copies need 16-byte aligned shared-memory destinations
+
+// Shared-memory bookkeeping that follows the Q/K/V tiles.
+struct AttnMisc {
+    uint64_t q_full, q_empty;
+    uint64_t near_end;                         // the K producer has issued an item's last K tile
+    uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];
+    uint64_t s_full[2], p_full[2];             // p_full[i]: all of P_i is in TMEM
+    uint64_t o_full, drain;
+    uint64_t item_ready[2], item_free[2];      // per item slot
+    uint64_t clc_bar;                          // cluster-launch-control response landed
+    uint32_t tmem_base;
+    int abort;
+    alignas(16) uint32_t clc_resp[4];
+    alignas(16) int32_t stage_doc[4][128];     // document ids of each stage's kv tile (bulk-copy target)
+    alignas(16) uint32_t flags[kMaxKvBlocks];  // bit0/bit1 present/full in tile 0, bit2/bit3 in tile 1
+    ItemSlot slot[2];
+};
+// bulk copies and the launch-control response need 16-byte aligned destinations
+static_assert(offsetof(AttnMisc, clc_resp) % 16 == 0, "clc_resp alignment");
 static_assert(offsetof(AttnMisc, stage_doc) % 16 == 0, "stage_doc alignment");
 static_assert(sizeof(AttnMisc::stage_doc[0]) % 16 == 0, "stage_doc row size");
+static_assert(offsetof(AttnMisc, slot) % 16 == 0 && sizeof(ItemSlot) % 16 == 0, "item slot alignment");
+// arrivals that free an item slot: both TMA producers, the MMA thread, 8 softmax warps
+constexpr uint32_t kItemConsumers = 11;
 
 template <int D>
 struct Bf16Cfg {
@@ -312,8 +333,85 @@ __device__ __forceinline__ void apply_document_mask(int q, int kv0, int doc_q, c
         x2[j] = keep_pair(x2[j], (keep[j / 16] >> ((2 * j) % 32)) & 1u, (keep[j / 16] >> ((2 * j + 1) % 32)) & 1u);
 }
 
+// Decode work item `item` (a CTA index of the launch grid): heads in groups of
+// kHeadGroup (their K/V stay in L2 while in flight); inside a group, q-block
+// pairs from the last (the longest kv lists for causal-like masks) to the
+// first, the group's heads innermost, so the heaviest items of each group come
+// first and the last items of the grid are light.
+__device__ __forceinline__ void decode_item(const Bf16Params &p, int item, int &b, int &h, int &qb0, int &has1) {
+    const int nbh = p.B * p.H;
+    const int group_items = kHeadGroup * p.npairs;
+    const int g0 = (item / group_items) * kHeadGroup;
+    const int gsize = min(kHeadGroup, nbh - g0);
+    const int r = item - (item / group_items) * group_items;
+    const int pair = p.npairs - 1 - r / gsize;
+    const int bh = g0 + r % gsize;
+    b = bh / p.H;
+    h = bh % p.H;
+    qb0 = 2 * pair;
+    has1 = qb0 + 1 < p.nqb ? 1 : 0;
+}
+
+// Build an item's union list into `sl` with the 32 lanes of one warp:
+// mark every kv tile of both q blocks (bounds-checked: a malformed BlockMask
+// cannot write outside the flag array), then compact the marked tiles in
+// descending kv order.
+__device__ __forceinline__ void build_item(const Bf16Params &p, AttnMisc &ms, ItemSlot &sl, int item, int lane) {
+    int b, h, qb0, has1;
+    decode_item(p, item, b, h, qb0, has1);
+    const int nkvb = p.nkvb;
+    for (int j = lane; j < nkvb; j += 32) ms.flags[j] = 0u;
+    __syncwarp();
+    const int64_t row0 = ((int64_t)b * p.H + h) * p.nqb + qb0;
+    const int32_t *pidx = p.kv_idx + row0 * nkvb, *fidx = p.full_idx + row0 * nkvb;
+    const int np0 = min(max(p.kv_num[row0], 0), nkvb), nf0 = min(max(p.full_num[row0], 0), nkvb);
+    const int np1 = has1 ? min(max(p.kv_num[row0 + 1], 0), nkvb) : 0;
+    const int nf1 = has1 ? min(max(p.full_num[row0 + 1], 0), nkvb) : 0;
+    for (int x = lane; x < np0; x += 32) {
+        const int j = pidx[x];
+        if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 1u);
+    }
+    for (int x = lane; x < nf0; x += 32) {
+        const int j = fidx[x];
+        if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 3u);
+    }
+    for (int x = lane; x < np1; x += 32) {
+        const int j = pidx[nkvb + x];
+        if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 4u);
+    }
+    for (int x = lane; x < nf1; x += 32) {
+        const int j = fidx[nkvb + x];
+        if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 12u);
+    }
+    __syncwarp();
+    int count = 0;
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = 0; base < nkvb; base += 32) {
+        const int c = nkvb - 1 - (base + lane);
+        const uint32_t f = c >= 0 ? ms.flags[c] : 0u;
+        const unsigned bal = __ballot_sync(0xffffffffu, f != 0u);
+        if (f != 0u) sl.ulist[count + __popc(bal & lt)] = (uint32_t)c | (f << 16);
+        count += __popc(bal);
+    }
+    if (lane == 0) {
+        sl.nu = count;
+        sl.b = b;
+        sl.h = h;
+        sl.qb0 = qb0;
+        sl.has1 = has1;
+    }
+    __syncwarp();
+}
+
 // DOC: the BlockMask's mask_mod is the document mask (its partial tiles read
 // per-tile document ids staged next to V); other kinds are interval masks.
+//
+// Persistent over work items: each CTA starts with the item of its own index
+// and then takes items from CTAs of the grid that have not started yet
+// (cluster launch control), so one CTA stays on each SM and the next item's
+// union list, Q tiles and first K/V tiles load while the current item
+// computes.  Every role walks the same sequence of published items; all
+// barrier phases (K/V ring, S/P hand-off, Q, O) continue across items.
 template <int D, int SCORE, bool DOC>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -325,26 +423,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     AttnMisc &ms = *reinterpret_cast<AttnMisc *>(smem + C::kMiscOff);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    // Work item: heads in groups of kHeadGroup (their K/V stay in L2 while in
-    // flight); inside a group, q-block pairs from the last (the longest kv
-    // lists for causal-like masks) to the first, the group's heads innermost,
-    // so the heaviest items of each group start first and the final wave is
-    // made of light items.
-    const int item = blockIdx.x;
-    const int nbh = p.B * p.H;
-    const int group_items = kHeadGroup * p.npairs;
-    const int g0 = (item / group_items) * kHeadGroup;
-    const int gsize = min(kHeadGroup, nbh - g0);
-    const int r = item - (item / group_items) * group_items;
-    const int pair = p.npairs - 1 - r / gsize;
-    const int bh = g0 + r % gsize;
-    const int b = bh / p.H, h = bh % p.H;
-    const int qb0 = 2 * pair;
-    const bool has1 = qb0 + 1 < p.nqb;
-    const int64_t row0 = (int64_t)bh * p.nqb + qb0;
-
     if (threadIdx.x == 0) {
         mbar_init(&ms.q_full, 1);
+        mbar_init(&ms.q_empty, 1);
+        mbar_init(&ms.near_end, 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(&ms.k_full[s], 1);
             mbar_init(&ms.v_full[s], 1);
@@ -353,83 +435,116 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ms.s_full[i], 1);
-            for (int c = 0; c < kPChunks; ++c) mbar_init(&ms.p_part[i][c], 128);
+            mbar_init(&ms.p_full[i], 128);
+            mbar_init(&ms.item_ready[i], 1);
+            mbar_init(&ms.item_free[i], kItemConsumers);
         }
         mbar_init(&ms.o_full, 1);
         mbar_init(&ms.drain, 1);
+        mbar_init(&ms.clc_bar, 1);
         ms.abort = 0;
         fence_barrier_init();
-        // Q tiles first: their load latency overlaps the union build below
-        prefetch_tensormap(&tmap_q);
-        mbar_arrive_expect_tx(&ms.q_full, (has1 ? 2u : 1u) * C::kTileBytes);
-        for (int a = 0; a < C::kAtoms; ++a) {
-            tma_load_4d(smem + C::kQOff + a * C::kAtomBytes, &tmap_q, &ms.q_full, 64 * a, qb0 * kBlock, h, b);
-            if (has1)
-                tma_load_4d(smem + C::kQOff + C::kTileBytes + a * C::kAtomBytes, &tmap_q, &ms.q_full, 64 * a,
-                            (qb0 + 1) * kBlock, h, b);
-        }
     }
     if (warp == kMmaWarp) {
         tmem_alloc(&ms.tmem_base, kTmemCols);
         tmem_relinquish();
     }
-    for (int i = threadIdx.x; i < p.nkvb; i += kAttnThreads) ms.flags[i] = 0u;
-    __syncthreads();
-
-    // Mark every kv tile of both q blocks (bounds-checked: a malformed
-    // BlockMask cannot write outside the flag array).
-    {
-        const int nkvb = p.nkvb;
-        const int32_t *pidx = p.kv_idx + row0 * nkvb, *fidx = p.full_idx + row0 * nkvb;
-        const int np0 = min(max(p.kv_num[row0], 0), nkvb), nf0 = min(max(p.full_num[row0], 0), nkvb);
-        const int np1 = has1 ? min(max(p.kv_num[row0 + 1], 0), nkvb) : 0;
-        const int nf1 = has1 ? min(max(p.full_num[row0 + 1], 0), nkvb) : 0;
-        for (int i = threadIdx.x; i < np0; i += kAttnThreads) {
-            const int j = pidx[i];
-            if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 1u);
-        }
-        for (int i = threadIdx.x; i < nf0; i += kAttnThreads) {
-            const int j = fidx[i];
-            if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 3u);
-        }
-        for (int i = threadIdx.x; i < np1; i += kAttnThreads) {
-            const int j = pidx[nkvb + i];
-            if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 4u);
-        }
-        for (int i = threadIdx.x; i < nf1; i += kAttnThreads) {
-            const int j = fidx[nkvb + i];
-            if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 12u);
-        }
-    }
-    __syncthreads();
-    if (warp == 0) {  // union of the two lists, descending kv order
-        int count = 0;
-        const unsigned lt = (1u << lane) - 1u;
-        for (int base = 0; base < p.nkvb; base += 32) {
-            const int c = p.nkvb - 1 - (base + lane);
-            const uint32_t f = c >= 0 ? ms.flags[c] : 0u;
-            const unsigned bal = __ballot_sync(0xffffffffu, f != 0u);
-            if (f != 0u) ms.ulist[count + __popc(bal & lt)] = (uint32_t)c | (f << 16);
-            count += __popc(bal);
-        }
-        if (lane == 0) ms.n_union = count;
-    }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = ms.tmem_base;
-    const int nu = ms.n_union;
     volatile int *abort_flag = &ms.abort;
 
     if (warp >= 8) {
         regs_decrease<kRegsControl>();
     }
-    if (warp == kTmaWarp || warp == kTmaVWarp) {
+    if (warp == kSchedWarp) {
+        // ----------------------------------------------------------- scheduler
+        // Item n goes to slot n % 2 once every consumer has released that
+        // slot's item n - 2.  The next item is taken from the grid when the
+        // current one has its last K tile on the way (near_end, about one
+        // ring depth before its end): late enough that no item sits claimed
+        // behind much work while other SMs run dry at the end of the grid,
+        // early enough that the next item's list is published (the K/V
+        // producers run on into it) and its Q tiles are prefetched into L2
+        // before the current item ends.  Q is loaded into shared memory as
+        // soon as the current item's last S MMAs are done with it (q_empty).
+        int item = blockIdx.x;
+        uint32_t nq = 0;    // Q loads issued
+        uint32_t nne = 0;   // near_end phases consumed
+        uint32_t nclc = 0;  // launch-control responses consumed
+        bool ok = true;
+        if (lane == 0) prefetch_tensormap(&tmap_q);
+        for (uint32_t n = 0;; ++n) {
+            const int k = (int)(n & 1u);
+            ItemSlot &sl = ms.slot[k];
+            if (n >= 2 && !warp_wait(&ms.item_free[k], ((n - 2) >> 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            if (item >= 0) {
+                build_item(p, ms, sl, item, lane);
+            } else if (lane == 0) {
+                sl.nu = -1;
+            }
+            __threadfence_block();  // every lane's slot writes before the release below
+            __syncwarp();
+            const int nu = sl.nu;
+            if (lane == 0) mbar_arrive(&ms.item_ready[k]);
+            if (item < 0) break;
+            if (nu > 0) {
+                const int has1 = sl.has1;
+                if (lane == 0)
+                    for (int a = 0; a < C::kAtoms; ++a)
+                        for (int i = 0; i <= has1; ++i) tma_prefetch_l2_4d(&tmap_q, 64 * a, (sl.qb0 + i) * kBlock, sl.h, sl.b);
+                // the previous item with work has finished its S MMAs
+                if (nq > 0 && !warp_wait(&ms.q_empty, (nq - 1) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&ms.q_full, (has1 ? 2u : 1u) * C::kTileBytes);
+                    for (int a = 0; a < C::kAtoms; ++a) {
+                        tma_load_4d(smem + C::kQOff + a * C::kAtomBytes, &tmap_q, &ms.q_full, 64 * a, sl.qb0 * kBlock,
+                                    sl.h, sl.b);
+                        if (has1)
+                            tma_load_4d(smem + C::kQOff + C::kTileBytes + a * C::kAtomBytes, &tmap_q, &ms.q_full,
+                                        64 * a, (sl.qb0 + 1) * kBlock, sl.h, sl.b);
+                    }
+                }
+                ++nq;
+                // wait until this item's last K tile is on the way
+                if (!warp_wait(&ms.near_end, nne & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ++nne;
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&ms.clc_bar, 16u);
+                clc_try_cancel(ms.clc_resp, &ms.clc_bar);
+            }
+            if (!warp_wait(&ms.clc_bar, nclc & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            ++nclc;
+            int next = 0;
+            if (lane == 0) next = clc_cancelled_x(ms.clc_resp);
+            item = __shfl_sync(0xffffffffu, next, 0);
+        }
+        if (!ok && lane == 0) record_failure(ms, p.status);
+        // every Q copy issued above lands before the CTA exits (normally the
+        // MMA thread has already consumed it)
+        if (lane == 0 && nq > 0) drain_wait(&ms.q_full, (nq - 1) & 1u);
+        __syncwarp();
+    } else if (warp == kTmaWarp || warp == kTmaVWarp) {
         // ----------------------------------------------------- TMA producers
-        // warp 8 loads Q and the K tiles, warp 10 the V tiles.  K of a stage is
-        // free once its step's S MMAs are done, V once its PV MMAs are; with
-        // one producer each, a late V release never holds back the next K.
-        if (lane == 0 && nu > 0) {
+        // warp 8 loads the K tiles, warp 10 the V tiles, into the stage ring
+        // indexed by the CTA's global step count.  K of a stage is free once
+        // its step's S MMAs are done, V once its PV MMAs are; with one
+        // producer each, a late V release never holds back the next K.
+        if (lane == 0) {
             const bool is_k = warp == kTmaWarp;
             const CUtensorMap *map = is_k ? &tmap_k : &tmap_v;
             uint64_t *full = is_k ? ms.k_full : ms.v_full;
@@ -438,37 +553,55 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // the kv tile's document ids travel with V: V's stage is released
             // only after both softmax groups are done with the tile
             const bool with_doc = DOC && !is_k;
-            const int32_t *doc_row = DOC ? p.mask.doc_ids + (int64_t)b * p.mask.doc_len : nullptr;
             prefetch_tensormap(map);
-            int issued = 0;
-            for (int u = 0; u < nu; ++u) {
-                const int s = u % NS;
-                const uint32_t use = (uint32_t)(u / NS);
-                const int kv0 = (int)(ms.ulist[u] & 0xFFFFu) * kBlock;
-                uint8_t *dst = smem + C::kKvOff + s * C::kStageBytes + half;
-                if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, abort_flag)) {
-                    record_failure(ms, p.status);
+            uint32_t g = 0;  // steps issued over all items
+            bool ok = true;
+            for (uint32_t n = 0; ok; ++n) {
+                const int k = (int)(n & 1u);
+                const ItemSlot &sl = ms.slot[k];
+                if (!mbar_wait(&ms.item_ready[k], (n >> 1) & 1u, abort_flag)) {
+                    ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&full[s], C::kTileBytes + (with_doc ? 512u : 0u));
-                for (int a = 0; a < C::kAtoms; ++a) tma_load_4d(dst + a * C::kAtomBytes, map, &full[s], 64 * a, kv0, h, b);
-                if (with_doc) bulk_load(ms.stage_doc[s], doc_row + kv0, 512u, &full[s]);
-                issued = u + 1;
+                const int nu = sl.nu;
+                if (nu < 0) break;
+                const int b = sl.b, h = sl.h;
+                const int32_t *doc_row = DOC ? p.mask.doc_ids + (int64_t)b * p.mask.doc_len : nullptr;
+                for (int u = 0; u < nu; ++u, ++g) {
+                    const int s = (int)(g % NS);
+                    const uint32_t use = g / NS;
+                    const int kv0 = (int)(sl.ulist[u] & 0xFFFFu) * kBlock;
+                    uint8_t *dst = smem + C::kKvOff + s * C::kStageBytes + half;
+                    if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], C::kTileBytes + (with_doc ? 512u : 0u));
+                    for (int a = 0; a < C::kAtoms; ++a) tma_load_4d(dst + a * C::kAtomBytes, map, &full[s], 64 * a, kv0, h, b);
+                    if (with_doc) bulk_load(ms.stage_doc[s], doc_row + kv0, 512u, &full[s]);
+                }
+                // The last K tile of the item is issued once its stage is free,
+                // about one ring depth (kStages steps) before the item ends:
+                // the scheduler takes the next item now.
+                if (ok && is_k && nu > 0) mbar_arrive(&ms.near_end);
+                if (ok) mbar_arrive(&ms.item_free[k]);
             }
-            // Drain: every copy issued above must land before the CTA exits.
-            for (int s = 0; s < NS && s < issued; ++s) {
-                const int last = s + ((issued - 1 - s) / NS) * NS;
-                drain_wait(&full[s], (uint32_t)(last / NS) & 1u);
+            if (!ok) record_failure(ms, p.status);
+            // Drain: every copy issued above lands before the CTA exits.
+            for (uint32_t s = 0; s < (uint32_t)NS && s < g; ++s) {
+                const uint32_t last = s + ((g - 1 - s) / NS) * NS;
+                drain_wait(&full[s], (last / NS) & 1u);
             }
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0 && nu > 0) {
+        if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
             const uint32_t q_addr0 = smem_u32(smem + C::kQOff);
-            uint32_t pv_done[2] = {0u, 0u};
+            uint32_t pv_total[2] = {0u, 0u};  // PV groups issued per tile, over all items
+            uint32_t pv_item[2] = {0u, 0u};   // ... within the current item
             // Q and K are K-major (rows of 64 elements per 128-byte swizzle
             // atom, 8-row groups 1024 bytes apart); V is MN-major (kv rows of
             // 64 head-dim elements, the two 64-wide halves 16 KB apart).
@@ -486,68 +619,89 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 mma_commit(&ms.s_full[i]);
             };
-            // O_i += P_i V, chunk by chunk of P_i (8 / kPChunks K = 16 steps each)
+            // O_i += P_i V once all of P_i is in TMEM; the first PV of an item
+            // overwrites O_i (its epilogue read of the previous item came
+            // before this P in the softmax warps' program order)
             auto issue_pv = [&](int i, int s) -> bool {
                 const uint32_t va = v_lo0 + ((s * C::kStageBytes) >> 4);
-                const uint32_t acc = pv_done[i] > 0 ? 1u : 0u;
+                const uint32_t acc = pv_item[i] > 0 ? 1u : 0u;
+                if (!mbar_wait(&ms.p_full[i], pv_total[i] & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
 #pragma unroll
-                for (int c = 0; c < kPChunks; ++c) {
-                    if (!mbar_wait(&ms.p_part[i][c], pv_done[i] & 1u, abort_flag)) return false;
-                    tc_fence_after_sync();
-#pragma unroll
-                    for (int kk = 0; kk < 8 / kPChunks; ++kk) {
-                        const int k = c * (8 / kPChunks) + kk;
-                        mma_ts_lo<kHi>(tmem + C::o_col(i), tmem + C::s_col(i) + k * 8, va + ((k * 2048) >> 4), idesc_o,
-                                       (k > 0 || acc) ? 1u : 0u);
-                    }
-                }
-                ++pv_done[i];
+                for (int k = 0; k < 8; ++k)
+                    mma_ts_lo<kHi>(tmem + C::o_col(i), tmem + C::s_col(i) + k * 8, va + ((k * 2048) >> 4), idesc_o,
+                                   (k > 0 || acc) ? 1u : 0u);
+                ++pv_total[i];
+                ++pv_item[i];
                 return true;
             };
-            bool ok = mbar_wait(&ms.q_full, 0, abort_flag) && mbar_wait(&ms.k_full[0], 0, abort_flag);
-            tc_fence_after_sync();
-            if (ok) {
-                const uint32_t f = ms.ulist[0] >> 16;
-                if (f & 1u) issue_s(0, 0);
-                if (f & 4u) issue_s(1, 0);
-                mma_commit(&ms.k_empty[0]);
-            }
-            for (int u = 0; ok && u < nu; ++u) {
-                const int s = u % NS;
-                const uint32_t f = ms.ulist[u] >> 16;
-                const bool nxt = u + 1 < nu;
-                const int s1 = (u + 1) % NS;
-                const uint32_t f1 = nxt ? (ms.ulist[u + 1] >> 16) : 0u;
-                if (!mbar_wait(&ms.v_full[s], (uint32_t)(u / NS) & 1u, abort_flag)) {
+            uint32_t g = 0;   // global step of the item's first union entry
+            uint32_t nq = 0;  // items with work so far (Q loads, o_full commits)
+            bool ok = true;
+            for (uint32_t n = 0; ok; ++n) {
+                const int k = (int)(n & 1u);
+                const ItemSlot &sl = ms.slot[k];
+                if (!mbar_wait(&ms.item_ready[k], (n >> 1) & 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
-                if ((f & 1u) && !issue_pv(0, s)) {
-                    ok = false;
-                    break;
-                }
-                if (nxt) {
-                    // K arrives by TMA: the mbarrier alone orders it for the MMA
-                    if (!mbar_wait(&ms.k_full[s1], (uint32_t)((u + 1) / NS) & 1u, abort_flag)) {
-                        ok = false;
-                        break;
+                const int nu = sl.nu;
+                if (nu < 0) break;
+                if (nu > 0) {
+                    pv_item[0] = pv_item[1] = 0u;
+                    const int s0 = (int)(g % NS);
+                    ok = mbar_wait(&ms.q_full, nq & 1u, abort_flag) &&
+                         mbar_wait(&ms.k_full[s0], (g / NS) & 1u, abort_flag);
+                    tc_fence_after_sync();
+                    if (ok) {
+                        const uint32_t f = sl.ulist[0] >> 16;
+                        if (f & 1u) issue_s(0, s0);
+                        if (f & 4u) issue_s(1, s0);
+                        mma_commit(&ms.k_empty[s0]);
+                        if (nu == 1) mma_commit(&ms.q_empty);  // Q no longer read
                     }
-                    if (f1 & 1u) issue_s(0, s1);
+                    for (int u = 0; ok && u < nu; ++u) {
+                        const uint32_t gu = g + (uint32_t)u;
+                        const int s = (int)(gu % NS);
+                        const uint32_t f = sl.ulist[u] >> 16;
+                        const bool nxt = u + 1 < nu;
+                        const int s1 = (int)((gu + 1) % NS);
+                        const uint32_t f1 = nxt ? (sl.ulist[u + 1] >> 16) : 0u;
+                        if (!mbar_wait(&ms.v_full[s], (gu / NS) & 1u, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        if ((f & 1u) && !issue_pv(0, s)) {
+                            ok = false;
+                            break;
+                        }
+                        if (nxt) {
+                            // K arrives by TMA: the mbarrier alone orders it for the MMA
+                            if (!mbar_wait(&ms.k_full[s1], ((gu + 1) / NS) & 1u, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            if (f1 & 1u) issue_s(0, s1);
+                        }
+                        if ((f & 4u) && !issue_pv(1, s)) {
+                            ok = false;
+                            break;
+                        }
+                        mma_commit(&ms.v_empty[s]);
+                        if (nxt) {
+                            if (f1 & 4u) issue_s(1, s1);
+                            mma_commit(&ms.k_empty[s1]);
+                            if (u + 2 == nu) mma_commit(&ms.q_empty);  // the item's last S is issued
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(&ms.o_full);
+                    g += (uint32_t)nu;
+                    ++nq;
                 }
-                if ((f & 4u) && !issue_pv(1, s)) {
-                    ok = false;
-                    break;
-                }
-                mma_commit(&ms.v_empty[s]);
-                if (nxt) {
-                    if (f1 & 4u) issue_s(1, s1);
-                    mma_commit(&ms.k_empty[s1]);
-                }
+                mbar_arrive(&ms.item_free[k]);
             }
-            if (ok)
-                mma_commit(&ms.o_full);
-            else
-                record_failure(ms, p.status);
+            if (!ok) record_failure(ms, p.status);
             mma_commit(&ms.drain);  // every MMA issued above completes before TMEM is freed
             drain_wait(&ms.drain, 0);
         }
@@ -557,28 +711,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         regs_increase<kRegsSoftmax>();
         const int i = warp / 4;
         const int t = threadIdx.x % 128;
-        const bool valid = i == 0 || has1;
-        const int q = (qb0 + i) * kBlock + t;
         const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
         const uint32_t s_addr = tmem + lane_base + C::s_col(i);
         const uint32_t o_addr = tmem + lane_base + C::o_col(i);
         const uint32_t present = i ? 4u : 1u, fullbit = i ? 8u : 2u;
-        ScoreLog2<SCORE> score;
-        score.init(p, h);
-        int doc_q = 0;
-        if constexpr (DOC) {
-            if (valid) doc_q = __ldg(p.mask.doc_ids + (int64_t)b * p.mask.doc_len + q);
-        }
-        float m_run = -INFINITY, l_run = 0.f;
-        uint32_t cnt = 0;
+        uint32_t cnt_total = 0;  // S_i tiles consumed over all items (s_full parity)
+        uint32_t g = 0;          // global step of the item's first union entry
+        uint32_t nq = 0;         // items with work so far (o_full parity)
         bool ok = true;
-        if (valid) {
+        for (uint32_t n = 0; ok; ++n) {
+          const int k = (int)(n & 1u);
+          const ItemSlot &sl = ms.slot[k];
+          if (!warp_wait(&ms.item_ready[k], (n >> 1) & 1u, abort_flag)) {
+              ok = false;
+              break;
+          }
+          const int nu = sl.nu;
+          if (nu < 0) break;
+          const int b = sl.b, h = sl.h;
+          const bool valid = i == 0 || sl.has1;
+          const int q = (sl.qb0 + i) * kBlock + t;
+          const int64_t bh = (int64_t)b * p.H + h;
+          ScoreLog2<SCORE> score;
+          score.init(p, h);
+          int doc_q = 0;
+          if constexpr (DOC) {
+              if (valid) doc_q = __ldg(p.mask.doc_ids + (int64_t)b * p.mask.doc_len + q);
+          }
+          float m_run = -INFINITY, l_run = 0.f;
+          uint32_t cnt = 0;  // tiles of this item
+          if (valid) {
             for (int u = 0; u < nu; ++u) {
-                const uint32_t e = ms.ulist[u];
+                const uint32_t e = sl.ulist[u];
                 const uint32_t f = e >> 16;
                 if (!(f & present)) continue;
                 const int kv0 = (int)(e & 0xFFFFu) * kBlock;
-                if (!warp_wait(&ms.s_full[i], cnt & 1u, abort_flag)) {
+                if (!warp_wait(&ms.s_full[i], cnt_total & 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -594,8 +762,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 if (!(f & fullbit)) {
                     if constexpr (DOC) {
-                        const int stage = u % NS;
-                        if (!warp_wait(&ms.v_full[stage], (uint32_t)(u / NS) & 1u, abort_flag)) {
+                        const uint32_t gu = g + (uint32_t)u;
+                        const int stage = (int)(gu % NS);
+                        if (!warp_wait(&ms.v_full[stage], (gu / NS) & 1u, abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -649,30 +818,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 uint64_t rs2[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) rs2[k] = 0ull;
-                // P in kPChunks column chunks: the MMA warp starts the PV of the
-                // first chunks while the later ones are computed
+                for (int k4 = 0; k4 < 4; ++k4) rs2[k4] = 0ull;
 #pragma unroll
-                for (int chunk = 0; chunk < kPChunks; ++chunk) {
+                for (int gq = 0; gq < 4; ++gq) {
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int g = chunk * (4 / kPChunks); g < (chunk + 1) * (4 / kPChunks); ++g) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int t2 = 0; t2 < 16; ++t2) {
-                            const int j = 16 * g + t2;
-                            float d0, d1;
-                            f2_unpack(f2_add(x2[j], sub2), d0, d1);
-                            const float p0 = ex2_approx(d0);
-                            const float p1 = ex2_approx(d1);
-                            rs2[j & 3] = f2_add(rs2[j & 3], f2_pack(p0, p1));
-                            pk[t2] = pack_bf16x2(p0, p1);
-                        }
-                        tmem_st16(s_addr + 16 * g, pk);
+                    for (int t2 = 0; t2 < 16; ++t2) {
+                        const int j = 16 * gq + t2;
+                        float d0, d1;
+                        f2_unpack(f2_add(x2[j], sub2), d0, d1);
+                        const float p0 = ex2_approx(d0);
+                        const float p1 = ex2_approx(d1);
+                        rs2[j & 3] = f2_add(rs2[j & 3], f2_pack(p0, p1));
+                        pk[t2] = pack_bf16x2(p0, p1);
                     }
-                    tmem_wait_st();
-                    tc_fence_before_sync();
-                    mbar_arrive(&ms.p_part[i][chunk]);
+                    tmem_st16(s_addr + 16 * gq, pk);
                 }
+                tmem_wait_st();
+                tc_fence_before_sync();
+                mbar_arrive(&ms.p_full[i]);
                 float rsum;
                 {
                     float a0, a1;
@@ -681,17 +845,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 l_run = fmaf(l_run, alpha, rsum);
                 ++cnt;
+                ++cnt_total;
             }
             // ---------------------------------------------------- epilogue
             bool have = ok && cnt > 0;
-            if (have && !warp_wait(&ms.o_full, 0, abort_flag)) {
+            if (have && !warp_wait(&ms.o_full, nq & 1u, abort_flag)) {
                 have = false;
                 ok = false;
             }
             if (!ok) record_failure(ms, p.status);
             if (ok) {
                 tc_fence_after_sync();
-                const int64_t orow = ((int64_t)bh * p.q_len + q);
+                const int64_t orow = bh * p.q_len + q;
                 uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D);
                 const bool live = have && l_run > 0.f;
                 const float inv = live ? 1.f / l_run : 0.f;
@@ -714,11 +879,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 p.lse[orow] = live ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
             }
+          }
+          if (nu > 0) {
+              g += (uint32_t)nu;
+              ++nq;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ms.item_free[k]);
         }
+        if (!ok) record_failure(ms, p.status);
     }
 
     // ---------------------------------------------------------- teardown
-    if (threadIdx.x == 0) drain_wait(&ms.q_full, 0);  // the Q copies issued in the prologue have landed
     tc_fence_before_sync();
     __syncthreads();
     if (warp == kMmaWarp) {

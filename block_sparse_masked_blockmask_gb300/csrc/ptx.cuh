@@ -96,6 +96,45 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Prefetch the 4-D tile at the given coordinates into L2 (no shared-memory
+// destination, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap *map, int32_t c0, int32_t c1, int32_t c2,
+                                                   int32_t c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+// ------------------------------------------------------ cluster launch control
+// Ask the hardware to cancel one CTA of this grid that has not started yet and
+// hand its index to the calling CTA.  The 16-byte response lands at `resp`
+// (16-byte aligned shared memory) and completes as 16 transaction bytes on
+// `bar` (the caller arms the barrier with an expect_tx of 16).
+__device__ __forceinline__ void clc_try_cancel(void *resp, uint64_t *bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+            smem_u32(resp)),
+        "r"(smem_u32(bar))
+        : "memory");
+}
+
+// The x index of the CTA a completed response cancelled, or -1 when none was
+// (every CTA of the grid has started or been taken).
+__device__ __forceinline__ int clc_cancelled_x(const void *resp) {
+    uint32_t ok, x;
+    asm volatile(
+        "{\n\t.reg .pred c;\n\t.reg .b128 r;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 c, r;\n\t"
+        "selp.u32 %0, 1, 0, c;\n\t"
+        "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(ok), "=r"(x)
+        : "r"(smem_u32(resp))
+        : "memory");
+    return ok ? (int)x : -1;
+}
+
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
