@@ -355,33 +355,37 @@ __device__ __forceinline__ void decode_item(const Bf16Params &p, int item, int &
 // Build an item's union list into `sl` with the 32 lanes of one warp:
 // mark every kv tile of both q blocks (bounds-checked: a malformed BlockMask
 // cannot write outside the flag array), then compact the marked tiles in
-// descending kv order.
+// descending kv order.  The index loads of a chunk are all issued before any
+// of them is used, so the build costs a couple of memory latencies rather than
+// one per 32 entries.
 __device__ __forceinline__ void build_item(const Bf16Params &p, AttnMisc &ms, ItemSlot &sl, int item, int lane) {
     int b, h, qb0, has1;
     decode_item(p, item, b, h, qb0, has1);
     const int nkvb = p.nkvb;
-    for (int j = lane; j < nkvb; j += 32) ms.flags[j] = 0u;
-    __syncwarp();
     const int64_t row0 = ((int64_t)b * p.H + h) * p.nqb + qb0;
     const int32_t *pidx = p.kv_idx + row0 * nkvb, *fidx = p.full_idx + row0 * nkvb;
-    const int np0 = min(max(p.kv_num[row0], 0), nkvb), nf0 = min(max(p.full_num[row0], 0), nkvb);
-    const int np1 = has1 ? min(max(p.kv_num[row0 + 1], 0), nkvb) : 0;
-    const int nf1 = has1 ? min(max(p.full_num[row0 + 1], 0), nkvb) : 0;
-    for (int x = lane; x < np0; x += 32) {
-        const int j = pidx[x];
-        if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 1u);
-    }
-    for (int x = lane; x < nf0; x += 32) {
-        const int j = fidx[x];
-        if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 3u);
-    }
-    for (int x = lane; x < np1; x += 32) {
-        const int j = pidx[nkvb + x];
-        if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 4u);
-    }
-    for (int x = lane; x < nf1; x += 32) {
-        const int j = fidx[nkvb + x];
-        if ((unsigned)j < (unsigned)nkvb) atomicOr(&ms.flags[j], 12u);
+    const int np0 = min(max(__ldg(p.kv_num + row0), 0), nkvb), nf0 = min(max(__ldg(p.full_num + row0), 0), nkvb);
+    const int np1 = has1 ? min(max(__ldg(p.kv_num + row0 + 1), 0), nkvb) : 0;
+    const int nf1 = has1 ? min(max(__ldg(p.full_num + row0 + 1), 0), nkvb) : 0;
+    for (int j = lane; j < nkvb; j += 32) ms.flags[j] = 0u;
+    __syncwarp();
+    constexpr int kUnroll = 4;
+    for (int base = 0; base < nkvb; base += 32 * kUnroll) {
+        int jj[4][kUnroll];
+#pragma unroll
+        for (int r = 0; r < kUnroll; ++r) {
+            const int x = base + 32 * r + lane;
+            jj[0][r] = x < np0 ? __ldg(pidx + x) : -1;
+            jj[1][r] = x < nf0 ? __ldg(fidx + x) : -1;
+            jj[2][r] = x < np1 ? __ldg(pidx + nkvb + x) : -1;
+            jj[3][r] = x < nf1 ? __ldg(fidx + nkvb + x) : -1;
+        }
+        constexpr uint32_t kBits[4] = {1u, 3u, 4u, 12u};  // present / full, tile 0 then tile 1
+#pragma unroll
+        for (int l = 0; l < 4; ++l)
+#pragma unroll
+            for (int r = 0; r < kUnroll; ++r)
+                if ((unsigned)jj[l][r] < (unsigned)nkvb) atomicOr(&ms.flags[jj[l][r]], kBits[l]);
     }
     __syncwarp();
     int count = 0;
