@@ -56,6 +56,8 @@ cudaError_t launch_attn_bf16(const AttnProblem &p, cudaStream_t stream) {
     kp.nqb = p.nqb;
     kp.nkvb = p.nkvb;
     kp.npairs = (p.nqb + 1) / 2;
+    kp.bh_begin = p.bh_begin;
+    kp.nbh = p.bh_count;
     kp.kv_num = p.kv_num;
     kp.kv_idx = p.kv_idx;
     kp.full_num = p.full_num;

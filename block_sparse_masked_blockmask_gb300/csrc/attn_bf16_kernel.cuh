@@ -83,6 +83,7 @@ static_assert(2 * kRegsSoftmax + kRegsControl == 3 * kRegsAtLaunch, "register sp
 
 struct Bf16Params {
     int B, H, q_len, kv_len, nqb, nkvb, npairs;
+    int bh_begin, nbh;  // the (b, h) pairs b * H + h in [bh_begin, bh_begin + nbh) are computed
     const int32_t *kv_num, *kv_idx, *full_num, *full_idx;
     MaskDesc mask;
     float scale, score_param;
@@ -339,13 +340,13 @@ __device__ __forceinline__ void apply_document_mask(int q, int kv0, int doc_q, c
 // first, the group's heads innermost, so the heaviest items of each group come
 // first and the last items of the grid are light.
 __device__ __forceinline__ void decode_item(const Bf16Params &p, int item, int &b, int &h, int &qb0, int &has1) {
-    const int nbh = p.B * p.H;
+    const int nbh = p.nbh;
     const int group_items = kHeadGroup * p.npairs;
     const int g0 = (item / group_items) * kHeadGroup;
     const int gsize = min(kHeadGroup, nbh - g0);
     const int r = item - (item / group_items) * group_items;
     const int pair = p.npairs - 1 - r / gsize;
-    const int bh = g0 + r % gsize;
+    const int bh = p.bh_begin + g0 + r % gsize;
     b = bh / p.H;
     h = bh % p.H;
     qb0 = 2 * pair;

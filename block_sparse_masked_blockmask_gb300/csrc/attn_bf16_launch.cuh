@@ -19,7 +19,7 @@ cudaError_t launch_bf16_kernel(const CUtensorMap &tq, const CUtensorMap &tk, con
     if (attr.numRegs != (int)kRegsAtLaunch) return cudaErrorInvalidDeviceFunction;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)((int64_t)kp.B * kp.H * kp.npairs);
+    const unsigned grid = (unsigned)((int64_t)kp.nbh * kp.npairs);
     kernel<<<grid, kAttnThreads, C::kSmemBytes, stream>>>(tq, tk, tv, kp);
     return cudaGetLastError();
 }

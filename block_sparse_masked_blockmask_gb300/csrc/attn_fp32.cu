@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(Fp32Cfg<D>::kThreads) attn_fp32_kernel(AttnPro
     float *ks = reinterpret_cast<float *>(smem4);
     float *vs = ks + kBlock * D;
 
-    const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int qb = blockIdx.x, bh = p.bh_begin + (int)blockIdx.y, h = bh % p.H, b = bh / p.H;
     const int row = threadIdx.x / C::kTpr, part = threadIdx.x % C::kTpr;
     const int q = qb * kBlock + row;
     const int64_t bhq = ((int64_t)b * p.H + h) * p.nqb + qb;
@@ -126,8 +126,16 @@ cudaError_t launch_d(const AttnProblem &p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(attn_fp32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)C::kSmem);
     if (e != cudaSuccess) return e;
-    attn_fp32_kernel<D><<<dim3(p.nqb, p.H, p.B), C::kThreads, C::kSmem, stream>>>(p);
-    return cudaGetLastError();
+    // grid.y holds at most 65535 (b, h) pairs per launch
+    for (int begin = 0; begin < p.bh_count; begin += 65535) {
+        AttnProblem part = p;
+        part.bh_begin = p.bh_begin + begin;
+        part.bh_count = p.bh_count - begin < 65535 ? p.bh_count - begin : 65535;
+        attn_fp32_kernel<D><<<dim3(p.nqb, part.bh_count), C::kThreads, C::kSmem, stream>>>(part);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace

@@ -67,6 +67,7 @@ __host__ __device__ __forceinline__ bool mask_row_interval(const MaskDesc &m, in
 // Problem description handed from the C-ABI layer to the attention launchers.
 struct AttnProblem {
     int B, H, q_len, kv_len, D, nqb, nkvb;
+    int bh_begin, bh_count;                          // the (b, h) pairs b * H + h in [bh_begin, +bh_count) are computed
     int64_t q_stride[4], k_stride[4], v_stride[4];  // elements
     const void *q, *k, *v;
     void *out;                                       // contiguous [B,H,q_len,D]

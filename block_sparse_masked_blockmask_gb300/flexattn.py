@@ -38,8 +38,8 @@ FLEX_DTYPE_BF16 = 0
 FLEX_DTYPE_FP32 = 1
 
 EXPORTED = ("flex_block_mask_sizes", "flex_block_mask_create", "flex_attention_fwd",
-            "flex_attention_fwd_noalloc", "flex_device_status", "flex_selftest_wait_timeout",
-            "flex_status_string")
+            "flex_attention_fwd_noalloc", "flex_attention_fwd_host", "flex_device_status",
+            "flex_selftest_wait_timeout", "flex_status_string")
 
 
 class FlexError(RuntimeError):
@@ -63,6 +63,13 @@ class flex_block_mask(ctypes.Structure):
 class flex_tensor(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class flex_device_buffers(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("lse", ctypes.c_void_p), ("doc_ids", ctypes.c_void_p), ("kv_num_blocks", ctypes.c_void_p),
+                ("kv_indices", ctypes.c_void_p), ("full_kv_num_blocks", ctypes.c_void_p),
+                ("full_kv_indices", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -97,6 +104,10 @@ def load_library():
                                                        ctypes.c_float, ctypes.c_float, vp, vp, vp,
                                                        ctypes.POINTER(ctypes.POINTER(ctypes.c_int))]
             lib.flex_attention_fwd_noalloc.restype = ctypes.c_int
+            lib.flex_attention_fwd_host.argtypes = [tp, tp, tp, i32, ctypes.POINTER(flex_mask_params), i32,
+                                                    ctypes.c_float, ctypes.c_float, vp, vp,
+                                                    ctypes.POINTER(flex_device_buffers), i32, vp]
+            lib.flex_attention_fwd_host.restype = ctypes.c_int
             lib.flex_device_status.argtypes = [vp]
             lib.flex_device_status.restype = ctypes.c_int
             lib.flex_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
@@ -236,6 +247,67 @@ def flex_attention_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor
     if rc != FLEX_OK:
         raise FlexError(rc, "flex_attention_fwd_noalloc")
     return ctypes.cast(status, ctypes.c_void_p).value
+
+
+class DeviceBuffers:
+    """Device working memory of flex_attention_fwd_host, allocated (and owned) through torch."""
+
+    def __init__(self, B: int, H: int, q_len: int, kv_len: int, D: int, dtype: torch.dtype,
+                 document: bool = False, device=None):
+        device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        self.q = torch.empty((B, H, q_len, D), dtype=dtype, device=device)
+        self.k = torch.empty((B, H, kv_len, D), dtype=dtype, device=device)
+        self.v = torch.empty((B, H, kv_len, D), dtype=dtype, device=device)
+        self.out = torch.empty((B, H, q_len, D), dtype=dtype, device=device)
+        self.lse = torch.empty((B, H, q_len), dtype=torch.float32, device=device)
+        self.doc_ids = torch.empty((B, q_len), dtype=torch.int32, device=device) if document else None
+        nqb, nkvb = q_len // 128, kv_len // 128
+        self.kv_num_blocks = torch.empty((B, H, nqb), dtype=torch.int32, device=device)
+        self.kv_indices = torch.empty((B, H, nqb, nkvb), dtype=torch.int32, device=device)
+        self.full_kv_num_blocks = torch.empty((B, H, nqb), dtype=torch.int32, device=device)
+        self.full_kv_indices = torch.empty((B, H, nqb, nkvb), dtype=torch.int32, device=device)
+        self.device = device
+
+    def struct(self) -> flex_device_buffers:
+        d = flex_device_buffers()
+        for name in ("q", "k", "v", "out", "lse", "kv_num_blocks", "kv_indices", "full_kv_num_blocks",
+                     "full_kv_indices"):
+            setattr(d, name, getattr(self, name).data_ptr())
+        d.doc_ids = self.doc_ids.data_ptr() if self.doc_ids is not None else None
+        return d
+
+
+def flex_attention_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, buffers: DeviceBuffers,
+                            mask_kind: int, out: torch.Tensor, lse: torch.Tensor, window: int = 0, prefix: int = 0,
+                            doc_ids: torch.Tensor | None = None, score_kind: int = FLEX_SCORE_IDENTITY,
+                            score_param: float = 0.0, scale: float | None = None, chunks: int = 8,
+                            stream=None) -> None:
+    """BlockMask build + attention from host q, k, v into host out, lse (see include/flexattn.h).
+
+    q, k, v, out, lse (and doc_ids) are contiguous CPU tensors, pinned for the
+    copies to overlap; `buffers` is the device working memory.  Asynchronous on
+    `stream`: the host outputs are valid once the stream has passed the call.
+    """
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    for t in (q, k, v, out, lse) + ((doc_ids,) if doc_ids is not None else ()):
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError("host tensors must be contiguous CPU tensors")
+    if lse.dtype != torch.float32 or out.dtype != q.dtype:
+        raise ValueError("out has the inputs' dtype, lse is float32")
+    if doc_ids is not None and doc_ids.dtype != torch.int32:
+        raise ValueError("doc_ids must be int32")
+    tq, tk, tv = _tensor(q), _tensor(k), _tensor(v)
+    params = flex_mask_params(window, prefix, doc_ids.data_ptr() if doc_ids is not None else None)
+    dev = buffers.struct()
+    with torch.cuda.device(buffers.device):
+        rc = load_library().flex_attention_fwd_host(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), mask_kind,
+                                                    ctypes.byref(params), score_kind, float(score_param),
+                                                    float(scale), ctypes.c_void_p(out.data_ptr()),
+                                                    ctypes.c_void_p(lse.data_ptr()), ctypes.byref(dev), int(chunks),
+                                                    _stream_handle(stream, buffers.device))
+    if rc != FLEX_OK:
+        raise FlexError(rc, "flex_attention_fwd_host")
 
 
 def flex_selftest_wait_timeout(limit_ms: int = 50, stream=None, device=None) -> None:

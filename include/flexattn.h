@@ -209,6 +209,57 @@ FLEX_API int flex_attention_fwd_noalloc(const flex_tensor *q, const flex_tensor 
                                         const int **device_status);
 
 /*
+ * Device buffers that flex_attention_fwd_host works in.  The caller allocates
+ * and owns them (16-byte aligned, contiguous) and must not touch them until
+ * `stream` has passed the call:
+ *   q, k, v     [B, H, S, D] in the inputs' dtype (S = q_len for q, kv_len for k, v)
+ *   out         [B, H, q_len, D] in the inputs' dtype;  lse [B, H, q_len] float32
+ *   doc_ids     [B, q_len] int32 (document masks; may be NULL otherwise)
+ *   kv_num_blocks ... full_kv_indices: the BlockMask index buffers, sized as
+ *               flex_block_mask_sizes gives.
+ */
+typedef struct {
+    void *q, *k, *v, *out;
+    float *lse;
+    int32_t *doc_ids;
+    int32_t *kv_num_blocks, *kv_indices, *full_kv_num_blocks, *full_kv_indices;
+} flex_device_buffers;
+
+/*
+ * flex_block_mask_create followed by flex_attention_fwd for inputs and outputs
+ * in host memory, with the copies overlapped with the work.  (No counterpart
+ * in the pages: it exists for callers whose tensors live on the host.)
+ *   q, k, v   host tensors, contiguous [B, H, S, D], dtype and shapes as for
+ *             flex_attention_fwd; page-locked (pinned) memory lets the copies
+ *             run asynchronously and overlap.
+ *   mask_kind, params  as for flex_block_mask_create, except that
+ *             params->doc_ids (document masks) is a host array [B, q_len].
+ *   score_kind, score_param, scale  as for flex_attention_fwd.
+ *   out, lse  host, contiguous [B, H, q_len, D] (inputs' dtype) and
+ *             [B, H, q_len] float32; written by the time `stream` has passed
+ *             the call.
+ *   dev       the device buffers described above.
+ *   chunks    1..64: the (b, h) pairs are split into this many contiguous
+ *             ranges.  The inputs of all ranges are copied in back to back on
+ *             a library stream; the attention of a range starts on `stream`
+ *             as soon as its inputs are in, and its out and lse are copied back
+ *             on a second library stream while the next range computes.  The
+ *             BlockMask of all heads is built once, on `stream`.
+ * Both library streams are created once per device, wait for `stream` at the
+ * start of the call, and `stream` waits for them at its end, so the call is
+ * ordered on `stream` like any other.  Calls from several host threads on one
+ * device enqueue one at a time.  Results are those of flex_attention_fwd.
+ * Errors: FLEX_ERR_INVALID_ARG (a NULL or non-contiguous tensor, chunks out of
+ * range, a missing parameter or buffer), and those of flex_block_mask_create
+ * and flex_attention_fwd, all detected before anything is enqueued;
+ * FLEX_ERR_CUDA if enqueueing fails.
+ */
+FLEX_API int flex_attention_fwd_host(const flex_tensor *q, const flex_tensor *k, const flex_tensor *v,
+                                     int32_t mask_kind, const flex_mask_params *params, int32_t score_kind,
+                                     float score_param, float scale, void *out, float *lse,
+                                     const flex_device_buffers *dev, int32_t chunks, void *stream);
+
+/*
  * Synchronises `stream`, then returns and clears the device status word of
  * the current device: FLEX_OK, or FLEX_ERR_DEVICE_TIMEOUT if a kernel gave up
  * on a wait since the last call.  FLEX_ERR_CUDA if the synchronisation failed.

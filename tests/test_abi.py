@@ -138,3 +138,38 @@ def test_product_path_has_no_oracle_dependency():
                 text = open(os.path.join(root, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "liboracle" not in text, f
+
+
+def test_host_entry_point_rejects_bad_arguments(lib):
+    # every case fails its checks before any CUDA call
+    bf = fa.FLEX_DTYPE_BF16
+    dev = fa.flex_device_buffers()
+    for name, addr in (("q", 0x10000), ("k", 0x20000), ("v", 0x30000), ("out", 0x40000), ("lse", 0x50000),
+                       ("kv_num_blocks", 0x60000), ("kv_indices", 0x70000), ("full_kv_num_blocks", 0x80000),
+                       ("full_kv_indices", 0x90000)):
+        setattr(dev, name, addr)
+
+    def call(q=None, k=None, v=None, kind=fa.FLEX_MASK_CAUSAL, params=None, score=fa.FLEX_SCORE_IDENTITY,
+             out=0x100000, lse=0x200000, devbuf=dev, chunks=4):
+        q = q or _tensor(bf, [1, 2, 256, 64])
+        k = k or _tensor(bf, [1, 2, 256, 64])
+        v = v or _tensor(bf, [1, 2, 256, 64])
+        return lib.flex_attention_fwd_host(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), kind,
+                                           ctypes.byref(params) if params is not None else None, score, 0.0, 0.125,
+                                           ctypes.c_void_p(out), ctypes.c_void_p(lse),
+                                           ctypes.byref(devbuf) if devbuf is not None else None, chunks, None)
+
+    assert call(chunks=0) == fa.FLEX_ERR_INVALID_ARG
+    assert call(chunks=65) == fa.FLEX_ERR_INVALID_ARG
+    assert call(devbuf=None) == fa.FLEX_ERR_INVALID_ARG
+    assert call(out=0) == fa.FLEX_ERR_INVALID_ARG
+    # host tensors must be contiguous
+    assert call(v=_tensor(bf, [1, 2, 256, 64], stride=[65536, 32768, 64, 1])) == fa.FLEX_ERR_INVALID_ARG
+    assert call(kind=9) == fa.FLEX_ERR_INVALID_ARG
+    assert call(kind=fa.FLEX_MASK_SLIDING_WINDOW) == fa.FLEX_ERR_INVALID_ARG  # needs params
+    assert call(kind=fa.FLEX_MASK_DOCUMENT, params=fa.flex_mask_params(0, 0, 0x1000)) == fa.FLEX_ERR_INVALID_ARG
+    assert call(q=_tensor(bf, [1, 2, 200, 64])) == fa.FLEX_ERR_SHAPE
+    assert call(score=7) == fa.FLEX_ERR_INVALID_ARG
+    unaligned = fa.flex_device_buffers.from_buffer_copy(dev)
+    unaligned.out = 0x40008
+    assert call(devbuf=unaligned) == fa.FLEX_ERR_ALIGNMENT
