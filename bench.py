@@ -221,7 +221,7 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=0.0,
                     help="oracle sample budget per reference step (0: fit the run in ~150 s)")
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--e2e-chunks", type=int, default=8,
+    ap.add_argument("--e2e-chunks", type=int, default=16,
                     help="(b, h) chunks of flex_attention_fwd_host, whose copies overlap the work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling a smaller case)")
