@@ -210,6 +210,21 @@ def config_dict(w: W.Workload) -> dict:
     return c
 
 
+def max_over_ranks(ms: float, dist=None, device="cuda") -> float:
+    """The largest of the ranks' times (every rank gets it); `ms` itself on one process."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(flops_per_rank: float, ms: float, world: int) -> float:
+    """TFLOP/s of all ranks together: each rank did flops_per_rank (weak scaling) in at most ms."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -306,13 +321,9 @@ def run_ours(args, w: W.Workload) -> None:
         raise SystemExit("device status reported a timeout during the timed region")
     step_ms = [a.elapsed_time(c) for a, _, c in ev]
     attn_ms = [b.elapsed_time(c) for _, b, c in ev]
-    total_ms = float(np.sum(step_ms))
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(np.sum(step_ms)), dist)
     ms_per_step = total_ms / args.steps
-    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_rate(flops, ms_per_step, world)
 
     # end to end through the public API: host inputs in, host outputs back, every step
     hq, hk, hv = (x.cpu().pin_memory() for x in (dq, dk, dv))
@@ -336,17 +347,19 @@ def run_ours(args, w: W.Workload) -> None:
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(args.e2e_steps):
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b) / args.e2e_steps
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / args.e2e_steps, dist)
         # the host result is the device path's result
         if not (torch.equal(hout[0, 0].float(), out[0, 0].float().cpu()) and torch.equal(hlse[-1, -1], lse[-1, -1].cpu())):
             raise SystemExit("flex_attention_fwd_host result differs from flex_attention_fwd")
-        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        e2e = {"value": whole_job_rate(flops, e2e_ms, world), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "api": "flex_attention_fwd_host",
                "chunks": args.e2e_chunks}
 
