@@ -24,6 +24,14 @@
  *       (OUTPUT_LOGSUMEXP in the same op's options); a row with no
  *       unmasked score gives out = 0 and lse = -inf (the guard that the
  *       ROWS_GUARANTEED_SAFE option lets a caller skip).
+ *   kernel options       the same op's kernel_options, read plainly:
+ *       OUTPUT_MAX   a third output, the row maximum of the masked,
+ *                    modified scores (natural units like lse; -inf for a
+ *                    row with no unmasked score);
+ *       PRESCALE_QK  Q is multiplied by scale before QK^T: the product
+ *                    scale * q is rounded once to the inputs' storage type
+ *                    (bfloat16 or float32, ties to even) and the scores are
+ *                    score_mod(q~ . k) with no further scale.
  *   block mask           -> kv_num_blocks, kv_indices, full_kv_num_blocks,
  *       full_kv_indices   (the BlockMask tuple passed to the same op): each
  *       BLOCK x BLOCK tile of the dense mask is full (all true), partial
@@ -111,6 +119,35 @@ static int or_mask_ok(int kind)
     return kind >= OR_MASK_CAUSAL && kind <= OR_MASK_ALL;
 }
 
+#define OR_PRESCALE_NONE 0
+#define OR_PRESCALE_BF16 1
+#define OR_PRESCALE_F32 2
+
+/*
+ * x rounded to bfloat16 (8 significant bits, float32's exponent range,
+ * subnormal quantum 2^-133), ties to even, overflow to +-inf.  One rounding
+ * from the exact double value.
+ */
+static double or_round_bf16(double x)
+{
+    if (x == 0.0 || !isfinite(x)) return x;
+    int e;
+    (void)frexp(x, &e);              /* 2^(e-1) <= |x| < 2^e */
+    int quantum = e - 8;
+    if (quantum < -133) quantum = -133;
+    const double r = ldexp(nearbyint(ldexp(x, -quantum)), quantum);  /* default mode: ties to even */
+    const double bf16_max = ldexp(255.0, 120);                       /* (2 - 2^-7) 2^127 */
+    return fabs(r) > bf16_max ? copysign(INFINITY, x) : r;
+}
+
+/* q~ = scale * q rounded to the storage type (PRESCALE_QK) */
+static double or_prescale(int prescale, double scale, float q)
+{
+    const double x = scale * (double)q;  /* exact: 24 x 24 bits fit a double */
+    if (prescale == OR_PRESCALE_BF16) return or_round_bf16(x);
+    return (double)(float)x;
+}
+
 /*
  * Dense mask evaluated tile by tile; one BLOCK-row band of the mask is
  * materialised at a time to bound memory.  Output layouts:
@@ -180,17 +217,22 @@ int oracle_block_mask(int kind, int window, int prefix, const int32_t *doc,
 /*
  * One output row (b, h, i):
  *   S[j] = mask_mod(b,h,i,j) ? score_mod(scale * sum_d q[i,d] k[j,d]) : -inf
- *   no unmasked j          -> out = 0, lse = -inf
+ *          (PRESCALE_QK: score_mod(sum_d q~[i,d] k[j,d]), q~ = round(scale q))
+ *   no unmasked j          -> out = 0, lse = -inf, row max = -inf
  *   else  mx = max_j S[j], Z = sum_j exp(S[j] - mx), lse = mx + ln Z,
- *         out[d] = sum_j exp(S[j] - lse) v[j,d]
+ *         out[d] = sum_j exp(S[j] - lse) v[j,d], row max = mx
  */
 static void or_row(const float *q, const float *k, const float *v,
                    int64_t H, int64_t s_kv, int64_t D, const or_mask *m,
-                   int score_kind, double score_param, double scale,
+                   int score_kind, double score_param, double scale, int prescale,
                    int64_t b, int64_t h, int64_t i,
-                   double *srow, unsigned char *mrow, double *out, double *lse)
+                   double *srow, unsigned char *mrow, double *qrow,
+                   double *out, double *lse, double *row_max)
 {
     const float *qi = q + i * D;
+    for (int64_t d = 0; d < D; ++d)
+        qrow[d] = prescale ? or_prescale(prescale, scale, qi[d]) : (double)qi[d];
+    const double post = prescale ? 1.0 : scale;  /* the scale still to apply to q.k */
     int any = 0;
     for (int64_t j = 0; j < s_kv; ++j) {
         mrow[j] = (unsigned char)or_mask_mod(m, b, h, i, j);
@@ -198,19 +240,21 @@ static void or_row(const float *q, const float *k, const float *v,
         double dot = 0.0;
         const float *kj = k + j * D;
         for (int64_t d = 0; d < D; ++d)
-            dot += (double)qi[d] * (double)kj[d];
-        double t = or_score_mod(score_kind, score_param, scale * dot, h, H, i, j);
+            dot += qrow[d] * (double)kj[d];
+        double t = or_score_mod(score_kind, score_param, post * dot, h, H, i, j);
         srow[j] = mrow[j] ? t : -INFINITY;
     }
     if (!any) {
         for (int64_t d = 0; d < D; ++d)
             out[d] = 0.0;
         *lse = -INFINITY;
+        if (row_max) *row_max = -INFINITY;
         return;
     }
     double mx = -INFINITY;
     for (int64_t j = 0; j < s_kv; ++j)
         if (mrow[j] && srow[j] > mx) mx = srow[j];
+    if (row_max) *row_max = mx;
     double Z = 0.0;
     for (int64_t j = 0; j < s_kv; ++j)
         if (mrow[j]) Z += exp(srow[j] - mx);
@@ -229,19 +273,23 @@ static void or_row(const float *q, const float *k, const float *v,
 
 /*
  * q: [B, H, s_q, D], k, v: [B, H, s_kv, D], contiguous float32.
- * rows == NULL: every row; out [B, H, s_q, D], lse [B, H, s_q].
- * rows != NULL: nrows flat row ids ((b*H + h)*s_q + i); out [nrows, D], lse [nrows].
+ * rows == NULL: every row; out [B, H, s_q, D], lse and row_max [B, H, s_q].
+ * rows != NULL: nrows flat row ids ((b*H + h)*s_q + i); out [nrows, D],
+ * lse and row_max [nrows].  row_max may be NULL (OUTPUT_MAX off).
+ * prescale: OR_PRESCALE_NONE, or the storage type q~ is rounded to.
  */
-int oracle_attention(const float *q, const float *k, const float *v,
-                     int B, int H, int s_q, int s_kv, int D,
-                     int mask_kind, int window, int prefix, const int32_t *doc,
-                     int score_kind, double score_param, double scale,
-                     const int64_t *rows, int64_t nrows,
-                     double *out, double *lse)
+int oracle_attention_opts(const float *q, const float *k, const float *v,
+                          int B, int H, int s_q, int s_kv, int D,
+                          int mask_kind, int window, int prefix, const int32_t *doc,
+                          int score_kind, double score_param, double scale, int prescale,
+                          const int64_t *rows, int64_t nrows,
+                          double *out, double *lse, double *row_max)
 {
     if (!or_mask_ok(mask_kind) || B <= 0 || H <= 0 || s_q <= 0 || s_kv <= 0 || D <= 0)
         return OR_ERR_ARG;
     if (score_kind < OR_SCORE_IDENTITY || score_kind > OR_SCORE_ALIBI)
+        return OR_ERR_ARG;
+    if (prescale < OR_PRESCALE_NONE || prescale > OR_PRESCALE_F32)
         return OR_ERR_ARG;
     if (mask_kind == OR_MASK_DOCUMENT && (doc == NULL || s_q != s_kv))
         return OR_ERR_ARG;
@@ -254,8 +302,9 @@ int oracle_attention(const float *q, const float *k, const float *v,
 #pragma omp parallel
     {
         double *srow = (double *)malloc((size_t)s_kv * sizeof(double));
+        double *qrow = (double *)malloc((size_t)D * sizeof(double));
         unsigned char *mrow = (unsigned char *)malloc((size_t)s_kv);
-        if (!srow || !mrow) {
+        if (!srow || !mrow || !qrow) {
 #pragma omp atomic write
             err = OR_ERR_NOMEM;
         } else {
@@ -267,13 +316,34 @@ int oracle_attention(const float *q, const float *k, const float *v,
                 if (b >= B) continue;
                 or_row(q + bh * (int64_t)s_q * D, k + bh * (int64_t)s_kv * D,
                        v + bh * (int64_t)s_kv * D, H, s_kv, D, &m, score_kind,
-                       score_param, scale, b, h, i, srow, mrow, out + r * D, lse + r);
+                       score_param, scale, prescale, b, h, i, srow, mrow, qrow,
+                       out + r * D, lse + r, row_max ? row_max + r : NULL);
             }
         }
         free(srow);
+        free(qrow);
         free(mrow);
     }
     return err;
+}
+
+/* the default kernel options: no prescale, no row max */
+int oracle_attention(const float *q, const float *k, const float *v,
+                     int B, int H, int s_q, int s_kv, int D,
+                     int mask_kind, int window, int prefix, const int32_t *doc,
+                     int score_kind, double score_param, double scale,
+                     const int64_t *rows, int64_t nrows,
+                     double *out, double *lse)
+{
+    return oracle_attention_opts(q, k, v, B, H, s_q, s_kv, D, mask_kind, window, prefix, doc,
+                                 score_kind, score_param, scale, OR_PRESCALE_NONE, rows, nrows,
+                                 out, lse, NULL);
+}
+
+/* bfloat16 rounding, exposed so tests can check it against a library conversion */
+double oracle_round_bf16(double x)
+{
+    return or_round_bf16(x);
 }
 
 /* the single predicate, exposed so tests can check it against the pages' examples */

@@ -60,6 +60,11 @@ class Oracle:
         lib.oracle_attention.argtypes = [f32p, f32p, f32p, I, I, I, I, I, I, I, I, i32p,
                                          I, D, D, i64p, L, f64p, f64p]
         lib.oracle_attention.restype = I
+        lib.oracle_attention_opts.argtypes = [f32p, f32p, f32p, I, I, I, I, I, I, I, I, i32p,
+                                              I, D, D, I, i64p, L, f64p, f64p, f64p]
+        lib.oracle_attention_opts.restype = I
+        lib.oracle_round_bf16.argtypes = [D]
+        lib.oracle_round_bf16.restype = D
         lib.oracle_mask_value.argtypes = [I, I, I, i32p, L, L, L, L, L]
         lib.oracle_mask_value.restype = I
         lib.oracle_num_threads.argtypes = []
@@ -119,6 +124,45 @@ class Oracle:
             raise ValueError(f"oracle_attention failed with {rc}")
         return out, lse
 
+    PRESCALE = {None: 0, "bf16": 1, "f32": 2}
+
+    def attention_opts(self, q, k, v, mask_kind: int, score_kind: int, scale: float,
+                       window: int = 0, prefix: int = 0, doc_ids=None, score_param: float = 0.0,
+                       rows=None, prescale: str | None = None):
+        """(out, lse, row_max) float64 under the kernel options.
+
+        OUTPUT_MAX is always on here (row_max); prescale None, "bf16" or "f32"
+        selects PRESCALE_QK with that storage type.  Other arguments as attention().
+        """
+        q = np.ascontiguousarray(q, dtype=np.float32)
+        k = np.ascontiguousarray(k, dtype=np.float32)
+        v = np.ascontiguousarray(v, dtype=np.float32)
+        B, H, s_q, D = q.shape
+        s_kv = k.shape[2]
+        doc = None if doc_ids is None else np.ascontiguousarray(doc_ids, dtype=np.int32)
+        if rows is None:
+            out = np.zeros((B, H, s_q, D), np.float64)
+            lse = np.zeros((B, H, s_q), np.float64)
+            rp, nrows = None, 0
+        else:
+            rows = np.ascontiguousarray(rows, dtype=np.int64)
+            out = np.zeros((rows.size, D), np.float64)
+            lse = np.zeros((rows.size,), np.float64)
+            rp, nrows = _ptr(rows, ctypes.c_int64), rows.size
+        row_max = np.zeros_like(lse)
+        rc = self.lib.oracle_attention_opts(_ptr(q, ctypes.c_float), _ptr(k, ctypes.c_float),
+                                            _ptr(v, ctypes.c_float), B, H, s_q, s_kv, D, mask_kind,
+                                            window, prefix, _ptr(doc, ctypes.c_int32), score_kind,
+                                            float(score_param), float(scale), self.PRESCALE[prescale],
+                                            rp, nrows, _ptr(out, ctypes.c_double),
+                                            _ptr(lse, ctypes.c_double), _ptr(row_max, ctypes.c_double))
+        if rc != 0:
+            raise ValueError(f"oracle_attention_opts failed with {rc}")
+        return out, lse, row_max
+
+    def round_bf16(self, x: float) -> float:
+        return float(self.lib.oracle_round_bf16(float(x)))
+
     def mask_value(self, kind: int, q: int, kv: int, b: int = 0, h: int = 0, window: int = 0,
                    prefix: int = 0, doc_ids=None) -> bool:
         doc = None if doc_ids is None else np.ascontiguousarray(doc_ids, dtype=np.int32)
@@ -162,6 +206,10 @@ def block_mask(*a, **kw):
 
 def mask_value(*a, **kw):
     return default().mask_value(*a, **kw)
+
+
+def attention_opts(*a, **kw):
+    return default().attention_opts(*a, **kw)
 
 
 def num_threads() -> int:

@@ -12,7 +12,11 @@ when the oracle disagrees with:
     softcap scores built through atanh; block counts of causal, sliding
     window and prefix masks; document tiles from the document intervals);
   * special cases (constant V, W = 1, W = 0, first causal row, a huge cap);
-  * a pure-Python brute force on tiny shapes (math.exp, plain loops).
+  * a pure-Python brute force on tiny shapes (math.exp, plain loops);
+  * for the kernel options: PyTorch's float32 -> bfloat16 conversion and a
+    nearest-neighbour check of the oracle's bfloat16 rounding, exact
+    power-of-two prescaling, brute force on a prescaled q computed outside
+    the oracle, and the bounds max S <= lse <= max S + ln n of the row max.
 
 The mutation test compiles deliberately broken copies of oracle.c and checks
 that at least one pin fails for each.
@@ -344,10 +348,11 @@ def _bf_score(kind, param, t, h, H, i, j):
 
 
 def brute_force(q, k, v, mask, score, scale, window=0, prefix=0, doc=None, param=0.0, block=2):
-    """Plain Python loops: (out, lse, block-mask dict) for tiny shapes."""
+    """Plain Python loops: (out, lse, block status, row max) for tiny shapes."""
     B, H, S, D = q.shape
     out = [[[[0.0] * D for _ in range(S)] for _ in range(H)] for _ in range(B)]
     lse = [[[0.0] * S for _ in range(H)] for _ in range(B)]
+    rmax = [[[0.0] * S for _ in range(H)] for _ in range(B)]
     for b in range(B):
         for h in range(H):
             for i in range(S):
@@ -358,8 +363,10 @@ def brute_force(q, k, v, mask, score, scale, window=0, prefix=0, doc=None, param
                         row.append((j, _bf_score(score, param, t, h, H, i, j)))
                 if not row:
                     lse[b][h][i] = -math.inf
+                    rmax[b][h][i] = -math.inf
                     continue
                 mx = max(s for _, s in row)
+                rmax[b][h][i] = mx
                 L = mx + math.log(math.fsum(math.exp(s - mx) for _, s in row))
                 lse[b][h][i] = L
                 for d in range(D):
@@ -374,7 +381,7 @@ def brute_force(q, k, v, mask, score, scale, window=0, prefix=0, doc=None, param
                             for i in range(qb * block, qb * block + block)
                             for j in range(kb * block, kb * block + block))
                     status[b, h, qb, kb] = 2 if c == block * block else (1 if c else 0)
-    return np.asarray(out), np.asarray(lse), status
+    return np.asarray(out), np.asarray(lse), status, np.asarray(rmax)
 
 
 def pin_brute_force_tiny(orc):
@@ -389,16 +396,120 @@ def pin_brute_force_tiny(orc):
                          (W.MASK_CAUSAL_PREFIX, {"prefix": 5}), (W.MASK_DOCUMENT, {"doc": doc}),
                          (W.MASK_ALL, {})]:
             for score, sp in [(W.SCORE_IDENTITY, 0.0), (W.SCORE_SOFTCAP, 0.9), (W.SCORE_ALIBI, 0.0)]:
-                bo, bl, bs = brute_force(q, k, v, mask, score, 0.7, param=sp, block=block,
-                                         window=kw.get("window", 0), prefix=kw.get("prefix", 0),
-                                         doc=kw.get("doc"))
+                bo, bl, bs, bx = brute_force(q, k, v, mask, score, 0.7, param=sp, block=block,
+                                             window=kw.get("window", 0), prefix=kw.get("prefix", 0),
+                                             doc=kw.get("doc"))
                 okw = {"window": kw.get("window", 0), "prefix": kw.get("prefix", 0),
                        "doc_ids": kw.get("doc")}
                 oo, ol = orc.attention(q, k, v, mask, score, 0.7, score_param=sp, **okw)
                 _close(oo, bo, 1e-12, f"brute out S{S} m{mask} s{score}")
                 _close(ol, bl, 1e-12, f"brute lse S{S} m{mask} s{score}")
+                _, _, ox = orc.attention_opts(q, k, v, mask, score, 0.7, score_param=sp, **okw)
+                _close(ox, bx, 1e-12, f"brute row max S{S} m{mask} s{score}")
                 bm = orc.block_mask(mask, B, H, S, S, block, **okw)
                 _check_lists(bm, bs, f"brute block mask S{S} m{mask}")
+
+
+# ------------------------------------------------------------ kernel options
+def _bf16(x):
+    """float32 values -> bfloat16 values by PyTorch's conversion (one rounding, ties to even)."""
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).float().numpy()
+
+
+def pin_round_bf16_is_library_conversion(orc):
+    # float32 inputs: PyTorch's float32 -> bfloat16 conversion is the reference
+    rng = np.random.default_rng(40)
+    bits = rng.integers(0, 2**31 - 1, 4000, dtype=np.int64).astype(np.uint32)
+    bits = bits[(bits & 0x7F800000) != 0x7F800000]                       # no inf / nan
+    ties = (rng.integers(0, 0x7F7F, 2000, dtype=np.int64).astype(np.uint32) << 16) | 0x8000
+    edge = np.array([0x7F7F0000, 0x7F7F7FFF, 0x7F7F8000, 0x7F7F8001, 0x7F7FFFFF, 0x7F000000,
+                     0x00800000, 0x00807FFF, 0x00808000, 0x00018000, 0x00008000, 0x00007FFF,
+                     0x00000001, 0x3F808000, 0x3F818000], np.uint32)
+    x = np.concatenate([bits, ties, edge]).view(np.float32)
+    x = np.concatenate([x, -x])
+    ref = _bf16(x).astype(np.float64)
+    got = np.array([orc.round_bf16(float(t)) for t in x])
+    bad = np.flatnonzero(got != ref)
+    assert bad.size == 0, f"bf16 rounding differs at {x[bad[:4]]}: {got[bad[:4]]} vs {ref[bad[:4]]}"
+
+
+def pin_round_bf16_nearest_on_exact_products(orc):
+    # scale * q (q bfloat16, scale float32) has up to 32 significant bits: the
+    # result must be a bfloat16 no farther from x than either bfloat16
+    # neighbour, and the even one on a tie
+    rng = np.random.default_rng(41)
+    q = _bf16(rng.standard_normal(3000).astype(np.float32))
+    for scale in (1 / math.sqrt(128), 1 / math.sqrt(96), 0.3):
+        x = q.astype(np.float64) * float(np.float32(scale))
+        r = np.array([orc.round_bf16(t) for t in x])
+        rb = torch.from_numpy(r.astype(np.float32)).to(torch.bfloat16)
+        assert np.array_equal(rb.float().numpy().astype(np.float64), r), "not a bfloat16 value"
+        b = rb.view(torch.int16).numpy().astype(np.int32)
+        d0 = np.abs(x - r)
+        for off in (-1, 1):
+            nb = torch.from_numpy((b + off).astype(np.int16)).view(torch.bfloat16).float().numpy()
+            d1 = np.abs(x - nb.astype(np.float64))
+            assert np.all(d0 <= d1), f"a neighbour is nearer (scale {scale})"
+            assert np.all((b[d0 == d1] & 1) == 0), f"tie not to even (scale {scale})"
+
+
+def pin_prescale_power_of_two_scale_changes_nothing(orc):
+    # scale = 2^-3 multiplies exactly in both storage types
+    B, H, S, D = 1, 2, 24, 8
+    q, k, v = _bf16(_rand((B, H, S, D), 42)), _bf16(_rand((B, H, S, D), 43)), _rand((B, H, S, D), 44)
+    for mask, kw in [(W.MASK_CAUSAL, {}), (W.MASK_SLIDING_WINDOW, {"window": 5})]:
+        for score, sp in [(W.SCORE_IDENTITY, 0.0), (W.SCORE_SOFTCAP, 1.5), (W.SCORE_ALIBI, 0.0)]:
+            o0, l0, m0 = orc.attention_opts(q, k, v, mask, score, 0.125, score_param=sp, **kw)
+            for ps in ("bf16", "f32"):
+                o1, l1, m1 = orc.attention_opts(q, k, v, mask, score, 0.125, score_param=sp,
+                                                prescale=ps, **kw)
+                _close(o1, o0, 0.0, f"prescale {ps} out")
+                _close(l1, l0, 0.0, f"prescale {ps} lse")
+                _close(m1, m0, 0.0, f"prescale {ps} row max")
+
+
+def pin_prescale_is_attention_on_rounded_q(orc):
+    # bfloat16: a scale with 8 significant bits keeps scale * q exact in
+    # float32, so PyTorch's conversion gives q~ with one rounding; float32:
+    # numpy rounds the exact double product once.  Brute force on q~, scale 1.
+    B, H, S, D = 1, 2, 12, 4
+    k, v = _rand((B, H, S, D), 46), _rand((B, H, S, D), 47)
+    qb = _bf16(_rand((B, H, S, D), 45) * 3.0)
+    qf = _rand((B, H, S, D), 48)
+    cases = [("bf16", qb, 179 / 256, _bf16((qb.astype(np.float64) * (179 / 256)).astype(np.float32))),
+             ("f32", qf, float(np.float32(0.3)), (qf.astype(np.float64) * float(np.float32(0.3))).astype(np.float32))]
+    for ps, q, scale, qt in cases:
+        assert not np.array_equal(qt.astype(np.float64), q.astype(np.float64) * scale), "no rounding exercised"
+        for mask, kw in [(W.MASK_CAUSAL, {}), (W.MASK_ALL, {})]:
+            for score, sp in [(W.SCORE_IDENTITY, 0.0), (W.SCORE_SOFTCAP, 0.9), (W.SCORE_ALIBI, 0.0)]:
+                bo, bl, _, bx = brute_force(qt, k, v, mask, score, 1.0, param=sp, block=4, **kw)
+                oo, ol, ox = orc.attention_opts(q, k, v, mask, score, scale, score_param=sp,
+                                                prescale=ps, **kw)
+                _close(oo, bo, 1e-12, f"prescale {ps} out m{mask} s{score}")
+                _close(ol, bl, 1e-12, f"prescale {ps} lse m{mask} s{score}")
+                _close(ox, bx, 1e-12, f"prescale {ps} row max m{mask} s{score}")
+
+
+def pin_row_max_bounds_lse(orc):
+    # max_j S_j <= ln sum_j exp(S_j) <= max_j S_j + ln n over the n unmasked
+    # keys of a row; equality on the left when n = 1; empty rows give -inf
+    B, H, S, D = 2, 2, 40, 8
+    q, k, v = _rand((B, H, S, D), 49), _rand((B, H, S, D), 50), _rand((B, H, S, D), 51)
+    doc = np.repeat(np.arange(5, dtype=np.int32), 8)[None, :].repeat(B, 0)
+    for mask, kw, bkw in [(W.MASK_CAUSAL, {}, {}), (W.MASK_SLIDING_WINDOW, {"window": 7}, {"window": 7}),
+                          (W.MASK_CAUSAL_PREFIX, {"prefix": 11}, {"prefix": 11}),
+                          (W.MASK_DOCUMENT, {"doc_ids": doc}, {"doc": doc}), (W.MASK_ALL, {}, {})]:
+        n = np.array([[[sum(_bf_mask(mask, b, h, i, j, bkw.get("window", 0), bkw.get("prefix", 0),
+                                     bkw.get("doc")) for j in range(S))
+                        for i in range(S)] for h in range(H)] for b in range(B)], np.float64)
+        for score, sp in [(W.SCORE_IDENTITY, 0.0), (W.SCORE_SOFTCAP, 2.0), (W.SCORE_ALIBI, 0.0)]:
+            _, lse, mx = orc.attention_opts(q, k, v, mask, score, 0.6, score_param=sp, **kw)
+            assert np.all(mx <= lse + 1e-12), (mask, score)
+            assert np.all(lse <= mx + np.log(n) + 1e-12), (mask, score)
+    _, lse, mx = orc.attention_opts(q, k, v, W.MASK_SLIDING_WINDOW, W.SCORE_ALIBI, 0.6, window=1)
+    _close(mx, lse, 1e-12, "W=1 row max = lse")
+    o0, l0, m0 = orc.attention_opts(q, k, v, W.MASK_SLIDING_WINDOW, W.SCORE_IDENTITY, 0.6, window=0)
+    assert np.all(np.isneginf(m0)) and np.all(np.isneginf(l0)) and np.all(o0 == 0.0), "W=0 rows"
 
 
 ALL_PINS = [
@@ -420,4 +531,9 @@ ALL_PINS = [
     pin_document_blocks_from_intervals,
     pin_golden_causal_prefix_predicate,
     pin_brute_force_tiny,
+    pin_round_bf16_is_library_conversion,
+    pin_round_bf16_nearest_on_exact_products,
+    pin_prescale_power_of_two_scale_changes_nothing,
+    pin_prescale_is_attention_on_rounded_q,
+    pin_row_max_bounds_lse,
 ]

@@ -26,14 +26,25 @@ MUTATIONS = [
     ("softcap scale inside", "return param * tanh(t / param);", "return param * tanh(t);"),
     ("lse drops max", "const double L = mx + log(Z);", "const double L = log(Z);"),
     ("out unnormalised", "const double p = exp(srow[j] - L);", "const double p = exp(srow[j] - mx);"),
-    ("scale dropped", "or_score_mod(score_kind, score_param, scale * dot, h, H, i, j)",
+    ("scale dropped", "or_score_mod(score_kind, score_param, post * dot, h, H, i, j)",
      "or_score_mod(score_kind, score_param, dot, h, H, i, j)"),
     ("v row index", "const float *vj = v + j * D;", "const float *vj = v + i * D;"),
     ("full tiles classed as partial", "const int64_t all = (int64_t)block * block;",
      "const int64_t all = (int64_t)block * block + 1;"),
     ("padding order", "if (!(count[j] > 0 && count[j] < all)) pi[tp++] = (int32_t)j;",
      "if (!(count[j] > 0 && count[j] < all)) pi[tp++] = (int32_t)(nkvb - 1 - j);"),
-    ("empty row guard", "        *lse = -INFINITY;\n        return;", "        *lse = 0.0;\n        return;"),
+    ("empty row guard", "        *lse = -INFINITY;\n        if (row_max)", "        *lse = 0.0;\n        if (row_max)"),
+    ("row max from the last key", "if (row_max) *row_max = mx;", "if (row_max) *row_max = srow[s_kv - 1];"),
+    ("empty row max", "if (row_max) *row_max = -INFINITY;", "if (row_max) *row_max = 0.0;"),
+    ("prescale applies scale twice", "const double post = prescale ? 1.0 : scale;", "const double post = scale;"),
+    ("prescale drops scale", "const double x = scale * (double)q;", "const double x = (double)q;"),
+    ("prescale bf16 not rounded", "if (prescale == OR_PRESCALE_BF16) return or_round_bf16(x);",
+     "if (prescale == OR_PRESCALE_BF16) return (double)(float)x;"),
+    ("prescale f32 not rounded", "    return (double)(float)x;\n}", "    return x;\n}"),
+    ("bf16 keeps 9 bits", "int quantum = e - 8;", "int quantum = e - 9;"),
+    ("bf16 ties away from zero", "nearbyint(ldexp(x, -quantum))", "round(ldexp(x, -quantum))"),
+    ("bf16 subnormal quantum", "if (quantum < -133) quantum = -133;", "if (quantum < -126) quantum = -126;"),
+    ("bf16 overflow bound", "ldexp(255.0, 120)", "ldexp(255.0, 119)"),
 ]
 
 
