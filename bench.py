@@ -238,6 +238,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--e2e-chunks", type=int, default=16,
                     help="(b, h) chunks of flex_attention_fwd_host, whose copies overlap the work")
+    ap.add_argument("--option-steps", type=int, default=20,
+                    help="launches per kernel-option variant (OUTPUT_MAX, PRESCALE_QK, ...); 0 skips them")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling a smaller case)")
@@ -250,6 +252,48 @@ def main():
         run_reference(args, w)
         return
     run_ours(args, w)
+
+
+def kernel_option_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flush, flops, steps):
+    """Attention launches under each kernel option (outside the headline's timed region).
+
+    The variants run interleaved, one launch each per round, on the same
+    BlockMask and inputs, so clock drift falls on all of them alike.
+    """
+    if steps <= 0:
+        return None
+    row_max = torch.empty_like(lse)
+    variants = {
+        "default": {},
+        "output_max": {"max_scores": row_max},
+        "prescale_qk": {"prescale_qk": True},
+        "rows_guaranteed_safe": {"rows_guaranteed_safe": True},
+        "all": {"max_scores": row_max, "prescale_qk": True, "rows_guaranteed_safe": True},
+    }
+
+    def launch(opts):
+        fa.flex_attention_fwd_opts(dq, dk, dv, bm, w.score, w.score_param, w.scale, out=out, lse=lse,
+                                   stream=stream, **opts)
+
+    for opts in variants.values():
+        launch(opts)
+    torch.cuda.synchronize()
+    ev = {name: [] for name in variants}
+    for _ in range(steps):
+        for name, opts in variants.items():
+            if flush is not None:
+                flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            launch(opts)
+            b.record(stream)
+            ev[name].append((a, b))
+    torch.cuda.synchronize()
+    if fa.flex_device_status() != fa.FLEX_OK:
+        raise SystemExit("device status reported a timeout during the kernel-option launches")
+    ms = {name: float(np.mean([a.elapsed_time(b) for a, b in pairs])) for name, pairs in ev.items()}
+    return {"api": "flex_attention_fwd_opts", "launches_each": steps, "ms_per_launch": ms,
+            "tflops": {name: flops / (t * 1e-3) / 1e12 for name, t in ms.items()}}
 
 
 def run_ours(args, w: W.Workload) -> None:
@@ -363,6 +407,9 @@ def run_ours(args, w: W.Workload) -> None:
                "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "api": "flex_attention_fwd_host",
                "chunks": args.e2e_chunks}
 
+    options = kernel_option_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flush, flops,
+                                    args.option_steps)
+
     if rank != 0:
         return
     peaks = measured_peaks()
@@ -387,7 +434,8 @@ def run_ours(args, w: W.Workload) -> None:
             "gpu_launches": 2 * args.steps, "clocks": clocks.summary(),
             "attn_ms_per_launch": {"mean": attn_mean_ms, "median": float(np.median(attn_ms)),
                                    "min": float(np.min(attn_ms))},
-            "block_mask_ms_per_launch": float(np.mean(np.asarray(step_ms) - np.asarray(attn_ms)))}
+            "block_mask_ms_per_launch": float(np.mean(np.asarray(step_ms) - np.asarray(attn_ms))),
+            "kernel_options": options}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -102,6 +102,8 @@ int prepare_attention(const flex_tensor *q, const flex_tensor *k, const flex_ten
     p.score_kind = score_kind;
     p.score_param = score_param;
     p.scale = scale;
+    p.prescale = 0;
+    p.row_max = nullptr;
     p.status = nullptr;
     return FLEX_OK;
 }
@@ -269,6 +271,29 @@ int flex_attention_fwd(const flex_tensor *q, const flex_tensor *k, const flex_te
     AttnProblem p;
     const int rc = prepare_attention(q, k, v, bm, score_kind, score_param, scale, out, lse, p);
     if (rc != FLEX_OK) return rc;
+    int err = FLEX_OK;
+    p.status = device_status_word(&err);
+    if (!p.status) return err;
+    return launch_attention(p, q->dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FLEX_OK : FLEX_ERR_CUDA;
+}
+
+int flex_attention_fwd_opts(const flex_tensor *q, const flex_tensor *k, const flex_tensor *v,
+                            const flex_block_mask *bm, int32_t score_kind, float score_param, float scale,
+                            void *out, float *lse, const flex_kernel_options *opts, void *stream) {
+    AttnProblem p;
+    int rc = prepare_attention(q, k, v, bm, score_kind, score_param, scale, out, lse, p);
+    if (rc != FLEX_OK) return rc;
+    if (opts) {
+        if ((opts->prescale_qk != 0 && opts->prescale_qk != 1) ||
+            (opts->rows_guaranteed_safe != 0 && opts->rows_guaranteed_safe != 1))
+            return FLEX_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(opts->max_scores) & 3u) return FLEX_ERR_ALIGNMENT;
+        // scale 0 makes q~ = 0: the same scores as scaling after QK^T
+        p.prescale = opts->prescale_qk && scale != 0.f;
+        p.row_max = opts->max_scores;
+        // rows_guaranteed_safe needs nothing: the kernels carry no per-tile
+        // guard for rows without an unmasked score (see the header)
+    }
     int err = FLEX_OK;
     p.status = device_status_word(&err);
     if (!p.status) return err;

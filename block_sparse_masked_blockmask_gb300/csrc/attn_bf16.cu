@@ -63,10 +63,13 @@ cudaError_t launch_attn_bf16(const AttnProblem &p, cudaStream_t stream) {
     kp.full_num = p.full_num;
     kp.full_idx = p.full_idx;
     kp.mask = p.mask;
-    kp.scale = p.scale;
+    // PRESCALE_QK moves the scale onto Q (in shared memory); the scores then take 1
+    kp.scale = p.prescale ? 1.f : p.scale;
+    kp.prescale = p.prescale ? p.scale : 0.f;
     kp.score_param = p.score_param;
     kp.out = static_cast<uint16_t *>(p.out);
     kp.lse = p.lse;
+    kp.row_max = p.row_max;
     kp.status = p.status;
     return p.D == 64 ? launch_bf16_d64(tq, tk, tv, kp, p.score_kind, stream)
                      : launch_bf16_d128(tq, tk, tv, kp, p.score_kind, stream);

@@ -45,6 +45,7 @@
 //     FLEX_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees TMEM, exits.
 #pragma once
 
+#include <cfloat>
 #include <cstddef>
 
 #include <cuda_bf16.h>
@@ -87,8 +88,10 @@ struct Bf16Params {
     const int32_t *kv_num, *kv_idx, *full_num, *full_idx;
     MaskDesc mask;
     float scale, score_param;
-    uint16_t *out;  // bf16 bits, contiguous [B, H, q_len, D]
-    float *lse;     // [B, H, q_len]
+    float prescale;   // PRESCALE_QK: 0 = off, else Q is multiplied by it in shared memory (scale is then 1)
+    uint16_t *out;    // bf16 bits, contiguous [B, H, q_len, D]
+    float *lse;       // [B, H, q_len]
+    float *row_max;   // OUTPUT_MAX: [B, H, q_len] or null
     int *status;
 };
 
@@ -104,6 +107,7 @@ struct ItemSlot {
 // Shared-memory bookkeeping that follows the Q/K/V tiles.
 struct AttnMisc {
     uint64_t q_full, q_empty;
+    uint64_t q_loaded;                         // PRESCALE_QK: the Q copies landed (q_full follows the scaling)
     uint64_t near_end;                         // the K producer has issued an item's last K tile
     uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];
     uint64_t s_full[2], p_full[2];             // p_full[i]: all of P_i is in TMEM
@@ -253,6 +257,35 @@ struct ScoreLog2 {
     }
 };
 
+// PRESCALE_QK on the Q tiles in shared memory: every bf16 element q becomes
+// bf16(s q), rounded once.  The float product is taken toward zero and its
+// last bit set when it was inexact (rounding to odd at 24 bits); rounding that
+// to nearest even at bf16's 8 bits gives the correctly rounded product, since
+// the float keeps at least two extra bits (S. Boldo, G. Melquiond, "Emulation
+// of FMA and correctly rounded sums: proved algorithms using rounding to odd",
+// IEEE Trans. Computers 57(4), 2008).  The 128-byte swizzle does not matter:
+// every element gets the same factor.
+__device__ __forceinline__ void prescale_q(uint4 *q, int n16, float s, int lane) {
+    const uint64_t s2 = f2_pack(s, s), ns2 = f2_pack(-s, -s);
+#pragma unroll 2
+    for (int i = lane; i < n16; i += 32) {
+        uint4 w = q[i];
+        uint32_t e[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint64_t x2 = f2_pack(__uint_as_float(e[j] << 16), __uint_as_float(e[j] & 0xFFFF0000u));
+            const uint64_t p2 = f2_mul_rz(x2, s2);
+            float p0, p1, r0, r1;
+            f2_unpack(p2, p0, p1);
+            f2_unpack(f2_fma(x2, ns2, p2), r0, r1);  // p - x s exactly: nonzero iff the product was inexact
+            p0 = __uint_as_float(__float_as_uint(p0) | (r0 != 0.f ? 1u : 0u));
+            p1 = __uint_as_float(__float_as_uint(p1) | (r1 != 0.f ? 1u : 0u));
+            e[j] = pack_bf16x2(p0, p1);
+        }
+        q[i] = make_uint4(e[0], e[1], e[2], e[3]);
+    }
+}
+
 // mask_mod on a partial tile for row q (columns kv0 .. kv0 + 127), on the
 // packed score pairs.
 __device__ __forceinline__ uint64_t keep_pair(uint64_t v, bool k0, bool k1) {
@@ -397,6 +430,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(&ms.q_full, 1);
         mbar_init(&ms.q_empty, 1);
+        mbar_init(&ms.q_loaded, 1);
         mbar_init(&ms.near_end, 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(&ms.k_full[s], 1);
@@ -445,6 +479,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         uint32_t nne = 0;   // near_end phases consumed
         uint32_t nclc = 0;  // launch-control responses consumed
         bool ok = true;
+        // the Q copies complete on q_full, or with PRESCALE_QK on q_loaded
+        const bool prescale = p.prescale != 0.f;
+        uint64_t *q_bar = prescale ? &ms.q_loaded : &ms.q_full;
         if (lane == 0) prefetch_tensormap(&tmap_q);
         for (uint32_t n = 0;; ++n) {
             const int k = (int)(n & 1u);
@@ -474,16 +511,29 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     break;
                 }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&ms.q_full, (has1 ? 2u : 1u) * C::kTileBytes);
+                    mbar_arrive_expect_tx(q_bar, (has1 ? 2u : 1u) * C::kTileBytes);
                     for (int a = 0; a < C::kAtoms; ++a) {
-                        tma_load_4d(smem + C::kQOff + a * C::kAtomBytes, &tmap_q, &ms.q_full, 64 * a, sl.qb0 * kBlock,
+                        tma_load_4d(smem + C::kQOff + a * C::kAtomBytes, &tmap_q, q_bar, 64 * a, sl.qb0 * kBlock,
                                     sl.h, sl.b);
                         if (has1)
-                            tma_load_4d(smem + C::kQOff + C::kTileBytes + a * C::kAtomBytes, &tmap_q, &ms.q_full,
+                            tma_load_4d(smem + C::kQOff + C::kTileBytes + a * C::kAtomBytes, &tmap_q, q_bar,
                                         64 * a, (sl.qb0 + 1) * kBlock, sl.h, sl.b);
                     }
                 }
                 ++nq;
+                if (prescale) {
+                    // PRESCALE_QK: scale Q in place once it has landed, then
+                    // hand it to the MMA thread through q_full
+                    if (!warp_wait(&ms.q_loaded, (nq - 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    prescale_q(reinterpret_cast<uint4 *>(smem + C::kQOff), (has1 ? 2 : 1) * (int)C::kTileBytes / 16,
+                               p.prescale, lane);
+                    fence_proxy_async_smem();  // the MMAs read these generic-proxy writes
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ms.q_full);
+                }
                 // wait until this item's last K tile is on the way
                 if (!warp_wait(&ms.near_end, nne & 1u, abort_flag)) {
                     ok = false;
@@ -507,7 +557,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (!ok && lane == 0) record_failure(ms, p.status);
         // every Q copy issued above lands before the CTA exits (normally the
         // MMA thread has already consumed it)
-        if (lane == 0 && nq > 0) drain_wait(&ms.q_full, (nq - 1) & 1u);
+        if (lane == 0 && nq > 0) drain_wait(q_bar, (nq - 1) & 1u);
         __syncwarp();
     } else if (warp == kTmaWarp || warp == kTmaVWarp) {
         // ----------------------------------------------------- TMA producers
@@ -709,7 +759,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           if constexpr (DOC) {
               if (valid) doc_q = __ldg(p.mask.doc_ids + (int64_t)b * p.mask.doc_len + q);
           }
-          float m_run = -INFINITY, l_run = 0.f;
+          // The running max starts at a finite floor, so a tile whose scores
+          // are all masked for this row gives exp2(-inf - floor) = 0 with no
+          // special case, and the first live tile rescales by exp2(floor - m)
+          // = 0.  Only the epilogue tells empty rows apart (l_run == 0).
+          float m_run = -FLT_MAX, l_run = 0.f;
+          float m_max = -INFINITY;  // exact row max (OUTPUT_MAX); m_run may lag it by < kRescaleThreshold
           uint32_t cnt = 0;  // tiles of this item
           if (valid) {
             for (int u = 0; u < nu; ++u) {
@@ -760,13 +815,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 const float m_tile = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) +
                                      score.offset;
+                m_max = fmaxf(m_max, m_tile);
                 float alpha = 1.f;
-                if (m_tile > m_run + kRescaleThreshold) {  // also taken when m_run = -inf
+                if (m_tile > m_run + kRescaleThreshold) {  // always taken at the row's first live tile
                     alpha = ex2_approx(m_run - m_tile);
                     m_run = m_tile;
                 }
-                const float m_use = m_run == -INFINITY ? 0.f : m_run;
-                const float sub = score.offset - m_use;
+                const float sub = score.offset - m_run;
                 const uint64_t sub2 = f2_pack(sub, sub);
                 // O rescale (rare) before the first half of P is handed over:
                 // the PV MMA of this step accumulates into the rescaled O
@@ -849,6 +904,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         dst[c0 / 8 + j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                 }
                 p.lse[orow] = live ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+                if (p.row_max) p.row_max[orow] = m_max * kLn2;
             }
           }
           if (nu > 0) {

@@ -47,10 +47,12 @@ __global__ void __launch_bounds__(Fp32Cfg<D>::kThreads) attn_fp32_kernel(AttnPro
 
     const float *qp = static_cast<const float *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1] +
                       (int64_t)q * p.q_stride[2] + part * kDimsPerThread;
+    // PRESCALE_QK: q~ = scale q rounded to float once, scores q~.k unscaled
+    const float post = p.prescale ? 1.f : p.scale;
     float qr[kDimsPerThread], acc[kDimsPerThread];
 #pragma unroll
     for (int d = 0; d < kDimsPerThread; ++d) {
-        qr[d] = qp[d];
+        qr[d] = p.prescale ? __fmul_rn(qp[d], p.scale) : qp[d];
         acc[d] = 0.f;
     }
     const float slope = exp2f(-8.f * (float)(h + 1) / (float)p.H);
@@ -86,7 +88,7 @@ __global__ void __launch_bounds__(Fp32Cfg<D>::kThreads) attn_fp32_kernel(AttnPro
                 for (int d = 0; d < kDimsPerThread; ++d) dot = fmaf(qr[d], kr[d], dot);
                 if constexpr (C::kTpr == 2) dot += __shfl_xor_sync(0xffffffffu, dot, 1);
                 const int kv = kv0 + c0 + j;
-                float x = score_mod_f32(p.score_kind, p.score_param, dot * p.scale, slope, q, kv);
+                float x = score_mod_f32(p.score_kind, p.score_param, dot * post, slope, q, kv);
                 if (!full && !mask_mod(p.mask, b, q, kv)) x = -INFINITY;
                 s[j] = x;
             }
@@ -117,7 +119,9 @@ __global__ void __launch_bounds__(Fp32Cfg<D>::kThreads) attn_fp32_kernel(AttnPro
     for (int d = 0; d < kDimsPerThread; d += 4)
         *reinterpret_cast<float4 *>(op + d) = make_float4(acc[d] * inv, acc[d + 1] * inv, acc[d + 2] * inv,
                                                           acc[d + 3] * inv);
-    if (part == 0) p.lse[((int64_t)b * p.H + h) * p.q_len + q] = l > 0.f ? m + logf(l) : -INFINITY;
+    const int64_t orow = ((int64_t)b * p.H + h) * p.q_len + q;
+    if (part == 0) p.lse[orow] = l > 0.f ? m + logf(l) : -INFINITY;
+    if (part == 0 && p.row_max) p.row_max[orow] = m;  // exact running max (OUTPUT_MAX); -inf for an empty row
 }
 
 template <int D>

@@ -77,6 +77,8 @@ struct AttnProblem {
     int score_kind;
     float score_param;
     float scale;
+    int prescale;                                    // PRESCALE_QK: Q is scaled (rounded to its dtype) before QK^T
+    float *row_max;                                  // OUTPUT_MAX: contiguous [B,H,q_len] or null
     int *status;                                     // device status word
 };
 

@@ -293,10 +293,23 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+// product rounded toward zero
+__device__ __forceinline__ uint64_t f2_mul_rz(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
+}
+
+// Orders this thread's generic-proxy shared-memory writes before the
+// async-proxy reads (tcgen05.mma operands, TMA) that a later mbarrier
+// hand-off orders after it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Two floats to a packed bf16x2 (round to nearest even); `lo` lands in bits 0-15.

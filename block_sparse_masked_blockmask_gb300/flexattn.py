@@ -38,7 +38,7 @@ FLEX_DTYPE_BF16 = 0
 FLEX_DTYPE_FP32 = 1
 
 EXPORTED = ("flex_block_mask_sizes", "flex_block_mask_create", "flex_attention_fwd",
-            "flex_attention_fwd_noalloc", "flex_attention_fwd_host", "flex_device_status",
+            "flex_attention_fwd_opts", "flex_attention_fwd_noalloc", "flex_attention_fwd_host", "flex_device_status",
             "flex_selftest_wait_timeout", "flex_status_string")
 
 
@@ -63,6 +63,11 @@ class flex_block_mask(ctypes.Structure):
 class flex_tensor(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class flex_kernel_options(ctypes.Structure):
+    _fields_ = [("prescale_qk", ctypes.c_int32), ("rows_guaranteed_safe", ctypes.c_int32),
+                ("max_scores", ctypes.c_void_p)]
 
 
 class flex_device_buffers(ctypes.Structure):
@@ -100,6 +105,10 @@ def load_library():
             lib.flex_attention_fwd.argtypes = [tp, tp, tp, ctypes.POINTER(flex_block_mask), i32, ctypes.c_float,
                                                ctypes.c_float, vp, vp, vp]
             lib.flex_attention_fwd.restype = ctypes.c_int
+            lib.flex_attention_fwd_opts.argtypes = [tp, tp, tp, ctypes.POINTER(flex_block_mask), i32,
+                                                    ctypes.c_float, ctypes.c_float, vp, vp,
+                                                    ctypes.POINTER(flex_kernel_options), vp]
+            lib.flex_attention_fwd_opts.restype = ctypes.c_int
             lib.flex_attention_fwd_noalloc.argtypes = [tp, tp, tp, ctypes.POINTER(flex_block_mask), i32,
                                                        ctypes.c_float, ctypes.c_float, vp, vp, vp,
                                                        ctypes.POINTER(ctypes.POINTER(ctypes.c_int))]
@@ -223,6 +232,46 @@ def flex_attention_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_
     if rc != FLEX_OK:
         raise FlexError(rc, "flex_attention_fwd")
     return out, lse
+
+
+def flex_attention_fwd_opts(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_mask: BlockMask,
+                            score_kind: int = FLEX_SCORE_IDENTITY, score_param: float = 0.0,
+                            scale: float | None = None, out: torch.Tensor | None = None,
+                            lse: torch.Tensor | None = None, prescale_qk: bool = False,
+                            rows_guaranteed_safe: bool = False, output_max: bool = False,
+                            max_scores: torch.Tensor | None = None, stream=None):
+    """flex_attention_fwd with the op's kernel options; returns (out, lse, max_scores).
+
+    max_scores (float32 [B, H, Sq]) is allocated when output_max is set and
+    none is given; it is None when OUTPUT_MAX is off.
+    """
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    B, H, Sq, D = q.shape
+    if out is None:
+        out = torch.empty((B, H, Sq, D), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if max_scores is None and output_max:
+        max_scores = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if not out.is_contiguous() or not lse.is_contiguous() or lse.dtype != torch.float32:
+        raise ValueError("out and lse must be contiguous; lse float32")
+    if max_scores is not None and (not max_scores.is_contiguous() or max_scores.dtype != torch.float32
+                                   or max_scores.shape != (B, H, Sq)):
+        raise ValueError("max_scores must be a contiguous float32 [B, H, q_len] tensor")
+    opts = flex_kernel_options(int(bool(prescale_qk)), int(bool(rows_guaranteed_safe)),
+                               None if max_scores is None else max_scores.data_ptr())
+    tq, tk, tv = _tensor(q), _tensor(k), _tensor(v)
+    with torch.cuda.device(q.device):
+        rc = load_library().flex_attention_fwd_opts(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                                    ctypes.byref(block_mask.struct), score_kind,
+                                                    float(score_param), float(scale),
+                                                    ctypes.c_void_p(out.data_ptr()),
+                                                    ctypes.c_void_p(lse.data_ptr()), ctypes.byref(opts),
+                                                    _stream_handle(stream, q.device))
+    if rc != FLEX_OK:
+        raise FlexError(rc, "flex_attention_fwd_opts")
+    return out, lse, max_scores
 
 
 def flex_attention_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_mask: BlockMask,

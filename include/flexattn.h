@@ -5,7 +5,9 @@
  *   flex_block_mask_create  builds a BlockMask from an enumerated mask_mod;
  *   flex_attention_fwd      runs softmax(mask(score_mod(Q K^T * scale))) V
  *                           block-sparsely from that BlockMask and returns the
- *                           output and the per-row log-sum-exp.
+ *                           output and the per-row log-sum-exp
+ *                           (flex_attention_fwd_opts: the same with the op's
+ *                           kernel options, e.g. the row max as a third output).
  * Helpers size the BlockMask buffers, name status codes and read the device
  * status word.
  *
@@ -258,6 +260,47 @@ FLEX_API int flex_attention_fwd_host(const flex_tensor *q, const flex_tensor *k,
                                      int32_t mask_kind, const flex_mask_params *params, int32_t score_kind,
                                      float score_param, float scale, void *out, float *lse,
                                      const flex_device_buffers *dev, int32_t chunks, void *stream);
+
+/*
+ * Kernel options of the flex_attention op (its kernel_options dictionary in
+ * PyTorch PR #167356, which names OUTPUT_MAX, PRESCALE_QK and
+ * ROWS_GUARANTEED_SAFE and defaults each to False).  A zeroed struct is the
+ * default and gives exactly what flex_attention_fwd gives.
+ *   prescale_qk   0 or 1.  PRESCALE_QK: q is multiplied by scale before
+ *                 Q K^T, the product rounded once to q's dtype (bfloat16 or
+ *                 float32, to nearest, ties to even), and the scores are
+ *                 score_mod(q~ . k[kv]) with no further scale.  The result
+ *                 differs from the default by that rounding only (none when
+ *                 scale is a power of two).
+ *   rows_guaranteed_safe  0 or 1.  ROWS_GUARANTEED_SAFE: the caller promises
+ *                 that every row keeps at least one unmasked score.  The
+ *                 option exists so a kernel may drop its guard for rows with
+ *                 none; these kernels carry no such guard in their inner
+ *                 loops (a finite floor on the running max makes all-masked
+ *                 tiles contribute exp(-inf) = 0), so the option changes
+ *                 neither results nor speed, and rows that break the promise
+ *                 still get out = 0, lse = -inf.
+ *   max_scores    OUTPUT_MAX: NULL, or device, contiguous [B, H, q_len]
+ *                 float32, 4-byte aligned: the row maximum of the masked,
+ *                 modified scores s[kv] (natural units, like lse), -inf for a
+ *                 row with no unmasked score.
+ */
+typedef struct {
+    int32_t prescale_qk;
+    int32_t rows_guaranteed_safe;
+    float *max_scores;
+} flex_kernel_options;
+
+/*
+ * flex_attention_fwd with kernel options; opts may be NULL (all default).
+ * Arguments, results and errors as flex_attention_fwd, plus
+ * FLEX_ERR_INVALID_ARG for an option flag other than 0 or 1 and
+ * FLEX_ERR_ALIGNMENT for a misaligned max_scores.
+ */
+FLEX_API int flex_attention_fwd_opts(const flex_tensor *q, const flex_tensor *k, const flex_tensor *v,
+                                     const flex_block_mask *bm, int32_t score_kind, float score_param,
+                                     float scale, void *out, float *lse, const flex_kernel_options *opts,
+                                     void *stream);
 
 /*
  * Synchronises `stream`, then returns and clears the device status word of

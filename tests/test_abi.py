@@ -173,3 +173,23 @@ def test_host_entry_point_rejects_bad_arguments(lib):
     unaligned = fa.flex_device_buffers.from_buffer_copy(dev)
     unaligned.out = 0x40008
     assert call(devbuf=unaligned) == fa.FLEX_ERR_ALIGNMENT
+
+
+def test_options_entry_point_rejects_bad_arguments(lib):
+    # flex_attention_fwd_opts: the checks of flex_attention_fwd plus the options',
+    # all before any CUDA call
+    bf = fa.FLEX_DTYPE_BF16
+    q, k, v = (_tensor(bf, [1, 2, 256, 64]) for _ in range(3))
+    bm = _mask_struct()
+
+    def call(opts, q=q, score=fa.FLEX_SCORE_IDENTITY):
+        return lib.flex_attention_fwd_opts(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(bm),
+                                           score, 0.0, 0.125, ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000),
+                                           ctypes.byref(opts) if opts is not None else None, None)
+
+    assert call(fa.flex_kernel_options(2, 0, None)) == fa.FLEX_ERR_INVALID_ARG
+    assert call(fa.flex_kernel_options(0, -1, None)) == fa.FLEX_ERR_INVALID_ARG
+    assert call(fa.flex_kernel_options(1, 1, 0x40002)) == fa.FLEX_ERR_ALIGNMENT
+    # the shared checks come first and still apply
+    assert call(fa.flex_kernel_options(1, 0, 0x40000), score=3) == fa.FLEX_ERR_INVALID_ARG
+    assert call(None, q=_tensor(bf, [1, 2, 384, 64])) == fa.FLEX_ERR_SHAPE
