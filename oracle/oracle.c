@@ -150,7 +150,10 @@ static double or_prescale(int prescale, double scale, float q)
 
 /*
  * Dense mask evaluated tile by tile; one BLOCK-row band of the mask is
- * materialised at a time to bound memory.  Output layouts:
+ * materialised at a time to bound memory.  Lengths need not be multiples of
+ * BLOCK: the dense mask is padded with false to whole tiles
+ * (NQB = ceil(Q_LEN / BLOCK), NKVB = ceil(KV_LEN / BLOCK)), so a tile that
+ * reaches past either length is never full.  Output layouts:
  *   kv_num, full_num : [B, H, NQB]
  *   kv_idx, full_idx : [B, H, NQB, NKVB]
  */
@@ -161,11 +164,10 @@ int oracle_block_mask(int kind, int window, int prefix, const int32_t *doc,
 {
     if (!or_mask_ok(kind) || B <= 0 || H <= 0 || q_len <= 0 || kv_len <= 0 || block <= 0)
         return OR_ERR_ARG;
-    if (q_len % block || kv_len % block)
-        return OR_ERR_ARG;
     if (kind == OR_MASK_DOCUMENT && (doc == NULL || q_len != kv_len))
         return OR_ERR_ARG;
-    const int64_t nqb = q_len / block, nkvb = kv_len / block;
+    const int64_t nqb = ((int64_t)q_len + block - 1) / block;
+    const int64_t nkvb = ((int64_t)kv_len + block - 1) / block;
     or_mask m = {kind, window, prefix, doc, (int64_t)q_len};
     int err = OR_OK;
 
@@ -184,8 +186,10 @@ int oracle_block_mask(int kind, int window, int prefix, const int32_t *doc,
                 continue;
             }
             for (int64_t r = 0; r < block; ++r)
-                for (int64_t kv = 0; kv < kv_len; ++kv)
-                    band[r * kv_len + kv] = (unsigned char)or_mask_mod(&m, b, h, qb * block + r, kv);
+                for (int64_t kv = 0; kv < kv_len; ++kv)  /* columns past KV_LEN: padding, false */
+                    band[r * kv_len + kv] = qb * block + r < q_len  /* rows past Q_LEN: padding, false */
+                                                ? (unsigned char)or_mask_mod(&m, b, h, qb * block + r, kv)
+                                                : 0;
             for (int64_t r = 0; r < block; ++r)
                 for (int64_t kv = 0; kv < kv_len; ++kv)
                     count[kv / block] += band[r * kv_len + kv];

@@ -75,7 +75,7 @@ class Oracle:
     def block_mask(self, kind: int, B: int, H: int, q_len: int, kv_len: int, block: int = 128,
                    window: int = 0, prefix: int = 0, doc_ids=None) -> dict:
         """kv_num_blocks, kv_indices, full_kv_num_blocks, full_kv_indices (int32)."""
-        nqb, nkvb = q_len // block, kv_len // block
+        nqb, nkvb = -(-q_len // block), -(-kv_len // block)  # ceil: tail tiles padded with false
         out = {
             "kv_num_blocks": np.zeros((B, H, nqb), np.int32),
             "kv_indices": np.zeros((B, H, nqb, nkvb), np.int32),

@@ -256,6 +256,26 @@ def pin_causal_block_counts_closed_form(orc):
         _check_lists(bm, np.broadcast_to(status, (1, 2, nb, nb)), f"causal nb={nb}")
 
 
+def pin_ragged_causal_block_counts_closed_form(orc):
+    # S not a multiple of 128: the mask is padded with false to whole tiles, so
+    # in the last q block (rows past S are padding) every tile 0..qb holds
+    # some true pairs but none is full; the other rows are as for whole tiles
+    # (kv tile NB-1 sits above their diagonal, empty)
+    for S in (1, 127, 129, 300, 1000):
+        nb = -(-S // 128)
+        bm = orc.block_mask(W.MASK_CAUSAL, 1, 2, S, S, 128)
+        qb = np.arange(nb)[:, None]
+        kb = np.arange(nb)[None, :]
+        status = np.where(kb < qb, 2, np.where(kb == qb, 1, 0))
+        status[nb - 1, :] = 1
+        _check_lists(bm, np.broadcast_to(status, (1, 2, nb, nb)), f"ragged causal S={S}")
+    # rectangular: Q_LEN 200, KV_LEN 333 with the all-true mask: only the tile
+    # of whole rows and whole columns (q block 0, kv blocks 0 and 1) is full
+    bm = orc.block_mask(W.MASK_ALL, 1, 1, 200, 333, 128)
+    status = np.array([[2, 2, 1], [1, 1, 1]])
+    _check_lists(bm, status[None, None], "ragged all-true 200x333")
+
+
 def pin_sliding_window_block_counts_closed_form(orc):
     # W = 256 = 2 blocks: row qb has kv block qb-1 full, qb-2 and qb partial.
     nb, S = 16, 2048
@@ -371,22 +391,22 @@ def brute_force(q, k, v, mask, score, scale, window=0, prefix=0, doc=None, param
                 lse[b][h][i] = L
                 for d in range(D):
                     out[b][h][i][d] = math.fsum(math.exp(s - L) * float(v[b, h, j, d]) for j, s in row)
-    nb = S // block
+    nb = -(-S // block)  # tiles past S are padded with false
     status = np.zeros((B, H, nb, nb), np.int64)
     for b in range(B):
         for h in range(H):
             for qb in range(nb):
                 for kb in range(nb):
                     c = sum(_bf_mask(mask, b, h, i, j, window, prefix, doc)
-                            for i in range(qb * block, qb * block + block)
-                            for j in range(kb * block, kb * block + block))
+                            for i in range(qb * block, min(S, qb * block + block))
+                            for j in range(kb * block, min(S, kb * block + block)))
                     status[b, h, qb, kb] = 2 if c == block * block else (1 if c else 0)
     return np.asarray(out), np.asarray(lse), status, np.asarray(rmax)
 
 
 def pin_brute_force_tiny(orc):
     B, H, D = 2, 2, 3
-    for S, block in [(8, 2), (12, 4), (16, 4)]:
+    for S, block in [(8, 2), (12, 4), (16, 4), (7, 2), (10, 4), (13, 4)]:
         q, k, v = _rand((B, H, S, D), S), _rand((B, H, S, D), S + 1), _rand((B, H, S, D), S + 2)
         doc = np.zeros((B, S), np.int32)
         doc[0, S // 3:] = 1
@@ -526,6 +546,7 @@ ALL_PINS = [
     pin_first_causal_row_is_v0,
     pin_alibi_diagonal_has_no_bias,
     pin_causal_block_counts_closed_form,
+    pin_ragged_causal_block_counts_closed_form,
     pin_sliding_window_block_counts_closed_form,
     pin_causal_prefix_block_counts_closed_form,
     pin_document_blocks_from_intervals,

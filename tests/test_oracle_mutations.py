@@ -45,6 +45,9 @@ MUTATIONS = [
     ("bf16 ties away from zero", "nearbyint(ldexp(x, -quantum))", "round(ldexp(x, -quantum))"),
     ("bf16 subnormal quantum", "if (quantum < -133) quantum = -133;", "if (quantum < -126) quantum = -126;"),
     ("bf16 overflow bound", "ldexp(255.0, 120)", "ldexp(255.0, 119)"),
+    ("padding rows counted", "band[r * kv_len + kv] = qb * block + r < q_len", "band[r * kv_len + kv] = 1"),
+    ("ragged tiles rounded down", "const int64_t nkvb = ((int64_t)kv_len + block - 1) / block;",
+     "const int64_t nkvb = ((int64_t)kv_len) / block + (kv_len % block > block / 2);"),
 ]
 
 
