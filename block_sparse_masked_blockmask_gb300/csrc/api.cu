@@ -22,8 +22,7 @@ bool valid_mask_kind(int k) { return k >= FLEX_MASK_CAUSAL && k <= FLEX_MASK_ALL
 int check_sizes(int32_t B, int32_t H, int32_t q_len, int32_t kv_len, int32_t block) {
     if (B <= 0 || H <= 0 || q_len <= 0 || kv_len <= 0 || block <= 0) return FLEX_ERR_INVALID_ARG;
     if (block != kBlock) return FLEX_ERR_UNSUPPORTED;
-    if (q_len % block != 0 || kv_len % block != 0) return FLEX_ERR_SHAPE;
-    if (kv_len / block > kMaxKvBlocks) return FLEX_ERR_UNSUPPORTED;
+    if (ceil_blocks(kv_len) > kMaxKvBlocks) return FLEX_ERR_UNSUPPORTED;
     if (B > 65535 || H > 65535) return FLEX_ERR_UNSUPPORTED;
     return FLEX_OK;
 }
@@ -67,11 +66,13 @@ int prepare_attention(const flex_tensor *q, const flex_tensor *k, const flex_ten
     rc = check_sizes(bm->B, bm->H, bm->q_len, bm->kv_len, bm->block);
     if (rc != FLEX_OK) return rc;
     if (bm->B != B || bm->H != H || bm->q_len != Sq || bm->kv_len != Skv) return FLEX_ERR_SHAPE;
-    if (bm->nqb != bm->q_len / bm->block || bm->nkvb != bm->kv_len / bm->block) return FLEX_ERR_SHAPE;
+    if (bm->nqb != ceil_blocks(bm->q_len) || bm->nkvb != ceil_blocks(bm->kv_len)) return FLEX_ERR_SHAPE;
     if (!bm->kv_num_blocks || !bm->kv_indices || !bm->full_kv_num_blocks || !bm->full_kv_indices)
         return FLEX_ERR_INVALID_ARG;
     if (bm->mask_kind == FLEX_MASK_DOCUMENT && (!bm->params.doc_ids || !aligned16(bm->params.doc_ids)))
         return FLEX_ERR_INVALID_ARG;
+    // each kv tile's document ids are bulk-copied as whole 16-byte words
+    if (bm->mask_kind == FLEX_MASK_DOCUMENT && Sq % 4 != 0) return FLEX_ERR_UNSUPPORTED;
     if (bm->mask_kind == FLEX_MASK_SLIDING_WINDOW && bm->params.window < 0) return FLEX_ERR_INVALID_ARG;
     if (B * H * ((bm->nqb + 1) / 2) > INT32_MAX) return FLEX_ERR_UNSUPPORTED;
 
@@ -98,7 +99,8 @@ int prepare_attention(const flex_tensor *q, const flex_tensor *k, const flex_ten
     p.kv_idx = bm->kv_indices;
     p.full_num = bm->full_kv_num_blocks;
     p.full_idx = bm->full_kv_indices;
-    p.mask = MaskDesc{bm->mask_kind, bm->params.window, bm->params.prefix, bm->q_len, bm->params.doc_ids};
+    p.mask = MaskDesc{bm->mask_kind, bm->params.window, bm->params.prefix, bm->q_len, bm->params.doc_ids,
+                      bm->q_len, bm->kv_len};
     p.score_kind = score_kind;
     p.score_param = score_param;
     p.scale = scale;
@@ -228,7 +230,7 @@ int flex_block_mask_sizes(int32_t B, int32_t H, int32_t q_len, int32_t kv_len, i
     if (!num_elems || !idx_elems) return FLEX_ERR_INVALID_ARG;
     const int rc = check_sizes(B, H, q_len, kv_len, block);
     if (rc != FLEX_OK) return rc;
-    const int64_t nqb = q_len / block, nkvb = kv_len / block;
+    const int64_t nqb = ceil_blocks(q_len), nkvb = ceil_blocks(kv_len);
     *num_elems = (int64_t)B * H * nqb;
     *idx_elems = (int64_t)B * H * nqb * nkvb;
     return FLEX_OK;
@@ -255,11 +257,11 @@ int flex_block_mask_create(int32_t mask_kind, const flex_mask_params *params, in
     bm->q_len = q_len;
     bm->kv_len = kv_len;
     bm->block = block;
-    bm->nqb = q_len / block;
-    bm->nkvb = kv_len / block;
+    bm->nqb = ceil_blocks(q_len);
+    bm->nkvb = ceil_blocks(kv_len);
     bm->mask_kind = mask_kind;
     bm->params = prm;
-    MaskDesc md{mask_kind, prm.window, prm.prefix, q_len, prm.doc_ids};
+    MaskDesc md{mask_kind, prm.window, prm.prefix, q_len, prm.doc_ids, q_len, kv_len};
     const cudaError_t e = launch_block_mask(md, B, H, q_len, kv_len, bm->kv_num_blocks, bm->kv_indices,
                                             bm->full_kv_num_blocks, bm->full_kv_indices,
                                             static_cast<cudaStream_t>(stream));
@@ -401,8 +403,8 @@ int flex_attention_fwd_host(const flex_tensor *q, const flex_tensor *k, const fl
     bm.q_len = Sq;
     bm.kv_len = Skv;
     bm.block = kBlock;
-    bm.nqb = Sq / kBlock;
-    bm.nkvb = Skv / kBlock;
+    bm.nqb = ceil_blocks(Sq);
+    bm.nkvb = ceil_blocks(Skv);
     bm.mask_kind = mask_kind;
     bm.params = params ? *params : flex_mask_params{0, 0, nullptr};
     bm.params.doc_ids = doc ? dev->doc_ids : nullptr;

@@ -295,11 +295,12 @@ __device__ __forceinline__ uint64_t keep_pair(uint64_t v, bool k0, bool k1) {
 }
 
 // Interval mask_mods (causal, sliding window, causal + prefix, all): the row
-// keeps exactly the kv in [lo, hi].
+// keeps exactly the kv in [lo, hi], and nothing at or past KV_LEN (the zero
+// rows that fill a tail tile).
 __device__ __forceinline__ void apply_interval_mask(const MaskDesc &m, int q, int kv0, uint64_t (&x2)[64]) {
     int lo, hi;
     mask_row_interval(m, q, lo, hi);
-    const int clo = lo - kv0, chi = hi - kv0;
+    const int clo = lo - kv0, chi = min(hi, m.kv_len - 1) - kv0;
 #pragma unroll
     for (int j = 0; j < 64; ++j)
         x2[j] = keep_pair(x2[j], 2 * j >= clo && 2 * j <= chi, 2 * j + 1 >= clo && 2 * j + 1 <= chi);
@@ -597,9 +598,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[s], C::kTileBytes + (with_doc ? 512u : 0u));
+                    // a tail tile's ids end at the length (a multiple of 4, so
+                    // whole 16-byte words); the columns past it are masked
+                    // by causality, since document masks have Q_LEN == KV_LEN
+                    const uint32_t doc_bytes =
+                        with_doc ? 4u * (uint32_t)min(kBlock, p.mask.doc_len - kv0) : 0u;
+                    mbar_arrive_expect_tx(&full[s], C::kTileBytes + doc_bytes);
                     for (int a = 0; a < C::kAtoms; ++a) tma_load_4d(dst + a * C::kAtomBytes, map, &full[s], 64 * a, kv0, h, b);
-                    if (with_doc) bulk_load(ms.stage_doc[s], doc_row + kv0, 512u, &full[s]);
+                    if (with_doc) bulk_load(ms.stage_doc[s], doc_row + kv0, doc_bytes, &full[s]);
                 }
                 // The last K tile of the item is issued once its stage is free,
                 // about one ring depth (kStages steps) before the item ends:
@@ -757,7 +763,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           score.init(p, h);
           int doc_q = 0;
           if constexpr (DOC) {
-              if (valid) doc_q = __ldg(p.mask.doc_ids + (int64_t)b * p.mask.doc_len + q);
+              if (valid && q < p.q_len) doc_q = __ldg(p.mask.doc_ids + (int64_t)b * p.mask.doc_len + q);
           }
           // The running max starts at a finite floor, so a tile whose scores
           // are all masked for this row gives exp2(-inf - floor) = 0 with no
@@ -884,6 +890,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 tc_fence_after_sync();
                 const int64_t orow = bh * p.q_len + q;
                 uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D);
+                const bool store = q < p.q_len;  // rows of a tail tile past Q_LEN are padding
                 const bool live = have && l_run > 0.f;
                 const float inv = live ? 1.f / l_run : 0.f;
 #pragma unroll 1
@@ -899,12 +906,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         pk[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+                    if (store) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        dst[c0 / 8 + j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                        for (int j = 0; j < 4; ++j)
+                            dst[c0 / 8 + j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    }
                 }
-                p.lse[orow] = live ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-                if (p.row_max) p.row_max[orow] = m_max * kLn2;
+                if (store) {
+                    p.lse[orow] = live ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+                    if (p.row_max) p.row_max[orow] = m_max * kLn2;
+                }
             }
           }
           if (nu > 0) {

@@ -11,7 +11,8 @@
 //
 // One CTA per (q block, head, batch); D/64 threads per query row, each owning
 // 64 dims of q and of the accumulator.  K and V tiles are staged in shared
-// memory and read as broadcasts.
+// memory and read as broadcasts.  Rows of a tail tile past the lengths are
+// staged as zeros and masked (kv) or left unwritten (q).
 #include "flex_internal.h"
 
 namespace flex {
@@ -45,14 +46,16 @@ __global__ void __launch_bounds__(Fp32Cfg<D>::kThreads) attn_fp32_kernel(AttnPro
     const int q = qb * kBlock + row;
     const int64_t bhq = ((int64_t)b * p.H + h) * p.nqb + qb;
 
+    const bool row_in = q < p.q_len;  // a tail tile's rows past Q_LEN are padding
     const float *qp = static_cast<const float *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1] +
-                      (int64_t)q * p.q_stride[2] + part * kDimsPerThread;
+                      (int64_t)(row_in ? q : 0) * p.q_stride[2] + part * kDimsPerThread;
     // PRESCALE_QK: q~ = scale q rounded to float once, scores q~.k unscaled
     const float post = p.prescale ? 1.f : p.scale;
     float qr[kDimsPerThread], acc[kDimsPerThread];
 #pragma unroll
     for (int d = 0; d < kDimsPerThread; ++d) {
-        qr[d] = p.prescale ? __fmul_rn(qp[d], p.scale) : qp[d];
+        const float x = row_in ? qp[d] : 0.f;
+        qr[d] = p.prescale ? __fmul_rn(x, p.scale) : x;
         acc[d] = 0.f;
     }
     const float slope = exp2f(-8.f * (float)(h + 1) / (float)p.H);
@@ -71,10 +74,12 @@ __global__ void __launch_bounds__(Fp32Cfg<D>::kThreads) attn_fp32_kernel(AttnPro
         __syncthreads();  // previous tile fully consumed
         for (int i = threadIdx.x; i < kBlock * D / 4; i += C::kThreads) {
             const int r = (i * 4) / D, c = (i * 4) % D;
+            const bool in = kv0 + r < p.kv_len;
             const int64_t ko = (int64_t)(kv0 + r) * p.k_stride[2] + c;
             const int64_t vo = (int64_t)(kv0 + r) * p.v_stride[2] + c;
-            reinterpret_cast<float4 *>(ks)[i] = *reinterpret_cast<const float4 *>(kbase + ko);
-            reinterpret_cast<float4 *>(vs)[i] = *reinterpret_cast<const float4 *>(vbase + vo);
+            const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+            reinterpret_cast<float4 *>(ks)[i] = in ? *reinterpret_cast<const float4 *>(kbase + ko) : zero;
+            reinterpret_cast<float4 *>(vs)[i] = in ? *reinterpret_cast<const float4 *>(vbase + vo) : zero;
         }
         __syncthreads();
 
@@ -89,7 +94,9 @@ __global__ void __launch_bounds__(Fp32Cfg<D>::kThreads) attn_fp32_kernel(AttnPro
                 if constexpr (C::kTpr == 2) dot += __shfl_xor_sync(0xffffffffu, dot, 1);
                 const int kv = kv0 + c0 + j;
                 float x = score_mod_f32(p.score_kind, p.score_param, dot * post, slope, q, kv);
-                if (!full && !mask_mod(p.mask, b, q, kv)) x = -INFINITY;
+                // tail tiles are never full; columns past KV_LEN are
+                // masked before mask_mod could read a document id there
+                if (!full && (kv >= p.kv_len || !row_in || !mask_mod(p.mask, b, q, kv))) x = -INFINITY;
                 s[j] = x;
             }
             float cmax = s[0];
@@ -114,6 +121,7 @@ __global__ void __launch_bounds__(Fp32Cfg<D>::kThreads) attn_fp32_kernel(AttnPro
     }
 
     float *op = static_cast<float *>(p.out) + (((int64_t)b * p.H + h) * p.q_len + q) * D + part * kDimsPerThread;
+    if (!row_in) return;
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
     for (int d = 0; d < kDimsPerThread; d += 4)

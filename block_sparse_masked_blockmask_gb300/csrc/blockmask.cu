@@ -14,6 +14,8 @@
 //    empty; a tile below it whose 256 row and column ids are one id is full;
 //    disjoint id ranges are empty), otherwise mask_mod is evaluated on all
 //    16384 pairs, so arbitrary ids stay exact.
+// Lengths need not be multiples of 128: positions past Q_LEN or KV_LEN are
+// padding and count as masked, so a tile reaching past either is never full.
 // None of the enumerated mask_mods depends on the head, so a row is
 // classified once and written for every head.  Index rows hold the selected kv
 // blocks in ascending order followed by the remaining kv blocks ascending.
@@ -29,16 +31,20 @@ constexpr int kBmWarps = kBmThreads / 32;
 
 enum : uint8_t { kEmpty = 0, kPartial = 1, kFull = 2 };
 
-// Interval kinds: lane `lane` tests rows lane + 32 j of the tile.
+// Interval kinds: lane `lane` tests rows lane + 32 j of the tile; a row's
+// interval ends at KV_LEN - 1, and rows past Q_LEN keep nothing.
 __device__ __forceinline__ uint8_t classify_interval_tile(const MaskDesc &m, int q0, int kv0, int lane) {
     bool any = false, all = true;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
+        const int q = q0 + lane + 32 * j;
         int lo, hi;
-        mask_row_interval(m, q0 + lane + 32 * j, lo, hi);
+        mask_row_interval(m, q, lo, hi);
+        hi = min(hi, m.kv_len - 1);
+        const bool row = q < m.q_len;
         const int a = max(lo, kv0), e = min(hi, kv0 + kBlock - 1);
-        any |= a <= e;
-        all &= lo <= kv0 && hi >= kv0 + kBlock - 1;
+        any |= row && a <= e;
+        all &= row && lo <= kv0 && hi >= kv0 + kBlock - 1;
     }
     any = __any_sync(0xffffffffu, any);
     all = __all_sync(0xffffffffu, all);
@@ -46,17 +52,22 @@ __device__ __forceinline__ uint8_t classify_interval_tile(const MaskDesc &m, int
 }
 
 // Document kind: quick exact decisions, else every (q, kv) pair of the tile.
+// Ids are read only inside the lengths; padding rows and columns keep nothing.
 __device__ __forceinline__ uint8_t classify_document_tile(const MaskDesc &m, int b, int qb, int kvb, int lane,
                                                           const int32_t *row_doc, int row_min, int row_max) {
     if (kvb > qb) return kEmpty;  // every kv of the tile is above every q: kv > q
     const int kv0 = kvb * kBlock;
+    const int q0 = qb * kBlock;
     int col_doc[4];
     int cmin = INT_MAX, cmax = INT_MIN;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        col_doc[j] = m.doc_ids[(int64_t)b * m.doc_len + kv0 + lane + 32 * j];
-        cmin = min(cmin, col_doc[j]);
-        cmax = max(cmax, col_doc[j]);
+        const int kv = kv0 + lane + 32 * j;
+        col_doc[j] = kv < m.kv_len ? m.doc_ids[(int64_t)b * m.doc_len + kv] : 0;
+        if (kv < m.kv_len) {
+            cmin = min(cmin, col_doc[j]);
+            cmax = max(cmax, col_doc[j]);
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -64,14 +75,15 @@ __device__ __forceinline__ uint8_t classify_document_tile(const MaskDesc &m, int
         cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
     }
     if (cmax < row_min || cmin > row_max) return kEmpty;  // no id in common
-    if (kvb < qb && cmin == cmax && row_min == row_max && cmin == row_min) return kFull;
-    const int q0 = qb * kBlock;
+    const bool whole = q0 + kBlock <= m.q_len && kv0 + kBlock <= m.kv_len;
+    if (whole && kvb < qb && cmin == cmax && row_min == row_max && cmin == row_min) return kFull;
     bool any = false, all = true;
     for (int r = 0; r < kBlock; ++r) {
         const int q = q0 + r;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const bool keep = q >= kv0 + lane + 32 * j && row_doc[r] == col_doc[j];
+            const int kv = kv0 + lane + 32 * j;
+            const bool keep = q < m.q_len && kv < m.kv_len && q >= kv && row_doc[r] == col_doc[j];
             any |= keep;
             all &= keep;
         }
@@ -126,6 +138,10 @@ __global__ void __launch_bounds__(kBmThreads) block_mask_kernel(MaskDesc m, int 
         }
         __syncthreads();
         for (int r = threadIdx.x; r < kBlock; r += kBmThreads) {
+            if (q0 + r >= m.q_len) {  // padding row
+                row_doc[r] = 0;
+                continue;
+            }
             const int d = m.doc_ids[(int64_t)b * m.doc_len + q0 + r];
             row_doc[r] = d;
             atomicMin(&row_range[0], d);
@@ -169,7 +185,7 @@ __global__ void __launch_bounds__(kBmThreads) block_mask_kernel(MaskDesc m, int 
 
 cudaError_t launch_block_mask(const MaskDesc &mask, int B, int H, int q_len, int kv_len, int32_t *kv_num,
                               int32_t *kv_idx, int32_t *full_num, int32_t *full_idx, cudaStream_t stream) {
-    const int nqb = q_len / kBlock, nkvb = kv_len / kBlock;
+    const int nqb = ceil_blocks(q_len), nkvb = ceil_blocks(kv_len);
     const dim3 grid(nqb, B), block(kBmThreads);
     switch (mask.kind) {
         case FLEX_MASK_CAUSAL:

@@ -21,7 +21,11 @@ struct MaskDesc {
     int32_t prefix;
     int32_t doc_len;            // row length of doc_ids (== q_len == kv_len)
     const int32_t *doc_ids;     // [B, doc_len]
+    int32_t q_len, kv_len;      // positions at or past these are padding: masked
 };
+
+// Tiles along a length: the last one may reach past it (padding, masked).
+__host__ __device__ constexpr int ceil_blocks(int64_t len) { return (int)((len + kBlock - 1) / kBlock); }
 
 // mask_mod(b, h, q, kv) for the enumerated kinds.  No kind depends on h.
 __host__ __device__ __forceinline__ bool mask_mod(const MaskDesc &m, int b, int q, int kv) {

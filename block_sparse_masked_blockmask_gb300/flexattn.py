@@ -168,7 +168,7 @@ def flex_block_mask_create(mask_kind: int, B: int, H: int, q_len: int, kv_len: i
     device = torch.device(device) if device is not None else (
         doc_ids.device if doc_ids is not None else torch.device("cuda", torch.cuda.current_device()))
     n_num, n_idx = flex_block_mask_sizes(B, H, q_len, kv_len, block)
-    nqb, nkvb = q_len // block, kv_len // block
+    nqb, nkvb = -(-q_len // block), -(-kv_len // block)  # a tail tile may reach past a length
     t = {
         "kv_num_blocks": torch.empty((B, H, nqb), dtype=torch.int32, device=device),
         "kv_indices": torch.empty((B, H, nqb, nkvb), dtype=torch.int32, device=device),
@@ -310,7 +310,7 @@ class DeviceBuffers:
         self.out = torch.empty((B, H, q_len, D), dtype=dtype, device=device)
         self.lse = torch.empty((B, H, q_len), dtype=torch.float32, device=device)
         self.doc_ids = torch.empty((B, q_len), dtype=torch.int32, device=device) if document else None
-        nqb, nkvb = q_len // 128, kv_len // 128
+        nqb, nkvb = -(-q_len // 128), -(-kv_len // 128)
         self.kv_num_blocks = torch.empty((B, H, nqb), dtype=torch.int32, device=device)
         self.kv_indices = torch.empty((B, H, nqb, nkvb), dtype=torch.int32, device=device)
         self.full_kv_num_blocks = torch.empty((B, H, nqb), dtype=torch.int32, device=device)

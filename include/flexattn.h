@@ -38,7 +38,9 @@
  *  - The library allocates one small per-device workspace (the status word)
  *    with cudaMalloc the first time a device is used; call any entry point
  *    once before capturing a stream into a CUDA graph.
- *  - Indices and counts are int32.  Lengths must be multiples of BLOCK = 128.
+ *  - Indices and counts are int32.  Lengths are any positive int32 (KV_LEN
+ *    up to 1024 * BLOCK): the last tile along a length may reach past it,
+ *    and the positions past a length count as masked.
  */
 #ifndef FLEXATTN_H
 #define FLEXATTN_H
@@ -59,7 +61,7 @@ typedef enum {
     FLEX_OK = 0,
     FLEX_ERR_INVALID_ARG = -1,     /* null pointer, bad enum, bad scale/parameter            */
     FLEX_ERR_UNSUPPORTED = -2,     /* head dim, dtype or size outside what the kernels cover  */
-    FLEX_ERR_SHAPE = -3,           /* shapes disagree or lengths are not multiples of BLOCK   */
+    FLEX_ERR_SHAPE = -3,           /* shapes or BlockMask sizes disagree                      */
     FLEX_ERR_ALIGNMENT = -4,       /* pointer or stride not 16-byte aligned / inner stride!=1 */
     FLEX_ERR_CUDA = -5,            /* a CUDA runtime/driver call failed                       */
     FLEX_ERR_DEVICE_TIMEOUT = -6   /* a kernel gave up on a wait (reported by status word)    */
@@ -99,6 +101,10 @@ typedef struct {
  *   full     the mask_mod is true on the whole tile  -> listed in full_kv_*
  *   partial  true on some of the tile                -> listed in kv_*
  *   empty    true nowhere                            -> listed in neither
+ * NQB = ceil(Q_LEN / BLOCK), NKVB = ceil(KV_LEN / BLOCK).  Positions past
+ * Q_LEN or KV_LEN count as masked (the mask padded with false to whole
+ * tiles), so a tile reaching past either length is never full; the
+ * attention kernels rely on that to bound the tail tiles.
  * kv_num_blocks[b,h,qb] counts the partial tiles; kv_indices[b,h,qb,:] holds
  * their kv-block indices in ascending order followed by all other kv-block
  * indices in ascending order, so each row is a permutation of 0..NKVB-1.
@@ -130,8 +136,7 @@ typedef struct {
  * *num_elems = B*H*NQB (each of kv_num_blocks, full_kv_num_blocks),
  * *idx_elems = B*H*NQB*NKVB (each of kv_indices, full_kv_indices).
  * Errors: FLEX_ERR_INVALID_ARG (null outputs, non-positive sizes),
- * FLEX_ERR_SHAPE (lengths not multiples of block), FLEX_ERR_UNSUPPORTED
- * (block != 128).
+ * FLEX_ERR_UNSUPPORTED (block != 128, or KV_LEN > 1024 * 128).
  */
 FLEX_API int flex_block_mask_sizes(int32_t B, int32_t H, int32_t q_len, int32_t kv_len, int32_t block,
                           int64_t *num_elems, int64_t *idx_elems);
@@ -164,6 +169,8 @@ FLEX_API int flex_block_mask_create(int32_t mask_kind, const flex_mask_params *p
  * and a row with no unmasked score gets out = 0, lse = -inf.
  *   q    : [B, H, q_len, D];  k, v : [B, H, kv_len, D]; same dtype, B, H, D.
  *          D in {64, 128}.  bf16 needs 16-byte-aligned base and strides.
+ *          Document masks need Q_LEN (== KV_LEN) a multiple of 4 (each
+ *          tile's ids are copied in whole 16-byte words).
  *   bm   : a BlockMask for (B, H, q_len, kv_len) from flex_block_mask_create.
  *   score_kind, score_param : flex_score_kind and the softcap value.
  *   scale: multiplies q.k before score_mod (finite).

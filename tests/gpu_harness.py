@@ -42,13 +42,22 @@ def run_attention(q, k, v, mask, score, scale, dtype, window=0, prefix=0, doc_id
     return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), bm
 
 
-def compare(out, lse, ref_out, ref_lse, dtype, what="", tol=None):
+def compare(out, lse, ref_out, ref_lse, dtype, what="", tol=None, ref_abs=None):
     """Element-wise max-abs check; -inf LSE (empty rows) must match exactly.
 
     tol: (out, lse) tolerances in place of the dtype's, for inputs outside
     the N(0, 1) draws those were set for.
+    ref_abs (bf16 only): the oracle's out for |V| (same scores and mask).  The
+    tensor-core path rounds P to bf16 for P V (relative error <= 2^-9 per
+    weight, with the row sum taken from the unrounded weights) and rounds
+    out to bf16, so element d may be off by 2^-9 (sum_j p_j |v_jd| / l +
+    |out_d|).  Over many keys these roundings average out far below 1e-2;
+    on a row with a handful of keys (a two-token document) they need not,
+    and there the element's bound replaces 1e-2 when it is larger.
     """
     tol_out, tol_lse = TOL[dtype] if tol is None else tol
+    if ref_abs is not None and dtype == "bf16":
+        tol_out = np.maximum(tol_out, 2.0**-9 * (np.asarray(ref_abs) + np.abs(ref_out)))
     assert out.shape == ref_out.shape and lse.shape == ref_lse.shape
     assert np.all(np.isfinite(out)), f"{what}: non-finite output"
     empty = np.isneginf(ref_lse)
@@ -56,9 +65,15 @@ def compare(out, lse, ref_out, ref_lse, dtype, what="", tol=None):
     assert np.all(np.isfinite(lse[~empty])), f"{what}: non-finite lse"
     if empty.any():
         assert np.all(out[empty] == 0.0), f"{what}: empty rows must be 0"
-    err_o = float(np.max(np.abs(out - ref_out))) if out.size else 0.0
     err_l = float(np.max(np.abs(lse[~empty] - ref_lse[~empty]))) if (~empty).any() else 0.0
-    assert err_o <= tol_out, f"{what}: out max-abs {err_o:.3e} > {tol_out:.0e}"
+    if np.ndim(tol_out):
+        over = np.abs(out - ref_out) - tol_out
+        worst = float(np.max(over)) if out.size else -1.0
+        assert worst <= 0.0, f"{what}: out exceeds its per-element bound by {worst:.3e}"
+        err_o = float(np.max(np.abs(out - ref_out))) if out.size else 0.0
+    else:
+        err_o = float(np.max(np.abs(out - ref_out))) if out.size else 0.0
+        assert err_o <= tol_out, f"{what}: out max-abs {err_o:.3e} > {tol_out:.0e}"
     assert err_l <= tol_lse, f"{what}: lse max-abs {err_l:.3e} > {tol_lse:.0e}"
     return err_o, err_l
 

@@ -44,10 +44,14 @@ def test_status_strings(lib):
 def test_block_mask_sizes(lib):
     assert fa.flex_block_mask_sizes(2, 32, 16384, 16384) == (2 * 32 * 128, 2 * 32 * 128 * 128)
     assert fa.flex_block_mask_sizes(1, 1, 128, 384) == (1, 3)
+    # lengths need not be multiples of the block: the tail tile is counted
+    assert fa.flex_block_mask_sizes(1, 1, 100, 128) == (1, 1)
+    assert fa.flex_block_mask_sizes(2, 3, 129, 300) == (2 * 3 * 2, 2 * 3 * 2 * 3)
+    assert fa.flex_block_mask_sizes(1, 1, 1, 128 * 1024) == (1, 1024)
     for args, code in [((0, 1, 128, 128), fa.FLEX_ERR_INVALID_ARG),
-                       ((1, 1, 100, 128), fa.FLEX_ERR_SHAPE),
-                       ((1, 1, 128, 130), fa.FLEX_ERR_SHAPE),
+                       ((1, 1, 0, 128), fa.FLEX_ERR_INVALID_ARG),
                        ((1, 1, 128, 128, 64), fa.FLEX_ERR_UNSUPPORTED),
+                       ((1, 1, 128, 128 * 1024 + 1), fa.FLEX_ERR_UNSUPPORTED),
                        ((1, 1, 128, 128 * 1025), fa.FLEX_ERR_UNSUPPORTED)]:
         with pytest.raises(fa.FlexError) as e:
             fa.flex_block_mask_sizes(*args)
@@ -65,7 +69,7 @@ def _call_create(lib, kind, params, B=1, H=1, q=256, kv=256, block=128, buffers=
 def test_block_mask_create_rejects_bad_arguments(lib):
     assert _call_create(lib, 7, None) == fa.FLEX_ERR_INVALID_ARG
     assert _call_create(lib, fa.FLEX_MASK_CAUSAL, None, buffers=False) == fa.FLEX_ERR_INVALID_ARG
-    assert _call_create(lib, fa.FLEX_MASK_CAUSAL, None, q=200) == fa.FLEX_ERR_SHAPE
+    assert _call_create(lib, fa.FLEX_MASK_CAUSAL, None, q=-200) == fa.FLEX_ERR_INVALID_ARG
     assert _call_create(lib, fa.FLEX_MASK_CAUSAL, None, block=64) == fa.FLEX_ERR_UNSUPPORTED
     assert _call_create(lib, fa.FLEX_MASK_SLIDING_WINDOW, None) == fa.FLEX_ERR_INVALID_ARG
     assert _call_create(lib, fa.FLEX_MASK_SLIDING_WINDOW, fa.flex_mask_params(-1, 0, None)) == \
@@ -91,8 +95,14 @@ def _tensor(dtype, shape, stride=None, data=0x10000):
 def _mask_struct(B=1, H=2, q=256, kv=256, kind=fa.FLEX_MASK_CAUSAL):
     bm = fa.flex_block_mask()
     bm.B, bm.H, bm.q_len, bm.kv_len, bm.block = B, H, q, kv, 128
-    bm.nqb, bm.nkvb, bm.mask_kind = q // 128, kv // 128, kind
+    bm.nqb, bm.nkvb, bm.mask_kind = -(-q // 128), -(-kv // 128), kind
     bm.kv_num_blocks = bm.kv_indices = bm.full_kv_num_blocks = bm.full_kv_indices = 0x1000
+    return bm
+
+
+def _doc_mask_struct(S):
+    bm = _mask_struct(q=S, kv=S, kind=fa.FLEX_MASK_DOCUMENT)
+    bm.params.doc_ids = 0x4000
     return bm
 
 
@@ -121,7 +131,11 @@ def test_attention_rejects_bad_arguments(lib):
         (dict(bm=_mask_struct(H=3)), fa.FLEX_ERR_SHAPE),
         (dict(bm=_mask_struct(q=384, kv=384)), fa.FLEX_ERR_SHAPE),
         (dict(bm=_mask_struct(kind=9)), fa.FLEX_ERR_INVALID_ARG),
-        (dict(q=_tensor(bf, [1, 2, 200, 64]), bm=_mask_struct(q=200)), fa.FLEX_ERR_SHAPE),
+        (dict(q=_tensor(bf, [1, 2, 200, 64])), fa.FLEX_ERR_SHAPE),  # the BlockMask is for 256 rows
+        (dict(bm=_mask_struct(q=256, kv=200)), fa.FLEX_ERR_SHAPE),  # ... or for 200 kv rows
+        # document masks need Q_LEN a multiple of 4
+        (dict(q=_tensor(bf, [1, 2, 202, 64]), k=_tensor(bf, [1, 2, 202, 64]), v=_tensor(bf, [1, 2, 202, 64]),
+              bm=_doc_mask_struct(202)), fa.FLEX_ERR_UNSUPPORTED),
     ]
     for change, code in cases:
         args = dict(q=q, k=_tensor(bf, [1, 2, 256, 64]), v=_tensor(bf, [1, 2, 256, 64]), bm=bm)
@@ -168,7 +182,8 @@ def test_host_entry_point_rejects_bad_arguments(lib):
     assert call(kind=9) == fa.FLEX_ERR_INVALID_ARG
     assert call(kind=fa.FLEX_MASK_SLIDING_WINDOW) == fa.FLEX_ERR_INVALID_ARG  # needs params
     assert call(kind=fa.FLEX_MASK_DOCUMENT, params=fa.flex_mask_params(0, 0, 0x1000)) == fa.FLEX_ERR_INVALID_ARG
-    assert call(q=_tensor(bf, [1, 2, 200, 64])) == fa.FLEX_ERR_SHAPE
+    assert call(q=_tensor(bf, [1, 2, 200, 64], stride=[1, 1, 1, 1])) == fa.FLEX_ERR_INVALID_ARG  # not contiguous
+    assert call(k=_tensor(bf, [1, 3, 256, 64])) == fa.FLEX_ERR_SHAPE
     assert call(score=7) == fa.FLEX_ERR_INVALID_ARG
     unaligned = fa.flex_device_buffers.from_buffer_copy(dev)
     unaligned.out = 0x40008
