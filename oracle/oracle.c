@@ -32,6 +32,13 @@
  *                    scale * q is rounded once to the inputs' storage type
  *                    (bfloat16 or float32, ties to even) and the scores are
  *                    score_mod(q~ . k) with no further scale.
+ *   backward             -> dq, dk, dv      the gradients of sum(dO * out)
+ *       (the flex_attention_backward op of the same PR's tests, which takes
+ *       the forward's out, lse and the output gradient and returns the
+ *       three gradients), written out as the softmax-attention chain rule;
+ *       the q side of the BlockMask (q_num_blocks, q_indices, ...), which
+ *       the same tuple carries for that pass, as the transpose of the kv
+ *       side.
  *   block mask           -> kv_num_blocks, kv_indices, full_kv_num_blocks,
  *       full_kv_indices   (the BlockMask tuple passed to the same op): each
  *       BLOCK x BLOCK tile of the dense mask is full (all true), partial
@@ -219,6 +226,64 @@ int oracle_block_mask(int kind, int window, int prefix, const int32_t *doc,
 }
 
 /*
+ * The q side of the BlockMask tuple (q_num_blocks, q_indices,
+ * full_q_num_blocks, full_q_indices), read by the backward pass: for every
+ * kv block j, the q blocks whose kv-side partial (full) list holds j, in
+ * ascending order, followed by the other q blocks ascending.  Output layouts:
+ *   q_num, full_q_num : [B, H, NKVB]
+ *   q_idx, full_q_idx : [B, H, NKVB, NQB]
+ */
+int oracle_block_mask_q(int kind, int window, int prefix, const int32_t *doc,
+                        int B, int H, int q_len, int kv_len, int block,
+                        int32_t *q_num, int32_t *q_idx, int32_t *full_q_num, int32_t *full_q_idx)
+{
+    if (block <= 0 || q_len <= 0 || kv_len <= 0 || B <= 0 || H <= 0)
+        return OR_ERR_ARG;
+    const int64_t nqb = ((int64_t)q_len + block - 1) / block;
+    const int64_t nkvb = ((int64_t)kv_len + block - 1) / block;
+    const int64_t rows = (int64_t)B * H * nqb;
+    int32_t *kn = (int32_t *)malloc((size_t)rows * sizeof(int32_t));
+    int32_t *ki = (int32_t *)malloc((size_t)(rows * nkvb) * sizeof(int32_t));
+    int32_t *fn = (int32_t *)malloc((size_t)rows * sizeof(int32_t));
+    int32_t *fi = (int32_t *)malloc((size_t)(rows * nkvb) * sizeof(int32_t));
+    unsigned char *st = (unsigned char *)calloc((size_t)(nqb * nkvb), 1);
+    int err = (kn && ki && fn && fi && st) ? OR_OK : OR_ERR_NOMEM;
+    if (err == OR_OK)
+        err = oracle_block_mask(kind, window, prefix, doc, B, H, q_len, kv_len, block, kn, ki, fn, fi);
+    for (int64_t bh = 0; err == OR_OK && bh < (int64_t)B * H; ++bh) {
+        /* tile classes of this (b, h) from its kv-side lists: 1 partial, 2 full */
+        memset(st, 0, (size_t)(nqb * nkvb));
+        for (int64_t i = 0; i < nqb; ++i) {
+            const int64_t row = bh * nqb + i;
+            for (int32_t t = 0; t < kn[row]; ++t) st[i * nkvb + ki[row * nkvb + t]] = 1;
+            for (int32_t t = 0; t < fn[row]; ++t) st[i * nkvb + fi[row * nkvb + t]] = 2;
+        }
+        for (int64_t j = 0; j < nkvb; ++j) {
+            const int64_t col = bh * nkvb + j;
+            int32_t *pq = q_idx + col * nqb, *fq = full_q_idx + col * nqb;
+            int32_t np = 0, nf = 0;
+            for (int64_t i = 0; i < nqb; ++i) {
+                if (st[i * nkvb + j] == 1) pq[np++] = (int32_t)i;
+                if (st[i * nkvb + j] == 2) fq[nf++] = (int32_t)i;
+            }
+            q_num[col] = np;
+            full_q_num[col] = nf;
+            int32_t tp = np, tf = nf;
+            for (int64_t i = 0; i < nqb; ++i) {
+                if (st[i * nkvb + j] != 1) pq[tp++] = (int32_t)i;
+                if (st[i * nkvb + j] != 2) fq[tf++] = (int32_t)i;
+            }
+        }
+    }
+    free(kn);
+    free(ki);
+    free(fn);
+    free(fi);
+    free(st);
+    return err;
+}
+
+/*
  * One output row (b, h, i):
  *   S[j] = mask_mod(b,h,i,j) ? score_mod(scale * sum_d q[i,d] k[j,d]) : -inf
  *          (PRESCALE_QK: score_mod(sum_d q~[i,d] k[j,d]), q~ = round(scale q))
@@ -327,6 +392,123 @@ int oracle_attention_opts(const float *q, const float *k, const float *v,
         free(srow);
         free(qrow);
         free(mrow);
+    }
+    return err;
+}
+
+/* d score_mod / dt at the scaled score t */
+static double or_score_grad(int kind, double param, double t)
+{
+    if (kind == OR_SCORE_SOFTCAP) {
+        const double u = tanh(t / param);
+        return 1.0 - u * u;
+    }
+    return 1.0;  /* identity; ALiBi adds a term that does not depend on t */
+}
+
+/*
+ * Backward pass: the gradients of L = sum_{i,d} dO[i,d] out[i,d] with
+ * respect to q, k and v, for out as oracle_attention defines it.  Per (b, h),
+ * with t_ij = scale q_i.k_j, S_ij = score_mod(t_ij) where mask_mod holds
+ * (else -inf), P_ij = exp(S_ij - lse_i) (0 on a row with no unmasked score):
+ *   dV_j = sum_i P_ij dO_i
+ *   dP_ij = dO_i . v_j,   D_i = dO_i . out_i = sum_j P_ij dP_ij
+ *   dS_ij = P_ij (dP_ij - D_i)          (softmax rows)
+ *   dT_ij = dS_ij score_mod'(t_ij)
+ *   dQ_i = scale sum_j dT_ij k_j,   dK_j = scale sum_i dT_ij q_i
+ * q, k, v, dout: float32 [B, H, S, D]; dq [B, H, s_q, D], dk, dv
+ * [B, H, s_kv, D] in double.  One (b, h) per thread; memory O(s_kv + D).
+ */
+int oracle_attention_bwd(const float *q, const float *k, const float *v, const float *dout,
+                         int B, int H, int s_q, int s_kv, int D,
+                         int mask_kind, int window, int prefix, const int32_t *doc,
+                         int score_kind, double score_param, double scale,
+                         double *dq, double *dk, double *dv)
+{
+    if (!or_mask_ok(mask_kind) || B <= 0 || H <= 0 || s_q <= 0 || s_kv <= 0 || D <= 0)
+        return OR_ERR_ARG;
+    if (score_kind < OR_SCORE_IDENTITY || score_kind > OR_SCORE_ALIBI)
+        return OR_ERR_ARG;
+    if (mask_kind == OR_MASK_DOCUMENT && (doc == NULL || s_q != s_kv))
+        return OR_ERR_ARG;
+    if (score_kind == OR_SCORE_SOFTCAP && !(score_param > 0.0))
+        return OR_ERR_ARG;
+    or_mask m = {mask_kind, window, prefix, doc, (int64_t)s_q};
+    int err = OR_OK;
+    memset(dk, 0, sizeof(double) * (size_t)B * H * s_kv * D);
+    memset(dv, 0, sizeof(double) * (size_t)B * H * s_kv * D);
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < (int64_t)B * H; ++bh) {
+        const int64_t b = bh / H, h = bh % H;
+        const float *qb = q + bh * s_q * D, *kb = k + bh * s_kv * D, *vb = v + bh * s_kv * D;
+        const float *gb = dout + bh * s_q * D;
+        double *dqb = dq + bh * s_q * D, *dkb = dk + bh * s_kv * D, *dvb = dv + bh * s_kv * D;
+        double *t = (double *)malloc((size_t)s_kv * sizeof(double));
+        double *pr = (double *)malloc((size_t)s_kv * sizeof(double));
+        double *o = (double *)malloc((size_t)D * sizeof(double));
+        unsigned char *mk = (unsigned char *)malloc((size_t)s_kv);
+        if (!t || !pr || !o || !mk) {
+#pragma omp atomic write
+            err = OR_ERR_NOMEM;
+            free(t); free(pr); free(o); free(mk);
+            continue;
+        }
+        for (int64_t i = 0; i < s_q; ++i) {
+            double *dqi = dqb + i * D;
+            for (int64_t d = 0; d < D; ++d)
+                dqi[d] = 0.0;
+            /* scores and the softmax of row i */
+            int any = 0;
+            double mx = -INFINITY;
+            for (int64_t j = 0; j < s_kv; ++j) {
+                double dot = 0.0;
+                for (int64_t d = 0; d < D; ++d)
+                    dot += (double)qb[i * D + d] * (double)kb[j * D + d];
+                t[j] = scale * dot;
+                mk[j] = (unsigned char)or_mask_mod(&m, b, h, i, j);
+                if (mk[j]) {
+                    any = 1;
+                    const double sij = or_score_mod(score_kind, score_param, t[j], h, H, i, j);
+                    pr[j] = sij;
+                    if (sij > mx) mx = sij;
+                }
+            }
+            if (!any) continue;  /* P = 0: the row contributes nothing */
+            double Z = 0.0;
+            for (int64_t j = 0; j < s_kv; ++j)
+                if (mk[j]) Z += exp(pr[j] - mx);
+            const double lse = mx + log(Z);
+            for (int64_t j = 0; j < s_kv; ++j)
+                pr[j] = mk[j] ? exp(pr[j] - lse) : 0.0;
+            /* out_i and D_i */
+            for (int64_t d = 0; d < D; ++d)
+                o[d] = 0.0;
+            for (int64_t j = 0; j < s_kv; ++j)
+                if (mk[j])
+                    for (int64_t d = 0; d < D; ++d)
+                        o[d] += pr[j] * (double)vb[j * D + d];
+            double Di = 0.0;
+            for (int64_t d = 0; d < D; ++d)
+                Di += (double)gb[i * D + d] * o[d];
+            for (int64_t j = 0; j < s_kv; ++j) {
+                if (!mk[j]) continue;
+                double dp = 0.0;
+                for (int64_t d = 0; d < D; ++d)
+                    dp += (double)gb[i * D + d] * (double)vb[j * D + d];
+                const double ds = pr[j] * (dp - Di);
+                const double dt = ds * or_score_grad(score_kind, score_param, t[j]);
+                for (int64_t d = 0; d < D; ++d) {
+                    dvb[j * D + d] += pr[j] * (double)gb[i * D + d];
+                    dqi[d] += scale * dt * (double)kb[j * D + d];
+                    dkb[j * D + d] += scale * dt * (double)qb[i * D + d];
+                }
+            }
+        }
+        free(t);
+        free(pr);
+        free(o);
+        free(mk);
     }
     return err;
 }

@@ -63,6 +63,11 @@ class Oracle:
         lib.oracle_attention_opts.argtypes = [f32p, f32p, f32p, I, I, I, I, I, I, I, I, i32p,
                                               I, D, D, I, i64p, L, f64p, f64p, f64p]
         lib.oracle_attention_opts.restype = I
+        lib.oracle_block_mask_q.argtypes = [I, I, I, i32p, I, I, I, I, I, i32p, i32p, i32p, i32p]
+        lib.oracle_block_mask_q.restype = I
+        lib.oracle_attention_bwd.argtypes = [f32p, f32p, f32p, f32p, I, I, I, I, I, I, I, I, i32p,
+                                             I, D, D, f64p, f64p, f64p]
+        lib.oracle_attention_bwd.restype = I
         lib.oracle_round_bf16.argtypes = [D]
         lib.oracle_round_bf16.restype = D
         lib.oracle_mask_value.argtypes = [I, I, I, i32p, L, L, L, L, L]
@@ -160,6 +165,45 @@ class Oracle:
             raise ValueError(f"oracle_attention_opts failed with {rc}")
         return out, lse, row_max
 
+    def block_mask_q(self, kind: int, B: int, H: int, q_len: int, kv_len: int, block: int = 128,
+                     window: int = 0, prefix: int = 0, doc_ids=None) -> dict:
+        """q_num_blocks, q_indices, full_q_num_blocks, full_q_indices (int32): the transposed lists."""
+        nqb, nkvb = -(-q_len // block), -(-kv_len // block)
+        out = {
+            "q_num_blocks": np.zeros((B, H, nkvb), np.int32),
+            "q_indices": np.zeros((B, H, nkvb, nqb), np.int32),
+            "full_q_num_blocks": np.zeros((B, H, nkvb), np.int32),
+            "full_q_indices": np.zeros((B, H, nkvb, nqb), np.int32),
+        }
+        doc = None if doc_ids is None else np.ascontiguousarray(doc_ids, dtype=np.int32)
+        rc = self.lib.oracle_block_mask_q(kind, window, prefix, _ptr(doc, ctypes.c_int32), B, H, q_len, kv_len,
+                                          block, _ptr(out["q_num_blocks"], ctypes.c_int32),
+                                          _ptr(out["q_indices"], ctypes.c_int32),
+                                          _ptr(out["full_q_num_blocks"], ctypes.c_int32),
+                                          _ptr(out["full_q_indices"], ctypes.c_int32))
+        if rc != 0:
+            raise ValueError(f"oracle_block_mask_q failed with {rc}")
+        return out
+
+    def attention_bwd(self, q, k, v, dout, mask_kind: int, score_kind: int, scale: float, window: int = 0,
+                      prefix: int = 0, doc_ids=None, score_param: float = 0.0):
+        """(dq, dk, dv) float64: the gradients of sum(dout * out) for out = attention(q, k, v)."""
+        q, k, v, dout = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k, v, dout))
+        B, H, s_q, D = q.shape
+        s_kv = k.shape[2]
+        doc = None if doc_ids is None else np.ascontiguousarray(doc_ids, dtype=np.int32)
+        dq = np.zeros((B, H, s_q, D), np.float64)
+        dk = np.zeros((B, H, s_kv, D), np.float64)
+        dv = np.zeros((B, H, s_kv, D), np.float64)
+        rc = self.lib.oracle_attention_bwd(_ptr(q, ctypes.c_float), _ptr(k, ctypes.c_float),
+                                           _ptr(v, ctypes.c_float), _ptr(dout, ctypes.c_float), B, H, s_q, s_kv,
+                                           D, mask_kind, window, prefix, _ptr(doc, ctypes.c_int32), score_kind,
+                                           float(score_param), float(scale), _ptr(dq, ctypes.c_double),
+                                           _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double))
+        if rc != 0:
+            raise ValueError(f"oracle_attention_bwd failed with {rc}")
+        return dq, dk, dv
+
     def round_bf16(self, x: float) -> float:
         return float(self.lib.oracle_round_bf16(float(x)))
 
@@ -210,6 +254,14 @@ def mask_value(*a, **kw):
 
 def attention_opts(*a, **kw):
     return default().attention_opts(*a, **kw)
+
+
+def attention_bwd(*a, **kw):
+    return default().attention_bwd(*a, **kw)
+
+
+def block_mask_q(*a, **kw):
+    return default().block_mask_q(*a, **kw)
 
 
 def num_threads() -> int:

@@ -532,6 +532,128 @@ def pin_row_max_bounds_lse(orc):
     assert np.all(np.isneginf(m0)) and np.all(np.isneginf(l0)) and np.all(o0 == 0.0), "W=0 rows"
 
 
+# ------------------------------------------------------------------ backward
+def _dense_mask(kind, B, S, window=0, prefix=0, doc=None):
+    i = np.arange(S)[:, None]
+    j = np.arange(S)[None, :]
+    if kind == W.MASK_CAUSAL:
+        m = i >= j
+    elif kind == W.MASK_SLIDING_WINDOW:
+        m = (i >= j) & (i - j < window)
+    elif kind == W.MASK_CAUSAL_PREFIX:
+        m = ((i <= prefix) & (j <= prefix)) | (i >= j)
+    elif kind == W.MASK_DOCUMENT:
+        return np.stack([(doc[b][:, None] == doc[b][None, :]) & (i >= j) for b in range(B)])[:, None]
+    else:
+        m = np.ones((S, S), bool)
+    return np.broadcast_to(m, (B, 1, S, S))
+
+
+def _sdpa_grads(q, k, v, dout, scale, attn_mask):
+    """(dq, dk, dv) of sum(dout * out) through PyTorch's float64 CPU attention (autograd)."""
+    tq, tk, tv = (torch.tensor(np.asarray(x, np.float64), requires_grad=True) for x in (q, k, v))
+    out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=attn_mask, scale=scale)
+    out.backward(torch.tensor(np.asarray(dout, np.float64)))
+    return tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+def pin_backward_is_library_autograd(orc):
+    # identity score: a boolean mask; ALiBi: the bias as an additive float mask
+    B, H, S, D, scale = 2, 3, 40, 8, 0.45
+    q, k, v, g = (_rand((B, H, S, D), 60 + t) for t in range(4))
+    doc = np.repeat(np.arange(5, dtype=np.int32), 8)[None, :].repeat(B, 0)
+    for mask, kw in [(W.MASK_CAUSAL, {}), (W.MASK_SLIDING_WINDOW, {"window": 6}),
+                     (W.MASK_CAUSAL_PREFIX, {"prefix": 13}), (W.MASK_DOCUMENT, {"doc": doc}), (W.MASK_ALL, {})]:
+        dm = _dense_mask(mask, B, S, kw.get("window", 0), kw.get("prefix", 0), kw.get("doc"))
+        okw = {"window": kw.get("window", 0), "prefix": kw.get("prefix", 0), "doc_ids": kw.get("doc")}
+        ref = _sdpa_grads(q, k, v, g, scale, torch.from_numpy(np.ascontiguousarray(dm)))
+        got = orc.attention_bwd(q, k, v, g, mask, W.SCORE_IDENTITY, scale, **okw)
+        for name, a, b in zip("qkv", got, ref):
+            _close(a, b, 1e-10, f"backward d{name} m{mask} identity")
+        slopes = 2.0 ** (-8.0 * (np.arange(H) + 1) / H)
+        i = np.arange(S)[:, None]
+        j = np.arange(S)[None, :]
+        bias = -slopes[None, :, None, None] * (i - j)[None, None]
+        fm = np.where(dm, bias, -np.inf)
+        ref = _sdpa_grads(q, k, v, g, scale, torch.from_numpy(np.ascontiguousarray(fm)))
+        got = orc.attention_bwd(q, k, v, g, mask, W.SCORE_ALIBI, scale, **okw)
+        for name, a, b in zip("qkv", got, ref):
+            _close(a, b, 1e-10, f"backward d{name} m{mask} alibi")
+
+
+def pin_backward_softcap_finite_differences(orc):
+    # central differences of L = sum(dout * out) through the (pinned) forward;
+    # inputs on a 2^-8 grid so q +- 2^-12 is exact in float32
+    B, H, S, D, scale, cap = 1, 2, 7, 3, 0.8, 0.9
+    q, k, v, g = (np.round(_rand((B, H, S, D), 70 + t) * 256) / 256 for t in range(4))
+    q, k, v, g = (x.astype(np.float32) for x in (q, k, v, g))
+    h = 2.0 ** -12
+    for mask, kw in [(W.MASK_CAUSAL, {}), (W.MASK_SLIDING_WINDOW, {"window": 3})]:
+        dq, dk, dv = orc.attention_bwd(q, k, v, g, mask, W.SCORE_SOFTCAP, scale, score_param=cap, **kw)
+
+        def loss(qq, kk, vv):
+            out, _ = orc.attention(qq, kk, vv, mask, W.SCORE_SOFTCAP, scale, score_param=cap, **kw)
+            return float(np.sum(out * g.astype(np.float64)))
+
+        for which, grad in ((0, dq), (1, dk), (2, dv)):
+            base = [q, k, v]
+            fd = np.zeros_like(grad)
+            for idx in np.ndindex(*base[which].shape):
+                hi, lo = [x.copy() for x in base], [x.copy() for x in base]
+                hi[which][idx] += np.float32(h)
+                lo[which][idx] -= np.float32(h)
+                fd[idx] = (loss(*hi) - loss(*lo)) / (2 * h)
+            _close(grad, fd, 2e-6, f"softcap d{'qkv'[which]} m{mask} vs finite differences")
+
+
+def pin_backward_invariants(orc):
+    # identity and ALiBi: every softmax row of dS sums to 0, so sum_j dK_j = 0;
+    # the weights of a row sum to 1, so sum_j dV_j = sum of dout over rows
+    # with a key; V equal on every key: out does not depend on q or k
+    B, H, S, D = 2, 2, 48, 8
+    q, k, v, g = (_rand((B, H, S, D), 80 + t) for t in range(4))
+    doc = np.repeat(np.arange(6, dtype=np.int32), 8)[None, :].repeat(B, 0)
+    for mask, kw in [(W.MASK_CAUSAL, {}), (W.MASK_SLIDING_WINDOW, {"window": 5}),
+                     (W.MASK_CAUSAL_PREFIX, {"prefix": 20}), (W.MASK_DOCUMENT, {"doc_ids": doc}),
+                     (W.MASK_ALL, {})]:
+        for score in (W.SCORE_IDENTITY, W.SCORE_ALIBI):
+            dq, dk, dv = orc.attention_bwd(q, k, v, g, mask, score, 0.6, **kw)
+            _close(dk.sum(axis=2), np.zeros((B, H, D)), 1e-11, f"sum dK m{mask} s{score}")
+            _close(dv.sum(axis=2), g.astype(np.float64).sum(axis=2), 1e-11, f"sum dV m{mask} s{score}")
+        vc = np.broadcast_to(_rand((B, H, 1, D), 90), (B, H, S, D)).copy()
+        for score, sp in [(W.SCORE_IDENTITY, 0.0), (W.SCORE_SOFTCAP, 1.5), (W.SCORE_ALIBI, 0.0)]:
+            dq, dk, _ = orc.attention_bwd(q, k, vc, g, mask, score, 0.6, score_param=sp, **kw)
+            assert np.max(np.abs(dq)) < 1e-12 and np.max(np.abs(dk)) < 1e-12, f"constant V m{mask} s{score}"
+    # an empty row (W = 0) contributes nothing
+    dq, dk, dv = orc.attention_bwd(q, k, v, g, W.MASK_SLIDING_WINDOW, W.SCORE_IDENTITY, 0.6, window=0)
+    assert not dq.any() and not dk.any() and not dv.any()
+
+
+def pin_block_mask_q_is_the_transpose(orc):
+    # brute-force tile classes, transposed: for kv block j, the q blocks of its
+    # partial / full tiles ascending, then the rest ascending
+    B, H = 2, 2
+    for S, block in [(8, 2), (12, 4), (13, 4), (10, 4)]:
+        q = k = v = _rand((B, H, S, 2), S)
+        doc = np.zeros((B, S), np.int32)
+        doc[0, S // 3:] = 1
+        doc[1, S // 2:] = 1
+        for mask, kw in [(W.MASK_CAUSAL, {}), (W.MASK_SLIDING_WINDOW, {"window": 3}),
+                         (W.MASK_CAUSAL_PREFIX, {"prefix": 5}), (W.MASK_DOCUMENT, {"doc": doc}),
+                         (W.MASK_ALL, {})]:
+            _, _, status, _ = brute_force(q, k, v, mask, W.SCORE_IDENTITY, 0.5, block=block,
+                                          window=kw.get("window", 0), prefix=kw.get("prefix", 0), doc=kw.get("doc"))
+            bq = orc.block_mask_q(mask, B, H, S, S, block, window=kw.get("window", 0), prefix=kw.get("prefix", 0),
+                                  doc_ids=kw.get("doc"))
+            for b in range(B):
+                for h in range(H):
+                    exp = _expected_lists(status[b, h].T)
+                    for key, qkey in (("kv_num_blocks", "q_num_blocks"), ("kv_indices", "q_indices"),
+                                      ("full_kv_num_blocks", "full_q_num_blocks"),
+                                      ("full_kv_indices", "full_q_indices")):
+                        assert np.array_equal(bq[qkey][b, h], exp[key]), f"{qkey} S{S} m{mask} b{b} h{h}"
+
+
 ALL_PINS = [
     pin_all_true_mask_is_textbook_attention,
     pin_causal_mask_is_library_causal,
@@ -557,4 +679,8 @@ ALL_PINS = [
     pin_prescale_power_of_two_scale_changes_nothing,
     pin_prescale_is_attention_on_rounded_q,
     pin_row_max_bounds_lse,
+    pin_backward_is_library_autograd,
+    pin_backward_softcap_finite_differences,
+    pin_backward_invariants,
+    pin_block_mask_q_is_the_transpose,
 ]

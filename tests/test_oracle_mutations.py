@@ -46,8 +46,20 @@ MUTATIONS = [
     ("bf16 subnormal quantum", "if (quantum < -133) quantum = -133;", "if (quantum < -126) quantum = -126;"),
     ("bf16 overflow bound", "ldexp(255.0, 120)", "ldexp(255.0, 119)"),
     ("padding rows counted", "band[r * kv_len + kv] = qb * block + r < q_len", "band[r * kv_len + kv] = 1"),
-    ("ragged tiles rounded down", "const int64_t nkvb = ((int64_t)kv_len + block - 1) / block;",
-     "const int64_t nkvb = ((int64_t)kv_len) / block + (kv_len % block > block / 2);"),
+    ("dS sign", "const double ds = pr[j] * (dp - Di);", "const double ds = pr[j] * (Di - dp);"),
+    ("dS drops the row term", "const double ds = pr[j] * (dp - Di);", "const double ds = pr[j] * dp;"),
+    ("softcap gradient dropped", "        return 1.0 - u * u;", "        return 1.0 + 0.0 * u;"),
+    ("dK from k", "dkb[j * D + d] += scale * dt * (double)qb[i * D + d];",
+     "dkb[j * D + d] += scale * dt * (double)kb[j * D + d];"),
+    ("dQ without scale", "dqi[d] += scale * dt * (double)kb[j * D + d];", "dqi[d] += dt * (double)kb[j * D + d];"),
+    ("dV from dS", "dvb[j * D + d] += pr[j] * (double)gb[i * D + d];", "dvb[j * D + d] += dt * (double)gb[i * D + d];"),
+    ("q-side padding order", "if (st[i * nkvb + j] != 1) pq[tp++] = (int32_t)i;",
+     "if (st[i * nkvb + j] != 1) pq[tp++] = (int32_t)(nqb - 1 - i);"),
+    ("q-side partial and full swapped", "if (st[i * nkvb + j] == 1) pq[np++] = (int32_t)i;",
+     "if (st[i * nkvb + j] == 2) pq[np++] = (int32_t)i;"),
+    ("ragged tiles rounded down",
+     "const int64_t nkvb = ((int64_t)kv_len + block - 1) / block;\n    or_mask m",
+     "const int64_t nkvb = ((int64_t)kv_len) / block + (kv_len % block > block / 2);\n    or_mask m"),
 ]
 
 
