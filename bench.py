@@ -240,6 +240,8 @@ def main():
                     help="(b, h) chunks of flex_attention_fwd_host, whose copies overlap the work")
     ap.add_argument("--option-steps", type=int, default=20,
                     help="launches per kernel-option variant (OUTPUT_MAX, PRESCALE_QK, ...); 0 skips them")
+    ap.add_argument("--backward-steps", type=int, default=3,
+                    help="timed flex_attention_bwd launches on the same workload; 0 skips them")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling a smaller case)")
@@ -294,6 +296,52 @@ def kernel_option_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flush,
     ms = {name: float(np.mean([a.elapsed_time(b) for a, b in pairs])) for name, pairs in ev.items()}
     return {"api": "flex_attention_fwd_opts", "launches_each": steps, "ms_per_launch": ms,
             "tflops": {name: flops / (t * 1e-3) / 1e12 for name, t in ms.items()}}
+
+
+# fp32 FMA on the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (maximum SM clock)
+FP32_CUDA_CORE_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def backward_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flops_fwd, steps):
+    """flex_attention_bwd on the bench workload (outside the headline's timed region).
+
+    Algorithmic FLOPs: per computed pair, the recomputed score and dP dots and
+    the dV, dK, dQ updates, 10 D, i.e. 2.5 x the forward's 4 D.
+    """
+    if steps <= 0:
+        return None
+    gen = torch.Generator(device=dq.device).manual_seed(1)
+    dout = torch.randn(out.shape, generator=gen, device=dq.device, dtype=torch.float32).to(out.dtype)
+    bq = fa.flex_block_mask_transpose(bm, stream=stream)
+    gq, gk, gv = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+    delta = torch.empty_like(lse)
+
+    def launch():
+        fa.flex_attention_bwd(dq, dk, dv, out, lse, dout, bm, bq, w.score, w.score_param, w.scale, dq=gq, dk=gk,
+                              dv=gv, delta=delta, stream=stream)
+
+    launch()
+    torch.cuda.synchronize()
+    ev = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        launch()
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    if fa.flex_device_status() != fa.FLEX_OK:
+        raise RuntimeError("device status reported a timeout during the backward launches")
+    if not (torch.isfinite(gq).all() and torch.isfinite(gk).all() and torch.isfinite(gv).all()):
+        raise RuntimeError("non-finite gradients")
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    flops = 2.5 * flops_fwd
+    achieved = flops / (ms * 1e-3) / 1e12
+    return {"api": "flex_attention_bwd", "launches": steps, "ms_per_launch": ms, "algorithmic_flops": flops,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_CUDA_CORE_TFLOPS, "unit": "TFLOP/s",
+                         "frac": achieved / FP32_CUDA_CORE_TFLOPS,
+                         "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
+                         "kernels": "attn_bwd_delta + attn_bwd_dkdv + attn_bwd_dq (fp32 FMA, CUDA cores)"}}
 
 
 def run_ours(args, w: W.Workload) -> None:
@@ -425,6 +473,13 @@ def run_ours(args, w: W.Workload) -> None:
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = oracle_rows_baseline(w, q, k, v, docs, bm_host, budget_s=args.cpu_seconds)
+    # the backward pass last: an error there is reported in its own field
+    # and leaves the forward's numbers above as measured
+    backward = None
+    try:
+        backward = backward_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flops, args.backward_steps)
+    except Exception as exc:  # noqa: BLE001
+        backward = {"error": f"{type(exc).__name__}: {exc}"}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
@@ -435,7 +490,7 @@ def run_ours(args, w: W.Workload) -> None:
             "attn_ms_per_launch": {"mean": attn_mean_ms, "median": float(np.median(attn_ms)),
                                    "min": float(np.min(attn_ms))},
             "block_mask_ms_per_launch": float(np.mean(np.asarray(step_ms) - np.asarray(attn_ms))),
-            "kernel_options": options}
+            "kernel_options": options, "backward": backward}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

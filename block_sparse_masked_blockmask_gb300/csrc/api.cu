@@ -302,6 +302,53 @@ int flex_attention_fwd_opts(const flex_tensor *q, const flex_tensor *k, const fl
     return launch_attention(p, q->dtype, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FLEX_OK : FLEX_ERR_CUDA;
 }
 
+int flex_block_mask_transpose(const flex_block_mask *bm, flex_block_mask_q *bq, void *stream) {
+    if (!bm || !bq) return FLEX_ERR_INVALID_ARG;
+    int rc = check_sizes(bm->B, bm->H, bm->q_len, bm->kv_len, bm->block);
+    if (rc != FLEX_OK) return rc;
+    if (bm->nqb != ceil_blocks(bm->q_len) || bm->nkvb != ceil_blocks(bm->kv_len)) return FLEX_ERR_SHAPE;
+    if (!bm->kv_num_blocks || !bm->kv_indices || !bm->full_kv_num_blocks || !bm->full_kv_indices)
+        return FLEX_ERR_INVALID_ARG;
+    if (!bq->q_num_blocks || !bq->q_indices || !bq->full_q_num_blocks || !bq->full_q_indices)
+        return FLEX_ERR_INVALID_ARG;
+    bq->B = bm->B;
+    bq->H = bm->H;
+    bq->q_len = bm->q_len;
+    bq->kv_len = bm->kv_len;
+    bq->block = bm->block;
+    bq->nqb = bm->nqb;
+    bq->nkvb = bm->nkvb;
+    return launch_block_mask_transpose(bm->kv_num_blocks, bm->kv_indices, bm->full_kv_num_blocks,
+                                       bm->full_kv_indices, bm->B, bm->H, bm->nqb, bm->nkvb, bq->q_num_blocks,
+                                       bq->q_indices, bq->full_q_num_blocks, bq->full_q_indices,
+                                       static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? FLEX_OK
+               : FLEX_ERR_CUDA;
+}
+
+int flex_attention_bwd(const flex_tensor *q, const flex_tensor *k, const flex_tensor *v, const void *out,
+                       const float *lse, const void *dout, const flex_block_mask *bm, const flex_block_mask_q *bq,
+                       int32_t score_kind, float score_param, float scale, void *dq, void *dk, void *dv,
+                       float *delta, void *stream) {
+    AttnProblem p;
+    int rc = prepare_attention(q, k, v, bm, score_kind, score_param, scale, const_cast<void *>(out),
+                               const_cast<float *>(lse), p);
+    if (rc != FLEX_OK) return rc;
+    if (!dout || !bq || !dq || !dk || !dv || !delta) return FLEX_ERR_INVALID_ARG;
+    if (!aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+        (reinterpret_cast<uintptr_t>(delta) & 3u))
+        return FLEX_ERR_ALIGNMENT;
+    if (bq->B != bm->B || bq->H != bm->H || bq->q_len != bm->q_len || bq->kv_len != bm->kv_len ||
+        bq->block != bm->block || bq->nqb != bm->nqb || bq->nkvb != bm->nkvb)
+        return FLEX_ERR_SHAPE;
+    if (!bq->q_num_blocks || !bq->q_indices || !bq->full_q_num_blocks || !bq->full_q_indices)
+        return FLEX_ERR_INVALID_ARG;
+    return launch_attn_bwd(p, q->dtype, dout, bq->q_num_blocks, bq->q_indices, bq->full_q_num_blocks,
+                           bq->full_q_indices, dq, dk, dv, delta, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? FLEX_OK
+               : FLEX_ERR_CUDA;
+}
+
 int flex_device_status(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FLEX_ERR_CUDA;
     int err = FLEX_OK;

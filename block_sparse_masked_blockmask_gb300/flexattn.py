@@ -37,8 +37,8 @@ FLEX_SCORE_ALIBI = 2
 FLEX_DTYPE_BF16 = 0
 FLEX_DTYPE_FP32 = 1
 
-EXPORTED = ("flex_block_mask_sizes", "flex_block_mask_create", "flex_attention_fwd",
-            "flex_attention_fwd_opts", "flex_attention_fwd_noalloc", "flex_attention_fwd_host", "flex_device_status",
+EXPORTED = ("flex_block_mask_sizes", "flex_block_mask_create", "flex_block_mask_transpose", "flex_attention_fwd",
+            "flex_attention_fwd_opts", "flex_attention_bwd", "flex_attention_fwd_noalloc", "flex_attention_fwd_host", "flex_device_status",
             "flex_selftest_wait_timeout", "flex_status_string")
 
 
@@ -63,6 +63,13 @@ class flex_block_mask(ctypes.Structure):
 class flex_tensor(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class flex_block_mask_q(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("q_len", ctypes.c_int32),
+                ("kv_len", ctypes.c_int32), ("block", ctypes.c_int32), ("nqb", ctypes.c_int32),
+                ("nkvb", ctypes.c_int32), ("q_num_blocks", ctypes.c_void_p), ("q_indices", ctypes.c_void_p),
+                ("full_q_num_blocks", ctypes.c_void_p), ("full_q_indices", ctypes.c_void_p)]
 
 
 class flex_kernel_options(ctypes.Structure):
@@ -109,6 +116,13 @@ def load_library():
                                                     ctypes.c_float, ctypes.c_float, vp, vp,
                                                     ctypes.POINTER(flex_kernel_options), vp]
             lib.flex_attention_fwd_opts.restype = ctypes.c_int
+            lib.flex_block_mask_transpose.argtypes = [ctypes.POINTER(flex_block_mask),
+                                                      ctypes.POINTER(flex_block_mask_q), vp]
+            lib.flex_block_mask_transpose.restype = ctypes.c_int
+            lib.flex_attention_bwd.argtypes = [tp, tp, tp, vp, vp, vp, ctypes.POINTER(flex_block_mask),
+                                               ctypes.POINTER(flex_block_mask_q), i32, ctypes.c_float,
+                                               ctypes.c_float, vp, vp, vp, vp, vp]
+            lib.flex_attention_bwd.restype = ctypes.c_int
             lib.flex_attention_fwd_noalloc.argtypes = [tp, tp, tp, ctypes.POINTER(flex_block_mask), i32,
                                                        ctypes.c_float, ctypes.c_float, vp, vp, vp,
                                                        ctypes.POINTER(ctypes.POINTER(ctypes.c_int))]
@@ -159,6 +173,41 @@ class BlockMask:
     def as_numpy(self) -> dict:
         return {k: getattr(self, k).cpu().numpy() for k in
                 ("kv_num_blocks", "kv_indices", "full_kv_num_blocks", "full_kv_indices")}
+
+
+class BlockMaskQ:
+    """Device q side of a BlockMask: the C struct plus the torch tensors that own its buffers."""
+
+    KEYS = ("q_num_blocks", "q_indices", "full_q_num_blocks", "full_q_indices")
+
+    def __init__(self, struct: flex_block_mask_q, tensors: dict):
+        self.struct = struct
+        for key in self.KEYS:
+            setattr(self, key, tensors[key])
+
+    def as_numpy(self) -> dict:
+        return {k: getattr(self, k).cpu().numpy() for k in self.KEYS}
+
+
+def flex_block_mask_transpose(block_mask: BlockMask, stream=None) -> BlockMaskQ:
+    """The q side of a BlockMask (asynchronous on `stream`)."""
+    s = block_mask.struct
+    device = block_mask.kv_num_blocks.device
+    t = {
+        "q_num_blocks": torch.empty((s.B, s.H, s.nkvb), dtype=torch.int32, device=device),
+        "q_indices": torch.empty((s.B, s.H, s.nkvb, s.nqb), dtype=torch.int32, device=device),
+        "full_q_num_blocks": torch.empty((s.B, s.H, s.nkvb), dtype=torch.int32, device=device),
+        "full_q_indices": torch.empty((s.B, s.H, s.nkvb, s.nqb), dtype=torch.int32, device=device),
+    }
+    bq = flex_block_mask_q()
+    for key in BlockMaskQ.KEYS:
+        setattr(bq, key, t[key].data_ptr())
+    with torch.cuda.device(device):
+        rc = load_library().flex_block_mask_transpose(ctypes.byref(s), ctypes.byref(bq),
+                                                      _stream_handle(stream, device))
+    if rc != FLEX_OK:
+        raise FlexError(rc, "flex_block_mask_transpose")
+    return BlockMaskQ(bq, t)
 
 
 def flex_block_mask_create(mask_kind: int, B: int, H: int, q_len: int, kv_len: int, block: int = 128,
@@ -272,6 +321,39 @@ def flex_attention_fwd_opts(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, b
     if rc != FLEX_OK:
         raise FlexError(rc, "flex_attention_fwd_opts")
     return out, lse, max_scores
+
+
+def flex_attention_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
+                       dout: torch.Tensor, block_mask: BlockMask, block_mask_q: BlockMaskQ,
+                       score_kind: int = FLEX_SCORE_IDENTITY, score_param: float = 0.0,
+                       scale: float | None = None, dq: torch.Tensor | None = None, dk: torch.Tensor | None = None,
+                       dv: torch.Tensor | None = None, delta: torch.Tensor | None = None, stream=None):
+    """Gradients (dq, dk, dv) of sum(dout * out); asynchronous on `stream`."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    B, H, Sq, D = q.shape
+    Skv = k.shape[2]
+    dq = torch.empty((B, H, Sq, D), dtype=q.dtype, device=q.device) if dq is None else dq
+    dk = torch.empty((B, H, Skv, D), dtype=q.dtype, device=q.device) if dk is None else dk
+    dv = torch.empty((B, H, Skv, D), dtype=q.dtype, device=q.device) if dv is None else dv
+    delta = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device) if delta is None else delta
+    for name, t in (("out", out), ("dout", dout), ("dq", dq), ("dk", dk), ("dv", dv)):
+        if not t.is_contiguous() or t.dtype != q.dtype:
+            raise ValueError(f"{name} must be contiguous in q's dtype")
+    if not lse.is_contiguous() or lse.dtype != torch.float32 or not delta.is_contiguous():
+        raise ValueError("lse and delta must be contiguous float32")
+    tq, tk, tv = _tensor(q), _tensor(k), _tensor(v)
+    with torch.cuda.device(q.device):
+        rc = load_library().flex_attention_bwd(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                               ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
+                                               ctypes.c_void_p(dout.data_ptr()), ctypes.byref(block_mask.struct),
+                                               ctypes.byref(block_mask_q.struct), score_kind, float(score_param),
+                                               float(scale), ctypes.c_void_p(dq.data_ptr()),
+                                               ctypes.c_void_p(dk.data_ptr()), ctypes.c_void_p(dv.data_ptr()),
+                                               ctypes.c_void_p(delta.data_ptr()), _stream_handle(stream, q.device))
+    if rc != FLEX_OK:
+        raise FlexError(rc, "flex_attention_bwd")
+    return dq, dk, dv
 
 
 def flex_attention_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block_mask: BlockMask,

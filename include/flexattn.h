@@ -8,6 +8,9 @@
  *                           output and the per-row log-sum-exp
  *                           (flex_attention_fwd_opts: the same with the op's
  *                           kernel options, e.g. the row max as a third output).
+ *   flex_attention_bwd      the gradients dq, dk, dv of the same attention,
+ *                           walking the q side of the BlockMask
+ *                           (flex_block_mask_transpose) for dk and dv.
  * Helpers size the BlockMask buffers, name status codes and read the device
  * status word.
  *
@@ -308,6 +311,58 @@ FLEX_API int flex_attention_fwd_opts(const flex_tensor *q, const flex_tensor *k,
                                      const flex_block_mask *bm, int32_t score_kind, float score_param,
                                      float scale, void *out, float *lse, const flex_kernel_options *opts,
                                      void *stream);
+
+/*
+ * The q side of a BlockMask (the q_num_blocks, q_indices, full_q_num_blocks,
+ * full_q_indices fields of the flex_attention op's BlockMask tuple, which
+ * its backward pass reads): for every (b, h, kv block j), the q blocks whose
+ * tile with j is partial (full), ascending, followed by all other q blocks
+ * ascending, so each row is a permutation of 0..NQB-1.
+ */
+typedef struct {
+    int32_t B, H, q_len, kv_len, block, nqb, nkvb;
+    int32_t *q_num_blocks;         /* device, [B, H, NKVB]       int32 */
+    int32_t *q_indices;            /* device, [B, H, NKVB, NQB]  int32 */
+    int32_t *full_q_num_blocks;    /* device, [B, H, NKVB]       int32 */
+    int32_t *full_q_indices;       /* device, [B, H, NKVB, NQB]  int32 */
+} flex_block_mask_q;
+
+/*
+ * Fill the q side of a BlockMask from its kv side on the device.
+ *   in : bm from flex_block_mask_create (its selected kv-block lists are
+ *        ascending, as that call writes them); bq's four buffers,
+ *        caller-allocated device memory of the sizes above.
+ *   out: bq's size fields, and its buffers written by a kernel on `stream`.
+ * Errors: FLEX_ERR_INVALID_ARG (null struct or buffer), FLEX_ERR_SHAPE,
+ * FLEX_ERR_UNSUPPORTED (as flex_block_mask_sizes), FLEX_ERR_CUDA.
+ */
+FLEX_API int flex_block_mask_transpose(const flex_block_mask *bm, flex_block_mask_q *bq, void *stream);
+
+/*
+ * Backward pass of flex_attention_fwd (the flex_attention_backward op of
+ * PyTorch PR #167356's tests): the gradients of sum(dout * out) with respect
+ * to q, k and v, for every (b, h), with t = scale q.k, s = score_mod(t) on the
+ * BlockMask's tiles (mask_mod on partial tiles), P = exp(s - lse):
+ *   dv[j] = sum_i P[i,j] dout[i]
+ *   dS[i,j] = P[i,j] (dout[i].v[j] - dout[i].out[i]) score_mod'(t[i,j])
+ *   dq[i] = scale sum_j dS[i,j] k[j],   dk[j] = scale sum_i dS[i,j] q[i]
+ * (score_mod' is 1 for identity and ALiBi, 1 - tanh^2(t / cap) for softcap).
+ *   q, k, v, bm, score_kind, score_param, scale: as given to the forward.
+ *   out, lse: device, the forward's outputs (contiguous, q's dtype; float32).
+ *   dout: device, contiguous [B, H, q_len, D] in q's dtype, 16-byte aligned.
+ *   bq:   the q side of bm, from flex_block_mask_transpose.
+ *   dq:   device, contiguous [B, H, q_len, D]; dk, dv: [B, H, kv_len, D];
+ *         q's dtype, 16-byte aligned.
+ *   delta: device workspace, [B, H, q_len] float32 (dout[i].out[i]).
+ * Rows whose lse is -inf (no unmasked score) contribute nothing.  The
+ * arithmetic is fp32 on the CUDA cores for both dtypes.  Errors: those of
+ * flex_attention_fwd, and FLEX_ERR_SHAPE when bq does not match bm.
+ * Asynchronous on `stream`.
+ */
+FLEX_API int flex_attention_bwd(const flex_tensor *q, const flex_tensor *k, const flex_tensor *v, const void *out,
+                                const float *lse, const void *dout, const flex_block_mask *bm,
+                                const flex_block_mask_q *bq, int32_t score_kind, float score_param, float scale,
+                                void *dq, void *dk, void *dv, float *delta, void *stream);
 
 /*
  * Synchronises `stream`, then returns and clears the device status word of

@@ -208,3 +208,33 @@ def test_options_entry_point_rejects_bad_arguments(lib):
     # the shared checks come first and still apply
     assert call(fa.flex_kernel_options(1, 0, 0x40000), score=3) == fa.FLEX_ERR_INVALID_ARG
     assert call(None, q=_tensor(bf, [1, 2, 384, 64])) == fa.FLEX_ERR_SHAPE
+
+
+def test_backward_entry_points_reject_bad_arguments(lib):
+    # flex_block_mask_transpose and flex_attention_bwd: every case fails its
+    # checks before any CUDA call
+    bf = fa.FLEX_DTYPE_BF16
+    bm = _mask_struct()
+    bq = fa.flex_block_mask_q()
+    bq.B, bq.H, bq.q_len, bq.kv_len, bq.block, bq.nqb, bq.nkvb = 1, 2, 256, 256, 128, 2, 2
+    bq.q_num_blocks = bq.q_indices = bq.full_q_num_blocks = bq.full_q_indices = 0x2000
+    assert lib.flex_block_mask_transpose(None, ctypes.byref(bq), None) == fa.FLEX_ERR_INVALID_ARG
+    empty = fa.flex_block_mask_q()
+    assert lib.flex_block_mask_transpose(ctypes.byref(bm), ctypes.byref(empty), None) == fa.FLEX_ERR_INVALID_ARG
+    q, k, v = (_tensor(bf, [1, 2, 256, 64]) for _ in range(3))
+
+    def call(bq=bq, dq=0x40000, delta=0x50000, dout=0x60000, score=fa.FLEX_SCORE_IDENTITY):
+        return lib.flex_attention_bwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.c_void_p(0x20000),
+                                      ctypes.c_void_p(0x30000), ctypes.c_void_p(dout), ctypes.byref(bm),
+                                      ctypes.byref(bq) if bq is not None else None, score, 0.0, 0.125,
+                                      ctypes.c_void_p(dq), ctypes.c_void_p(0x70000), ctypes.c_void_p(0x80000),
+                                      ctypes.c_void_p(delta), None)
+
+    assert call(bq=None) == fa.FLEX_ERR_INVALID_ARG
+    assert call(dq=0x40008) == fa.FLEX_ERR_ALIGNMENT
+    assert call(delta=0x50002) == fa.FLEX_ERR_ALIGNMENT
+    assert call(dout=0) == fa.FLEX_ERR_INVALID_ARG
+    assert call(score=5) == fa.FLEX_ERR_INVALID_ARG
+    other = fa.flex_block_mask_q.from_buffer_copy(bq)
+    other.nkvb = 3
+    assert call(bq=other) == fa.FLEX_ERR_SHAPE
