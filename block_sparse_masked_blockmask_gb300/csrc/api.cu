@@ -6,7 +6,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "flex_internal.h"
+#include "bwd_internal.h"
 
 namespace flex {
 namespace {

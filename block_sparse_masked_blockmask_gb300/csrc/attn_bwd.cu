@@ -18,7 +18,7 @@
 // Each thread owns 32 of a row's D dims, as 8 groups of 4 contiguous floats
 // spaced 4 * (threads per row) apart, so the row's threads read distinct
 // shared-memory banks when they fetch the same staged row.
-#include "flex_internal.h"
+#include "bwd_internal.h"
 #include "ptx.cuh"
 
 namespace flex {

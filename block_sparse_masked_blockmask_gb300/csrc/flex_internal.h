@@ -92,16 +92,6 @@ cudaError_t launch_block_mask(const MaskDesc &mask, int B, int H, int q_len, int
 cudaError_t launch_attn_fp32(const AttnProblem &p, cudaStream_t stream);
 cudaError_t launch_attn_bf16(const AttnProblem &p, cudaStream_t stream);
 
-// Backward pass (attn_bwd.cu): delta, dK/dV and dQ kernels; out and lse of p
-// are the forward's outputs, read here.
-cudaError_t launch_attn_bwd(const AttnProblem &p, int dtype, const void *dout, const int32_t *q_num,
-                            const int32_t *q_idx, const int32_t *fq_num, const int32_t *fq_idx, void *dq, void *dk,
-                            void *dv, float *delta, cudaStream_t stream);
-// q side of the BlockMask from its kv side (attn_bwd.cu).
-cudaError_t launch_block_mask_transpose(const int32_t *kv_num, const int32_t *kv_idx, const int32_t *full_num,
-                                        const int32_t *full_idx, int B, int H, int nqb, int nkvb, int32_t *q_num,
-                                        int32_t *q_idx, int32_t *fq_num, int32_t *fq_idx, cudaStream_t stream);
-
 cudaError_t launch_wait_timeout_selftest(int *status, uint64_t limit_ns, cudaStream_t stream);
 
 // The per-device workspace holding the status word (allocated once per device).
