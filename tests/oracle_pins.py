@@ -652,6 +652,13 @@ def pin_block_mask_q_is_the_transpose(orc):
                                       ("full_kv_num_blocks", "full_q_num_blocks"),
                                       ("full_kv_indices", "full_q_indices")):
                         assert np.array_equal(bq[qkey][b, h], exp[key]), f"{qkey} S{S} m{mask} b{b} h{h}"
+    # rectangular and ragged: the all-true mask at Q_LEN 200, KV_LEN 333 has
+    # full tiles only where both the rows and the columns are whole
+    bq = orc.block_mask_q(W.MASK_ALL, 1, 1, 200, 333, 128)
+    exp = _expected_lists(np.array([[2, 2, 1], [1, 1, 1]]).T)
+    for key, qkey in (("kv_num_blocks", "q_num_blocks"), ("kv_indices", "q_indices"),
+                      ("full_kv_num_blocks", "full_q_num_blocks"), ("full_kv_indices", "full_q_indices")):
+        assert np.array_equal(bq[qkey][0, 0], exp[key]), f"{qkey} 200x333"
 
 
 ALL_PINS = [
