@@ -407,6 +407,83 @@ static double or_score_grad(int kind, double param, double t)
 }
 
 /*
+ * The backward terms of one row i of one (b, h): dq_i, and, when dk and dv
+ * are given, row i's contributions to every dk_j and dv_j.  qb .. gb point at
+ * the (b, h) slices; t, pr (s_kv doubles), o (D doubles) and mk (s_kv bytes)
+ * are scratch.
+ */
+static void or_bwd_row(const float *qb, const float *kb, const float *vb, const float *gb,
+                       int64_t H, int64_t s_kv, int64_t D, const or_mask *m,
+                       int score_kind, double score_param, double scale,
+                       int64_t b, int64_t h, int64_t i,
+                       double *t, double *pr, double *o, unsigned char *mk,
+                       double *dqi, double *dkb, double *dvb)
+{
+    for (int64_t d = 0; d < D; ++d)
+        dqi[d] = 0.0;
+    /* scores and the softmax of row i */
+    int any = 0;
+    double mx = -INFINITY;
+    for (int64_t j = 0; j < s_kv; ++j) {
+        double dot = 0.0;
+        for (int64_t d = 0; d < D; ++d)
+            dot += (double)qb[i * D + d] * (double)kb[j * D + d];
+        t[j] = scale * dot;
+        mk[j] = (unsigned char)or_mask_mod(m, b, h, i, j);
+        if (mk[j]) {
+            any = 1;
+            const double sij = or_score_mod(score_kind, score_param, t[j], h, H, i, j);
+            pr[j] = sij;
+            if (sij > mx) mx = sij;
+        }
+    }
+    if (!any) return;  /* P = 0: the row contributes nothing */
+    double Z = 0.0;
+    for (int64_t j = 0; j < s_kv; ++j)
+        if (mk[j]) Z += exp(pr[j] - mx);
+    const double lse = mx + log(Z);
+    for (int64_t j = 0; j < s_kv; ++j)
+        pr[j] = mk[j] ? exp(pr[j] - lse) : 0.0;
+    /* out_i and D_i */
+    for (int64_t d = 0; d < D; ++d)
+        o[d] = 0.0;
+    for (int64_t j = 0; j < s_kv; ++j)
+        if (mk[j])
+            for (int64_t d = 0; d < D; ++d)
+                o[d] += pr[j] * (double)vb[j * D + d];
+    double Di = 0.0;
+    for (int64_t d = 0; d < D; ++d)
+        Di += (double)gb[i * D + d] * o[d];
+    for (int64_t j = 0; j < s_kv; ++j) {
+        if (!mk[j]) continue;
+        double dp = 0.0;
+        for (int64_t d = 0; d < D; ++d)
+            dp += (double)gb[i * D + d] * (double)vb[j * D + d];
+        const double ds = pr[j] * (dp - Di);
+        const double dt = ds * or_score_grad(score_kind, score_param, t[j]);
+        for (int64_t d = 0; d < D; ++d) {
+            if (dvb) dvb[j * D + d] += pr[j] * (double)gb[i * D + d];
+            dqi[d] += scale * dt * (double)kb[j * D + d];
+            if (dkb) dkb[j * D + d] += scale * dt * (double)qb[i * D + d];
+        }
+    }
+}
+
+static int or_bwd_args_ok(int B, int H, int s_q, int s_kv, int D, int mask_kind, const int32_t *doc,
+                          int score_kind, double score_param)
+{
+    if (!or_mask_ok(mask_kind) || B <= 0 || H <= 0 || s_q <= 0 || s_kv <= 0 || D <= 0)
+        return 0;
+    if (score_kind < OR_SCORE_IDENTITY || score_kind > OR_SCORE_ALIBI)
+        return 0;
+    if (mask_kind == OR_MASK_DOCUMENT && (doc == NULL || s_q != s_kv))
+        return 0;
+    if (score_kind == OR_SCORE_SOFTCAP && !(score_param > 0.0))
+        return 0;
+    return 1;
+}
+
+/*
  * Backward pass: the gradients of L = sum_{i,d} dO[i,d] out[i,d] with
  * respect to q, k and v, for out as oracle_attention defines it.  Per (b, h),
  * with t_ij = scale q_i.k_j, S_ij = score_mod(t_ij) where mask_mod holds
@@ -425,13 +502,7 @@ int oracle_attention_bwd(const float *q, const float *k, const float *v, const f
                          int score_kind, double score_param, double scale,
                          double *dq, double *dk, double *dv)
 {
-    if (!or_mask_ok(mask_kind) || B <= 0 || H <= 0 || s_q <= 0 || s_kv <= 0 || D <= 0)
-        return OR_ERR_ARG;
-    if (score_kind < OR_SCORE_IDENTITY || score_kind > OR_SCORE_ALIBI)
-        return OR_ERR_ARG;
-    if (mask_kind == OR_MASK_DOCUMENT && (doc == NULL || s_q != s_kv))
-        return OR_ERR_ARG;
-    if (score_kind == OR_SCORE_SOFTCAP && !(score_param > 0.0))
+    if (!or_bwd_args_ok(B, H, s_q, s_kv, D, mask_kind, doc, score_kind, score_param))
         return OR_ERR_ARG;
     or_mask m = {mask_kind, window, prefix, doc, (int64_t)s_q};
     int err = OR_OK;
@@ -441,9 +512,6 @@ int oracle_attention_bwd(const float *q, const float *k, const float *v, const f
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t bh = 0; bh < (int64_t)B * H; ++bh) {
         const int64_t b = bh / H, h = bh % H;
-        const float *qb = q + bh * s_q * D, *kb = k + bh * s_kv * D, *vb = v + bh * s_kv * D;
-        const float *gb = dout + bh * s_q * D;
-        double *dqb = dq + bh * s_q * D, *dkb = dk + bh * s_kv * D, *dvb = dv + bh * s_kv * D;
         double *t = (double *)malloc((size_t)s_kv * sizeof(double));
         double *pr = (double *)malloc((size_t)s_kv * sizeof(double));
         double *o = (double *)malloc((size_t)D * sizeof(double));
@@ -451,58 +519,52 @@ int oracle_attention_bwd(const float *q, const float *k, const float *v, const f
         if (!t || !pr || !o || !mk) {
 #pragma omp atomic write
             err = OR_ERR_NOMEM;
-            free(t); free(pr); free(o); free(mk);
-            continue;
+        } else {
+            for (int64_t i = 0; i < s_q; ++i)
+                or_bwd_row(q + bh * s_q * D, k + bh * s_kv * D, v + bh * s_kv * D, dout + bh * s_q * D,
+                           H, s_kv, D, &m, score_kind, score_param, scale, b, h, i, t, pr, o, mk,
+                           dq + (bh * s_q + i) * D, dk + bh * s_kv * D, dv + bh * s_kv * D);
         }
-        for (int64_t i = 0; i < s_q; ++i) {
-            double *dqi = dqb + i * D;
-            for (int64_t d = 0; d < D; ++d)
-                dqi[d] = 0.0;
-            /* scores and the softmax of row i */
-            int any = 0;
-            double mx = -INFINITY;
-            for (int64_t j = 0; j < s_kv; ++j) {
-                double dot = 0.0;
-                for (int64_t d = 0; d < D; ++d)
-                    dot += (double)qb[i * D + d] * (double)kb[j * D + d];
-                t[j] = scale * dot;
-                mk[j] = (unsigned char)or_mask_mod(&m, b, h, i, j);
-                if (mk[j]) {
-                    any = 1;
-                    const double sij = or_score_mod(score_kind, score_param, t[j], h, H, i, j);
-                    pr[j] = sij;
-                    if (sij > mx) mx = sij;
-                }
-            }
-            if (!any) continue;  /* P = 0: the row contributes nothing */
-            double Z = 0.0;
-            for (int64_t j = 0; j < s_kv; ++j)
-                if (mk[j]) Z += exp(pr[j] - mx);
-            const double lse = mx + log(Z);
-            for (int64_t j = 0; j < s_kv; ++j)
-                pr[j] = mk[j] ? exp(pr[j] - lse) : 0.0;
-            /* out_i and D_i */
-            for (int64_t d = 0; d < D; ++d)
-                o[d] = 0.0;
-            for (int64_t j = 0; j < s_kv; ++j)
-                if (mk[j])
-                    for (int64_t d = 0; d < D; ++d)
-                        o[d] += pr[j] * (double)vb[j * D + d];
-            double Di = 0.0;
-            for (int64_t d = 0; d < D; ++d)
-                Di += (double)gb[i * D + d] * o[d];
-            for (int64_t j = 0; j < s_kv; ++j) {
-                if (!mk[j]) continue;
-                double dp = 0.0;
-                for (int64_t d = 0; d < D; ++d)
-                    dp += (double)gb[i * D + d] * (double)vb[j * D + d];
-                const double ds = pr[j] * (dp - Di);
-                const double dt = ds * or_score_grad(score_kind, score_param, t[j]);
-                for (int64_t d = 0; d < D; ++d) {
-                    dvb[j * D + d] += pr[j] * (double)gb[i * D + d];
-                    dqi[d] += scale * dt * (double)kb[j * D + d];
-                    dkb[j * D + d] += scale * dt * (double)qb[i * D + d];
-                }
+        free(t);
+        free(pr);
+        free(o);
+        free(mk);
+    }
+    return err;
+}
+
+/*
+ * dq of the flat rows ((b*H + h)*s_q + i) listed in rows: dq [nrows, D].  A
+ * row's dq needs only that row's scores, so this stays cheap at lengths where
+ * the whole backward would not.
+ */
+int oracle_attention_bwd_dq_rows(const float *q, const float *k, const float *v, const float *dout,
+                                 int B, int H, int s_q, int s_kv, int D,
+                                 int mask_kind, int window, int prefix, const int32_t *doc,
+                                 int score_kind, double score_param, double scale,
+                                 const int64_t *rows, int64_t nrows, double *dq)
+{
+    if (!or_bwd_args_ok(B, H, s_q, s_kv, D, mask_kind, doc, score_kind, score_param) || !rows)
+        return OR_ERR_ARG;
+    or_mask m = {mask_kind, window, prefix, doc, (int64_t)s_q};
+    int err = OR_OK;
+#pragma omp parallel
+    {
+        double *t = (double *)malloc((size_t)s_kv * sizeof(double));
+        double *pr = (double *)malloc((size_t)s_kv * sizeof(double));
+        double *o = (double *)malloc((size_t)D * sizeof(double));
+        unsigned char *mk = (unsigned char *)malloc((size_t)s_kv);
+        if (!t || !pr || !o || !mk) {
+#pragma omp atomic write
+            err = OR_ERR_NOMEM;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t r = 0; r < nrows; ++r) {
+                const int64_t i = rows[r] % s_q, bh = rows[r] / s_q;
+                if (bh >= (int64_t)B * H) continue;
+                or_bwd_row(q + bh * s_q * D, k + bh * s_kv * D, v + bh * s_kv * D, dout + bh * s_q * D,
+                           H, s_kv, D, &m, score_kind, score_param, scale, bh / H, bh % H, i, t, pr, o, mk,
+                           dq + r * D, NULL, NULL);
             }
         }
         free(t);

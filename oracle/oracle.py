@@ -68,6 +68,9 @@ class Oracle:
         lib.oracle_attention_bwd.argtypes = [f32p, f32p, f32p, f32p, I, I, I, I, I, I, I, I, i32p,
                                              I, D, D, f64p, f64p, f64p]
         lib.oracle_attention_bwd.restype = I
+        lib.oracle_attention_bwd_dq_rows.argtypes = [f32p, f32p, f32p, f32p, I, I, I, I, I, I, I, I, i32p,
+                                                     I, D, D, i64p, L, f64p]
+        lib.oracle_attention_bwd_dq_rows.restype = I
         lib.oracle_round_bf16.argtypes = [D]
         lib.oracle_round_bf16.restype = D
         lib.oracle_mask_value.argtypes = [I, I, I, i32p, L, L, L, L, L]
@@ -204,6 +207,24 @@ class Oracle:
             raise ValueError(f"oracle_attention_bwd failed with {rc}")
         return dq, dk, dv
 
+    def attention_bwd_dq_rows(self, q, k, v, dout, rows, mask_kind: int, score_kind: int, scale: float,
+                              window: int = 0, prefix: int = 0, doc_ids=None, score_param: float = 0.0):
+        """dq of the flat rows ((b*H + h)*Sq + i) in `rows`: float64 [len(rows), D]."""
+        q, k, v, dout = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k, v, dout))
+        B, H, s_q, D = q.shape
+        s_kv = k.shape[2]
+        doc = None if doc_ids is None else np.ascontiguousarray(doc_ids, dtype=np.int32)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        dq = np.zeros((rows.size, D), np.float64)
+        rc = self.lib.oracle_attention_bwd_dq_rows(_ptr(q, ctypes.c_float), _ptr(k, ctypes.c_float),
+                                                   _ptr(v, ctypes.c_float), _ptr(dout, ctypes.c_float), B, H, s_q,
+                                                   s_kv, D, mask_kind, window, prefix, _ptr(doc, ctypes.c_int32),
+                                                   score_kind, float(score_param), float(scale),
+                                                   _ptr(rows, ctypes.c_int64), rows.size, _ptr(dq, ctypes.c_double))
+        if rc != 0:
+            raise ValueError(f"oracle_attention_bwd_dq_rows failed with {rc}")
+        return dq
+
     def round_bf16(self, x: float) -> float:
         return float(self.lib.oracle_round_bf16(float(x)))
 
@@ -262,6 +283,10 @@ def attention_bwd(*a, **kw):
 
 def block_mask_q(*a, **kw):
     return default().block_mask_q(*a, **kw)
+
+
+def attention_bwd_dq_rows(*a, **kw):
+    return default().attention_bwd_dq_rows(*a, **kw)
 
 
 def num_threads() -> int:

@@ -629,6 +629,18 @@ def pin_backward_invariants(orc):
     assert not dq.any() and not dk.any() and not dv.any()
 
 
+def pin_backward_dq_rows_match_the_full_backward(orc):
+    # the row-sampled dq is the full backward's dq, row for row and bit for bit
+    B, H, S, D = 2, 2, 40, 8
+    q, k, v, g = (_rand((B, H, S, D), 95 + t) for t in range(4))
+    rows = np.array([0, 1, 39, 40, 77, 120, 159], np.int64)
+    for mask, kw in [(W.MASK_CAUSAL, {}), (W.MASK_SLIDING_WINDOW, {"window": 0})]:
+        for score, sp in [(W.SCORE_SOFTCAP, 1.5), (W.SCORE_ALIBI, 0.0)]:
+            dq, _, _ = orc.attention_bwd(q, k, v, g, mask, score, 0.6, score_param=sp, **kw)
+            got = orc.attention_bwd_dq_rows(q, k, v, g, rows, mask, score, 0.6, score_param=sp, **kw)
+            _close(got, dq.reshape(-1, D)[rows], 0.0, f"dq rows m{mask} s{score}")
+
+
 def pin_block_mask_q_is_the_transpose(orc):
     # brute-force tile classes, transposed: for kv block j, the q blocks of its
     # partial / full tiles ascending, then the rest ascending
@@ -690,4 +702,5 @@ ALL_PINS = [
     pin_backward_softcap_finite_differences,
     pin_backward_invariants,
     pin_block_mask_q_is_the_transpose,
+    pin_backward_dq_rows_match_the_full_backward,
 ]
