@@ -7,6 +7,7 @@ least one pin must fail on it.  CPU only; the real oracle is untouched.
 import os
 import subprocess
 import sys
+from concurrent.futures import ThreadPoolExecutor
 
 import pytest
 
@@ -81,17 +82,36 @@ for pin in oracle_pins.ALL_PINS:
 """
 
 
-@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
-def test_pins_catch_mutation(tmp_path, name, old, new):
+def _run_mutant(tmp_dir, index, name, old, new):
+    """(names of the pins that fail, exit code) for one mutant, in its own interpreter."""
     src = open(oracle.oracle.SOURCE).read()
-    assert src.count(old) == 1, f"mutation anchor not unique: {name}"
-    path = os.path.join(tmp_path, "mutant.c")
+    if src.count(old) != 1:
+        return None, f"mutation anchor not unique: {name}"
+    d = os.path.join(tmp_dir, f"mutant{index}")
+    os.makedirs(d, exist_ok=True)
+    path = os.path.join(d, "mutant.c")
     with open(path, "w") as f:
         f.write(src.replace(old, new))
-    lib = oracle.compile_oracle(path, os.path.join(tmp_path, "libmutant.so"))
+    lib = oracle.compile_oracle(path, os.path.join(d, "libmutant.so"))
     here = os.path.dirname(os.path.abspath(__file__))
     code = _RUNNER.format(root=os.path.dirname(here), tests=here, lib=lib)
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
-    failed = [line.split()[1] for line in r.stdout.splitlines() if line.startswith("FAILED")]
-    # a mutant that crashes its interpreter is caught as well, but report it
-    assert failed or r.returncode != 0, f"no pin caught the mutation '{name}'"
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=900, env=env)
+    return [line.split()[1] for line in r.stdout.splitlines() if line.startswith("FAILED")], r.returncode
+
+
+@pytest.fixture(scope="module")
+def mutant_results(tmp_path_factory):
+    tmp_dir = str(tmp_path_factory.mktemp("mutants"))
+    workers = max(1, min(len(MUTATIONS), (os.cpu_count() or 2) // 2))
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        futures = {m[0]: ex.submit(_run_mutant, tmp_dir, i, *m) for i, m in enumerate(MUTATIONS)}
+        return {name: f.result() for name, f in futures.items()}
+
+
+@pytest.mark.parametrize("name", [m[0] for m in MUTATIONS])
+def test_pins_catch_mutation(mutant_results, name):
+    failed, rc = mutant_results[name]
+    assert failed is not None, rc
+    # a mutant that crashes its interpreter is caught as well
+    assert failed or rc != 0, f"no pin caught the mutation '{name}'"
