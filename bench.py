@@ -31,6 +31,9 @@ UNIT = "TFLOP/s"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
+# NVIDIA's published dense bf16 tensor rate of one GB300 GPU: 36 PFLOP/s for an
+# 8-GPU HGX B300 board is quoted with 2:4 sparsity, i.e. 2.25 PFLOP/s dense each.
+SPEC_BF16_TFLOPS = 2250.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_bf16_traffic.txt")
 KERNEL_SOURCES = ["attn_bf16_kernel.cuh", "attn_bf16_launch.cuh", "attn_bf16.cu", "attn_bf16_d64.cu",
                   "attn_bf16_d128.cu", "ptx.cuh", "flex_internal.h"]
@@ -242,6 +245,8 @@ def main():
                     help="launches per kernel-option variant (OUTPUT_MAX, PRESCALE_QK, ...); 0 skips them")
     ap.add_argument("--backward-steps", type=int, default=3,
                     help="timed flex_attention_bwd launches on the same workload; 0 skips them")
+    ap.add_argument("--config-steps", type=int, default=20,
+                    help="timed attention launches on each of the five synthetic configurations; 0 skips them")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling a smaller case)")
@@ -254,6 +259,73 @@ def main():
         run_reference(args, w)
         return
     run_ours(args, w)
+
+
+def prepare_device_inputs(torch, w: W.Workload):
+    """The workload's seeded inputs on the device (the same bits the oracle sees)."""
+    q, k, v, docs = W.workload_inputs(w)
+
+    def to_dev(x):
+        if w.dtype == "bf16":
+            return torch.from_numpy(W.bf16_bits(x).view(np.int16)).cuda().view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+    dd = torch.from_numpy(docs).cuda() if docs is not None else None
+    return (q, k, v, docs), (to_dev(q), to_dev(k), to_dev(v), dd)
+
+
+def config_timings(fa, torch, device_index: int, steps: int, peaks: dict) -> dict | None:
+    """Attention-kernel throughput on every synthetic configuration (outside the headline's timed region).
+
+    Per configuration: the BlockMask is built once, then `steps` attention
+    launches are timed one by one with CUDA events on the launching stream,
+    L2 flushed before each launch when the inputs fit in L2, clocks sampled
+    while they run.  TFLOP/s counts unmasked-block FLOPs.
+    """
+    if steps <= 0:
+        return None
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 2**20, dtype=torch.uint8, device="cuda")
+    res = {}
+    for w in W.CONFIGS:
+        _, (dq, dk, dv, dd) = prepare_device_inputs(torch, w)
+        out = torch.empty_like(dq)
+        lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+        bm = fa.flex_block_mask_create(w.mask, w.B, w.H, w.S, w.S, 128, window=w.window, prefix=w.prefix,
+                                       doc_ids=dd, stream=stream)
+        flops = unmasked_block_flops(w, bm.as_numpy())
+        small = 3 * dq.numel() * dq.element_size() <= L2_BYTES
+
+        def launch():
+            fa.flex_attention_fwd(dq, dk, dv, bm, w.score, w.score_param, w.scale, out=out, lse=lse, stream=stream)
+
+        for _ in range(3):
+            launch()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        with ClockSampler(device_index) as clocks:
+            for a, b in ev:
+                if small:
+                    flush.zero_()
+                a.record(stream)
+                launch()
+                b.record(stream)
+            torch.cuda.synchronize()
+        if fa.flex_device_status() != fa.FLEX_OK:
+            raise RuntimeError(f"device status reported a timeout on {w.name}")
+        ms = [a.elapsed_time(b) for a, b in ev]
+        mean = float(np.mean(ms))
+        tflops = flops / (mean * 1e-3) / 1e12
+        res[w.name] = {"dtype": w.dtype, "unmasked_block_flops": flops, "attn_ms_mean": mean,
+                       "attn_ms_median": float(np.median(ms)), "tflops": tflops,
+                       "frac_of_measured_bf16_peak": tflops / peaks["bf16"],
+                       "frac_of_spec_bf16_peak": tflops / SPEC_BF16_TFLOPS,
+                       "kernel": "attn_bf16_kernel" if w.dtype == "bf16" else "attn_fp32_kernel (CUDA cores)",
+                       "l2": "flushed before each launch" if small else "inputs larger than L2",
+                       "launches": steps, "clocks": clocks.summary()}
+        del dq, dk, dv, dd, out, lse, bm
+        torch.cuda.empty_cache()
+    return res
 
 
 def kernel_option_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flush, flops, steps):
@@ -357,16 +429,7 @@ def run_ours(args, w: W.Workload) -> None:
         import torch.distributed as dist
         dist.init_process_group("nccl")
 
-    q, k, v, docs = W.workload_inputs(w)
-    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
-
-    def to_dev(x):
-        if w.dtype == "bf16":
-            return torch.from_numpy(W.bf16_bits(x).view(np.int16)).cuda().view(torch.bfloat16)
-        return torch.from_numpy(x).cuda()
-
-    dq, dk, dv = to_dev(q), to_dev(k), to_dev(v)
-    dd = torch.from_numpy(docs).cuda() if docs is not None else None
+    (q, k, v, docs), (dq, dk, dv, dd) = prepare_device_inputs(torch, w)
     out = torch.empty_like(dq)
     lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
@@ -470,6 +533,11 @@ def run_ours(args, w: W.Workload) -> None:
                 "peak_source": f"{peaks['source']} bf16 burst (dense cuBLAS)",
                 "achieved_hbm_gbs": None if traffic is None else traffic / (attn_mean_ms * 1e-3) / 1e9,
                 "algorithmic_flops_per_launch": flops, "mean_launch_ms": attn_mean_ms}
+    configs = None
+    try:
+        configs = config_timings(fa, torch, local, args.config_steps, peaks)
+    except Exception as exc:  # noqa: BLE001
+        configs = {"error": f"{type(exc).__name__}: {exc}"}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = oracle_rows_baseline(w, q, k, v, docs, bm_host, budget_s=args.cpu_seconds)
@@ -484,13 +552,17 @@ def run_ours(args, w: W.Workload) -> None:
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
             "config": config_dict(w), "pct_of_bf16_peak": 100.0 * value / peaks["bf16"],
+            "pct_of_spec_bf16_peak": 100.0 * value / SPEC_BF16_TFLOPS,
+            "spec_bf16_peak": {"value": SPEC_BF16_TFLOPS, "unit": "TFLOP/s",
+                               "source": "NVIDIA HGX B300: 36 PFLOP/s bf16 per 8 GPUs with 2:4 sparsity, "
+                                         "i.e. 2.25 PFLOP/s dense per GPU"},
             "roofline": roofline, "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": 2 * args.steps, "clocks": clocks.summary(),
             "attn_ms_per_launch": {"mean": attn_mean_ms, "median": float(np.median(attn_ms)),
                                    "min": float(np.min(attn_ms))},
             "block_mask_ms_per_launch": float(np.mean(np.asarray(step_ms) - np.asarray(attn_ms))),
-            "kernel_options": options, "backward": backward}
+            "kernel_options": options, "backward": backward, "configs": configs}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

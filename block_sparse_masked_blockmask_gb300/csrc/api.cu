@@ -71,6 +71,8 @@ int prepare_attention(const flex_tensor *q, const flex_tensor *k, const flex_ten
         return FLEX_ERR_INVALID_ARG;
     if (bm->mask_kind == FLEX_MASK_DOCUMENT && (!bm->params.doc_ids || !aligned16(bm->params.doc_ids)))
         return FLEX_ERR_INVALID_ARG;
+    // document ids are one row per batch entry, indexed by q and by kv alike
+    if (bm->mask_kind == FLEX_MASK_DOCUMENT && Sq != Skv) return FLEX_ERR_SHAPE;
     // each kv tile's document ids are bulk-copied as whole 16-byte words
     if (bm->mask_kind == FLEX_MASK_DOCUMENT && Sq % 4 != 0) return FLEX_ERR_UNSUPPORTED;
     if (bm->mask_kind == FLEX_MASK_SLIDING_WINDOW && bm->params.window < 0) return FLEX_ERR_INVALID_ARG;
@@ -379,7 +381,7 @@ const char *flex_status_string(int status) {
         case FLEX_ERR_UNSUPPORTED:
             return "unsupported configuration";
         case FLEX_ERR_SHAPE:
-            return "shape mismatch or length not a multiple of the block size";
+            return "shapes, lengths or BlockMask sizes disagree";
         case FLEX_ERR_ALIGNMENT:
             return "pointer or stride not 16-byte aligned, or inner stride is not 1";
         case FLEX_ERR_CUDA:

@@ -200,8 +200,11 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]
 
 // score_mod in base-2 units, two columns (c, c+1) at a time on packed fp32x2:
 //   identity : x = k0 s                              k0 = scale log2(e)
-//   softcap  : x = k2 + k1 / (2^(k0 s) + 1)          = log2(e) cap tanh(scale s / cap)
+//   softcap  : x = k1 tanh(k0 s)                     k0 = scale / cap, k1 = log2(e) cap
 //   ALiBi    : x = k0 s + slope2 c                   slope2 = log2(e) slope_h
+// The softcap's tanh is the hardware's single-instruction approximation
+// (tanh.approx.f32, relative error about 2^-11), one special-function
+// operation per score beside the softmax's exponential.
 // For ALiBi the per-tile term slope2 (kv0 - q) is kept out of x as `offset`:
 // it shifts the whole row, so it is added to the row max and subtracted in
 // the exponent instead of being added to every element.  The column term
@@ -209,24 +212,20 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]
 // seven adds each, error below 1e-4 in base-2 units on the tile's columns).
 template <int SCORE>
 struct ScoreLog2 {
-    uint64_t k0, k1, k2, one;
+    uint64_t k0, k1;
     float slope2, offset;
     uint64_t bias[8];  // ALiBi: slope2 * (2j, 2j+1) for the next pair j of each of 8 chains
     uint64_t step;     // ALiBi: 16 slope2 in both lanes (8 pairs further on)
     __device__ __forceinline__ void init(const Bf16Params &p, int h) {
-        float a0, a1 = 0.f, a2 = 0.f;
+        float a0, a1 = 0.f;
         if constexpr (SCORE == FLEX_SCORE_SOFTCAP) {
-            // cap tanh(y) = cap - 2 cap / (exp(2y) + 1),  y = scale s / cap
-            a0 = 2.f * p.scale * kLog2e / p.score_param;
-            a1 = -2.f * p.score_param * kLog2e;
-            a2 = p.score_param * kLog2e;
+            a0 = p.scale / p.score_param;
+            a1 = p.score_param * kLog2e;
         } else {
             a0 = p.scale * kLog2e;
         }
         k0 = f2_pack(a0, a0);
         k1 = f2_pack(a1, a1);
-        k2 = f2_pack(a2, a2);
-        one = f2_pack(1.f, 1.f);
         slope2 = SCORE == FLEX_SCORE_ALIBI ? kLog2e * exp2f(-8.f * (float)(h + 1) / (float)p.H) : 0.f;
         step = f2_pack(16.f * slope2, 16.f * slope2);
         offset = 0.f;
@@ -244,9 +243,7 @@ struct ScoreLog2 {
         if constexpr (SCORE == FLEX_SCORE_SOFTCAP) {
             float t0, t1;
             f2_unpack(f2_mul(s2, k0), t0, t1);
-            float u0, u1;
-            f2_unpack(f2_add(f2_pack(ex2_approx(t0), ex2_approx(t1)), one), u0, u1);
-            return f2_fma(k1, f2_pack(rcp_approx(u0), rcp_approx(u1)), k2);
+            return f2_mul(f2_pack(tanh_approx(t0), tanh_approx(t1)), k1);
         } else if constexpr (SCORE == FLEX_SCORE_ALIBI) {
             const uint64_t x = f2_fma(s2, k0, bias[j & 7]);
             bias[j & 7] = f2_add(bias[j & 7], step);
@@ -848,9 +845,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         tmem_st32(o_addr + c0, o);
                     }
                 }
-                uint64_t rs2[4];
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) rs2[k4] = 0ull;
+                float rsum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int gq = 0; gq < 4; ++gq) {
                     uint32_t pk[16];
@@ -859,22 +854,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const int j = 16 * gq + t2;
                         float d0, d1;
                         f2_unpack(f2_add(x2[j], sub2), d0, d1);
-                        const float p0 = ex2_approx(d0);
-                        const float p1 = ex2_approx(d1);
-                        rs2[j & 3] = f2_add(rs2[j & 3], f2_pack(p0, p1));
-                        pk[t2] = pack_bf16x2(p0, p1);
+                        pk[t2] = pack_bf16x2(ex2_approx(d0), ex2_approx(d1));
                     }
                     tmem_st16(s_addr + 16 * gq, pk);
+                    // the row sum takes the bf16 weights the PV MMA reads,
+                    // so each row's weights sum to l exactly
+#pragma unroll
+                    for (int t2 = 0; t2 < 16; ++t2) add_bf16x2_to_f32(rsum4[2 * (t2 & 1)], rsum4[2 * (t2 & 1) + 1], pk[t2]);
                 }
                 tmem_wait_st();
                 tc_fence_before_sync();
                 mbar_arrive(&ms.p_full[i]);
-                float rsum;
-                {
-                    float a0, a1;
-                    f2_unpack(f2_add(f2_add(rs2[0], rs2[1]), f2_add(rs2[2], rs2[3])), a0, a1);
-                    rsum = a0 + a1;
-                }
+                const float rsum = (rsum4[0] + rsum4[1]) + (rsum4[2] + rsum4[3]);
                 l_run = fmaf(l_run, alpha, rsum);
                 ++cnt;
                 ++cnt_total;

@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_dkdv_kernel(A
     const float slope = exp2f(-8.f * (float)(h + 1) / (float)p.H);
 
     const int64_t col = (int64_t)bh * p.nkvb + kvb;
-    const int nfull = a.fq_num[col], npart = a.q_num[col];
+    // counts clamped and out-of-range indices skipped (malformed lists stay in bounds)
+    const int nfull = min(max(a.fq_num[col], 0), p.nqb), npart = min(max(a.q_num[col], 0), p.nqb);
     const int32_t *fidx = a.fq_idx + col * p.nqb, *pidx = a.q_idx + col * p.nqb;
     const T *qbase = static_cast<const T *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1];
     const T *gbase = static_cast<const T *>(a.dout) + (int64_t)bh * p.q_len * D;
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_dkdv_kernel(A
     for (int t = 0; t < nfull + npart; ++t) {
         const bool full = t < nfull;
         const int qb = full ? fidx[t] : pidx[t - nfull];
+        if ((unsigned)qb >= (unsigned)p.nqb) continue;  // uniform over the CTA
         const int q0 = qb * kBlock;
         __syncthreads();  // the previous q block is consumed
         stage_tile<D, C::kThreads>(qs, qbase, p.q_stride[2], q0, p.q_len);
@@ -238,14 +240,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_dq_kernel(Att
     const float slope = exp2f(-8.f * (float)(h + 1) / (float)p.H);
 
     const int64_t bhq = (int64_t)bh * p.nqb + qb;
-    const int nfull = p.full_num[bhq], npart = p.kv_num[bhq];
+    const int nfull = min(max(p.full_num[bhq], 0), p.nkvb), npart = min(max(p.kv_num[bhq], 0), p.nkvb);
     const int32_t *fidx = p.full_idx + bhq * p.nkvb, *pidx = p.kv_idx + bhq * p.nkvb;
     const T *kbase = static_cast<const T *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
     const T *vbase = static_cast<const T *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1];
 
     for (int t = 0; t < nfull + npart; ++t) {
         const bool full = t < nfull;
-        const int kv0 = (full ? fidx[t] : pidx[t - nfull]) * kBlock;
+        const int kvb = full ? fidx[t] : pidx[t - nfull];
+        if ((unsigned)kvb >= (unsigned)p.nkvb) continue;  // uniform over the CTA
+        const int kv0 = kvb * kBlock;
         __syncthreads();
         stage_tile<D, C::kThreads>(ks, kbase, p.k_stride[2], kv0, p.kv_len);
         stage_tile<D, C::kThreads>(vs, vbase, p.v_stride[2], kv0, p.kv_len);

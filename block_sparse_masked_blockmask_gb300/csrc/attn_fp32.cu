@@ -61,7 +61,9 @@ __global__ void __launch_bounds__(Fp32Cfg<D>::kThreads) attn_fp32_kernel(AttnPro
     const float slope = exp2f(-8.f * (float)(h + 1) / (float)p.H);
     float m = -INFINITY, l = 0.f;
 
-    const int nfull = p.full_num[bhq], npart = p.kv_num[bhq];
+    // counts clamped to [0, NKVB] and indices outside [0, NKVB) skipped, so a
+    // malformed BlockMask cannot send a load out of bounds
+    const int nfull = min(max(p.full_num[bhq], 0), p.nkvb), npart = min(max(p.kv_num[bhq], 0), p.nkvb);
     const int32_t *fidx = p.full_idx + bhq * p.nkvb;
     const int32_t *pidx = p.kv_idx + bhq * p.nkvb;
     const float *kbase = static_cast<const float *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
@@ -70,6 +72,7 @@ __global__ void __launch_bounds__(Fp32Cfg<D>::kThreads) attn_fp32_kernel(AttnPro
     for (int t = 0; t < nfull + npart; ++t) {
         const bool full = t < nfull;
         const int kvb = full ? fidx[t] : pidx[t - nfull];
+        if ((unsigned)kvb >= (unsigned)p.nkvb) continue;  // the same for every thread of the CTA
         const int kv0 = kvb * kBlock;
         __syncthreads();  // previous tile fully consumed
         for (int i = threadIdx.x; i < kBlock * D / 4; i += C::kThreads) {

@@ -263,6 +263,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Hyperbolic tangent, the hardware's approximation (relative error ~2^-11).
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float rcp_approx(float x) {
     float y;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -317,6 +324,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// a += lo, b += hi of a packed bf16x2 (`lo` in bits 0-15), each bf16 taken
+// exactly into the fp32 add (mixed-precision add of sm_100 and later).
+__device__ __forceinline__ void add_bf16x2_to_f32(float &a, float &b, uint32_t v) {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %0;\n\t"
+        "add.rn.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(a), "+f"(b)
+        : "r"(v));
 }
 
 }  // namespace flex

@@ -106,6 +106,12 @@ def _doc_mask_struct(S):
     return bm
 
 
+def _doc_kv_mask_struct(q, kv):
+    bm = _mask_struct(q=q, kv=kv, kind=fa.FLEX_MASK_DOCUMENT)
+    bm.params.doc_ids = 0x4000
+    return bm
+
+
 def _fwd(lib, q, k, v, bm, score=fa.FLEX_SCORE_IDENTITY, param=0.0, scale=0.125, out=0x20000, lse=0x30000):
     return lib.flex_attention_fwd(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(bm), score,
                                   param, scale, ctypes.c_void_p(out), ctypes.c_void_p(lse), None)
@@ -136,6 +142,10 @@ def test_attention_rejects_bad_arguments(lib):
         # document masks need Q_LEN a multiple of 4
         (dict(q=_tensor(bf, [1, 2, 202, 64]), k=_tensor(bf, [1, 2, 202, 64]), v=_tensor(bf, [1, 2, 202, 64]),
               bm=_doc_mask_struct(202)), fa.FLEX_ERR_UNSUPPORTED),
+        # ... and Q_LEN == KV_LEN: a caller-filled document BlockMask with more
+        # kv rows than ids per row is refused before anything is launched
+        (dict(k=_tensor(bf, [1, 2, 384, 64]), v=_tensor(bf, [1, 2, 384, 64]),
+              bm=_doc_kv_mask_struct(256, 384)), fa.FLEX_ERR_SHAPE),
     ]
     for change, code in cases:
         args = dict(q=q, k=_tensor(bf, [1, 2, 256, 64]), v=_tensor(bf, [1, 2, 256, 64]), bm=bm)
