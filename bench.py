@@ -243,7 +243,7 @@ def main():
                     help="(b, h) chunks of flex_attention_fwd_host, whose copies overlap the work")
     ap.add_argument("--option-steps", type=int, default=20,
                     help="launches per kernel-option variant (OUTPUT_MAX, PRESCALE_QK, ...); 0 skips them")
-    ap.add_argument("--backward-steps", type=int, default=3,
+    ap.add_argument("--backward-steps", type=int, default=5,
                     help="timed flex_attention_bwd launches on the same workload; 0 skips them")
     ap.add_argument("--config-steps", type=int, default=20,
                     help="timed attention launches on each of the five synthetic configurations; 0 skips them")
@@ -374,11 +374,14 @@ def kernel_option_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flush,
 FP32_CUDA_CORE_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
-def backward_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flops_fwd, steps):
+def backward_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flops_fwd, steps, peaks):
     """flex_attention_bwd on the bench workload (outside the headline's timed region).
 
     Algorithmic FLOPs: per computed pair, the recomputed score and dP dots and
-    the dV, dK, dQ updates, 10 D, i.e. 2.5 x the forward's 4 D.
+    the dV, dK, dQ updates, 10 D, i.e. 2.5 x the forward's 4 D.  The bf16
+    kernels execute 14 D per pair (the dQ kernel recomputes the score and dP
+    dots instead of accumulating dQ across CTAs); the roofline counts the
+    algorithmic 10 D.
     """
     if steps <= 0:
         return None
@@ -409,11 +412,20 @@ def backward_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flops_fwd, 
     ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
     flops = 2.5 * flops_fwd
     achieved = flops / (ms * 1e-3) / 1e12
+    if w.dtype == "bf16":
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16"],
+                "frac_of_sustained": achieved / peaks["bf16_sustained"] if peaks["bf16_sustained"] else None,
+                "peak_source": f"{peaks['source']} bf16 burst (dense cuBLAS); frac_of_sustained: the seconds-long figure",
+                "executed_mma_flops": 3.5 * flops_fwd,
+                "kernels": "attn_bwd_delta (CUDA cores) + attn_bwd_tc<dK,dV> + attn_bwd_tc<dQ> (tcgen05)"}
+    else:
+        roof = {"bound": "alu", "achieved": achieved, "peak": FP32_CUDA_CORE_TFLOPS, "unit": "TFLOP/s",
+                "frac": achieved / FP32_CUDA_CORE_TFLOPS,
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
+                "kernels": "attn_bwd_delta + attn_bwd_dkdv + attn_bwd_dq (fp32 FMA, CUDA cores)"}
     return {"api": "flex_attention_bwd", "launches": steps, "ms_per_launch": ms, "algorithmic_flops": flops,
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_CUDA_CORE_TFLOPS, "unit": "TFLOP/s",
-                         "frac": achieved / FP32_CUDA_CORE_TFLOPS,
-                         "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
-                         "kernels": "attn_bwd_delta + attn_bwd_dkdv + attn_bwd_dq (fp32 FMA, CUDA cores)"}}
+            "roofline": roof}
 
 
 def run_ours(args, w: W.Workload) -> None:
@@ -545,7 +557,8 @@ def run_ours(args, w: W.Workload) -> None:
     # and leaves the forward's numbers above as measured
     backward = None
     try:
-        backward = backward_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flops, args.backward_steps)
+        backward = backward_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flops, args.backward_steps,
+                                    peaks)
     except Exception as exc:  # noqa: BLE001
         backward = {"error": f"{type(exc).__name__}: {exc}"}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

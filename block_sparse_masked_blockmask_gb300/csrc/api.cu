@@ -345,6 +345,8 @@ int flex_attention_bwd(const flex_tensor *q, const flex_tensor *k, const flex_te
         return FLEX_ERR_SHAPE;
     if (!bq->q_num_blocks || !bq->q_indices || !bq->full_q_num_blocks || !bq->full_q_indices)
         return FLEX_ERR_INVALID_ARG;
+    // the tensor-core backward holds a kv block's list of q blocks on chip
+    if (q->dtype == FLEX_DTYPE_BF16 && bm->nqb > kBwdTcMaxQBlocks) return FLEX_ERR_UNSUPPORTED;
     return launch_attn_bwd(p, q->dtype, dout, bq->q_num_blocks, bq->q_indices, bq->full_q_num_blocks,
                            bq->full_q_indices, dq, dk, dv, delta, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? FLEX_OK

@@ -26,9 +26,11 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+}  // namespace
+
 // [B, H, S, D] bf16 with element strides st (st[3] == 1) as a 4-D tensor map
 // whose box is 64 (D) x 128 (S) x 1 x 1.
-bool make_map(CUtensorMap *map, const void *base, int B, int H, int S, int D, const int64_t st[4]) {
+bool make_bf16_tile_map(CUtensorMap *map, const void *base, int B, int H, int S, int D, const int64_t st[4]) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
@@ -40,13 +42,11 @@ bool make_map(CUtensorMap *map, const void *base, int B, int H, int S, int D, co
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
 cudaError_t launch_attn_bf16(const AttnProblem &p, cudaStream_t stream) {
     CUtensorMap tq, tk, tv;
-    if (!make_map(&tq, p.q, p.B, p.H, p.q_len, p.D, p.q_stride) ||
-        !make_map(&tk, p.k, p.B, p.H, p.kv_len, p.D, p.k_stride) ||
-        !make_map(&tv, p.v, p.B, p.H, p.kv_len, p.D, p.v_stride))
+    if (!make_bf16_tile_map(&tq, p.q, p.B, p.H, p.q_len, p.D, p.q_stride) ||
+        !make_bf16_tile_map(&tk, p.k, p.B, p.H, p.kv_len, p.D, p.k_stride) ||
+        !make_bf16_tile_map(&tv, p.v, p.B, p.H, p.kv_len, p.D, p.v_stride))
         return cudaErrorInvalidValue;
     Bf16Params kp;
     kp.B = p.B;

@@ -1,8 +1,10 @@
 // Backward pass of the block-sparse attention (the flex_attention_backward op
 // of "[Inductor][Flex Attention] Add Subtiling Option for Alpha Scaling",
 // PyTorch PR #167356, test diffs: it takes q, k, v, the forward's out and lse,
-// and the output gradient, and returns dq, dk, dv), on the CUDA cores with
-// fp32 arithmetic for bf16 and fp32 inputs.
+// and the output gradient, and returns dq, dk, dv).  fp32 inputs run on the
+// CUDA cores with fp32 arithmetic (the kernels below); bf16 inputs take delta
+// from the kernel below and dq, dk, dv from the tensor-core kernels of
+// attn_bwd_tc.cuh.
 //
 // With t = scale q.k, s = score_mod(t) where mask_mod holds, P = exp(s - lse):
 //   delta_i = dO_i . out_i
@@ -18,6 +20,7 @@
 // Each thread owns 32 of a row's D dims, as 8 groups of 4 contiguous floats
 // spaced 4 * (threads per row) apart, so the row's threads read distinct
 // shared-memory banks when they fetch the same staged row.
+#include "attn_bwd_tc.cuh"
 #include "bwd_internal.h"
 #include "ptx.cuh"
 
@@ -384,12 +387,71 @@ cudaError_t launch_block_mask_transpose(const int32_t *kv_num, const int32_t *kv
     return cudaGetLastError();
 }
 
+static_assert(kBwdTcMaxQBlocks == kBwdMaxList, "list capacity of the tensor-core backward");
+
+namespace {
+
+// bf16: delta on the CUDA cores, then the tensor-core dK/dV and dQ kernels.
+cudaError_t launch_bwd_bf16_tc(const AttnProblem &p, const BwdArgs &a, cudaStream_t stream) {
+    const int64_t rows = (int64_t)p.B * p.H * p.q_len;
+    if (p.D == 64)
+        attn_bwd_delta_kernel<64, uint16_t><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, stream>>>(p, a, rows);
+    else
+        attn_bwd_delta_kernel<128, uint16_t><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, stream>>>(p, a, rows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t dstr[4] = {(int64_t)p.H * p.q_len * p.D, (int64_t)p.q_len * p.D, p.D, 1};
+    CUtensorMap mq, mk, mv, mdo;
+    if (!make_bf16_tile_map(&mq, p.q, p.B, p.H, p.q_len, p.D, p.q_stride) ||
+        !make_bf16_tile_map(&mk, p.k, p.B, p.H, p.kv_len, p.D, p.k_stride) ||
+        !make_bf16_tile_map(&mv, p.v, p.B, p.H, p.kv_len, p.D, p.v_stride) ||
+        !make_bf16_tile_map(&mdo, a.dout, p.B, p.H, p.q_len, p.D, dstr))
+        return cudaErrorInvalidValue;
+    BwdTcParams kp;
+    kp.B = p.B;
+    kp.H = p.H;
+    kp.q_len = p.q_len;
+    kp.kv_len = p.kv_len;
+    kp.bh_begin = p.bh_begin;
+    kp.nbh = p.bh_count;
+    kp.mask = p.mask;
+    kp.scale = p.scale;
+    kp.score_param = p.score_param;
+    kp.lse = p.lse;
+    kp.delta = a.delta;
+    kp.status = p.status;
+    // dK, dV: own the kv blocks, walk the q side of the BlockMask
+    kp.nblocks = p.nkvb;
+    kp.nlist = p.nqb;
+    kp.num = a.q_num;
+    kp.idx = a.q_idx;
+    kp.fnum = a.fq_num;
+    kp.fidx = a.fq_idx;
+    kp.out0 = static_cast<uint16_t *>(a.dv);
+    kp.out1 = static_cast<uint16_t *>(a.dk);
+    const CUtensorMap kv_maps[4] = {mk, mv, mq, mdo};
+    e = launch_bwd_tc_dkdv(kv_maps, kp, p.D, p.score_kind, stream);
+    if (e != cudaSuccess) return e;
+    // dQ: own the q blocks, walk the kv side
+    kp.nblocks = p.nqb;
+    kp.nlist = p.nkvb;
+    kp.num = p.kv_num;
+    kp.idx = p.kv_idx;
+    kp.fnum = p.full_num;
+    kp.fidx = p.full_idx;
+    kp.out0 = static_cast<uint16_t *>(a.dq);
+    kp.out1 = nullptr;
+    const CUtensorMap q_maps[4] = {mq, mdo, mk, mv};
+    return launch_bwd_tc_dq(q_maps, kp, p.D, p.score_kind, stream);
+}
+
+}  // namespace
+
 cudaError_t launch_attn_bwd(const AttnProblem &p, int dtype, const void *dout, const int32_t *q_num,
                             const int32_t *q_idx, const int32_t *fq_num, const int32_t *fq_idx, void *dq, void *dk,
                             void *dv, float *delta, cudaStream_t stream) {
     const BwdArgs a{dout, q_num, q_idx, fq_num, fq_idx, dq, dk, dv, delta};
-    if (dtype == FLEX_DTYPE_BF16)
-        return p.D == 64 ? launch_bwd_typed<64, uint16_t>(p, a, stream) : launch_bwd_typed<128, uint16_t>(p, a, stream);
+    if (dtype == FLEX_DTYPE_BF16) return launch_bwd_bf16_tc(p, a, stream);
     return p.D == 64 ? launch_bwd_typed<64, float>(p, a, stream) : launch_bwd_typed<128, float>(p, a, stream);
 }
 

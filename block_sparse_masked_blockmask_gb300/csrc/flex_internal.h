@@ -92,6 +92,10 @@ cudaError_t launch_block_mask(const MaskDesc &mask, int B, int H, int q_len, int
 cudaError_t launch_attn_fp32(const AttnProblem &p, cudaStream_t stream);
 cudaError_t launch_attn_bf16(const AttnProblem &p, cudaStream_t stream);
 
+// TMA tensor map of a bf16 [B, H, S, D] tensor with element strides st
+// (st[3] == 1): 64 x 128 boxes (head dims x rows), 128-byte swizzle.
+bool make_bf16_tile_map(CUtensorMap *map, const void *base, int B, int H, int S, int D, const int64_t st[4]);
+
 cudaError_t launch_wait_timeout_selftest(int *status, uint64_t limit_ns, cudaStream_t stream);
 
 // The per-device workspace holding the status word (allocated once per device).

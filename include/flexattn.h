@@ -354,10 +354,12 @@ FLEX_API int flex_block_mask_transpose(const flex_block_mask *bm, flex_block_mas
  *   dq:   device, contiguous [B, H, q_len, D]; dk, dv: [B, H, kv_len, D];
  *         q's dtype, 16-byte aligned.
  *   delta: device workspace, [B, H, q_len] float32 (dout[i].out[i]).
- * Rows whose lse is -inf (no unmasked score) contribute nothing.  The
- * arithmetic is fp32 on the CUDA cores for both dtypes.  Errors: those of
- * flex_attention_fwd, and FLEX_ERR_SHAPE when bq does not match bm.
- * Asynchronous on `stream`.
+ * Rows whose lse is -inf (no unmasked score) contribute nothing.  bf16
+ * inputs run on the tensor cores (S, dP and the gradient products as tcgen05
+ * MMAs with fp32 accumulation; P and dS rounded to bf16 as MMA operands) and
+ * need NQB <= 2048; fp32 inputs run in fp32 on the CUDA cores.  Errors: those
+ * of flex_attention_fwd, FLEX_ERR_SHAPE when bq does not match bm, and
+ * FLEX_ERR_UNSUPPORTED for bf16 with NQB > 2048.  Asynchronous on `stream`.
  */
 FLEX_API int flex_attention_bwd(const flex_tensor *q, const flex_tensor *k, const flex_tensor *v, const void *out,
                                 const float *lse, const void *dout, const flex_block_mask *bm,
