@@ -22,11 +22,14 @@
 //               S = Q_i K_j^T, dP = dO_i V_j^T, dS, dQ_i += dS K_j.
 // Each CTA owns its output rows, so nothing is accumulated across CTAs and
 // the result does not depend on scheduling.  P is recomputed from the saved
-// lse (no running max).  Roles (192 threads, one CTA per SM):
-//   warps 0-3  elementwise, one thread per owned row (TMEM lane = row)
-//   warp 4     TMA: the CTA's two resident tiles, then the two streamed
+// lse (no running max).  Roles (320 threads, one CTA per SM):
+//   warps 0-7  elementwise, two threads per owned row (TMEM lane = row):
+//              warps w and w + 4 share a TMEM lane quarter, the first takes
+//              the walked columns 0-63, the second 64-127 (the backward
+//              needs no row reductions, so the halves never talk)
+//   warp 8     TMA: the CTA's two resident tiles, then the two streamed
 //              tiles of each list step into a ring of stages
-//   warp 5     one thread issues every tcgen05.mma
+//   warp 9     one thread issues every tcgen05.mma
 // The MMA thread issues, per step n: dV(n) once P(n) is in TMEM, S(n+1)
 // (into the columns P(n) was read from: MMAs execute in issue order), dK(n)
 // (or dQ(n)) once dS(n) is in TMEM, then dP(n+1) (over dS(n)), so the
@@ -43,9 +46,9 @@
 
 namespace flex {
 
-constexpr int kBwdThreads = 192;
-constexpr int kBwdTmaWarp = 4;
-constexpr int kBwdMmaWarp = 5;
+constexpr int kBwdThreads = 320;
+constexpr int kBwdTmaWarp = 8;
+constexpr int kBwdMmaWarp = 9;
 constexpr int kBwdMaxList = 2048;    // list steps per CTA held on chip (q blocks of a kv block)
 constexpr int kBwdHeadGroup = 4;     // (batch, head) pairs scheduled together (their tiles stay in L2)
 constexpr float kBwdLog2e = 1.4426950408889634f;
@@ -90,8 +93,10 @@ struct BwdTcCfg {
     static constexpr uint32_t kStageBytes = 2 * kTileBytes;
     static constexpr uint32_t kMiscOff = kStrOff + kStages * kStageBytes;
     static constexpr uint32_t kSmemBytes = kMiscOff + sizeof(BwdMisc) + 1024;
-    // TMEM columns: S | dP | acc0 | acc1.  P (KV_MAJOR) overwrites S's first
-    // 64 columns as bf16, dS overwrites dP's.
+    // TMEM columns: S | dP | acc0 | acc1.  P (KV_MAJOR) and dS are written
+    // back as bf16 over the columns they came from: the walked columns
+    // 64h .. 64h + 63 of S (dP) pack into S's (dP's) columns 64h .. 64h + 31,
+    // so each column half writes only where it has read.
     static constexpr uint32_t kS = 0, kDP = 128, kAcc0 = 256, kAcc1 = 256 + D;
     static constexpr uint32_t kTmemCols = 512;
 };
@@ -131,6 +136,30 @@ __device__ __forceinline__ void bwd_tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
           "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
           "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr)
+        : "memory");
+}
+
+// TMEM read of 64 columns of this thread's lane (two 32-column loads, one
+// wait), completed before returning.
+__device__ __forceinline__ void bwd_tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+        "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]),
+          "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]),
+          "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
+          "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]),
+          "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr), "r"(taddr + 32)
         : "memory");
 }
 
@@ -203,8 +232,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mbar_init(&ms.s_full, 1);
         mbar_init(&ms.dp_full, 1);
-        mbar_init(&ms.p_ready, 128);
-        mbar_init(&ms.ds_ready, 128);
+        mbar_init(&ms.p_ready, 256);
+        mbar_init(&ms.ds_ready, 256);
         mbar_init(&ms.acc_full, 1);
         mbar_init(&ms.drain, 1);
         mbar_init(&ms.col_ready[0], 128);
@@ -313,12 +342,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mma_ss_lo<kHi, kHi>(tmem + dcol, a_lo + off, b_lo + off, idesc_ss, k > 0 ? 1u : 0u);
                 }
             };
-            // acc (128 x D) += A (TMEM, 128 x 128 bf16) times B (128 walked rows x D, MN-major)
+            // acc (128 x D) += A (TMEM, 128 x 128 bf16) times B (128 walked rows x D, MN-major);
+            // A's walked columns 16k .. 16k + 15 sit at TMEM column 64 (k / 4) + 8 (k % 4)
             auto issue_ts = [&](uint32_t dcol, uint32_t acol, uint32_t b_mn, bool acc) {
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
-                    mma_ts_lo<kHi>(tmem + dcol, tmem + acol + k * 8, b_mn + ((k * 2048) >> 4), idesc_acc,
-                                   (k > 0 || acc) ? 1u : 0u);
+                    mma_ts_lo<kHi>(tmem + dcol, tmem + acol + 64 * (k / 4) + 8 * (k % 4), b_mn + ((k * 2048) >> 4),
+                                   idesc_acc, (k > 0 || acc) ? 1u : 0u);
             };
             constexpr uint32_t stage16 = C::kStageBytes >> 4;
             bool ok = mbar_wait(&ms.res_full, 0, abort_flag) && mbar_wait(&ms.str_full[0], 0, abort_flag);
@@ -368,7 +398,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncwarp();
     } else {
         // ----------------------------------------------------- elementwise
-        const int t = threadIdx.x;  // 0..127: owned row within the block, TMEM lane
+        const int t = threadIdx.x % 128;   // owned row within the block, TMEM lane
+        const int half = threadIdx.x / 128;  // walked columns 64 half .. 64 half + 63
+        const int cbase = 64 * half;
         const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
         const uint32_t trow = tmem + lane_base;
         const int row = own * 128 + t;  // kv (KV_MAJOR) or q
@@ -393,11 +425,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 ndelta_row = -__ldg(p.delta + (int64_t)bh * p.q_len + row);
             }
         }
-        // Per-column data of a step, column t loaded by thread t:
+        // Per-column data of a step, column t loaded by thread t of the first
+        // half:
         //   KV_MAJOR: colv = -(lse2 + slope2 c) of q column c (-inf for a q
         //             row without unmasked scores or past Q_LEN), dltv = -delta
         //   Q-major : colv = slope2 c (ALiBi column term)
         //   DOC     : docv = document id of the walked row
+        const bool loader = half == 0;
         float cv = 0.f, dv_ = 0.f;
         int dc = 0;
         auto load_col = [&](int n) {
@@ -423,13 +457,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_arrive(&ms.col_ready[buf]);
         };
         bool ok = true;
-        if (N > 0) {
+        if (N > 0 && loader) {
             load_col(0);
             store_col(0);
         }
         for (int n = 0; n < N; ++n) {
             const int buf = n & 1;
-            if (n + 1 < N) load_col(n + 1);  // in flight while this step computes
+            if (n + 1 < N && loader) load_col(n + 1);  // in flight while this step computes
             if (!bwd_warp_wait(&ms.col_ready[buf], (uint32_t)(n >> 1) & 1u, abort_flag)) {
                 ok = false;
                 break;
@@ -474,74 +508,76 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 rowc = SCORE == FLEX_SCORE_ALIBI ? slope2 * (float)(w0 - row) - lse2_row : -lse2_row;
             }
             const uint64_t rowc2 = f2_pack(rowc, rowc);
-            const float4 *colv4 = reinterpret_cast<const float4 *>(ms.colv[buf]);
-            const float4 *dltv4 = reinterpret_cast<const float4 *>(ms.dltv[buf]);
-            const int4 *docv4 = reinterpret_cast<const int4 *>(ms.docv[buf]);
+            const float4 *colv4 = reinterpret_cast<const float4 *>(ms.colv[buf] + cbase);
+            const float4 *dltv4 = reinterpret_cast<const float4 *>(ms.dltv[buf] + cbase);
+            const int4 *docv4 = reinterpret_cast<const int4 *>(ms.docv[buf] + cbase);
 
             if (!bwd_warp_wait(&ms.s_full, (uint32_t)n & 1u, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
-            // ---- phase 1: P (and P score_mod') from S
-            float pg[128];
+            // ---- phase 1: P (and P score_mod') from S, this half's 64 columns
+            float pg[64];
+            {
+                uint32_t r[64];
+                bwd_tmem_ld64(trow + C::kS + cbase, r);
 #pragma unroll
-            for (int c0 = 0; c0 < 4; ++c0) {
-                uint32_t r[32];
-                bwd_tmem_ld32(trow + C::kS + 32 * c0, r);
-                uint32_t keep = 0xFFFFFFFFu;
-                if (!full) {
-                    keep = interval_bits(clo, chi, 32 * c0);
-                    if constexpr (DOC) {
-                        uint32_t same = 0u;
+                for (int c0 = 0; c0 < 2; ++c0) {
+                    uint32_t keep = 0xFFFFFFFFu;
+                    if (!full) {
+                        keep = interval_bits(clo, chi, cbase + 32 * c0);
+                        if constexpr (DOC) {
+                            uint32_t same = 0u;
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const int4 d = docv4[8 * c0 + j];
-                            same |= ((uint32_t)(d.x == doc_own) | ((uint32_t)(d.y == doc_own) << 1) |
-                                     ((uint32_t)(d.z == doc_own) << 2) | ((uint32_t)(d.w == doc_own) << 3))
-                                    << (4 * j);
+                            for (int j = 0; j < 8; ++j) {
+                                const int4 d = docv4[8 * c0 + j];
+                                same |= ((uint32_t)(d.x == doc_own) | ((uint32_t)(d.y == doc_own) << 1) |
+                                         ((uint32_t)(d.z == doc_own) << 2) | ((uint32_t)(d.w == doc_own) << 3))
+                                        << (4 * j);
+                            }
+                            keep &= same;
                         }
-                        keep &= same;
                     }
-                }
-                uint32_t pk[16];
+                    uint32_t pk[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int c = 32 * c0 + 2 * j;
-                    // bias of the pair
-                    uint64_t bias2;
-                    if constexpr (KV_MAJOR) {
-                        const float4 cc = colv4[c / 4];
-                        const uint64_t cpair = (c & 2) ? f2_pack(cc.z, cc.w) : f2_pack(cc.x, cc.y);
-                        bias2 = SCORE == FLEX_SCORE_ALIBI ? f2_add(rowc2, cpair) : cpair;
-                    } else {
-                        if constexpr (SCORE == FLEX_SCORE_ALIBI) {
+                    for (int j = 0; j < 16; ++j) {
+                        const int c = 32 * c0 + 2 * j;  // within the half
+                        uint64_t bias2;
+                        if constexpr (KV_MAJOR) {
                             const float4 cc = colv4[c / 4];
-                            bias2 = f2_add(rowc2, (c & 2) ? f2_pack(cc.z, cc.w) : f2_pack(cc.x, cc.y));
+                            const uint64_t cpair = (c & 2) ? f2_pack(cc.z, cc.w) : f2_pack(cc.x, cc.y);
+                            bias2 = SCORE == FLEX_SCORE_ALIBI ? f2_add(rowc2, cpair) : cpair;
                         } else {
-                            bias2 = rowc2;
+                            if constexpr (SCORE == FLEX_SCORE_ALIBI) {
+                                const float4 cc = colv4[c / 4];
+                                bias2 = f2_add(rowc2, (c & 2) ? f2_pack(cc.z, cc.w) : f2_pack(cc.x, cc.y));
+                            } else {
+                                bias2 = rowc2;
+                            }
                         }
+                        const uint64_t s2 = f2_pack(__uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+                        float x0, x1, g0 = 1.f, g1 = 1.f;
+                        if constexpr (SCORE == FLEX_SCORE_SOFTCAP) {
+                            float t0, t1;
+                            f2_unpack(f2_mul(s2, k0_2), t0, t1);
+                            const float u0 = tanh_approx(t0), u1 = tanh_approx(t1);
+                            f2_unpack(f2_fma(f2_pack(u0, u1), k1_2, bias2), x0, x1);
+                            g0 = fmaf(-u0, u0, 1.f);
+                            g1 = fmaf(-u1, u1, 1.f);
+                        } else {
+                            f2_unpack(f2_fma(s2, k0_2, bias2), x0, x1);
+                        }
+                        if (!((keep >> (2 * j)) & 1u)) x0 = -INFINITY;
+                        if (!((keep >> (2 * j + 1)) & 1u)) x1 = -INFINITY;
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        if constexpr (KV_MAJOR) pk[j] = pack_bf16x2(p0, p1);
+                        pg[c] = p0 * g0;
+                        pg[c + 1] = p1 * g1;
                     }
-                    const uint64_t s2 = f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                    float x0, x1, g0 = 1.f, g1 = 1.f;
-                    if constexpr (SCORE == FLEX_SCORE_SOFTCAP) {
-                        float t0, t1;
-                        f2_unpack(f2_mul(s2, k0_2), t0, t1);
-                        const float u0 = tanh_approx(t0), u1 = tanh_approx(t1);
-                        f2_unpack(f2_fma(f2_pack(u0, u1), k1_2, bias2), x0, x1);
-                        g0 = fmaf(-u0, u0, 1.f);
-                        g1 = fmaf(-u1, u1, 1.f);
-                    } else {
-                        f2_unpack(f2_fma(s2, k0_2, bias2), x0, x1);
-                    }
-                    if (!((keep >> (2 * j)) & 1u)) x0 = -INFINITY;
-                    if (!((keep >> (2 * j + 1)) & 1u)) x1 = -INFINITY;
-                    const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                    if constexpr (KV_MAJOR) pk[j] = pack_bf16x2(p0, p1);
-                    pg[c] = p0 * g0;
-                    pg[c + 1] = p1 * g1;
+                    // over this half's S columns, all read above
+                    if constexpr (KV_MAJOR) tmem_st16(trow + C::kS + cbase + 16 * c0, pk);
                 }
-                if constexpr (KV_MAJOR) tmem_st16(trow + C::kS + 16 * c0, pk);  // over S columns already read
             }
             if constexpr (KV_MAJOR) tmem_wait_st();
             tc_fence_before_sync();
@@ -553,33 +589,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             tc_fence_after_sync();
             // ---- phase 2: dS = P score_mod' (dP - delta) from dP
-            const uint64_t nd_row2 = f2_pack(ndelta_row, ndelta_row);
+            {
+                const uint64_t nd_row2 = f2_pack(ndelta_row, ndelta_row);
+                uint32_t r[64];
+                bwd_tmem_ld64(trow + C::kDP + cbase, r);
 #pragma unroll
-            for (int c0 = 0; c0 < 4; ++c0) {
-                uint32_t r[32];
-                bwd_tmem_ld32(trow + C::kDP + 32 * c0, r);
-                uint32_t pk[16];
+                for (int c0 = 0; c0 < 2; ++c0) {
+                    uint32_t pk[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int c = 32 * c0 + 2 * j;
-                    uint64_t nd2;
-                    if constexpr (KV_MAJOR) {
-                        const float4 dd = dltv4[c / 4];
-                        nd2 = (c & 2) ? f2_pack(dd.z, dd.w) : f2_pack(dd.x, dd.y);
-                    } else {
-                        nd2 = nd_row2;
+                    for (int j = 0; j < 16; ++j) {
+                        const int c = 32 * c0 + 2 * j;
+                        uint64_t nd2;
+                        if constexpr (KV_MAJOR) {
+                            const float4 dd = dltv4[c / 4];
+                            nd2 = (c & 2) ? f2_pack(dd.z, dd.w) : f2_pack(dd.x, dd.y);
+                        } else {
+                            nd2 = nd_row2;
+                        }
+                        const uint64_t dp2 = f2_pack(__uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+                        float d0, d1;
+                        f2_unpack(f2_mul(f2_add(dp2, nd2), f2_pack(pg[c], pg[c + 1])), d0, d1);
+                        pk[j] = pack_bf16x2(d0, d1);
                     }
-                    const uint64_t dp2 = f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                    float d0, d1;
-                    f2_unpack(f2_mul(f2_add(dp2, nd2), f2_pack(pg[c], pg[c + 1])), d0, d1);
-                    pk[j] = pack_bf16x2(d0, d1);
+                    tmem_st16(trow + C::kDP + cbase + 16 * c0, pk);  // over this half's dP columns, all read
                 }
-                tmem_st16(trow + C::kDP + 16 * c0, pk);  // over dP columns already read
             }
             tmem_wait_st();
             tc_fence_before_sync();
             mbar_arrive(&ms.ds_ready);
-            if (n + 1 < N) store_col((n + 1) & 1);
+            if (n + 1 < N && loader) store_col((n + 1) & 1);
         }
         // ------------------------------------------------------- epilogue
         bool have = ok && N > 0;
@@ -594,14 +632,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_after_sync();
             const bool store = row < own_len;
             const int64_t orow = (int64_t)bh * own_len + (store ? row : 0);
-            // KV_MAJOR: acc0 = dV, acc1 = dK (scaled); Q-major: acc0 = dQ (scaled)
+            // KV_MAJOR: acc0 = dV, acc1 = dK (scaled); Q-major: acc0 = dQ (scaled).
+            // Each half writes D / 2 of the row's columns.
 #pragma unroll 1
             for (int which = 0; which < (KV_MAJOR ? 2 : 1); ++which) {
                 const float mul = (KV_MAJOR && which == 0) ? 1.f : p.scale;
                 uint4 *dst = reinterpret_cast<uint4 *>((which == 0 ? p.out0 : p.out1) + orow * D);
-                const uint32_t col = which == 0 ? C::kAcc0 : C::kAcc1;
+                const uint32_t col = (which == 0 ? C::kAcc0 : C::kAcc1) + half * (D / 2);
 #pragma unroll 1
-                for (int c0 = 0; c0 < D; c0 += 32) {
+                for (int c0 = 0; c0 < D / 2; c0 += 32) {
                     uint32_t o[32];
                     if (have) {
                         bwd_tmem_ld32(trow + col + c0, o);
@@ -616,7 +655,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (store) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            dst[c0 / 8 + j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                            dst[(half * (D / 2) + c0) / 8 + j] =
+                                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
                     }
                 }
             }
