@@ -40,11 +40,12 @@
  *       the same tuple carries for that pass, as the transpose of the kv
  *       side.
  *   block mask           -> kv_num_blocks, kv_indices, full_kv_num_blocks,
- *       full_kv_indices   (the BlockMask tuple passed to the same op): each
- *       BLOCK x BLOCK tile of the dense mask is full (all true), partial
- *       (some true) or empty; each row of an index tensor lists the selected
- *       kv blocks in ascending order followed by the unselected ones, also
- *       ascending (a stable descending sort of the 0/1 tile row).
+ *       full_kv_indices   (the BlockMask tuple passed to the same op, which
+ *       carries a Q block size and a KV block size): each Q_BLOCK x KV_BLOCK
+ *       tile of the dense mask is full (all true), partial (some true) or
+ *       empty; each row of an index tensor lists the selected kv blocks in
+ *       ascending order followed by the unselected ones, also ascending (a
+ *       stable descending sort of the 0/1 tile row).
  *
  * Inputs are float32 arrays holding the exact values the device reads
  * (bf16 values are exact in float32); every product and sum is taken in
@@ -156,25 +157,25 @@ static double or_prescale(int prescale, double scale, float q)
 }
 
 /*
- * Dense mask evaluated tile by tile; one BLOCK-row band of the mask is
+ * Dense mask evaluated tile by tile; one Q_BLOCK-row band of the mask is
  * materialised at a time to bound memory.  Lengths need not be multiples of
- * BLOCK: the dense mask is padded with false to whole tiles
- * (NQB = ceil(Q_LEN / BLOCK), NKVB = ceil(KV_LEN / BLOCK)), so a tile that
- * reaches past either length is never full.  Output layouts:
+ * the block sizes: the dense mask is padded with false to whole tiles
+ * (NQB = ceil(Q_LEN / Q_BLOCK), NKVB = ceil(KV_LEN / KV_BLOCK)), so a tile
+ * that reaches past either length is never full.  Output layouts:
  *   kv_num, full_num : [B, H, NQB]
  *   kv_idx, full_idx : [B, H, NQB, NKVB]
  */
 int oracle_block_mask(int kind, int window, int prefix, const int32_t *doc,
-                      int B, int H, int q_len, int kv_len, int block,
+                      int B, int H, int q_len, int kv_len, int q_block, int kv_block,
                       int32_t *kv_num, int32_t *kv_idx,
                       int32_t *full_num, int32_t *full_idx)
 {
-    if (!or_mask_ok(kind) || B <= 0 || H <= 0 || q_len <= 0 || kv_len <= 0 || block <= 0)
+    if (!or_mask_ok(kind) || B <= 0 || H <= 0 || q_len <= 0 || kv_len <= 0 || q_block <= 0 || kv_block <= 0)
         return OR_ERR_ARG;
     if (kind == OR_MASK_DOCUMENT && (doc == NULL || q_len != kv_len))
         return OR_ERR_ARG;
-    const int64_t nqb = ((int64_t)q_len + block - 1) / block;
-    const int64_t nkvb = ((int64_t)kv_len + block - 1) / block;
+    const int64_t nqb = ((int64_t)q_len + q_block - 1) / q_block;
+    const int64_t nkvb = ((int64_t)kv_len + kv_block - 1) / kv_block;
     or_mask m = {kind, window, prefix, doc, (int64_t)q_len};
     int err = OR_OK;
 
@@ -182,8 +183,8 @@ int oracle_block_mask(int kind, int window, int prefix, const int32_t *doc,
     for (int64_t bh = 0; bh < (int64_t)B * H; ++bh) {
         for (int64_t qb = 0; qb < nqb; ++qb) {
             int64_t b = bh / H, h = bh % H;
-            /* the dense mask of rows [qb*block, (qb+1)*block) */
-            unsigned char *band = (unsigned char *)malloc((size_t)block * (size_t)kv_len);
+            /* the dense mask of rows [qb*q_block, (qb+1)*q_block) */
+            unsigned char *band = (unsigned char *)malloc((size_t)q_block * (size_t)kv_len);
             int64_t *count = (int64_t *)calloc((size_t)nkvb, sizeof(int64_t));
             if (!band || !count) {
                 free(band);
@@ -192,16 +193,16 @@ int oracle_block_mask(int kind, int window, int prefix, const int32_t *doc,
                 err = OR_ERR_NOMEM;
                 continue;
             }
-            for (int64_t r = 0; r < block; ++r)
+            for (int64_t r = 0; r < q_block; ++r)
                 for (int64_t kv = 0; kv < kv_len; ++kv)  /* columns past KV_LEN: padding, false */
-                    band[r * kv_len + kv] = qb * block + r < q_len  /* rows past Q_LEN: padding, false */
-                                                ? (unsigned char)or_mask_mod(&m, b, h, qb * block + r, kv)
+                    band[r * kv_len + kv] = qb * q_block + r < q_len  /* rows past Q_LEN: padding, false */
+                                                ? (unsigned char)or_mask_mod(&m, b, h, qb * q_block + r, kv)
                                                 : 0;
-            for (int64_t r = 0; r < block; ++r)
+            for (int64_t r = 0; r < q_block; ++r)
                 for (int64_t kv = 0; kv < kv_len; ++kv)
-                    count[kv / block] += band[r * kv_len + kv];
+                    count[kv / kv_block] += band[r * kv_len + kv];
 
-            const int64_t all = (int64_t)block * block;
+            const int64_t all = (int64_t)q_block * kv_block;
             const int64_t row = bh * nqb + qb;
             int32_t *pi = kv_idx + row * nkvb, *fi = full_idx + row * nkvb;
             int32_t np = 0, nf = 0;
@@ -234,13 +235,13 @@ int oracle_block_mask(int kind, int window, int prefix, const int32_t *doc,
  *   q_idx, full_q_idx : [B, H, NKVB, NQB]
  */
 int oracle_block_mask_q(int kind, int window, int prefix, const int32_t *doc,
-                        int B, int H, int q_len, int kv_len, int block,
+                        int B, int H, int q_len, int kv_len, int q_block, int kv_block,
                         int32_t *q_num, int32_t *q_idx, int32_t *full_q_num, int32_t *full_q_idx)
 {
-    if (block <= 0 || q_len <= 0 || kv_len <= 0 || B <= 0 || H <= 0)
+    if (q_block <= 0 || kv_block <= 0 || q_len <= 0 || kv_len <= 0 || B <= 0 || H <= 0)
         return OR_ERR_ARG;
-    const int64_t nqb = ((int64_t)q_len + block - 1) / block;
-    const int64_t nkvb = ((int64_t)kv_len + block - 1) / block;
+    const int64_t nqb = ((int64_t)q_len + q_block - 1) / q_block;
+    const int64_t nkvb = ((int64_t)kv_len + kv_block - 1) / kv_block;
     const int64_t rows = (int64_t)B * H * nqb;
     int32_t *kn = (int32_t *)malloc((size_t)rows * sizeof(int32_t));
     int32_t *ki = (int32_t *)malloc((size_t)(rows * nkvb) * sizeof(int32_t));
@@ -249,7 +250,7 @@ int oracle_block_mask_q(int kind, int window, int prefix, const int32_t *doc,
     unsigned char *st = (unsigned char *)calloc((size_t)(nqb * nkvb), 1);
     int err = (kn && ki && fn && fi && st) ? OR_OK : OR_ERR_NOMEM;
     if (err == OR_OK)
-        err = oracle_block_mask(kind, window, prefix, doc, B, H, q_len, kv_len, block, kn, ki, fn, fi);
+        err = oracle_block_mask(kind, window, prefix, doc, B, H, q_len, kv_len, q_block, kv_block, kn, ki, fn, fi);
     for (int64_t bh = 0; err == OR_OK && bh < (int64_t)B * H; ++bh) {
         /* tile classes of this (b, h) from its kv-side lists: 1 partial, 2 full */
         memset(st, 0, (size_t)(nqb * nkvb));

@@ -55,7 +55,7 @@ class Oracle:
         f64p = ctypes.POINTER(ctypes.c_double)
         i64p = ctypes.POINTER(ctypes.c_int64)
         I, L, D = ctypes.c_int, ctypes.c_int64, ctypes.c_double
-        lib.oracle_block_mask.argtypes = [I, I, I, i32p, I, I, I, I, I, i32p, i32p, i32p, i32p]
+        lib.oracle_block_mask.argtypes = [I, I, I, i32p, I, I, I, I, I, I, i32p, i32p, i32p, i32p]
         lib.oracle_block_mask.restype = I
         lib.oracle_attention.argtypes = [f32p, f32p, f32p, I, I, I, I, I, I, I, I, i32p,
                                          I, D, D, i64p, L, f64p, f64p]
@@ -63,7 +63,7 @@ class Oracle:
         lib.oracle_attention_opts.argtypes = [f32p, f32p, f32p, I, I, I, I, I, I, I, I, i32p,
                                               I, D, D, I, i64p, L, f64p, f64p, f64p]
         lib.oracle_attention_opts.restype = I
-        lib.oracle_block_mask_q.argtypes = [I, I, I, i32p, I, I, I, I, I, i32p, i32p, i32p, i32p]
+        lib.oracle_block_mask_q.argtypes = [I, I, I, i32p, I, I, I, I, I, I, i32p, i32p, i32p, i32p]
         lib.oracle_block_mask_q.restype = I
         lib.oracle_attention_bwd.argtypes = [f32p, f32p, f32p, f32p, I, I, I, I, I, I, I, I, i32p,
                                              I, D, D, f64p, f64p, f64p]
@@ -81,9 +81,13 @@ class Oracle:
         self.path = path
 
     def block_mask(self, kind: int, B: int, H: int, q_len: int, kv_len: int, block: int = 128,
-                   window: int = 0, prefix: int = 0, doc_ids=None) -> dict:
-        """kv_num_blocks, kv_indices, full_kv_num_blocks, full_kv_indices (int32)."""
-        nqb, nkvb = -(-q_len // block), -(-kv_len // block)  # ceil: tail tiles padded with false
+                   window: int = 0, prefix: int = 0, doc_ids=None, kv_block: int | None = None) -> dict:
+        """kv_num_blocks, kv_indices, full_kv_num_blocks, full_kv_indices (int32).
+
+        Tiles are block (Q_BLOCK) rows by kv_block (KV_BLOCK, default: block) columns.
+        """
+        kv_block = block if kv_block is None else kv_block
+        nqb, nkvb = -(-q_len // block), -(-kv_len // kv_block)  # ceil: tail tiles padded with false
         out = {
             "kv_num_blocks": np.zeros((B, H, nqb), np.int32),
             "kv_indices": np.zeros((B, H, nqb, nkvb), np.int32),
@@ -92,7 +96,7 @@ class Oracle:
         }
         doc = None if doc_ids is None else np.ascontiguousarray(doc_ids, dtype=np.int32)
         rc = self.lib.oracle_block_mask(kind, window, prefix, _ptr(doc, ctypes.c_int32), B, H,
-                                        q_len, kv_len, block,
+                                        q_len, kv_len, block, kv_block,
                                         _ptr(out["kv_num_blocks"], ctypes.c_int32),
                                         _ptr(out["kv_indices"], ctypes.c_int32),
                                         _ptr(out["full_kv_num_blocks"], ctypes.c_int32),
@@ -169,9 +173,10 @@ class Oracle:
         return out, lse, row_max
 
     def block_mask_q(self, kind: int, B: int, H: int, q_len: int, kv_len: int, block: int = 128,
-                     window: int = 0, prefix: int = 0, doc_ids=None) -> dict:
+                     window: int = 0, prefix: int = 0, doc_ids=None, kv_block: int | None = None) -> dict:
         """q_num_blocks, q_indices, full_q_num_blocks, full_q_indices (int32): the transposed lists."""
-        nqb, nkvb = -(-q_len // block), -(-kv_len // block)
+        kv_block = block if kv_block is None else kv_block
+        nqb, nkvb = -(-q_len // block), -(-kv_len // kv_block)
         out = {
             "q_num_blocks": np.zeros((B, H, nkvb), np.int32),
             "q_indices": np.zeros((B, H, nkvb, nqb), np.int32),
@@ -180,7 +185,7 @@ class Oracle:
         }
         doc = None if doc_ids is None else np.ascontiguousarray(doc_ids, dtype=np.int32)
         rc = self.lib.oracle_block_mask_q(kind, window, prefix, _ptr(doc, ctypes.c_int32), B, H, q_len, kv_len,
-                                          block, _ptr(out["q_num_blocks"], ctypes.c_int32),
+                                          block, kv_block, _ptr(out["q_num_blocks"], ctypes.c_int32),
                                           _ptr(out["q_indices"], ctypes.c_int32),
                                           _ptr(out["full_q_num_blocks"], ctypes.c_int32),
                                           _ptr(out["full_q_indices"], ctypes.c_int32))

@@ -367,8 +367,11 @@ def _bf_score(kind, param, t, h, H, i, j):
     return t
 
 
-def brute_force(q, k, v, mask, score, scale, window=0, prefix=0, doc=None, param=0.0, block=2):
-    """Plain Python loops: (out, lse, block status, row max) for tiny shapes."""
+def brute_force(q, k, v, mask, score, scale, window=0, prefix=0, doc=None, param=0.0, block=2, kv_block=None):
+    """Plain Python loops: (out, lse, block status, row max) for tiny shapes.
+
+    Tiles are block (Q_BLOCK) rows by kv_block (KV_BLOCK, default: block) columns."""
+    kv_block = block if kv_block is None else kv_block
     B, H, S, D = q.shape
     out = [[[[0.0] * D for _ in range(S)] for _ in range(H)] for _ in range(B)]
     lse = [[[0.0] * S for _ in range(H)] for _ in range(B)]
@@ -391,17 +394,60 @@ def brute_force(q, k, v, mask, score, scale, window=0, prefix=0, doc=None, param
                 lse[b][h][i] = L
                 for d in range(D):
                     out[b][h][i][d] = math.fsum(math.exp(s - L) * float(v[b, h, j, d]) for j, s in row)
-    nb = -(-S // block)  # tiles past S are padded with false
-    status = np.zeros((B, H, nb, nb), np.int64)
+    nqb, nkb = -(-S // block), -(-S // kv_block)  # tiles past S are padded with false
+    status = np.zeros((B, H, nqb, nkb), np.int64)
     for b in range(B):
         for h in range(H):
-            for qb in range(nb):
-                for kb in range(nb):
+            for qb in range(nqb):
+                for kb in range(nkb):
                     c = sum(_bf_mask(mask, b, h, i, j, window, prefix, doc)
                             for i in range(qb * block, min(S, qb * block + block))
-                            for j in range(kb * block, min(S, kb * block + block)))
-                    status[b, h, qb, kb] = 2 if c == block * block else (1 if c else 0)
+                            for j in range(kb * kv_block, min(S, kb * kv_block + kv_block)))
+                    status[b, h, qb, kb] = 2 if c == block * kv_block else (1 if c else 0)
     return np.asarray(out), np.asarray(lse), status, np.asarray(rmax)
+
+
+def pin_brute_force_block_shapes(orc):
+    # BlockMasks whose Q block and KV block differ (the tuple carries both
+    # sizes), against the brute-force tile classes of the same dense mask
+    B, H = 2, 1
+    for S, qbs, kbs in [(12, 2, 4), (12, 4, 2), (13, 4, 2), (10, 2, 4), (16, 8, 2), (9, 1, 4)]:
+        q = k = v = _rand((B, H, S, 2), S)
+        doc = np.zeros((B, S), np.int32)
+        doc[0, S // 3:] = 1
+        doc[1, S // 2:] = 1
+        for mask, kw in [(W.MASK_CAUSAL, {}), (W.MASK_SLIDING_WINDOW, {"window": 3}),
+                         (W.MASK_CAUSAL_PREFIX, {"prefix": 5}), (W.MASK_DOCUMENT, {"doc": doc}),
+                         (W.MASK_ALL, {})]:
+            _, _, bs, _ = brute_force(q, k, v, mask, W.SCORE_IDENTITY, 0.5, block=qbs, kv_block=kbs,
+                                      window=kw.get("window", 0), prefix=kw.get("prefix", 0), doc=kw.get("doc"))
+            okw = {"window": kw.get("window", 0), "prefix": kw.get("prefix", 0), "doc_ids": kw.get("doc")}
+            bm = orc.block_mask(mask, B, H, S, S, qbs, kv_block=kbs, **okw)
+            _check_lists(bm, bs, f"brute block mask S{S} {qbs}x{kbs} m{mask}")
+            bq = orc.block_mask_q(mask, B, H, S, S, qbs, kv_block=kbs, **okw)
+            for b in range(B):
+                for h in range(H):
+                    exp = _expected_lists(bs[b, h].T)
+                    for key, qkey in (("kv_num_blocks", "q_num_blocks"), ("kv_indices", "q_indices"),
+                                      ("full_kv_num_blocks", "full_q_num_blocks"),
+                                      ("full_kv_indices", "full_q_indices")):
+                        assert np.array_equal(bq[qkey][b, h], exp[key]), f"{qkey} S{S} {qbs}x{kbs} m{mask}"
+
+
+def pin_causal_block_shapes_closed_form(orc):
+    # causal, Q_BLOCK a and KV_BLOCK c: tile (i, j) holds rows a i .. a i + a - 1
+    # and columns c j .. c j + c - 1; it is full when its first row reaches
+    # its last column (a i >= c j + c - 1) and empty when its last row is
+    # before its first column (a i + a - 1 < c j)
+    for S, a, c in [(1024, 64, 128), (1024, 128, 64), (1024, 256, 128), (1000, 64, 256), (768, 256, 64)]:
+        bm = orc.block_mask(W.MASK_CAUSAL, 1, 1, S, S, a, kv_block=c)
+        nqb, nkb = -(-S // a), -(-S // c)
+        for i in range(nqb):
+            full = [j for j in range(nkb) if a * i >= c * j + c - 1 and c * j + c <= S and a * i + a <= S]
+            part = [j for j in range(nkb) if not (a * i + a - 1 < c * j) and j not in full]
+            assert list(bm["full_kv_indices"][0, 0, i, :len(full)]) == full, (S, a, c, i)
+            assert list(bm["kv_indices"][0, 0, i, :len(part)]) == part, (S, a, c, i)
+            assert bm["full_kv_num_blocks"][0, 0, i] == len(full) and bm["kv_num_blocks"][0, 0, i] == len(part)
 
 
 def pin_brute_force_tiny(orc):
@@ -693,6 +739,8 @@ ALL_PINS = [
     pin_document_blocks_from_intervals,
     pin_golden_causal_prefix_predicate,
     pin_brute_force_tiny,
+    pin_brute_force_block_shapes,
+    pin_causal_block_shapes_closed_form,
     pin_round_bf16_is_library_conversion,
     pin_round_bf16_nearest_on_exact_products,
     pin_prescale_power_of_two_scale_changes_nothing,

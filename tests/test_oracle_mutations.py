@@ -32,8 +32,14 @@ MUTATIONS = [
     ("scale dropped", "or_score_mod(score_kind, score_param, post * dot, h, H, i, j)",
      "or_score_mod(score_kind, score_param, dot, h, H, i, j)"),
     ("v row index", "const float *vj = v + j * D;", "const float *vj = v + i * D;"),
-    ("full tiles classed as partial", "const int64_t all = (int64_t)block * block;",
-     "const int64_t all = (int64_t)block * block + 1;"),
+    ("full tiles classed as partial", "const int64_t all = (int64_t)q_block * kv_block;",
+     "const int64_t all = (int64_t)q_block * kv_block + 1;"),
+    ("tile area from one block size", "const int64_t all = (int64_t)q_block * kv_block;",
+     "const int64_t all = (int64_t)q_block * q_block;"),
+    ("columns binned by the q block", "count[kv / kv_block] += band[r * kv_len + kv];",
+     "count[kv / q_block] += band[r * kv_len + kv];"),
+    ("kv block count from the q block", "const int64_t nkvb = ((int64_t)kv_len + kv_block - 1) / kv_block;\n    or_mask m",
+     "const int64_t nkvb = ((int64_t)kv_len + q_block - 1) / q_block;\n    or_mask m"),
     ("padding order", "if (!(count[j] > 0 && count[j] < all)) pi[tp++] = (int32_t)j;",
      "if (!(count[j] > 0 && count[j] < all)) pi[tp++] = (int32_t)(nkvb - 1 - j);"),
     ("empty row guard", "        *lse = -INFINITY;\n        if (row_max)", "        *lse = 0.0;\n        if (row_max)"),
@@ -48,7 +54,7 @@ MUTATIONS = [
     ("bf16 ties away from zero", "nearbyint(ldexp(x, -quantum))", "round(ldexp(x, -quantum))"),
     ("bf16 subnormal quantum", "if (quantum < -133) quantum = -133;", "if (quantum < -126) quantum = -126;"),
     ("bf16 overflow bound", "ldexp(255.0, 120)", "ldexp(255.0, 119)"),
-    ("padding rows counted", "band[r * kv_len + kv] = qb * block + r < q_len", "band[r * kv_len + kv] = 1"),
+    ("padding rows counted", "band[r * kv_len + kv] = qb * q_block + r < q_len", "band[r * kv_len + kv] = 1"),
     ("dS sign", "const double ds = pr[j] * (dp - Di);", "const double ds = pr[j] * (Di - dp);"),
     ("dS drops the row term", "const double ds = pr[j] * (dp - Di);", "const double ds = pr[j] * dp;"),
     ("softcap gradient dropped", "        return 1.0 - u * u;", "        return 1.0 + 0.0 * u;"),
@@ -61,8 +67,8 @@ MUTATIONS = [
     ("q-side partial and full swapped", "if (st[i * nkvb + j] == 1) pq[np++] = (int32_t)i;",
      "if (st[i * nkvb + j] == 2) pq[np++] = (int32_t)i;"),
     ("ragged tiles rounded down",
-     "const int64_t nkvb = ((int64_t)kv_len + block - 1) / block;\n    or_mask m",
-     "const int64_t nkvb = ((int64_t)kv_len) / block + (kv_len % block > block / 2);\n    or_mask m"),
+     "const int64_t nkvb = ((int64_t)kv_len + kv_block - 1) / kv_block;\n    or_mask m",
+     "const int64_t nkvb = ((int64_t)kv_len) / kv_block + (kv_len % kv_block > kv_block / 2);\n    or_mask m"),
 ]
 
 
