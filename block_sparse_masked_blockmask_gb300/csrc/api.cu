@@ -19,9 +19,9 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 bool valid_mask_kind(int k) { return k >= FLEX_MASK_CAUSAL && k <= FLEX_MASK_ALL; }
 
-int check_sizes(int32_t B, int32_t H, int32_t q_len, int32_t kv_len, int32_t block) {
-    if (B <= 0 || H <= 0 || q_len <= 0 || kv_len <= 0 || block <= 0) return FLEX_ERR_INVALID_ARG;
-    if (block != kBlock) return FLEX_ERR_UNSUPPORTED;
+int check_sizes(int32_t B, int32_t H, int32_t q_len, int32_t kv_len, int32_t q_block, int32_t kv_block) {
+    if (B <= 0 || H <= 0 || q_len <= 0 || kv_len <= 0 || q_block <= 0 || kv_block <= 0) return FLEX_ERR_INVALID_ARG;
+    if (!valid_block_size(q_block) || !valid_block_size(kv_block)) return FLEX_ERR_UNSUPPORTED;
     if (ceil_blocks(kv_len) > kMaxKvBlocks) return FLEX_ERR_UNSUPPORTED;
     if (B > 65535 || H > 65535) return FLEX_ERR_UNSUPPORTED;
     return FLEX_OK;
@@ -63,10 +63,11 @@ int prepare_attention(const flex_tensor *q, const flex_tensor *k, const flex_ten
     if (!aligned16(out) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return FLEX_ERR_ALIGNMENT;
     // BlockMask consistency
     if (!valid_mask_kind(bm->mask_kind)) return FLEX_ERR_INVALID_ARG;
-    rc = check_sizes(bm->B, bm->H, bm->q_len, bm->kv_len, bm->block);
+    rc = check_sizes(bm->B, bm->H, bm->q_len, bm->kv_len, bm->q_block, bm->kv_block);
     if (rc != FLEX_OK) return rc;
     if (bm->B != B || bm->H != H || bm->q_len != Sq || bm->kv_len != Skv) return FLEX_ERR_SHAPE;
-    if (bm->nqb != ceil_blocks(bm->q_len) || bm->nkvb != ceil_blocks(bm->kv_len)) return FLEX_ERR_SHAPE;
+    if (bm->nqb != ceil_div(bm->q_len, bm->q_block) || bm->nkvb != ceil_div(bm->kv_len, bm->kv_block))
+        return FLEX_ERR_SHAPE;
     if (!bm->kv_num_blocks || !bm->kv_indices || !bm->full_kv_num_blocks || !bm->full_kv_indices)
         return FLEX_ERR_INVALID_ARG;
     if (bm->mask_kind == FLEX_MASK_DOCUMENT && (!bm->params.doc_ids || !aligned16(bm->params.doc_ids)))
@@ -76,7 +77,7 @@ int prepare_attention(const flex_tensor *q, const flex_tensor *k, const flex_ten
     // each kv tile's document ids are bulk-copied as whole 16-byte words
     if (bm->mask_kind == FLEX_MASK_DOCUMENT && Sq % 4 != 0) return FLEX_ERR_UNSUPPORTED;
     if (bm->mask_kind == FLEX_MASK_SLIDING_WINDOW && bm->params.window < 0) return FLEX_ERR_INVALID_ARG;
-    if (B * H * ((bm->nqb + 1) / 2) > INT32_MAX) return FLEX_ERR_UNSUPPORTED;
+    if (B * H * ((ceil_blocks(Sq) + 1) / 2) > INT32_MAX) return FLEX_ERR_UNSUPPORTED;
 
     p.B = (int)B;
     p.H = (int)H;
@@ -85,8 +86,12 @@ int prepare_attention(const flex_tensor *q, const flex_tensor *k, const flex_ten
     p.q_len = (int)Sq;
     p.kv_len = (int)Skv;
     p.D = (int)D;
+    p.q_block = bm->q_block;
+    p.kv_block = bm->kv_block;
     p.nqb = bm->nqb;
     p.nkvb = bm->nkvb;
+    p.nqt = ceil_blocks(Sq);
+    p.nkvt = ceil_blocks(Skv);
     for (int i = 0; i < 4; ++i) {
         p.q_stride[i] = q->stride[i];
         p.k_stride[i] = k->stride[i];
@@ -227,21 +232,32 @@ using namespace flex;
 
 extern "C" {
 
-int flex_block_mask_sizes(int32_t B, int32_t H, int32_t q_len, int32_t kv_len, int32_t block, int64_t *num_elems,
-                          int64_t *idx_elems) {
+int flex_block_mask_sizes_qkv(int32_t B, int32_t H, int32_t q_len, int32_t kv_len, int32_t q_block,
+                              int32_t kv_block, int64_t *num_elems, int64_t *idx_elems) {
     if (!num_elems || !idx_elems) return FLEX_ERR_INVALID_ARG;
-    const int rc = check_sizes(B, H, q_len, kv_len, block);
+    const int rc = check_sizes(B, H, q_len, kv_len, q_block, kv_block);
     if (rc != FLEX_OK) return rc;
-    const int64_t nqb = ceil_blocks(q_len), nkvb = ceil_blocks(kv_len);
+    const int64_t nqb = ceil_div(q_len, q_block), nkvb = ceil_div(kv_len, kv_block);
     *num_elems = (int64_t)B * H * nqb;
     *idx_elems = (int64_t)B * H * nqb * nkvb;
     return FLEX_OK;
 }
 
+int flex_block_mask_sizes(int32_t B, int32_t H, int32_t q_len, int32_t kv_len, int32_t block, int64_t *num_elems,
+                          int64_t *idx_elems) {
+    return flex_block_mask_sizes_qkv(B, H, q_len, kv_len, block, block, num_elems, idx_elems);
+}
+
 int flex_block_mask_create(int32_t mask_kind, const flex_mask_params *params, int32_t B, int32_t H, int32_t q_len,
                            int32_t kv_len, int32_t block, flex_block_mask *bm, void *stream) {
+    return flex_block_mask_create_qkv(mask_kind, params, B, H, q_len, kv_len, block, block, bm, stream);
+}
+
+int flex_block_mask_create_qkv(int32_t mask_kind, const flex_mask_params *params, int32_t B, int32_t H,
+                               int32_t q_len, int32_t kv_len, int32_t q_block, int32_t kv_block, flex_block_mask *bm,
+                               void *stream) {
     if (!bm || !valid_mask_kind(mask_kind)) return FLEX_ERR_INVALID_ARG;
-    const int rc = check_sizes(B, H, q_len, kv_len, block);
+    const int rc = check_sizes(B, H, q_len, kv_len, q_block, kv_block);
     if (rc != FLEX_OK) return rc;
     if (!bm->kv_num_blocks || !bm->kv_indices || !bm->full_kv_num_blocks || !bm->full_kv_indices)
         return FLEX_ERR_INVALID_ARG;
@@ -258,14 +274,15 @@ int flex_block_mask_create(int32_t mask_kind, const flex_mask_params *params, in
     bm->H = H;
     bm->q_len = q_len;
     bm->kv_len = kv_len;
-    bm->block = block;
-    bm->nqb = ceil_blocks(q_len);
-    bm->nkvb = ceil_blocks(kv_len);
+    bm->q_block = q_block;
+    bm->kv_block = kv_block;
+    bm->nqb = ceil_div(q_len, q_block);
+    bm->nkvb = ceil_div(kv_len, kv_block);
     bm->mask_kind = mask_kind;
     bm->params = prm;
     MaskDesc md{mask_kind, prm.window, prm.prefix, q_len, prm.doc_ids, q_len, kv_len};
-    const cudaError_t e = launch_block_mask(md, B, H, q_len, kv_len, bm->kv_num_blocks, bm->kv_indices,
-                                            bm->full_kv_num_blocks, bm->full_kv_indices,
+    const cudaError_t e = launch_block_mask(md, B, H, q_len, kv_len, q_block, kv_block, bm->kv_num_blocks,
+                                            bm->kv_indices, bm->full_kv_num_blocks, bm->full_kv_indices,
                                             static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FLEX_OK : FLEX_ERR_CUDA;
 }
@@ -306,9 +323,10 @@ int flex_attention_fwd_opts(const flex_tensor *q, const flex_tensor *k, const fl
 
 int flex_block_mask_transpose(const flex_block_mask *bm, flex_block_mask_q *bq, void *stream) {
     if (!bm || !bq) return FLEX_ERR_INVALID_ARG;
-    int rc = check_sizes(bm->B, bm->H, bm->q_len, bm->kv_len, bm->block);
+    int rc = check_sizes(bm->B, bm->H, bm->q_len, bm->kv_len, bm->q_block, bm->kv_block);
     if (rc != FLEX_OK) return rc;
-    if (bm->nqb != ceil_blocks(bm->q_len) || bm->nkvb != ceil_blocks(bm->kv_len)) return FLEX_ERR_SHAPE;
+    if (bm->nqb != ceil_div(bm->q_len, bm->q_block) || bm->nkvb != ceil_div(bm->kv_len, bm->kv_block))
+        return FLEX_ERR_SHAPE;
     if (!bm->kv_num_blocks || !bm->kv_indices || !bm->full_kv_num_blocks || !bm->full_kv_indices)
         return FLEX_ERR_INVALID_ARG;
     if (!bq->q_num_blocks || !bq->q_indices || !bq->full_q_num_blocks || !bq->full_q_indices)
@@ -317,7 +335,8 @@ int flex_block_mask_transpose(const flex_block_mask *bm, flex_block_mask_q *bq, 
     bq->H = bm->H;
     bq->q_len = bm->q_len;
     bq->kv_len = bm->kv_len;
-    bq->block = bm->block;
+    bq->q_block = bm->q_block;
+    bq->kv_block = bm->kv_block;
     bq->nqb = bm->nqb;
     bq->nkvb = bm->nkvb;
     return launch_block_mask_transpose(bm->kv_num_blocks, bm->kv_indices, bm->full_kv_num_blocks,
@@ -341,12 +360,12 @@ int flex_attention_bwd(const flex_tensor *q, const flex_tensor *k, const flex_te
         (reinterpret_cast<uintptr_t>(delta) & 3u))
         return FLEX_ERR_ALIGNMENT;
     if (bq->B != bm->B || bq->H != bm->H || bq->q_len != bm->q_len || bq->kv_len != bm->kv_len ||
-        bq->block != bm->block || bq->nqb != bm->nqb || bq->nkvb != bm->nkvb)
+        bq->q_block != bm->q_block || bq->kv_block != bm->kv_block || bq->nqb != bm->nqb || bq->nkvb != bm->nkvb)
         return FLEX_ERR_SHAPE;
     if (!bq->q_num_blocks || !bq->q_indices || !bq->full_q_num_blocks || !bq->full_q_indices)
         return FLEX_ERR_INVALID_ARG;
-    // the tensor-core backward holds a kv block's list of q blocks on chip
-    if (q->dtype == FLEX_DTYPE_BF16 && bm->nqb > kBwdTcMaxQBlocks) return FLEX_ERR_UNSUPPORTED;
+    // the tensor-core backward holds a kv tile's list of q tiles on chip
+    if (q->dtype == FLEX_DTYPE_BF16 && p.nqt > kBwdTcMaxQBlocks) return FLEX_ERR_UNSUPPORTED;
     return launch_attn_bwd(p, q->dtype, dout, bq->q_num_blocks, bq->q_indices, bq->full_q_num_blocks,
                            bq->full_q_indices, dq, dk, dv, delta, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? FLEX_OK
@@ -438,7 +457,7 @@ int flex_attention_fwd_host(const flex_tensor *q, const flex_tensor *k, const fl
     if (B64 <= 0 || H64 <= 0 || Sq64 <= 0 || Skv64 <= 0) return FLEX_ERR_SHAPE;
     if (B64 > INT32_MAX || H64 > INT32_MAX || Sq64 > INT32_MAX || Skv64 > INT32_MAX) return FLEX_ERR_UNSUPPORTED;
     const int B = (int)B64, H = (int)H64, Sq = (int)Sq64, Skv = (int)Skv64;
-    int rc = check_sizes(B, H, Sq, Skv, kBlock);
+    int rc = check_sizes(B, H, Sq, Skv, kBlock, kBlock);
     if (rc != FLEX_OK) return rc;
     if (doc && Sq != Skv) return FLEX_ERR_SHAPE;
 
@@ -453,7 +472,8 @@ int flex_attention_fwd_host(const flex_tensor *q, const flex_tensor *k, const fl
     bm.H = H;
     bm.q_len = Sq;
     bm.kv_len = Skv;
-    bm.block = kBlock;
+    bm.q_block = kBlock;
+    bm.kv_block = kBlock;
     bm.nqb = ceil_blocks(Sq);
     bm.nkvb = ceil_blocks(Skv);
     bm.mask_kind = mask_kind;
@@ -488,8 +508,8 @@ int flex_attention_fwd_host(const flex_tensor *q, const flex_tensor *k, const fl
         good = ok(cudaMemcpyAsync(dev->doc_ids, params->doc_ids, (size_t)B64 * Sq64 * sizeof(int32_t),
                                   cudaMemcpyHostToDevice, s));
     if (good)
-        good = ok(launch_block_mask(p.mask, B, H, Sq, Skv, bm.kv_num_blocks, bm.kv_indices, bm.full_kv_num_blocks,
-                                    bm.full_kv_indices, s));
+        good = ok(launch_block_mask(p.mask, B, H, Sq, Skv, kBlock, kBlock, bm.kv_num_blocks, bm.kv_indices,
+                                    bm.full_kv_num_blocks, bm.full_kv_indices, s));
     // inputs of every chunk, back to back on the copy-in stream
     for (int c = 0; good && c < nch; ++c) {
         const int64_t b0 = (int64_t)c * per, n = std::min<int64_t>(per, nbh - b0);

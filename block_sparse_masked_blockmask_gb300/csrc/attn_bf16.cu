@@ -53,15 +53,12 @@ cudaError_t launch_attn_bf16(const AttnProblem &p, cudaStream_t stream) {
     kp.H = p.H;
     kp.q_len = p.q_len;
     kp.kv_len = p.kv_len;
-    kp.nqb = p.nqb;
-    kp.nkvb = p.nkvb;
-    kp.npairs = (p.nqb + 1) / 2;
+    kp.nqt = p.nqt;
+    kp.nkvt = p.nkvt;
+    kp.npairs = (p.nqt + 1) / 2;
     kp.bh_begin = p.bh_begin;
     kp.nbh = p.bh_count;
-    kp.kv_num = p.kv_num;
-    kp.kv_idx = p.kv_idx;
-    kp.full_num = p.full_num;
-    kp.full_idx = p.full_idx;
+    kp.lists = TileLists{p.kv_num, p.kv_idx, p.full_num, p.full_idx, p.nqb, p.nkvb, p.q_block, p.kv_block, p.nkvt};
     kp.mask = p.mask;
     // PRESCALE_QK moves the scale onto Q (in shared memory); the scores then take 1
     kp.scale = p.prescale ? 1.f : p.scale;

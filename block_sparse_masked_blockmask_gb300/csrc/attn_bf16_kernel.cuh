@@ -52,6 +52,7 @@
 
 #include "flex_internal.h"
 #include "ptx.cuh"
+#include "tilelist.cuh"
 
 namespace flex {
 
@@ -83,9 +84,9 @@ constexpr uint32_t kRegsControl = 72;
 static_assert(2 * kRegsSoftmax + kRegsControl == 3 * kRegsAtLaunch, "register split");
 
 struct Bf16Params {
-    int B, H, q_len, kv_len, nqb, nkvb, npairs;
+    int B, H, q_len, kv_len, nqt, nkvt, npairs;  // nqt, nkvt: 128-tiles along q and kv
     int bh_begin, nbh;  // the (b, h) pairs b * H + h in [bh_begin, bh_begin + nbh) are computed
-    const int32_t *kv_num, *kv_idx, *full_num, *full_idx;
+    TileLists lists;    // the BlockMask's kv side (any Q_BLOCK, KV_BLOCK), read as 128-tiles
     MaskDesc mask;
     float scale, score_param;
     float prescale;   // PRESCALE_QK: 0 = off, else Q is multiplied by it in shared memory (scale is then 1)
@@ -118,7 +119,7 @@ struct AttnMisc {
     int abort;
     alignas(16) uint32_t clc_resp[4];
     alignas(16) int32_t stage_doc[4][128];     // document ids of each stage's kv tile (bulk-copy target)
-    alignas(16) uint32_t flags[kMaxKvBlocks];  // bit0/bit1 present/full in tile 0, bit2/bit3 in tile 1
+    alignas(16) uint32_t flags[kMaxKvBlocks];  // per kv tile: listed / full-pair counts of Q tiles 0 and 1
     ItemSlot slot[2];
 };
 // bulk copies and the launch-control response need 16-byte aligned destinations
@@ -347,53 +348,81 @@ __device__ __forceinline__ void decode_item(const Bf16Params &p, int item, int &
     b = bh / p.H;
     h = bh % p.H;
     qb0 = 2 * pair;
-    has1 = qb0 + 1 < p.nqb ? 1 : 0;
+    has1 = qb0 + 1 < p.nqt ? 1 : 0;
 }
 
 // Build an item's union list into `sl` with the 32 lanes of one warp:
 // mark every kv tile of both q blocks (bounds-checked: a malformed BlockMask
 // cannot write outside the flag array), then compact the marked tiles in
-// descending kv order.  The index loads of a chunk are all issued before any
-// of them is used, so the build costs a couple of memory latencies rather than
-// one per 32 entries.
+// descending kv order with their present / full bits (1, 2 for tile 0; 4, 8
+// for tile 1).  The index loads of a chunk are all issued before any of them
+// is used, so the build costs a couple of memory latencies rather than one
+// per 32 entries.  BLOCKS128: the lists hold 128-tiles directly (the code the
+// MMA-issuing warpgroup's register budget was tuned with); otherwise they
+// are read as 128-tiles through the general mapping (tilelist.cuh).
+template <bool BLOCKS128>
 __device__ __forceinline__ void build_item(const Bf16Params &p, AttnMisc &ms, ItemSlot &sl, int item, int lane) {
     int b, h, qb0, has1;
     decode_item(p, item, b, h, qb0, has1);
-    const int nkvb = p.nkvb;
-    const int64_t row0 = ((int64_t)b * p.H + h) * p.nqb + qb0;
-    const int32_t *pidx = p.kv_idx + row0 * nkvb, *fidx = p.full_idx + row0 * nkvb;
-    const int np0 = min(max(__ldg(p.kv_num + row0), 0), nkvb), nf0 = min(max(__ldg(p.full_num + row0), 0), nkvb);
-    const int np1 = has1 ? min(max(__ldg(p.kv_num + row0 + 1), 0), nkvb) : 0;
-    const int nf1 = has1 ? min(max(__ldg(p.full_num + row0 + 1), 0), nkvb) : 0;
-    for (int j = lane; j < nkvb; j += 32) ms.flags[j] = 0u;
-    __syncwarp();
-    constexpr int kUnroll = 4;
-    for (int base = 0; base < nkvb; base += 32 * kUnroll) {
-        int jj[4][kUnroll];
-#pragma unroll
-        for (int r = 0; r < kUnroll; ++r) {
-            const int x = base + 32 * r + lane;
-            jj[0][r] = x < np0 ? __ldg(pidx + x) : -1;
-            jj[1][r] = x < nf0 ? __ldg(fidx + x) : -1;
-            jj[2][r] = x < np1 ? __ldg(pidx + nkvb + x) : -1;
-            jj[3][r] = x < nf1 ? __ldg(fidx + nkvb + x) : -1;
-        }
-        constexpr uint32_t kBits[4] = {1u, 3u, 4u, 12u};  // present / full, tile 0 then tile 1
-#pragma unroll
-        for (int l = 0; l < 4; ++l)
-#pragma unroll
-            for (int r = 0; r < kUnroll; ++r)
-                if ((unsigned)jj[l][r] < (unsigned)nkvb) atomicOr(&ms.flags[jj[l][r]], kBits[l]);
-    }
-    __syncwarp();
-    int count = 0;
+    const int nkvt = p.nkvt;
     const unsigned lt = (1u << lane) - 1u;
-    for (int base = 0; base < nkvb; base += 32) {
-        const int c = nkvb - 1 - (base + lane);
-        const uint32_t f = c >= 0 ? ms.flags[c] : 0u;
-        const unsigned bal = __ballot_sync(0xffffffffu, f != 0u);
-        if (f != 0u) sl.ulist[count + __popc(bal & lt)] = (uint32_t)c | (f << 16);
-        count += __popc(bal);
+    int count = 0;
+    if constexpr (BLOCKS128) {
+        const int nkvb = nkvt;
+        const int64_t row0 = ((int64_t)b * p.H + h) * p.nqt + qb0;
+        const int32_t *pidx = p.lists.idx + row0 * nkvb, *fidx = p.lists.fidx + row0 * nkvb;
+        const int np0 = min(max(__ldg(p.lists.num + row0), 0), nkvb);
+        const int nf0 = min(max(__ldg(p.lists.fnum + row0), 0), nkvb);
+        const int np1 = has1 ? min(max(__ldg(p.lists.num + row0 + 1), 0), nkvb) : 0;
+        const int nf1 = has1 ? min(max(__ldg(p.lists.fnum + row0 + 1), 0), nkvb) : 0;
+        for (int j = lane; j < nkvb; j += 32) ms.flags[j] = 0u;
+        __syncwarp();
+        constexpr int kUnroll = 4;
+        for (int base = 0; base < nkvb; base += 32 * kUnroll) {
+            int jj[4][kUnroll];
+#pragma unroll
+            for (int r = 0; r < kUnroll; ++r) {
+                const int x = base + 32 * r + lane;
+                jj[0][r] = x < np0 ? __ldg(pidx + x) : -1;
+                jj[1][r] = x < nf0 ? __ldg(fidx + x) : -1;
+                jj[2][r] = x < np1 ? __ldg(pidx + nkvb + x) : -1;
+                jj[3][r] = x < nf1 ? __ldg(fidx + nkvb + x) : -1;
+            }
+            constexpr uint32_t kBits[4] = {1u, 3u, 4u, 12u};  // present / full, tile 0 then tile 1
+#pragma unroll
+            for (int l = 0; l < 4; ++l)
+#pragma unroll
+                for (int r = 0; r < kUnroll; ++r)
+                    if ((unsigned)jj[l][r] < (unsigned)nkvb) atomicOr(&ms.flags[jj[l][r]], kBits[l]);
+        }
+        __syncwarp();
+        for (int base = 0; base < nkvb; base += 32) {
+            const int c = nkvb - 1 - (base + lane);
+            const uint32_t f = c >= 0 ? ms.flags[c] : 0u;
+            const unsigned bal = __ballot_sync(0xffffffffu, f != 0u);
+            if (f != 0u) sl.ulist[count + __popc(bal & lt)] = (uint32_t)c | (f << 16);
+            count += __popc(bal);
+        }
+    } else {
+        for (int j = lane; j < nkvt; j += 32) ms.flags[j] = 0u;
+        __syncwarp();
+        const int64_t bh = (int64_t)b * p.H + h;
+        tl_mark_warp(p.lists, bh, qb0, 0, ms.flags, 0, nkvt, lane);
+        if (has1) tl_mark_warp(p.lists, bh, qb0 + 1, 1, ms.flags, 0, nkvt, lane);
+        __syncwarp();
+        const uint32_t expect = tl_expect(p.lists);
+        for (int base = 0; base < nkvt; base += 32) {
+            const int c = nkvt - 1 - (base + lane);
+            uint32_t f = 0u;
+            if (c >= 0) {
+                const uint32_t w = ms.flags[c];
+                f = (tl_listed(w, 0) ? 1u : 0u) | (tl_full(expect, w, 0) ? 2u : 0u) | (tl_listed(w, 1) ? 4u : 0u) |
+                    (tl_full(expect, w, 1) ? 8u : 0u);
+            }
+            const unsigned bal = __ballot_sync(0xffffffffu, f != 0u);
+            if (f != 0u) sl.ulist[count + __popc(bal & lt)] = (uint32_t)c | (f << 16);
+            count += __popc(bal);
+        }
     }
     if (lane == 0) {
         sl.nu = count;
@@ -407,6 +436,8 @@ __device__ __forceinline__ void build_item(const Bf16Params &p, AttnMisc &ms, It
 
 // DOC: the BlockMask's mask_mod is the document mask (its partial tiles read
 // per-tile document ids staged next to V); other kinds are interval masks.
+// BLOCKS128: the BlockMask's blocks are 128 x 128 (else any Q_BLOCK, KV_BLOCK,
+// read as 128-tiles when the scheduler builds an item).
 //
 // Persistent over work items: each CTA starts with the item of its own index
 // and then takes items from CTAs of the grid that have not started yet
@@ -414,7 +445,7 @@ __device__ __forceinline__ void build_item(const Bf16Params &p, AttnMisc &ms, It
 // union list, Q tiles and first K/V tiles load while the current item
 // computes.  Every role walks the same sequence of published items; all
 // barrier phases (K/V ring, S/P hand-off, Q, O) continue across items.
-template <int D, int SCORE, bool DOC>
+template <int D, int SCORE, bool DOC, bool BLOCKS128>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const Bf16Params p) {
@@ -489,7 +520,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 break;
             }
             if (item >= 0) {
-                build_item(p, ms, sl, item, lane);
+                build_item<BLOCKS128>(p, ms, sl, item, lane);
             } else if (lane == 0) {
                 sl.nu = -1;
             }

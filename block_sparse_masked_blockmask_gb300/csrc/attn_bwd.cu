@@ -23,6 +23,7 @@
 #include "attn_bwd_tc.cuh"
 #include "bwd_internal.h"
 #include "ptx.cuh"
+#include "tilelist.cuh"
 
 namespace flex {
 namespace {
@@ -37,7 +38,9 @@ struct BwdCfg {
     static constexpr int kThreads = kBwdRows * kTpr;   // 128 or 256
     static constexpr int kStride = 4 * kTpr;           // distance between a thread's groups
     // two staged 128 x D fp32 tiles, then two 128-float row vectors
-    static constexpr size_t kSmem = 2ull * kBlock * D * sizeof(float) + 2ull * kBlock * sizeof(float);
+    // plus one flag word per walked tile of a chunk (the BlockMask read as 128-tiles)
+    static constexpr size_t kSmem =
+        2ull * kBlock * D * sizeof(float) + 2ull * kBlock * sizeof(float) + kMaxKvBlocks * sizeof(uint32_t);
 };
 
 __device__ __forceinline__ float4 load4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
@@ -110,6 +113,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_dkdv_kernel(A
     float *gs = qs + kBlock * D;
     float *ls = gs + kBlock * D;
     float *dl = ls + kBlock;
+    uint32_t *flags = reinterpret_cast<uint32_t *>(dl + kBlock);
 
     const int kvb = blockIdx.x / 2;
     const int bh = p.bh_begin + (int)blockIdx.y, h = bh % p.H, b = bh / p.H;
@@ -132,19 +136,26 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_dkdv_kernel(A
     for (int e = 0; e < kDimsPer; ++e) dk[e] = dv[e] = 0.f;
     const float slope = exp2f(-8.f * (float)(h + 1) / (float)p.H);
 
-    const int64_t col = (int64_t)bh * p.nkvb + kvb;
-    // counts clamped and out-of-range indices skipped (malformed lists stay in bounds)
-    const int nfull = min(max(a.fq_num[col], 0), p.nqb), npart = min(max(a.q_num[col], 0), p.nqb);
-    const int32_t *fidx = a.fq_idx + col * p.nqb, *pidx = a.q_idx + col * p.nqb;
+    // the q side of the BlockMask (any block sizes) read as 128-tiles, in
+    // chunks of kMaxKvBlocks q tiles; counts clamped and malformed entries
+    // dropped, so no load leaves the tensors
+    const TileLists lists{a.q_num, a.q_idx, a.fq_num, a.fq_idx, p.nkvb, p.nqb, p.kv_block, p.q_block, p.nqt};
     const T *qbase = static_cast<const T *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1];
     const T *gbase = static_cast<const T *>(a.dout) + (int64_t)bh * p.q_len * D;
     const float *lbase = p.lse + (int64_t)bh * p.q_len;
     const float *dbase = a.delta + (int64_t)bh * p.q_len;
 
-    for (int t = 0; t < nfull + npart; ++t) {
-        const bool full = t < nfull;
-        const int qb = full ? fidx[t] : pidx[t - nfull];
-        if ((unsigned)qb >= (unsigned)p.nqb) continue;  // uniform over the CTA
+    for (int tlo = 0; tlo < p.nqt; tlo += kMaxKvBlocks) {
+      const int thi = min(p.nqt, tlo + kMaxKvBlocks);
+      __syncthreads();  // the previous chunk's flags are consumed
+      for (int i = threadIdx.x; i < thi - tlo; i += C::kThreads) flags[i] = 0u;
+      __syncthreads();
+      if (threadIdx.x < 32) tl_mark_warp(lists, bh, kvb, 0, flags, tlo, thi, threadIdx.x);
+      __syncthreads();
+      for (int qb = tlo; qb < thi; ++qb) {
+        const uint32_t w = flags[qb - tlo];  // uniform over the CTA
+        if (!tl_listed(w, 0)) continue;
+        const bool full = tl_full(tl_expect(lists), w, 0);
         const int q0 = qb * kBlock;
         __syncthreads();  // the previous q block is consumed
         stage_tile<D, C::kThreads>(qs, qbase, p.q_stride[2], q0, p.q_len);
@@ -195,6 +206,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_dkdv_kernel(A
                 dk[e] = fmaf(dts, qv[e], dk[e]);
             }
         }
+      }
     }
     if (!kv_in) return;
     const int64_t orow = (int64_t)bh * p.kv_len + kv;
@@ -216,6 +228,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_dq_kernel(Att
     extern __shared__ float4 smem4[];
     float *ks = reinterpret_cast<float *>(smem4);
     float *vs = ks + kBlock * D;
+    uint32_t *flags = reinterpret_cast<uint32_t *>(vs + kBlock * D + 2 * kBlock);
 
     const int qb = blockIdx.x / 2;
     const int bh = p.bh_begin + (int)blockIdx.y, h = bh % p.H, b = bh / p.H;
@@ -242,16 +255,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_dq_kernel(Att
     const float dlt = q_in ? a.delta[orow] : 0.f;
     const float slope = exp2f(-8.f * (float)(h + 1) / (float)p.H);
 
-    const int64_t bhq = (int64_t)bh * p.nqb + qb;
-    const int nfull = min(max(p.full_num[bhq], 0), p.nkvb), npart = min(max(p.kv_num[bhq], 0), p.nkvb);
-    const int32_t *fidx = p.full_idx + bhq * p.nkvb, *pidx = p.kv_idx + bhq * p.nkvb;
+    // the kv side of the BlockMask (any block sizes) read as 128-tiles (at
+    // most kMaxKvBlocks kv tiles)
+    const TileLists lists{p.kv_num, p.kv_idx, p.full_num, p.full_idx, p.nqb, p.nkvb, p.q_block, p.kv_block, p.nkvt};
+    for (int i = threadIdx.x; i < p.nkvt; i += C::kThreads) flags[i] = 0u;
+    __syncthreads();
+    if (threadIdx.x < 32) tl_mark_warp(lists, bh, qb, 0, flags, 0, p.nkvt, threadIdx.x);
+    __syncthreads();
     const T *kbase = static_cast<const T *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
     const T *vbase = static_cast<const T *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1];
 
-    for (int t = 0; t < nfull + npart; ++t) {
-        const bool full = t < nfull;
-        const int kvb = full ? fidx[t] : pidx[t - nfull];
-        if ((unsigned)kvb >= (unsigned)p.nkvb) continue;  // uniform over the CTA
+    for (int kvb = 0; kvb < p.nkvt; ++kvb) {
+        const uint32_t w = flags[kvb];  // uniform over the CTA
+        if (!tl_listed(w, 0)) continue;
+        const bool full = tl_full(tl_expect(lists), w, 0);
         const int kv0 = kvb * kBlock;
         __syncthreads();
         stage_tile<D, C::kThreads>(ks, kbase, p.k_stride[2], kv0, p.kv_len);
@@ -368,9 +385,9 @@ cudaError_t launch_bwd_typed(const AttnProblem &p, const BwdArgs &a, cudaStream_
         AttnProblem part = p;
         part.bh_begin = begin;
         const int count = p.B * p.H - begin < 65535 ? p.B * p.H - begin : 65535;
-        attn_bwd_dkdv_kernel<D, T><<<dim3(2 * p.nkvb, count), C::kThreads, C::kSmem, stream>>>(part, a);
+        attn_bwd_dkdv_kernel<D, T><<<dim3(2 * p.nkvt, count), C::kThreads, C::kSmem, stream>>>(part, a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        attn_bwd_dq_kernel<D, T><<<dim3(2 * p.nqb, count), C::kThreads, C::kSmem, stream>>>(part, a);
+        attn_bwd_dq_kernel<D, T><<<dim3(2 * p.nqt, count), C::kThreads, C::kSmem, stream>>>(part, a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -420,25 +437,17 @@ cudaError_t launch_bwd_bf16_tc(const AttnProblem &p, const BwdArgs &a, cudaStrea
     kp.lse = p.lse;
     kp.delta = a.delta;
     kp.status = p.status;
-    // dK, dV: own the kv blocks, walk the q side of the BlockMask
-    kp.nblocks = p.nkvb;
-    kp.nlist = p.nqb;
-    kp.num = a.q_num;
-    kp.idx = a.q_idx;
-    kp.fnum = a.fq_num;
-    kp.fidx = a.fq_idx;
+    // dK, dV: own the kv tiles, walk the q side of the BlockMask
+    kp.nblocks = p.nkvt;
+    kp.lists = TileLists{a.q_num, a.q_idx, a.fq_num, a.fq_idx, p.nkvb, p.nqb, p.kv_block, p.q_block, p.nqt};
     kp.out0 = static_cast<uint16_t *>(a.dv);
     kp.out1 = static_cast<uint16_t *>(a.dk);
     const CUtensorMap kv_maps[4] = {mk, mv, mq, mdo};
     e = launch_bwd_tc_dkdv(kv_maps, kp, p.D, p.score_kind, stream);
     if (e != cudaSuccess) return e;
-    // dQ: own the q blocks, walk the kv side
-    kp.nblocks = p.nqb;
-    kp.nlist = p.nkvb;
-    kp.num = p.kv_num;
-    kp.idx = p.kv_idx;
-    kp.fnum = p.full_num;
-    kp.fidx = p.full_idx;
+    // dQ: own the q tiles, walk the kv side
+    kp.nblocks = p.nqt;
+    kp.lists = TileLists{p.kv_num, p.kv_idx, p.full_num, p.full_idx, p.nqb, p.nkvb, p.q_block, p.kv_block, p.nkvt};
     kp.out0 = static_cast<uint16_t *>(a.dq);
     kp.out1 = nullptr;
     const CUtensorMap q_maps[4] = {mq, mdo, mk, mv};

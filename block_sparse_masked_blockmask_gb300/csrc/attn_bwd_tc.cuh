@@ -43,6 +43,7 @@
 
 #include "flex_internal.h"
 #include "ptx.cuh"
+#include "tilelist.cuh"
 
 namespace flex {
 
@@ -55,10 +56,9 @@ constexpr float kBwdLog2e = 1.4426950408889634f;
 
 struct BwdTcParams {
     int B, H, q_len, kv_len;
-    int nblocks;                  // blocks of the owned dimension (NKVB when KV_MAJOR, else NQB)
-    int nlist;                    // blocks of the walked dimension (the list rows' length)
+    int nblocks;                  // 128-tiles of the owned dimension (kv when KV_MAJOR, else q)
     int bh_begin, nbh;
-    const int32_t *num, *idx, *fnum, *fidx;  // the walked side of the BlockMask
+    TileLists lists;              // the BlockMask side that lists the walked dimension, read as 128-tiles
     MaskDesc mask;
     float scale, score_param;
     const float *lse, *delta;     // [B, H, q_len]
@@ -78,7 +78,8 @@ struct BwdMisc {
     alignas(16) float colv[2][128];         // per column of a step (see the elementwise code)
     alignas(16) float dltv[2][128];         // KV_MAJOR: -delta of each q column
     alignas(16) int32_t docv[2][128];       // document ids of the walked block's rows
-    alignas(16) uint32_t list[kBwdMaxList]; // walked block | full << 16
+    alignas(16) uint32_t list[kBwdMaxList]; // walked tile | full << 16
+    alignas(16) uint32_t words[kBwdMaxList];// per walked tile: listed bit and full-pair count (tilelist.cuh)
 };
 
 template <int D>
@@ -242,34 +243,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         fence_barrier_init();
     }
     if (warp == 0) {
-        // the walked blocks: full ones, then partial ones; counts clamped and
-        // indices outside the list dropped, so a malformed BlockMask stays
-        // in bounds
-        const int64_t row = (int64_t)bh * p.nblocks + own;
-        const int nf = min(max(__ldg(p.fnum + row), 0), p.nlist);
-        const int np = min(max(__ldg(p.num + row), 0), p.nlist);
-        const int32_t *fi = p.fidx + row * p.nlist, *pi = p.idx + row * p.nlist;
+        // the walked tiles of this block: the BlockMask's lists (any block
+        // sizes) read as 128-tiles, in ascending order; counts are clamped
+        // and malformed entries dropped, so nothing is written or loaded out
+        // of bounds
+        const int nt = min(p.lists.walk_nt, kBwdMaxList);
+        for (int i = lane; i < nt; i += 32) ms.words[i] = 0u;
+        __syncwarp();
+        tl_mark_warp(p.lists, bh, own, 0, ms.words, 0, nt, lane);
+        __syncwarp();
         const unsigned lt = (1u << lane) - 1u;
+        const uint32_t expect = tl_expect(p.lists);
         int cnt = 0;
-        for (int base = 0; base < nf + np; base += 32) {
+        for (int base = 0; base < nt; base += 32) {
             const int i = base + lane;
-            uint32_t e = 0u;
-            bool ok = false;
-            if (i < nf) {
-                const int v = __ldg(fi + i);
-                ok = (unsigned)v < (unsigned)p.nlist;
-                e = (uint32_t)v | (1u << 16);
-            } else if (i < nf + np) {
-                const int v = __ldg(pi + i - nf);
-                ok = (unsigned)v < (unsigned)p.nlist;
-                e = (uint32_t)v;
-            }
+            const uint32_t w = i < nt ? ms.words[i] : 0u;
+            const bool ok = tl_listed(w, 0);
             const unsigned bal = __ballot_sync(0xffffffffu, ok);
-            const int at = cnt + __popc(bal & lt);
-            if (ok && at < kBwdMaxList) ms.list[at] = e;
+            if (ok) ms.list[cnt + __popc(bal & lt)] = (uint32_t)i | (tl_full(expect, w, 0) ? (1u << 16) : 0u);
             cnt += __popc(bal);
         }
-        if (lane == 0) ms.n = min(cnt, kBwdMaxList);
+        if (lane == 0) ms.n = cnt;
     }
     if (warp == kBwdMmaWarp) {
         tmem_alloc(&ms.tmem_base, C::kTmemCols);

@@ -14,6 +14,7 @@
 // memory and read as broadcasts.  Rows of a tail tile past the lengths are
 // staged as zeros and masked (kv) or left unwritten (q).
 #include "flex_internal.h"
+#include "tilelist.cuh"
 
 namespace flex {
 namespace {
@@ -25,7 +26,8 @@ template <int D>
 struct Fp32Cfg {
     static constexpr int kTpr = D / kDimsPerThread;      // threads per row
     static constexpr int kThreads = kBlock * kTpr;
-    static constexpr size_t kSmem = 2ull * kBlock * D * sizeof(float);
+    // K and V tiles, then one flag word per kv tile (the BlockMask read as 128-tiles)
+    static constexpr size_t kSmem = 2ull * kBlock * D * sizeof(float) + kMaxKvBlocks * sizeof(uint32_t);
 };
 
 __device__ __forceinline__ float score_mod_f32(int kind, float param, float s, float slope, int q, int kv) {
@@ -40,11 +42,11 @@ __global__ void __launch_bounds__(Fp32Cfg<D>::kThreads) attn_fp32_kernel(AttnPro
     extern __shared__ float4 smem4[];
     float *ks = reinterpret_cast<float *>(smem4);
     float *vs = ks + kBlock * D;
+    uint32_t *flags = reinterpret_cast<uint32_t *>(vs + kBlock * D);
 
     const int qb = blockIdx.x, bh = p.bh_begin + (int)blockIdx.y, h = bh % p.H, b = bh / p.H;
     const int row = threadIdx.x / C::kTpr, part = threadIdx.x % C::kTpr;
     const int q = qb * kBlock + row;
-    const int64_t bhq = ((int64_t)b * p.H + h) * p.nqb + qb;
 
     const bool row_in = q < p.q_len;  // a tail tile's rows past Q_LEN are padding
     const float *qp = static_cast<const float *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1] +
@@ -61,18 +63,21 @@ __global__ void __launch_bounds__(Fp32Cfg<D>::kThreads) attn_fp32_kernel(AttnPro
     const float slope = exp2f(-8.f * (float)(h + 1) / (float)p.H);
     float m = -INFINITY, l = 0.f;
 
-    // counts clamped to [0, NKVB] and indices outside [0, NKVB) skipped, so a
-    // malformed BlockMask cannot send a load out of bounds
-    const int nfull = min(max(p.full_num[bhq], 0), p.nkvb), npart = min(max(p.kv_num[bhq], 0), p.nkvb);
-    const int32_t *fidx = p.full_idx + bhq * p.nkvb;
-    const int32_t *pidx = p.kv_idx + bhq * p.nkvb;
+    // the kv tiles of this q tile: the BlockMask's lists (any block sizes)
+    // read as 128-tiles by the first warp; counts are clamped and malformed
+    // entries dropped, so no load leaves the tensors
+    const TileLists lists{p.kv_num, p.kv_idx, p.full_num, p.full_idx, p.nqb, p.nkvb, p.q_block, p.kv_block, p.nkvt};
+    for (int i = threadIdx.x; i < p.nkvt; i += C::kThreads) flags[i] = 0u;
+    __syncthreads();
+    if (threadIdx.x < 32) tl_mark_warp(lists, bh, qb, 0, flags, 0, p.nkvt, threadIdx.x);
+    __syncthreads();
     const float *kbase = static_cast<const float *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
     const float *vbase = static_cast<const float *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1];
 
-    for (int t = 0; t < nfull + npart; ++t) {
-        const bool full = t < nfull;
-        const int kvb = full ? fidx[t] : pidx[t - nfull];
-        if ((unsigned)kvb >= (unsigned)p.nkvb) continue;  // the same for every thread of the CTA
+    for (int kvb = 0; kvb < p.nkvt; ++kvb) {
+        const uint32_t w = flags[kvb];  // the same for every thread of the CTA
+        if (!tl_listed(w, 0)) continue;
+        const bool full = tl_full(tl_expect(lists), w, 0);
         const int kv0 = kvb * kBlock;
         __syncthreads();  // previous tile fully consumed
         for (int i = threadIdx.x; i < kBlock * D / 4; i += C::kThreads) {
@@ -146,7 +151,7 @@ cudaError_t launch_d(const AttnProblem &p, cudaStream_t stream) {
         AttnProblem part = p;
         part.bh_begin = p.bh_begin + begin;
         part.bh_count = p.bh_count - begin < 65535 ? p.bh_count - begin : 65535;
-        attn_fp32_kernel<D><<<dim3(p.nqb, part.bh_count), C::kThreads, C::kSmem, stream>>>(part);
+        attn_fp32_kernel<D><<<dim3(p.nqt, part.bh_count), C::kThreads, C::kSmem, stream>>>(part);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -1,24 +1,26 @@
-// BlockMask build: classify every 128 x 128 tile of mask_mod as full, partial
-// or empty and write the kv-side BlockMask tensors of the flex_attention op
-// ("[Inductor][Flex Attention] Add Subtiling Option for Alpha Scaling",
-// PyTorch PR #167356, the BlockMask tuple: kv_num_blocks, kv_indices,
-// full_kv_num_blocks, full_kv_indices at Q_BLOCK = KV_BLOCK = 128).
+// BlockMask build: classify every Q_BLOCK x KV_BLOCK tile of mask_mod as
+// full, partial or empty and write the kv-side BlockMask tensors of the
+// flex_attention op ("[Inductor][Flex Attention] Add Subtiling Option for
+// Alpha Scaling", PyTorch PR #167356, the BlockMask tuple: kv_num_blocks,
+// kv_indices, full_kv_num_blocks, full_kv_indices and its Q_BLOCK and
+// KV_BLOCK sizes).
 //
 // One CTA per (batch b, q block qb); each warp classifies whole tiles.
 //  * causal, sliding window, causal + prefix, all: for a fixed row q the kept
 //    kv form exactly the interval [lo(q), hi(q)] (mask_row_interval), so a
-//    tile is full when every row's interval covers the tile's 128 columns and
-//    empty when no row's interval meets them: 128 row tests instead of 16384
-//    predicate evaluations.
+//    tile is full when every row's interval covers the tile's columns and
+//    empty when no row's interval meets them: Q_BLOCK row tests instead of
+//    Q_BLOCK x KV_BLOCK predicate evaluations.
 //  * document: exact quick decisions first (a tile above the diagonal is
-//    empty; a tile below it whose 256 row and column ids are one id is full;
-//    disjoint id ranges are empty), otherwise mask_mod is evaluated on all
-//    16384 pairs, so arbitrary ids stay exact.
-// Lengths need not be multiples of 128: positions past Q_LEN or KV_LEN are
-// padding and count as masked, so a tile reaching past either is never full.
-// None of the enumerated mask_mods depends on the head, so a row is
-// classified once and written for every head.  Index rows hold the selected kv
-// blocks in ascending order followed by the remaining kv blocks ascending.
+//    empty; a tile on or below it whose row and column ids are one id is
+//    full; disjoint id ranges are empty), otherwise mask_mod is evaluated on
+//    every pair of the tile, so arbitrary ids stay exact.
+// Lengths need not be multiples of the block sizes: positions past Q_LEN or
+// KV_LEN are padding and count as masked, so a tile reaching past either is
+// never full.  None of the enumerated mask_mods depends on the head, so a
+// row is classified once and written for every head.  Index rows hold the
+// selected kv blocks in ascending order followed by the remaining kv blocks
+// ascending.
 #include <climits>
 
 #include "flex_internal.h"
@@ -31,20 +33,21 @@ constexpr int kBmWarps = kBmThreads / 32;
 
 enum : uint8_t { kEmpty = 0, kPartial = 1, kFull = 2 };
 
-// Interval kinds: lane `lane` tests rows lane + 32 j of the tile; a row's
-// interval ends at KV_LEN - 1, and rows past Q_LEN keep nothing.
-__device__ __forceinline__ uint8_t classify_interval_tile(const MaskDesc &m, int q0, int kv0, int lane) {
+// Interval kinds: lane `lane` tests rows lane + 32 j of the qbs x kvbs tile
+// at (q0, kv0); a row's interval ends at KV_LEN - 1, and rows past Q_LEN
+// keep nothing.
+__device__ __forceinline__ uint8_t classify_interval_tile(const MaskDesc &m, int q0, int kv0, int qbs, int kvbs,
+                                                          int lane) {
     bool any = false, all = true;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int q = q0 + lane + 32 * j;
+    for (int r = lane; r < qbs; r += 32) {
+        const int q = q0 + r;
         int lo, hi;
         mask_row_interval(m, q, lo, hi);
         hi = min(hi, m.kv_len - 1);
         const bool row = q < m.q_len;
-        const int a = max(lo, kv0), e = min(hi, kv0 + kBlock - 1);
+        const int a = max(lo, kv0), e = min(hi, kv0 + kvbs - 1);
         any |= row && a <= e;
-        all &= row && lo <= kv0 && hi >= kv0 + kBlock - 1;
+        all &= row && lo <= kv0 && hi >= kv0 + kvbs - 1;
     }
     any = __any_sync(0xffffffffu, any);
     all = __all_sync(0xffffffffu, all);
@@ -53,20 +56,18 @@ __device__ __forceinline__ uint8_t classify_interval_tile(const MaskDesc &m, int
 
 // Document kind: quick exact decisions, else every (q, kv) pair of the tile.
 // Ids are read only inside the lengths; padding rows and columns keep nothing.
-__device__ __forceinline__ uint8_t classify_document_tile(const MaskDesc &m, int b, int qb, int kvb, int lane,
-                                                          const int32_t *row_doc, int row_min, int row_max) {
-    if (kvb > qb) return kEmpty;  // every kv of the tile is above every q: kv > q
-    const int kv0 = kvb * kBlock;
-    const int q0 = qb * kBlock;
-    int col_doc[4];
+__device__ __forceinline__ uint8_t classify_document_tile(const MaskDesc &m, int b, int q0, int kv0, int qbs,
+                                                          int kvbs, int lane, const int32_t *row_doc, int row_min,
+                                                          int row_max) {
+    if (kv0 > q0 + qbs - 1) return kEmpty;  // every kv of the tile is above every q: kv > q
+    const int32_t *ids = m.doc_ids + (int64_t)b * m.doc_len;
     int cmin = INT_MAX, cmax = INT_MIN;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int kv = kv0 + lane + 32 * j;
-        col_doc[j] = kv < m.kv_len ? m.doc_ids[(int64_t)b * m.doc_len + kv] : 0;
+    for (int c = lane; c < kvbs; c += 32) {
+        const int kv = kv0 + c;
         if (kv < m.kv_len) {
-            cmin = min(cmin, col_doc[j]);
-            cmax = max(cmax, col_doc[j]);
+            const int d = ids[kv];
+            cmin = min(cmin, d);
+            cmax = max(cmax, d);
         }
     }
 #pragma unroll
@@ -75,17 +76,21 @@ __device__ __forceinline__ uint8_t classify_document_tile(const MaskDesc &m, int
         cmax = max(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
     }
     if (cmax < row_min || cmin > row_max) return kEmpty;  // no id in common
-    const bool whole = q0 + kBlock <= m.q_len && kv0 + kBlock <= m.kv_len;
-    if (whole && kvb < qb && cmin == cmax && row_min == row_max && cmin == row_min) return kFull;
+    const bool whole = q0 + qbs <= m.q_len && kv0 + kvbs <= m.kv_len;
+    if (whole && kv0 + kvbs - 1 <= q0 && cmin == cmax && row_min == row_max && cmin == row_min) return kFull;
     bool any = false, all = true;
-    for (int r = 0; r < kBlock; ++r) {
-        const int q = q0 + r;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int kv = kv0 + lane + 32 * j;
-            const bool keep = q < m.q_len && kv < m.kv_len && q >= kv && row_doc[r] == col_doc[j];
-            any |= keep;
-            all &= keep;
+    for (int c0 = 0; c0 < kvbs; c0 += 32) {  // every lane runs every group: the votes below need all 32
+        const int c = c0 + lane;
+        const int kv = kv0 + c;
+        const bool col = c < kvbs;
+        const int cd = col && kv < m.kv_len ? ids[kv] : 0;
+        for (int r = 0; r < qbs; ++r) {
+            const int q = q0 + r;
+            const bool keep = q < m.q_len && kv < m.kv_len && q >= kv && row_doc[r] == cd;
+            if (col) {
+                any |= keep;
+                all &= keep;
+            }
         }
     }
     any = __any_sync(0xffffffffu, any);
@@ -116,20 +121,27 @@ __device__ __forceinline__ int compact_row(const uint8_t *status, int nkvb, uint
     return nsel;
 }
 
+// Dynamic shared memory of one CTA: the row's tile classes, its two compacted
+// lists, and the document ids of its rows.
+__host__ __device__ constexpr size_t block_mask_smem(int nkvb, int qbs) {
+    return (size_t)nkvb * 2 * sizeof(int32_t) + (size_t)qbs * sizeof(int32_t) + (size_t)nkvb;
+}
+
 template <int KIND>
-__global__ void __launch_bounds__(kBmThreads) block_mask_kernel(MaskDesc m, int H, int nqb, int nkvb,
-                                                                int32_t *kv_num, int32_t *kv_idx,
+__global__ void __launch_bounds__(kBmThreads) block_mask_kernel(MaskDesc m, int H, int nqb, int nkvb, int qbs,
+                                                                int kvbs, int32_t *kv_num, int32_t *kv_idx,
                                                                 int32_t *full_num, int32_t *full_idx) {
-    __shared__ uint8_t status[kMaxKvBlocks];
-    __shared__ int32_t part_list[kMaxKvBlocks];
-    __shared__ int32_t full_list[kMaxKvBlocks];
-    __shared__ int32_t row_doc[kBlock];
+    extern __shared__ int32_t bm_smem[];
+    int32_t *part_list = bm_smem;
+    int32_t *full_list = part_list + nkvb;
+    int32_t *row_doc = full_list + nkvb;
+    uint8_t *status = reinterpret_cast<uint8_t *>(row_doc + qbs);
     __shared__ int32_t row_range[2];
     __shared__ int32_t counts[2];
 
     const int qb = blockIdx.x, b = blockIdx.y;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int q0 = qb * kBlock;
+    const int q0 = qb * qbs;
 
     if constexpr (KIND == FLEX_MASK_DOCUMENT) {
         if (threadIdx.x == 0) {
@@ -137,7 +149,7 @@ __global__ void __launch_bounds__(kBmThreads) block_mask_kernel(MaskDesc m, int 
             row_range[1] = INT_MIN;
         }
         __syncthreads();
-        for (int r = threadIdx.x; r < kBlock; r += kBmThreads) {
+        for (int r = threadIdx.x; r < qbs; r += kBmThreads) {
             if (q0 + r >= m.q_len) {  // padding row
                 row_doc[r] = 0;
                 continue;
@@ -152,9 +164,9 @@ __global__ void __launch_bounds__(kBmThreads) block_mask_kernel(MaskDesc m, int 
     for (int kvb = warp; kvb < nkvb; kvb += kBmWarps) {
         uint8_t st;
         if constexpr (KIND == FLEX_MASK_DOCUMENT)
-            st = classify_document_tile(m, b, qb, kvb, lane, row_doc, row_range[0], row_range[1]);
+            st = classify_document_tile(m, b, q0, kvb * kvbs, qbs, kvbs, lane, row_doc, row_range[0], row_range[1]);
         else
-            st = classify_interval_tile(m, q0, kvb * kBlock, lane);
+            st = classify_interval_tile(m, q0, kvb * kvbs, qbs, kvbs, lane);
         if (lane == 0) status[kvb] = st;
     }
     __syncthreads();
@@ -181,35 +193,41 @@ __global__ void __launch_bounds__(kBmThreads) block_mask_kernel(MaskDesc m, int 
     }
 }
 
+template <int KIND>
+cudaError_t launch_kind(const MaskDesc &mask, int B, int H, int nqb, int nkvb, int qbs, int kvbs, int32_t *kv_num,
+                        int32_t *kv_idx, int32_t *full_num, int32_t *full_idx, cudaStream_t stream) {
+    const size_t smem = block_mask_smem(nkvb, qbs);
+    cudaError_t e = cudaFuncSetAttribute(block_mask_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    block_mask_kernel<KIND><<<dim3(nqb, B), kBmThreads, smem, stream>>>(mask, H, nqb, nkvb, qbs, kvbs, kv_num,
+                                                                      kv_idx, full_num, full_idx);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
-cudaError_t launch_block_mask(const MaskDesc &mask, int B, int H, int q_len, int kv_len, int32_t *kv_num,
-                              int32_t *kv_idx, int32_t *full_num, int32_t *full_idx, cudaStream_t stream) {
-    const int nqb = ceil_blocks(q_len), nkvb = ceil_blocks(kv_len);
-    const dim3 grid(nqb, B), block(kBmThreads);
+cudaError_t launch_block_mask(const MaskDesc &mask, int B, int H, int q_len, int kv_len, int q_block, int kv_block,
+                              int32_t *kv_num, int32_t *kv_idx, int32_t *full_num, int32_t *full_idx,
+                              cudaStream_t stream) {
+    const int nqb = ceil_div(q_len, q_block), nkvb = ceil_div(kv_len, kv_block);
     switch (mask.kind) {
         case FLEX_MASK_CAUSAL:
-            block_mask_kernel<FLEX_MASK_CAUSAL><<<grid, block, 0, stream>>>(mask, H, nqb, nkvb, kv_num, kv_idx,
-                                                                            full_num, full_idx);
-            break;
+            return launch_kind<FLEX_MASK_CAUSAL>(mask, B, H, nqb, nkvb, q_block, kv_block, kv_num, kv_idx,
+                                                 full_num, full_idx, stream);
         case FLEX_MASK_SLIDING_WINDOW:
-            block_mask_kernel<FLEX_MASK_SLIDING_WINDOW><<<grid, block, 0, stream>>>(mask, H, nqb, nkvb, kv_num,
-                                                                                    kv_idx, full_num, full_idx);
-            break;
+            return launch_kind<FLEX_MASK_SLIDING_WINDOW>(mask, B, H, nqb, nkvb, q_block, kv_block, kv_num, kv_idx,
+                                                         full_num, full_idx, stream);
         case FLEX_MASK_CAUSAL_PREFIX:
-            block_mask_kernel<FLEX_MASK_CAUSAL_PREFIX><<<grid, block, 0, stream>>>(mask, H, nqb, nkvb, kv_num,
-                                                                                   kv_idx, full_num, full_idx);
-            break;
+            return launch_kind<FLEX_MASK_CAUSAL_PREFIX>(mask, B, H, nqb, nkvb, q_block, kv_block, kv_num, kv_idx,
+                                                        full_num, full_idx, stream);
         case FLEX_MASK_DOCUMENT:
-            block_mask_kernel<FLEX_MASK_DOCUMENT><<<grid, block, 0, stream>>>(mask, H, nqb, nkvb, kv_num,
-                                                                              kv_idx, full_num, full_idx);
-            break;
+            return launch_kind<FLEX_MASK_DOCUMENT>(mask, B, H, nqb, nkvb, q_block, kv_block, kv_num, kv_idx,
+                                                   full_num, full_idx, stream);
         default:
-            block_mask_kernel<FLEX_MASK_ALL><<<grid, block, 0, stream>>>(mask, H, nqb, nkvb, kv_num, kv_idx,
-                                                                         full_num, full_idx);
-            break;
+            return launch_kind<FLEX_MASK_ALL>(mask, B, H, nqb, nkvb, q_block, kv_block, kv_num, kv_idx, full_num,
+                                              full_idx, stream);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace flex

@@ -11,8 +11,15 @@
 
 namespace flex {
 
-constexpr int kBlock = 128;       // BlockMask granularity (Q_BLOCK = KV_BLOCK = 128)
-constexpr int kMaxKvBlocks = 1024;  // kv blocks per BlockMask row the kernels stage on chip
+constexpr int kBlock = 128;         // compute tile (128 x 128); BlockMask blocks of other sizes map onto it
+constexpr int kMaxKvBlocks = 1024;  // kv tiles (of 128) per row the kernels stage on chip
+constexpr int kMinListBlock = 16, kMaxListBlock = 1024;  // BlockMask block sizes: powers of two in this range
+
+__host__ __device__ constexpr bool valid_block_size(int b) {
+    return b >= kMinListBlock && b <= kMaxListBlock && (b & (b - 1)) == 0;
+}
+// Blocks of size bs along a length (the last one may reach past it).
+__host__ __device__ constexpr int ceil_div(int64_t len, int bs) { return (int)((len + bs - 1) / bs); }
 
 // mask_mod as the kernels see it.
 struct MaskDesc {
@@ -70,7 +77,9 @@ __host__ __device__ __forceinline__ bool mask_row_interval(const MaskDesc &m, in
 
 // Problem description handed from the C-ABI layer to the attention launchers.
 struct AttnProblem {
-    int B, H, q_len, kv_len, D, nqb, nkvb;
+    int B, H, q_len, kv_len, D;
+    int q_block, kv_block, nqb, nkvb;                // BlockMask granularity: block sizes, blocks per row/column
+    int nqt, nkvt;                                   // 128-tiles along q and kv
     int bh_begin, bh_count;                          // the (b, h) pairs b * H + h in [bh_begin, +bh_count) are computed
     int64_t q_stride[4], k_stride[4], v_stride[4];  // elements
     const void *q, *k, *v;
@@ -87,8 +96,9 @@ struct AttnProblem {
 };
 
 // Launchers (return a cudaError_t from the launch).
-cudaError_t launch_block_mask(const MaskDesc &mask, int B, int H, int q_len, int kv_len, int32_t *kv_num,
-                              int32_t *kv_idx, int32_t *full_num, int32_t *full_idx, cudaStream_t stream);
+cudaError_t launch_block_mask(const MaskDesc &mask, int B, int H, int q_len, int kv_len, int q_block, int kv_block,
+                              int32_t *kv_num, int32_t *kv_idx, int32_t *full_num, int32_t *full_idx,
+                              cudaStream_t stream);
 cudaError_t launch_attn_fp32(const AttnProblem &p, cudaStream_t stream);
 cudaError_t launch_attn_bf16(const AttnProblem &p, cudaStream_t stream);
 

@@ -37,7 +37,8 @@ FLEX_SCORE_ALIBI = 2
 FLEX_DTYPE_BF16 = 0
 FLEX_DTYPE_FP32 = 1
 
-EXPORTED = ("flex_block_mask_sizes", "flex_block_mask_create", "flex_block_mask_transpose", "flex_attention_fwd",
+EXPORTED = ("flex_block_mask_sizes", "flex_block_mask_sizes_qkv", "flex_block_mask_create", "flex_block_mask_create_qkv",
+            "flex_block_mask_transpose", "flex_attention_fwd",
             "flex_attention_fwd_opts", "flex_attention_bwd", "flex_attention_fwd_noalloc", "flex_attention_fwd_host", "flex_device_status",
             "flex_selftest_wait_timeout", "flex_status_string")
 
@@ -54,8 +55,9 @@ class flex_mask_params(ctypes.Structure):
 
 class flex_block_mask(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("q_len", ctypes.c_int32),
-                ("kv_len", ctypes.c_int32), ("block", ctypes.c_int32), ("nqb", ctypes.c_int32),
-                ("nkvb", ctypes.c_int32), ("mask_kind", ctypes.c_int32), ("params", flex_mask_params),
+                ("kv_len", ctypes.c_int32), ("q_block", ctypes.c_int32), ("kv_block", ctypes.c_int32),
+                ("nqb", ctypes.c_int32), ("nkvb", ctypes.c_int32), ("mask_kind", ctypes.c_int32),
+                ("params", flex_mask_params),
                 ("kv_num_blocks", ctypes.c_void_p), ("kv_indices", ctypes.c_void_p),
                 ("full_kv_num_blocks", ctypes.c_void_p), ("full_kv_indices", ctypes.c_void_p)]
 
@@ -67,8 +69,9 @@ class flex_tensor(ctypes.Structure):
 
 class flex_block_mask_q(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("H", ctypes.c_int32), ("q_len", ctypes.c_int32),
-                ("kv_len", ctypes.c_int32), ("block", ctypes.c_int32), ("nqb", ctypes.c_int32),
-                ("nkvb", ctypes.c_int32), ("q_num_blocks", ctypes.c_void_p), ("q_indices", ctypes.c_void_p),
+                ("kv_len", ctypes.c_int32), ("q_block", ctypes.c_int32), ("kv_block", ctypes.c_int32),
+                ("nqb", ctypes.c_int32), ("nkvb", ctypes.c_int32),
+                ("q_num_blocks", ctypes.c_void_p), ("q_indices", ctypes.c_void_p),
                 ("full_q_num_blocks", ctypes.c_void_p), ("full_q_indices", ctypes.c_void_p)]
 
 
@@ -105,9 +108,14 @@ def load_library():
             i32, i64p, vp = ctypes.c_int32, ctypes.POINTER(ctypes.c_int64), ctypes.c_void_p
             lib.flex_block_mask_sizes.argtypes = [i32, i32, i32, i32, i32, i64p, i64p]
             lib.flex_block_mask_sizes.restype = ctypes.c_int
+            lib.flex_block_mask_sizes_qkv.argtypes = [i32, i32, i32, i32, i32, i32, i64p, i64p]
+            lib.flex_block_mask_sizes_qkv.restype = ctypes.c_int
             lib.flex_block_mask_create.argtypes = [i32, ctypes.POINTER(flex_mask_params), i32, i32, i32, i32, i32,
                                                    ctypes.POINTER(flex_block_mask), vp]
             lib.flex_block_mask_create.restype = ctypes.c_int
+            lib.flex_block_mask_create_qkv.argtypes = [i32, ctypes.POINTER(flex_mask_params), i32, i32, i32, i32,
+                                                       i32, i32, ctypes.POINTER(flex_block_mask), vp]
+            lib.flex_block_mask_create_qkv.restype = ctypes.c_int
             tp = ctypes.POINTER(flex_tensor)
             lib.flex_attention_fwd.argtypes = [tp, tp, tp, ctypes.POINTER(flex_block_mask), i32, ctypes.c_float,
                                                ctypes.c_float, vp, vp, vp]
@@ -151,9 +159,16 @@ def flex_status_string(code: int) -> str:
     return load_library().flex_status_string(int(code)).decode()
 
 
-def flex_block_mask_sizes(B: int, H: int, q_len: int, kv_len: int, block: int = 128) -> tuple[int, int]:
+def flex_block_mask_sizes(B: int, H: int, q_len: int, kv_len: int, block: int = 128,
+                          kv_block: int | None = None) -> tuple[int, int]:
+    """Element counts of the count and index tensors (Q_BLOCK = block, KV_BLOCK = kv_block or block)."""
     n_num, n_idx = ctypes.c_int64(), ctypes.c_int64()
-    rc = load_library().flex_block_mask_sizes(B, H, q_len, kv_len, block, ctypes.byref(n_num), ctypes.byref(n_idx))
+    if kv_block is None:
+        rc = load_library().flex_block_mask_sizes(B, H, q_len, kv_len, block, ctypes.byref(n_num),
+                                                  ctypes.byref(n_idx))
+    else:
+        rc = load_library().flex_block_mask_sizes_qkv(B, H, q_len, kv_len, block, kv_block, ctypes.byref(n_num),
+                                                      ctypes.byref(n_idx))
     if rc != FLEX_OK:
         raise FlexError(rc, "flex_block_mask_sizes")
     return n_num.value, n_idx.value
@@ -212,12 +227,17 @@ def flex_block_mask_transpose(block_mask: BlockMask, stream=None) -> BlockMaskQ:
 
 def flex_block_mask_create(mask_kind: int, B: int, H: int, q_len: int, kv_len: int, block: int = 128,
                            window: int = 0, prefix: int = 0, doc_ids: torch.Tensor | None = None,
-                           device=None, stream=None) -> BlockMask:
-    """Build a BlockMask on the device (asynchronous on `stream`)."""
+                           device=None, stream=None, kv_block: int | None = None) -> BlockMask:
+    """Build a BlockMask on the device (asynchronous on `stream`).
+
+    Tiles are block (Q_BLOCK) rows by kv_block (KV_BLOCK; default: block)
+    columns; flex_block_mask_create_qkv is called when kv_block is given.
+    """
     device = torch.device(device) if device is not None else (
         doc_ids.device if doc_ids is not None else torch.device("cuda", torch.cuda.current_device()))
-    n_num, n_idx = flex_block_mask_sizes(B, H, q_len, kv_len, block)
-    nqb, nkvb = -(-q_len // block), -(-kv_len // block)  # a tail tile may reach past a length
+    n_num, n_idx = flex_block_mask_sizes(B, H, q_len, kv_len, block, kv_block)
+    kvb = block if kv_block is None else kv_block
+    nqb, nkvb = -(-q_len // block), -(-kv_len // kvb)  # a tail tile may reach past a length
     t = {
         "kv_num_blocks": torch.empty((B, H, nqb), dtype=torch.int32, device=device),
         "kv_indices": torch.empty((B, H, nqb, nkvb), dtype=torch.int32, device=device),
@@ -234,8 +254,13 @@ def flex_block_mask_create(mask_kind: int, B: int, H: int, q_len: int, kv_len: i
     bm.full_kv_num_blocks = t["full_kv_num_blocks"].data_ptr()
     bm.full_kv_indices = t["full_kv_indices"].data_ptr()
     with torch.cuda.device(device):
-        rc = load_library().flex_block_mask_create(mask_kind, ctypes.byref(params), B, H, q_len, kv_len, block,
-                                                   ctypes.byref(bm), _stream_handle(stream, device))
+        if kv_block is None:
+            rc = load_library().flex_block_mask_create(mask_kind, ctypes.byref(params), B, H, q_len, kv_len, block,
+                                                       ctypes.byref(bm), _stream_handle(stream, device))
+        else:
+            rc = load_library().flex_block_mask_create_qkv(mask_kind, ctypes.byref(params), B, H, q_len, kv_len,
+                                                           block, kv_block, ctypes.byref(bm),
+                                                           _stream_handle(stream, device))
     if rc != FLEX_OK:
         raise FlexError(rc, "flex_block_mask_create")
     return BlockMask(bm, t, doc_ids)

@@ -42,8 +42,13 @@
  *    with cudaMalloc the first time a device is used; call any entry point
  *    once before capturing a stream into a CUDA graph.
  *  - Indices and counts are int32.  Lengths are any positive int32 (KV_LEN
- *    up to 1024 * BLOCK): the last tile along a length may reach past it,
- *    and the positions past a length count as masked.
+ *    up to 131072): the last tile along a length may reach past it, and the
+ *    positions past a length count as masked.
+ *  - Block sizes (Q_BLOCK, KV_BLOCK) are powers of two from 16 to 1024 and
+ *    may differ.  The kernels compute on 128 x 128 tiles and read a
+ *    BlockMask of any of these sizes as such tiles: a 128-tile is computed
+ *    when some block overlapping it is listed, and skips mask_mod when every
+ *    block overlapping it is full.
  */
 #ifndef FLEXATTN_H
 #define FLEXATTN_H
@@ -99,13 +104,13 @@ typedef struct {
 } flex_mask_params;
 
 /*
- * A BlockMask at BLOCK x BLOCK granularity (the BlockMask tuple of the
+ * A BlockMask at Q_BLOCK x KV_BLOCK granularity (the BlockMask tuple of the
  * flex_attention op, kv side).  For every (b, h, q-block qb) and kv block:
  *   full     the mask_mod is true on the whole tile  -> listed in full_kv_*
  *   partial  true on some of the tile                -> listed in kv_*
  *   empty    true nowhere                            -> listed in neither
- * NQB = ceil(Q_LEN / BLOCK), NKVB = ceil(KV_LEN / BLOCK).  Positions past
- * Q_LEN or KV_LEN count as masked (the mask padded with false to whole
+ * NQB = ceil(Q_LEN / Q_BLOCK), NKVB = ceil(KV_LEN / KV_BLOCK).  Positions
+ * past Q_LEN or KV_LEN count as masked (the mask padded with false to whole
  * tiles), so a tile reaching past either length is never full; the
  * attention kernels rely on that to bound the tail tiles.
  * kv_num_blocks[b,h,qb] counts the partial tiles; kv_indices[b,h,qb,:] holds
@@ -116,7 +121,9 @@ typedef struct {
  * evaluates the mask_mod on partial tiles only.
  */
 typedef struct {
-    int32_t B, H, q_len, kv_len, block, nqb, nkvb;
+    int32_t B, H, q_len, kv_len;
+    int32_t q_block, kv_block;     /* tile rows and columns (Q_BLOCK, KV_BLOCK)   */
+    int32_t nqb, nkvb;             /* ceil(q_len / q_block), ceil(kv_len / kv_block) */
     int32_t mask_kind;             /* flex_mask_kind the mask was built from      */
     flex_mask_params params;       /* its parameters (doc_ids stays caller-owned) */
     int32_t *kv_num_blocks;        /* device, [B, H, NQB]        int32            */
@@ -135,14 +142,20 @@ typedef struct {
 } flex_tensor;
 
 /*
- * Element counts of the BlockMask buffers for the given sizes:
+ * Element counts of the BlockMask buffers for the given sizes, with
+ * Q_BLOCK = KV_BLOCK = block:
  * *num_elems = B*H*NQB (each of kv_num_blocks, full_kv_num_blocks),
  * *idx_elems = B*H*NQB*NKVB (each of kv_indices, full_kv_indices).
  * Errors: FLEX_ERR_INVALID_ARG (null outputs, non-positive sizes),
- * FLEX_ERR_UNSUPPORTED (block != 128, or KV_LEN > 1024 * 128).
+ * FLEX_ERR_UNSUPPORTED (block not a power of two in 16..1024, KV_LEN >
+ * 131072, B or H > 65535).
  */
 FLEX_API int flex_block_mask_sizes(int32_t B, int32_t H, int32_t q_len, int32_t kv_len, int32_t block,
                           int64_t *num_elems, int64_t *idx_elems);
+
+/* flex_block_mask_sizes with separate Q_BLOCK and KV_BLOCK (same errors). */
+FLEX_API int flex_block_mask_sizes_qkv(int32_t B, int32_t H, int32_t q_len, int32_t kv_len, int32_t q_block,
+                                       int32_t kv_block, int64_t *num_elems, int64_t *idx_elems);
 
 /*
  * Build the BlockMask of an enumerated mask_mod on the device (the block
@@ -154,13 +167,23 @@ FLEX_API int flex_block_mask_sizes(int32_t B, int32_t H, int32_t q_len, int32_t 
  *   out: every other field of *bm is filled (sizes, mask kind, parameters), and
  *        the four buffers are written by a kernel enqueued on `stream`.
  * params may be NULL for kinds without parameters.  doc_ids must stay valid
- * while the BlockMask is used by flex_attention_fwd.
- * Errors: FLEX_ERR_INVALID_ARG, FLEX_ERR_SHAPE, FLEX_ERR_UNSUPPORTED
- * (block != 128, or NKVB > 1024), FLEX_ERR_CUDA.
+ * while the BlockMask is used by flex_attention_fwd.  Tiles are block x block
+ * (Q_BLOCK = KV_BLOCK = block).
+ * Errors: FLEX_ERR_INVALID_ARG, FLEX_ERR_SHAPE, FLEX_ERR_UNSUPPORTED (as
+ * flex_block_mask_sizes), FLEX_ERR_CUDA.
  */
 FLEX_API int flex_block_mask_create(int32_t mask_kind, const flex_mask_params *params, int32_t B, int32_t H,
                            int32_t q_len, int32_t kv_len, int32_t block, flex_block_mask *bm,
                            void *stream);
+
+/*
+ * flex_block_mask_create with tiles of q_block rows by kv_block columns (the
+ * BlockMask tuple's Q_BLOCK and KV_BLOCK fields); buffers sized by
+ * flex_block_mask_sizes_qkv.  Same arguments otherwise, same errors.
+ */
+FLEX_API int flex_block_mask_create_qkv(int32_t mask_kind, const flex_mask_params *params, int32_t B, int32_t H,
+                                        int32_t q_len, int32_t kv_len, int32_t q_block, int32_t kv_block,
+                                        flex_block_mask *bm, void *stream);
 
 /*
  * Block-sparse attention forward (the flex_attention op of PyTorch PR
@@ -320,7 +343,7 @@ FLEX_API int flex_attention_fwd_opts(const flex_tensor *q, const flex_tensor *k,
  * ascending, so each row is a permutation of 0..NQB-1.
  */
 typedef struct {
-    int32_t B, H, q_len, kv_len, block, nqb, nkvb;
+    int32_t B, H, q_len, kv_len, q_block, kv_block, nqb, nkvb;
     int32_t *q_num_blocks;         /* device, [B, H, NKVB]       int32 */
     int32_t *q_indices;            /* device, [B, H, NKVB, NQB]  int32 */
     int32_t *full_q_num_blocks;    /* device, [B, H, NKVB]       int32 */
@@ -357,9 +380,10 @@ FLEX_API int flex_block_mask_transpose(const flex_block_mask *bm, flex_block_mas
  * Rows whose lse is -inf (no unmasked score) contribute nothing.  bf16
  * inputs run on the tensor cores (S, dP and the gradient products as tcgen05
  * MMAs with fp32 accumulation; P and dS rounded to bf16 as MMA operands) and
- * need NQB <= 2048; fp32 inputs run in fp32 on the CUDA cores.  Errors: those
- * of flex_attention_fwd, FLEX_ERR_SHAPE when bq does not match bm, and
- * FLEX_ERR_UNSUPPORTED for bf16 with NQB > 2048.  Asynchronous on `stream`.
+ * need Q_LEN <= 262144 (2048 tiles of 128 rows); fp32 inputs run in fp32 on
+ * the CUDA cores.  Errors: those of flex_attention_fwd, FLEX_ERR_SHAPE when
+ * bq does not match bm, and FLEX_ERR_UNSUPPORTED for bf16 with Q_LEN >
+ * 262144.  Asynchronous on `stream`.
  */
 FLEX_API int flex_attention_bwd(const flex_tensor *q, const flex_tensor *k, const flex_tensor *v, const void *out,
                                 const float *lse, const void *dout, const flex_block_mask *bm,

@@ -41,6 +41,16 @@ def test_status_strings(lib):
     assert fa.flex_status_string(12345) == "unknown status"
 
 
+def test_block_mask_sizes_other_blocks(lib):
+    # Q_BLOCK and KV_BLOCK: powers of two from 16 to 1024, possibly different
+    assert fa.flex_block_mask_sizes(2, 3, 1024, 1024, 64) == (2 * 3 * 16, 2 * 3 * 16 * 16)
+    assert fa.flex_block_mask_sizes(1, 1, 1000, 300, 256, kv_block=64) == (4, 4 * 5)
+    assert fa.flex_block_mask_sizes(1, 1, 100, 100, 16, kv_block=1024) == (7, 7)
+    with pytest.raises(fa.FlexError) as e:
+        fa.flex_block_mask_sizes(1, 1, 128, 128, 128, kv_block=100)
+    assert e.value.code == fa.FLEX_ERR_UNSUPPORTED
+
+
 def test_block_mask_sizes(lib):
     assert fa.flex_block_mask_sizes(2, 32, 16384, 16384) == (2 * 32 * 128, 2 * 32 * 128 * 128)
     assert fa.flex_block_mask_sizes(1, 1, 128, 384) == (1, 3)
@@ -50,7 +60,9 @@ def test_block_mask_sizes(lib):
     assert fa.flex_block_mask_sizes(1, 1, 1, 128 * 1024) == (1, 1024)
     for args, code in [((0, 1, 128, 128), fa.FLEX_ERR_INVALID_ARG),
                        ((1, 1, 0, 128), fa.FLEX_ERR_INVALID_ARG),
-                       ((1, 1, 128, 128, 64), fa.FLEX_ERR_UNSUPPORTED),
+                       ((1, 1, 128, 128, 96), fa.FLEX_ERR_UNSUPPORTED),  # not a power of two
+                       ((1, 1, 128, 128, 8), fa.FLEX_ERR_UNSUPPORTED),
+                       ((1, 1, 128, 128, 2048), fa.FLEX_ERR_UNSUPPORTED),
                        ((1, 1, 128, 128 * 1024 + 1), fa.FLEX_ERR_UNSUPPORTED),
                        ((1, 1, 128, 128 * 1025), fa.FLEX_ERR_UNSUPPORTED)]:
         with pytest.raises(fa.FlexError) as e:
@@ -70,7 +82,8 @@ def test_block_mask_create_rejects_bad_arguments(lib):
     assert _call_create(lib, 7, None) == fa.FLEX_ERR_INVALID_ARG
     assert _call_create(lib, fa.FLEX_MASK_CAUSAL, None, buffers=False) == fa.FLEX_ERR_INVALID_ARG
     assert _call_create(lib, fa.FLEX_MASK_CAUSAL, None, q=-200) == fa.FLEX_ERR_INVALID_ARG
-    assert _call_create(lib, fa.FLEX_MASK_CAUSAL, None, block=64) == fa.FLEX_ERR_UNSUPPORTED
+    assert _call_create(lib, fa.FLEX_MASK_CAUSAL, None, block=96) == fa.FLEX_ERR_UNSUPPORTED
+    assert _call_create(lib, fa.FLEX_MASK_CAUSAL, None, block=2048) == fa.FLEX_ERR_UNSUPPORTED
     assert _call_create(lib, fa.FLEX_MASK_SLIDING_WINDOW, None) == fa.FLEX_ERR_INVALID_ARG
     assert _call_create(lib, fa.FLEX_MASK_SLIDING_WINDOW, fa.flex_mask_params(-1, 0, None)) == \
         fa.FLEX_ERR_INVALID_ARG
@@ -94,7 +107,7 @@ def _tensor(dtype, shape, stride=None, data=0x10000):
 
 def _mask_struct(B=1, H=2, q=256, kv=256, kind=fa.FLEX_MASK_CAUSAL):
     bm = fa.flex_block_mask()
-    bm.B, bm.H, bm.q_len, bm.kv_len, bm.block = B, H, q, kv, 128
+    bm.B, bm.H, bm.q_len, bm.kv_len, bm.q_block, bm.kv_block = B, H, q, kv, 128, 128
     bm.nqb, bm.nkvb, bm.mask_kind = -(-q // 128), -(-kv // 128), kind
     bm.kv_num_blocks = bm.kv_indices = bm.full_kv_num_blocks = bm.full_kv_indices = 0x1000
     return bm
@@ -226,7 +239,7 @@ def test_backward_entry_points_reject_bad_arguments(lib):
     bf = fa.FLEX_DTYPE_BF16
     bm = _mask_struct()
     bq = fa.flex_block_mask_q()
-    bq.B, bq.H, bq.q_len, bq.kv_len, bq.block, bq.nqb, bq.nkvb = 1, 2, 256, 256, 128, 2, 2
+    bq.B, bq.H, bq.q_len, bq.kv_len, bq.q_block, bq.kv_block, bq.nqb, bq.nkvb = 1, 2, 256, 256, 128, 128, 2, 2
     bq.q_num_blocks = bq.q_indices = bq.full_q_num_blocks = bq.full_q_indices = 0x2000
     assert lib.flex_block_mask_transpose(None, ctypes.byref(bq), None) == fa.FLEX_ERR_INVALID_ARG
     empty = fa.flex_block_mask_q()
