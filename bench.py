@@ -36,7 +36,7 @@ FALLBACK_HBM_GBS = 6800.0
 SPEC_BF16_TFLOPS = 2250.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_bf16_traffic.txt")
 KERNEL_SOURCES = ["attn_bf16_kernel.cuh", "attn_bf16_launch.cuh", "attn_bf16.cu", "attn_bf16_d64.cu",
-                  "attn_bf16_d128.cu", "ptx.cuh", "flex_internal.h"]
+                  "attn_bf16_d128.cu", "ptx.cuh", "flex_internal.h", "tilelist.cuh"]
 
 
 def workload_by_name(name: str) -> W.Workload:
