@@ -82,9 +82,8 @@ def test_attention(dtype, qbs, kbs, mask, mkw, score, param):
     out, lse = fa.flex_attention_fwd(dq, dk, dv, bm, score, param, scale)
     assert fa.flex_device_status() == fa.FLEX_OK
     ref_out, ref_lse = oracle.attention(q, k, v, mask, score, scale, doc_ids=docs, score_param=param, **mkw)
-    ref_abs, _ = oracle.attention(q, k, np.abs(v), mask, score, scale, doc_ids=docs, score_param=param, **mkw)
     compare(out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ref_out, ref_lse,
-            dtype, f"{dtype} {qbs}x{kbs} m{mask} s{score}", ref_abs=ref_abs)
+            dtype, f"{dtype} {qbs}x{kbs} m{mask} s{score}")
 
 
 def test_attention_matches_block_128():

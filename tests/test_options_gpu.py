@@ -80,9 +80,8 @@ def test_output_max(dtype, D, mask, mkw, score, param):
     out, lse, mx = _run(q, k, v, mask, score, scale, dtype, doc_ids=docs, score_param=param, **mkw)
     ref_out, ref_lse, ref_mx = oracle.attention_opts(q, k, v, mask, score, scale, doc_ids=docs,
                                                      score_param=param, **mkw)
-    ref_abs, _ = oracle.attention(q, k, np.abs(v), mask, score, scale, doc_ids=docs, score_param=param, **mkw)
     what = f"{dtype} D{D} m{mask} s{score}"
-    compare(out, lse, ref_out, ref_lse, dtype, what, ref_abs=ref_abs)
+    compare(out, lse, ref_out, ref_lse, dtype, what)
     _compare_max(mx, ref_mx, dtype, what)
     assert np.all(mx <= lse + TOL[dtype][1])
 

@@ -84,9 +84,8 @@ def test_attention_ragged(dtype, D, mask, mkw, score, param, S):
     scale = 1.0 / np.sqrt(D)
     out, lse, mx = _run(q, k, v, mask, score, scale, dtype, doc_ids=docs, score_param=param, **mkw)
     ro, rl, rx = oracle.attention_opts(q, k, v, mask, score, scale, doc_ids=docs, score_param=param, **mkw)
-    ra, _ = oracle.attention(q, k, np.abs(v), mask, score, scale, doc_ids=docs, score_param=param, **mkw)
     what = f"{dtype} D{D} m{mask} s{score} S{S}"
-    compare(out, lse, ro, rl, dtype, what, ref_abs=ra)
+    compare(out, lse, ro, rl, dtype, what)
     fin = np.isfinite(rx)
     assert np.array_equal(np.isfinite(mx), fin), what
     assert np.max(np.abs(mx[fin] - rx[fin])) <= TOL[dtype][1], what
