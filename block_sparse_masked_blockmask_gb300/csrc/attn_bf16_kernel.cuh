@@ -22,18 +22,23 @@
 //   * warps 8 / 10 (TMA): load the K tiles / the V tiles of each union step
 //                         into a ring of shared-memory stages (128-byte
 //                         swizzle, the layout tcgen05 descriptors read) that
-//                         runs on across items.
+//                         runs on across items.  At D = 64 warp 8 loads both.
 //   * warp 9  (MMA)     : one thread issues tcgen05.mma: S_i = Q_i K^T into
 //                         tensor memory (TMEM) and O_i += P_i V with P_i read
 //                         from TMEM; order per step PV0, S0(next), PV1,
 //                         S1(next), so each softmax group has two MMAs of
 //                         slack while the tensor core works for the other.
+//                         P_i overwrites the first 64 columns of S_i.
+//     D = 64 (TMEM has room for P apart from S): warps 9 and 10 each issue
+//                         one Q tile's MMAs, S two steps ahead of PV (the
+//                         next S only waits for the softmax to have read the
+//                         S it replaces), so the softmax never waits for an
+//                         S MMA and neither tile waits behind the other's.
 //   * warps 0-3 / 4-7   : softmax of Q tile 0 / 1, one thread per row (TMEM
 //                         lane = row).  Score_mod on every listed tile,
 //                         mask_mod only on partial tiles (the row's kept
 //                         interval or document id is hoisted out of the
-//                         column loop).  P goes back to TMEM over the S
-//                         columns as bf16.
+//                         column loop).  P goes back to TMEM as bf16.
 //   * O rescale: the running max is only raised when a tile's max exceeds it
 //     by more than 2^8, so exp2(s - m) <= 256 stays exact in fp32/bf16 and
 //     the O rescale (a TMEM read-modify-write by the softmax warp, between
@@ -112,7 +117,8 @@ struct AttnMisc {
     uint64_t near_end;                         // the K producer has issued an item's last K tile
     uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];
     uint64_t s_full[2], p_full[2];             // p_full[i]: all of P_i is in TMEM
-    uint64_t o_full, drain;
+    uint64_t s_free[2], pv_done[2];            // D = 64: S_i read by the softmax / PV_i complete
+    uint64_t o_full, drain[2];
     uint64_t item_ready[2], item_free[2];      // per item slot
     uint64_t clc_bar;                          // cluster-launch-control response landed
     uint32_t tmem_base;
@@ -127,7 +133,8 @@ static_assert(offsetof(AttnMisc, clc_resp) % 16 == 0, "clc_resp alignment");
 static_assert(offsetof(AttnMisc, stage_doc) % 16 == 0, "stage_doc alignment");
 static_assert(sizeof(AttnMisc::stage_doc[0]) % 16 == 0, "stage_doc row size");
 static_assert(offsetof(AttnMisc, slot) % 16 == 0 && sizeof(ItemSlot) % 16 == 0, "item slot alignment");
-// arrivals that free an item slot: both TMA producers, the MMA thread, 8 softmax warps
+// arrivals that free an item slot: 8 softmax warps and three control warps
+// (K and V producers and the MMA thread; at D = 64 one producer, two MMA threads)
 constexpr uint32_t kItemConsumers = 11;
 
 template <int D>
@@ -142,9 +149,19 @@ struct Bf16Cfg {
     static constexpr uint32_t kStageBytes = 2 * kTileBytes;  // K then V
     static constexpr uint32_t kMiscOff = kKvOff + kStages * kStageBytes;
     static constexpr uint32_t kSmemBytes = kMiscOff + sizeof(AttnMisc) + 1024;
-    // TMEM columns: S0 | S1 | O0 | O1 (P_i overwrites the first 64 columns of S_i)
+    // TMEM columns: S0 | S1 | O0 | O1, and P_i (64 columns of bf16 pairs).
+    // D = 128: P_i overwrites the first 64 columns of S_i, so the next S_i
+    // waits for the PV MMA that reads P_i.  D = 64: P0 | P1 in the last 128
+    // columns (kSepP), so the next S_i only waits for the softmax to have
+    // read S_i and is computed while the softmax still works on the tile.
+    static constexpr bool kSepP = D == 64;
+    // kSepP: one MMA-issuing thread per Q tile (warps 9 and 10), the K and V
+    // tiles loaded by one producer (warp 8); otherwise one issuer (warp 9)
+    // and one producer each for K (warp 8) and V (warp 10)
+    static constexpr uint32_t kIssuers = kSepP ? 2u : 1u;
     __host__ __device__ static constexpr uint32_t s_col(int i) { return i ? 128u : 0u; }
     __host__ __device__ static constexpr uint32_t o_col(int i) { return i ? 256u + D : 256u; }
+    __host__ __device__ static constexpr uint32_t p_col(int i) { return kSepP ? 384u + 64u * i : s_col(i); }
 };
 
 __device__ __forceinline__ void record_failure(AttnMisc &ms, int *status) {
@@ -199,10 +216,11 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]
         : "memory");
 }
 
-// score_mod in base-2 units, two columns (c, c+1) at a time on packed fp32x2:
-//   identity : x = k0 s                              k0 = scale log2(e)
-//   softcap  : x = k1 tanh(k0 s)                     k0 = scale / cap, k1 = log2(e) cap
-//   ALiBi    : x = k0 s + slope2 c                   slope2 = log2(e) slope_h
+// score_mod in base-2 units, two columns (c, c+1) at a time on packed fp32x2,
+// plus a per-tile addend A (the softmax folds its running-max shift into it):
+//   identity : x = k0 s + A                          k0 = scale log2(e)
+//   softcap  : x = k1 tanh(k0 s) + A                 k0 = scale / cap, k1 = log2(e) cap
+//   ALiBi    : x = k0 s + slope2 c + A               slope2 = log2(e) slope_h
 // The softcap's tanh is the hardware's single-instruction approximation
 // (tanh.approx.f32, relative error about 2^-11), one special-function
 // operation per score beside the softmax's exponential.
@@ -213,7 +231,7 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]
 // seven adds each, error below 1e-4 in base-2 units on the tile's columns).
 template <int SCORE>
 struct ScoreLog2 {
-    uint64_t k0, k1;
+    uint64_t k0, k1, add2;
     float slope2, offset;
     uint64_t bias[8];  // ALiBi: slope2 * (2j, 2j+1) for the next pair j of each of 8 chains
     uint64_t step;     // ALiBi: 16 slope2 in both lanes (8 pairs further on)
@@ -231,12 +249,19 @@ struct ScoreLog2 {
         step = f2_pack(16.f * slope2, 16.f * slope2);
         offset = 0.f;
     }
-    // start of a tile: per-tile row offset and the eight bias chains
-    __device__ __forceinline__ void tile(int kv0, int q) {
+    // row offset of a tile (ALiBi: slope2 (kv0 - q); 0 otherwise)
+    __device__ __forceinline__ float tile_offset(int kv0, int q) const {
+        return SCORE == FLEX_SCORE_ALIBI ? slope2 * (float)(kv0 - q) : 0.f;
+    }
+    // start of a tile: its row offset, the addend A, and the eight bias chains
+    __device__ __forceinline__ void tile(int kv0, int q, float a) {
         if constexpr (SCORE == FLEX_SCORE_ALIBI) {
             offset = slope2 * (float)(kv0 - q);
 #pragma unroll
-            for (int t = 0; t < 8; ++t) bias[t] = f2_pack(slope2 * (float)(2 * t), slope2 * (float)(2 * t + 1));
+            for (int t = 0; t < 8; ++t)
+                bias[t] = f2_pack(fmaf(slope2, (float)(2 * t), a), fmaf(slope2, (float)(2 * t + 1), a));
+        } else {
+            add2 = f2_pack(a, a);
         }
     }
     // columns 2j, 2j+1 (called for j = 0, 1, ..., 63 in order)
@@ -244,13 +269,13 @@ struct ScoreLog2 {
         if constexpr (SCORE == FLEX_SCORE_SOFTCAP) {
             float t0, t1;
             f2_unpack(f2_mul(s2, k0), t0, t1);
-            return f2_mul(f2_pack(tanh_approx(t0), tanh_approx(t1)), k1);
+            return f2_fma(f2_pack(tanh_approx(t0), tanh_approx(t1)), k1, add2);
         } else if constexpr (SCORE == FLEX_SCORE_ALIBI) {
             const uint64_t x = f2_fma(s2, k0, bias[j & 7]);
             bias[j & 7] = f2_add(bias[j & 7], step);
             return x;
         } else {
-            return f2_mul(s2, k0);
+            return f2_fma(s2, k0, add2);
         }
     }
 };
@@ -458,23 +483,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&ms.q_full, 1);
-        mbar_init(&ms.q_empty, 1);
+        mbar_init(&ms.q_empty, C::kIssuers);
         mbar_init(&ms.q_loaded, 1);
         mbar_init(&ms.near_end, 1);
         for (int s = 0; s < NS; ++s) {
             mbar_init(&ms.k_full[s], 1);
             mbar_init(&ms.v_full[s], 1);
-            mbar_init(&ms.k_empty[s], 1);
-            mbar_init(&ms.v_empty[s], 1);
+            mbar_init(&ms.k_empty[s], C::kIssuers);
+            mbar_init(&ms.v_empty[s], C::kIssuers);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ms.s_full[i], 1);
             mbar_init(&ms.p_full[i], 128);
+            mbar_init(&ms.s_free[i], 128);
+            mbar_init(&ms.pv_done[i], 1);
             mbar_init(&ms.item_ready[i], 1);
             mbar_init(&ms.item_free[i], kItemConsumers);
         }
-        mbar_init(&ms.o_full, 1);
-        mbar_init(&ms.drain, 1);
+        mbar_init(&ms.o_full, C::kIssuers);
+        mbar_init(&ms.drain[0], 1);
+        mbar_init(&ms.drain[1], 1);
         mbar_init(&ms.clc_bar, 1);
         ms.abort = 0;
         fence_barrier_init();
@@ -588,13 +616,62 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // MMA thread has already consumed it)
         if (lane == 0 && nq > 0) drain_wait(q_bar, (nq - 1) & 1u);
         __syncwarp();
-    } else if (warp == kTmaWarp || warp == kTmaVWarp) {
+    } else if (warp == kTmaWarp || (!C::kSepP && warp == kTmaVWarp)) {
         // ----------------------------------------------------- TMA producers
         // warp 8 loads the K tiles, warp 10 the V tiles, into the stage ring
         // indexed by the CTA's global step count.  K of a stage is free once
         // its step's S MMAs are done, V once its PV MMAs are; with one
         // producer each, a late V release never holds back the next K.
-        if (lane == 0) {
+        if (C::kSepP && lane == 0) {
+            // one producer: K then V of every step (the V wait never holds
+            // back a K that an S MMA is waiting for: V of a stage is freed
+            // by the PV MMAs of kStages steps ago)
+            const int32_t *doc_base = DOC ? p.mask.doc_ids : nullptr;
+            prefetch_tensormap(&tmap_k);
+            prefetch_tensormap(&tmap_v);
+            uint32_t g = 0;
+            bool ok = true;
+            for (uint32_t n = 0; ok; ++n) {
+                const int k = (int)(n & 1u);
+                const ItemSlot &sl = ms.slot[k];
+                if (!mbar_wait(&ms.item_ready[k], (n >> 1) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int nu = sl.nu;
+                if (nu < 0) break;
+                const int b = sl.b, h = sl.h;
+                for (int u = 0; u < nu; ++u, ++g) {
+                    const int s = (int)(g % NS);
+                    const uint32_t use = g / NS;
+                    const int kv0 = (int)(sl.ulist[u] & 0xFFFFu) * kBlock;
+                    uint8_t *dst = smem + C::kKvOff + s * C::kStageBytes;
+                    if (use > 0 && !mbar_wait(&ms.k_empty[s], (use - 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&ms.k_full[s], C::kTileBytes);
+                    for (int a = 0; a < C::kAtoms; ++a) tma_load_4d(dst + a * C::kAtomBytes, &tmap_k, &ms.k_full[s], 64 * a, kv0, h, b);
+                    if (use > 0 && !mbar_wait(&ms.v_empty[s], (use - 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t doc_bytes = DOC ? 4u * (uint32_t)min(kBlock, p.mask.doc_len - kv0) : 0u;
+                    mbar_arrive_expect_tx(&ms.v_full[s], C::kTileBytes + doc_bytes);
+                    for (int a = 0; a < C::kAtoms; ++a)
+                        tma_load_4d(dst + C::kTileBytes + a * C::kAtomBytes, &tmap_v, &ms.v_full[s], 64 * a, kv0, h, b);
+                    if (DOC) bulk_load(ms.stage_doc[s], doc_base + (int64_t)b * p.mask.doc_len + kv0, doc_bytes, &ms.v_full[s]);
+                }
+                if (ok && nu > 0) mbar_arrive(&ms.near_end);
+                if (ok) mbar_arrive(&ms.item_free[k]);
+            }
+            if (!ok) record_failure(ms, p.status);
+            for (uint32_t s = 0; s < (uint32_t)NS && s < g; ++s) {
+                const uint32_t last = s + ((g - 1 - s) / NS) * NS;
+                drain_wait(&ms.k_full[s], (last / NS) & 1u);
+                drain_wait(&ms.v_full[s], (last / NS) & 1u);
+            }
+        } else if (lane == 0) {
             const bool is_k = warp == kTmaWarp;
             const CUtensorMap *map = is_k ? &tmap_k : &tmap_v;
             uint64_t *full = is_k ? ms.k_full : ms.v_full;
@@ -647,6 +724,112 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const uint32_t last = s + ((g - 1 - s) / NS) * NS;
                 drain_wait(&full[s], (last / NS) & 1u);
             }
+        }
+        __syncwarp();
+    } else if (C::kSepP && (warp == kMmaWarp || warp == kTmaVWarp)) {
+        // ------------------------------------------- MMA issuers (kSepP)
+        // One thread per Q tile ti, each walking every item and step: S runs
+        // two steps ahead (S_ti(u + 2) replaces S_ti(u + 1) once the softmax
+        // has read it, and is issued right after PV_ti(u)), so the softmax
+        // never waits for an S MMA, and neither tile's MMAs wait behind the
+        // other tile's barriers.  The ring, Q and O barriers take one commit
+        // from each thread per step or item, tile present or not.
+        if (lane == 0) {
+            const int ti = warp == kMmaWarp ? 0 : 1;
+            const uint32_t present = ti ? 4u : 1u;
+            constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
+            constexpr uint32_t kHi = smem_desc_hi_sw128(1024);
+            const uint32_t kv_lo0 = smem_desc_lo(smem_u32(smem + C::kKvOff), 16);
+            const uint32_t v_lo0 = smem_desc_lo(smem_u32(smem + C::kKvOff + C::kTileBytes), C::kAtomBytes);
+            const uint32_t qa = smem_desc_lo(smem_u32(smem + C::kQOff + ti * C::kTileBytes), 16);
+            uint32_t s_total = 0, pv_total = 0;  // this tile's S and PV groups over all items
+            auto issue_s = [&](int s) -> bool {
+                if (s_total > 0 && !mbar_wait(&ms.s_free[ti], (s_total - 1) & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+                ++s_total;
+                const uint32_t ka = kv_lo0 + ((s * C::kStageBytes) >> 4);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = ((k / 4) * C::kAtomBytes + (k % 4) * 32) >> 4;
+                    mma_ss_lo<kHi, kHi>(tmem + C::s_col(ti), qa + off, ka + off, idesc_s, k > 0 ? 1u : 0u);
+                }
+                mma_commit(&ms.s_full[ti]);
+                return true;
+            };
+            auto issue_pv = [&](int s, bool acc) -> bool {
+                if (!mbar_wait(&ms.p_full[ti], pv_total & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+                const uint32_t va = v_lo0 + ((s * C::kStageBytes) >> 4);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    mma_ts_lo<kHi>(tmem + C::o_col(ti), tmem + C::p_col(ti) + k * 8, va + ((k * 2048) >> 4), idesc_o,
+                                   (k > 0 || acc) ? 1u : 0u);
+                mma_commit(&ms.pv_done[ti]);
+                ++pv_total;
+                return true;
+            };
+            uint32_t g = 0, nq = 0;
+            bool ok = true;
+            for (uint32_t n = 0; ok; ++n) {
+                const int k = (int)(n & 1u);
+                const ItemSlot &sl = ms.slot[k];
+                if (!mbar_wait(&ms.item_ready[k], (n >> 1) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int nu = sl.nu;
+                if (nu < 0) break;
+                if (nu > 0) {
+                    ok = mbar_wait(&ms.q_full, nq & 1u, abort_flag);
+                    tc_fence_after_sync();
+                    // S of the first two steps
+                    for (int u = 0; ok && u < min(nu, 2); ++u) {
+                        const uint32_t gu = g + (uint32_t)u;
+                        const int s = (int)(gu % NS);
+                        ok = mbar_wait(&ms.k_full[s], (gu / NS) & 1u, abort_flag) &&
+                             (!((sl.ulist[u] >> 16) & present) || issue_s(s));
+                        mma_commit(&ms.k_empty[s]);
+                        if (u + 1 == nu) mma_commit(&ms.q_empty);  // the item's last S is issued
+                    }
+                    uint32_t pv_item = 0;
+                    for (int u = 0; ok && u < nu; ++u) {
+                        const uint32_t gu = g + (uint32_t)u;
+                        const int s = (int)(gu % NS);
+                        if (!mbar_wait(&ms.v_full[s], (gu / NS) & 1u, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        if ((sl.ulist[u] >> 16) & present) {
+                            if (!issue_pv(s, pv_item > 0)) {
+                                ok = false;
+                                break;
+                            }
+                            ++pv_item;
+                        }
+                        mma_commit(&ms.v_empty[s]);
+                        if (u + 2 < nu) {
+                            const uint32_t g2 = gu + 2;
+                            const int s2 = (int)(g2 % NS);
+                            if (!mbar_wait(&ms.k_full[s2], (g2 / NS) & 1u, abort_flag) ||
+                                (((sl.ulist[u + 2] >> 16) & present) && !issue_s(s2))) {
+                                ok = false;
+                                break;
+                            }
+                            mma_commit(&ms.k_empty[s2]);
+                            if (u + 3 == nu) mma_commit(&ms.q_empty);
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(&ms.o_full);
+                    g += (uint32_t)nu;
+                    ++nq;
+                }
+                mbar_arrive(&ms.item_free[k]);
+            }
+            if (!ok) record_failure(ms, p.status);
+            mma_commit(&ms.drain[ti]);  // every MMA issued above completes before TMEM is freed
+            drain_wait(&ms.drain[ti], 0);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -722,7 +905,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const bool nxt = u + 1 < nu;
                         const int s1 = (int)((gu + 1) % NS);
                         const uint32_t f1 = nxt ? (sl.ulist[u + 1] >> 16) : 0u;
-                        if (!mbar_wait(&ms.v_full[s], (gu / NS) & 1u, abort_flag)) {
+                        // V of this step and K of the next arrive by TMA (the
+                        // mbarriers alone order them for the MMA); both are
+                        // waited for before P_0, which is usually last to come
+                        if (!mbar_wait(&ms.v_full[s], (gu / NS) & 1u, abort_flag) ||
+                            (nxt && !mbar_wait(&ms.k_full[s1], ((gu + 1) / NS) & 1u, abort_flag))) {
                             ok = false;
                             break;
                         }
@@ -730,14 +917,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             ok = false;
                             break;
                         }
-                        if (nxt) {
-                            // K arrives by TMA: the mbarrier alone orders it for the MMA
-                            if (!mbar_wait(&ms.k_full[s1], ((gu + 1) / NS) & 1u, abort_flag)) {
-                                ok = false;
-                                break;
-                            }
-                            if (f1 & 1u) issue_s(0, s1);
-                        }
+                        if (nxt && (f1 & 1u)) issue_s(0, s1);
                         if ((f & 4u) && !issue_pv(1, s)) {
                             ok = false;
                             break;
@@ -757,8 +937,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 mbar_arrive(&ms.item_free[k]);
             }
             if (!ok) record_failure(ms, p.status);
-            mma_commit(&ms.drain);  // every MMA issued above completes before TMEM is freed
-            drain_wait(&ms.drain, 0);
+            mma_commit(&ms.drain[0]);  // every MMA issued above completes before TMEM is freed
+            drain_wait(&ms.drain[0], 0);
         }
         __syncwarp();
     } else if (warp < 8) {
@@ -768,6 +948,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int t = threadIdx.x % 128;
         const uint32_t lane_base = (uint32_t)((warp % 4) * 32) << 16;
         const uint32_t s_addr = tmem + lane_base + C::s_col(i);
+        const uint32_t p_addr = tmem + lane_base + C::p_col(i);
         const uint32_t o_addr = tmem + lane_base + C::o_col(i);
         const uint32_t present = i ? 4u : 1u, fullbit = i ? 8u : 2u;
         uint32_t cnt_total = 0;  // S_i tiles consumed over all items (s_full parity)
@@ -811,11 +992,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
+                // The scores come out shifted by A: by the running max's
+                // shift (offset - m_run) once the row has a finite running
+                // max, so that most tiles need no separate subtraction pass;
+                // by nothing before that.
+                const float a_shift = m_run > -FLT_MAX ? score.tile_offset(kv0, q) - m_run : 0.f;
                 uint64_t x2[64];
                 {
                     uint32_t r[128];
                     tmem_ld128_sync(s_addr, r);
-                    score.tile(kv0, q);
+                    if constexpr (C::kSepP) {
+                        tc_fence_before_sync();
+                        mbar_arrive(&ms.s_free[i]);  // S_i may be overwritten by the next S MMA
+                    }
+                    score.tile(kv0, q, a_shift);
 #pragma unroll
                     for (int j = 0; j < 64; ++j)
                         x2[j] = score.pair(f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), j);
@@ -847,51 +1037,86 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     f2_unpack(x2[j], lo, hi);
                     mx[j & 7] = fmax3(mx[j & 7], lo, hi);
                 }
-                const float m_tile = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) +
-                                     score.offset;
+                const float m_tile = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) -
+                                     a_shift + score.offset;
                 m_max = fmaxf(m_max, m_tile);
                 float alpha = 1.f;
                 if (m_tile > m_run + kRescaleThreshold) {  // always taken at the row's first live tile
                     alpha = ex2_approx(m_run - m_tile);
                     m_run = m_tile;
                 }
-                const float sub = score.offset - m_run;
-                const uint64_t sub2 = f2_pack(sub, sub);
-                // O rescale (rare) before the first half of P is handed over:
-                // the PV MMA of this step accumulates into the rescaled O
-                if (cnt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld32_sync(o_addr + c0, o);
-                        const uint64_t a2 = f2_pack(alpha, alpha);
+                // the exponent is s - m_run: what the scores already carry
+                // unless this tile raised the running max (or it was not
+                // finite when the tile started); one pass over the tile then
+                const float shift = (score.offset - m_run) - a_shift;
+                if (__any_sync(0xffffffffu, shift != 0.f)) {
+                    const uint64_t shift2 = f2_pack(shift, shift);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            float lo, hi;
-                            f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * j]), __uint_as_float(o[2 * j + 1])), a2), lo,
-                                      hi);
-                            o[2 * j] = __float_as_uint(lo);
-                            o[2 * j + 1] = __float_as_uint(hi);
-                        }
-                        tmem_st32(o_addr + c0, o);
-                    }
+                    for (int j = 0; j < 64; ++j) x2[j] = f2_add(x2[j], shift2);
                 }
-                float rsum4[4] = {0.f, 0.f, 0.f, 0.f};
+                // O rescale (rare) before P is handed over: the PV MMA of
+                // this step accumulates into the rescaled O
+                auto rescale_o = [&]() {
+                    if (cnt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t o[32];
+                            tmem_ld32_sync(o_addr + c0, o);
+                            const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-                for (int gq = 0; gq < 4; ++gq) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int t2 = 0; t2 < 16; ++t2) {
-                        const int j = 16 * gq + t2;
-                        float d0, d1;
-                        f2_unpack(f2_add(x2[j], sub2), d0, d1);
-                        pk[t2] = pack_bf16x2(ex2_approx(d0), ex2_approx(d1));
+                            for (int j = 0; j < 16; ++j) {
+                                float lo, hi;
+                                f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * j]), __uint_as_float(o[2 * j + 1])), a2),
+                                          lo, hi);
+                                o[2 * j] = __float_as_uint(lo);
+                                o[2 * j + 1] = __float_as_uint(hi);
+                            }
+                            tmem_st32(o_addr + c0, o);
+                        }
                     }
-                    tmem_st16(s_addr + 16 * gq, pk);
-                    // the row sum takes the bf16 weights the PV MMA reads,
-                    // so each row's weights sum to l exactly
+                };
+                // the row sum takes the bf16 weights the PV MMA reads, so
+                // each row's weights sum to l exactly
+                float rsum4[4] = {0.f, 0.f, 0.f, 0.f};
+                if constexpr (C::kSepP) {
+                    // all of P in registers first; P_i and O_i are written
+                    // once the previous PV MMA of this tile has read P_i and
+                    // accumulated into O_i
+                    uint32_t pk[64];
 #pragma unroll
-                    for (int t2 = 0; t2 < 16; ++t2) add_bf16x2_to_f32(rsum4[2 * (t2 & 1)], rsum4[2 * (t2 & 1) + 1], pk[t2]);
+                    for (int j = 0; j < 64; ++j) {
+                        float d0, d1;
+                        f2_unpack(x2[j], d0, d1);
+                        pk[j] = pack_bf16x2(ex2_approx(d0), ex2_approx(d1));
+                    }
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) add_bf16x2_to_f32(rsum4[2 * (j & 1)], rsum4[2 * (j & 1) + 1], pk[j]);
+                    if (cnt_total > 0 && !warp_wait(&ms.pv_done[i], (cnt_total - 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    rescale_o();
+#pragma unroll
+                    for (int gq = 0; gq < 4; ++gq)
+                        tmem_st16(p_addr + 16 * gq, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * gq]));
+                } else {
+                    rescale_o();
+#pragma unroll
+                    for (int gq = 0; gq < 4; ++gq) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int t2 = 0; t2 < 16; ++t2) {
+                            const int j = 16 * gq + t2;
+                            float d0, d1;
+                            f2_unpack(x2[j], d0, d1);
+                            pk[t2] = pack_bf16x2(ex2_approx(d0), ex2_approx(d1));
+                        }
+                        tmem_st16(p_addr + 16 * gq, pk);
+#pragma unroll
+                        for (int t2 = 0; t2 < 16; ++t2)
+                            add_bf16x2_to_f32(rsum4[2 * (t2 & 1)], rsum4[2 * (t2 & 1) + 1], pk[t2]);
+                    }
                 }
                 tmem_wait_st();
                 tc_fence_before_sync();
