@@ -200,6 +200,13 @@ __device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t (&r)[12
         : "memory");
 }
 
+// 32-byte global store (eight 32-bit words) to a 32-byte aligned address.
+__device__ __forceinline__ void st_global_32B(void *dst, const uint32_t *w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                 "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // TMEM read of 32 columns of this thread's lane, completed before returning.
 __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
@@ -1136,7 +1143,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (ok) {
                 tc_fence_after_sync();
                 const int64_t orow = bh * p.q_len + q;
-                uint4 *dst = reinterpret_cast<uint4 *>(p.out + orow * D);
+                uint16_t *dst = p.out + orow * D;
                 const bool store = q < p.q_len;  // rows of a tail tile past Q_LEN are padding
                 const bool live = have && l_run > 0.f;
                 const float inv = live ? 1.f / l_run : 0.f;
@@ -1153,10 +1160,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         pk[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+                    // whole 32-byte sectors per store (the row's 16 values)
                     if (store) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            dst[c0 / 8 + j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                        st_global_32B(dst + c0, &pk[0]);
+                        st_global_32B(dst + c0 + 16, &pk[8]);
                     }
                 }
                 if (store) {
