@@ -200,13 +200,6 @@ __device__ __forceinline__ void tmem_ld128_sync(uint32_t taddr, uint32_t (&r)[12
         : "memory");
 }
 
-// 32-byte global store (eight 32-bit words) to a 32-byte aligned address.
-__device__ __forceinline__ void st_global_32B(void *dst, const uint32_t *w) {
-    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                 "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                 : "memory");
-}
-
 // TMEM read of 32 columns of this thread's lane, completed before returning.
 __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(

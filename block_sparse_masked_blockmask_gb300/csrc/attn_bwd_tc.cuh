@@ -631,7 +631,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll 1
             for (int which = 0; which < (KV_MAJOR ? 2 : 1); ++which) {
                 const float mul = (KV_MAJOR && which == 0) ? 1.f : p.scale;
-                uint4 *dst = reinterpret_cast<uint4 *>((which == 0 ? p.out0 : p.out1) + orow * D);
+                uint16_t *dst = (which == 0 ? p.out0 : p.out1) + orow * D + half * (D / 2);
                 const uint32_t col = (which == 0 ? C::kAcc0 : C::kAcc1) + half * (D / 2);
 #pragma unroll 1
                 for (int c0 = 0; c0 < D / 2; c0 += 32) {
@@ -646,11 +646,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         pk[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * mul, __uint_as_float(o[2 * j + 1]) * mul);
+                    // whole 32-byte sectors per store
                     if (store) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            dst[(half * (D / 2) + c0) / 8 + j] =
-                                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                        st_global_32B(dst + c0, &pk[0]);
+                        st_global_32B(dst + c0 + 16, &pk[8]);
                     }
                 }
             }
