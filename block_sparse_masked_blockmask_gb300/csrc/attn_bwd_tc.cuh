@@ -68,7 +68,8 @@ struct BwdTcParams {
 
 struct BwdMisc {
     uint64_t res_full;
-    uint64_t str_full[4], str_empty[4];
+    uint64_t a_full[4], a_empty[4];         // ring of the first streamed tile (K, or Q when KV_MAJOR)
+    uint64_t b_full[4], b_empty[4];         // ring of the second (V, or dO when KV_MAJOR)
     uint64_t s_full, dp_full, p_ready, ds_ready, acc_full, drain;
     uint64_t col_ready[2];                  // the elementwise warps' per-column data of a step
     uint32_t tmem_base;
@@ -82,17 +83,28 @@ struct BwdMisc {
     alignas(16) uint32_t words[kBwdMaxList];// per walked tile: listed bit and full-pair count (tilelist.cuh)
 };
 
-template <int D>
+// The two streamed tiles of a step have rings of their own.  The first (K, or
+// Q when KV_MAJOR) is read by the step's S MMA, issued a step ahead, and by
+// its dQ (dK) MMA at the end of the step; the second (V, or dO) by the dP
+// MMA, issued a step ahead, and when KV_MAJOR by the dV MMA in mid-step.  At
+// D = 128 shared memory holds four streamed tiles: two of each when
+// KV_MAJOR; otherwise three K and one V, since V is released as soon as its
+// dP MMA is done and K must arrive a step before its S MMA.
+template <int D, bool KV_MAJOR>
 struct BwdTcCfg {
     static_assert(D == 64 || D == 128, "head dim");
     static constexpr int kAtoms = D / 64;
     static constexpr uint32_t kAtomBytes = 128 * 128;
     static constexpr uint32_t kTileBytes = 128 * D * 2;
-    static constexpr int kStages = D == 128 ? 2 : 4;
-    static constexpr uint32_t kResOff = 0;                       // two resident tiles
-    static constexpr uint32_t kStrOff = 2 * kTileBytes;          // stages of two streamed tiles
-    static constexpr uint32_t kStageBytes = 2 * kTileBytes;
-    static constexpr uint32_t kMiscOff = kStrOff + kStages * kStageBytes;
+    static constexpr int kNA = D == 128 ? (KV_MAJOR ? 2 : 3) : 4;  // ring depths
+    static constexpr int kNB = D == 128 ? (KV_MAJOR ? 2 : 1) : 4;
+    // rings of equal depth share the first ring's barriers (one wait and one
+    // release per step for both tiles, as one stage of two tiles)
+    static constexpr bool kSplit = kNA != kNB;
+    static constexpr uint32_t kResOff = 0;                         // two resident tiles
+    static constexpr uint32_t kAOff = 2 * kTileBytes;              // ring of the first streamed tile
+    static constexpr uint32_t kBOff = kAOff + kNA * kTileBytes;    // ring of the second
+    static constexpr uint32_t kMiscOff = kBOff + kNB * kTileBytes;
     static constexpr uint32_t kSmemBytes = kMiscOff + sizeof(BwdMisc) + 1024;
     // TMEM columns: S | dP | acc0 | acc1.  P (KV_MAJOR) and dS are written
     // back as bf16 over the columns they came from: the walked columns
@@ -201,8 +213,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap map_r0, const __grid_constant__ CUtensorMap map_r1,
                        const __grid_constant__ CUtensorMap map_s0, const __grid_constant__ CUtensorMap map_s1,
                        const BwdTcParams p) {
-    using C = BwdTcCfg<D>;
-    constexpr int NS = C::kStages;
+    using C = BwdTcCfg<D, KV_MAJOR>;
+    constexpr int NA = C::kNA, NB = C::kNB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     BwdMisc &ms = *reinterpret_cast<BwdMisc *>(smem + C::kMiscOff);
@@ -227,9 +239,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&ms.res_full, 1);
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&ms.str_full[s], 1);
-            mbar_init(&ms.str_empty[s], 1);
+        for (int s = 0; s < 4; ++s) {
+            mbar_init(&ms.a_full[s], 1);
+            mbar_init(&ms.a_empty[s], 1);
+            mbar_init(&ms.b_full[s], 1);
+            mbar_init(&ms.b_empty[s], 1);
         }
         mbar_init(&ms.s_full, 1);
         mbar_init(&ms.dp_full, 1);
@@ -290,29 +304,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             own * 128, h, b);
             }
             bool ok = true;
-            int n = 0;
-            for (; n < N; ++n) {
-                const int s = n % NS;
-                const uint32_t use = (uint32_t)(n / NS);
-                if (use > 0 && !mbar_wait(&ms.str_empty[s], (use - 1) & 1u, abort_flag)) {
+            int na = 0, nb = 0;  // tiles issued into each ring
+            for (int n = 0; n < N; ++n) {
+                const int sa = n % NA, sb = n % NB;
+                const uint32_t ua = (uint32_t)(n / NA), ub = (uint32_t)(n / NB);
+                const int blk = (int)(ms.list[n] & 0xFFFFu);
+                if (ua > 0 && !mbar_wait(&ms.a_empty[sa], (ua - 1) & 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const int blk = (int)(ms.list[n] & 0xFFFFu);
-                uint8_t *dst = smem + C::kStrOff + s * C::kStageBytes;
-                mbar_arrive_expect_tx(&ms.str_full[s], 2 * C::kTileBytes);
-                for (int a = 0; a < C::kAtoms; ++a) {
-                    tma_load_4d(dst + a * C::kAtomBytes, &map_s0, &ms.str_full[s], 64 * a, blk * 128, h, b);
-                    tma_load_4d(dst + C::kTileBytes + a * C::kAtomBytes, &map_s1, &ms.str_full[s], 64 * a,
-                                blk * 128, h, b);
+                uint8_t *dst = smem + C::kAOff + sa * C::kTileBytes;
+                mbar_arrive_expect_tx(&ms.a_full[sa], (C::kSplit ? 1u : 2u) * C::kTileBytes);
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_4d(dst + a * C::kAtomBytes, &map_s0, &ms.a_full[sa], 64 * a, blk * 128, h, b);
+                ++na;
+                uint64_t *bbar = &ms.a_full[sa];
+                if constexpr (C::kSplit) {
+                    if (ub > 0 && !mbar_wait(&ms.b_empty[sb], (ub - 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    bbar = &ms.b_full[sb];
+                    mbar_arrive_expect_tx(bbar, C::kTileBytes);
                 }
+                dst = smem + C::kBOff + sb * C::kTileBytes;
+                for (int a = 0; a < C::kAtoms; ++a)
+                    tma_load_4d(dst + a * C::kAtomBytes, &map_s1, bbar, 64 * a, blk * 128, h, b);
+                ++nb;
             }
             if (!ok) bwd_fail(ms, p.status);
             // every copy issued above lands before the CTA exits
             drain_wait_bwd(&ms.res_full, 0);
-            for (int s = 0; s < NS && s < n; ++s) {
-                const int last = s + ((n - 1 - s) / NS) * NS;
-                drain_wait_bwd(&ms.str_full[s], (uint32_t)(last / NS) & 1u);
+            for (int s = 0; s < NA && s < na; ++s) {
+                const int last = s + ((na - 1 - s) / NA) * NA;
+                drain_wait_bwd(&ms.a_full[s], (uint32_t)(last / NA) & 1u);
+            }
+            for (int s = 0; C::kSplit && s < NB && s < nb; ++s) {
+                const int last = s + ((nb - 1 - s) / NB) * NB;
+                drain_wait_bwd(&ms.b_full[s], (uint32_t)(last / NB) & 1u);
             }
         }
         __syncwarp();
@@ -324,10 +353,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr uint32_t kHi = smem_desc_hi_sw128(1024);
             const uint32_t r0_lo = smem_desc_lo(smem_u32(smem + C::kResOff), 16);
             const uint32_t r1_lo = smem_desc_lo(smem_u32(smem + C::kResOff + C::kTileBytes), 16);
-            const uint32_t s0_lo = smem_desc_lo(smem_u32(smem + C::kStrOff), 16);
-            const uint32_t s1_lo = smem_desc_lo(smem_u32(smem + C::kStrOff + C::kTileBytes), 16);
-            const uint32_t s0_mn = smem_desc_lo(smem_u32(smem + C::kStrOff), C::kAtomBytes);
-            const uint32_t s1_mn = smem_desc_lo(smem_u32(smem + C::kStrOff + C::kTileBytes), C::kAtomBytes);
+            const uint32_t s0_lo = smem_desc_lo(smem_u32(smem + C::kAOff), 16);
+            const uint32_t s1_lo = smem_desc_lo(smem_u32(smem + C::kBOff), 16);
+            const uint32_t s0_mn = smem_desc_lo(smem_u32(smem + C::kAOff), C::kAtomBytes);
+            const uint32_t s1_mn = smem_desc_lo(smem_u32(smem + C::kBOff), C::kAtomBytes);
             // A (M = 128 resident rows, K = D) times B^T (N = 128 walked rows, K = D), both K-major
             auto issue_ss = [&](uint32_t dcol, uint32_t a_lo, uint32_t b_lo) {
 #pragma unroll
@@ -344,31 +373,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mma_ts_lo<kHi>(tmem + dcol, tmem + acol + 64 * (k / 4) + 8 * (k % 4), b_mn + ((k * 2048) >> 4),
                                    idesc_acc, (k > 0 || acc) ? 1u : 0u);
             };
-            constexpr uint32_t stage16 = C::kStageBytes >> 4;
-            bool ok = mbar_wait(&ms.res_full, 0, abort_flag) && mbar_wait(&ms.str_full[0], 0, abort_flag);
+            constexpr uint32_t tile16 = C::kTileBytes >> 4;
+            bool ok = mbar_wait(&ms.res_full, 0, abort_flag) && mbar_wait(&ms.a_full[0], 0, abort_flag) &&
+                      (!C::kSplit || mbar_wait(&ms.b_full[0], 0, abort_flag));
             if (ok) {
                 tc_fence_after_sync();
                 issue_ss(C::kS, r0_lo, s0_lo);
                 mma_commit(&ms.s_full);
                 issue_ss(C::kDP, r1_lo, s1_lo);
                 mma_commit(&ms.dp_full);
+                if constexpr (C::kSplit && !KV_MAJOR) mma_commit(&ms.b_empty[0]);  // V is read by dP alone
             }
             for (int n = 0; ok && n < N; ++n) {
-                const int s = n % NS;
+                const int sa = n % NA, sb = n % NB;
                 const bool nxt = n + 1 < N;
-                const int s1 = (n + 1) % NS;
+                const int sa1 = (n + 1) % NA, sb1 = (n + 1) % NB;
                 if (!mbar_wait(&ms.p_ready, (uint32_t)n & 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                if constexpr (KV_MAJOR) issue_ts(C::kAcc0, C::kS, s1_mn + s * stage16, n > 0);  // dV += P^T dO
+                if constexpr (KV_MAJOR) {
+                    issue_ts(C::kAcc0, C::kS, s1_mn + sb * tile16, n > 0);  // dV += P^T dO
+                    if constexpr (C::kSplit) mma_commit(&ms.b_empty[sb]);   // dO no longer read
+                }
                 if (nxt) {
-                    if (!mbar_wait(&ms.str_full[s1], (uint32_t)((n + 1) / NS) & 1u, abort_flag)) {
+                    if (!mbar_wait(&ms.a_full[sa1], (uint32_t)((n + 1) / NA) & 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    issue_ss(C::kS, r0_lo, s0_lo + s1 * stage16);
+                    issue_ss(C::kS, r0_lo, s0_lo + sa1 * tile16);
                     mma_commit(&ms.s_full);
                 }
                 if (!mbar_wait(&ms.ds_ready, (uint32_t)n & 1u, abort_flag)) {
@@ -377,11 +411,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
                 tc_fence_after_sync();
                 // dK += dS^T Q (KV_MAJOR) or dQ += dS K
-                issue_ts(KV_MAJOR ? C::kAcc1 : C::kAcc0, C::kDP, s0_mn + s * stage16, n > 0);
-                mma_commit(&ms.str_empty[s]);
+                issue_ts(KV_MAJOR ? C::kAcc1 : C::kAcc0, C::kDP, s0_mn + sa * tile16, n > 0);
+                mma_commit(&ms.a_empty[sa]);
                 if (nxt) {
-                    issue_ss(C::kDP, r1_lo, s1_lo + s1 * stage16);
+                    if (C::kSplit && !mbar_wait(&ms.b_full[sb1], (uint32_t)((n + 1) / NB) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    issue_ss(C::kDP, r1_lo, s1_lo + sb1 * tile16);
                     mma_commit(&ms.dp_full);
+                    if constexpr (C::kSplit && !KV_MAJOR) mma_commit(&ms.b_empty[sb1]);
                 }
             }
             if (ok) mma_commit(&ms.acc_full);

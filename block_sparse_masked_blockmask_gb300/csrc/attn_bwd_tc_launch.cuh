@@ -9,7 +9,7 @@ namespace flex {
 
 template <int D, int SCORE, bool DOC, bool KV_MAJOR>
 cudaError_t launch_bwd_tc_kernel(const CUtensorMap (&maps)[4], const BwdTcParams &kp, cudaStream_t stream) {
-    using C = BwdTcCfg<D>;
+    using C = BwdTcCfg<D, KV_MAJOR>;
     auto kernel = attn_bwd_tc_kernel<D, SCORE, DOC, KV_MAJOR>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
