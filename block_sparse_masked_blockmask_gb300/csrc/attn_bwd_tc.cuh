@@ -40,6 +40,7 @@
 
 #include <cfloat>
 #include <climits>
+#include <type_traits>
 
 #include "flex_internal.h"
 #include "ptx.cuh"
@@ -555,23 +556,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             {
                 uint32_t r[64];
                 bwd_tmem_ld64(trow + C::kS + cbase, r);
-#pragma unroll
-                for (int c0 = 0; c0 < 2; ++c0) {
-                    uint32_t keep = 0xFFFFFFFFu;
-                    if (!full) {
-                        keep = interval_bits(clo, chi, cbase + 32 * c0);
-                        if constexpr (DOC) {
-                            uint32_t same = 0u;
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const int4 d = docv4[8 * c0 + j];
-                                same |= ((uint32_t)(d.x == doc_own) | ((uint32_t)(d.y == doc_own) << 1) |
-                                         ((uint32_t)(d.z == doc_own) << 2) | ((uint32_t)(d.w == doc_own) << 3))
-                                        << (4 * j);
-                            }
-                            keep &= same;
-                        }
-                    }
+                // one column chunk; PARTIAL: apply the keep bits (full steps
+                // carry no mask work)
+                auto p_chunk = [&](auto partial, int c0, uint32_t keep) {
+                    constexpr bool PARTIAL = decltype(partial)::value;
                     uint32_t pk[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
@@ -601,8 +589,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         } else {
                             f2_unpack(f2_fma(s2, k0_2, bias2), x0, x1);
                         }
-                        if (!((keep >> (2 * j)) & 1u)) x0 = -INFINITY;
-                        if (!((keep >> (2 * j + 1)) & 1u)) x1 = -INFINITY;
+                        if constexpr (PARTIAL) {
+                            if (!((keep >> (2 * j)) & 1u)) x0 = -INFINITY;
+                            if (!((keep >> (2 * j + 1)) & 1u)) x1 = -INFINITY;
+                        }
                         const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                         if constexpr (KV_MAJOR) pk[j] = pack_bf16x2(p0, p1);
                         pg[c] = p0 * g0;
@@ -610,6 +600,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     }
                     // over this half's S columns, all read above
                     if constexpr (KV_MAJOR) tmem_st16(trow + C::kS + cbase + 16 * c0, pk);
+                };
+#pragma unroll
+                for (int c0 = 0; c0 < 2; ++c0) {
+                    if (full) {
+                        // (document masks keep one code path: their steps are
+                        // often partial, and a second copy measured slower)
+                        if constexpr (DOC) p_chunk(std::true_type{}, c0, 0xFFFFFFFFu);
+                        else p_chunk(std::false_type{}, c0, 0u);
+                    } else {
+                        uint32_t keep = interval_bits(clo, chi, cbase + 32 * c0);
+                        if constexpr (DOC) {
+                            uint32_t same = 0u;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const int4 d = docv4[8 * c0 + j];
+                                same |= ((uint32_t)(d.x == doc_own) | ((uint32_t)(d.y == doc_own) << 1) |
+                                         ((uint32_t)(d.z == doc_own) << 2) | ((uint32_t)(d.w == doc_own) << 3))
+                                        << (4 * j);
+                            }
+                            keep &= same;
+                        }
+                        p_chunk(std::true_type{}, c0, keep);
+                    }
                 }
             }
             if constexpr (KV_MAJOR) tmem_wait_st();
