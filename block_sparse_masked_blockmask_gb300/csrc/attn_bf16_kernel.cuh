@@ -118,7 +118,7 @@ struct AttnMisc {
     uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];
     uint64_t s_full[2], p_full[2];             // p_full[i]: all of P_i is in TMEM
     uint64_t s_free[2], pv_done[2];            // D = 64: S_i read by the softmax / PV_i complete
-    uint64_t o_full, drain[2];
+    uint64_t o_full[2], drain[2];              // o_full[i]: O_i final (kSepP: per tile; else [0] for both)
     uint64_t item_ready[2], item_free[2];      // per item slot
     uint64_t clc_bar;                          // cluster-launch-control response landed
     uint32_t tmem_base;
@@ -500,7 +500,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(&ms.item_ready[i], 1);
             mbar_init(&ms.item_free[i], kItemConsumers);
         }
-        mbar_init(&ms.o_full, C::kIssuers);
+        mbar_init(&ms.o_full[0], 1);
+        mbar_init(&ms.o_full[1], 1);
         mbar_init(&ms.drain[0], 1);
         mbar_init(&ms.drain[1], 1);
         mbar_init(&ms.clc_bar, 1);
@@ -821,7 +822,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         }
                     }
                     if (!ok) break;
-                    mma_commit(&ms.o_full);
+                    mma_commit(&ms.o_full[ti]);
                     g += (uint32_t)nu;
                     ++nq;
                 }
@@ -930,7 +931,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         }
                     }
                     if (!ok) break;
-                    mma_commit(&ms.o_full);
+                    mma_commit(&ms.o_full[0]);
                     g += (uint32_t)nu;
                     ++nq;
                 }
@@ -1128,7 +1129,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             // ---------------------------------------------------- epilogue
             bool have = ok && cnt > 0;
-            if (have && !warp_wait(&ms.o_full, nq & 1u, abort_flag)) {
+            // kSepP: this tile's own issuer signals its O; else one barrier for both
+            if (have && !warp_wait(&ms.o_full[C::kSepP ? i : 0], nq & 1u, abort_flag)) {
                 have = false;
                 ok = false;
             }
