@@ -10,7 +10,7 @@
 //   dS_ij = P_ij (dO_i . v_j - delta_i) score_mod'(t_ij)
 //   dK_j = scale sum_i dS_ij q_i,   dQ_i = scale sum_j dS_ij k_j
 //
-// Two launches of one kernel template, each CTA owning one 128-row block:
+// Two launches of one kernel template, each work item one owned 128-row block:
 //   KV_MAJOR  a kv block j, walking the q blocks of the q side of the
 //             BlockMask (q_num_blocks / q_indices and the full variants):
 //               S^T  = K_j Q_i^T          (SS MMA, TMEM)
@@ -20,8 +20,8 @@
 //               dK_j += dS^T Q_i          (TS MMA: dS^T read from TMEM)
 //   Q-major   a q block i, walking the kv side of the BlockMask:
 //               S = Q_i K_j^T, dP = dO_i V_j^T, dS, dQ_i += dS K_j.
-// Each CTA owns its output rows, so nothing is accumulated across CTAs and
-// the result does not depend on scheduling.  P is recomputed from the saved
+// One CTA computes an item's output rows whole, so nothing is accumulated
+// across CTAs and the result does not depend on scheduling.  P is recomputed from the saved
 // lse (no running max).  Roles (320 threads, one CTA per SM):
 //   warps 0-7  elementwise, two threads per owned row (TMEM lane = row):
 //              warps w and w + 4 share a TMEM lane quarter, the first takes
