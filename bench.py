@@ -247,6 +247,8 @@ def main():
                     help="timed flex_attention_bwd launches on the same workload; 0 skips them")
     ap.add_argument("--config-steps", type=int, default=20,
                     help="timed attention launches on each of the five synthetic configurations; 0 skips them")
+    ap.add_argument("--fp32-steps", type=int, default=10,
+                    help="timed float32 launches at B1 H16 S4096 (D = 64, 128); 0 skips them")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling a smaller case)")
@@ -372,6 +374,57 @@ def kernel_option_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flush,
 
 # fp32 FMA on the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (maximum SM clock)
 FP32_CUDA_CORE_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# TF32 dense tensor rate relative to bf16 (NVIDIA's nominal figures: 1.1 of 2.25 PFLOP/s per GPU)
+TF32_OVER_BF16 = 1.1 / 2.25
+
+
+def fp32_scale_timings(fa, torch, device_index: int, steps: int, peaks: dict) -> dict | None:
+    """The float32 path (split TF32 on tcgen05) at a size where it is throughput-bound.
+
+    The five synthetic configurations hold one float32 case, small enough for
+    the oracle; this one is the same kind (causal, identity score) at
+    B1 H16 S4096, D = 64 and 128.  Each product takes three TF32 MMAs, so the
+    tensor cores execute 3x the algorithmic FLOPs; the roofline peak is the
+    measured bf16 burst scaled by NVIDIA's nominal TF32 / bf16 ratio.
+    """
+    if steps <= 0:
+        return None
+    stream = torch.cuda.current_stream()
+    tf32_peak = peaks["bf16"] * TF32_OVER_BF16
+    res = {"peak_tf32_tflops": tf32_peak,
+           "peak_source": f"{peaks['source']} bf16 burst x {TF32_OVER_BF16:.4f} (nominal TF32 / bf16: 1.1 / 2.25)"}
+    for D in (64, 128):
+        w = W.scaled(W.FP32_CAUSAL_S256, name=f"fp32_causal_b1h16s4096d{D}", H=16, S=4096, D=D)
+        _, (dq, dk, dv, _) = prepare_device_inputs(torch, w)
+        out = torch.empty_like(dq)
+        lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device="cuda")
+        bm = fa.flex_block_mask_create(w.mask, w.B, w.H, w.S, w.S, 128, stream=stream)
+        flops = unmasked_block_flops(w, bm.as_numpy())
+
+        def launch():
+            fa.flex_attention_fwd(dq, dk, dv, bm, w.score, w.score_param, w.scale, out=out, lse=lse, stream=stream)
+
+        for _ in range(3):
+            launch()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        with ClockSampler(device_index) as clocks:
+            for a, b in ev:
+                a.record(stream)
+                launch()
+                b.record(stream)
+            torch.cuda.synchronize()
+        if fa.flex_device_status() != fa.FLEX_OK:
+            raise RuntimeError(f"device status reported a timeout on {w.name}")
+        ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+        achieved = flops / (ms * 1e-3) / 1e12
+        res[w.name] = {"ms_per_launch": ms, "unmasked_block_flops": flops, "tflops": achieved,
+                       "executed_mma_tflops": 3.0 * achieved, "frac_of_tf32_peak": 3.0 * achieved / tf32_peak,
+                       "l2": "K and V (64 MB at D = 128) stay in L2 across launches", "launches": steps,
+                       "clocks": clocks.summary()}
+        del dq, dk, dv, out, lse, bm
+        torch.cuda.empty_cache()
+    return res
 
 
 def backward_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flops_fwd, steps, peaks):
@@ -555,6 +608,11 @@ def run_ours(args, w: W.Workload) -> None:
         cpu = oracle_rows_baseline(w, q, k, v, docs, bm_host, budget_s=args.cpu_seconds)
     # the backward pass last: an error there is reported in its own field
     # and leaves the forward's numbers above as measured
+    fp32_scale = None
+    try:
+        fp32_scale = fp32_scale_timings(fa, torch, local, args.fp32_steps, peaks)
+    except Exception as exc:  # noqa: BLE001
+        fp32_scale = {"error": f"{type(exc).__name__}: {exc}"}
     backward = None
     try:
         backward = backward_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flops, args.backward_steps,
@@ -575,7 +633,8 @@ def run_ours(args, w: W.Workload) -> None:
             "attn_ms_per_launch": {"mean": attn_mean_ms, "median": float(np.median(attn_ms)),
                                    "min": float(np.min(attn_ms))},
             "block_mask_ms_per_launch": float(np.mean(np.asarray(step_ms) - np.asarray(attn_ms))),
-            "kernel_options": options, "backward": backward, "configs": configs}
+            "kernel_options": options, "backward": backward, "configs": configs,
+            "fp32_at_scale": fp32_scale}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
