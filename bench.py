@@ -322,7 +322,7 @@ def config_timings(fa, torch, device_index: int, steps: int, peaks: dict) -> dic
                        "attn_ms_median": float(np.median(ms)), "tflops": tflops,
                        "frac_of_measured_bf16_peak": tflops / peaks["bf16"],
                        "frac_of_spec_bf16_peak": tflops / SPEC_BF16_TFLOPS,
-                       "kernel": "attn_bf16_kernel" if w.dtype == "bf16" else "attn_tf32_kernel (split TF32, tcgen05)",
+                       "kernel": "attn_bf16_kernel" if w.dtype == "bf16" else "attn_fp32_kernel (three-way bf16 split, tcgen05)",
                        "l2": "flushed before each launch" if small else "inputs larger than L2",
                        "launches": steps, "clocks": clocks.summary()}
         del dq, dk, dv, dd, out, lse, bm
@@ -594,7 +594,7 @@ def run_ours(args, w: W.Workload) -> None:
     traffic = recorded_traffic(w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
                 "frac": achieved / peaks["bf16"], "traffic": traffic,
-                "kernel": "attn_bf16_kernel" if w.dtype == "bf16" else "attn_tf32_kernel",
+                "kernel": "attn_bf16_kernel" if w.dtype == "bf16" else "attn_fp32_kernel",
                 "peak_source": f"{peaks['source']} bf16 burst (dense cuBLAS)",
                 "achieved_hbm_gbs": None if traffic is None else traffic / (attn_mean_ms * 1e-3) / 1e9,
                 "algorithmic_flops_per_launch": flops, "mean_launch_ms": attn_mean_ms}

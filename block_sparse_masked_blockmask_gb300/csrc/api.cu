@@ -118,7 +118,7 @@ int prepare_attention(const flex_tensor *q, const flex_tensor *k, const flex_ten
 }
 
 cudaError_t launch_attention(const AttnProblem &p, int dtype, cudaStream_t s) {
-    return dtype == FLEX_DTYPE_BF16 ? launch_attn_bf16(p, s) : launch_attn_tf32(p, s);
+    return dtype == FLEX_DTYPE_BF16 ? launch_attn_bf16(p, s) : launch_attn_fp32(p, s);
 }
 
 }  // namespace

@@ -1,0 +1,572 @@
+// Block-sparse attention forward for float32 inputs on sm_103a tensor cores,
+// with the float32 accuracy of the inputs kept by a three-way bf16 split
+// (six bf16 MMAs per product).
+//
+// What it computes is the flex_attention op of "[Inductor][Flex Attention]
+// Add Subtiling Option for Alpha Scaling" (PyTorch PR #167356) with
+// OUTPUT_LOGSUMEXP, as on the bf16 path: s = score_mod(scale * q.k) on every
+// listed tile, -inf where mask_mod is false (partial tiles only), online
+// softmax (the forward_block_mn step: running max m, running sum
+// l = l * alpha + sum(p), acc = acc * alpha + p V), out = acc / l,
+// lse = m + ln l; a row with no unmasked score gets out = 0, lse = -inf.
+//
+// Three-way split: every float32 operand x is written as x1 + x2 + x3 with
+// x1 = bf16(x), x2 = bf16(x - x1), x3 = bf16(x - x1 - x2) (round to nearest;
+// both differences are exact in float32), which leaves |x - x1 - x2 - x3|
+// below about 2^-27 |x|.  A product a.b is then accumulated in float32 in
+// tensor memory as
+//   a1 b1 + a1 b2 + a2 b1 + a1 b3 + a2 b2 + a3 b1,
+// the dropped terms a2 b3, a3 b2, a3 b3 being below 2^-23 |a| |b|: float32
+// accuracy on the tcgen05 kind::f16 datapath.  A bf16 MMA does twice the
+// work of a TF32 MMA of the same shape, so six of them cost what three
+// split-TF32 MMAs cost; the bf16 parts take half the on-chip space, which
+// lets S be computed 64 kv columns at a time and double-buffered (an MMA
+// issue costs ~50 cycles whatever its width up to N = 64, so narrow S MMAs
+// leave the tensor cores idle).
+//
+// Design (one CTA per (batch, head, 128-row q tile), 416 threads):
+//   warps 0-3   softmax, one thread per q row (TMEM lane = row); at the start
+//               they read their Q rows, split them and write Q1, Q2, Q3
+//               (bf16 pairs) into tensor memory, where the S MMAs read them
+//               as the A operand
+//   warps 4-7   K producers: read each chunk of 64 kv rows of K from global
+//               memory, split it and write the three parts into a
+//               shared-memory ring (rows of 64 bf16 per 128-byte swizzled
+//               atom, as a TMA load with 128-byte swizzle writes them); the
+//               loads of a chunk are issued before its slot is waited for
+//   warps 8-11  V producers: the same for V, in the same row layout, which
+//               the PV MMAs read as an MN-major B operand (no transpose)
+//   warp 12     one thread issues every tcgen05.mma
+// Tensor memory (512 columns): Q1 | Q2 | Q3 | O | S0 | P3_0 | S1 | P3_1.
+// S of chunk u + 1 is computed while the softmax works on chunk u; P1 and
+// P2 (bf16 pairs) overwrite their S in place, P3 has its own columns.  The
+// MMA thread issues PV(u) and then S(u + 2).  The softmax keeps a reference
+// maximum m and rescales O and l only when a chunk's maximum exceeds m by
+// more than kF32RescaleNats (then waiting for PV(u - 1)); out = O / l and
+// lse = m + ln l do not depend on which m was used.  The kv tiles of the
+// BlockMask (any block sizes, read as 128-tiles) are walked in chunks of 64
+// kv rows.  CTAs take q tiles longest first.  Every wait is bounded; on
+// timeout the CTA records FLEX_ERR_DEVICE_TIMEOUT in the status word, drains
+// its MMAs, frees TMEM and exits.
+#include <cfloat>
+
+#include "flex_internal.h"
+#include "ptx.cuh"
+#include "tilelist.cuh"
+
+namespace flex {
+namespace {
+
+constexpr int kF32KWarp = 4;   // first of the four K producer warps
+constexpr int kF32VWarp = 8;   // first of the four V producer warps
+constexpr int kF32MmaWarp = 12;
+constexpr int kF32Threads = 13 * 32;
+constexpr uint32_t kF32TmemCols = 512;
+constexpr int kF32KS = 64;                // kv rows per chunk
+constexpr float kF32RescaleNats = 8.0f;   // O and l are rescaled when the maximum grows by more
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct F32Cfg {
+    static_assert(D == 64 || D == 128, "head dim");
+    static constexpr int KS = kF32KS;
+    static constexpr int kSub = kBlock / KS;               // chunks per 128-tile
+    static constexpr int kSlots = D == 128 ? 2 : 3;        // ring depth, K and V alike
+    static constexpr int kUnits = KS * D / 8 / 128;        // 8-float units per producer thread per chunk
+    static constexpr uint32_t kAtom = KS * 128;            // 64 bf16 of a row, all KS rows
+    static constexpr uint32_t kPart = KS * D * 2;          // one bf16 part of a chunk
+    static constexpr uint32_t kSlot = 3 * kPart;           // parts 1 | 2 | 3
+    static constexpr uint32_t kK0 = 0, kV0 = kSlots * kSlot;
+    static constexpr uint32_t kMiscOff = 2 * kSlots * kSlot;
+    // tensor memory columns (a column holds a bf16 pair of an A operand)
+    __host__ __device__ static constexpr uint32_t q_col(int j) { return (uint32_t)(j * D / 2); }
+    static constexpr uint32_t kO = 3 * D / 2;
+    __host__ __device__ static constexpr uint32_t s_col(int i) { return 5 * D / 2 + (uint32_t)i * (KS + KS / 2); }
+    __host__ __device__ static constexpr uint32_t p_col(int i, int j) {
+        return j < 2 ? s_col(i) + (uint32_t)j * (KS / 2) : s_col(i) + KS;
+    }
+    static_assert(5 * D / 2 + 3 * KS <= (int)kF32TmemCols, "tensor memory");
+    static_assert(kMiscOff % 1024 == 0, "ring alignment");
+};
+
+struct F32Misc {
+    uint64_t q_ready, k_full[3], k_empty[3], v_full[3], v_empty[3];
+    uint64_t s_full[2], p_full[2], pv_done, o_full, drain;
+    uint32_t tmem_base;
+    int abort;
+    int n;  // 128-tiles listed for this q tile
+    int pad;
+    alignas(16) uint32_t flags[kMaxKvBlocks];  // listed / full count per kv tile (tilelist.cuh)
+    alignas(16) uint32_t list[kMaxKvBlocks];   // kv tile | full << 16, ascending
+};
+
+template <int D>
+constexpr size_t f32_smem_bytes() {
+    return F32Cfg<D>::kMiscOff + sizeof(F32Misc) + 1024;
+}
+
+// Offset of 16-byte chunk c (8 bf16) of row r in a row-major tile with
+// 128-byte swizzled rows: atoms of 64 bf16 along the row, each atom all rows
+// x 128 bytes; 8-row groups 1024 bytes apart; the chunk index XORed with the
+// row's index within its 8-row group.
+__device__ __forceinline__ uint32_t sw128_chunk(int r, int c, uint32_t atom_bytes) {
+    return (uint32_t)(c / 8) * atom_bytes + (uint32_t)(r / 8) * 1024u + (uint32_t)(r % 8) * 128u +
+           (uint32_t)(((c % 8) ^ (r % 8)) * 16);
+}
+
+__device__ __forceinline__ float bf16lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi_f(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// The three bf16 parts of two floats, as packed pairs (a in bits 0-15).
+__device__ __forceinline__ void split3(float a, float b, uint32_t &w1, uint32_t &w2, uint32_t &w3) {
+    w1 = pack_bf16x2(a, b);
+    const float ra = a - bf16lo_f(w1), rb = b - bf16hi_f(w1);
+    w2 = pack_bf16x2(ra, rb);
+    w3 = pack_bf16x2(ra - bf16lo_f(w2), rb - bf16hi_f(w2));
+}
+
+__device__ __forceinline__ float f4_at(const float4 &v, int e) {
+    return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ void f32_fail(F32Misc &ms, int *status) {
+    *reinterpret_cast<volatile int *>(&ms.abort) = 1;
+    atomicCAS(status, 0, kDeviceTimeout);
+}
+
+// A wait taken by all 32 lanes of a warp, with one outcome for the warp.
+__device__ __forceinline__ bool f32_warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        const int stop = (*abort != 0) || (global_timer_ns() - t0 > kWaitLimitNs);
+        if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+}
+
+__device__ __forceinline__ void f32_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Each thread of the warp writes 8 consecutive 32-bit columns of its own lane.
+__device__ __forceinline__ void f32_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+// One producer group (four warps, thread lt in 0..127): each chunk of KS kv
+// rows of a [.., kv, D] float32 tensor is split and written, part j at
+// slot + j * kPart, in 128-byte swizzled rows.  Thread lt takes units
+// i = lt + 128 u (row i / (D/8), 8 floats at column 8 (i % (D/8))): a warp's
+// loads are whole rows, a quarter warp's stores hit eight distinct 16-byte
+// bank groups.
+template <int D>
+__device__ __forceinline__ bool f32_produce(F32Misc &ms, uint8_t *ring, uint64_t *full, uint64_t *empty,
+                                            const float *base, int64_t row_stride, int kv_len, int nsub, int lt,
+                                            int lane, volatile int *abort_flag) {
+    using C = F32Cfg<D>;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < nsub; ++u) {
+        const int kv0 = (int)(ms.list[u / C::kSub] & 0xFFFFu) * kBlock + (u % C::kSub) * C::KS;
+        float4 x[2 * C::kUnits];
+#pragma unroll
+        for (int j = 0; j < C::kUnits; ++j) {
+            const int i = lt + 128 * j, r = i / (D / 8), c = i % (D / 8);
+            const float4 *src = reinterpret_cast<const float4 *>(base + (int64_t)(kv0 + r) * row_stride) + 2 * c;
+            const bool in = kv0 + r < kv_len;
+            x[2 * j] = in ? __ldg(src) : zero;
+            x[2 * j + 1] = in ? __ldg(src + 1) : zero;
+        }
+        const int s = u % C::kSlots;
+        const uint32_t use = (uint32_t)(u / C::kSlots);
+        if (use > 0 && !f32_warp_wait(&empty[s], (use - 1) & 1u, abort_flag)) return false;
+        uint8_t *slot = ring + s * C::kSlot;
+#pragma unroll
+        for (int j = 0; j < C::kUnits; ++j) {
+            const int i = lt + 128 * j, r = i / (D / 8), c = i % (D / 8);
+            uint4 p1, p2, p3;
+            split3(x[2 * j].x, x[2 * j].y, p1.x, p2.x, p3.x);
+            split3(x[2 * j].z, x[2 * j].w, p1.y, p2.y, p3.y);
+            split3(x[2 * j + 1].x, x[2 * j + 1].y, p1.z, p2.z, p3.z);
+            split3(x[2 * j + 1].z, x[2 * j + 1].w, p1.w, p2.w, p3.w);
+            const uint32_t off = sw128_chunk(r, c, C::kAtom);
+            *reinterpret_cast<uint4 *>(slot + off) = p1;
+            *reinterpret_cast<uint4 *>(slot + C::kPart + off) = p2;
+            *reinterpret_cast<uint4 *>(slot + 2 * C::kPart + off) = p3;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+    }
+    return true;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kF32Threads, 1) attn_fp32_kernel(AttnProblem p, int bh_major) {
+    using C = F32Cfg<D>;
+    constexpr int KS = C::KS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    F32Misc &ms = *reinterpret_cast<F32Misc *>(smem + C::kMiscOff);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // longest first: under a causal mask the last q tiles list the most kv tiles
+    const int qt = p.nqt - 1 - (int)(bh_major ? blockIdx.y : blockIdx.x);
+    const int bh = p.bh_begin + (int)(bh_major ? blockIdx.x : blockIdx.y), h = bh % p.H, b = bh / p.H;
+    const int q0 = qt * kBlock;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&ms.q_ready, 4);
+        for (int s = 0; s < C::kSlots; ++s) {
+            mbar_init(&ms.k_full[s], 4);
+            mbar_init(&ms.k_empty[s], 1);
+            mbar_init(&ms.v_full[s], 4);
+            mbar_init(&ms.v_empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ms.s_full[i], 1);
+            mbar_init(&ms.p_full[i], 4);
+        }
+        mbar_init(&ms.pv_done, 1);
+        mbar_init(&ms.o_full, 1);
+        mbar_init(&ms.drain, 1);
+        ms.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        // the kv tiles of this q tile: the BlockMask's lists (any block sizes)
+        // read as 128-tiles; counts clamped and malformed entries dropped
+        const TileLists lists{p.kv_num, p.kv_idx, p.full_num, p.full_idx, p.nqb, p.nkvb, p.q_block, p.kv_block,
+                              p.nkvt};
+        for (int i = lane; i < p.nkvt; i += 32) ms.flags[i] = 0u;
+        __syncwarp();
+        tl_mark_warp(lists, bh, qt, 0, ms.flags, 0, p.nkvt, lane);
+        __syncwarp();
+        const uint32_t expect = tl_expect(lists);
+        const unsigned lt = (1u << lane) - 1u;
+        int cnt = 0;
+        for (int base = 0; base < p.nkvt; base += 32) {
+            const int i = base + lane;
+            const uint32_t w = i < p.nkvt ? ms.flags[i] : 0u;
+            const bool on = tl_listed(w, 0);
+            const unsigned bal = __ballot_sync(0xffffffffu, on);
+            if (on) ms.list[cnt + __popc(bal & lt)] = (uint32_t)i | (tl_full(expect, w, 0) ? (1u << 16) : 0u);
+            cnt += __popc(bal);
+        }
+        if (lane == 0) ms.n = cnt;
+    }
+    if (warp == kF32MmaWarp) {
+        tmem_alloc(&ms.tmem_base, kF32TmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = ms.tmem_base;
+    volatile int *abort_flag = &ms.abort;
+    const int nsub = ms.n * C::kSub;  // kv chunks
+
+    if (warp >= kF32KWarp && warp < kF32KWarp + 4) {
+        // --------------------------------------------------------- K producers
+        const float *kbase = static_cast<const float *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
+        if (!f32_produce<D>(ms, smem + C::kK0, ms.k_full, ms.k_empty, kbase, p.k_stride[2], p.kv_len, nsub,
+                            threadIdx.x - 32 * kF32KWarp, lane, abort_flag))
+            f32_fail(ms, p.status);
+    } else if (warp >= kF32VWarp && warp < kF32VWarp + 4) {
+        // --------------------------------------------------------- V producers
+        const float *vbase = static_cast<const float *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1];
+        if (!f32_produce<D>(ms, smem + C::kV0, ms.v_full, ms.v_empty, vbase, p.v_stride[2], p.kv_len, nsub,
+                            threadIdx.x - 32 * kF32VWarp, lane, abort_flag))
+            f32_fail(ms, p.status);
+    } else if (warp == kF32MmaWarp) {
+        // ---------------------------------------------------------------- MMA
+        if (lane == 0 && nsub > 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(128, KS, 0, 0);
+            constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
+            constexpr uint32_t kHi = smem_desc_hi_sw128(1024);
+            // the six part products t, first the largest: (A part, B part) =
+            // (0,0) (0,1) (1,0) (0,2) (1,1) (2,0)
+            auto pa = [](int t) { return t == 2 || t == 4 ? 1 : t == 5 ? 2 : 0; };
+            auto pbp = [](int t) { return t == 1 || t == 4 ? 1 : t == 3 ? 2 : 0; };
+            // S(j) = sum of the part products Q_a K_b^T into S buffer j % 2;
+            // K is K-major (K steps of 16 bf16 = 32 bytes within a 64-wide atom)
+            auto issue_s = [&](int j) -> bool {
+                const int s = j % C::kSlots;
+                if (!mbar_wait(&ms.k_full[s], (uint32_t)(j / C::kSlots) & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+                const uint32_t kd = smem_desc_lo(smem_u32(smem + C::kK0 + s * C::kSlot), 16);
+                const uint32_t d = tmem + C::s_col(j & 1);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = ((k / 4) * C::kAtom + (k % 4) * 32) >> 4;
+#pragma unroll
+                    for (int t = 0; t < 6; ++t)
+                        mma_ts_lo<kHi>(d, tmem + C::q_col(pa(t)) + 8 * k, kd + ((pbp(t) * C::kPart) >> 4) + off,
+                                       idesc_s, (k > 0 || t > 0) ? 1u : 0u);
+                }
+                mma_commit(&ms.k_empty[s]);
+                mma_commit(&ms.s_full[j & 1]);
+                return true;
+            };
+            bool ok = mbar_wait(&ms.q_ready, 0, abort_flag);
+            if (ok) {
+                tc_fence_after_sync();
+                ok = issue_s(0);
+            }
+            if (ok && nsub > 1) ok = issue_s(1);
+            for (int u = 0; ok && u < nsub; ++u) {
+                const int pb = u & 1, s = u % C::kSlots;
+                if (!mbar_wait(&ms.p_full[pb], (uint32_t)(u >> 1) & 1u, abort_flag) ||
+                    !mbar_wait(&ms.v_full[s], (uint32_t)(u / C::kSlots) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                // O += sum of the part products P_a V_b; V is MN-major (kv rows
+                // of 64 head-dim elements, the 64-wide halves kAtom apart),
+                // K steps of 16 kv rows = 2048 bytes
+                const uint32_t vd = smem_desc_lo(smem_u32(smem + C::kV0 + s * C::kSlot), C::kAtom);
+#pragma unroll
+                for (int k = 0; k < KS / 16; ++k) {
+#pragma unroll
+                    for (int t = 0; t < 6; ++t)
+                        mma_ts_lo<kHi>(tmem + C::kO, tmem + C::p_col(pb, pa(t)) + 8 * k,
+                                       vd + ((pbp(t) * C::kPart + k * 2048) >> 4), idesc_o,
+                                       (u > 0 || k > 0 || t > 0) ? 1u : 0u);
+                }
+                mma_commit(&ms.v_empty[s]);
+                mma_commit(&ms.pv_done);
+                // S(u + 2) reuses the buffer PV(u) reads: MMAs of one thread run in order
+                if (u + 2 < nsub && !issue_s(u + 2)) ok = false;
+            }
+            if (ok) mma_commit(&ms.o_full);
+            if (!ok) f32_fail(ms, p.status);
+            mma_commit(&ms.drain);  // every MMA issued above completes before TMEM is freed
+            int never = 0;
+            (void)mbar_wait(&ms.drain, 0, &never);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ softmax
+        const int t = threadIdx.x;
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        const int q = q0 + t;
+        const bool row_in = q < p.q_len;
+        const float post = p.prescale ? 1.f : p.scale;
+        const float slope = exp2f(-8.f * (float)(h + 1) / (float)p.H);
+        int doc_q = 0;
+        if (p.mask.kind == FLEX_MASK_DOCUMENT && row_in) doc_q = p.mask.doc_ids[(int64_t)b * p.mask.doc_len + q];
+        int lo = 0, hi = -1;  // the kept kv interval of an interval mask_mod
+        if (p.mask.kind != FLEX_MASK_DOCUMENT && row_in) {
+            mask_row_interval(p.mask, q, lo, hi);
+            hi = min(hi, p.kv_len - 1);
+        }
+        bool ok = true;
+        if (nsub > 0) {
+            // Q row -> Q1, Q2, Q3 columns of this lane (bf16 pairs);
+            // PRESCALE_QK multiplies by scale first (one rounding)
+            const float *qrow = static_cast<const float *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1] +
+                                (int64_t)(row_in ? q : 0) * p.q_stride[2];
+            const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {  // 8 loads in flight, then 16 columns of each part
+                float4 x[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    x[j] = row_in ? __ldg(reinterpret_cast<const float4 *>(qrow + c0) + j) : zero;
+                uint32_t w1[16], w2[16], w3[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    float a = f4_at(x[j / 2], 2 * (j % 2)), c = f4_at(x[j / 2], 2 * (j % 2) + 1);
+                    if (p.prescale) {
+                        a = __fmul_rn(a, p.scale);
+                        c = __fmul_rn(c, p.scale);
+                    }
+                    split3(a, c, w1[j], w2[j], w3[j]);
+                }
+                const uint32_t col = (uint32_t)c0 / 2;
+                tmem_st16(trow + C::q_col(0) + col, w1);
+                tmem_st16(trow + C::q_col(1) + col, w2);
+                tmem_st16(trow + C::q_col(2) + col, w3);
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.q_ready);
+        }
+        float m = -INFINITY, m_true = -INFINITY, l = 0.f;
+        for (int u = 0; u < nsub; ++u) {
+            const int pb = u & 1;
+            const uint32_t e = ms.list[u / C::kSub];
+            const bool full = (e >> 16) & 1u;
+            const int kv0 = (int)(e & 0xFFFFu) * kBlock + (u % C::kSub) * KS;
+            if (!f32_warp_wait(&ms.s_full[pb], (uint32_t)(u >> 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            float x[KS];
+#pragma unroll
+            for (int c0 = 0; c0 < KS; c0 += 32) {
+                uint32_t r[32];
+                f32_ld32(trow + C::s_col(pb) + c0, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int kv = kv0 + c0 + j;
+                    float s = __uint_as_float(r[j]) * post;
+                    if (p.score_kind == FLEX_SCORE_SOFTCAP) s = p.score_param * tanhf(s / p.score_param);
+                    else if (p.score_kind == FLEX_SCORE_ALIBI) s -= slope * (float)(q - kv);
+                    if (!full) {
+                        bool keep;
+                        if (p.mask.kind == FLEX_MASK_DOCUMENT)
+                            keep = row_in && kv <= q && kv < p.kv_len &&
+                                   p.mask.doc_ids[(int64_t)b * p.mask.doc_len + kv] == doc_q;
+                        else
+                            keep = kv >= lo && kv <= hi;
+                        if (!keep) s = -INFINITY;
+                    }
+                    x[c0 + j] = s;
+                }
+            }
+            float mt = x[0];
+#pragma unroll
+            for (int j = 1; j < KS; ++j) mt = fmaxf(mt, x[j]);
+            m_true = fmaxf(m_true, mt);
+            // the reference maximum moves only when this chunk's exceeds it by
+            // more than kF32RescaleNats (so p <= e^8); from -inf it moves to
+            // the first finite maximum
+            const bool grow = mt > m + kF32RescaleNats;
+            if (__any_sync(0xffffffffu, grow)) {
+                const float m_new = grow ? mt : m;
+                const float alpha = grow ? expf(m - m_new) : 1.f;  // 0 when m was -inf
+                if (u > 0) {
+                    // PV(u - 1) has completed before O is rescaled in place
+                    if (!f32_warp_wait(&ms.pv_done, (uint32_t)(u - 1) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        f32_ld32(trow + C::kO + c0, o);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+                        tmem_st32(trow + C::kO + c0, o);
+                    }
+                }
+                l *= alpha;
+                m = m_new;
+            }
+            // p = e^(s - m) = 2^(s log2 e - m log2 e); a row with m = -inf has
+            // every s = -inf and gets p = 2^-inf = 0
+            const float mb = m == -INFINITY ? 0.f : m * kLog2e;
+            float sum = 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < KS; c0 += 16) {  // 16 columns at a time: x is consumed as P is stored
+                uint32_t w1[8], w2[8], w3[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float pa = ex2_approx(fmaf(x[c0 + 2 * j], kLog2e, -mb));
+                    const float pc = ex2_approx(fmaf(x[c0 + 2 * j + 1], kLog2e, -mb));
+                    sum += pa + pc;
+                    split3(pa, pc, w1[j], w2[j], w3[j]);
+                }
+                const uint32_t col = (uint32_t)c0 / 2;
+                f32_st8(trow + C::p_col(pb, 0) + col, w1);  // over S columns, all read above
+                f32_st8(trow + C::p_col(pb, 1) + col, w2);
+                f32_st8(trow + C::p_col(pb, 2) + col, w3);
+            }
+            l += sum;
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.p_full[pb]);
+        }
+        // ------------------------------------------------------------ epilogue
+        bool have = ok && nsub > 0;
+        if (have && !f32_warp_wait(&ms.o_full, 0, abort_flag)) {
+            have = false;
+            ok = false;
+        }
+        if (!ok) f32_fail(ms, p.status);
+        if (ok) {
+            tc_fence_after_sync();
+            const int64_t orow = (int64_t)bh * p.q_len + (row_in ? q : 0);
+            float *op = static_cast<float *>(p.out) + orow * D;
+            const bool live = have && l > 0.f;
+            const float inv = live ? 1.f / l : 0.f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {  // every lane takes the warp-collective loads
+                uint32_t o[32];
+                if (have) {
+                    f32_ld32(trow + C::kO + c0, o);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = 0u;
+                }
+                if (row_in) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(op + c0 + j) =
+                            make_float4(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv,
+                                        __uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
+                }
+            }
+            if (row_in) {
+                p.lse[orow] = live ? m + logf(l) : -INFINITY;
+                if (p.row_max) p.row_max[orow] = live ? m_true : -INFINITY;
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kF32MmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kF32TmemCols);
+    }
+}
+
+template <int D>
+cudaError_t launch_fp32_d(const AttnProblem &p, cudaStream_t stream) {
+    const size_t smem = f32_smem_bytes<D>();
+    cudaError_t e = cudaFuncSetAttribute(attn_fp32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (p.nqt <= 65535) {
+        // (b, h) pairs along x, q tiles (longest first) along y: the first
+        // CTAs to run are the longest of every pair
+        attn_fp32_kernel<D><<<dim3(p.bh_count, p.nqt), kF32Threads, smem, stream>>>(p, 1);
+        return cudaGetLastError();
+    }
+    // grid.y holds at most 65535 (b, h) pairs per launch
+    for (int begin = 0; begin < p.bh_count; begin += 65535) {
+        AttnProblem part = p;
+        part.bh_begin = p.bh_begin + begin;
+        part.bh_count = p.bh_count - begin < 65535 ? p.bh_count - begin : 65535;
+        attn_fp32_kernel<D><<<dim3(p.nqt, part.bh_count), kF32Threads, smem, stream>>>(part, 0);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fp32(const AttnProblem &p, cudaStream_t stream) {
+    return p.D == 64 ? launch_fp32_d<64>(p, stream) : launch_fp32_d<128>(p, stream);
+}
+
+}  // namespace flex

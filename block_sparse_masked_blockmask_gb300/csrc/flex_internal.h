@@ -99,7 +99,7 @@ struct AttnProblem {
 cudaError_t launch_block_mask(const MaskDesc &mask, int B, int H, int q_len, int kv_len, int q_block, int kv_block,
                               int32_t *kv_num, int32_t *kv_idx, int32_t *full_num, int32_t *full_idx,
                               cudaStream_t stream);
-cudaError_t launch_attn_tf32(const AttnProblem &p, cudaStream_t stream);
+cudaError_t launch_attn_fp32(const AttnProblem &p, cudaStream_t stream);
 cudaError_t launch_attn_bf16(const AttnProblem &p, cudaStream_t stream);
 
 // TMA tensor map of a bf16 [B, H, S, D] tensor with element strides st

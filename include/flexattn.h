@@ -93,7 +93,7 @@ typedef enum {
 
 typedef enum {
     FLEX_DTYPE_BF16 = 0,           /* bfloat16 storage; tensor-core path, fp32 accumulation */
-    FLEX_DTYPE_FP32 = 1            /* float32 storage; CUDA-core fp32 path                  */
+    FLEX_DTYPE_FP32 = 1            /* float32 storage; float32-accurate tensor-core forward */
 } flex_dtype;
 
 /* Parameters of a mask_mod.  Unused fields are ignored for kinds that do not need them. */
