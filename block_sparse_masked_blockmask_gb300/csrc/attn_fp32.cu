@@ -172,9 +172,9 @@ __device__ __forceinline__ void f32_st8(uint32_t taddr, const uint32_t (&r)[8]) 
 // slot + j * kPart, in 128-byte swizzled rows.  Thread lt takes units
 // i = lt + 128 u (row i / (D/8), 8 floats at column 8 (i % (D/8))): a warp's
 // loads are whole rows, a quarter warp's stores hit eight distinct 16-byte
-// bank groups.
+// bank groups.  Not inlined: the K and V groups run one copy of the code.
 template <int D>
-__device__ __forceinline__ bool f32_produce(F32Misc &ms, uint8_t *ring, uint64_t *full, uint64_t *empty,
+__device__ __noinline__ bool f32_produce(F32Misc &ms, uint8_t *ring, uint64_t *full, uint64_t *empty,
                                             const float *base, int64_t row_stride, int kv_len, int nsub, int lt,
                                             int lane, volatile int *abort_flag) {
     using C = F32Cfg<D>;
@@ -214,7 +214,7 @@ __device__ __forceinline__ bool f32_produce(F32Misc &ms, uint8_t *ring, uint64_t
     return true;
 }
 
-template <int D>
+template <int D, int SCORE, bool DOC>
 __global__ void __launch_bounds__(kF32Threads, 1) attn_fp32_kernel(AttnProblem p, int bh_major) {
     using C = F32Cfg<D>;
     constexpr int KS = C::KS;
@@ -365,11 +365,11 @@ __global__ void __launch_bounds__(kF32Threads, 1) attn_fp32_kernel(AttnProblem p
         const int q = q0 + t;
         const bool row_in = q < p.q_len;
         const float post = p.prescale ? 1.f : p.scale;
-        const float slope = exp2f(-8.f * (float)(h + 1) / (float)p.H);
+        const float slope = SCORE == FLEX_SCORE_ALIBI ? exp2f(-8.f * (float)(h + 1) / (float)p.H) : 0.f;
         int doc_q = 0;
-        if (p.mask.kind == FLEX_MASK_DOCUMENT && row_in) doc_q = p.mask.doc_ids[(int64_t)b * p.mask.doc_len + q];
+        if (DOC && row_in) doc_q = p.mask.doc_ids[(int64_t)b * p.mask.doc_len + q];
         int lo = 0, hi = -1;  // the kept kv interval of an interval mask_mod
-        if (p.mask.kind != FLEX_MASK_DOCUMENT && row_in) {
+        if (!DOC && row_in) {
             mask_row_interval(p.mask, q, lo, hi);
             hi = min(hi, p.kv_len - 1);
         }
@@ -426,11 +426,11 @@ __global__ void __launch_bounds__(kF32Threads, 1) attn_fp32_kernel(AttnProblem p
                 for (int j = 0; j < 32; ++j) {
                     const int kv = kv0 + c0 + j;
                     float s = __uint_as_float(r[j]) * post;
-                    if (p.score_kind == FLEX_SCORE_SOFTCAP) s = p.score_param * tanhf(s / p.score_param);
-                    else if (p.score_kind == FLEX_SCORE_ALIBI) s -= slope * (float)(q - kv);
+                    if constexpr (SCORE == FLEX_SCORE_SOFTCAP) s = p.score_param * tanhf(s / p.score_param);
+                    if constexpr (SCORE == FLEX_SCORE_ALIBI) s -= slope * (float)(q - kv);
                     if (!full) {
                         bool keep;
-                        if (p.mask.kind == FLEX_MASK_DOCUMENT)
+                        if constexpr (DOC)
                             keep = row_in && kv <= q && kv < p.kv_len &&
                                    p.mask.doc_ids[(int64_t)b * p.mask.doc_len + kv] == doc_q;
                         else
@@ -541,15 +541,16 @@ __global__ void __launch_bounds__(kF32Threads, 1) attn_fp32_kernel(AttnProblem p
     }
 }
 
-template <int D>
-cudaError_t launch_fp32_d(const AttnProblem &p, cudaStream_t stream) {
+template <int D, int SCORE, bool DOC>
+cudaError_t launch_fp32_kernel(const AttnProblem &p, cudaStream_t stream) {
     const size_t smem = f32_smem_bytes<D>();
-    cudaError_t e = cudaFuncSetAttribute(attn_fp32_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kern = attn_fp32_kernel<D, SCORE, DOC>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (p.nqt <= 65535) {
         // (b, h) pairs along x, q tiles (longest first) along y: the first
         // CTAs to run are the longest of every pair
-        attn_fp32_kernel<D><<<dim3(p.bh_count, p.nqt), kF32Threads, smem, stream>>>(p, 1);
+        kern<<<dim3(p.bh_count, p.nqt), kF32Threads, smem, stream>>>(p, 1);
         return cudaGetLastError();
     }
     // grid.y holds at most 65535 (b, h) pairs per launch
@@ -557,10 +558,28 @@ cudaError_t launch_fp32_d(const AttnProblem &p, cudaStream_t stream) {
         AttnProblem part = p;
         part.bh_begin = p.bh_begin + begin;
         part.bh_count = p.bh_count - begin < 65535 ? p.bh_count - begin : 65535;
-        attn_fp32_kernel<D><<<dim3(p.nqt, part.bh_count), kF32Threads, smem, stream>>>(part, 0);
+        kern<<<dim3(p.nqt, part.bh_count), kF32Threads, smem, stream>>>(part, 0);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+template <int D, bool DOC>
+cudaError_t launch_fp32_score(const AttnProblem &p, cudaStream_t stream) {
+    switch (p.score_kind) {
+        case FLEX_SCORE_SOFTCAP:
+            return launch_fp32_kernel<D, FLEX_SCORE_SOFTCAP, DOC>(p, stream);
+        case FLEX_SCORE_ALIBI:
+            return launch_fp32_kernel<D, FLEX_SCORE_ALIBI, DOC>(p, stream);
+        default:
+            return launch_fp32_kernel<D, FLEX_SCORE_IDENTITY, DOC>(p, stream);
+    }
+}
+
+template <int D>
+cudaError_t launch_fp32_d(const AttnProblem &p, cudaStream_t stream) {
+    return p.mask.kind == FLEX_MASK_DOCUMENT ? launch_fp32_score<D, true>(p, stream)
+                                             : launch_fp32_score<D, false>(p, stream);
 }
 
 }  // namespace
