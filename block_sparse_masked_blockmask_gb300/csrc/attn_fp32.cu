@@ -24,7 +24,7 @@
 // issue costs ~50 cycles whatever its width up to N = 64, so narrow S MMAs
 // leave the tensor cores idle).
 //
-// Design (one CTA per (batch, head, 128-row q tile), 416 threads):
+// Design (one CTA per (batch, head, 128-row q tile), 448 threads):
 //   warps 0-3   softmax, one thread per q row (TMEM lane = row); at the start
 //               they read their Q rows, split them and write Q1, Q2, Q3
 //               (bf16 pairs) into tensor memory, where the S MMAs read them
@@ -36,11 +36,14 @@
 //               loads of a chunk are issued before its slot is waited for
 //   warps 8-11  V producers: the same for V, in the same row layout, which
 //               the PV MMAs read as an MN-major B operand (no transpose)
-//   warp 12     one thread issues every tcgen05.mma
+//   warp 12     one thread issues the MMAs; at D = 64 the PV MMAs only, and
+//   warp 13     one thread the S MMAs (the fixed ~50-cycle cost of an MMA
+//               issue on one thread overlaps the other's)
 // Tensor memory (512 columns): Q1 | Q2 | Q3 | O | S0 | P3_0 | S1 | P3_1.
 // S of chunk u + 1 is computed while the softmax works on chunk u; P1 and
-// P2 (bf16 pairs) overwrite their S in place, P3 has its own columns.  The
-// MMA thread issues PV(u) and then S(u + 2).  The softmax keeps a reference
+// P2 (bf16 pairs) overwrite their S in place, P3 has its own columns;
+// S(u + 2) is issued after PV(u) (one issuer: right behind it; two: once it
+// has completed).  The softmax keeps a reference
 // maximum m and rescales O and l only when a chunk's maximum exceeds m by
 // more than kF32RescaleNats (then waiting for PV(u - 1)); out = O / l and
 // lse = m + ln l do not depend on which m was used.  The kv tiles of the
@@ -59,8 +62,9 @@ namespace {
 
 constexpr int kF32KWarp = 4;   // first of the four K producer warps
 constexpr int kF32VWarp = 8;   // first of the four V producer warps
-constexpr int kF32MmaWarp = 12;
-constexpr int kF32Threads = 13 * 32;
+constexpr int kF32MmaWarp = 12;  // issues the PV MMAs (and allocates TMEM)
+constexpr int kF32SWarp = 13;    // issues the S MMAs
+constexpr int kF32Threads = 14 * 32;
 constexpr uint32_t kF32TmemCols = 512;
 constexpr int kF32KS = 64;                // kv rows per chunk
 constexpr float kF32RescaleNats = 8.0f;   // O and l are rescaled when the maximum grows by more
@@ -72,6 +76,11 @@ struct F32Cfg {
     static constexpr int KS = kF32KS;
     static constexpr int kSub = kBlock / KS;               // chunks per 128-tile
     static constexpr int kSlots = D == 128 ? 2 : 3;        // ring depth, K and V alike
+    // two MMA issuers at D = 64 (S and PV MMAs, each ~50 cycles of fixed
+    // issue cost at N = 64, overlap); one at D = 128, where PV's N = 128
+    // MMAs keep the tensor pipe busy and S(u + 2) is better issued right
+    // behind PV(u) than after a wait for its completion
+    static constexpr bool kTwoIssuers = D == 64;
     static constexpr int kUnits = KS * D / 8 / 128;        // 8-float units per producer thread per chunk
     static constexpr uint32_t kAtom = KS * 128;            // 64 bf16 of a row, all KS rows
     static constexpr uint32_t kPart = KS * D * 2;          // one bf16 part of a chunk
@@ -91,7 +100,7 @@ struct F32Cfg {
 
 struct F32Misc {
     uint64_t q_ready, k_full[3], k_empty[3], v_full[3], v_empty[3];
-    uint64_t s_full[2], p_full[2], pv_done, o_full, drain;
+    uint64_t s_full[2], p_full[2], pv_done, o_full, drain;  // drain: one commit per issuing thread
     uint32_t tmem_base;
     int abort;
     int n;  // 128-tiles listed for this q tile
@@ -241,7 +250,7 @@ __global__ void __launch_bounds__(kF32Threads, 1) attn_fp32_kernel(AttnProblem p
         }
         mbar_init(&ms.pv_done, 1);
         mbar_init(&ms.o_full, 1);
-        mbar_init(&ms.drain, 1);
+        mbar_init(&ms.drain, C::kTwoIssuers ? 2 : 1);
         ms.abort = 0;
         fence_barrier_init();
     }
@@ -290,12 +299,12 @@ __global__ void __launch_bounds__(kF32Threads, 1) attn_fp32_kernel(AttnProblem p
         if (!f32_produce<D>(ms, smem + C::kV0, ms.v_full, ms.v_empty, vbase, p.v_stride[2], p.kv_len, nsub,
                             threadIdx.x - 32 * kF32VWarp, lane, abort_flag))
             f32_fail(ms, p.status);
-    } else if (warp == kF32MmaWarp) {
+    } else if (warp == kF32SWarp || warp == kF32MmaWarp) {
         // ---------------------------------------------------------------- MMA
-        if (lane == 0 && nsub > 0) {
+        if (lane == 0 && nsub > 0 && (C::kTwoIssuers || warp == kF32MmaWarp)) {
+            constexpr uint32_t kHi = smem_desc_hi_sw128(1024);
             constexpr uint32_t idesc_s = idesc_bf16_f32(128, KS, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
-            constexpr uint32_t kHi = smem_desc_hi_sw128(1024);
             // the six part products t, first the largest: (A part, B part) =
             // (0,0) (0,1) (1,0) (0,2) (1,1) (2,0)
             auto pa = [](int t) { return t == 2 || t == 4 ? 1 : t == 5 ? 2 : 0; };
@@ -320,23 +329,15 @@ __global__ void __launch_bounds__(kF32Threads, 1) attn_fp32_kernel(AttnProblem p
                 mma_commit(&ms.s_full[j & 1]);
                 return true;
             };
-            bool ok = mbar_wait(&ms.q_ready, 0, abort_flag);
-            if (ok) {
-                tc_fence_after_sync();
-                ok = issue_s(0);
-            }
-            if (ok && nsub > 1) ok = issue_s(1);
-            for (int u = 0; ok && u < nsub; ++u) {
+            // O += sum of the part products P_a V_b; V is MN-major (kv rows of
+            // 64 head-dim elements, the 64-wide halves kAtom apart), K steps
+            // of 16 kv rows = 2048 bytes
+            auto issue_pv = [&](int u) -> bool {
                 const int pb = u & 1, s = u % C::kSlots;
                 if (!mbar_wait(&ms.p_full[pb], (uint32_t)(u >> 1) & 1u, abort_flag) ||
-                    !mbar_wait(&ms.v_full[s], (uint32_t)(u / C::kSlots) & 1u, abort_flag)) {
-                    ok = false;
-                    break;
-                }
+                    !mbar_wait(&ms.v_full[s], (uint32_t)(u / C::kSlots) & 1u, abort_flag))
+                    return false;
                 tc_fence_after_sync();
-                // O += sum of the part products P_a V_b; V is MN-major (kv rows
-                // of 64 head-dim elements, the 64-wide halves kAtom apart),
-                // K steps of 16 kv rows = 2048 bytes
                 const uint32_t vd = smem_desc_lo(smem_u32(smem + C::kV0 + s * C::kSlot), C::kAtom);
 #pragma unroll
                 for (int k = 0; k < KS / 16; ++k) {
@@ -348,10 +349,35 @@ __global__ void __launch_bounds__(kF32Threads, 1) attn_fp32_kernel(AttnProblem p
                 }
                 mma_commit(&ms.v_empty[s]);
                 mma_commit(&ms.pv_done);
-                // S(u + 2) reuses the buffer PV(u) reads: MMAs of one thread run in order
-                if (u + 2 < nsub && !issue_s(u + 2)) ok = false;
+                return true;
+            };
+            bool ok = true;
+            if (!C::kTwoIssuers) {
+                // one issuer: S(0), S(1), then PV(u) and S(u + 2) (MMAs of
+                // one thread run in order, so S(u + 2) follows PV(u))
+                ok = mbar_wait(&ms.q_ready, 0, abort_flag);
+                if (ok) {
+                    tc_fence_after_sync();
+                    ok = issue_s(0);
+                }
+                if (ok && nsub > 1) ok = issue_s(1);
+                for (int u = 0; ok && u < nsub; ++u) ok = issue_pv(u) && (u + 2 >= nsub || issue_s(u + 2));
+                if (ok) mma_commit(&ms.o_full);
+            } else if (warp == kF32SWarp) {
+                // S(j) overwrites the buffer PV(j - 2) read its P from
+                ok = mbar_wait(&ms.q_ready, 0, abort_flag);
+                for (int j = 0; ok && j < nsub; ++j) {
+                    if (j >= 2 && !mbar_wait(&ms.pv_done, (uint32_t)(j - 2) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    ok = issue_s(j);
+                }
+            } else {
+                for (int u = 0; ok && u < nsub; ++u) ok = issue_pv(u);
+                if (ok) mma_commit(&ms.o_full);
             }
-            if (ok) mma_commit(&ms.o_full);
             if (!ok) f32_fail(ms, p.status);
             mma_commit(&ms.drain);  // every MMA issued above completes before TMEM is freed
             int never = 0;
