@@ -374,25 +374,25 @@ def kernel_option_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flush,
 
 # fp32 FMA on the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (maximum SM clock)
 FP32_CUDA_CORE_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
-# TF32 dense tensor rate relative to bf16 (NVIDIA's nominal figures: 1.1 of 2.25 PFLOP/s per GPU)
-TF32_OVER_BF16 = 1.1 / 2.25
+# bf16 MMA FLOPs the float32 forward executes per algorithmic FLOP (three-way split, six products)
+FP32_SPLIT_PRODUCTS = 6
 
 
 def fp32_scale_timings(fa, torch, device_index: int, steps: int, peaks: dict) -> dict | None:
-    """The float32 path (split TF32 on tcgen05) at a size where it is throughput-bound.
+    """The float32 path (three-way bf16 split on tcgen05) at a size where it is throughput-bound.
 
     The five synthetic configurations hold one float32 case, small enough for
     the oracle; this one is the same kind (causal, identity score) at
-    B1 H16 S4096, D = 64 and 128.  Each product takes three TF32 MMAs, so the
-    tensor cores execute 3x the algorithmic FLOPs; the roofline peak is the
-    measured bf16 burst scaled by NVIDIA's nominal TF32 / bf16 ratio.
+    B1 H16 S4096, D = 64 and 128.  Each product takes six bf16 MMAs, so the
+    tensor cores execute 6x the algorithmic FLOPs; the ceiling of the
+    algorithmic rate is the measured bf16 burst / 6.
     """
     if steps <= 0:
         return None
     stream = torch.cuda.current_stream()
-    tf32_peak = peaks["bf16"] * TF32_OVER_BF16
-    res = {"peak_tf32_tflops": tf32_peak,
-           "peak_source": f"{peaks['source']} bf16 burst x {TF32_OVER_BF16:.4f} (nominal TF32 / bf16: 1.1 / 2.25)"}
+    ceiling = peaks["bf16"] / FP32_SPLIT_PRODUCTS
+    res = {"kernel": "attn_fp32_kernel (three-way bf16 split, tcgen05)", "ceiling_tflops": ceiling,
+           "ceiling_source": f"{peaks['source']} bf16 burst / {FP32_SPLIT_PRODUCTS} (bf16 MMA FLOPs per FLOP)"}
     for D in (64, 128):
         w = W.scaled(W.FP32_CAUSAL_S256, name=f"fp32_causal_b1h16s4096d{D}", H=16, S=4096, D=D)
         _, (dq, dk, dv, _) = prepare_device_inputs(torch, w)
@@ -419,7 +419,8 @@ def fp32_scale_timings(fa, torch, device_index: int, steps: int, peaks: dict) ->
         ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
         achieved = flops / (ms * 1e-3) / 1e12
         res[w.name] = {"ms_per_launch": ms, "unmasked_block_flops": flops, "tflops": achieved,
-                       "executed_mma_tflops": 3.0 * achieved, "frac_of_tf32_peak": 3.0 * achieved / tf32_peak,
+                       "executed_bf16_mma_tflops": FP32_SPLIT_PRODUCTS * achieved,
+                       "frac_of_ceiling": achieved / ceiling,
                        "l2": "K and V (64 MB at D = 128) stay in L2 across launches", "launches": steps,
                        "clocks": clocks.summary()}
         del dq, dk, dv, out, lse, bm
