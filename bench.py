@@ -385,7 +385,9 @@ def fp32_scale_timings(fa, torch, device_index: int, steps: int, peaks: dict) ->
     the oracle; this one is the same kind (causal, identity score) at
     B1 H16 S4096, D = 64 and 128.  Each product takes six bf16 MMAs, so the
     tensor cores execute 6x the algorithmic FLOPs; the ceiling of the
-    algorithmic rate is the measured bf16 burst / 6.
+    algorithmic rate is the measured bf16 burst / 6.  The float32 backward
+    (CUDA-core kernels) is timed on the same inputs against the fp32 FMA
+    rate of the CUDA cores.
     """
     if steps <= 0:
         return None
@@ -418,12 +420,38 @@ def fp32_scale_timings(fa, torch, device_index: int, steps: int, peaks: dict) ->
             raise RuntimeError(f"device status reported a timeout on {w.name}")
         ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
         achieved = flops / (ms * 1e-3) / 1e12
+        # backward: 2.5x the forward's algorithmic FLOPs (see backward_timings)
+        gen = torch.Generator(device=dq.device).manual_seed(1)
+        dout = torch.randn(out.shape, generator=gen, device=dq.device, dtype=torch.float32)
+        bq = fa.flex_block_mask_transpose(bm, stream=stream)
+        gq, gk, gv = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+
+        def launch_bwd():
+            fa.flex_attention_bwd(dq, dk, dv, out, lse, dout, bm, bq, w.score, w.score_param, w.scale, dq=gq,
+                                  dk=gk, dv=gv, stream=stream)
+
+        launch_bwd()
+        torch.cuda.synchronize()
+        evb = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(2)]
+        for a, b in evb:
+            a.record(stream)
+            launch_bwd()
+            b.record(stream)
+        torch.cuda.synchronize()
+        if fa.flex_device_status() != fa.FLEX_OK:
+            raise RuntimeError(f"device status reported a timeout in the backward on {w.name}")
+        ms_b = float(np.mean([a.elapsed_time(b) for a, b in evb]))
+        bwd_tflops = 2.5 * flops / (ms_b * 1e-3) / 1e12
         res[w.name] = {"ms_per_launch": ms, "unmasked_block_flops": flops, "tflops": achieved,
                        "executed_bf16_mma_tflops": FP32_SPLIT_PRODUCTS * achieved,
                        "frac_of_ceiling": achieved / ceiling,
                        "l2": "K and V (64 MB at D = 128) stay in L2 across launches", "launches": steps,
-                       "clocks": clocks.summary()}
-        del dq, dk, dv, out, lse, bm
+                       "clocks": clocks.summary(),
+                       "backward": {"ms_per_launch": ms_b, "launches": len(evb), "tflops": bwd_tflops,
+                                    "bound": "alu", "peak": FP32_CUDA_CORE_TFLOPS,
+                                    "frac": bwd_tflops / FP32_CUDA_CORE_TFLOPS,
+                                    "kernels": "attn_bwd_delta + attn_bwd_dkdv + attn_bwd_dq (fp32 FMA, CUDA cores)"}}
+        del dq, dk, dv, out, lse, bm, bq, dout, gq, gk, gv
         torch.cuda.empty_cache()
     return res
 

@@ -95,6 +95,26 @@ def test_single_key_rows_return_v(dtype, score):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("direction", [1.0, -1.0], ids=["rising", "falling"])
+@pytest.mark.parametrize("mask", [W.MASK_CAUSAL, W.MASK_ALL])
+def test_row_max_moving_along_kv(dtype, direction, mask):
+    # scores that rise (or fall) by ~4 per 64 keys along every row: the
+    # running maximum keeps moving by more than the rescale threshold, so O
+    # and l are rescaled over and over on whichever end the kernel walks from
+    B, H, S, D = 1, 2, 1024, 64
+    rng = np.random.default_rng(12)
+    q = (1.0 + 0.1 * rng.standard_normal((B, H, S, D))).astype(np.float32)
+    ramp = direction * 8.0 * (np.arange(S) / S)[None, None, :, None]
+    k = (ramp + 0.1 * rng.standard_normal((B, H, S, D))).astype(np.float32)
+    v = rng.standard_normal((B, H, S, D), dtype=np.float32)
+    if dtype == "bf16":
+        q, k, v = W.round_to_bf16(q), W.round_to_bf16(k), W.round_to_bf16(v)
+    out, lse, _ = run_attention(q, k, v, mask, W.SCORE_IDENTITY, 0.125, dtype)
+    ref_out, ref_lse = oracle.attention(q, k, v, mask, W.SCORE_IDENTITY, 0.125)
+    compare(out, lse, ref_out, ref_lse, dtype, "moving max")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("q_len,kv_len", [(256, 640), (640, 256)])
 @pytest.mark.parametrize("mask", [W.MASK_CAUSAL, W.MASK_ALL])
 def test_rectangular(dtype, q_len, kv_len, mask):
