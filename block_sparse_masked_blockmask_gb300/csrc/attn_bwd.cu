@@ -17,9 +17,15 @@
 // forward does.  P is recomputed from the saved lse in both, so nothing is
 // accumulated across CTAs.  A fourth kernel transposes the kv-side lists.
 //
-// Each thread owns 32 of a row's D dims, as 8 groups of 4 contiguous floats
-// spaced 4 * (threads per row) apart, so the row's threads read distinct
-// shared-memory banks when they fetch the same staged row.
+// The fp32 dK/dV and dQ kernels are register-tiled on the CUDA cores: a CTA
+// of 256 threads holds its 64 owned rows of two tensors in shared memory
+// and walks the other side in steps of 64 rows (two tiles of 64 x D).  Per
+// step a thread computes a 4 x 4 patch of the two 64 x 64 products over D
+// (the recomputed score and dP), applies score_mod, mask_mod, exp and the
+// dS formula to it, writes it to shared memory transposed, and then
+// accumulates a 4 x (D / 16) block of its output rows over the 64 walked
+// rows.  Rows are padded by 4 floats, so the 16-byte loads of a quarter warp
+// fall in eight distinct bank groups.
 #include "attn_bwd_tc.cuh"
 #include "bwd_internal.h"
 #include "ptx.cuh"
@@ -28,19 +34,19 @@
 namespace flex {
 namespace {
 
-constexpr int kBwdRows = 64;    // rows per CTA (kv rows for dK/dV, q rows for dQ)
-constexpr int kDimsPer = 32;    // dims per thread
-constexpr int kGroups = kDimsPer / 4;
+constexpr int kTRows = 64;       // owned rows per CTA, walked rows per step
+constexpr int kTThreads = 256;
 
 template <int D>
-struct BwdCfg {
-    static constexpr int kTpr = D / kDimsPer;          // threads per row: 2 (D = 64) or 4 (D = 128)
-    static constexpr int kThreads = kBwdRows * kTpr;   // 128 or 256
-    static constexpr int kStride = 4 * kTpr;           // distance between a thread's groups
-    // two staged 128 x D fp32 tiles, then two 128-float row vectors
-    // plus one flag word per walked tile of a chunk (the BlockMask read as 128-tiles)
+struct TiledCfg {
+    static constexpr int kLd = D + 4;          // padded row stride of a 64 x D tile (floats)
+    static constexpr int kZLd = kTRows + 4;    // padded row stride of a 64 x 64 tile
+    static constexpr int kTile = kTRows * kLd;
+    static constexpr int kZ = kTRows * kZLd;
+    static constexpr int kCols = D / 16;       // output columns per thread (two float4 at D = 128)
+    // four 64 x D tiles (two owned, two walked), two 64 x 64 tiles, two row vectors, one flag word per walked tile
     static constexpr size_t kSmem =
-        2ull * kBlock * D * sizeof(float) + 2ull * kBlock * sizeof(float) + kMaxKvBlocks * sizeof(uint32_t);
+        (4ull * kTile + 2ull * kZ + 2ull * kTRows) * sizeof(float) + kMaxKvBlocks * sizeof(uint32_t);
 };
 
 __device__ __forceinline__ float4 load4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
@@ -49,20 +55,17 @@ __device__ __forceinline__ float4 load4(const uint16_t *p) {
     return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
 }
-__device__ __forceinline__ void store4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
-__device__ __forceinline__ void store4(uint16_t *p, float4 v) {
-    *reinterpret_cast<uint2 *>(p) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
-}
 
 // score_mod at the scaled score t, and its derivative d score_mod / dt
-__device__ __forceinline__ float score_fwd(int kind, float cap, float t, float slope, int q, int kv, float &grad) {
-    if (kind == FLEX_SCORE_SOFTCAP) {
+template <int SCORE>
+__device__ __forceinline__ float score_fwd(float cap, float t, float slope, int q, int kv, float &grad) {
+    if constexpr (SCORE == FLEX_SCORE_SOFTCAP) {
         const float u = tanhf(t / cap);
         grad = 1.f - u * u;
         return cap * u;
     }
     grad = 1.f;
-    if (kind == FLEX_SCORE_ALIBI) return t - slope * (float)(q - kv);
+    if constexpr (SCORE == FLEX_SCORE_ALIBI) return t - slope * (float)(q - kv);
     return t;
 }
 
@@ -92,63 +95,142 @@ __global__ void __launch_bounds__(256) attn_bwd_delta_kernel(AttnProblem p, BwdA
     if (lane == 0) a.delta[r] = acc;
 }
 
-// Stage 128 rows of a [.., S, D] tensor (row stride `rs` elements) starting
-// at row r0 into shared memory as fp32; rows at or past `len` become zeros.
-template <int D, int THREADS, typename T>
-__device__ __forceinline__ void stage_tile(float *dst, const T *src, int64_t rs, int r0, int len) {
-    for (int i = threadIdx.x; i < kBlock * D / 4; i += THREADS) {
-        const int r = (i * 4) / D, c = (i * 4) % D;
-        const float4 v = r0 + r < len ? load4(src + (int64_t)(r0 + r) * rs + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-        reinterpret_cast<float4 *>(dst)[i] = v;
+// 64 rows of a [.., S, D] float32 tensor (row stride `rs` elements) from
+// row r0 into a padded shared-memory tile; rows at or past `len` are zeros.
+template <int D>
+__device__ __forceinline__ void load_rows(float *dst, const float *src, int64_t rs, int r0, int len) {
+    constexpr int kV = D / 4;  // float4 per row
+#pragma unroll
+    for (int u = 0; u < kTRows * kV / kTThreads; ++u) {
+        const int i = (int)threadIdx.x + kTThreads * u, r = i / kV, c = i % kV;
+        const float4 v = r0 + r < len ? __ldg(reinterpret_cast<const float4 *>(src + (int64_t)(r0 + r) * rs) + c)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(dst + r * TiledCfg<D>::kLd + 4 * c) = v;
     }
 }
 
-// dK, dV: CTA = 64 kv rows of one kv block; the q blocks come from the
-// transposed lists (full tiles first, then partial ones).
-template <int D, typename T>
-__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_dkdv_kernel(AttnProblem p, BwdArgs a) {
-    using C = BwdCfg<D>;
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
+}
+
+// x1[i][j] = A1[4 ta + i] . W1[tw + 16 j] and x2 likewise, over the D columns
+// of the padded 64 x D tiles.
+template <int D>
+__device__ __forceinline__ void dots4x4(const float *a1, const float *w1, const float *a2, const float *w2, int ta,
+                                        int tw, float (&x1)[4][4], float (&x2)[4][4]) {
+    constexpr int kLd = TiledCfg<D>::kLd;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x1[i][j] = x2[i][j] = 0.f;
+#pragma unroll 2
+    for (int d = 0; d < D; d += 4) {
+        float4 ra1[4], ra2[4], rw1[4], rw2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ra1[i] = *reinterpret_cast<const float4 *>(a1 + (4 * ta + i) * kLd + d);
+            ra2[i] = *reinterpret_cast<const float4 *>(a2 + (4 * ta + i) * kLd + d);
+            rw1[i] = *reinterpret_cast<const float4 *>(w1 + (tw + 16 * i) * kLd + d);
+            rw2[i] = *reinterpret_cast<const float4 *>(w2 + (tw + 16 * i) * kLd + d);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                x1[i][j] = dot4(ra1[i], rw1[j], x1[i][j]);
+                x2[i][j] = dot4(ra2[i], rw2[j], x2[i][j]);
+            }
+    }
+}
+
+// z[i][j] (owned row 4 ta + i, walked row tw + 16 j) into the 64 x 64 tile
+// stored walked-row-major: zs[tw + 16 j][4 ta + i].
+__device__ __forceinline__ void store_patch(float *zs, int ta, int tw, const float (&z)[4][4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<float4 *>(zs + (tw + 16 * j) * (kTRows + 4) + 4 * ta) =
+            make_float4(z[0][j], z[1][j], z[2][j], z[3][j]);
+}
+
+// y[i][c] += sum over the 64 walked rows w of zs[w][4 ta + i] * W[w][col c],
+// the thread's columns being 4 td .. 4 td + 3 and, at D = 128, 64 + the same.
+template <int D>
+__device__ __forceinline__ void accumulate(const float *zs, const float *w, int ta, int td,
+                                           float (&y)[4][TiledCfg<D>::kCols]) {
+    constexpr int kLd = TiledCfg<D>::kLd;
+#pragma unroll 4
+    for (int r = 0; r < kTRows; ++r) {
+        const float4 z = *reinterpret_cast<const float4 *>(zs + r * (kTRows + 4) + 4 * ta);
+        const float zz[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+            const float4 v = *reinterpret_cast<const float4 *>(w + r * kLd + 64 * h + 4 * td);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                y[i][4 * h] = fmaf(zz[i], v.x, y[i][4 * h]);
+                y[i][4 * h + 1] = fmaf(zz[i], v.y, y[i][4 * h + 1]);
+                y[i][4 * h + 2] = fmaf(zz[i], v.z, y[i][4 * h + 2]);
+                y[i][4 * h + 3] = fmaf(zz[i], v.w, y[i][4 * h + 3]);
+            }
+        }
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void store_rows(float *dst, int row0, int len, int ta, int td,
+                                           const float (&y)[4][TiledCfg<D>::kCols]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int r = row0 + 4 * ta + i;
+        if (r >= len) continue;
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h)
+            *reinterpret_cast<float4 *>(dst + (int64_t)r * D + 64 * h + 4 * td) =
+                make_float4(y[i][4 * h], y[i][4 * h + 1], y[i][4 * h + 2], y[i][4 * h + 3]);
+    }
+}
+
+// dK, dV (fp32): CTA = 64 kv rows of one kv block; the q blocks come from the
+// transposed lists, each walked in two steps of 64 q rows.
+template <int D, int SCORE>
+__global__ void __launch_bounds__(kTThreads, 1) attn_bwd_dkdv_kernel(AttnProblem p, BwdArgs a) {
+    using C = TiledCfg<D>;
     extern __shared__ float4 smem4[];
-    float *qs = reinterpret_cast<float *>(smem4);
-    float *gs = qs + kBlock * D;
-    float *ls = gs + kBlock * D;
-    float *dl = ls + kBlock;
-    uint32_t *flags = reinterpret_cast<uint32_t *>(dl + kBlock);
+    float *ks = reinterpret_cast<float *>(smem4), *vs = ks + C::kTile;   // owned
+    float *qs = vs + C::kTile, *gs = qs + C::kTile;                        // walked
+    float *ps = gs + C::kTile, *dss = ps + C::kZ;                          // P^T, dS^T patches (walked-row-major)
+    float *ls = dss + C::kZ, *dl = ls + kTRows;
+    uint32_t *flags = reinterpret_cast<uint32_t *>(dl + kTRows);
 
     const int kvb = blockIdx.x / 2;
     const int bh = p.bh_begin + (int)blockIdx.y, h = bh % p.H, b = bh / p.H;
-    const int row = threadIdx.x / C::kTpr, part = threadIdx.x % C::kTpr;
-    const int kv = kvb * kBlock + (blockIdx.x & 1) * kBwdRows + row;
-    const bool kv_in = kv < p.kv_len;
-
-    const T *kp = static_cast<const T *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1] + (int64_t)kv * p.k_stride[2];
-    const T *vp = static_cast<const T *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1] + (int64_t)kv * p.v_stride[2];
-    float kr[kDimsPer], vr[kDimsPer], dk[kDimsPer], dv[kDimsPer];
+    const int kv0 = kvb * kBlock + (blockIdx.x & 1) * kTRows;
+    if (kv0 >= p.kv_len) return;  // the second half of a short tail tile
+    const int ta = threadIdx.x / 16, tw = threadIdx.x % 16;
+    const float slope = SCORE == FLEX_SCORE_ALIBI ? exp2f(-8.f * (float)(h + 1) / (float)p.H) : 0.f;
+    const float *kbase = static_cast<const float *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
+    const float *vbase = static_cast<const float *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1];
+    load_rows<D>(ks, kbase, p.k_stride[2], kv0, p.kv_len);
+    load_rows<D>(vs, vbase, p.v_stride[2], kv0, p.kv_len);
+    float dk[4][C::kCols], dv[4][C::kCols];
 #pragma unroll
-    for (int gi = 0; gi < kGroups; ++gi) {
-        const int d = gi * C::kStride + 4 * part;
-        const float4 x = kv_in ? load4(kp + d) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 y = kv_in ? load4(vp + d) : make_float4(0.f, 0.f, 0.f, 0.f);
-        kr[4 * gi] = x.x, kr[4 * gi + 1] = x.y, kr[4 * gi + 2] = x.z, kr[4 * gi + 3] = x.w;
-        vr[4 * gi] = y.x, vr[4 * gi + 1] = y.y, vr[4 * gi + 2] = y.z, vr[4 * gi + 3] = y.w;
-    }
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int e = 0; e < kDimsPer; ++e) dk[e] = dv[e] = 0.f;
-    const float slope = exp2f(-8.f * (float)(h + 1) / (float)p.H);
+        for (int c = 0; c < C::kCols; ++c) dk[i][c] = dv[i][c] = 0.f;
 
     // the q side of the BlockMask (any block sizes) read as 128-tiles, in
     // chunks of kMaxKvBlocks q tiles; counts clamped and malformed entries
     // dropped, so no load leaves the tensors
     const TileLists lists{a.q_num, a.q_idx, a.fq_num, a.fq_idx, p.nkvb, p.nqb, p.kv_block, p.q_block, p.nqt};
-    const T *qbase = static_cast<const T *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1];
-    const T *gbase = static_cast<const T *>(a.dout) + (int64_t)bh * p.q_len * D;
+    const float *qbase = static_cast<const float *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1];
+    const float *gbase = static_cast<const float *>(a.dout) + (int64_t)bh * p.q_len * D;
     const float *lbase = p.lse + (int64_t)bh * p.q_len;
     const float *dbase = a.delta + (int64_t)bh * p.q_len;
 
     for (int tlo = 0; tlo < p.nqt; tlo += kMaxKvBlocks) {
       const int thi = min(p.nqt, tlo + kMaxKvBlocks);
       __syncthreads();  // the previous chunk's flags are consumed
-      for (int i = threadIdx.x; i < thi - tlo; i += C::kThreads) flags[i] = 0u;
+      for (int i = threadIdx.x; i < thi - tlo; i += kTThreads) flags[i] = 0u;
       __syncthreads();
       if (threadIdx.x < 32) tl_mark_warp(lists, bh, kvb, 0, flags, tlo, thi, threadIdx.x);
       __syncthreads();
@@ -156,168 +238,127 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_dkdv_kernel(A
         const uint32_t w = flags[qb - tlo];  // uniform over the CTA
         if (!tl_listed(w, 0)) continue;
         const bool full = tl_full(tl_expect(lists), w, 0);
-        const int q0 = qb * kBlock;
-        __syncthreads();  // the previous q block is consumed
-        stage_tile<D, C::kThreads>(qs, qbase, p.q_stride[2], q0, p.q_len);
-        stage_tile<D, C::kThreads>(gs, gbase, D, q0, p.q_len);
-        for (int r = threadIdx.x; r < kBlock; r += C::kThreads) {
-            const bool in = q0 + r < p.q_len;
-            ls[r] = in ? lbase[q0 + r] : -INFINITY;
-            dl[r] = in ? dbase[q0 + r] : 0.f;
-        }
-        __syncthreads();
-        for (int r = 0; r < kBlock; ++r) {
-            const int q = q0 + r;
-            float qv[kDimsPer], gv[kDimsPer];
-            float t4[4] = {0.f, 0.f, 0.f, 0.f}, p4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int q0 = qb * kBlock; q0 < min(qb * kBlock + kBlock, p.q_len); q0 += kTRows) {
+            __syncthreads();  // the previous step's walked tiles and patches are consumed
+            load_rows<D>(qs, qbase, p.q_stride[2], q0, p.q_len);
+            load_rows<D>(gs, gbase, D, q0, p.q_len);
+            if (threadIdx.x < kTRows) {
+                const int q = q0 + (int)threadIdx.x;
+                ls[threadIdx.x] = q < p.q_len ? lbase[q] : -INFINITY;
+                dl[threadIdx.x] = q < p.q_len ? dbase[q] : 0.f;
+            }
+            __syncthreads();
+            float st[4][4], dp[4][4];
+            dots4x4<D>(ks, qs, vs, gs, ta, tw, st, dp);
 #pragma unroll
-            for (int gi = 0; gi < kGroups; ++gi) {
-                const int d = gi * C::kStride + 4 * part;
-                const float4 x = reinterpret_cast<const float4 *>(qs + r * D + d)[0];
-                const float4 y = reinterpret_cast<const float4 *>(gs + r * D + d)[0];
-                qv[4 * gi] = x.x, qv[4 * gi + 1] = x.y, qv[4 * gi + 2] = x.z, qv[4 * gi + 3] = x.w;
-                gv[4 * gi] = y.x, gv[4 * gi + 1] = y.y, gv[4 * gi + 2] = y.z, gv[4 * gi + 3] = y.w;
+            for (int j = 0; j < 4; ++j) {
+                const int q = q0 + tw + 16 * j;
+                const float lse = ls[tw + 16 * j], dlt = dl[tw + 16 * j];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    t4[c] = fmaf(qv[4 * gi + c], kr[4 * gi + c], t4[c]);
-                    p4[c] = fmaf(gv[4 * gi + c], vr[4 * gi + c], p4[c]);
+                for (int i = 0; i < 4; ++i) {
+                    const int kv = kv0 + 4 * ta + i;
+                    const bool keep = lse != -INFINITY && (full || (kv < p.kv_len && mask_mod(p.mask, b, q, kv)));
+                    float pr = 0.f, dts = 0.f;
+                    if (keep) {
+                        float grad;
+                        const float x = score_fwd<SCORE>(p.score_param, st[i][j] * p.scale, slope, q, kv, grad);
+                        pr = expf(x - lse);
+                        dts = p.scale * pr * (dp[i][j] - dlt) * grad;
+                    }
+                    st[i][j] = pr;
+                    dp[i][j] = dts;
                 }
             }
-            float dot = (t4[0] + t4[1]) + (t4[2] + t4[3]);
-            float dp = (p4[0] + p4[1]) + (p4[2] + p4[3]);
-#pragma unroll
-            for (int s = 1; s < C::kTpr; s <<= 1) {
-                dot += __shfl_xor_sync(0xffffffffu, dot, s);
-                dp += __shfl_xor_sync(0xffffffffu, dp, s);
-            }
-            const float lse = ls[r];
-            const bool keep = lse != -INFINITY &&
-                              (full || (kv_in && q < p.q_len && mask_mod(p.mask, b, q, kv)));
-            float pr = 0.f, dts = 0.f;
-            if (keep) {
-                float grad;
-                const float x = score_fwd(p.score_kind, p.score_param, dot * p.scale, slope, q, kv, grad);
-                pr = expf(x - lse);
-                dts = p.scale * pr * (dp - dl[r]) * grad;
-            }
-#pragma unroll
-            for (int e = 0; e < kDimsPer; ++e) {
-                dv[e] = fmaf(pr, gv[e], dv[e]);
-                dk[e] = fmaf(dts, qv[e], dk[e]);
-            }
+            store_patch(ps, ta, tw, st);
+            store_patch(dss, ta, tw, dp);
+            __syncthreads();
+            accumulate<D>(ps, gs, ta, tw, dv);
+            accumulate<D>(dss, qs, ta, tw, dk);
         }
       }
     }
-    if (!kv_in) return;
-    const int64_t orow = (int64_t)bh * p.kv_len + kv;
-    T *dkp = static_cast<T *>(a.dk) + orow * D;
-    T *dvp = static_cast<T *>(a.dv) + orow * D;
-#pragma unroll
-    for (int gi = 0; gi < kGroups; ++gi) {
-        const int d = gi * C::kStride + 4 * part;
-        store4(dkp + d, make_float4(dk[4 * gi], dk[4 * gi + 1], dk[4 * gi + 2], dk[4 * gi + 3]));
-        store4(dvp + d, make_float4(dv[4 * gi], dv[4 * gi + 1], dv[4 * gi + 2], dv[4 * gi + 3]));
-    }
+    const int64_t orow = (int64_t)bh * p.kv_len;
+    store_rows<D>(static_cast<float *>(a.dk) + orow * D, kv0, p.kv_len, ta, tw, dk);
+    store_rows<D>(static_cast<float *>(a.dv) + orow * D, kv0, p.kv_len, ta, tw, dv);
 }
 
-// dQ: CTA = 64 q rows of one q block; the kv tiles come from the kv side of
-// the BlockMask, as in the forward pass.
-template <int D, typename T>
-__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1) attn_bwd_dq_kernel(AttnProblem p, BwdArgs a) {
-    using C = BwdCfg<D>;
+// dQ (fp32): CTA = 64 q rows of one q block; the kv tiles come from the kv
+// side of the BlockMask, as in the forward pass, each walked in two steps.
+template <int D, int SCORE>
+__global__ void __launch_bounds__(kTThreads, 1) attn_bwd_dq_kernel(AttnProblem p, BwdArgs a) {
+    using C = TiledCfg<D>;
     extern __shared__ float4 smem4[];
-    float *ks = reinterpret_cast<float *>(smem4);
-    float *vs = ks + kBlock * D;
-    uint32_t *flags = reinterpret_cast<uint32_t *>(vs + kBlock * D + 2 * kBlock);
+    float *qs = reinterpret_cast<float *>(smem4), *gs = qs + C::kTile;   // owned
+    float *ks = gs + C::kTile, *vs = ks + C::kTile;                        // walked
+    float *dss = vs + C::kTile;                                            // dS patches (walked-row-major)
+    uint32_t *flags = reinterpret_cast<uint32_t *>(dss + 2 * C::kZ + 2 * kTRows);
 
     const int qb = blockIdx.x / 2;
     const int bh = p.bh_begin + (int)blockIdx.y, h = bh % p.H, b = bh / p.H;
-    const int row = threadIdx.x / C::kTpr, part = threadIdx.x % C::kTpr;
-    const int q = qb * kBlock + (blockIdx.x & 1) * kBwdRows + row;
-    const bool q_in = q < p.q_len;
-
-    const T *qp = static_cast<const T *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1] +
-                  (int64_t)(q_in ? q : 0) * p.q_stride[2];
-    const T *gp = static_cast<const T *>(a.dout) + ((int64_t)bh * p.q_len + (q_in ? q : 0)) * D;
-    float qv[kDimsPer], gv[kDimsPer], dq[kDimsPer];
+    const int q0 = qb * kBlock + (blockIdx.x & 1) * kTRows;
+    if (q0 >= p.q_len) return;  // the second half of a short tail tile
+    const int ta = threadIdx.x / 16, tw = threadIdx.x % 16;
+    const float slope = SCORE == FLEX_SCORE_ALIBI ? exp2f(-8.f * (float)(h + 1) / (float)p.H) : 0.f;
+    const float *qbase = static_cast<const float *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1];
+    const float *gbase = static_cast<const float *>(a.dout) + (int64_t)bh * p.q_len * D;
+    load_rows<D>(qs, qbase, p.q_stride[2], q0, p.q_len);
+    load_rows<D>(gs, gbase, D, q0, p.q_len);
+    float lse[4], dlt[4];
 #pragma unroll
-    for (int gi = 0; gi < kGroups; ++gi) {
-        const int d = gi * C::kStride + 4 * part;
-        const float4 x = q_in ? load4(qp + d) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 y = q_in ? load4(gp + d) : make_float4(0.f, 0.f, 0.f, 0.f);
-        qv[4 * gi] = x.x, qv[4 * gi + 1] = x.y, qv[4 * gi + 2] = x.z, qv[4 * gi + 3] = x.w;
-        gv[4 * gi] = y.x, gv[4 * gi + 1] = y.y, gv[4 * gi + 2] = y.z, gv[4 * gi + 3] = y.w;
+    for (int i = 0; i < 4; ++i) {
+        const int q = q0 + 4 * ta + i;
+        lse[i] = q < p.q_len ? p.lse[(int64_t)bh * p.q_len + q] : -INFINITY;
+        dlt[i] = q < p.q_len ? a.delta[(int64_t)bh * p.q_len + q] : 0.f;
     }
+    float dq[4][C::kCols];
 #pragma unroll
-    for (int e = 0; e < kDimsPer; ++e) dq[e] = 0.f;
-    const int64_t orow = (int64_t)bh * p.q_len + q;
-    const float lse = q_in ? p.lse[orow] : -INFINITY;
-    const float dlt = q_in ? a.delta[orow] : 0.f;
-    const float slope = exp2f(-8.f * (float)(h + 1) / (float)p.H);
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int c = 0; c < C::kCols; ++c) dq[i][c] = 0.f;
 
     // the kv side of the BlockMask (any block sizes) read as 128-tiles (at
     // most kMaxKvBlocks kv tiles)
     const TileLists lists{p.kv_num, p.kv_idx, p.full_num, p.full_idx, p.nqb, p.nkvb, p.q_block, p.kv_block, p.nkvt};
-    for (int i = threadIdx.x; i < p.nkvt; i += C::kThreads) flags[i] = 0u;
+    for (int i = threadIdx.x; i < p.nkvt; i += kTThreads) flags[i] = 0u;
     __syncthreads();
     if (threadIdx.x < 32) tl_mark_warp(lists, bh, qb, 0, flags, 0, p.nkvt, threadIdx.x);
     __syncthreads();
-    const T *kbase = static_cast<const T *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
-    const T *vbase = static_cast<const T *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1];
+    const float *kbase = static_cast<const float *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
+    const float *vbase = static_cast<const float *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1];
 
     for (int kvb = 0; kvb < p.nkvt; ++kvb) {
         const uint32_t w = flags[kvb];  // uniform over the CTA
         if (!tl_listed(w, 0)) continue;
         const bool full = tl_full(tl_expect(lists), w, 0);
-        const int kv0 = kvb * kBlock;
-        __syncthreads();
-        stage_tile<D, C::kThreads>(ks, kbase, p.k_stride[2], kv0, p.kv_len);
-        stage_tile<D, C::kThreads>(vs, vbase, p.v_stride[2], kv0, p.kv_len);
-        __syncthreads();
-        // Every thread runs the column loop, whose shuffles need all 32
-        // lanes; an empty or padding row (lse = -inf) only keeps no column.
-        for (int c = 0; c < kBlock; ++c) {
-            const int kv = kv0 + c;
-            float kc[kDimsPer];
-            float t4[4] = {0.f, 0.f, 0.f, 0.f}, p4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int kv0 = kvb * kBlock; kv0 < min(kvb * kBlock + kBlock, p.kv_len); kv0 += kTRows) {
+            __syncthreads();  // the previous step's walked tiles and patch are consumed
+            load_rows<D>(ks, kbase, p.k_stride[2], kv0, p.kv_len);
+            load_rows<D>(vs, vbase, p.v_stride[2], kv0, p.kv_len);
+            __syncthreads();
+            float st[4][4], dp[4][4];
+            dots4x4<D>(qs, ks, gs, vs, ta, tw, st, dp);
 #pragma unroll
-            for (int gi = 0; gi < kGroups; ++gi) {
-                const int d = gi * C::kStride + 4 * part;
-                const float4 x = reinterpret_cast<const float4 *>(ks + c * D + d)[0];
-                const float4 y = reinterpret_cast<const float4 *>(vs + c * D + d)[0];
-                kc[4 * gi] = x.x, kc[4 * gi + 1] = x.y, kc[4 * gi + 2] = x.z, kc[4 * gi + 3] = x.w;
-                const float yv[4] = {y.x, y.y, y.z, y.w};
+            for (int i = 0; i < 4; ++i) {
+                const int q = q0 + 4 * ta + i;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    t4[e] = fmaf(qv[4 * gi + e], kc[4 * gi + e], t4[e]);
-                    p4[e] = fmaf(gv[4 * gi + e], yv[e], p4[e]);
+                for (int j = 0; j < 4; ++j) {
+                    const int kv = kv0 + tw + 16 * j;
+                    const bool keep = lse[i] != -INFINITY && (full || (kv < p.kv_len && mask_mod(p.mask, b, q, kv)));
+                    float dts = 0.f;
+                    if (keep) {
+                        float grad;
+                        const float x = score_fwd<SCORE>(p.score_param, st[i][j] * p.scale, slope, q, kv, grad);
+                        dts = p.scale * expf(x - lse[i]) * (dp[i][j] - dlt[i]) * grad;
+                    }
+                    dp[i][j] = dts;
                 }
             }
-            float dot = (t4[0] + t4[1]) + (t4[2] + t4[3]);
-            float dp = (p4[0] + p4[1]) + (p4[2] + p4[3]);
-#pragma unroll
-            for (int s = 1; s < C::kTpr; s <<= 1) {
-                dot += __shfl_xor_sync(0xffffffffu, dot, s);
-                dp += __shfl_xor_sync(0xffffffffu, dp, s);
-            }
-            const bool keep = lse != -INFINITY && (full || (kv < p.kv_len && mask_mod(p.mask, b, q, kv)));
-            float dts = 0.f;
-            if (keep) {
-                float grad;
-                const float x = score_fwd(p.score_kind, p.score_param, dot * p.scale, slope, q, kv, grad);
-                dts = p.scale * expf(x - lse) * (dp - dlt) * grad;
-            }
-#pragma unroll
-            for (int e = 0; e < kDimsPer; ++e) dq[e] = fmaf(dts, kc[e], dq[e]);
+            store_patch(dss, ta, tw, dp);
+            __syncthreads();
+            accumulate<D>(dss, ks, ta, tw, dq);
         }
     }
-    if (!q_in) return;
-    T *dqp = static_cast<T *>(a.dq) + orow * D;
-#pragma unroll
-    for (int gi = 0; gi < kGroups; ++gi) {
-        const int d = gi * C::kStride + 4 * part;
-        store4(dqp + d, make_float4(dq[4 * gi], dq[4 * gi + 1], dq[4 * gi + 2], dq[4 * gi + 3]));
-    }
+    store_rows<D>(static_cast<float *>(a.dq) + (int64_t)bh * p.q_len * D, q0, p.q_len, ta, tw, dq);
 }
 
 // Whether the ascending list[0, n) holds x.
@@ -369,28 +410,43 @@ __global__ void __launch_bounds__(128) block_mask_transpose_kernel(const int32_t
     }
 }
 
-template <int D, typename T>
-cudaError_t launch_bwd_typed(const AttnProblem &p, const BwdArgs &a, cudaStream_t stream) {
-    using C = BwdCfg<D>;
-    const int64_t rows = (int64_t)p.B * p.H * p.q_len;
-    attn_bwd_delta_kernel<D, T><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, stream>>>(p, a, rows);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+template <int D, int SCORE>
+cudaError_t launch_bwd_fp32_score(const AttnProblem &p, const BwdArgs &a, cudaStream_t stream) {
+    using C = TiledCfg<D>;
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, SCORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+        e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, SCORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)C::kSmem);
     if (e != cudaSuccess) return e;
     // grid.y holds at most 65535 (b, h) pairs per launch
     for (int begin = 0; begin < p.B * p.H; begin += 65535) {
         AttnProblem part = p;
         part.bh_begin = begin;
         const int count = p.B * p.H - begin < 65535 ? p.B * p.H - begin : 65535;
-        attn_bwd_dkdv_kernel<D, T><<<dim3(2 * p.nkvt, count), C::kThreads, C::kSmem, stream>>>(part, a);
+        attn_bwd_dkdv_kernel<D, SCORE><<<dim3(2 * p.nkvt, count), kTThreads, C::kSmem, stream>>>(part, a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        attn_bwd_dq_kernel<D, T><<<dim3(2 * p.nqt, count), C::kThreads, C::kSmem, stream>>>(part, a);
+        attn_bwd_dq_kernel<D, SCORE><<<dim3(2 * p.nqt, count), kTThreads, C::kSmem, stream>>>(part, a);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+// fp32: delta, then the register-tiled dK/dV and dQ kernels.
+template <int D>
+cudaError_t launch_bwd_fp32(const AttnProblem &p, const BwdArgs &a, cudaStream_t stream) {
+    const int64_t rows = (int64_t)p.B * p.H * p.q_len;
+    attn_bwd_delta_kernel<D, float><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, stream>>>(p, a, rows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    switch (p.score_kind) {
+        case FLEX_SCORE_SOFTCAP:
+            return launch_bwd_fp32_score<D, FLEX_SCORE_SOFTCAP>(p, a, stream);
+        case FLEX_SCORE_ALIBI:
+            return launch_bwd_fp32_score<D, FLEX_SCORE_ALIBI>(p, a, stream);
+        default:
+            return launch_bwd_fp32_score<D, FLEX_SCORE_IDENTITY>(p, a, stream);
+    }
 }
 
 }  // namespace
@@ -461,7 +517,7 @@ cudaError_t launch_attn_bwd(const AttnProblem &p, int dtype, const void *dout, c
                             void *dv, float *delta, cudaStream_t stream) {
     const BwdArgs a{dout, q_num, q_idx, fq_num, fq_idx, dq, dk, dv, delta};
     if (dtype == FLEX_DTYPE_BF16) return launch_bwd_bf16_tc(p, a, stream);
-    return p.D == 64 ? launch_bwd_typed<64, float>(p, a, stream) : launch_bwd_typed<128, float>(p, a, stream);
+    return p.D == 64 ? launch_bwd_fp32<64>(p, a, stream) : launch_bwd_fp32<128>(p, a, stream);
 }
 
 }  // namespace flex
