@@ -24,8 +24,9 @@
 // (the recomputed score and dP), applies score_mod, mask_mod, exp and the
 // dS formula to it, writes it to shared memory transposed, and then
 // accumulates a 4 x (D / 16) block of its output rows over the 64 walked
-// rows.  Rows are padded by 4 floats, so the 16-byte loads of a quarter warp
-// fall in eight distinct bank groups.
+// rows; the FMAs are packed fp32x2 (fma.rn.f32x2, two per instruction).
+// Rows are padded by 4 floats, so the 16-byte loads of a quarter warp fall
+// in eight distinct bank groups.
 #include "attn_bwd_tc.cuh"
 #include "bwd_internal.h"
 #include "ptx.cuh"
@@ -109,38 +110,41 @@ __device__ __forceinline__ void load_rows(float *dst, const float *src, int64_t 
     }
 }
 
-__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
-    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
-}
-
-// x1[i][j] = A1[4 ta + i] . W1[tw + 16 j] and x2 likewise, over the D columns
-// of the padded 64 x D tiles.
+// x[i][j] = A[4 ta + i] . W[tw + 16 j] over the D columns of two padded
+// 64 x D tiles, with packed fp32x2 FMAs (even and odd columns in the two
+// halves of an accumulator, added at the end).
 template <int D>
-__device__ __forceinline__ void dots4x4(const float *a1, const float *w1, const float *a2, const float *w2, int ta,
-                                        int tw, float (&x1)[4][4], float (&x2)[4][4]) {
+__device__ __forceinline__ void dots4x4(const float *a, const float *w, int ta, int tw, float (&x)[4][4]) {
     constexpr int kLd = TiledCfg<D>::kLd;
+    uint64_t acc[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) x1[i][j] = x2[i][j] = 0.f;
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0ull;  // (0.f, 0.f)
 #pragma unroll 2
     for (int d = 0; d < D; d += 4) {
-        float4 ra1[4], ra2[4], rw1[4], rw2[4];
+        ulonglong2 ra[4], rw[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            ra1[i] = *reinterpret_cast<const float4 *>(a1 + (4 * ta + i) * kLd + d);
-            ra2[i] = *reinterpret_cast<const float4 *>(a2 + (4 * ta + i) * kLd + d);
-            rw1[i] = *reinterpret_cast<const float4 *>(w1 + (tw + 16 * i) * kLd + d);
-            rw2[i] = *reinterpret_cast<const float4 *>(w2 + (tw + 16 * i) * kLd + d);
+            ra[i] = *reinterpret_cast<const ulonglong2 *>(a + (4 * ta + i) * kLd + d);
+            rw[i] = *reinterpret_cast<const ulonglong2 *>(w + (tw + 16 * i) * kLd + d);
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                x1[i][j] = dot4(ra1[i], rw1[j], x1[i][j]);
-                x2[i][j] = dot4(ra2[i], rw2[j], x2[i][j]);
+                acc[i][j] = f2_fma(ra[i].x, rw[j].x, acc[i][j]);
+                acc[i][j] = f2_fma(ra[i].y, rw[j].y, acc[i][j]);
             }
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float lo, hi;
+            f2_unpack(acc[i][j], lo, hi);
+            x[i][j] = lo + hi;
+        }
 }
 
 // z[i][j] (owned row 4 ta + i, walked row tw + 16 j) into the 64 x 64 tile
@@ -153,24 +157,24 @@ __device__ __forceinline__ void store_patch(float *zs, int ta, int tw, const flo
 }
 
 // y[i][c] += sum over the 64 walked rows w of zs[w][4 ta + i] * W[w][col c],
-// the thread's columns being 4 td .. 4 td + 3 and, at D = 128, 64 + the same.
+// the thread's columns being 4 td .. 4 td + 3 and, at D = 128, 64 + the
+// same, held as packed pairs: y[i][2 h] = columns (64 h + 4 td, + 1),
+// y[i][2 h + 1] = (+ 2, + 3).
 template <int D>
 __device__ __forceinline__ void accumulate(const float *zs, const float *w, int ta, int td,
-                                           float (&y)[4][TiledCfg<D>::kCols]) {
+                                           uint64_t (&y)[4][TiledCfg<D>::kCols / 2]) {
     constexpr int kLd = TiledCfg<D>::kLd;
 #pragma unroll 4
     for (int r = 0; r < kTRows; ++r) {
         const float4 z = *reinterpret_cast<const float4 *>(zs + r * (kTRows + 4) + 4 * ta);
-        const float zz[4] = {z.x, z.y, z.z, z.w};
+        const uint64_t zz[4] = {f2_pack(z.x, z.x), f2_pack(z.y, z.y), f2_pack(z.z, z.z), f2_pack(z.w, z.w)};
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
-            const float4 v = *reinterpret_cast<const float4 *>(w + r * kLd + 64 * h + 4 * td);
+            const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(w + r * kLd + 64 * h + 4 * td);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                y[i][4 * h] = fmaf(zz[i], v.x, y[i][4 * h]);
-                y[i][4 * h + 1] = fmaf(zz[i], v.y, y[i][4 * h + 1]);
-                y[i][4 * h + 2] = fmaf(zz[i], v.z, y[i][4 * h + 2]);
-                y[i][4 * h + 3] = fmaf(zz[i], v.w, y[i][4 * h + 3]);
+                y[i][2 * h] = f2_fma(zz[i], v.x, y[i][2 * h]);
+                y[i][2 * h + 1] = f2_fma(zz[i], v.y, y[i][2 * h + 1]);
             }
         }
     }
@@ -178,15 +182,18 @@ __device__ __forceinline__ void accumulate(const float *zs, const float *w, int 
 
 template <int D>
 __device__ __forceinline__ void store_rows(float *dst, int row0, int len, int ta, int td,
-                                           const float (&y)[4][TiledCfg<D>::kCols]) {
+                                           const uint64_t (&y)[4][TiledCfg<D>::kCols / 2]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int r = row0 + 4 * ta + i;
         if (r >= len) continue;
 #pragma unroll
-        for (int h = 0; h < D / 64; ++h)
-            *reinterpret_cast<float4 *>(dst + (int64_t)r * D + 64 * h + 4 * td) =
-                make_float4(y[i][4 * h], y[i][4 * h + 1], y[i][4 * h + 2], y[i][4 * h + 3]);
+        for (int h = 0; h < D / 64; ++h) {
+            float4 o;
+            f2_unpack(y[i][2 * h], o.x, o.y);
+            f2_unpack(y[i][2 * h + 1], o.z, o.w);
+            *reinterpret_cast<float4 *>(dst + (int64_t)r * D + 64 * h + 4 * td) = o;
+        }
     }
 }
 
@@ -212,11 +219,11 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_bwd_dkdv_kernel(AttnProblem
     const float *vbase = static_cast<const float *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1];
     load_rows<D>(ks, kbase, p.k_stride[2], kv0, p.kv_len);
     load_rows<D>(vs, vbase, p.v_stride[2], kv0, p.kv_len);
-    float dk[4][C::kCols], dv[4][C::kCols];
+    uint64_t dk[4][C::kCols / 2], dv[4][C::kCols / 2];  // packed column pairs
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int c = 0; c < C::kCols; ++c) dk[i][c] = dv[i][c] = 0.f;
+        for (int c = 0; c < C::kCols / 2; ++c) dk[i][c] = dv[i][c] = 0ull;
 
     // the q side of the BlockMask (any block sizes) read as 128-tiles, in
     // chunks of kMaxKvBlocks q tiles; counts clamped and malformed entries
@@ -249,7 +256,8 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_bwd_dkdv_kernel(AttnProblem
             }
             __syncthreads();
             float st[4][4], dp[4][4];
-            dots4x4<D>(ks, qs, vs, gs, ta, tw, st, dp);
+            dots4x4<D>(ks, qs, ta, tw, st);
+            dots4x4<D>(vs, gs, ta, tw, dp);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int q = q0 + tw + 16 * j;
@@ -310,11 +318,11 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_bwd_dq_kernel(AttnProblem p
         lse[i] = q < p.q_len ? p.lse[(int64_t)bh * p.q_len + q] : -INFINITY;
         dlt[i] = q < p.q_len ? a.delta[(int64_t)bh * p.q_len + q] : 0.f;
     }
-    float dq[4][C::kCols];
+    uint64_t dq[4][C::kCols / 2];  // packed column pairs
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int c = 0; c < C::kCols; ++c) dq[i][c] = 0.f;
+        for (int c = 0; c < C::kCols / 2; ++c) dq[i][c] = 0ull;
 
     // the kv side of the BlockMask (any block sizes) read as 128-tiles (at
     // most kMaxKvBlocks kv tiles)
@@ -336,7 +344,8 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_bwd_dq_kernel(AttnProblem p
             load_rows<D>(vs, vbase, p.v_stride[2], kv0, p.kv_len);
             __syncthreads();
             float st[4][4], dp[4][4];
-            dots4x4<D>(qs, ks, gs, vs, ta, tw, st, dp);
+            dots4x4<D>(qs, ks, ta, tw, st);
+            dots4x4<D>(gs, vs, ta, tw, dp);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int q = q0 + 4 * ta + i;
