@@ -24,7 +24,9 @@
 // issue costs ~50 cycles whatever its width up to N = 64, so narrow S MMAs
 // leave the tensor cores idle).
 //
-// Design (one CTA per (batch, head, 128-row q tile), 448 threads):
+// Design (one CTA per (batch, head, 128-row q tile), 448 threads at D = 64,
+// 480 at D = 128, where the producers move off the MMA issuer's
+// sub-partition; warp numbers below are those of D = 64):
 //   warps 0-3   softmax, one thread per q row (TMEM lane = row); at the start
 //               they read their Q rows, split them and write Q1, Q2, Q3
 //               (bf16 pairs) into tensor memory, where the S MMAs read them
@@ -60,11 +62,9 @@
 namespace flex {
 namespace {
 
-constexpr int kF32KWarp = 4;   // first of the four K producer warps
-constexpr int kF32VWarp = 8;   // first of the four V producer warps
-constexpr int kF32MmaWarp = 12;  // issues the PV MMAs (and allocates TMEM)
-constexpr int kF32SWarp = 13;    // issues the S MMAs
-constexpr int kF32Threads = 14 * 32;
+constexpr int kF32MmaWarp = 12;  // issues the (PV) MMAs and allocates TMEM
+constexpr int kF32SWarp = 13;    // D = 64: issues the S MMAs
+constexpr int kF32MaxThreads = 16 * 32;  // launch bound: at most 128 registers a thread
 constexpr uint32_t kF32TmemCols = 512;
 constexpr int kF32KS = 64;                // kv rows per chunk
 constexpr float kF32RescaleNats = 8.0f;   // O and l are rescaled when the maximum grows by more
@@ -81,6 +81,23 @@ struct F32Cfg {
     // MMAs keep the tensor pipe busy and S(u + 2) is better issued right
     // behind PV(u) than after a wait for its completion
     static constexpr bool kTwoIssuers = D == 64;
+    // Warp roles.  Warps are dealt to the four sub-partitions round robin
+    // (warp w on sub-partition w % 4), and a thread issuing MMAs slows down
+    // when its sub-partition is busy (~50 cycles an MMA alone, ~75 beside a
+    // TMEM-traffic warp and a shared-memory-store warp).  D = 128: the
+    // issuer (warp 12) shares its sub-partition only with softmax warp 0,
+    // warps 4 and 8 stay idle, the producers run on warps 5-7, 9 (K) and
+    // 10, 11, 13, 14 (V).  D = 64: K on 4-7, V on 8-11, PV issuer 12,
+    // S issuer 13.
+    static constexpr int kWarps = D == 128 ? 15 : 14;
+    __device__ static int k_index(int w) {
+        if (D == 64) return w >= 4 && w < 8 ? w - 4 : -1;
+        return w >= 5 && w < 8 ? w - 5 : w == 9 ? 3 : -1;
+    }
+    __device__ static int v_index(int w) {
+        if (D == 64) return w >= 8 && w < 12 ? w - 8 : -1;
+        return w == 10 || w == 11 ? w - 10 : w == 13 || w == 14 ? w - 11 : -1;
+    }
     static constexpr int kUnits = KS * D / 8 / 128;        // 8-float units per producer thread per chunk
     static constexpr uint32_t kAtom = KS * 128;            // 64 bf16 of a row, all KS rows
     static constexpr uint32_t kPart = KS * D * 2;          // one bf16 part of a chunk
@@ -224,7 +241,7 @@ __device__ __noinline__ bool f32_produce(F32Misc &ms, uint8_t *ring, uint64_t *f
 }
 
 template <int D, int SCORE, bool DOC>
-__global__ void __launch_bounds__(kF32Threads, 1) attn_fp32_kernel(AttnProblem p, int bh_major) {
+__global__ void __launch_bounds__(kF32MaxThreads, 1) attn_fp32_kernel(AttnProblem p, int bh_major) {
     using C = F32Cfg<D>;
     constexpr int KS = C::KS;
     extern __shared__ uint8_t smem_raw[];
@@ -287,21 +304,22 @@ __global__ void __launch_bounds__(kF32Threads, 1) attn_fp32_kernel(AttnProblem p
     volatile int *abort_flag = &ms.abort;
     const int nsub = ms.n * C::kSub;  // kv chunks
 
-    if (warp >= kF32KWarp && warp < kF32KWarp + 4) {
+    const int kidx = C::k_index(warp), vidx = C::v_index(warp);
+    if (kidx >= 0) {
         // --------------------------------------------------------- K producers
         const float *kbase = static_cast<const float *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
         if (!f32_produce<D>(ms, smem + C::kK0, ms.k_full, ms.k_empty, kbase, p.k_stride[2], p.kv_len, nsub,
-                            threadIdx.x - 32 * kF32KWarp, lane, abort_flag))
+                            32 * kidx + lane, lane, abort_flag))
             f32_fail(ms, p.status);
-    } else if (warp >= kF32VWarp && warp < kF32VWarp + 4) {
+    } else if (vidx >= 0) {
         // --------------------------------------------------------- V producers
         const float *vbase = static_cast<const float *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1];
         if (!f32_produce<D>(ms, smem + C::kV0, ms.v_full, ms.v_empty, vbase, p.v_stride[2], p.kv_len, nsub,
-                            threadIdx.x - 32 * kF32VWarp, lane, abort_flag))
+                            32 * vidx + lane, lane, abort_flag))
             f32_fail(ms, p.status);
-    } else if (warp == kF32SWarp || warp == kF32MmaWarp) {
+    } else if (warp == kF32MmaWarp || (C::kTwoIssuers && warp == kF32SWarp)) {
         // ---------------------------------------------------------------- MMA
-        if (lane == 0 && nsub > 0 && (C::kTwoIssuers || warp == kF32MmaWarp)) {
+        if (lane == 0 && nsub > 0) {
             constexpr uint32_t kHi = smem_desc_hi_sw128(1024);
             constexpr uint32_t idesc_s = idesc_bf16_f32(128, KS, 0, 0);
             constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
@@ -569,6 +587,7 @@ __global__ void __launch_bounds__(kF32Threads, 1) attn_fp32_kernel(AttnProblem p
 
 template <int D, int SCORE, bool DOC>
 cudaError_t launch_fp32_kernel(const AttnProblem &p, cudaStream_t stream) {
+    using C = F32Cfg<D>;
     const size_t smem = f32_smem_bytes<D>();
     auto kern = attn_fp32_kernel<D, SCORE, DOC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -576,7 +595,7 @@ cudaError_t launch_fp32_kernel(const AttnProblem &p, cudaStream_t stream) {
     if (p.nqt <= 65535) {
         // (b, h) pairs along x, q tiles (longest first) along y: the first
         // CTAs to run are the longest of every pair
-        kern<<<dim3(p.bh_count, p.nqt), kF32Threads, smem, stream>>>(p, 1);
+        kern<<<dim3(p.bh_count, p.nqt), C::kWarps * 32, smem, stream>>>(p, 1);
         return cudaGetLastError();
     }
     // grid.y holds at most 65535 (b, h) pairs per launch
@@ -584,7 +603,7 @@ cudaError_t launch_fp32_kernel(const AttnProblem &p, cudaStream_t stream) {
         AttnProblem part = p;
         part.bh_begin = p.bh_begin + begin;
         part.bh_count = p.bh_count - begin < 65535 ? p.bh_count - begin : 65535;
-        kern<<<dim3(p.nqt, part.bh_count), kF32Threads, smem, stream>>>(part, 0);
+        kern<<<dim3(p.nqt, part.bh_count), C::kWarps * 32, smem, stream>>>(part, 0);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
