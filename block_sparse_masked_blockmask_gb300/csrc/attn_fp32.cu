@@ -24,19 +24,19 @@
 // issue costs ~50 cycles whatever its width up to N = 64, so narrow S MMAs
 // leave the tensor cores idle).
 //
-// Design (one CTA per (batch, head, 128-row q tile), 448 threads at D = 64,
-// 480 at D = 128, where the producers move off the MMA issuer's
-// sub-partition; warp numbers below are those of D = 64):
+// Design (one CTA per (batch, head, 128-row q tile), 512 threads at D = 64,
+// 480 at D = 128; the producer warps are placed away from the MMA issuers'
+// sub-partitions, see F32Cfg; roles by group):
 //   warps 0-3   softmax, one thread per q row (TMEM lane = row); at the start
 //               they read their Q rows, split them and write Q1, Q2, Q3
 //               (bf16 pairs) into tensor memory, where the S MMAs read them
 //               as the A operand
-//   warps 4-7   K producers: read each chunk of 64 kv rows of K from global
+//   K group     four warps: read each chunk of 64 kv rows of K from global
 //               memory, split it and write the three parts into a
 //               shared-memory ring (rows of 64 bf16 per 128-byte swizzled
 //               atom, as a TMA load with 128-byte swizzle writes them); the
 //               loads of a chunk are issued before its slot is waited for
-//   warps 8-11  V producers: the same for V, in the same row layout, which
+//   V group     four warps: the same for V, in the same row layout, which
 //               the PV MMAs read as an MN-major B operand (no transpose)
 //   warp 12     one thread issues the MMAs; at D = 64 the PV MMAs only, and
 //   warp 13     one thread the S MMAs (the fixed ~50-cycle cost of an MMA
@@ -87,15 +87,15 @@ struct F32Cfg {
     // TMEM-traffic warp and a shared-memory-store warp).  D = 128: the
     // issuer (warp 12) shares its sub-partition only with softmax warp 0,
     // warps 4 and 8 stay idle, the producers run on warps 5-7, 9 (K) and
-    // 10, 11, 13, 14 (V).  D = 64: K on 4-7, V on 8-11, PV issuer 12,
-    // S issuer 13.
-    static constexpr int kWarps = D == 128 ? 15 : 14;
+    // 10, 11, 13, 14 (V).  D = 64: PV issuer 12 and S issuer 13 each beside
+    // one producer warp (V on 4, 5, 14, 15; K on 6, 7, 10, 11; 8 and 9 idle).
+    static constexpr int kWarps = D == 128 ? 15 : 16;
     __device__ static int k_index(int w) {
-        if (D == 64) return w >= 4 && w < 8 ? w - 4 : -1;
+        if (D == 64) return w == 6 || w == 7 ? w - 6 : w == 10 || w == 11 ? w - 8 : -1;
         return w >= 5 && w < 8 ? w - 5 : w == 9 ? 3 : -1;
     }
     __device__ static int v_index(int w) {
-        if (D == 64) return w >= 8 && w < 12 ? w - 8 : -1;
+        if (D == 64) return w == 14 || w == 15 ? w - 14 : w == 4 || w == 5 ? w - 2 : -1;
         return w == 10 || w == 11 ? w - 10 : w == 13 || w == 14 ? w - 11 : -1;
     }
     static constexpr int kUnits = KS * D / 8 / 128;        // 8-float units per producer thread per chunk
