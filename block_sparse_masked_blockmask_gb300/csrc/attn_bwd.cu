@@ -200,7 +200,7 @@ __device__ __forceinline__ void store_rows(float *dst, int row0, int len, int ta
 // dK, dV (fp32): CTA = 64 kv rows of one kv block; the q blocks come from the
 // transposed lists, each walked in two steps of 64 q rows.
 template <int D, int SCORE>
-__global__ void __launch_bounds__(kTThreads, 1) attn_bwd_dkdv_kernel(AttnProblem p, BwdArgs a) {
+__global__ void __launch_bounds__(kTThreads, D == 64 ? 2 : 1) attn_bwd_dkdv_kernel(AttnProblem p, BwdArgs a) {
     using C = TiledCfg<D>;
     extern __shared__ float4 smem4[];
     float *ks = reinterpret_cast<float *>(smem4), *vs = ks + C::kTile;   // owned
@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_bwd_dkdv_kernel(AttnProblem
 // dQ (fp32): CTA = 64 q rows of one q block; the kv tiles come from the kv
 // side of the BlockMask, as in the forward pass, each walked in two steps.
 template <int D, int SCORE>
-__global__ void __launch_bounds__(kTThreads, 1) attn_bwd_dq_kernel(AttnProblem p, BwdArgs a) {
+__global__ void __launch_bounds__(kTThreads, D == 64 ? 2 : 1) attn_bwd_dq_kernel(AttnProblem p, BwdArgs a) {
     using C = TiledCfg<D>;
     extern __shared__ float4 smem4[];
     float *qs = reinterpret_cast<float *>(smem4), *gs = qs + C::kTile;   // owned
