@@ -26,7 +26,9 @@
 // accumulates a 4 x (D / 16) block of its output rows over the 64 walked
 // rows; the FMAs are packed fp32x2 (fma.rn.f32x2, two per instruction).
 // Rows are padded by 4 floats, so the 16-byte loads of a quarter warp fall
-// in eight distinct bank groups.
+// in eight distinct bank groups.  At D = 64 two CTAs share an SM (at most
+// 128 registers a thread, 109 KB of shared memory each); at D = 128 one
+// (175 KB).
 #include "attn_bwd_tc.cuh"
 #include "bwd_internal.h"
 #include "ptx.cuh"
