@@ -41,11 +41,12 @@
 //   warp 12     one thread issues the MMAs; at D = 64 the PV MMAs only, and
 //   warp 13     one thread the S MMAs (the fixed ~50-cycle cost of an MMA
 //               issue on one thread overlaps the other's)
-// Tensor memory (512 columns): Q1 | Q2 | Q3 | O | S0 | P3_0 | S1 | P3_1.
-// S of chunk u + 1 is computed while the softmax works on chunk u; P1 and
-// P2 (bf16 pairs) overwrite their S in place, P3 has its own columns;
-// S(u + 2) is issued after PV(u) (one issuer: right behind it; two: once it
-// has completed).  The softmax keeps a reference
+// Tensor memory (512 columns): Q1 | Q2 | Q3 | O | S0 | P3_0 | S1 | P3_1
+// (| S2 | P3_2 at D = 64).  S of the next chunks is computed while the
+// softmax works on chunk u; P1 and P2 (bf16 pairs) overwrite their S in
+// place, P3 has its own columns; S(u + NB), NB the number of S buffers, is
+// issued after PV(u) (one issuer: right behind it; two: once it has
+// completed).  The softmax keeps a reference
 // maximum m and rescales O and l only when a chunk's maximum exceeds m by
 // more than kF32RescaleNats (then waiting for PV(u - 1)); out = O / l and
 // lse = m + ln l do not depend on which m was used.  The kv tiles of the
@@ -81,6 +82,11 @@ struct F32Cfg {
     // MMAs keep the tensor pipe busy and S(u + 2) is better issued right
     // behind PV(u) than after a wait for its completion
     static constexpr bool kTwoIssuers = D == 64;
+    // S/P buffers in TMEM: with two issuers S(j) must wait for PV(j - NB)
+    // to complete, so each buffer is a chain S -> softmax -> PV -> S; three
+    // buffers at D = 64 run three such chains at once (TMEM: 448 columns),
+    // two at D = 128 (512)
+    static constexpr int kSBufs = D == 64 ? 3 : 2;
     // Warp roles.  Warps are dealt to the four sub-partitions round robin
     // (warp w on sub-partition w % 4), and a thread issuing MMAs slows down
     // when its sub-partition is busy (~50 cycles an MMA alone, ~75 beside a
@@ -111,13 +117,15 @@ struct F32Cfg {
     __host__ __device__ static constexpr uint32_t p_col(int i, int j) {
         return j < 2 ? s_col(i) + (uint32_t)j * (KS / 2) : s_col(i) + KS;
     }
-    static_assert(5 * D / 2 + 3 * KS <= (int)kF32TmemCols, "tensor memory");
+    static_assert(5 * D / 2 + kSBufs * (KS + KS / 2) <= (int)kF32TmemCols, "tensor memory");
     static_assert(kMiscOff % 1024 == 0, "ring alignment");
 };
 
 struct F32Misc {
     uint64_t q_ready, k_full[3], k_empty[3], v_full[3], v_empty[3];
-    uint64_t s_full[2], p_full[2], pv_done, o_full, drain;  // drain: one commit per issuing thread
+    // per S/P buffer; pv_done[b]: the PV MMAs that read buffer b, so that
+    // every parity wait on it is at most one phase behind
+    uint64_t s_full[3], p_full[3], pv_done[3], o_full, drain;  // drain: one commit per issuing thread
     uint32_t tmem_base;
     int abort;
     int n;  // 128-tiles listed for this q tile
@@ -261,11 +269,11 @@ __global__ void __launch_bounds__(kF32MaxThreads, 1) attn_fp32_kernel(AttnProble
             mbar_init(&ms.v_full[s], 4);
             mbar_init(&ms.v_empty[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::kSBufs; ++i) {
             mbar_init(&ms.s_full[i], 1);
             mbar_init(&ms.p_full[i], 4);
+            mbar_init(&ms.pv_done[i], 1);
         }
-        mbar_init(&ms.pv_done, 1);
         mbar_init(&ms.o_full, 1);
         mbar_init(&ms.drain, C::kTwoIssuers ? 2 : 1);
         ms.abort = 0;
@@ -334,7 +342,7 @@ __global__ void __launch_bounds__(kF32MaxThreads, 1) attn_fp32_kernel(AttnProble
                 if (!mbar_wait(&ms.k_full[s], (uint32_t)(j / C::kSlots) & 1u, abort_flag)) return false;
                 tc_fence_after_sync();
                 const uint32_t kd = smem_desc_lo(smem_u32(smem + C::kK0 + s * C::kSlot), 16);
-                const uint32_t d = tmem + C::s_col(j & 1);
+                const uint32_t d = tmem + C::s_col(j % C::kSBufs);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = ((k / 4) * C::kAtom + (k % 4) * 32) >> 4;
@@ -344,15 +352,15 @@ __global__ void __launch_bounds__(kF32MaxThreads, 1) attn_fp32_kernel(AttnProble
                                        idesc_s, (k > 0 || t > 0) ? 1u : 0u);
                 }
                 mma_commit(&ms.k_empty[s]);
-                mma_commit(&ms.s_full[j & 1]);
+                mma_commit(&ms.s_full[j % C::kSBufs]);
                 return true;
             };
             // O += sum of the part products P_a V_b; V is MN-major (kv rows of
             // 64 head-dim elements, the 64-wide halves kAtom apart), K steps
             // of 16 kv rows = 2048 bytes
             auto issue_pv = [&](int u) -> bool {
-                const int pb = u & 1, s = u % C::kSlots;
-                if (!mbar_wait(&ms.p_full[pb], (uint32_t)(u >> 1) & 1u, abort_flag) ||
+                const int pb = u % C::kSBufs, s = u % C::kSlots;
+                if (!mbar_wait(&ms.p_full[pb], (uint32_t)(u / C::kSBufs) & 1u, abort_flag) ||
                     !mbar_wait(&ms.v_full[s], (uint32_t)(u / C::kSlots) & 1u, abort_flag))
                     return false;
                 tc_fence_after_sync();
@@ -366,26 +374,26 @@ __global__ void __launch_bounds__(kF32MaxThreads, 1) attn_fp32_kernel(AttnProble
                                        (u > 0 || k > 0 || t > 0) ? 1u : 0u);
                 }
                 mma_commit(&ms.v_empty[s]);
-                mma_commit(&ms.pv_done);
+                mma_commit(&ms.pv_done[pb]);
                 return true;
             };
             bool ok = true;
             if (!C::kTwoIssuers) {
-                // one issuer: S(0), S(1), then PV(u) and S(u + 2) (MMAs of
-                // one thread run in order, so S(u + 2) follows PV(u))
+                // one issuer: S of the first kSBufs chunks, then PV(u) and
+                // S(u + kSBufs) (MMAs of one thread run in order, so
+                // S(u + kSBufs) follows PV(u), which read the same buffer)
                 ok = mbar_wait(&ms.q_ready, 0, abort_flag);
-                if (ok) {
-                    tc_fence_after_sync();
-                    ok = issue_s(0);
-                }
-                if (ok && nsub > 1) ok = issue_s(1);
-                for (int u = 0; ok && u < nsub; ++u) ok = issue_pv(u) && (u + 2 >= nsub || issue_s(u + 2));
+                if (ok) tc_fence_after_sync();
+                for (int j = 0; ok && j < min(nsub, C::kSBufs); ++j) ok = issue_s(j);
+                for (int u = 0; ok && u < nsub; ++u)
+                    ok = issue_pv(u) && (u + C::kSBufs >= nsub || issue_s(u + C::kSBufs));
                 if (ok) mma_commit(&ms.o_full);
             } else if (warp == kF32SWarp) {
-                // S(j) overwrites the buffer PV(j - 2) read its P from
+                // S(j) overwrites the buffer PV(j - kSBufs) read its P from
                 ok = mbar_wait(&ms.q_ready, 0, abort_flag);
                 for (int j = 0; ok && j < nsub; ++j) {
-                    if (j >= 2 && !mbar_wait(&ms.pv_done, (uint32_t)(j - 2) & 1u, abort_flag)) {
+                    if (j >= C::kSBufs &&
+                        !mbar_wait(&ms.pv_done[j % C::kSBufs], (uint32_t)(j / C::kSBufs - 1) & 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -452,11 +460,11 @@ __global__ void __launch_bounds__(kF32MaxThreads, 1) attn_fp32_kernel(AttnProble
         }
         float m = -INFINITY, m_true = -INFINITY, l = 0.f;
         for (int u = 0; u < nsub; ++u) {
-            const int pb = u & 1;
+            const int pb = u % C::kSBufs;
             const uint32_t e = ms.list[u / C::kSub];
             const bool full = (e >> 16) & 1u;
             const int kv0 = (int)(e & 0xFFFFu) * kBlock + (u % C::kSub) * KS;
-            if (!f32_warp_wait(&ms.s_full[pb], (uint32_t)(u >> 1) & 1u, abort_flag)) {
+            if (!f32_warp_wait(&ms.s_full[pb], (uint32_t)(u / C::kSBufs) & 1u, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -497,7 +505,8 @@ __global__ void __launch_bounds__(kF32MaxThreads, 1) attn_fp32_kernel(AttnProble
                 const float alpha = grow ? expf(m - m_new) : 1.f;  // 0 when m was -inf
                 if (u > 0) {
                     // PV(u - 1) has completed before O is rescaled in place
-                    if (!f32_warp_wait(&ms.pv_done, (uint32_t)(u - 1) & 1u, abort_flag)) {
+                    const int pv = (u - 1) % C::kSBufs;  // PV(u - 1) and, in order, every PV before it
+                    if (!f32_warp_wait(&ms.pv_done[pv], (uint32_t)((u - 1) / C::kSBufs) & 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
