@@ -94,6 +94,24 @@ def test_single_key_rows_return_v(dtype, score):
     assert np.max(np.abs(lse - diag)) <= TOL[dtype][1]
 
 
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("mask", [W.MASK_CAUSAL, W.MASK_ALL])
+@pytest.mark.parametrize("score,param", [(W.SCORE_IDENTITY, 0.0), (W.SCORE_ALIBI, 0.0), (W.SCORE_SOFTCAP, 20.0)],
+                         ids=lambda x: str(x))
+def test_fp32_accuracy_well_inside_tolerance(D, mask, score, param):
+    # The float32 path splits every operand into three bf16 parts (six MMAs
+    # per product, relative error ~2^-23 per product): out and lse land
+    # within 1e-5 of float64, ten times inside the 1e-4 tolerance.  A single
+    # TF32 pass (10 stored mantissa bits) would put score errors near
+    # 2^-11 |q||k| ~ 1e-3 on these N(0, 1) rows and fail this bound.
+    B, H, S = 1, 2, 1024
+    q, k, v = W.draw_qkv(B, H, S, D, seed=13, dtype="fp32")
+    scale = 1.0 / np.sqrt(D)
+    out, lse, _ = run_attention(q, k, v, mask, score, scale, "fp32", score_param=param)
+    ref_out, ref_lse = oracle.attention(q, k, v, mask, score, scale, score_param=param)
+    compare(out, lse, ref_out, ref_lse, "fp32", "fp32 accuracy", tol=(1e-5, 1e-5))
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("direction", [1.0, -1.0], ids=["rising", "falling"])
 @pytest.mark.parametrize("mask", [W.MASK_CAUSAL, W.MASK_ALL])
