@@ -1,0 +1,441 @@
+// dK and dV of the block-sparse attention for float32 inputs at head dim 64
+// on sm_103a tensor cores, with float32 accuracy kept by the three-way bf16
+// split of the float32 forward (bf16x3.cuh): every operand x = x1 + x2 + x3
+// and each product takes the six part products a1 b1 + a1 b2 + a2 b1 +
+// a1 b3 + a2 b2 + a3 b1, accumulated in float32 in tensor memory.
+//
+// What it computes is the dk and dv outputs of the flex_attention_backward
+// op ("[Inductor][Flex Attention] Add Subtiling Option for Alpha Scaling",
+// PyTorch PR #167356, test diffs), for one 128-row kv block j, walking the q
+// blocks of the q side of the BlockMask in chunks of 64 q rows i:
+//   S^T  = K_j Q_i^T,  dP^T = V_j dO_i^T              (SS MMAs)
+//   P^T  = exp(score_mod(scale S^T) - lse_i) where mask_mod holds, else 0
+//   dS^T = scale P^T (dP^T - delta_i) score_mod'      (elementwise, float32)
+//   dV_j += P^T dO_i,  dK_j += dS^T Q_i               (TS MMAs: P^T, dS^T
+//                                                      read from TMEM)
+// Roles (480 threads, one CTA per kv block):
+//   warps 0-3   elementwise, one thread per kv row (TMEM lane = row)
+//   Q group     warps 5-7, 9: split the resident K tile, then each Q chunk
+//               and its lse into a two-stage ring
+//   dO group    warps 10, 11, 13, 14: the resident V tile, each dO chunk and
+//               its delta
+//   warp 12     one thread issues every MMA (warps 4 and 8 stay idle, so
+//               that the issuer shares its sub-partition with warp 0 only)
+// Tensor memory (512 columns): dV | dK | two buffers of S^T (64) | dP^T (64)
+// | 64 more.  P^T and dS^T are split into bf16 parts over the columns they
+// were computed from, a half of the 64 q columns at a time: the parts of
+// columns 32h .. 32h + 31 take S^T (dP^T) columns 32h .. 32h + 31 and 16 of
+// the spare columns, so each half only overwrites columns it has already
+// read.  Every wait is bounded; on timeout the CTA records
+// FLEX_ERR_DEVICE_TIMEOUT, drains its MMAs, frees TMEM and exits.
+#pragma once
+
+#include <cfloat>
+
+#include "bf16x3.cuh"
+#include "flex_internal.h"
+#include "ptx.cuh"
+#include "tilelist.cuh"
+
+namespace flex {
+
+// q tiles of a kv block the kernel walks on chip (longer q sides take the
+// CUDA-core kernel)
+constexpr int kBwdF32TcMaxQTiles = 2048;
+
+struct BwdF32TcArgs {
+    const float *dout;                               // contiguous [B, H, q_len, 64]
+    const float *delta;                              // [B, H, q_len]
+    const int32_t *q_num, *q_idx, *fq_num, *fq_idx;  // q side of the BlockMask
+    float *dk, *dv;                                  // contiguous [B, H, kv_len, 64]
+};
+
+namespace bwdf32 {
+
+constexpr int D = 64;
+constexpr int kKvRows = 128;     // owned kv rows (MMA M)
+constexpr int kQc = 64;          // q rows per chunk (MMA N of S^T and dP^T, K of dV and dK)
+constexpr int kThreads = 15 * 32;
+constexpr int kMmaWarp = 12;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// shared memory: K parts | V parts | two ring stages (Q parts, dO parts, lse, delta) | misc
+constexpr uint32_t kOwnPart = kKvRows * D * 2;   // 16 KB: one bf16 part of a 128 x 64 tile
+constexpr uint32_t kChunkPart = kQc * D * 2;     // 8 KB: one bf16 part of a 64 x 64 chunk
+constexpr uint32_t kK0 = 0, kV0 = 3 * kOwnPart;
+constexpr uint32_t kStage0 = 6 * kOwnPart;
+constexpr uint32_t kStQ = 0, kStDo = 3 * kChunkPart, kStLse = 6 * kChunkPart, kStDelta = kStLse + kQc * 4;
+constexpr uint32_t kStageBytes = 6 * kChunkPart + 1024;  // parts, lse and delta, 1024-aligned
+constexpr uint32_t kMiscOff = kStage0 + 2 * kStageBytes;
+
+// tensor memory columns
+constexpr uint32_t kDv = 0, kDk = 64;
+__host__ __device__ constexpr uint32_t buf_col(int b) { return 128u + 192u * (uint32_t)b; }
+// A-operand column of part `part` (0..2) of P^T (dS: + 64 and + 32 in the
+// spare columns) for K step k (16 q columns: half k / 2, 8 words into it when k is odd)
+__host__ __device__ constexpr uint32_t p_part_col(int b, int part, int k) {
+    return part < 2 ? buf_col(b) + 32u * (uint32_t)(k / 2) + 16u * (uint32_t)part + 8u * (uint32_t)(k % 2)
+                    : buf_col(b) + 128u + 16u * (uint32_t)(k / 2) + 8u * (uint32_t)(k % 2);
+}
+__host__ __device__ constexpr uint32_t ds_part_col(int b, int part, int k) {
+    return part < 2 ? buf_col(b) + 64u + 32u * (uint32_t)(k / 2) + 16u * (uint32_t)part + 8u * (uint32_t)(k % 2)
+                    : buf_col(b) + 160u + 16u * (uint32_t)(k / 2) + 8u * (uint32_t)(k % 2);
+}
+static_assert(buf_col(1) + 192 == kTmemCols, "tensor memory");
+
+struct Misc {
+    uint64_t kv_ready, st_full[2], st_empty[2], s_full[2], p_full[2], acc_full, drain;
+    uint32_t tmem_base;
+    int abort;
+    int ntiles;  // q tiles listed for this kv block
+    int pad;
+    alignas(16) uint32_t flags[kBwdF32TcMaxQTiles];  // listed / full count per q tile (tilelist.cuh)
+    alignas(16) uint32_t list[kBwdF32TcMaxQTiles];   // q tile | full << 16, ascending
+};
+constexpr size_t kSmemBytes = kMiscOff + sizeof(Misc) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+// Producer group of four warps (thread lt in 0..127): the rows r0 .. r0 +
+// rows - 1 of a [.., len, 64] float32 tensor, split into three bf16 parts at
+// dst + j * part_bytes in 128-byte swizzled rows (rows past len are zeros).
+// Thread lt takes units i = lt + 128 u: row i / 8, 8 floats at column 8 (i % 8).
+template <int ROWS>
+__device__ __forceinline__ void load_split(uint8_t *dst, uint32_t part_bytes, const float *src, int64_t rs, int r0,
+                                           int len, int lt) {
+    constexpr int kUnits = ROWS * 8 / 128;
+    float4 x[2 * kUnits];
+#pragma unroll
+    for (int u = 0; u < kUnits; ++u) {
+        const int i = lt + 128 * u, r = i / 8, c = i % 8;
+        const bool in = r0 + r < len;
+        const float4 *p = reinterpret_cast<const float4 *>(src + (int64_t)(in ? r0 + r : 0) * rs) + 2 * c;
+        x[2 * u] = in ? __ldg(p) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[2 * u + 1] = in ? __ldg(p + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnits; ++u) {
+        const int i = lt + 128 * u, r = i / 8, c = i % 8;
+        uint4 p1, p2, p3;
+        split3(x[2 * u].x, x[2 * u].y, p1.x, p2.x, p3.x);
+        split3(x[2 * u].z, x[2 * u].w, p1.y, p2.y, p3.y);
+        split3(x[2 * u + 1].x, x[2 * u + 1].y, p1.z, p2.z, p3.z);
+        split3(x[2 * u + 1].z, x[2 * u + 1].w, p1.w, p2.w, p3.w);
+        const uint32_t off = sw128_chunk(r, c, ROWS * 128);
+        *reinterpret_cast<uint4 *>(dst + off) = p1;
+        *reinterpret_cast<uint4 *>(dst + part_bytes + off) = p2;
+        *reinterpret_cast<uint4 *>(dst + 2 * part_bytes + off) = p3;
+    }
+}
+
+__device__ __forceinline__ void fail(Misc &ms, int *status) {
+    *reinterpret_cast<volatile int *>(&ms.abort) = 1;
+    atomicCAS(status, 0, kDeviceTimeout);
+}
+
+// warp -> index in the Q group (5, 6, 7, 9) or the dO group (10, 11, 13, 14), else -1
+__device__ __forceinline__ int q_index(int w) { return w >= 5 && w < 8 ? w - 5 : w == 9 ? 3 : -1; }
+__device__ __forceinline__ int do_index(int w) { return w == 10 || w == 11 ? w - 10 : w == 13 || w == 14 ? w - 11 : -1; }
+
+// score_mod at the scaled score t, and its derivative d score_mod / dt
+template <int SCORE>
+__device__ __forceinline__ float score_t(float cap, float t, float slope, int q, int kv, float &grad) {
+    if constexpr (SCORE == FLEX_SCORE_SOFTCAP) {
+        const float u = tanhf(t / cap);
+        grad = 1.f - u * u;
+        return cap * u;
+    }
+    grad = 1.f;
+    if constexpr (SCORE == FLEX_SCORE_ALIBI) return t - slope * (float)(q - kv);
+    return t;
+}
+
+template <int SCORE>
+__global__ void __launch_bounds__(16 * 32, 1) dkdv_kernel(AttnProblem p, BwdF32TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Misc &ms = *reinterpret_cast<Misc *>(smem + kMiscOff);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int kvb = blockIdx.x;
+    const int bh = p.bh_begin + (int)blockIdx.y, h = bh % p.H, b = bh / p.H;
+    const int kv0 = kvb * kBlock;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&ms.kv_ready, 8);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ms.st_full[i], 8);
+            mbar_init(&ms.st_empty[i], 1);
+            mbar_init(&ms.s_full[i], 1);
+            mbar_init(&ms.p_full[i], 4);
+        }
+        mbar_init(&ms.acc_full, 1);
+        mbar_init(&ms.drain, 1);
+        ms.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        // the q side of the BlockMask (any block sizes) read as 128-tiles:
+        // counts clamped, malformed entries dropped
+        const TileLists lists{a.q_num, a.q_idx, a.fq_num, a.fq_idx, p.nkvb, p.nqb, p.kv_block, p.q_block, p.nqt};
+        for (int i = lane; i < p.nqt; i += 32) ms.flags[i] = 0u;
+        __syncwarp();
+        tl_mark_warp(lists, bh, kvb, 0, ms.flags, 0, p.nqt, lane);
+        __syncwarp();
+        const uint32_t expect = tl_expect(lists);
+        const unsigned lt = (1u << lane) - 1u;
+        int cnt = 0;
+        for (int base = 0; base < p.nqt; base += 32) {
+            const int i = base + lane;
+            const uint32_t w = i < p.nqt ? ms.flags[i] : 0u;
+            const bool on = tl_listed(w, 0);
+            const unsigned bal = __ballot_sync(0xffffffffu, on);
+            if (on) ms.list[cnt + __popc(bal & lt)] = (uint32_t)i | (tl_full(expect, w, 0) ? (1u << 16) : 0u);
+            cnt += __popc(bal);
+        }
+        if (lane == 0) ms.ntiles = cnt;
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&ms.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = ms.tmem_base;
+    volatile int *abort_flag = &ms.abort;
+    const int nchunk = 2 * ms.ntiles;  // two 64-row chunks per q tile
+    auto chunk_q0 = [&](int j) { return (int)(ms.list[j / 2] & 0xFFFFu) * kBlock + (j % 2) * kQc; };
+    const int qi = q_index(warp), di = do_index(warp);
+
+    if (qi >= 0 || di >= 0) {
+        // ----------------------------------------------------------- producers
+        const int lt = 32 * (qi >= 0 ? qi : di) + lane;
+        if (qi >= 0) {
+            const float *kbase = static_cast<const float *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
+            load_split<kKvRows>(smem + kK0, kOwnPart, kbase, p.k_stride[2], kv0, p.kv_len, lt);
+        } else {
+            const float *vbase = static_cast<const float *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1];
+            load_split<kKvRows>(smem + kV0, kOwnPart, vbase, p.v_stride[2], kv0, p.kv_len, lt);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms.kv_ready);
+        const float *qbase = static_cast<const float *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1];
+        const float *gbase = a.dout + (int64_t)bh * p.q_len * D;
+        const float *lbase = p.lse + (int64_t)bh * p.q_len;
+        const float *dbase = a.delta + (int64_t)bh * p.q_len;
+        bool ok = true;
+        for (int j = 0; j < nchunk; ++j) {
+            const int s = j & 1;
+            if (j >= 2 && !f32_warp_wait(&ms.st_empty[s], (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            uint8_t *st = smem + kStage0 + s * kStageBytes;
+            const int q0 = chunk_q0(j);
+            if (qi >= 0) {
+                load_split<kQc>(st + kStQ, kChunkPart, qbase, p.q_stride[2], q0, p.q_len, lt);
+                if (lt < kQc) {
+                    const int q = q0 + lt;
+                    reinterpret_cast<float *>(st + kStLse)[lt] = q < p.q_len ? lbase[q] : -INFINITY;
+                }
+            } else {
+                load_split<kQc>(st + kStDo, kChunkPart, gbase, D, q0, p.q_len, lt);
+                if (lt < kQc) {
+                    const int q = q0 + lt;
+                    reinterpret_cast<float *>(st + kStDelta)[lt] = q < p.q_len ? dbase[q] : 0.f;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.st_full[s]);
+        }
+        if (!ok) fail(ms, p.status);
+    } else if (warp == kMmaWarp) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0 && nchunk > 0) {
+            constexpr uint32_t kHi = smem_desc_hi_sw128(1024);
+            constexpr uint32_t idesc_kmaj = idesc_bf16_f32(128, kQc, 0, 0);  // S^T, dP^T: B K-major
+            constexpr uint32_t idesc_mn = idesc_bf16_f32(128, D, 0, 1);      // dV, dK: B MN-major
+            // the six part products t: (A part, B part) = (0,0) (0,1) (1,0) (0,2) (1,1) (2,0)
+            auto pa = [](int t) { return t == 2 || t == 4 ? 1 : t == 5 ? 2 : 0; };
+            auto pbp = [](int t) { return t == 1 || t == 4 ? 1 : t == 3 ? 2 : 0; };
+            const uint32_t kd = smem_desc_lo(smem_u32(smem + kK0), 16), vd = smem_desc_lo(smem_u32(smem + kV0), 16);
+            // S^T(j) and dP^T(j) into buffer j % 2 (K steps of 16 head dims = 32 bytes)
+            auto issue_sdp = [&](int j) -> bool {
+                const int s = j & 1;
+                if (!mbar_wait(&ms.st_full[s], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+                const uint32_t st = smem_u32(smem + kStage0 + s * kStageBytes);
+                const uint32_t qd = smem_desc_lo(st + kStQ, 16), gd = smem_desc_lo(st + kStDo, 16);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t) {
+                        const uint32_t acc = (k > 0 || t > 0) ? 1u : 0u;
+                        mma_ss_lo<kHi, kHi>(tmem + buf_col(s), kd + ((pa(t) * kOwnPart + k * 32) >> 4),
+                                            qd + ((pbp(t) * kChunkPart + k * 32) >> 4), idesc_kmaj, acc);
+                        mma_ss_lo<kHi, kHi>(tmem + buf_col(s) + 64, vd + ((pa(t) * kOwnPart + k * 32) >> 4),
+                                            gd + ((pbp(t) * kChunkPart + k * 32) >> 4), idesc_kmaj, acc);
+                    }
+                mma_commit(&ms.s_full[s]);
+                return true;
+            };
+            // dV += P^T dO(j), dK += dS^T Q(j): A from TMEM, B MN-major (rows
+            // of 64 head dims, K steps of 16 q rows = 2048 bytes)
+            auto issue_acc = [&](int j) -> bool {
+                const int s = j & 1;
+                if (!mbar_wait(&ms.p_full[s], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+                const uint32_t st = smem_u32(smem + kStage0 + s * kStageBytes);
+                const uint32_t qm = smem_desc_lo(st + kStQ, kChunkPart), gm = smem_desc_lo(st + kStDo, kChunkPart);
+#pragma unroll
+                for (int k = 0; k < kQc / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t) {
+                        const uint32_t acc = (j > 0 || k > 0 || t > 0) ? 1u : 0u;
+                        mma_ts_lo<kHi>(tmem + kDv, tmem + p_part_col(s, pa(t), k),
+                                       gm + ((pbp(t) * kChunkPart + k * 2048) >> 4), idesc_mn, acc);
+                        mma_ts_lo<kHi>(tmem + kDk, tmem + ds_part_col(s, pa(t), k),
+                                       qm + ((pbp(t) * kChunkPart + k * 2048) >> 4), idesc_mn, acc);
+                    }
+                mma_commit(&ms.st_empty[s]);
+                return true;
+            };
+            bool ok = mbar_wait(&ms.kv_ready, 0, abort_flag);
+            if (ok) tc_fence_after_sync();
+            for (int j = 0; ok && j < min(nchunk, 2); ++j) ok = issue_sdp(j);
+            // S^T(j + 2) reuses the buffer dV(j), dK(j) read: MMAs of one thread run in order
+            for (int j = 0; ok && j < nchunk; ++j) ok = issue_acc(j) && (j + 2 >= nchunk || issue_sdp(j + 2));
+            if (ok) mma_commit(&ms.acc_full);
+            if (!ok) fail(ms, p.status);
+            mma_commit(&ms.drain);  // every MMA issued above completes before TMEM is freed
+            int never = 0;
+            (void)mbar_wait(&ms.drain, 0, &never);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ---------------------------------------------------------- elementwise
+        const int kv = kv0 + (int)threadIdx.x;
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        const float slope = SCORE == FLEX_SCORE_ALIBI ? exp2f(-8.f * (float)(h + 1) / (float)p.H) : 0.f;
+        const float scale = p.scale;
+        bool ok = true;
+        for (int j = 0; j < nchunk; ++j) {
+            const int s = j & 1;
+            const bool full = (ms.list[j / 2] >> 16) & 1u;
+            const int q0 = chunk_q0(j);
+            // S^T and dP^T of the chunk are in TMEM; its lse and delta (written
+            // by the producers) are read after their own barrier
+            if (!f32_warp_wait(&ms.s_full[s], (uint32_t)(j >> 1) & 1u, abort_flag) ||
+                !f32_warp_wait(&ms.st_full[s], (uint32_t)(j >> 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const float *lse_s = reinterpret_cast<const float *>(smem + kStage0 + s * kStageBytes + kStLse);
+            const float *dl_s = reinterpret_cast<const float *>(smem + kStage0 + s * kStageBytes + kStDelta);
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                uint32_t sr[32], dr[32];
+                f32_ld32(trow + buf_col(s) + 32 * half, sr);
+                f32_ld32(trow + buf_col(s) + 64 + 32 * half, dr);
+                float pv[32], dsv[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int q = q0 + 32 * half + c;
+                    const float lse = lse_s[32 * half + c];
+                    const bool keep = lse != -INFINITY && (full || (kv < p.kv_len && mask_mod(p.mask, b, q, kv)));
+                    float grad;
+                    const float x = score_t<SCORE>(p.score_param, __uint_as_float(sr[c]) * scale, slope, q, kv, grad);
+                    const float pr = keep ? ex2_approx(fmaf(x, kLog2e, -lse * kLog2e)) : 0.f;
+                    pv[c] = pr;
+                    dsv[c] = keep ? scale * pr * (__uint_as_float(dr[c]) - dl_s[32 * half + c]) * grad : 0.f;
+                }
+                uint32_t w1[16], w2[16], w3[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) split3(pv[2 * c], pv[2 * c + 1], w1[c], w2[c], w3[c]);
+                // over S^T columns 32 half .. 32 half + 31, all read above
+                tmem_st16(trow + buf_col(s) + 32 * half, w1);
+                tmem_st16(trow + buf_col(s) + 32 * half + 16, w2);
+                tmem_st16(trow + buf_col(s) + 128 + 16 * half, w3);
+#pragma unroll
+                for (int c = 0; c < 16; ++c) split3(dsv[2 * c], dsv[2 * c + 1], w1[c], w2[c], w3[c]);
+                tmem_st16(trow + buf_col(s) + 64 + 32 * half, w1);
+                tmem_st16(trow + buf_col(s) + 64 + 32 * half + 16, w2);
+                tmem_st16(trow + buf_col(s) + 160 + 16 * half, w3);
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.p_full[s]);
+        }
+        // ------------------------------------------------------------ epilogue
+        const bool have = ok && nchunk > 0;
+        if (have && !f32_warp_wait(&ms.acc_full, 0, abort_flag)) ok = false;
+        if (!ok) fail(ms, p.status);
+        if (ok) {
+            tc_fence_after_sync();
+            const int64_t orow = (int64_t)bh * p.kv_len + (kv < p.kv_len ? kv : 0);
+#pragma unroll 1
+            for (int o = 0; o < 2; ++o) {  // dV, then dK
+                float *dst = (o ? a.dk : a.dv) + orow * D;
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 32) {  // every lane takes the warp-collective loads
+                    uint32_t r[32];
+                    if (have) {
+                        f32_ld32(trow + (o ? kDk : kDv) + c0, r);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) r[c] = 0u;
+                    }
+                    if (kv < p.kv_len) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 4)
+                            *reinterpret_cast<float4 *>(dst + c0 + c) =
+                                make_float4(__uint_as_float(r[c]), __uint_as_float(r[c + 1]),
+                                            __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]));
+                    }
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace bwdf32
+
+// dK and dV of fp32 inputs at D = 64 on the tensor cores (p.D == 64; p.nqt
+// <= kBwdF32TcMaxQTiles).
+inline cudaError_t launch_bwd_fp32_tc_dkdv(const AttnProblem &p, const BwdF32TcArgs &a, cudaStream_t stream) {
+    using namespace bwdf32;
+    auto pick = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        for (int begin = 0; begin < p.B * p.H; begin += 65535) {
+            AttnProblem part = p;
+            part.bh_begin = begin;
+            const int count = p.B * p.H - begin < 65535 ? p.B * p.H - begin : 65535;
+            kern<<<dim3(p.nkvt, count), kThreads, kSmemBytes, stream>>>(part, a);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    };
+    switch (p.score_kind) {
+        case FLEX_SCORE_SOFTCAP:
+            return pick(dkdv_kernel<FLEX_SCORE_SOFTCAP>);
+        case FLEX_SCORE_ALIBI:
+            return pick(dkdv_kernel<FLEX_SCORE_ALIBI>);
+        default:
+            return pick(dkdv_kernel<FLEX_SCORE_IDENTITY>);
+    }
+}
+
+}  // namespace flex
