@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(128) block_mask_transpose_kernel(const int32_t
 }
 
 template <int D, int SCORE>
-cudaError_t launch_bwd_fp32_score(const AttnProblem &p, const BwdArgs &a, bool dkdv, cudaStream_t stream) {
+cudaError_t launch_bwd_fp32_score(const AttnProblem &p, const BwdArgs &a, bool dkdv, bool dq, cudaStream_t stream) {
     using C = TiledCfg<D>;
     cudaError_t e =
         cudaFuncSetAttribute(attn_bwd_dkdv_kernel<D, SCORE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
@@ -440,33 +440,36 @@ cudaError_t launch_bwd_fp32_score(const AttnProblem &p, const BwdArgs &a, bool d
             attn_bwd_dkdv_kernel<D, SCORE><<<dim3(2 * p.nkvt, count), kTThreads, C::kSmem, stream>>>(part, a);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
-        attn_bwd_dq_kernel<D, SCORE><<<dim3(2 * p.nqt, count), kTThreads, C::kSmem, stream>>>(part, a);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (dq) {
+            attn_bwd_dq_kernel<D, SCORE><<<dim3(2 * p.nqt, count), kTThreads, C::kSmem, stream>>>(part, a);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
     }
     return cudaSuccess;
 }
 
-// fp32: delta, then dK/dV (at D = 64 on the tensor cores, three-way bf16
-// split; else the register-tiled kernel) and dQ (register-tiled).
+// fp32: delta, then dK/dV and dQ: at D = 64 on the tensor cores (three-way
+// bf16 split; dK/dV up to kBwdF32TcMaxQTiles q tiles), else the
+// register-tiled CUDA-core kernels.
 template <int D>
 cudaError_t launch_bwd_fp32(const AttnProblem &p, const BwdArgs &a, cudaStream_t stream) {
     const int64_t rows = (int64_t)p.B * p.H * p.q_len;
     attn_bwd_delta_kernel<D, float><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, stream>>>(p, a, rows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const bool tc = D == 64 && p.nqt <= kBwdF32TcMaxQTiles;
-    if (tc) {
-        const BwdF32TcArgs ta{static_cast<const float *>(a.dout), a.delta, a.q_num, a.q_idx, a.fq_num, a.fq_idx,
-                              static_cast<float *>(a.dk), static_cast<float *>(a.dv)};
-        if ((e = launch_bwd_fp32_tc_dkdv(p, ta, stream)) != cudaSuccess) return e;
-    }
+    const bool tc_dkdv = D == 64 && p.nqt <= kBwdF32TcMaxQTiles, tc_dq = D == 64;
+    const BwdF32TcArgs ta{static_cast<const float *>(a.dout), a.delta, a.q_num, a.q_idx, a.fq_num, a.fq_idx,
+                          static_cast<float *>(a.dk), static_cast<float *>(a.dv), static_cast<float *>(a.dq)};
+    if (tc_dkdv && (e = launch_bwd_fp32_tc_dkdv(p, ta, stream)) != cudaSuccess) return e;
+    if (tc_dq && (e = launch_bwd_fp32_tc_dq(p, ta, stream)) != cudaSuccess) return e;
+    if (tc_dkdv && tc_dq) return cudaSuccess;
     switch (p.score_kind) {
         case FLEX_SCORE_SOFTCAP:
-            return launch_bwd_fp32_score<D, FLEX_SCORE_SOFTCAP>(p, a, !tc, stream);
+            return launch_bwd_fp32_score<D, FLEX_SCORE_SOFTCAP>(p, a, !tc_dkdv, !tc_dq, stream);
         case FLEX_SCORE_ALIBI:
-            return launch_bwd_fp32_score<D, FLEX_SCORE_ALIBI>(p, a, !tc, stream);
+            return launch_bwd_fp32_score<D, FLEX_SCORE_ALIBI>(p, a, !tc_dkdv, !tc_dq, stream);
         default:
-            return launch_bwd_fp32_score<D, FLEX_SCORE_IDENTITY>(p, a, !tc, stream);
+            return launch_bwd_fp32_score<D, FLEX_SCORE_IDENTITY>(p, a, !tc_dkdv, !tc_dq, stream);
     }
 }
 

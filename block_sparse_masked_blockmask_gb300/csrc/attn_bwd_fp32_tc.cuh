@@ -1,5 +1,5 @@
-// dK and dV of the block-sparse attention for float32 inputs at head dim 64
-// on sm_103a tensor cores, with float32 accuracy kept by the three-way bf16
+// dK, dV and dQ of the block-sparse attention for float32 inputs at head dim
+// 64 on sm_103a tensor cores, with float32 accuracy kept by the three-way bf16
 // split of the float32 forward (bf16x3.cuh): every operand x = x1 + x2 + x3
 // and each product takes the six part products a1 b1 + a1 b2 + a2 b1 +
 // a1 b3 + a2 b2 + a3 b1, accumulated in float32 in tensor memory.
@@ -13,7 +13,11 @@
 //   dS^T = scale P^T (dP^T - delta_i) score_mod'      (elementwise, float32)
 //   dV_j += P^T dO_i,  dK_j += dS^T Q_i               (TS MMAs: P^T, dS^T
 //                                                      read from TMEM)
-// Roles (480 threads, one CTA per kv block):
+// and, in a second kernel for one 128-row q block i walking the kv side in
+// chunks of 64 kv rows j, S = Q_i K_j^T, dP = dO_i V_j^T, dS as above and
+// dQ_i += dS K_j (its rows of P are not needed).
+// Roles of the dK/dV kernel (480 threads, one CTA per kv block; the dQ
+// kernel the same with Q and dO resident and K and V streamed):
 //   warps 0-3   elementwise, one thread per kv row (TMEM lane = row)
 //   Q group     warps 5-7, 9: split the resident K tile, then each Q chunk
 //               and its lse into a two-stage ring
@@ -48,6 +52,7 @@ struct BwdF32TcArgs {
     const float *delta;                              // [B, H, q_len]
     const int32_t *q_num, *q_idx, *fq_num, *fq_idx;  // q side of the BlockMask
     float *dk, *dv;                                  // contiguous [B, H, kv_len, 64]
+    float *dq;                                       // contiguous [B, H, q_len, 64]
 };
 
 namespace bwdf32 {
@@ -410,6 +415,252 @@ __global__ void __launch_bounds__(16 * 32, 1) dkdv_kernel(AttnProblem p, BwdF32T
     }
 }
 
+// dQ: one CTA per 128-row q block (TMEM: dQ | two buffers of S (64) and dP
+// (64); the bf16 parts of dS of columns 32h .. 32h + 31 go over S columns
+// 32h .. 32h + 31 and dP columns 32h .. 32h + 15).
+__host__ __device__ constexpr uint32_t dq_buf_col(int b) { return 64u + 128u * (uint32_t)b; }
+__host__ __device__ constexpr uint32_t dq_ds_part_col(int b, int part, int k) {
+    return part < 2 ? dq_buf_col(b) + 32u * (uint32_t)(k / 2) + 16u * (uint32_t)part + 8u * (uint32_t)(k % 2)
+                    : dq_buf_col(b) + 64u + 32u * (uint32_t)(k / 2) + 8u * (uint32_t)(k % 2);
+}
+static_assert(dq_buf_col(1) + 128 <= kTmemCols, "tensor memory");
+constexpr uint32_t kQ0 = 0, kDo0 = 3 * kOwnPart;            // resident Q and dO parts
+constexpr uint32_t kStK = 0, kStV = 3 * kChunkPart;          // a stage: K chunk parts, V chunk parts
+constexpr uint32_t kDqStageBytes = 6 * kChunkPart;
+constexpr uint32_t kDqMiscOff = kStage0 + 2 * kDqStageBytes;
+constexpr size_t kDqSmemBytes = kDqMiscOff + sizeof(Misc) + 1024;
+static_assert(kDqSmemBytes <= 232448, "shared memory per CTA");
+
+template <int SCORE>
+__global__ void __launch_bounds__(16 * 32, 1) dq_kernel(AttnProblem p, BwdF32TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Misc &ms = *reinterpret_cast<Misc *>(smem + kDqMiscOff);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int qb = blockIdx.x;
+    const int bh = p.bh_begin + (int)blockIdx.y, h = bh % p.H, b = bh / p.H;
+    const int q0 = qb * kBlock;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&ms.kv_ready, 8);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ms.st_full[i], 8);
+            mbar_init(&ms.st_empty[i], 1);
+            mbar_init(&ms.s_full[i], 1);
+            mbar_init(&ms.p_full[i], 4);
+        }
+        mbar_init(&ms.acc_full, 1);
+        mbar_init(&ms.drain, 1);
+        ms.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        // the kv side of the BlockMask (any block sizes) read as 128-tiles
+        const TileLists lists{p.kv_num, p.kv_idx, p.full_num, p.full_idx, p.nqb, p.nkvb, p.q_block, p.kv_block,
+                              p.nkvt};
+        for (int i = lane; i < p.nkvt; i += 32) ms.flags[i] = 0u;
+        __syncwarp();
+        tl_mark_warp(lists, bh, qb, 0, ms.flags, 0, p.nkvt, lane);
+        __syncwarp();
+        const uint32_t expect = tl_expect(lists);
+        const unsigned lt = (1u << lane) - 1u;
+        int cnt = 0;
+        for (int base = 0; base < p.nkvt; base += 32) {
+            const int i = base + lane;
+            const uint32_t w = i < p.nkvt ? ms.flags[i] : 0u;
+            const bool on = tl_listed(w, 0);
+            const unsigned bal = __ballot_sync(0xffffffffu, on);
+            if (on) ms.list[cnt + __popc(bal & lt)] = (uint32_t)i | (tl_full(expect, w, 0) ? (1u << 16) : 0u);
+            cnt += __popc(bal);
+        }
+        if (lane == 0) ms.ntiles = cnt;
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&ms.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = ms.tmem_base;
+    volatile int *abort_flag = &ms.abort;
+    const int nchunk = 2 * ms.ntiles;  // two 64-row chunks per kv tile
+    auto chunk_kv0 = [&](int j) { return (int)(ms.list[j / 2] & 0xFFFFu) * kBlock + (j % 2) * kQc; };
+    const int qi = q_index(warp), di = do_index(warp);
+
+    if (qi >= 0 || di >= 0) {
+        // ----------------------------------------------------------- producers
+        const int lt = 32 * (qi >= 0 ? qi : di) + lane;
+        if (qi >= 0) {
+            const float *qbase = static_cast<const float *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1];
+            load_split<kKvRows>(smem + kQ0, kOwnPart, qbase, p.q_stride[2], q0, p.q_len, lt);
+        } else {
+            load_split<kKvRows>(smem + kDo0, kOwnPart, a.dout + (int64_t)bh * p.q_len * D, D, q0, p.q_len, lt);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ms.kv_ready);
+        const float *kbase = static_cast<const float *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
+        const float *vbase = static_cast<const float *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1];
+        bool ok = true;
+        for (int j = 0; j < nchunk; ++j) {
+            const int s = j & 1;
+            if (j >= 2 && !f32_warp_wait(&ms.st_empty[s], (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            uint8_t *st = smem + kStage0 + s * kDqStageBytes;
+            const int kv0 = chunk_kv0(j);
+            if (qi >= 0)
+                load_split<kQc>(st + kStK, kChunkPart, kbase, p.k_stride[2], kv0, p.kv_len, lt);
+            else
+                load_split<kQc>(st + kStV, kChunkPart, vbase, p.v_stride[2], kv0, p.kv_len, lt);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.st_full[s]);
+        }
+        if (!ok) fail(ms, p.status);
+    } else if (warp == kMmaWarp) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0 && nchunk > 0) {
+            constexpr uint32_t kHi = smem_desc_hi_sw128(1024);
+            constexpr uint32_t idesc_kmaj = idesc_bf16_f32(128, kQc, 0, 0);  // S, dP: B K-major
+            constexpr uint32_t idesc_mn = idesc_bf16_f32(128, D, 0, 1);      // dQ: B MN-major
+            auto pa = [](int t) { return t == 2 || t == 4 ? 1 : t == 5 ? 2 : 0; };
+            auto pbp = [](int t) { return t == 1 || t == 4 ? 1 : t == 3 ? 2 : 0; };
+            const uint32_t qd = smem_desc_lo(smem_u32(smem + kQ0), 16), gd = smem_desc_lo(smem_u32(smem + kDo0), 16);
+            // S(j) = Q K_j^T and dP(j) = dO V_j^T into buffer j % 2
+            auto issue_sdp = [&](int j) -> bool {
+                const int s = j & 1;
+                if (!mbar_wait(&ms.st_full[s], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+                const uint32_t st = smem_u32(smem + kStage0 + s * kDqStageBytes);
+                const uint32_t kd = smem_desc_lo(st + kStK, 16), vd = smem_desc_lo(st + kStV, 16);
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t) {
+                        const uint32_t acc = (k > 0 || t > 0) ? 1u : 0u;
+                        mma_ss_lo<kHi, kHi>(tmem + dq_buf_col(s), qd + ((pa(t) * kOwnPart + k * 32) >> 4),
+                                            kd + ((pbp(t) * kChunkPart + k * 32) >> 4), idesc_kmaj, acc);
+                        mma_ss_lo<kHi, kHi>(tmem + dq_buf_col(s) + 64, gd + ((pa(t) * kOwnPart + k * 32) >> 4),
+                                            vd + ((pbp(t) * kChunkPart + k * 32) >> 4), idesc_kmaj, acc);
+                    }
+                mma_commit(&ms.s_full[s]);
+                return true;
+            };
+            // dQ += dS K_j: A from TMEM, B MN-major (K steps of 16 kv rows = 2048 bytes)
+            auto issue_acc = [&](int j) -> bool {
+                const int s = j & 1;
+                if (!mbar_wait(&ms.p_full[s], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+                const uint32_t km = smem_desc_lo(smem_u32(smem + kStage0 + s * kDqStageBytes + kStK), kChunkPart);
+#pragma unroll
+                for (int k = 0; k < kQc / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t)
+                        mma_ts_lo<kHi>(tmem + 0, tmem + dq_ds_part_col(s, pa(t), k),
+                                       km + ((pbp(t) * kChunkPart + k * 2048) >> 4), idesc_mn,
+                                       (j > 0 || k > 0 || t > 0) ? 1u : 0u);
+                mma_commit(&ms.st_empty[s]);
+                return true;
+            };
+            bool ok = mbar_wait(&ms.kv_ready, 0, abort_flag);
+            if (ok) tc_fence_after_sync();
+            for (int j = 0; ok && j < min(nchunk, 2); ++j) ok = issue_sdp(j);
+            // S(j + 2) reuses the buffer dQ(j) read: MMAs of one thread run in order
+            for (int j = 0; ok && j < nchunk; ++j) ok = issue_acc(j) && (j + 2 >= nchunk || issue_sdp(j + 2));
+            if (ok) mma_commit(&ms.acc_full);
+            if (!ok) fail(ms, p.status);
+            mma_commit(&ms.drain);  // every MMA issued above completes before TMEM is freed
+            int never = 0;
+            (void)mbar_wait(&ms.drain, 0, &never);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ---------------------------------------------------------- elementwise
+        const int q = q0 + (int)threadIdx.x;
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        const float slope = SCORE == FLEX_SCORE_ALIBI ? exp2f(-8.f * (float)(h + 1) / (float)p.H) : 0.f;
+        const float scale = p.scale;
+        const bool q_in = q < p.q_len;
+        const float lse = q_in ? p.lse[(int64_t)bh * p.q_len + q] : -INFINITY;
+        const float dlt = q_in ? a.delta[(int64_t)bh * p.q_len + q] : 0.f;
+        const float lb = lse * kLog2e;
+        bool ok = true;
+        for (int j = 0; j < nchunk; ++j) {
+            const int s = j & 1;
+            const bool full = (ms.list[j / 2] >> 16) & 1u;
+            const int kv0 = chunk_kv0(j);
+            if (!f32_warp_wait(&ms.s_full[s], (uint32_t)(j >> 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                uint32_t sr[32], dr[32];
+                f32_ld32(trow + dq_buf_col(s) + 32 * half, sr);
+                f32_ld32(trow + dq_buf_col(s) + 64 + 32 * half, dr);
+                float dsv[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int kv = kv0 + 32 * half + c;
+                    const bool keep = lse != -INFINITY && (full || (kv < p.kv_len && mask_mod(p.mask, b, q, kv)));
+                    float grad;
+                    const float x = score_t<SCORE>(p.score_param, __uint_as_float(sr[c]) * scale, slope, q, kv, grad);
+                    const float pr = ex2_approx(fmaf(x, kLog2e, -lb));
+                    dsv[c] = keep ? scale * pr * (__uint_as_float(dr[c]) - dlt) * grad : 0.f;
+                }
+                uint32_t w1[16], w2[16], w3[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) split3(dsv[2 * c], dsv[2 * c + 1], w1[c], w2[c], w3[c]);
+                // over S columns 32 half .. + 31 and dP columns 32 half .. + 15, all read above
+                tmem_st16(trow + dq_buf_col(s) + 32 * half, w1);
+                tmem_st16(trow + dq_buf_col(s) + 32 * half + 16, w2);
+                tmem_st16(trow + dq_buf_col(s) + 64 + 32 * half, w3);
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.p_full[s]);
+        }
+        // ------------------------------------------------------------ epilogue
+        const bool have = ok && nchunk > 0;
+        if (have && !f32_warp_wait(&ms.acc_full, 0, abort_flag)) ok = false;
+        if (!ok) fail(ms, p.status);
+        if (ok) {
+            tc_fence_after_sync();
+            float *dst = a.dq + ((int64_t)bh * p.q_len + (q_in ? q : 0)) * D;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {  // every lane takes the warp-collective loads
+                uint32_t r[32];
+                if (have) {
+                    f32_ld32(trow + c0, r);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) r[c] = 0u;
+                }
+                if (q_in) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        *reinterpret_cast<float4 *>(dst + c0 + c) =
+                            make_float4(__uint_as_float(r[c]), __uint_as_float(r[c + 1]), __uint_as_float(r[c + 2]),
+                                        __uint_as_float(r[c + 3]));
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
 }  // namespace bwdf32
 
 // dK and dV of fp32 inputs at D = 64 on the tensor cores (p.D == 64; p.nqt
@@ -435,6 +686,31 @@ inline cudaError_t launch_bwd_fp32_tc_dkdv(const AttnProblem &p, const BwdF32TcA
             return pick(dkdv_kernel<FLEX_SCORE_ALIBI>);
         default:
             return pick(dkdv_kernel<FLEX_SCORE_IDENTITY>);
+    }
+}
+
+// dQ of fp32 inputs at D = 64 on the tensor cores (p.D == 64).
+inline cudaError_t launch_bwd_fp32_tc_dq(const AttnProblem &p, const BwdF32TcArgs &a, cudaStream_t stream) {
+    using namespace bwdf32;
+    auto pick = [&](auto kern) -> cudaError_t {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDqSmemBytes);
+        if (e != cudaSuccess) return e;
+        for (int begin = 0; begin < p.B * p.H; begin += 65535) {
+            AttnProblem part = p;
+            part.bh_begin = begin;
+            const int count = p.B * p.H - begin < 65535 ? p.B * p.H - begin : 65535;
+            kern<<<dim3(p.nqt, count), kThreads, kDqSmemBytes, stream>>>(part, a);
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    };
+    switch (p.score_kind) {
+        case FLEX_SCORE_SOFTCAP:
+            return pick(dq_kernel<FLEX_SCORE_SOFTCAP>);
+        case FLEX_SCORE_ALIBI:
+            return pick(dq_kernel<FLEX_SCORE_ALIBI>);
+        default:
+            return pick(dq_kernel<FLEX_SCORE_IDENTITY>);
     }
 }
 
