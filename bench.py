@@ -386,8 +386,9 @@ def fp32_scale_timings(fa, torch, device_index: int, steps: int, peaks: dict) ->
     B1 H16 S4096, D = 64 and 128.  Each product takes six bf16 MMAs, so the
     tensor cores execute 6x the algorithmic FLOPs; the ceiling of the
     algorithmic rate is the measured bf16 burst / 6.  The float32 backward
-    (CUDA-core kernels) is timed on the same inputs against the fp32 FMA
-    rate of the CUDA cores.
+    is timed on the same inputs: at D = 64 on the tensor cores (the same
+    split, against the same ceiling), at D = 128 on the CUDA cores (against
+    their fp32 FMA rate).
     """
     if steps <= 0:
         return None
@@ -442,15 +443,22 @@ def fp32_scale_timings(fa, torch, device_index: int, steps: int, peaks: dict) ->
             raise RuntimeError(f"device status reported a timeout in the backward on {w.name}")
         ms_b = float(np.mean([a.elapsed_time(b) for a, b in evb]))
         bwd_tflops = 2.5 * flops / (ms_b * 1e-3) / 1e12
+        if D == 64:
+            # tensor cores (three-way bf16 split): 14 D of executed product FLOPs per
+            # computed pair (score and dP recomputed in both kernels), six bf16 MMAs each
+            bwd_roof = {"bound": "tensor", "peak": ceiling, "frac": bwd_tflops / ceiling,
+                        "peak_source": "measured bf16 burst / 6",
+                        "executed_bf16_mma_tflops": bwd_tflops * 1.4 * FP32_SPLIT_PRODUCTS,
+                        "kernels": "attn_bwd_delta (CUDA cores) + bwdf32::dkdv_kernel + bwdf32::dq_kernel (tcgen05)"}
+        else:
+            bwd_roof = {"bound": "alu", "peak": FP32_CUDA_CORE_TFLOPS, "frac": bwd_tflops / FP32_CUDA_CORE_TFLOPS,
+                        "kernels": "attn_bwd_delta + attn_bwd_dkdv + attn_bwd_dq (fp32 FMA, CUDA cores)"}
         res[w.name] = {"ms_per_launch": ms, "unmasked_block_flops": flops, "tflops": achieved,
                        "executed_bf16_mma_tflops": FP32_SPLIT_PRODUCTS * achieved,
                        "frac_of_ceiling": achieved / ceiling,
                        "l2": "K and V (64 MB at D = 128) stay in L2 across launches", "launches": steps,
                        "clocks": clocks.summary(),
-                       "backward": {"ms_per_launch": ms_b, "launches": len(evb), "tflops": bwd_tflops,
-                                    "bound": "alu", "peak": FP32_CUDA_CORE_TFLOPS,
-                                    "frac": bwd_tflops / FP32_CUDA_CORE_TFLOPS,
-                                    "kernels": "attn_bwd_delta + attn_bwd_dkdv + attn_bwd_dq (fp32 FMA, CUDA cores)"}}
+                       "backward": {"ms_per_launch": ms_b, "launches": len(evb), "tflops": bwd_tflops, **bwd_roof}}
         del dq, dk, dv, out, lse, bm, bq, dout, gq, gk, gv
         torch.cuda.empty_cache()
     return res
