@@ -102,35 +102,50 @@ constexpr size_t kSmemBytes = kMiscOff + sizeof(Misc) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 // Producer group of four warps (thread lt in 0..127): the rows r0 .. r0 +
-// rows - 1 of a [.., len, 64] float32 tensor, split into three bf16 parts at
-// dst + j * part_bytes in 128-byte swizzled rows (rows past len are zeros).
-// Thread lt takes units i = lt + 128 u: row i / 8, 8 floats at column 8 (i % 8).
+// ROWS - 1 of a [.., len, 64] float32 tensor (rows past len read as zeros)
+// into registers, then split into three bf16 parts at dst + j * part_bytes
+// in 128-byte swizzled rows.  Thread lt takes units i = lt + 128 u: row
+// i / 8, 8 floats at column 8 (i % 8).  The loads of a chunk are issued
+// before its ring slot is waited for.
 template <int ROWS>
-__device__ __forceinline__ void load_split(uint8_t *dst, uint32_t part_bytes, const float *src, int64_t rs, int r0,
-                                           int len, int lt) {
+struct RowsRegs {
+    float4 x[ROWS * 8 / 128 * 2];
+};
+template <int ROWS>
+__device__ __forceinline__ void load_rows(RowsRegs<ROWS> &g, const float *src, int64_t rs, int r0, int len, int lt) {
     constexpr int kUnits = ROWS * 8 / 128;
-    float4 x[2 * kUnits];
 #pragma unroll
     for (int u = 0; u < kUnits; ++u) {
         const int i = lt + 128 * u, r = i / 8, c = i % 8;
         const bool in = r0 + r < len;
         const float4 *p = reinterpret_cast<const float4 *>(src + (int64_t)(in ? r0 + r : 0) * rs) + 2 * c;
-        x[2 * u] = in ? __ldg(p) : make_float4(0.f, 0.f, 0.f, 0.f);
-        x[2 * u + 1] = in ? __ldg(p + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        g.x[2 * u] = in ? __ldg(p) : make_float4(0.f, 0.f, 0.f, 0.f);
+        g.x[2 * u + 1] = in ? __ldg(p + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+}
+template <int ROWS>
+__device__ __forceinline__ void store_split(uint8_t *dst, uint32_t part_bytes, const RowsRegs<ROWS> &g, int lt) {
+    constexpr int kUnits = ROWS * 8 / 128;
 #pragma unroll
     for (int u = 0; u < kUnits; ++u) {
         const int i = lt + 128 * u, r = i / 8, c = i % 8;
         uint4 p1, p2, p3;
-        split3(x[2 * u].x, x[2 * u].y, p1.x, p2.x, p3.x);
-        split3(x[2 * u].z, x[2 * u].w, p1.y, p2.y, p3.y);
-        split3(x[2 * u + 1].x, x[2 * u + 1].y, p1.z, p2.z, p3.z);
-        split3(x[2 * u + 1].z, x[2 * u + 1].w, p1.w, p2.w, p3.w);
+        split3(g.x[2 * u].x, g.x[2 * u].y, p1.x, p2.x, p3.x);
+        split3(g.x[2 * u].z, g.x[2 * u].w, p1.y, p2.y, p3.y);
+        split3(g.x[2 * u + 1].x, g.x[2 * u + 1].y, p1.z, p2.z, p3.z);
+        split3(g.x[2 * u + 1].z, g.x[2 * u + 1].w, p1.w, p2.w, p3.w);
         const uint32_t off = sw128_chunk(r, c, ROWS * 128);
         *reinterpret_cast<uint4 *>(dst + off) = p1;
         *reinterpret_cast<uint4 *>(dst + part_bytes + off) = p2;
         *reinterpret_cast<uint4 *>(dst + 2 * part_bytes + off) = p3;
     }
+}
+template <int ROWS>
+__device__ __forceinline__ void load_split(uint8_t *dst, uint32_t part_bytes, const float *src, int64_t rs, int r0,
+                                           int len, int lt) {
+    RowsRegs<ROWS> g;
+    load_rows<ROWS>(g, src, rs, r0, len, lt);
+    store_split<ROWS>(dst, part_bytes, g, lt);
 }
 
 __device__ __forceinline__ void fail(Misc &ms, int *status) {
@@ -232,25 +247,25 @@ __global__ void __launch_bounds__(16 * 32, 1) dkdv_kernel(AttnProblem p, BwdF32T
         bool ok = true;
         for (int j = 0; j < nchunk; ++j) {
             const int s = j & 1;
+            const int q0 = chunk_q0(j);
+            // this chunk's rows (and its lse or delta) into registers, then the slot
+            RowsRegs<kQc> g;
+            float rowv = 0.f;
+            const int q = q0 + lt;
+            if (qi >= 0) {
+                load_rows<kQc>(g, qbase, p.q_stride[2], q0, p.q_len, lt);
+                if (lt < kQc) rowv = q < p.q_len ? lbase[q] : -INFINITY;
+            } else {
+                load_rows<kQc>(g, gbase, D, q0, p.q_len, lt);
+                if (lt < kQc) rowv = q < p.q_len ? dbase[q] : 0.f;
+            }
             if (j >= 2 && !f32_warp_wait(&ms.st_empty[s], (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
                 ok = false;
                 break;
             }
             uint8_t *st = smem + kStage0 + s * kStageBytes;
-            const int q0 = chunk_q0(j);
-            if (qi >= 0) {
-                load_split<kQc>(st + kStQ, kChunkPart, qbase, p.q_stride[2], q0, p.q_len, lt);
-                if (lt < kQc) {
-                    const int q = q0 + lt;
-                    reinterpret_cast<float *>(st + kStLse)[lt] = q < p.q_len ? lbase[q] : -INFINITY;
-                }
-            } else {
-                load_split<kQc>(st + kStDo, kChunkPart, gbase, D, q0, p.q_len, lt);
-                if (lt < kQc) {
-                    const int q = q0 + lt;
-                    reinterpret_cast<float *>(st + kStDelta)[lt] = q < p.q_len ? dbase[q] : 0.f;
-                }
-            }
+            store_split<kQc>(st + (qi >= 0 ? kStQ : kStDo), kChunkPart, g, lt);
+            if (lt < kQc) reinterpret_cast<float *>(st + (qi >= 0 ? kStLse : kStDelta))[lt] = rowv;
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ms.st_full[s]);
@@ -437,7 +452,8 @@ __global__ void __launch_bounds__(16 * 32, 1) dq_kernel(AttnProblem p, BwdF32TcA
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Misc &ms = *reinterpret_cast<Misc *>(smem + kDqMiscOff);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int qb = blockIdx.x;
+    // longest first: under a causal mask the last q blocks list the most kv tiles
+    const int qb = p.nqt - 1 - (int)blockIdx.x;
     const int bh = p.bh_begin + (int)blockIdx.y, h = bh % p.H, b = bh / p.H;
     const int q0 = qb * kBlock;
 
@@ -505,16 +521,19 @@ __global__ void __launch_bounds__(16 * 32, 1) dq_kernel(AttnProblem p, BwdF32TcA
         bool ok = true;
         for (int j = 0; j < nchunk; ++j) {
             const int s = j & 1;
+            const int kv0 = chunk_kv0(j);
+            // this chunk's rows into registers, then the slot
+            RowsRegs<kQc> g;
+            if (qi >= 0)
+                load_rows<kQc>(g, kbase, p.k_stride[2], kv0, p.kv_len, lt);
+            else
+                load_rows<kQc>(g, vbase, p.v_stride[2], kv0, p.kv_len, lt);
             if (j >= 2 && !f32_warp_wait(&ms.st_empty[s], (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
                 ok = false;
                 break;
             }
             uint8_t *st = smem + kStage0 + s * kDqStageBytes;
-            const int kv0 = chunk_kv0(j);
-            if (qi >= 0)
-                load_split<kQc>(st + kStK, kChunkPart, kbase, p.k_stride[2], kv0, p.kv_len, lt);
-            else
-                load_split<kQc>(st + kStV, kChunkPart, vbase, p.v_stride[2], kv0, p.kv_len, lt);
+            store_split<kQc>(st + (qi >= 0 ? kStK : kStV), kChunkPart, g, lt);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ms.st_full[s]);
