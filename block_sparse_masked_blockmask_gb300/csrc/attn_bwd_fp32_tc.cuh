@@ -90,7 +90,9 @@ __host__ __device__ constexpr uint32_t ds_part_col(int b, int part, int k) {
 static_assert(buf_col(1) + 192 == kTmemCols, "tensor memory");
 
 struct Misc {
-    uint64_t kv_ready, st_full[2], st_empty[2], s_full[2], p_full[2], acc_full, drain;
+    // ring stage s, producer group g (0: Q in the dK/dV kernel, K in the dQ
+    // kernel; 1: dO, V): each half of a stage is filled and freed on its own
+    uint64_t kv_ready, st_full[2][2], st_empty[2][2], s_full[2], p_full[2], acc_full, drain;
     uint32_t tmem_base;
     int abort;
     int ntiles;  // q tiles listed for this kv block
@@ -183,8 +185,10 @@ __global__ void __launch_bounds__(16 * 32, 1) dkdv_kernel(AttnProblem p, BwdF32T
     if (threadIdx.x == 0) {
         mbar_init(&ms.kv_ready, 8);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&ms.st_full[i], 8);
-            mbar_init(&ms.st_empty[i], 1);
+            for (int g = 0; g < 2; ++g) {
+                mbar_init(&ms.st_full[i][g], 4);
+                mbar_init(&ms.st_empty[i][g], 1);
+            }
             mbar_init(&ms.s_full[i], 1);
             mbar_init(&ms.p_full[i], 4);
         }
@@ -229,7 +233,7 @@ __global__ void __launch_bounds__(16 * 32, 1) dkdv_kernel(AttnProblem p, BwdF32T
 
     if (qi >= 0 || di >= 0) {
         // ----------------------------------------------------------- producers
-        const int lt = 32 * (qi >= 0 ? qi : di) + lane;
+        const int lt = 32 * (qi >= 0 ? qi : di) + lane, grp = qi >= 0 ? 0 : 1;
         if (qi >= 0) {
             const float *kbase = static_cast<const float *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
             load_split<kKvRows>(smem + kK0, kOwnPart, kbase, p.k_stride[2], kv0, p.kv_len, lt);
@@ -259,7 +263,7 @@ __global__ void __launch_bounds__(16 * 32, 1) dkdv_kernel(AttnProblem p, BwdF32T
                 load_rows<kQc>(g, gbase, D, q0, p.q_len, lt);
                 if (lt < kQc) rowv = q < p.q_len ? dbase[q] : 0.f;
             }
-            if (j >= 2 && !f32_warp_wait(&ms.st_empty[s], (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
+            if (j >= 2 && !f32_warp_wait(&ms.st_empty[s][grp], (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -268,7 +272,7 @@ __global__ void __launch_bounds__(16 * 32, 1) dkdv_kernel(AttnProblem p, BwdF32T
             if (lt < kQc) reinterpret_cast<float *>(st + (qi >= 0 ? kStLse : kStDelta))[lt] = rowv;
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ms.st_full[s]);
+            if (lane == 0) mbar_arrive(&ms.st_full[s][grp]);
         }
         if (!ok) fail(ms, p.status);
     } else if (warp == kMmaWarp) {
@@ -282,22 +286,29 @@ __global__ void __launch_bounds__(16 * 32, 1) dkdv_kernel(AttnProblem p, BwdF32T
             auto pbp = [](int t) { return t == 1 || t == 4 ? 1 : t == 3 ? 2 : 0; };
             const uint32_t kd = smem_desc_lo(smem_u32(smem + kK0), 16), vd = smem_desc_lo(smem_u32(smem + kV0), 16);
             // S^T(j) and dP^T(j) into buffer j % 2 (K steps of 16 head dims = 32 bytes)
+            // (dP^T first: the dO half of a stage is refilled while dK(j - 2) runs)
             auto issue_sdp = [&](int j) -> bool {
                 const int s = j & 1;
-                if (!mbar_wait(&ms.st_full[s], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
-                tc_fence_after_sync();
                 const uint32_t st = smem_u32(smem + kStage0 + s * kStageBytes);
                 const uint32_t qd = smem_desc_lo(st + kStQ, 16), gd = smem_desc_lo(st + kStDo, 16);
+                if (!mbar_wait(&ms.st_full[s][1], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
 #pragma unroll
-                    for (int t = 0; t < 6; ++t) {
-                        const uint32_t acc = (k > 0 || t > 0) ? 1u : 0u;
-                        mma_ss_lo<kHi, kHi>(tmem + buf_col(s), kd + ((pa(t) * kOwnPart + k * 32) >> 4),
-                                            qd + ((pbp(t) * kChunkPart + k * 32) >> 4), idesc_kmaj, acc);
+                    for (int t = 0; t < 6; ++t)
                         mma_ss_lo<kHi, kHi>(tmem + buf_col(s) + 64, vd + ((pa(t) * kOwnPart + k * 32) >> 4),
-                                            gd + ((pbp(t) * kChunkPart + k * 32) >> 4), idesc_kmaj, acc);
-                    }
+                                            gd + ((pbp(t) * kChunkPart + k * 32) >> 4), idesc_kmaj,
+                                            (k > 0 || t > 0) ? 1u : 0u);
+                if (!mbar_wait(&ms.st_full[s][0], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t)
+                        mma_ss_lo<kHi, kHi>(tmem + buf_col(s), kd + ((pa(t) * kOwnPart + k * 32) >> 4),
+                                            qd + ((pbp(t) * kChunkPart + k * 32) >> 4), idesc_kmaj,
+                                            (k > 0 || t > 0) ? 1u : 0u);
                 mma_commit(&ms.s_full[s]);
                 return true;
             };
@@ -309,17 +320,23 @@ __global__ void __launch_bounds__(16 * 32, 1) dkdv_kernel(AttnProblem p, BwdF32T
                 tc_fence_after_sync();
                 const uint32_t st = smem_u32(smem + kStage0 + s * kStageBytes);
                 const uint32_t qm = smem_desc_lo(st + kStQ, kChunkPart), gm = smem_desc_lo(st + kStDo, kChunkPart);
+                // dV, then the dO half of the stage is free; dK, then the Q half
 #pragma unroll
                 for (int k = 0; k < kQc / 16; ++k)
 #pragma unroll
-                    for (int t = 0; t < 6; ++t) {
-                        const uint32_t acc = (j > 0 || k > 0 || t > 0) ? 1u : 0u;
+                    for (int t = 0; t < 6; ++t)
                         mma_ts_lo<kHi>(tmem + kDv, tmem + p_part_col(s, pa(t), k),
-                                       gm + ((pbp(t) * kChunkPart + k * 2048) >> 4), idesc_mn, acc);
+                                       gm + ((pbp(t) * kChunkPart + k * 2048) >> 4), idesc_mn,
+                                       (j > 0 || k > 0 || t > 0) ? 1u : 0u);
+                mma_commit(&ms.st_empty[s][1]);
+#pragma unroll
+                for (int k = 0; k < kQc / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t)
                         mma_ts_lo<kHi>(tmem + kDk, tmem + ds_part_col(s, pa(t), k),
-                                       qm + ((pbp(t) * kChunkPart + k * 2048) >> 4), idesc_mn, acc);
-                    }
-                mma_commit(&ms.st_empty[s]);
+                                       qm + ((pbp(t) * kChunkPart + k * 2048) >> 4), idesc_mn,
+                                       (j > 0 || k > 0 || t > 0) ? 1u : 0u);
+                mma_commit(&ms.st_empty[s][0]);
                 return true;
             };
             bool ok = mbar_wait(&ms.kv_ready, 0, abort_flag);
@@ -348,7 +365,8 @@ __global__ void __launch_bounds__(16 * 32, 1) dkdv_kernel(AttnProblem p, BwdF32T
             // S^T and dP^T of the chunk are in TMEM; its lse and delta (written
             // by the producers) are read after their own barrier
             if (!f32_warp_wait(&ms.s_full[s], (uint32_t)(j >> 1) & 1u, abort_flag) ||
-                !f32_warp_wait(&ms.st_full[s], (uint32_t)(j >> 1) & 1u, abort_flag)) {
+                !f32_warp_wait(&ms.st_full[s][0], (uint32_t)(j >> 1) & 1u, abort_flag) ||
+                !f32_warp_wait(&ms.st_full[s][1], (uint32_t)(j >> 1) & 1u, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -460,8 +478,10 @@ __global__ void __launch_bounds__(16 * 32, 1) dq_kernel(AttnProblem p, BwdF32TcA
     if (threadIdx.x == 0) {
         mbar_init(&ms.kv_ready, 8);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&ms.st_full[i], 8);
-            mbar_init(&ms.st_empty[i], 1);
+            for (int g = 0; g < 2; ++g) {
+                mbar_init(&ms.st_full[i][g], 4);
+                mbar_init(&ms.st_empty[i][g], 1);
+            }
             mbar_init(&ms.s_full[i], 1);
             mbar_init(&ms.p_full[i], 4);
         }
@@ -506,7 +526,7 @@ __global__ void __launch_bounds__(16 * 32, 1) dq_kernel(AttnProblem p, BwdF32TcA
 
     if (qi >= 0 || di >= 0) {
         // ----------------------------------------------------------- producers
-        const int lt = 32 * (qi >= 0 ? qi : di) + lane;
+        const int lt = 32 * (qi >= 0 ? qi : di) + lane, grp = qi >= 0 ? 0 : 1;
         if (qi >= 0) {
             const float *qbase = static_cast<const float *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1];
             load_split<kKvRows>(smem + kQ0, kOwnPart, qbase, p.q_stride[2], q0, p.q_len, lt);
@@ -528,7 +548,7 @@ __global__ void __launch_bounds__(16 * 32, 1) dq_kernel(AttnProblem p, BwdF32TcA
                 load_rows<kQc>(g, kbase, p.k_stride[2], kv0, p.kv_len, lt);
             else
                 load_rows<kQc>(g, vbase, p.v_stride[2], kv0, p.kv_len, lt);
-            if (j >= 2 && !f32_warp_wait(&ms.st_empty[s], (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
+            if (j >= 2 && !f32_warp_wait(&ms.st_empty[s][grp], (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -536,7 +556,7 @@ __global__ void __launch_bounds__(16 * 32, 1) dq_kernel(AttnProblem p, BwdF32TcA
             store_split<kQc>(st + (qi >= 0 ? kStK : kStV), kChunkPart, g, lt);
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ms.st_full[s]);
+            if (lane == 0) mbar_arrive(&ms.st_full[s][grp]);
         }
         if (!ok) fail(ms, p.status);
     } else if (warp == kMmaWarp) {
@@ -549,22 +569,31 @@ __global__ void __launch_bounds__(16 * 32, 1) dq_kernel(AttnProblem p, BwdF32TcA
             auto pbp = [](int t) { return t == 1 || t == 4 ? 1 : t == 3 ? 2 : 0; };
             const uint32_t qd = smem_desc_lo(smem_u32(smem + kQ0), 16), gd = smem_desc_lo(smem_u32(smem + kDo0), 16);
             // S(j) = Q K_j^T and dP(j) = dO V_j^T into buffer j % 2
+            // (dP first: V is read by nothing else, so its half of the stage
+            // is free as soon as these MMAs are done)
             auto issue_sdp = [&](int j) -> bool {
                 const int s = j & 1;
-                if (!mbar_wait(&ms.st_full[s], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
-                tc_fence_after_sync();
                 const uint32_t st = smem_u32(smem + kStage0 + s * kDqStageBytes);
                 const uint32_t kd = smem_desc_lo(st + kStK, 16), vd = smem_desc_lo(st + kStV, 16);
+                if (!mbar_wait(&ms.st_full[s][1], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
 #pragma unroll
-                    for (int t = 0; t < 6; ++t) {
-                        const uint32_t acc = (k > 0 || t > 0) ? 1u : 0u;
-                        mma_ss_lo<kHi, kHi>(tmem + dq_buf_col(s), qd + ((pa(t) * kOwnPart + k * 32) >> 4),
-                                            kd + ((pbp(t) * kChunkPart + k * 32) >> 4), idesc_kmaj, acc);
+                    for (int t = 0; t < 6; ++t)
                         mma_ss_lo<kHi, kHi>(tmem + dq_buf_col(s) + 64, gd + ((pa(t) * kOwnPart + k * 32) >> 4),
-                                            vd + ((pbp(t) * kChunkPart + k * 32) >> 4), idesc_kmaj, acc);
-                    }
+                                            vd + ((pbp(t) * kChunkPart + k * 32) >> 4), idesc_kmaj,
+                                            (k > 0 || t > 0) ? 1u : 0u);
+                mma_commit(&ms.st_empty[s][1]);
+                if (!mbar_wait(&ms.st_full[s][0], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t)
+                        mma_ss_lo<kHi, kHi>(tmem + dq_buf_col(s), qd + ((pa(t) * kOwnPart + k * 32) >> 4),
+                                            kd + ((pbp(t) * kChunkPart + k * 32) >> 4), idesc_kmaj,
+                                            (k > 0 || t > 0) ? 1u : 0u);
                 mma_commit(&ms.s_full[s]);
                 return true;
             };
@@ -581,7 +610,7 @@ __global__ void __launch_bounds__(16 * 32, 1) dq_kernel(AttnProblem p, BwdF32TcA
                         mma_ts_lo<kHi>(tmem + 0, tmem + dq_ds_part_col(s, pa(t), k),
                                        km + ((pbp(t) * kChunkPart + k * 2048) >> 4), idesc_mn,
                                        (j > 0 || k > 0 || t > 0) ? 1u : 0u);
-                mma_commit(&ms.st_empty[s]);
+                mma_commit(&ms.st_empty[s][0]);  // the K half of the stage
                 return true;
             };
             bool ok = mbar_wait(&ms.kv_ready, 0, abort_flag);
