@@ -387,8 +387,9 @@ def fp32_scale_timings(fa, torch, device_index: int, steps: int, peaks: dict) ->
     tensor cores execute 6x the algorithmic FLOPs; the ceiling of the
     algorithmic rate is the measured bf16 burst / 6.  The float32 backward
     is timed on the same inputs: at D = 64 on the tensor cores (the same
-    split, against the same ceiling), at D = 128 on the CUDA cores (against
-    their fp32 FMA rate).
+    split, against the same ceiling); at D = 128 dK/dV run on the CUDA cores
+    and dQ on the tensor cores, reported against the CUDA cores' fp32 FMA
+    rate.
     """
     if steps <= 0:
         return None
@@ -451,8 +452,10 @@ def fp32_scale_timings(fa, torch, device_index: int, steps: int, peaks: dict) ->
                         "executed_bf16_mma_tflops": bwd_tflops * 1.4 * FP32_SPLIT_PRODUCTS,
                         "kernels": "attn_bwd_delta (CUDA cores) + bwdf32::dkdv_kernel + bwdf32::dq_kernel (tcgen05)"}
         else:
+            # dK/dV on the CUDA cores (most of the time), dQ on the tensor cores
             bwd_roof = {"bound": "alu", "peak": FP32_CUDA_CORE_TFLOPS, "frac": bwd_tflops / FP32_CUDA_CORE_TFLOPS,
-                        "kernels": "attn_bwd_delta + attn_bwd_dkdv + attn_bwd_dq (fp32 FMA, CUDA cores)"}
+                        "kernels": "attn_bwd_delta + attn_bwd_dkdv (fp32 FMA, CUDA cores) + bwdf32::dq128_kernel "
+                                   "(tcgen05, three-way bf16 split)"}
         res[w.name] = {"ms_per_launch": ms, "unmasked_block_flops": flops, "tflops": achieved,
                        "executed_bf16_mma_tflops": FP32_SPLIT_PRODUCTS * achieved,
                        "frac_of_ceiling": achieved / ceiling,

@@ -457,7 +457,7 @@ cudaError_t launch_bwd_fp32(const AttnProblem &p, const BwdArgs &a, cudaStream_t
     attn_bwd_delta_kernel<D, float><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, stream>>>(p, a, rows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const bool tc_dkdv = D == 64 && p.nqt <= kBwdF32TcMaxQTiles, tc_dq = D == 64;
+    const bool tc_dkdv = D == 64 && p.nqt <= kBwdF32TcMaxQTiles, tc_dq = true;
     const BwdF32TcArgs ta{static_cast<const float *>(a.dout), a.delta, a.q_num, a.q_idx, a.fq_num, a.fq_idx,
                           static_cast<float *>(a.dk), static_cast<float *>(a.dv), static_cast<float *>(a.dq)};
     if (tc_dkdv && (e = launch_bwd_fp32_tc_dkdv(p, ta, stream)) != cudaSuccess) return e;

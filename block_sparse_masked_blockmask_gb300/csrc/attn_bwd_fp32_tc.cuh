@@ -709,6 +709,330 @@ __global__ void __launch_bounds__(16 * 32, 1) dq_kernel(AttnProblem p, BwdF32TcA
     }
 }
 
+// dQ at D = 128.  Q parts are the A operand of S from tensor memory (as in
+// the forward), dO parts the A operand of dP from shared memory; one ring
+// stage of K and V parts and one S/dP buffer (the split parts of 128 head
+// dims leave no room for two), so a chunk's MMAs, its elementwise work and
+// the next chunk's loads follow each other: S, dP -> dS -> dQ -> S, dP.
+// TMEM: Q1 | Q2 | Q3 (64 each) | dQ (128) | S (64) | dP (64).
+namespace d128 {
+constexpr int D = 128;
+constexpr uint32_t kQcol = 0, kDq = 192, kS = 320, kDp = 384;
+__host__ __device__ constexpr uint32_t ds_part_col(int part, int k) {
+    return part < 2 ? kS + 32u * (uint32_t)(k / 2) + 16u * (uint32_t)part + 8u * (uint32_t)(k % 2)
+                    : kDp + 32u * (uint32_t)(k / 2) + 8u * (uint32_t)(k % 2);
+}
+constexpr uint32_t kDoPart = 128 * D * 2;      // 32 KB: one part of the resident dO (two 64-wide atoms)
+constexpr uint32_t kDoAtom = 128 * 128;        // 128 rows x 64 bf16
+constexpr uint32_t kChPart = kQc * D * 2;      // 16 KB: one part of a 64-row K or V chunk
+constexpr uint32_t kChAtom = kQc * 128;        // 64 rows x 64 bf16
+constexpr uint32_t kDo0 = 0, kStK = 3 * kDoPart, kStV = kStK + 3 * kChPart;
+constexpr uint32_t kMiscOff = kStV + 3 * kChPart;
+constexpr size_t kSmemBytes = kMiscOff + sizeof(Misc) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(kDp + 64 <= kTmemCols, "tensor memory");
+
+// rows r0 .. r0 + 63 of a [.., len, 128] float32 tensor (zeros past len),
+// split into three bf16 parts stored as tile rows row_base .. row_base + 63
+// of a tile with 128-byte swizzled rows (atoms of atom_bytes) at dst + j *
+// part_bytes.  Thread lt (0..127) takes units i = lt + 128 u: row i / 16, 8
+// floats at column 8 (i % 16).
+struct Rows64 {
+    float4 x[16];
+};
+__device__ __forceinline__ void load64(Rows64 &g, const float *src, int64_t rs, int r0, int len, int lt) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int i = lt + 128 * u, r = i / 16, c = i % 16;
+        const bool in = r0 + r < len;
+        const float4 *p = reinterpret_cast<const float4 *>(src + (int64_t)(in ? r0 + r : 0) * rs) + 2 * c;
+        g.x[2 * u] = in ? __ldg(p) : make_float4(0.f, 0.f, 0.f, 0.f);
+        g.x[2 * u + 1] = in ? __ldg(p + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+__device__ __forceinline__ void store64(uint8_t *dst, uint32_t part_bytes, uint32_t atom_bytes, int row_base,
+                                        const Rows64 &g, int lt) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int i = lt + 128 * u, r = i / 16, c = i % 16;
+        uint4 p1, p2, p3;
+        split3(g.x[2 * u].x, g.x[2 * u].y, p1.x, p2.x, p3.x);
+        split3(g.x[2 * u].z, g.x[2 * u].w, p1.y, p2.y, p3.y);
+        split3(g.x[2 * u + 1].x, g.x[2 * u + 1].y, p1.z, p2.z, p3.z);
+        split3(g.x[2 * u + 1].z, g.x[2 * u + 1].w, p1.w, p2.w, p3.w);
+        const uint32_t off = sw128_chunk(row_base + r, c, atom_bytes);
+        *reinterpret_cast<uint4 *>(dst + off) = p1;
+        *reinterpret_cast<uint4 *>(dst + part_bytes + off) = p2;
+        *reinterpret_cast<uint4 *>(dst + 2 * part_bytes + off) = p3;
+    }
+}
+}  // namespace d128
+
+template <int SCORE>
+__global__ void __launch_bounds__(16 * 32, 1) dq128_kernel(AttnProblem p, BwdF32TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Misc &ms = *reinterpret_cast<Misc *>(smem + d128::kMiscOff);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // longest first: under a causal mask the last q blocks list the most kv tiles
+    const int qb = p.nqt - 1 - (int)blockIdx.x;
+    const int bh = p.bh_begin + (int)blockIdx.y, h = bh % p.H, b = bh / p.H;
+    const int q0 = qb * kBlock;
+
+    // kv_ready: dO resident (4 dO-group warps) and Q in TMEM (4 elementwise
+    // warps); st_full[0][g] / st_empty[0][g]: the K (g = 0) and V (g = 1)
+    // halves of the single stage
+    if (threadIdx.x == 0) {
+        mbar_init(&ms.kv_ready, 8);
+        for (int g = 0; g < 2; ++g) {
+            mbar_init(&ms.st_full[0][g], 4);
+            mbar_init(&ms.st_empty[0][g], 1);
+        }
+        mbar_init(&ms.s_full[0], 1);
+        mbar_init(&ms.p_full[0], 4);
+        mbar_init(&ms.acc_full, 1);
+        mbar_init(&ms.drain, 1);
+        ms.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        const TileLists lists{p.kv_num, p.kv_idx, p.full_num, p.full_idx, p.nqb, p.nkvb, p.q_block, p.kv_block,
+                              p.nkvt};
+        for (int i = lane; i < p.nkvt; i += 32) ms.flags[i] = 0u;
+        __syncwarp();
+        tl_mark_warp(lists, bh, qb, 0, ms.flags, 0, p.nkvt, lane);
+        __syncwarp();
+        const uint32_t expect = tl_expect(lists);
+        const unsigned lt = (1u << lane) - 1u;
+        int cnt = 0;
+        for (int base = 0; base < p.nkvt; base += 32) {
+            const int i = base + lane;
+            const uint32_t w = i < p.nkvt ? ms.flags[i] : 0u;
+            const bool on = tl_listed(w, 0);
+            const unsigned bal = __ballot_sync(0xffffffffu, on);
+            if (on) ms.list[cnt + __popc(bal & lt)] = (uint32_t)i | (tl_full(expect, w, 0) ? (1u << 16) : 0u);
+            cnt += __popc(bal);
+        }
+        if (lane == 0) ms.ntiles = cnt;
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&ms.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = ms.tmem_base;
+    volatile int *abort_flag = &ms.abort;
+    const int nchunk = 2 * ms.ntiles;
+    auto chunk_kv0 = [&](int j) { return (int)(ms.list[j / 2] & 0xFFFFu) * kBlock + (j % 2) * kQc; };
+    const int qi = q_index(warp), di = do_index(warp);
+
+    if (qi >= 0 || di >= 0) {
+        // ----------------------------------------------------------- producers
+        const int lt = 32 * (qi >= 0 ? qi : di) + lane, grp = qi >= 0 ? 0 : 1;
+        if (grp == 1 && nchunk > 0) {
+            // the resident dO: two 64-row halves of the 128-row tile
+            const float *gbase = a.dout + (int64_t)bh * p.q_len * d128::D;
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                d128::Rows64 g;
+                d128::load64(g, gbase, d128::D, q0 + 64 * half, p.q_len, lt);
+                d128::store64(smem + d128::kDo0, d128::kDoPart, d128::kDoAtom, 64 * half, g, lt);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.kv_ready);
+        }
+        const float *base = grp == 0 ? static_cast<const float *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1]
+                                     : static_cast<const float *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1];
+        const int64_t rs = grp == 0 ? p.k_stride[2] : p.v_stride[2];
+        bool ok = true;
+        for (int j = 0; j < nchunk; ++j) {
+            d128::Rows64 g;
+            d128::load64(g, base, rs, chunk_kv0(j), p.kv_len, lt);
+            if (j >= 1 && !f32_warp_wait(&ms.st_empty[0][grp], (uint32_t)(j - 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            d128::store64(smem + (grp == 0 ? d128::kStK : d128::kStV), d128::kChPart, d128::kChAtom, 0, g, lt);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.st_full[0][grp]);
+        }
+        if (!ok) fail(ms, p.status);
+    } else if (warp == kMmaWarp) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0 && nchunk > 0) {
+            constexpr uint32_t kHi = smem_desc_hi_sw128(1024);
+            constexpr uint32_t idesc_kmaj = idesc_bf16_f32(128, kQc, 0, 0);  // S, dP: N = 64 kv, B K-major
+            constexpr uint32_t idesc_mn = idesc_bf16_f32(128, d128::D, 0, 1);      // dQ: N = 128, B MN-major
+            auto pa = [](int t) { return t == 2 || t == 4 ? 1 : t == 5 ? 2 : 0; };
+            auto pbp = [](int t) { return t == 1 || t == 4 ? 1 : t == 3 ? 2 : 0; };
+            const uint32_t gd = smem_desc_lo(smem_u32(smem + d128::kDo0), 16);
+            const uint32_t kd = smem_desc_lo(smem_u32(smem + d128::kStK), 16), vd = smem_desc_lo(smem_u32(smem + d128::kStV), 16);
+            const uint32_t km = smem_desc_lo(smem_u32(smem + d128::kStK), d128::kChAtom);
+            bool ok = mbar_wait(&ms.kv_ready, 0, abort_flag);
+            for (int j = 0; ok && j < nchunk; ++j) {
+                const uint32_t ph = (uint32_t)j & 1u;
+                // dP = dO V^T (A: dO parts in shared memory), then the V half is free
+                if (!mbar_wait(&ms.st_full[0][1], ph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < d128::D / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t)
+                        mma_ss_lo<kHi, kHi>(tmem + d128::kDp,
+                                            gd + ((pa(t) * d128::kDoPart + (k / 4) * d128::kDoAtom + (k % 4) * 32) >> 4),
+                                            vd + ((pbp(t) * d128::kChPart + (k / 4) * d128::kChAtom + (k % 4) * 32) >> 4),
+                                            idesc_kmaj, (k > 0 || t > 0) ? 1u : 0u);
+                mma_commit(&ms.st_empty[0][1]);
+                // S = Q K^T (A: Q parts in TMEM, 8 columns per K step of 16 head dims)
+                if (!mbar_wait(&ms.st_full[0][0], ph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < d128::D / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t)
+                        mma_ts_lo<kHi>(tmem + d128::kS, tmem + d128::kQcol + 64 * pa(t) + 8 * k,
+                                       kd + ((pbp(t) * d128::kChPart + (k / 4) * d128::kChAtom + (k % 4) * 32) >> 4),
+                                       idesc_kmaj, (k > 0 || t > 0) ? 1u : 0u);
+                mma_commit(&ms.s_full[0]);
+                // dQ += dS K (A: dS parts in TMEM; B: K MN-major, the two
+                // 64-wide halves d128::kChAtom apart, K steps of 16 kv rows)
+                if (!mbar_wait(&ms.p_full[0], ph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < kQc / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t)
+                        mma_ts_lo<kHi>(tmem + d128::kDq, tmem + d128::ds_part_col(pa(t), k),
+                                       km + ((pbp(t) * d128::kChPart + k * 2048) >> 4), idesc_mn,
+                                       (j > 0 || k > 0 || t > 0) ? 1u : 0u);
+                mma_commit(&ms.st_empty[0][0]);  // the K half
+            }
+            if (ok) mma_commit(&ms.acc_full);
+            if (!ok) fail(ms, p.status);
+            mma_commit(&ms.drain);
+            int never = 0;
+            (void)mbar_wait(&ms.drain, 0, &never);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ---------------------------------------------------------- elementwise
+        const int q = q0 + (int)threadIdx.x;
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        const float slope = SCORE == FLEX_SCORE_ALIBI ? exp2f(-8.f * (float)(h + 1) / (float)p.H) : 0.f;
+        const float scale = p.scale;
+        const bool q_in = q < p.q_len;
+        const float lse = q_in ? p.lse[(int64_t)bh * p.q_len + q] : -INFINITY;
+        const float dlt = q_in ? a.delta[(int64_t)bh * p.q_len + q] : 0.f;
+        const float lb = lse * kLog2e;
+        bool ok = true;
+        if (nchunk > 0) {
+            // this row of Q -> Q1, Q2, Q3 columns of this lane (bf16 pairs)
+            const float *qrow = static_cast<const float *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1] +
+                                (int64_t)(q_in ? q : 0) * p.q_stride[2];
+#pragma unroll 1
+            for (int c0 = 0; c0 < d128::D; c0 += 32) {
+                float4 x[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    x[j] = q_in ? __ldg(reinterpret_cast<const float4 *>(qrow + c0) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                uint32_t w1[16], w2[16], w3[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    split3(f4_at(x[j / 2], 2 * (j % 2)), f4_at(x[j / 2], 2 * (j % 2) + 1), w1[j], w2[j], w3[j]);
+                tmem_st16(trow + d128::kQcol + c0 / 2, w1);
+                tmem_st16(trow + d128::kQcol + 64 + c0 / 2, w2);
+                tmem_st16(trow + d128::kQcol + 128 + c0 / 2, w3);
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.kv_ready);
+        }
+        for (int j = 0; j < nchunk; ++j) {
+            const bool full = (ms.list[j / 2] >> 16) & 1u;
+            const int kv0 = chunk_kv0(j);
+            if (!f32_warp_wait(&ms.s_full[0], (uint32_t)j & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                uint32_t sr[32], dr[32];
+                f32_ld32(trow + d128::kS + 32 * half, sr);
+                f32_ld32(trow + d128::kDp + 32 * half, dr);
+                float dsv[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int kv = kv0 + 32 * half + c;
+                    const bool keep = lse != -INFINITY && (full || (kv < p.kv_len && mask_mod(p.mask, b, q, kv)));
+                    float grad;
+                    const float x = score_t<SCORE>(p.score_param, __uint_as_float(sr[c]) * scale, slope, q, kv, grad);
+                    const float pr = ex2_approx(fmaf(x, kLog2e, -lb));
+                    dsv[c] = keep ? scale * pr * (__uint_as_float(dr[c]) - dlt) * grad : 0.f;
+                }
+                uint32_t w1[16], w2[16], w3[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) split3(dsv[2 * c], dsv[2 * c + 1], w1[c], w2[c], w3[c]);
+                // over S columns 32 half .. + 31 and dP columns 32 half .. + 15, all read above
+                tmem_st16(trow + d128::kS + 32 * half, w1);
+                tmem_st16(trow + d128::kS + 32 * half + 16, w2);
+                tmem_st16(trow + d128::kDp + 32 * half, w3);
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.p_full[0]);
+        }
+        // ------------------------------------------------------------ epilogue
+        const bool have = ok && nchunk > 0;
+        if (have && !f32_warp_wait(&ms.acc_full, 0, abort_flag)) ok = false;
+        if (!ok) fail(ms, p.status);
+        if (ok) {
+            tc_fence_after_sync();
+            float *dst = a.dq + ((int64_t)bh * p.q_len + (q_in ? q : 0)) * d128::D;
+#pragma unroll 1
+            for (int c0 = 0; c0 < d128::D; c0 += 32) {  // every lane takes the warp-collective loads
+                uint32_t r[32];
+                if (have) {
+                    f32_ld32(trow + d128::kDq + c0, r);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) r[c] = 0u;
+                }
+                if (q_in) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        *reinterpret_cast<float4 *>(dst + c0 + c) =
+                            make_float4(__uint_as_float(r[c]), __uint_as_float(r[c + 1]), __uint_as_float(r[c + 2]),
+                                        __uint_as_float(r[c + 3]));
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
 }  // namespace bwdf32
 
 // dK and dV of fp32 inputs at D = 64 on the tensor cores (p.D == 64; p.nqt
@@ -737,28 +1061,30 @@ inline cudaError_t launch_bwd_fp32_tc_dkdv(const AttnProblem &p, const BwdF32TcA
     }
 }
 
-// dQ of fp32 inputs at D = 64 on the tensor cores (p.D == 64).
+// dQ of fp32 inputs on the tensor cores (p.D == 64 or 128).
 inline cudaError_t launch_bwd_fp32_tc_dq(const AttnProblem &p, const BwdF32TcArgs &a, cudaStream_t stream) {
     using namespace bwdf32;
+    const size_t smem = p.D == 64 ? kDqSmemBytes : d128::kSmemBytes;
     auto pick = [&](auto kern) -> cudaError_t {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDqSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         for (int begin = 0; begin < p.B * p.H; begin += 65535) {
             AttnProblem part = p;
             part.bh_begin = begin;
             const int count = p.B * p.H - begin < 65535 ? p.B * p.H - begin : 65535;
-            kern<<<dim3(p.nqt, count), kThreads, kDqSmemBytes, stream>>>(part, a);
+            kern<<<dim3(p.nqt, count), kThreads, smem, stream>>>(part, a);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
         return cudaSuccess;
     };
+    const bool d64 = p.D == 64;
     switch (p.score_kind) {
         case FLEX_SCORE_SOFTCAP:
-            return pick(dq_kernel<FLEX_SCORE_SOFTCAP>);
+            return d64 ? pick(dq_kernel<FLEX_SCORE_SOFTCAP>) : pick(dq128_kernel<FLEX_SCORE_SOFTCAP>);
         case FLEX_SCORE_ALIBI:
-            return pick(dq_kernel<FLEX_SCORE_ALIBI>);
+            return d64 ? pick(dq_kernel<FLEX_SCORE_ALIBI>) : pick(dq128_kernel<FLEX_SCORE_ALIBI>);
         default:
-            return pick(dq_kernel<FLEX_SCORE_IDENTITY>);
+            return d64 ? pick(dq_kernel<FLEX_SCORE_IDENTITY>) : pick(dq128_kernel<FLEX_SCORE_IDENTITY>);
     }
 }
 
