@@ -448,16 +448,16 @@ cudaError_t launch_bwd_fp32_score(const AttnProblem &p, const BwdArgs &a, bool d
     return cudaSuccess;
 }
 
-// fp32: delta, then dK/dV and dQ: at D = 64 on the tensor cores (three-way
-// bf16 split; dK/dV up to kBwdF32TcMaxQTiles q tiles), else the
-// register-tiled CUDA-core kernels.
+// fp32: delta, then dK/dV and dQ on the tensor cores (three-way bf16 split);
+// dK/dV of a q side longer than kBwdF32TcMaxQTiles tiles falls to the
+// register-tiled CUDA-core kernel.
 template <int D>
 cudaError_t launch_bwd_fp32(const AttnProblem &p, const BwdArgs &a, cudaStream_t stream) {
     const int64_t rows = (int64_t)p.B * p.H * p.q_len;
     attn_bwd_delta_kernel<D, float><<<(unsigned)((rows * 32 + 255) / 256), 256, 0, stream>>>(p, a, rows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const bool tc_dkdv = D == 64 && p.nqt <= kBwdF32TcMaxQTiles, tc_dq = true;
+    const bool tc_dkdv = p.nqt <= kBwdF32TcMaxQTiles, tc_dq = true;
     const BwdF32TcArgs ta{static_cast<const float *>(a.dout), a.delta, a.q_num, a.q_idx, a.fq_num, a.fq_idx,
                           static_cast<float *>(a.dk), static_cast<float *>(a.dv), static_cast<float *>(a.dq)};
     if (tc_dkdv && (e = launch_bwd_fp32_tc_dkdv(p, ta, stream)) != cudaSuccess) return e;

@@ -1,5 +1,5 @@
-// dK, dV and dQ of the block-sparse attention for float32 inputs at head dim
-// 64 on sm_103a tensor cores, with float32 accuracy kept by the three-way bf16
+// dK, dV and dQ of the block-sparse attention for float32 inputs at head
+// dims 64 and 128 on sm_103a tensor cores, with float32 accuracy kept by the three-way bf16
 // split of the float32 forward (bf16x3.cuh): every operand x = x1 + x2 + x3
 // and each product takes the six part products a1 b1 + a1 b2 + a2 b1 +
 // a1 b3 + a2 b2 + a3 b1, accumulated in float32 in tensor memory.
@@ -25,7 +25,10 @@
 //               its delta
 //   warp 12     one thread issues every MMA (warps 4 and 8 stay idle, so
 //               that the issuer shares its sub-partition with warp 0 only)
-// Tensor memory (512 columns): dV | dK | two buffers of S^T (64) | dP^T (64)
+// At head dim 128 the dK/dV kernel runs two CTAs per kv block, one per
+// 64-column half of dK and dV, and the dQ kernel keeps the Q parts in tensor
+// memory; the comments at those kernels give their layouts.
+// Tensor memory at head dim 64 (512 columns): dV | dK | two buffers of S^T (64) | dP^T (64)
 // | 64 more.  P^T and dS^T are split into bf16 parts over the columns they
 // were computed from, a half of the 64 q columns at a time: the parts of
 // columns 32h .. 32h + 31 take S^T (dP^T) columns 32h .. 32h + 31 and 16 of
@@ -1033,31 +1036,393 @@ __global__ void __launch_bounds__(16 * 32, 1) dq128_kernel(AttnProblem p, BwdF32
     }
 }
 
+// dK, dV at D = 128: one CTA per (128-row kv block, 64-column half h of
+// dK and dV).  V parts are the A operand of dP^T from tensor memory, K parts
+// the A operand of S^T from shared memory (96 KB); Q and dO stream in chunks
+// of 32 q rows through a two-stage ring.  S^T and dP^T are computed whole
+// (over all 128 head dims) by both halves' CTAs; each accumulates only its
+// half of dK and dV, so the accumulators, the V parts and two S^T/dP^T
+// buffers fit the 512 TMEM columns:
+// V1 | V2 | V3 (64 each) | dV_h (64) | dK_h (64) | two buffers of S^T (32) |
+// dP^T (32) | 32 spare (P3, dS3).
+namespace d128kv {
+constexpr int D = 128;
+constexpr int kQr = 32;                           // q rows per chunk
+constexpr uint32_t kVcol = 0, kDv = 192, kDk = 256;
+__host__ __device__ constexpr uint32_t buf_col(int b) { return 320u + 96u * (uint32_t)b; }
+constexpr uint32_t kKPart = 128 * D * 2;          // 32 KB: one part of the resident K (two 64-wide atoms)
+constexpr uint32_t kKAtom = 128 * 128;            // 128 rows x 64 bf16
+constexpr uint32_t kCPart = kQr * D * 2;          // 8 KB: one part of a 32-row Q or dO chunk
+constexpr uint32_t kCAtom = kQr * 128;            // 32 rows x 64 bf16
+constexpr uint32_t kK0 = 0, kSt0 = 3 * kKPart;
+constexpr uint32_t kStQ = 0, kStDo = 3 * kCPart, kStLse = 6 * kCPart, kStDelta = kStLse + kQr * 4;
+constexpr uint32_t kStBytes = 6 * kCPart + 1024;
+constexpr uint32_t kMiscOff = kSt0 + 2 * kStBytes;
+constexpr size_t kSmemBytes = kMiscOff + sizeof(Misc) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(buf_col(1) + 96 == kTmemCols, "tensor memory");
+static_assert(kSt0 % 1024 == 0 && kStBytes % 1024 == 0, "ring alignment");
+
+// 32 rows r0 .. r0 + 31 of a [.., len, 128] float32 tensor into registers
+// (zeros past len), then split into a 32-row tile (atoms of kCAtom).
+// Thread lt (0..127) takes units i = lt + 128 u: row i / 16, 8 floats at
+// column 8 (i % 16).
+struct Rows32 {
+    float4 x[8];
+};
+__device__ __forceinline__ void load32(Rows32 &g, const float *src, int64_t rs, int r0, int len, int lt) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = lt + 128 * u, r = i / 16, c = i % 16;
+        const bool in = r0 + r < len;
+        const float4 *p = reinterpret_cast<const float4 *>(src + (int64_t)(in ? r0 + r : 0) * rs) + 2 * c;
+        g.x[2 * u] = in ? __ldg(p) : make_float4(0.f, 0.f, 0.f, 0.f);
+        g.x[2 * u + 1] = in ? __ldg(p + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+__device__ __forceinline__ void store32(uint8_t *dst, const Rows32 &g, int lt) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int i = lt + 128 * u, r = i / 16, c = i % 16;
+        uint4 p1, p2, p3;
+        split3(g.x[2 * u].x, g.x[2 * u].y, p1.x, p2.x, p3.x);
+        split3(g.x[2 * u].z, g.x[2 * u].w, p1.y, p2.y, p3.y);
+        split3(g.x[2 * u + 1].x, g.x[2 * u + 1].y, p1.z, p2.z, p3.z);
+        split3(g.x[2 * u + 1].z, g.x[2 * u + 1].w, p1.w, p2.w, p3.w);
+        const uint32_t off = sw128_chunk(r, c, kCAtom);
+        *reinterpret_cast<uint4 *>(dst + off) = p1;
+        *reinterpret_cast<uint4 *>(dst + kCPart + off) = p2;
+        *reinterpret_cast<uint4 *>(dst + 2 * kCPart + off) = p3;
+    }
+}
+}  // namespace d128kv
+
+template <int SCORE>
+__global__ void __launch_bounds__(16 * 32, 1) dkdv128_kernel(AttnProblem p, BwdF32TcArgs a) {
+    namespace c = d128kv;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Misc &ms = *reinterpret_cast<Misc *>(smem + c::kMiscOff);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int kvb = (int)blockIdx.x / 2, dh = (int)blockIdx.x & 1;  // kv block, half of dK and dV
+    const int bh = p.bh_begin + (int)blockIdx.y, h = bh % p.H, b = bh / p.H;
+    const int kv0 = kvb * kBlock;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&ms.kv_ready, 8);  // K resident (Q group) and V in TMEM (elementwise warps)
+        for (int i = 0; i < 2; ++i) {
+            for (int g = 0; g < 2; ++g) {
+                mbar_init(&ms.st_full[i][g], 4);
+                mbar_init(&ms.st_empty[i][g], 1);
+            }
+            mbar_init(&ms.s_full[i], 1);
+            mbar_init(&ms.p_full[i], 4);
+        }
+        mbar_init(&ms.acc_full, 1);
+        mbar_init(&ms.drain, 1);
+        ms.abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        const TileLists lists{a.q_num, a.q_idx, a.fq_num, a.fq_idx, p.nkvb, p.nqb, p.kv_block, p.q_block, p.nqt};
+        for (int i = lane; i < p.nqt; i += 32) ms.flags[i] = 0u;
+        __syncwarp();
+        tl_mark_warp(lists, bh, kvb, 0, ms.flags, 0, p.nqt, lane);
+        __syncwarp();
+        const uint32_t expect = tl_expect(lists);
+        const unsigned lt = (1u << lane) - 1u;
+        int cnt = 0;
+        for (int base = 0; base < p.nqt; base += 32) {
+            const int i = base + lane;
+            const uint32_t w = i < p.nqt ? ms.flags[i] : 0u;
+            const bool on = tl_listed(w, 0);
+            const unsigned bal = __ballot_sync(0xffffffffu, on);
+            if (on) ms.list[cnt + __popc(bal & lt)] = (uint32_t)i | (tl_full(expect, w, 0) ? (1u << 16) : 0u);
+            cnt += __popc(bal);
+        }
+        if (lane == 0) ms.ntiles = cnt;
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&ms.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = ms.tmem_base;
+    volatile int *abort_flag = &ms.abort;
+    const int nchunk = 4 * ms.ntiles;  // four 32-row chunks per q tile
+    auto chunk_q0 = [&](int j) { return (int)(ms.list[j / 4] & 0xFFFFu) * kBlock + (j % 4) * c::kQr; };
+    const int qi = q_index(warp), di = do_index(warp);
+
+    if (qi >= 0 || di >= 0) {
+        // ----------------------------------------------------------- producers
+        const int lt = 32 * (qi >= 0 ? qi : di) + lane, grp = qi >= 0 ? 0 : 1;
+        if (grp == 0 && nchunk > 0) {
+            // the resident K: two 64-row halves of the 128-row tile
+            const float *kbase = static_cast<const float *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                d128::Rows64 g;
+                d128::load64(g, kbase, p.k_stride[2], kv0 + 64 * half, p.kv_len, lt);
+                d128::store64(smem + c::kK0, c::kKPart, c::kKAtom, 64 * half, g, lt);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.kv_ready);
+        }
+        const float *base = grp == 0 ? static_cast<const float *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1]
+                                     : a.dout + (int64_t)bh * p.q_len * c::D;
+        const int64_t rs = grp == 0 ? p.q_stride[2] : c::D;
+        const float *rowv_base = (grp == 0 ? p.lse : a.delta) + (int64_t)bh * p.q_len;
+        bool ok = true;
+        for (int j = 0; j < nchunk; ++j) {
+            const int s = j & 1;
+            const int q0 = chunk_q0(j);
+            c::Rows32 g;
+            c::load32(g, base, rs, q0, p.q_len, lt);
+            float rowv = 0.f;
+            if (lt < c::kQr) {
+                const int q = q0 + lt;
+                rowv = q < p.q_len ? rowv_base[q] : (grp == 0 ? -INFINITY : 0.f);
+            }
+            if (j >= 2 && !f32_warp_wait(&ms.st_empty[s][grp], (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            uint8_t *st = smem + c::kSt0 + s * c::kStBytes;
+            c::store32(st + (grp == 0 ? c::kStQ : c::kStDo), g, lt);
+            if (lt < c::kQr) reinterpret_cast<float *>(st + (grp == 0 ? c::kStLse : c::kStDelta))[lt] = rowv;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.st_full[s][grp]);
+        }
+        if (!ok) fail(ms, p.status);
+    } else if (warp == kMmaWarp) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0 && nchunk > 0) {
+            constexpr uint32_t kHi = smem_desc_hi_sw128(1024);
+            constexpr uint32_t idesc_kmaj = idesc_bf16_f32(128, c::kQr, 0, 0);  // S^T, dP^T: N = 32 q
+            constexpr uint32_t idesc_mn = idesc_bf16_f32(128, 64, 0, 1);       // dV_h, dK_h: N = 64, B MN-major
+            auto pa = [](int t) { return t == 2 || t == 4 ? 1 : t == 5 ? 2 : 0; };
+            auto pbp = [](int t) { return t == 1 || t == 4 ? 1 : t == 3 ? 2 : 0; };
+            const uint32_t kd = smem_desc_lo(smem_u32(smem + c::kK0), 16);
+            // dP^T(j) = V dO^T (A: V parts in TMEM), then S^T(j) = K Q^T (A: K
+            // parts in shared memory); K steps of 16 head dims
+            auto issue_sdp = [&](int j) -> bool {
+                const int s = j & 1;
+                const uint32_t st = smem_u32(smem + c::kSt0 + s * c::kStBytes);
+                const uint32_t qd = smem_desc_lo(st + c::kStQ, 16), gd = smem_desc_lo(st + c::kStDo, 16);
+                if (!mbar_wait(&ms.st_full[s][1], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < c::D / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t)
+                        mma_ts_lo<kHi>(tmem + c::buf_col(s) + 32, tmem + c::kVcol + 64 * pa(t) + 8 * k,
+                                       gd + ((pbp(t) * c::kCPart + (k / 4) * c::kCAtom + (k % 4) * 32) >> 4),
+                                       idesc_kmaj, (k > 0 || t > 0) ? 1u : 0u);
+                if (!mbar_wait(&ms.st_full[s][0], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int k = 0; k < c::D / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t)
+                        mma_ss_lo<kHi, kHi>(tmem + c::buf_col(s),
+                                            kd + ((pa(t) * c::kKPart + (k / 4) * c::kKAtom + (k % 4) * 32) >> 4),
+                                            qd + ((pbp(t) * c::kCPart + (k / 4) * c::kCAtom + (k % 4) * 32) >> 4),
+                                            idesc_kmaj, (k > 0 || t > 0) ? 1u : 0u);
+                mma_commit(&ms.s_full[s]);
+                return true;
+            };
+            // dV_h += P^T dO[:, h], then dK_h += dS^T Q[:, h] (B MN-major: the
+            // half's 64-wide atom, K steps of 16 q rows = 2048 bytes)
+            auto issue_acc = [&](int j) -> bool {
+                const int s = j & 1;
+                if (!mbar_wait(&ms.p_full[s], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+                const uint32_t st = smem_u32(smem + c::kSt0 + s * c::kStBytes);
+                const uint32_t qm = smem_desc_lo(st + c::kStQ + dh * c::kCAtom, c::kCAtom);
+                const uint32_t gm = smem_desc_lo(st + c::kStDo + dh * c::kCAtom, c::kCAtom);
+                const uint32_t bc = c::buf_col(s);
+#pragma unroll
+                for (int k = 0; k < c::kQr / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t) {
+                        const int ap = pa(t);
+                        const uint32_t pcol = ap < 2 ? bc + 16u * ap + 8u * k : bc + 64u + 8u * k;
+                        mma_ts_lo<kHi>(tmem + c::kDv, tmem + pcol, gm + ((pbp(t) * c::kCPart + k * 2048) >> 4),
+                                       idesc_mn, (j > 0 || k > 0 || t > 0) ? 1u : 0u);
+                    }
+                mma_commit(&ms.st_empty[s][1]);
+#pragma unroll
+                for (int k = 0; k < c::kQr / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t) {
+                        const int ap = pa(t);
+                        const uint32_t dcol = ap < 2 ? bc + 32u + 16u * ap + 8u * k : bc + 80u + 8u * k;
+                        mma_ts_lo<kHi>(tmem + c::kDk, tmem + dcol, qm + ((pbp(t) * c::kCPart + k * 2048) >> 4),
+                                       idesc_mn, (j > 0 || k > 0 || t > 0) ? 1u : 0u);
+                    }
+                mma_commit(&ms.st_empty[s][0]);
+                return true;
+            };
+            bool ok = mbar_wait(&ms.kv_ready, 0, abort_flag);
+            if (ok) tc_fence_after_sync();
+            for (int j = 0; ok && j < min(nchunk, 2); ++j) ok = issue_sdp(j);
+            // S^T(j + 2) reuses the buffer dV(j), dK(j) read: MMAs of one thread run in order
+            for (int j = 0; ok && j < nchunk; ++j) ok = issue_acc(j) && (j + 2 >= nchunk || issue_sdp(j + 2));
+            if (ok) mma_commit(&ms.acc_full);
+            if (!ok) fail(ms, p.status);
+            mma_commit(&ms.drain);
+            int never = 0;
+            (void)mbar_wait(&ms.drain, 0, &never);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ---------------------------------------------------------- elementwise
+        const int kv = kv0 + (int)threadIdx.x;
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        const float slope = SCORE == FLEX_SCORE_ALIBI ? exp2f(-8.f * (float)(h + 1) / (float)p.H) : 0.f;
+        const float scale = p.scale;
+        bool ok = true;
+        if (nchunk > 0) {
+            // this kv row of V -> V1, V2, V3 columns of this lane (bf16 pairs)
+            const bool kv_in = kv < p.kv_len;
+            const float *vrow = static_cast<const float *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1] +
+                                (int64_t)(kv_in ? kv : 0) * p.v_stride[2];
+#pragma unroll 1
+            for (int c0 = 0; c0 < c::D; c0 += 32) {
+                float4 x[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    x[j] = kv_in ? __ldg(reinterpret_cast<const float4 *>(vrow + c0) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                uint32_t w1[16], w2[16], w3[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    split3(f4_at(x[j / 2], 2 * (j % 2)), f4_at(x[j / 2], 2 * (j % 2) + 1), w1[j], w2[j], w3[j]);
+                tmem_st16(trow + c::kVcol + c0 / 2, w1);
+                tmem_st16(trow + c::kVcol + 64 + c0 / 2, w2);
+                tmem_st16(trow + c::kVcol + 128 + c0 / 2, w3);
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.kv_ready);
+        }
+        for (int j = 0; j < nchunk; ++j) {
+            const int s = j & 1;
+            const bool full = (ms.list[j / 4] >> 16) & 1u;
+            const int q0 = chunk_q0(j);
+            if (!f32_warp_wait(&ms.s_full[s], (uint32_t)(j >> 1) & 1u, abort_flag) ||
+                !f32_warp_wait(&ms.st_full[s][0], (uint32_t)(j >> 1) & 1u, abort_flag) ||
+                !f32_warp_wait(&ms.st_full[s][1], (uint32_t)(j >> 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const float *lse_s = reinterpret_cast<const float *>(smem + c::kSt0 + s * c::kStBytes + c::kStLse);
+            const float *dl_s = reinterpret_cast<const float *>(smem + c::kSt0 + s * c::kStBytes + c::kStDelta);
+            uint32_t sr[32], dr[32];
+            f32_ld32(trow + c::buf_col(s), sr);
+            f32_ld32(trow + c::buf_col(s) + 32, dr);
+            float pv[32], dsv[32];
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+                const int q = q0 + cc;
+                const float lse = lse_s[cc];
+                const bool keep = lse != -INFINITY && (full || (kv < p.kv_len && mask_mod(p.mask, b, q, kv)));
+                float grad;
+                const float x = score_t<SCORE>(p.score_param, __uint_as_float(sr[cc]) * scale, slope, q, kv, grad);
+                const float pr = keep ? ex2_approx(fmaf(x, kLog2e, -lse * kLog2e)) : 0.f;
+                pv[cc] = pr;
+                dsv[cc] = keep ? scale * pr * (__uint_as_float(dr[cc]) - dl_s[cc]) * grad : 0.f;
+            }
+            uint32_t w1[16], w2[16], w3[16];
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc) split3(pv[2 * cc], pv[2 * cc + 1], w1[cc], w2[cc], w3[cc]);
+            tmem_st16(trow + c::buf_col(s), w1);        // over S^T, all read above
+            tmem_st16(trow + c::buf_col(s) + 16, w2);
+            tmem_st16(trow + c::buf_col(s) + 64, w3);
+#pragma unroll
+            for (int cc = 0; cc < 16; ++cc) split3(dsv[2 * cc], dsv[2 * cc + 1], w1[cc], w2[cc], w3[cc]);
+            tmem_st16(trow + c::buf_col(s) + 32, w1);   // over dP^T, all read above
+            tmem_st16(trow + c::buf_col(s) + 48, w2);
+            tmem_st16(trow + c::buf_col(s) + 80, w3);
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.p_full[s]);
+        }
+        // ------------------------------------------------------------ epilogue
+        const bool have = ok && nchunk > 0;
+        if (have && !f32_warp_wait(&ms.acc_full, 0, abort_flag)) ok = false;
+        if (!ok) fail(ms, p.status);
+        if (ok) {
+            tc_fence_after_sync();
+            const int64_t orow = (int64_t)bh * p.kv_len + (kv < p.kv_len ? kv : 0);
+#pragma unroll 1
+            for (int o = 0; o < 2; ++o) {  // dV_h, then dK_h
+                float *dst = (o ? a.dk : a.dv) + orow * c::D + 64 * dh;
+#pragma unroll 1
+                for (int c0 = 0; c0 < 64; c0 += 32) {  // every lane takes the warp-collective loads
+                    uint32_t r[32];
+                    if (have) {
+                        f32_ld32(trow + (o ? c::kDk : c::kDv) + c0, r);
+                    } else {
+#pragma unroll
+                        for (int cc = 0; cc < 32; ++cc) r[cc] = 0u;
+                    }
+                    if (kv < p.kv_len) {
+#pragma unroll
+                        for (int cc = 0; cc < 32; cc += 4)
+                            *reinterpret_cast<float4 *>(dst + c0 + cc) =
+                                make_float4(__uint_as_float(r[cc]), __uint_as_float(r[cc + 1]),
+                                            __uint_as_float(r[cc + 2]), __uint_as_float(r[cc + 3]));
+                    }
+                }
+            }
+        }
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
 }  // namespace bwdf32
 
-// dK and dV of fp32 inputs at D = 64 on the tensor cores (p.D == 64; p.nqt
-// <= kBwdF32TcMaxQTiles).
+// dK and dV of fp32 inputs on the tensor cores (p.D == 64 or 128; p.nqt <=
+// kBwdF32TcMaxQTiles).
 inline cudaError_t launch_bwd_fp32_tc_dkdv(const AttnProblem &p, const BwdF32TcArgs &a, cudaStream_t stream) {
     using namespace bwdf32;
+    const bool d64 = p.D == 64;
+    const size_t smem = d64 ? kSmemBytes : d128kv::kSmemBytes;
+    // D = 128: two CTAs per kv block, one per half of dK and dV
+    const unsigned gx = (unsigned)p.nkvt * (d64 ? 1u : 2u);
     auto pick = [&](auto kern) -> cudaError_t {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         for (int begin = 0; begin < p.B * p.H; begin += 65535) {
             AttnProblem part = p;
             part.bh_begin = begin;
             const int count = p.B * p.H - begin < 65535 ? p.B * p.H - begin : 65535;
-            kern<<<dim3(p.nkvt, count), kThreads, kSmemBytes, stream>>>(part, a);
+            kern<<<dim3(gx, count), kThreads, smem, stream>>>(part, a);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
         return cudaSuccess;
     };
     switch (p.score_kind) {
         case FLEX_SCORE_SOFTCAP:
-            return pick(dkdv_kernel<FLEX_SCORE_SOFTCAP>);
+            return d64 ? pick(dkdv_kernel<FLEX_SCORE_SOFTCAP>) : pick(dkdv128_kernel<FLEX_SCORE_SOFTCAP>);
         case FLEX_SCORE_ALIBI:
-            return pick(dkdv_kernel<FLEX_SCORE_ALIBI>);
+            return d64 ? pick(dkdv_kernel<FLEX_SCORE_ALIBI>) : pick(dkdv128_kernel<FLEX_SCORE_ALIBI>);
         default:
-            return pick(dkdv_kernel<FLEX_SCORE_IDENTITY>);
+            return d64 ? pick(dkdv_kernel<FLEX_SCORE_IDENTITY>) : pick(dkdv128_kernel<FLEX_SCORE_IDENTITY>);
     }
 }
 

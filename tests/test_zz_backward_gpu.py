@@ -9,7 +9,9 @@ rounded to bf16 (2^-9 relative each, errors that average out over the
 summed keys), each gradient is rounded to bf16 (2^-9), and delta = dout . out
 is taken from the forward's bf16-rounded out (2^-9 on the row term of dS),
 so 1e-2 = 5 x 2^-9 of the largest gradient bounds their sum.  The fp32 path
-runs in fp32 on the CUDA cores.  The forward's out and lse come from the
+runs on the tensor cores with every operand split into three bf16 parts
+(six part products, float32 accumulation: about 2^-22 relative per
+product), well inside 1e-4.  The forward's out and lse come from the
 library's own forward, as a caller would pass them; the oracle
 differentiates the exact attention.
 """
@@ -130,6 +132,18 @@ def test_backward_medium():
     got = _backward(q, k, v, g, W.MASK_CAUSAL, W.SCORE_ALIBI, scale, "bf16")
     ref = oracle.attention_bwd(q, k, v, g, W.MASK_CAUSAL, W.SCORE_ALIBI, scale)
     _compare(got, ref, "bf16", "medium")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_backward_medium_fp32(D):
+    # causal + softcap, fp32, S = 2048: sixteen q tiles per head, so the
+    # two-stage chunk rings of the tensor-core kernels wrap many times
+    B, H, S = 1, 2, 2048
+    q, k, v, g = _draw(B, H, S, S, D, 36, "fp32")
+    scale = 1.0 / np.sqrt(D)
+    got = _backward(q, k, v, g, W.MASK_CAUSAL, W.SCORE_SOFTCAP, scale, "fp32", score_param=20.0)
+    ref = oracle.attention_bwd(q, k, v, g, W.MASK_CAUSAL, W.SCORE_SOFTCAP, scale, score_param=20.0)
+    _compare(got, ref, "fp32", f"medium fp32 D{D}")
 
 
 def test_backward_at_scale():
