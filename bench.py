@@ -372,10 +372,21 @@ def kernel_option_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flush,
             "tflops": {name: flops / (t * 1e-3) / 1e12 for name, t in ms.items()}}
 
 
-# fp32 FMA on the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (maximum SM clock)
-FP32_CUDA_CORE_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
-# bf16 MMA FLOPs the float32 forward executes per algorithmic FLOP (three-way split, six products)
+# bf16 MMA FLOPs the float32 path executes per product FLOP (three-way split, six products)
 FP32_SPLIT_PRODUCTS = 6
+
+
+def fp32_bwd_executed(D):
+    """Product FLOPs the fp32 backward executes per algorithmic FLOP (10 D per
+    computed pair): S and dP are recomputed by the dK/dV and the dQ kernels
+    (14 D), and at D = 128 by both 64-column halves of dK/dV (18 D)."""
+    return 1.4 if D == 64 else 1.8
+
+
+def fp32_bwd_kernels(D):
+    if D == 64:
+        return "attn_bwd_delta (CUDA cores) + bwdf32::dkdv_kernel + bwdf32::dq_kernel (tcgen05)"
+    return "attn_bwd_delta (CUDA cores) + bwdf32::dkdv128_kernel + bwdf32::dq128_kernel (tcgen05)"
 
 
 def fp32_scale_timings(fa, torch, device_index: int, steps: int, peaks: dict) -> dict | None:
@@ -444,18 +455,10 @@ def fp32_scale_timings(fa, torch, device_index: int, steps: int, peaks: dict) ->
             raise RuntimeError(f"device status reported a timeout in the backward on {w.name}")
         ms_b = float(np.mean([a.elapsed_time(b) for a, b in evb]))
         bwd_tflops = 2.5 * flops / (ms_b * 1e-3) / 1e12
-        if D == 64:
-            # tensor cores (three-way bf16 split): 14 D of executed product FLOPs per
-            # computed pair (score and dP recomputed in both kernels), six bf16 MMAs each
-            bwd_roof = {"bound": "tensor", "peak": ceiling, "frac": bwd_tflops / ceiling,
-                        "peak_source": "measured bf16 burst / 6",
-                        "executed_bf16_mma_tflops": bwd_tflops * 1.4 * FP32_SPLIT_PRODUCTS,
-                        "kernels": "attn_bwd_delta (CUDA cores) + bwdf32::dkdv_kernel + bwdf32::dq_kernel (tcgen05)"}
-        else:
-            # dK/dV on the CUDA cores (most of the time), dQ on the tensor cores
-            bwd_roof = {"bound": "alu", "peak": FP32_CUDA_CORE_TFLOPS, "frac": bwd_tflops / FP32_CUDA_CORE_TFLOPS,
-                        "kernels": "attn_bwd_delta + attn_bwd_dkdv (fp32 FMA, CUDA cores) + bwdf32::dq128_kernel "
-                                   "(tcgen05, three-way bf16 split)"}
+        bwd_roof = {"bound": "tensor", "peak": ceiling, "frac": bwd_tflops / ceiling,
+                    "peak_source": "measured bf16 burst / 6",
+                    "executed_bf16_mma_tflops": bwd_tflops * fp32_bwd_executed(D) * FP32_SPLIT_PRODUCTS,
+                    "kernels": fp32_bwd_kernels(D)}
         res[w.name] = {"ms_per_launch": ms, "unmasked_block_flops": flops, "tflops": achieved,
                        "executed_bf16_mma_tflops": FP32_SPLIT_PRODUCTS * achieved,
                        "frac_of_ceiling": achieved / ceiling,
@@ -513,10 +516,11 @@ def backward_timings(fa, torch, w, dq, dk, dv, bm, out, lse, stream, flops_fwd, 
                 "executed_mma_flops": 3.5 * flops_fwd,
                 "kernels": "attn_bwd_delta (CUDA cores) + attn_bwd_tc<dK,dV> + attn_bwd_tc<dQ> (tcgen05)"}
     else:
-        roof = {"bound": "alu", "achieved": achieved, "peak": FP32_CUDA_CORE_TFLOPS, "unit": "TFLOP/s",
-                "frac": achieved / FP32_CUDA_CORE_TFLOPS,
-                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz",
-                "kernels": "attn_bwd_delta + attn_bwd_dkdv + attn_bwd_dq (fp32 FMA, CUDA cores)"}
+        ceiling = peaks["bf16"] / FP32_SPLIT_PRODUCTS
+        roof = {"bound": "tensor", "achieved": achieved, "peak": ceiling, "unit": "TFLOP/s",
+                "frac": achieved / ceiling, "peak_source": f"{peaks['source']} bf16 burst / 6",
+                "executed_bf16_mma_flops": fp32_bwd_executed(w.D) * FP32_SPLIT_PRODUCTS * flops,
+                "kernels": fp32_bwd_kernels(w.D)}
     return {"api": "flex_attention_bwd", "launches": steps, "ms_per_launch": ms, "algorithmic_flops": flops,
             "roofline": roof}
 

@@ -25,8 +25,8 @@
 //               its delta
 //   warp 12     one thread issues every MMA (warps 4 and 8 stay idle, so
 //               that the issuer shares its sub-partition with warp 0 only)
-// At head dim 128 the dK/dV kernel runs two CTAs per kv block, one per
-// 64-column half of dK and dV, and the dQ kernel keeps the Q parts in tensor
+// At head dim 128 the dK/dV kernel runs two CTAs per kv block, one for dK
+// and one for dV, and the dQ kernel keeps the Q parts in tensor
 // memory; the comments at those kernels give their layouts.
 // Tensor memory at head dim 64 (512 columns): dV | dK | two buffers of S^T (64) | dP^T (64)
 // | 64 more.  P^T and dS^T are split into bf16 parts over the columns they
@@ -1036,37 +1036,62 @@ __global__ void __launch_bounds__(16 * 32, 1) dq128_kernel(AttnProblem p, BwdF32
     }
 }
 
-// dK, dV at D = 128: one CTA per (128-row kv block, 64-column half h of
-// dK and dV).  V parts are the A operand of dP^T from tensor memory, K parts
-// the A operand of S^T from shared memory (96 KB); Q and dO stream in chunks
-// of 32 q rows through a two-stage ring.  S^T and dP^T are computed whole
-// (over all 128 head dims) by both halves' CTAs; each accumulates only its
-// half of dK and dV, so the accumulators, the V parts and two S^T/dP^T
-// buffers fit the 512 TMEM columns:
-// V1 | V2 | V3 (64 each) | dV_h (64) | dK_h (64) | two buffers of S^T (32) |
-// dP^T (32) | 32 spare (P3, dS3).
+// dK and dV at D = 128: two CTAs per 128-row kv block, so that each holds
+// one accumulator of all 128 columns and only the products it needs.
+//   role 0 (dK): S^T = K Q^T (K parts resident in shared memory), dP^T = V
+//     dO^T (V parts the A operand from tensor memory), dS^T elementwise and
+//     dK += dS^T Q, over the q side in chunks of 32 rows;
+//   role 1 (dV): S^T = K Q^T (K parts the A operand from tensor memory), P^T
+//     elementwise and dV += P^T dO, in chunks of 64 q rows; it needs neither
+//     dP^T nor delta.
+// Tensor memory (512 columns): A parts (V or K: 3 x 64) | accumulator (128) |
+// two buffers: role 0 S^T (32) | dP^T (32), the dS^T parts over dP^T and the
+// first half of S^T; role 1 S^T (64) | P3 (32), P1 and P2 over S^T.
+// The row values of a chunk (lse, delta) travel with the half of its ring
+// stage that is freed last: the Q half in role 0 (read by dK), the dO half
+// in role 1 (read by dV); the other half is freed as soon as its one MMA
+// group has read it.
 namespace d128kv {
 constexpr int D = 128;
-constexpr int kQr = 32;                           // q rows per chunk
-constexpr uint32_t kVcol = 0, kDv = 192, kDk = 256;
-__host__ __device__ constexpr uint32_t buf_col(int b) { return 320u + 96u * (uint32_t)b; }
-constexpr uint32_t kKPart = 128 * D * 2;          // 32 KB: one part of the resident K (two 64-wide atoms)
-constexpr uint32_t kKAtom = 128 * 128;            // 128 rows x 64 bf16
-constexpr uint32_t kCPart = kQr * D * 2;          // 8 KB: one part of a 32-row Q or dO chunk
-constexpr uint32_t kCAtom = kQr * 128;            // 32 rows x 64 bf16
-constexpr uint32_t kK0 = 0, kSt0 = 3 * kKPart;
-constexpr uint32_t kStQ = 0, kStDo = 3 * kCPart, kStLse = 6 * kCPart, kStDelta = kStLse + kQr * 4;
-constexpr uint32_t kStBytes = 6 * kCPart + 1024;
-constexpr uint32_t kMiscOff = kSt0 + 2 * kStBytes;
+constexpr uint32_t kA = 0, kAcc = 192;
+constexpr uint32_t kKPart = 128 * D * 2;  // 32 KB: one part of role 0's resident K (two 64-wide atoms)
+constexpr uint32_t kKAtom = 128 * 128;    // 128 rows x 64 bf16
+template <int ROLE>
+struct Role;
+template <>
+struct Role<0> {
+    static constexpr int kQr = 32;                                 // q rows per chunk
+    static constexpr uint32_t kCPart = kQr * D * 2, kCAtom = kQr * 128;
+    static constexpr uint32_t kSt0 = 3 * kKPart;                   // after the resident K
+    static constexpr uint32_t kStQ = 0, kStDo = 3 * kCPart, kStRows = 6 * kCPart;  // rows: lse[32], delta[32]
+    static constexpr uint32_t kStBytes = 6 * kCPart + 1024;
+    static constexpr uint32_t kBufCols = 64;
+    static constexpr int kRowGrp = 0, kRowVals = 64;
+};
+template <>
+struct Role<1> {
+    static constexpr int kQr = 64;
+    static constexpr uint32_t kCPart = kQr * D * 2, kCAtom = kQr * 128;
+    static constexpr uint32_t kSt0 = 0;
+    static constexpr uint32_t kStQ = 0, kStDo = 3 * kCPart, kStRows = 6 * kCPart;  // rows: lse[64]
+    static constexpr uint32_t kStBytes = 6 * kCPart + 1024;
+    static constexpr uint32_t kBufCols = 96;
+    static constexpr int kRowGrp = 1, kRowVals = 64;
+};
+template <int ROLE>
+__host__ __device__ constexpr uint32_t buf_col(int b) { return 320u + Role<ROLE>::kBufCols * (uint32_t)b; }
+constexpr uint32_t kMiscOff = 3 * kKPart + 2 * Role<0>::kStBytes;
+static_assert(kMiscOff == 2 * Role<1>::kStBytes, "both roles place Misc at one offset");
 constexpr size_t kSmemBytes = kMiscOff + sizeof(Misc) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-static_assert(buf_col(1) + 96 == kTmemCols, "tensor memory");
-static_assert(kSt0 % 1024 == 0 && kStBytes % 1024 == 0, "ring alignment");
+static_assert(buf_col<0>(2) <= kTmemCols && buf_col<1>(2) == kTmemCols, "tensor memory");
+static_assert(Role<0>::kStBytes % 1024 == 0 && Role<1>::kStBytes % 1024 == 0 && (3 * kKPart) % 1024 == 0,
+              "ring alignment");
 
 // 32 rows r0 .. r0 + 31 of a [.., len, 128] float32 tensor into registers
-// (zeros past len), then split into a 32-row tile (atoms of kCAtom).
-// Thread lt (0..127) takes units i = lt + 128 u: row i / 16, 8 floats at
-// column 8 (i % 16).
+// (zeros past len), then split into a 32-row tile (atoms of 32 rows x 128
+// bytes).  Thread lt (0..127) takes units i = lt + 128 u: row i / 16, 8
+// floats at column 8 (i % 16).
 struct Rows32 {
     float4 x[8];
 };
@@ -1081,6 +1106,7 @@ __device__ __forceinline__ void load32(Rows32 &g, const float *src, int64_t rs, 
     }
 }
 __device__ __forceinline__ void store32(uint8_t *dst, const Rows32 &g, int lt) {
+    constexpr uint32_t kPart = Role<0>::kCPart;
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         const int i = lt + 128 * u, r = i / 16, c = i % 16;
@@ -1089,27 +1115,327 @@ __device__ __forceinline__ void store32(uint8_t *dst, const Rows32 &g, int lt) {
         split3(g.x[2 * u].z, g.x[2 * u].w, p1.y, p2.y, p3.y);
         split3(g.x[2 * u + 1].x, g.x[2 * u + 1].y, p1.z, p2.z, p3.z);
         split3(g.x[2 * u + 1].z, g.x[2 * u + 1].w, p1.w, p2.w, p3.w);
-        const uint32_t off = sw128_chunk(r, c, kCAtom);
+        const uint32_t off = sw128_chunk(r, c, Role<0>::kCAtom);
         *reinterpret_cast<uint4 *>(dst + off) = p1;
-        *reinterpret_cast<uint4 *>(dst + kCPart + off) = p2;
-        *reinterpret_cast<uint4 *>(dst + 2 * kCPart + off) = p3;
+        *reinterpret_cast<uint4 *>(dst + kPart + off) = p2;
+        *reinterpret_cast<uint4 *>(dst + 2 * kPart + off) = p3;
     }
 }
+// The rows of a chunk into registers, then into the ring (role 0: 32 rows,
+// role 1: 64 rows, both with atoms of the chunk's rows x 128 bytes).
+template <int ROLE>
+struct Chunk {
+    Rows32 g;
+    __device__ __forceinline__ void load(const float *src, int64_t rs, int r0, int len, int lt) {
+        load32(g, src, rs, r0, len, lt);
+    }
+    __device__ __forceinline__ void store(uint8_t *dst, int lt) const { store32(dst, g, lt); }
+};
+template <>
+struct Chunk<1> {
+    d128::Rows64 g;
+    __device__ __forceinline__ void load(const float *src, int64_t rs, int r0, int len, int lt) {
+        d128::load64(g, src, rs, r0, len, lt);
+    }
+    __device__ __forceinline__ void store(uint8_t *dst, int lt) const {
+        d128::store64(dst, Role<1>::kCPart, Role<1>::kCAtom, 0, g, lt);
+    }
+};
 }  // namespace d128kv
+
+template <int SCORE, int ROLE>
+__device__ __forceinline__ void dkdv128_role(const AttnProblem &p, const BwdF32TcArgs &a, uint8_t *smem, Misc &ms,
+                                             int kvb, int bh, int warp, int lane) {
+    namespace c = d128kv;
+    using R = c::Role<ROLE>;
+    const int h = bh % p.H, b = bh / p.H;
+    const int kv0 = kvb * kBlock;
+    const uint32_t tmem = ms.tmem_base;
+    volatile int *abort_flag = &ms.abort;
+    constexpr int kPerTile = kBlock / R::kQr;
+    const int nchunk = kPerTile * ms.ntiles;
+    auto chunk_q0 = [&](int j) { return (int)(ms.list[j / kPerTile] & 0xFFFFu) * kBlock + (j % kPerTile) * R::kQr; };
+    auto stage = [&](int s) { return smem + R::kSt0 + s * R::kStBytes; };
+    const int qi = q_index(warp), di = do_index(warp);
+
+    if (qi >= 0 || di >= 0) {
+        // ----------------------------------------------------------- producers
+        const int lt = 32 * (qi >= 0 ? qi : di) + lane, grp = qi >= 0 ? 0 : 1;
+        if (ROLE == 0 && grp == 0 && nchunk > 0) {
+            // role 0's resident K: two 64-row halves of the 128-row tile
+            const float *kbase = static_cast<const float *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                d128::Rows64 g;
+                d128::load64(g, kbase, p.k_stride[2], kv0 + 64 * half, p.kv_len, lt);
+                d128::store64(smem, c::kKPart, c::kKAtom, 64 * half, g, lt);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.kv_ready);
+        }
+        const float *base = grp == 0 ? static_cast<const float *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1]
+                                     : a.dout + (int64_t)bh * p.q_len * c::D;
+        const int64_t rs = grp == 0 ? p.q_stride[2] : c::D;
+        const float *lse_g = p.lse + (int64_t)bh * p.q_len, *delta_g = a.delta + (int64_t)bh * p.q_len;
+        const bool rows = grp == R::kRowGrp && lt < R::kRowVals;
+        bool ok = true;
+        for (int j = 0; j < nchunk; ++j) {
+            const int s = j & 1;
+            const int q0 = chunk_q0(j);
+            c::Chunk<ROLE> g;
+            g.load(base, rs, q0, p.q_len, lt);
+            // role 0: lse of rows 0-31, then delta; role 1: lse of rows 0-63
+            float rowv = 0.f;
+            if (rows) {
+                const bool is_lse = ROLE == 1 || lt < 32;
+                const int q = q0 + (is_lse ? lt : lt - 32);
+                rowv = q < p.q_len ? (is_lse ? lse_g[q] : delta_g[q]) : (is_lse ? -INFINITY : 0.f);
+            }
+            if (j >= 2 && !f32_warp_wait(&ms.st_empty[s][grp], (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            g.store(stage(s) + (grp == 0 ? R::kStQ : R::kStDo), lt);
+            if (rows) reinterpret_cast<float *>(stage(s) + R::kStRows)[lt] = rowv;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.st_full[s][grp]);
+        }
+        if (!ok) fail(ms, p.status);
+    } else if (warp == kMmaWarp) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0 && nchunk > 0) {
+            constexpr uint32_t kHi = smem_desc_hi_sw128(1024);
+            constexpr uint32_t idesc_kmaj = idesc_bf16_f32(128, R::kQr, 0, 0);  // S^T, dP^T: N = chunk rows
+            constexpr uint32_t idesc_mn = idesc_bf16_f32(128, c::D, 0, 1);      // dK, dV: N = 128, B MN-major
+            auto pa = [](int t) { return t == 2 || t == 4 ? 1 : t == 5 ? 2 : 0; };
+            auto pbp = [](int t) { return t == 1 || t == 4 ? 1 : t == 3 ? 2 : 0; };
+            // The K steps stay rolled loops: unrolled, the issue code of the
+            // MMAs no longer fits the instruction cache beside the other roles'
+            // (measured: the issue rate and the elementwise warps both slowed).
+            // K-major B of a chunk (rows = q), part pt, K step k of 16 head dims
+            auto kstep = [](int pt, int k) {
+                return (pt * R::kCPart + (k / 4) * R::kCAtom + (k % 4) * 32) >> 4;
+            };
+            // role 0: dP^T(j) = V dO^T, free the dO half, then S^T(j) = K Q^T
+            // role 1: S^T(j) = K Q^T, free the Q half
+            auto issue_s = [&](int j) -> bool {
+                const int s = j & 1;
+                const uint32_t st = smem_u32(stage(s));
+                const uint32_t qd = smem_desc_lo(st + R::kStQ, 16);
+                if (ROLE == 0) {
+                    const uint32_t gd = smem_desc_lo(st + R::kStDo, 16);
+                    if (!mbar_wait(&ms.st_full[s][1], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                    tc_fence_after_sync();
+#pragma unroll 1
+                    for (int k = 0; k < c::D / 16; ++k)
+#pragma unroll
+                        for (int t = 0; t < 6; ++t)
+                            mma_ts_lo<kHi>(tmem + c::buf_col<ROLE>(s) + 32, tmem + c::kA + 64 * pa(t) + 8 * k,
+                                           gd + kstep(pbp(t), k), idesc_kmaj, (k > 0 || t > 0) ? 1u : 0u);
+                    mma_commit(&ms.st_empty[s][1]);
+                }
+                if (!mbar_wait(&ms.st_full[s][0], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+                if (ROLE == 0) {
+                    const uint32_t kd = smem_desc_lo(smem_u32(smem), 16);
+#pragma unroll 1
+                    for (int k = 0; k < c::D / 16; ++k)
+#pragma unroll
+                        for (int t = 0; t < 6; ++t)
+                            mma_ss_lo<kHi, kHi>(tmem + c::buf_col<ROLE>(s),
+                                                kd + ((pa(t) * c::kKPart + (k / 4) * c::kKAtom + (k % 4) * 32) >> 4),
+                                                qd + kstep(pbp(t), k), idesc_kmaj, (k > 0 || t > 0) ? 1u : 0u);
+                } else {
+#pragma unroll 1
+                    for (int k = 0; k < c::D / 16; ++k)
+#pragma unroll
+                        for (int t = 0; t < 6; ++t)
+                            mma_ts_lo<kHi>(tmem + c::buf_col<ROLE>(s), tmem + c::kA + 64 * pa(t) + 8 * k,
+                                           qd + kstep(pbp(t), k), idesc_kmaj, (k > 0 || t > 0) ? 1u : 0u);
+                    mma_commit(&ms.st_empty[s][0]);
+                }
+                mma_commit(&ms.s_full[s]);
+                return true;
+            };
+            // role 0: dK += dS^T Q; role 1: dV += P^T dO (B MN-major: two
+            // 64-wide slabs one atom apart, K steps of 16 q rows = 2048 bytes)
+            auto issue_acc = [&](int j) -> bool {
+                const int s = j & 1;
+                if (!mbar_wait(&ms.p_full[s], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                if (ROLE == 1 && !mbar_wait(&ms.st_full[s][1], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+                const uint32_t bm =
+                    smem_desc_lo(smem_u32(stage(s)) + (ROLE == 0 ? R::kStQ : R::kStDo), R::kCAtom);
+                const uint32_t bc = c::buf_col<ROLE>(s);
+#pragma unroll 1
+                for (int k = 0; k < R::kQr / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t) {
+                        const int ap = pa(t);
+                        // role 0: dS1, dS2 over dP^T, dS3 over S^T; role 1: P1, P2
+                        // over S^T columns 32 (k / 2) .., P3 in the spare columns
+                        const uint32_t col =
+                            ROLE == 0 ? (ap < 2 ? bc + 32u + 16u * ap + 8u * k : bc + 8u * k)
+                                      : (ap < 2 ? bc + 32u * (k / 2) + 16u * ap + 8u * (k % 2)
+                                                : bc + 64u + 16u * (k / 2) + 8u * (k % 2));
+                        mma_ts_lo<kHi>(tmem + c::kAcc, tmem + col, bm + ((pbp(t) * R::kCPart + k * 2048) >> 4),
+                                       idesc_mn, (j > 0 || k > 0 || t > 0) ? 1u : 0u);
+                    }
+                mma_commit(&ms.st_empty[s][ROLE == 0 ? 0 : 1]);
+                return true;
+            };
+            bool ok = mbar_wait(&ms.kv_ready, 0, abort_flag);
+            if (ok) tc_fence_after_sync();
+            for (int j = 0; ok && j < min(nchunk, 2); ++j) ok = issue_s(j);
+            // S^T(j + 2) reuses the buffer acc(j) read: MMAs of one thread run in order
+            for (int j = 0; ok && j < nchunk; ++j) ok = issue_acc(j) && (j + 2 >= nchunk || issue_s(j + 2));
+            if (ok) mma_commit(&ms.acc_full);
+            if (!ok) fail(ms, p.status);
+            mma_commit(&ms.drain);  // every MMA issued above completes before TMEM is freed
+            int never = 0;
+            (void)mbar_wait(&ms.drain, 0, &never);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ---------------------------------------------------------- elementwise
+        const int kv = kv0 + (int)threadIdx.x;
+        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        const float slope = SCORE == FLEX_SCORE_ALIBI ? exp2f(-8.f * (float)(h + 1) / (float)p.H) : 0.f;
+        const float scale = p.scale;
+        bool ok = true;
+        if (nchunk > 0) {
+            // this kv row of V (role 0) or K (role 1) -> the three A parts (bf16 pairs)
+            const bool kv_in = kv < p.kv_len;
+            const float *arow =
+                ROLE == 0 ? static_cast<const float *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1] +
+                                (int64_t)(kv_in ? kv : 0) * p.v_stride[2]
+                          : static_cast<const float *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1] +
+                                (int64_t)(kv_in ? kv : 0) * p.k_stride[2];
+#pragma unroll 1
+            for (int c0 = 0; c0 < c::D; c0 += 32) {
+                float4 x[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    x[i] = kv_in ? __ldg(reinterpret_cast<const float4 *>(arow + c0) + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                uint32_t w1[16], w2[16], w3[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    split3(f4_at(x[i / 2], 2 * (i % 2)), f4_at(x[i / 2], 2 * (i % 2) + 1), w1[i], w2[i], w3[i]);
+                tmem_st16(trow + c::kA + c0 / 2, w1);
+                tmem_st16(trow + c::kA + 64 + c0 / 2, w2);
+                tmem_st16(trow + c::kA + 128 + c0 / 2, w3);
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.kv_ready);
+        }
+        for (int j = 0; j < nchunk; ++j) {
+            const int s = j & 1;
+            const bool full = (ms.list[j / kPerTile] >> 16) & 1u;
+            const int q0 = chunk_q0(j);
+            if (!f32_warp_wait(&ms.s_full[s], (uint32_t)(j >> 1) & 1u, abort_flag) ||
+                !f32_warp_wait(&ms.st_full[s][R::kRowGrp], (uint32_t)(j >> 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            const float *rows_s = reinterpret_cast<const float *>(stage(s) + R::kStRows);
+            const uint32_t bc = c::buf_col<ROLE>(s);
+            if (ROLE == 0) {
+                uint32_t sr[32], dr[32];
+                f32_ld32(trow + bc, sr);
+                f32_ld32(trow + bc + 32, dr);
+                float dsv[32];
+#pragma unroll
+                for (int cc = 0; cc < 32; ++cc) {
+                    const int q = q0 + cc;
+                    const float lse = rows_s[cc];
+                    const bool keep = lse != -INFINITY && (full || (kv < p.kv_len && mask_mod(p.mask, b, q, kv)));
+                    float grad;
+                    const float x = score_t<SCORE>(p.score_param, __uint_as_float(sr[cc]) * scale, slope, q, kv, grad);
+                    const float pr = keep ? ex2_approx(fmaf(x, kLog2e, -lse * kLog2e)) : 0.f;
+                    dsv[cc] = keep ? scale * pr * (__uint_as_float(dr[cc]) - rows_s[32 + cc]) * grad : 0.f;
+                }
+                uint32_t w1[16], w2[16], w3[16];
+#pragma unroll
+                for (int cc = 0; cc < 16; ++cc) split3(dsv[2 * cc], dsv[2 * cc + 1], w1[cc], w2[cc], w3[cc]);
+                tmem_st16(trow + bc + 32, w1);  // over dP^T and S^T, all read above
+                tmem_st16(trow + bc + 48, w2);
+                tmem_st16(trow + bc, w3);
+            } else {
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t sr[32];
+                    f32_ld32(trow + bc + 32 * half, sr);
+                    float pv[32];
+#pragma unroll
+                    for (int cc = 0; cc < 32; ++cc) {
+                        const int q = q0 + 32 * half + cc;
+                        const float lse = rows_s[32 * half + cc];
+                        const bool keep = lse != -INFINITY && (full || (kv < p.kv_len && mask_mod(p.mask, b, q, kv)));
+                        float grad;
+                        const float x =
+                            score_t<SCORE>(p.score_param, __uint_as_float(sr[cc]) * scale, slope, q, kv, grad);
+                        pv[cc] = keep ? ex2_approx(fmaf(x, kLog2e, -lse * kLog2e)) : 0.f;
+                    }
+                    uint32_t w1[16], w2[16], w3[16];
+#pragma unroll
+                    for (int cc = 0; cc < 16; ++cc) split3(pv[2 * cc], pv[2 * cc + 1], w1[cc], w2[cc], w3[cc]);
+                    // over S^T columns 32 half .. 32 half + 31, all read above
+                    tmem_st16(trow + bc + 32 * half, w1);
+                    tmem_st16(trow + bc + 32 * half + 16, w2);
+                    tmem_st16(trow + bc + 64 + 16 * half, w3);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ms.p_full[s]);
+        }
+        // ------------------------------------------------------------ epilogue
+        const bool have = ok && nchunk > 0;
+        if (have && !f32_warp_wait(&ms.acc_full, 0, abort_flag)) ok = false;
+        if (!ok) fail(ms, p.status);
+        if (ok) {
+            tc_fence_after_sync();
+            const int64_t orow = (int64_t)bh * p.kv_len + (kv < p.kv_len ? kv : 0);
+            float *dst = (ROLE == 0 ? a.dk : a.dv) + orow * c::D;
+#pragma unroll 1
+            for (int c0 = 0; c0 < c::D; c0 += 32) {  // every lane takes the warp-collective loads
+                uint32_t r[32];
+                if (have) {
+                    f32_ld32(trow + c::kAcc + c0, r);
+                } else {
+#pragma unroll
+                    for (int cc = 0; cc < 32; ++cc) r[cc] = 0u;
+                }
+                if (kv < p.kv_len) {
+#pragma unroll
+                    for (int cc = 0; cc < 32; cc += 4)
+                        *reinterpret_cast<float4 *>(dst + c0 + cc) =
+                            make_float4(__uint_as_float(r[cc]), __uint_as_float(r[cc + 1]),
+                                        __uint_as_float(r[cc + 2]), __uint_as_float(r[cc + 3]));
+                }
+            }
+        }
+    }
+}
 
 template <int SCORE>
 __global__ void __launch_bounds__(16 * 32, 1) dkdv128_kernel(AttnProblem p, BwdF32TcArgs a) {
-    namespace c = d128kv;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Misc &ms = *reinterpret_cast<Misc *>(smem + c::kMiscOff);
+    Misc &ms = *reinterpret_cast<Misc *>(smem + d128kv::kMiscOff);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int kvb = (int)blockIdx.x / 2, dh = (int)blockIdx.x & 1;  // kv block, half of dK and dV
-    const int bh = p.bh_begin + (int)blockIdx.y, h = bh % p.H, b = bh / p.H;
-    const int kv0 = kvb * kBlock;
+    const int kvb = (int)blockIdx.x / 2, role = (int)blockIdx.x & 1;  // role 0: dK, role 1: dV
+    const int bh = p.bh_begin + (int)blockIdx.y;
 
     if (threadIdx.x == 0) {
-        mbar_init(&ms.kv_ready, 8);  // K resident (Q group) and V in TMEM (elementwise warps)
+        // role 0: K resident (Q group) and V in TMEM (elementwise warps); role 1: K in TMEM
+        mbar_init(&ms.kv_ready, role == 0 ? 8 : 4);
         for (int i = 0; i < 2; ++i) {
             for (int g = 0; g < 2; ++g) {
                 mbar_init(&ms.st_full[i][g], 4);
@@ -1149,248 +1475,18 @@ __global__ void __launch_bounds__(16 * 32, 1) dkdv128_kernel(AttnProblem p, BwdF
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    const uint32_t tmem = ms.tmem_base;
-    volatile int *abort_flag = &ms.abort;
-    const int nchunk = 4 * ms.ntiles;  // four 32-row chunks per q tile
-    auto chunk_q0 = [&](int j) { return (int)(ms.list[j / 4] & 0xFFFFu) * kBlock + (j % 4) * c::kQr; };
-    const int qi = q_index(warp), di = do_index(warp);
 
-    if (qi >= 0 || di >= 0) {
-        // ----------------------------------------------------------- producers
-        const int lt = 32 * (qi >= 0 ? qi : di) + lane, grp = qi >= 0 ? 0 : 1;
-        if (grp == 0 && nchunk > 0) {
-            // the resident K: two 64-row halves of the 128-row tile
-            const float *kbase = static_cast<const float *>(p.k) + b * p.k_stride[0] + h * p.k_stride[1];
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                d128::Rows64 g;
-                d128::load64(g, kbase, p.k_stride[2], kv0 + 64 * half, p.kv_len, lt);
-                d128::store64(smem + c::kK0, c::kKPart, c::kKAtom, 64 * half, g, lt);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ms.kv_ready);
-        }
-        const float *base = grp == 0 ? static_cast<const float *>(p.q) + b * p.q_stride[0] + h * p.q_stride[1]
-                                     : a.dout + (int64_t)bh * p.q_len * c::D;
-        const int64_t rs = grp == 0 ? p.q_stride[2] : c::D;
-        const float *rowv_base = (grp == 0 ? p.lse : a.delta) + (int64_t)bh * p.q_len;
-        bool ok = true;
-        for (int j = 0; j < nchunk; ++j) {
-            const int s = j & 1;
-            const int q0 = chunk_q0(j);
-            c::Rows32 g;
-            c::load32(g, base, rs, q0, p.q_len, lt);
-            float rowv = 0.f;
-            if (lt < c::kQr) {
-                const int q = q0 + lt;
-                rowv = q < p.q_len ? rowv_base[q] : (grp == 0 ? -INFINITY : 0.f);
-            }
-            if (j >= 2 && !f32_warp_wait(&ms.st_empty[s][grp], (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
-                ok = false;
-                break;
-            }
-            uint8_t *st = smem + c::kSt0 + s * c::kStBytes;
-            c::store32(st + (grp == 0 ? c::kStQ : c::kStDo), g, lt);
-            if (lt < c::kQr) reinterpret_cast<float *>(st + (grp == 0 ? c::kStLse : c::kStDelta))[lt] = rowv;
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ms.st_full[s][grp]);
-        }
-        if (!ok) fail(ms, p.status);
-    } else if (warp == kMmaWarp) {
-        // ----------------------------------------------------------------- MMA
-        if (lane == 0 && nchunk > 0) {
-            constexpr uint32_t kHi = smem_desc_hi_sw128(1024);
-            constexpr uint32_t idesc_kmaj = idesc_bf16_f32(128, c::kQr, 0, 0);  // S^T, dP^T: N = 32 q
-            constexpr uint32_t idesc_mn = idesc_bf16_f32(128, 64, 0, 1);       // dV_h, dK_h: N = 64, B MN-major
-            auto pa = [](int t) { return t == 2 || t == 4 ? 1 : t == 5 ? 2 : 0; };
-            auto pbp = [](int t) { return t == 1 || t == 4 ? 1 : t == 3 ? 2 : 0; };
-            const uint32_t kd = smem_desc_lo(smem_u32(smem + c::kK0), 16);
-            // dP^T(j) = V dO^T (A: V parts in TMEM), then S^T(j) = K Q^T (A: K
-            // parts in shared memory); K steps of 16 head dims
-            auto issue_sdp = [&](int j) -> bool {
-                const int s = j & 1;
-                const uint32_t st = smem_u32(smem + c::kSt0 + s * c::kStBytes);
-                const uint32_t qd = smem_desc_lo(st + c::kStQ, 16), gd = smem_desc_lo(st + c::kStDo, 16);
-                if (!mbar_wait(&ms.st_full[s][1], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
-                tc_fence_after_sync();
-#pragma unroll
-                for (int k = 0; k < c::D / 16; ++k)
-#pragma unroll
-                    for (int t = 0; t < 6; ++t)
-                        mma_ts_lo<kHi>(tmem + c::buf_col(s) + 32, tmem + c::kVcol + 64 * pa(t) + 8 * k,
-                                       gd + ((pbp(t) * c::kCPart + (k / 4) * c::kCAtom + (k % 4) * 32) >> 4),
-                                       idesc_kmaj, (k > 0 || t > 0) ? 1u : 0u);
-                if (!mbar_wait(&ms.st_full[s][0], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
-                tc_fence_after_sync();
-#pragma unroll
-                for (int k = 0; k < c::D / 16; ++k)
-#pragma unroll
-                    for (int t = 0; t < 6; ++t)
-                        mma_ss_lo<kHi, kHi>(tmem + c::buf_col(s),
-                                            kd + ((pa(t) * c::kKPart + (k / 4) * c::kKAtom + (k % 4) * 32) >> 4),
-                                            qd + ((pbp(t) * c::kCPart + (k / 4) * c::kCAtom + (k % 4) * 32) >> 4),
-                                            idesc_kmaj, (k > 0 || t > 0) ? 1u : 0u);
-                mma_commit(&ms.s_full[s]);
-                return true;
-            };
-            // dV_h += P^T dO[:, h], then dK_h += dS^T Q[:, h] (B MN-major: the
-            // half's 64-wide atom, K steps of 16 q rows = 2048 bytes)
-            auto issue_acc = [&](int j) -> bool {
-                const int s = j & 1;
-                if (!mbar_wait(&ms.p_full[s], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
-                tc_fence_after_sync();
-                const uint32_t st = smem_u32(smem + c::kSt0 + s * c::kStBytes);
-                const uint32_t qm = smem_desc_lo(st + c::kStQ + dh * c::kCAtom, c::kCAtom);
-                const uint32_t gm = smem_desc_lo(st + c::kStDo + dh * c::kCAtom, c::kCAtom);
-                const uint32_t bc = c::buf_col(s);
-#pragma unroll
-                for (int k = 0; k < c::kQr / 16; ++k)
-#pragma unroll
-                    for (int t = 0; t < 6; ++t) {
-                        const int ap = pa(t);
-                        const uint32_t pcol = ap < 2 ? bc + 16u * ap + 8u * k : bc + 64u + 8u * k;
-                        mma_ts_lo<kHi>(tmem + c::kDv, tmem + pcol, gm + ((pbp(t) * c::kCPart + k * 2048) >> 4),
-                                       idesc_mn, (j > 0 || k > 0 || t > 0) ? 1u : 0u);
-                    }
-                mma_commit(&ms.st_empty[s][1]);
-#pragma unroll
-                for (int k = 0; k < c::kQr / 16; ++k)
-#pragma unroll
-                    for (int t = 0; t < 6; ++t) {
-                        const int ap = pa(t);
-                        const uint32_t dcol = ap < 2 ? bc + 32u + 16u * ap + 8u * k : bc + 80u + 8u * k;
-                        mma_ts_lo<kHi>(tmem + c::kDk, tmem + dcol, qm + ((pbp(t) * c::kCPart + k * 2048) >> 4),
-                                       idesc_mn, (j > 0 || k > 0 || t > 0) ? 1u : 0u);
-                    }
-                mma_commit(&ms.st_empty[s][0]);
-                return true;
-            };
-            bool ok = mbar_wait(&ms.kv_ready, 0, abort_flag);
-            if (ok) tc_fence_after_sync();
-            for (int j = 0; ok && j < min(nchunk, 2); ++j) ok = issue_sdp(j);
-            // S^T(j + 2) reuses the buffer dV(j), dK(j) read: MMAs of one thread run in order
-            for (int j = 0; ok && j < nchunk; ++j) ok = issue_acc(j) && (j + 2 >= nchunk || issue_sdp(j + 2));
-            if (ok) mma_commit(&ms.acc_full);
-            if (!ok) fail(ms, p.status);
-            mma_commit(&ms.drain);
-            int never = 0;
-            (void)mbar_wait(&ms.drain, 0, &never);
-        }
-        __syncwarp();
-    } else if (warp < 4) {
-        // ---------------------------------------------------------- elementwise
-        const int kv = kv0 + (int)threadIdx.x;
-        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-        const float slope = SCORE == FLEX_SCORE_ALIBI ? exp2f(-8.f * (float)(h + 1) / (float)p.H) : 0.f;
-        const float scale = p.scale;
-        bool ok = true;
-        if (nchunk > 0) {
-            // this kv row of V -> V1, V2, V3 columns of this lane (bf16 pairs)
-            const bool kv_in = kv < p.kv_len;
-            const float *vrow = static_cast<const float *>(p.v) + b * p.v_stride[0] + h * p.v_stride[1] +
-                                (int64_t)(kv_in ? kv : 0) * p.v_stride[2];
-#pragma unroll 1
-            for (int c0 = 0; c0 < c::D; c0 += 32) {
-                float4 x[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    x[j] = kv_in ? __ldg(reinterpret_cast<const float4 *>(vrow + c0) + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-                uint32_t w1[16], w2[16], w3[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    split3(f4_at(x[j / 2], 2 * (j % 2)), f4_at(x[j / 2], 2 * (j % 2) + 1), w1[j], w2[j], w3[j]);
-                tmem_st16(trow + c::kVcol + c0 / 2, w1);
-                tmem_st16(trow + c::kVcol + 64 + c0 / 2, w2);
-                tmem_st16(trow + c::kVcol + 128 + c0 / 2, w3);
-            }
-            tmem_wait_st();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ms.kv_ready);
-        }
-        for (int j = 0; j < nchunk; ++j) {
-            const int s = j & 1;
-            const bool full = (ms.list[j / 4] >> 16) & 1u;
-            const int q0 = chunk_q0(j);
-            if (!f32_warp_wait(&ms.s_full[s], (uint32_t)(j >> 1) & 1u, abort_flag) ||
-                !f32_warp_wait(&ms.st_full[s][0], (uint32_t)(j >> 1) & 1u, abort_flag) ||
-                !f32_warp_wait(&ms.st_full[s][1], (uint32_t)(j >> 1) & 1u, abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after_sync();
-            const float *lse_s = reinterpret_cast<const float *>(smem + c::kSt0 + s * c::kStBytes + c::kStLse);
-            const float *dl_s = reinterpret_cast<const float *>(smem + c::kSt0 + s * c::kStBytes + c::kStDelta);
-            uint32_t sr[32], dr[32];
-            f32_ld32(trow + c::buf_col(s), sr);
-            f32_ld32(trow + c::buf_col(s) + 32, dr);
-            float pv[32], dsv[32];
-#pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-                const int q = q0 + cc;
-                const float lse = lse_s[cc];
-                const bool keep = lse != -INFINITY && (full || (kv < p.kv_len && mask_mod(p.mask, b, q, kv)));
-                float grad;
-                const float x = score_t<SCORE>(p.score_param, __uint_as_float(sr[cc]) * scale, slope, q, kv, grad);
-                const float pr = keep ? ex2_approx(fmaf(x, kLog2e, -lse * kLog2e)) : 0.f;
-                pv[cc] = pr;
-                dsv[cc] = keep ? scale * pr * (__uint_as_float(dr[cc]) - dl_s[cc]) * grad : 0.f;
-            }
-            uint32_t w1[16], w2[16], w3[16];
-#pragma unroll
-            for (int cc = 0; cc < 16; ++cc) split3(pv[2 * cc], pv[2 * cc + 1], w1[cc], w2[cc], w3[cc]);
-            tmem_st16(trow + c::buf_col(s), w1);        // over S^T, all read above
-            tmem_st16(trow + c::buf_col(s) + 16, w2);
-            tmem_st16(trow + c::buf_col(s) + 64, w3);
-#pragma unroll
-            for (int cc = 0; cc < 16; ++cc) split3(dsv[2 * cc], dsv[2 * cc + 1], w1[cc], w2[cc], w3[cc]);
-            tmem_st16(trow + c::buf_col(s) + 32, w1);   // over dP^T, all read above
-            tmem_st16(trow + c::buf_col(s) + 48, w2);
-            tmem_st16(trow + c::buf_col(s) + 80, w3);
-            tmem_wait_st();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ms.p_full[s]);
-        }
-        // ------------------------------------------------------------ epilogue
-        const bool have = ok && nchunk > 0;
-        if (have && !f32_warp_wait(&ms.acc_full, 0, abort_flag)) ok = false;
-        if (!ok) fail(ms, p.status);
-        if (ok) {
-            tc_fence_after_sync();
-            const int64_t orow = (int64_t)bh * p.kv_len + (kv < p.kv_len ? kv : 0);
-#pragma unroll 1
-            for (int o = 0; o < 2; ++o) {  // dV_h, then dK_h
-                float *dst = (o ? a.dk : a.dv) + orow * c::D + 64 * dh;
-#pragma unroll 1
-                for (int c0 = 0; c0 < 64; c0 += 32) {  // every lane takes the warp-collective loads
-                    uint32_t r[32];
-                    if (have) {
-                        f32_ld32(trow + (o ? c::kDk : c::kDv) + c0, r);
-                    } else {
-#pragma unroll
-                        for (int cc = 0; cc < 32; ++cc) r[cc] = 0u;
-                    }
-                    if (kv < p.kv_len) {
-#pragma unroll
-                        for (int cc = 0; cc < 32; cc += 4)
-                            *reinterpret_cast<float4 *>(dst + c0 + cc) =
-                                make_float4(__uint_as_float(r[cc]), __uint_as_float(r[cc + 1]),
-                                            __uint_as_float(r[cc + 2]), __uint_as_float(r[cc + 3]));
-                    }
-                }
-            }
-        }
-    }
+    if (role == 0)
+        dkdv128_role<SCORE, 0>(p, a, smem, ms, kvb, bh, warp, lane);
+    else
+        dkdv128_role<SCORE, 1>(p, a, smem, ms, kvb, bh, warp, lane);
 
     // ------------------------------------------------------------ teardown
     tc_fence_before_sync();
     __syncthreads();
     if (warp == kMmaWarp) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(ms.tmem_base, kTmemCols);
     }
 }
 
@@ -1402,7 +1498,7 @@ inline cudaError_t launch_bwd_fp32_tc_dkdv(const AttnProblem &p, const BwdF32TcA
     using namespace bwdf32;
     const bool d64 = p.D == 64;
     const size_t smem = d64 ? kSmemBytes : d128kv::kSmemBytes;
-    // D = 128: two CTAs per kv block, one per half of dK and dV
+    // D = 128: two CTAs per kv block, one for dK and one for dV
     const unsigned gx = (unsigned)p.nkvt * (d64 ? 1u : 2u);
     auto pick = [&](auto kern) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
