@@ -181,8 +181,11 @@ __global__ void __launch_bounds__(16 * 32, 1) dkdv_kernel(AttnProblem p, BwdF32T
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Misc &ms = *reinterpret_cast<Misc *>(smem + kMiscOff);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int kvb = blockIdx.x;
-    const int bh = p.bh_begin + (int)blockIdx.y, h = bh % p.H, b = bh / p.H;
+    // (b, h) pairs along x, kv blocks along y (at most 1024): the first CTAs
+    // to run are the kv blocks that come first in every pair (the longest q
+    // sides of a causal mask)
+    const int kvb = blockIdx.y;
+    const int bh = p.bh_begin + (int)blockIdx.x, h = bh % p.H, b = bh / p.H;
     const int kv0 = kvb * kBlock;
 
     if (threadIdx.x == 0) {
@@ -468,14 +471,16 @@ constexpr size_t kDqSmemBytes = kDqMiscOff + sizeof(Misc) + 1024;
 static_assert(kDqSmemBytes <= 232448, "shared memory per CTA");
 
 template <int SCORE>
-__global__ void __launch_bounds__(16 * 32, 1) dq_kernel(AttnProblem p, BwdF32TcArgs a) {
+__global__ void __launch_bounds__(16 * 32, 1) dq_kernel(AttnProblem p, BwdF32TcArgs a, int bh_x) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Misc &ms = *reinterpret_cast<Misc *>(smem + kDqMiscOff);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     // longest first: under a causal mask the last q blocks list the most kv tiles
-    const int qb = p.nqt - 1 - (int)blockIdx.x;
-    const int bh = p.bh_begin + (int)blockIdx.y, h = bh % p.H, b = bh / p.H;
+    // (b, h) pairs along x and q tiles (longest first) along y when they fit
+    // grid.y, so that the first CTAs to run are the longest of every pair
+    const int qb = p.nqt - 1 - (int)(bh_x ? blockIdx.y : blockIdx.x);
+    const int bh = p.bh_begin + (int)(bh_x ? blockIdx.x : blockIdx.y), h = bh % p.H, b = bh / p.H;
     const int q0 = qb * kBlock;
 
     if (threadIdx.x == 0) {
@@ -772,14 +777,16 @@ __device__ __forceinline__ void store64(uint8_t *dst, uint32_t part_bytes, uint3
 }  // namespace d128
 
 template <int SCORE>
-__global__ void __launch_bounds__(16 * 32, 1) dq128_kernel(AttnProblem p, BwdF32TcArgs a) {
+__global__ void __launch_bounds__(16 * 32, 1) dq128_kernel(AttnProblem p, BwdF32TcArgs a, int bh_x) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Misc &ms = *reinterpret_cast<Misc *>(smem + d128::kMiscOff);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     // longest first: under a causal mask the last q blocks list the most kv tiles
-    const int qb = p.nqt - 1 - (int)blockIdx.x;
-    const int bh = p.bh_begin + (int)blockIdx.y, h = bh % p.H, b = bh / p.H;
+    // (b, h) pairs along x and q tiles (longest first) along y when they fit
+    // grid.y, so that the first CTAs to run are the longest of every pair
+    const int qb = p.nqt - 1 - (int)(bh_x ? blockIdx.y : blockIdx.x);
+    const int bh = p.bh_begin + (int)(bh_x ? blockIdx.x : blockIdx.y), h = bh % p.H, b = bh / p.H;
     const int q0 = qb * kBlock;
 
     // kv_ready: dO resident (4 dO-group warps) and Q in TMEM (4 elementwise
@@ -1430,8 +1437,8 @@ __global__ void __launch_bounds__(16 * 32, 1) dkdv128_kernel(AttnProblem p, BwdF
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Misc &ms = *reinterpret_cast<Misc *>(smem + d128kv::kMiscOff);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int kvb = (int)blockIdx.x / 2, role = (int)blockIdx.x & 1;  // role 0: dK, role 1: dV
-    const int bh = p.bh_begin + (int)blockIdx.y;
+    const int kvb = (int)blockIdx.y / 2, role = (int)blockIdx.y & 1;  // role 0: dK, role 1: dV
+    const int bh = p.bh_begin + (int)blockIdx.x;
 
     if (threadIdx.x == 0) {
         // role 0: K resident (Q group) and V in TMEM (elementwise warps); role 1: K in TMEM
@@ -1499,7 +1506,8 @@ inline cudaError_t launch_bwd_fp32_tc_dkdv(const AttnProblem &p, const BwdF32TcA
     const bool d64 = p.D == 64;
     const size_t smem = d64 ? kSmemBytes : d128kv::kSmemBytes;
     // D = 128: two CTAs per kv block, one for dK and one for dV
-    const unsigned gx = (unsigned)p.nkvt * (d64 ? 1u : 2u);
+    const unsigned gy = (unsigned)p.nkvt * (d64 ? 1u : 2u);
+    static_assert(2 * kMaxKvBlocks <= 65535, "kv blocks along grid.y");
     auto pick = [&](auto kern) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -1507,7 +1515,7 @@ inline cudaError_t launch_bwd_fp32_tc_dkdv(const AttnProblem &p, const BwdF32TcA
             AttnProblem part = p;
             part.bh_begin = begin;
             const int count = p.B * p.H - begin < 65535 ? p.B * p.H - begin : 65535;
-            kern<<<dim3(gx, count), kThreads, smem, stream>>>(part, a);
+            kern<<<dim3(count, gy), kThreads, smem, stream>>>(part, a);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
         return cudaSuccess;
@@ -1526,6 +1534,7 @@ inline cudaError_t launch_bwd_fp32_tc_dkdv(const AttnProblem &p, const BwdF32TcA
 inline cudaError_t launch_bwd_fp32_tc_dq(const AttnProblem &p, const BwdF32TcArgs &a, cudaStream_t stream) {
     using namespace bwdf32;
     const size_t smem = p.D == 64 ? kDqSmemBytes : d128::kSmemBytes;
+    const bool bh_x = p.nqt <= 65535;
     auto pick = [&](auto kern) -> cudaError_t {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -1533,7 +1542,10 @@ inline cudaError_t launch_bwd_fp32_tc_dq(const AttnProblem &p, const BwdF32TcArg
             AttnProblem part = p;
             part.bh_begin = begin;
             const int count = p.B * p.H - begin < 65535 ? p.B * p.H - begin : 65535;
-            kern<<<dim3(p.nqt, count), kThreads, smem, stream>>>(part, a);
+            if (bh_x)
+                kern<<<dim3(count, p.nqt), kThreads, smem, stream>>>(part, a, 1);
+            else
+                kern<<<dim3(p.nqt, count), kThreads, smem, stream>>>(part, a, 0);
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
         }
         return cudaSuccess;
