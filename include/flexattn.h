@@ -382,8 +382,8 @@ FLEX_API int flex_block_mask_transpose(const flex_block_mask *bm, flex_block_mas
  * MMAs with fp32 accumulation; P and dS rounded to bf16 as MMA operands) and
  * need Q_LEN <= 262144 (2048 tiles of 128 rows); fp32 inputs keep float32
  * accuracy on the tensor cores (each operand split into three bf16 parts,
- * six MMAs per product), except dk and dv at D = 128 (and of q sides longer
- * than 2048 tiles), computed in fp32 on the CUDA cores.  Errors: those of
+ * six MMAs per product), except dk and dv of q sides longer than 2048
+ * tiles, computed in fp32 on the CUDA cores.  Errors: those of
  * flex_attention_fwd, FLEX_ERR_SHAPE when
  * bq does not match bm, and FLEX_ERR_UNSUPPORTED for bf16 with Q_LEN >
  * 262144.  Asynchronous on `stream`.
