@@ -1,6 +1,7 @@
 // Host side of the bf16 tensor-core attention: TMA tensor maps for Q, K, V
 // (4-D [B, H, S, D] views with 64 x 128 boxes and 128-byte swizzle) and
 // dispatch on head dim and score kind.
+#include <algorithm>
 #include <mutex>
 
 #include "attn_bf16_launch.cuh"
@@ -58,6 +59,16 @@ cudaError_t launch_attn_bf16(const AttnProblem &p, cudaStream_t stream) {
     kp.npairs = (p.nqt + 1) / 2;
     kp.bh_begin = p.bh_begin;
     kp.nbh = p.bh_count;
+    // (b, h) pairs scheduled together: as many as keep their K and V within
+    // 64 MB of L2 (at least kHeadGroup), so that with small heads the longest
+    // items of more heads run first and fewer short ones are left at the end
+    // of the grid (measured: causal + prefix B4 H16 S4096 D64 -7%, document +
+    // softcap B8 H16 S8192 D128 -8%; 8 heads of S16384 D128 as fast as 4)
+    {
+        const int64_t kv_bytes = 4 * (int64_t)p.kv_len * p.D;  // K and V of one (b, h), bf16
+        const int64_t fit = (int64_t(64) << 20) / kv_bytes;
+        kp.head_group = (int)std::max<int64_t>(kHeadGroup, std::min<int64_t>(fit, p.bh_count));
+    }
     kp.lists = TileLists{p.kv_num, p.kv_idx, p.full_num, p.full_idx, p.nqb, p.nkvb, p.q_block, p.kv_block, p.nkvt};
     kp.mask = p.mask;
     // PRESCALE_QK moves the scale onto Q (in shared memory); the scores then take 1

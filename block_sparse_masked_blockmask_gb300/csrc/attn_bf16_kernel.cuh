@@ -69,7 +69,7 @@ constexpr int kSchedWarp = 11; // work items: union lists, Q loads, next item by
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kHeadGroup = 4;              // (batch, head) pairs scheduled together
+constexpr int kHeadGroup = 4;              // fewest (batch, head) pairs scheduled together
 constexpr float kRescaleThreshold = 8.0f;  // raise the running max only beyond 2^8
 // P_i is handed to the MMA warp whole (one mbarrier per tile), not in column
 // chunks: the thread that issues the MMAs spends ~46 cycles issuing each
@@ -91,6 +91,7 @@ static_assert(2 * kRegsSoftmax + kRegsControl == 3 * kRegsAtLaunch, "register sp
 struct Bf16Params {
     int B, H, q_len, kv_len, nqt, nkvt, npairs;  // nqt, nkvt: 128-tiles along q and kv
     int bh_begin, nbh;  // the (b, h) pairs b * H + h in [bh_begin, bh_begin + nbh) are computed
+    int head_group;     // (b, h) pairs scheduled together (at least kHeadGroup)
     TileLists lists;    // the BlockMask's kv side (any Q_BLOCK, KV_BLOCK), read as 128-tiles
     MaskDesc mask;
     float scale, score_param;
@@ -358,15 +359,15 @@ __device__ __forceinline__ void apply_document_mask(int q, int kv0, int doc_q, c
 }
 
 // Decode work item `item` (a CTA index of the launch grid): heads in groups of
-// kHeadGroup (their K/V stay in L2 while in flight); inside a group, q-block
+// p.head_group (their K/V stay in L2 while in flight); inside a group, q-block
 // pairs from the last (the longest kv lists for causal-like masks) to the
 // first, the group's heads innermost, so the heaviest items of each group come
 // first and the last items of the grid are light.
 __device__ __forceinline__ void decode_item(const Bf16Params &p, int item, int &b, int &h, int &qb0, int &has1) {
     const int nbh = p.nbh;
-    const int group_items = kHeadGroup * p.npairs;
-    const int g0 = (item / group_items) * kHeadGroup;
-    const int gsize = min(kHeadGroup, nbh - g0);
+    const int group_items = p.head_group * p.npairs;
+    const int g0 = (item / group_items) * p.head_group;
+    const int gsize = min(p.head_group, nbh - g0);
     const int r = item - (item / group_items) * group_items;
     const int pair = p.npairs - 1 - r / gsize;
     const int bh = p.bh_begin + g0 + r % gsize;
