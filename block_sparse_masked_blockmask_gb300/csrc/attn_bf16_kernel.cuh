@@ -408,11 +408,24 @@ __device__ __forceinline__ void build_item(const Bf16Params &p, AttnMisc &ms, It
             int jj[4][kUnroll];
 #pragma unroll
             for (int r = 0; r < kUnroll; ++r) {
+                // the first chunk is read whole (every entry below nkvb lies
+                // in its row), so its loads do not wait for the counts and a
+                // short list costs one memory latency; entries past a count
+                // are dropped below
                 const int x = base + 32 * r + lane;
-                jj[0][r] = x < np0 ? __ldg(pidx + x) : -1;
-                jj[1][r] = x < nf0 ? __ldg(fidx + x) : -1;
-                jj[2][r] = x < np1 ? __ldg(pidx + nkvb + x) : -1;
-                jj[3][r] = x < nf1 ? __ldg(fidx + nkvb + x) : -1;
+                const bool any = base == 0 && x < nkvb;
+                jj[0][r] = x < np0 || any ? __ldg(pidx + x) : -1;
+                jj[1][r] = x < nf0 || any ? __ldg(fidx + x) : -1;
+                jj[2][r] = x < np1 || (any && has1) ? __ldg(pidx + nkvb + x) : -1;
+                jj[3][r] = x < nf1 || (any && has1) ? __ldg(fidx + nkvb + x) : -1;
+            }
+#pragma unroll
+            for (int r = 0; r < kUnroll; ++r) {
+                const int x = base + 32 * r + lane;
+                if (x >= np0) jj[0][r] = -1;
+                if (x >= nf0) jj[1][r] = -1;
+                if (x >= np1) jj[2][r] = -1;
+                if (x >= nf1) jj[3][r] = -1;
             }
             constexpr uint32_t kBits[4] = {1u, 3u, 4u, 12u};  // present / full, tile 0 then tile 1
 #pragma unroll

@@ -87,29 +87,41 @@ __device__ __forceinline__ void tl_mark_entry(const TileLists &L, int wb, bool f
 // tile `ot` of (b, h) pair `bh` as own slot u into words[t - tlo] (zeroed by
 // the caller).  Counts are clamped to [0, walk_nb] and entries outside
 // [0, walk_nb) are dropped, so a malformed BlockMask never writes outside
-// words.  The index loads of a chunk are all issued before any is used.
+// words.  The index loads of a chunk are all issued before any is used, and
+// those of a row's first chunk together with its counts (every entry below
+// walk_nb lies in the row; entries past a count are dropped), so a short list
+// costs one memory latency.
 __device__ __forceinline__ void tl_mark_warp(const TileLists &L, int64_t bh, int ot, int u, uint32_t *words,
                                              int tlo, int thi, int lane) {
     int r0, r1;
     tl_rows(L, ot, r0, r1);
+    constexpr int kUnroll = 2;
     for (int r = r0; r < r1; ++r) {
         const int64_t row = bh * L.own_nb + r;
+        const int32_t *pi = L.idx + row * L.walk_nb, *fi = L.fidx + row * L.walk_nb;
+        int jp[kUnroll], jf[kUnroll];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            const int x = 32 * k + lane;
+            jp[k] = x < L.walk_nb ? __ldg(pi + x) : -1;
+            jf[k] = x < L.walk_nb ? __ldg(fi + x) : -1;
+        }
         const int np = min(max(__ldg(L.num + row), 0), L.walk_nb);
         const int nf = min(max(__ldg(L.fnum + row), 0), L.walk_nb);
-        const int32_t *pi = L.idx + row * L.walk_nb, *fi = L.fidx + row * L.walk_nb;
-        constexpr int kUnroll = 2;
         for (int base = 0; base < max(np, nf); base += 32 * kUnroll) {
-            int jp[kUnroll], jf[kUnroll];
+            if (base > 0) {
 #pragma unroll
-            for (int k = 0; k < kUnroll; ++k) {
-                const int x = base + 32 * k + lane;
-                jp[k] = x < np ? __ldg(pi + x) : -1;
-                jf[k] = x < nf ? __ldg(fi + x) : -1;
+                for (int k = 0; k < kUnroll; ++k) {
+                    const int x = base + 32 * k + lane;
+                    jp[k] = x < np ? __ldg(pi + x) : -1;
+                    jf[k] = x < nf ? __ldg(fi + x) : -1;
+                }
             }
 #pragma unroll
             for (int k = 0; k < kUnroll; ++k) {
-                tl_mark_entry(L, jp[k], false, u, words, tlo, thi);
-                tl_mark_entry(L, jf[k], true, u, words, tlo, thi);
+                const int x = base + 32 * k + lane;
+                tl_mark_entry(L, x < np ? jp[k] : -1, false, u, words, tlo, thi);
+                tl_mark_entry(L, x < nf ? jf[k] : -1, true, u, words, tlo, thi);
             }
         }
     }
