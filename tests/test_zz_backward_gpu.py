@@ -146,6 +146,25 @@ def test_backward_medium_fp32(D):
     _compare(got, ref, "fp32", f"medium fp32 D{D}")
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_backward_fp32_long_q_side(D):
+    # more than 2048 q tiles (Q_LEN 262400, KV_LEN 1024): dK/dV take the
+    # CUDA-core kernels, dQ the tensor cores.  Sliding window 256: q row i
+    # sees keys i - 255 .. i, so rows from 1279 on see none, and the exact
+    # gradients are those of the first 1280 q rows alone (the oracle's)
+    # with dq = 0 past them
+    B, H, Sq, Skv, Sc, W_ = 1, 1, 262400, 1024, 1280, 256
+    q, k, v = W.draw_qkv(B, H, Sc, D, seed=37, dtype="fp32", S_kv=Skv)
+    g = W.draw_qkv(B, H, Sc, D, seed=38, dtype="fp32")[0]
+    rng = np.random.default_rng(39)
+    pad = lambda x: np.concatenate([x, rng.standard_normal((B, H, Sq - Sc, D), dtype=np.float32)], axis=2)
+    got = _backward(pad(q), k, v, pad(g), W.MASK_SLIDING_WINDOW, W.SCORE_IDENTITY, 1.0 / np.sqrt(D), "fp32",
+                    window=W_)
+    ref = oracle.attention_bwd(q, k, v, g, W.MASK_SLIDING_WINDOW, W.SCORE_IDENTITY, 1.0 / np.sqrt(D), window=W_)
+    assert np.all(got[0][:, :, Sc:] == 0.0), "dq past the last row with keys"
+    _compare([got[0][:, :, :Sc], got[1], got[2]], ref, "fp32", f"long q side D{D}")
+
+
 def test_backward_at_scale():
     # the headline shape's sequence length (causal + ALiBi, S = 16384, two
     # heads): dq on sampled rows against the oracle (a row's dq needs only
