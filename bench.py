@@ -245,7 +245,7 @@ def main():
                     help="launches per kernel-option variant (OUTPUT_MAX, PRESCALE_QK, ...); 0 skips them")
     ap.add_argument("--backward-steps", type=int, default=5,
                     help="timed flex_attention_bwd launches on the same workload; 0 skips them")
-    ap.add_argument("--config-steps", type=int, default=20,
+    ap.add_argument("--config-steps", type=int, default=50,
                     help="timed attention launches on each of the five synthetic configurations; 0 skips them")
     ap.add_argument("--fp32-steps", type=int, default=10,
                     help="timed float32 launches at B1 H16 S4096 (D = 64, 128); 0 skips them")
@@ -279,10 +279,11 @@ def prepare_device_inputs(torch, w: W.Workload):
 def config_timings(fa, torch, device_index: int, steps: int, peaks: dict) -> dict | None:
     """Attention-kernel throughput on every synthetic configuration (outside the headline's timed region).
 
-    Per configuration: the BlockMask is built once, then `steps` attention
-    launches are timed one by one with CUDA events on the launching stream,
-    L2 flushed before each launch when the inputs fit in L2, clocks sampled
-    while they run.  TFLOP/s counts unmasked-block FLOPs.
+    Per configuration: the BlockMask is built once, 10 untimed launches, then
+    `steps` attention launches are timed one by one with CUDA events on the
+    launching stream, L2 flushed before each launch when the inputs fit in L2,
+    clocks sampled while they run.  TFLOP/s counts unmasked-block FLOPs over
+    the median launch time (the mean is reported beside it).
     """
     if steps <= 0:
         return None
@@ -301,7 +302,7 @@ def config_timings(fa, torch, device_index: int, steps: int, peaks: dict) -> dic
         def launch():
             fa.flex_attention_fwd(dq, dk, dv, bm, w.score, w.score_param, w.scale, out=out, lse=lse, stream=stream)
 
-        for _ in range(3):
+        for _ in range(10):
             launch()
         torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
@@ -316,10 +317,10 @@ def config_timings(fa, torch, device_index: int, steps: int, peaks: dict) -> dic
         if fa.flex_device_status() != fa.FLEX_OK:
             raise RuntimeError(f"device status reported a timeout on {w.name}")
         ms = [a.elapsed_time(b) for a, b in ev]
-        mean = float(np.mean(ms))
-        tflops = flops / (mean * 1e-3) / 1e12
+        mean, median = float(np.mean(ms)), float(np.median(ms))
+        tflops = flops / (median * 1e-3) / 1e12
         res[w.name] = {"dtype": w.dtype, "unmasked_block_flops": flops, "attn_ms_mean": mean,
-                       "attn_ms_median": float(np.median(ms)), "tflops": tflops,
+                       "attn_ms_median": median, "tflops": tflops, "tflops_of_mean": flops / (mean * 1e-3) / 1e12,
                        "frac_of_measured_bf16_peak": tflops / peaks["bf16"],
                        "frac_of_spec_bf16_peak": tflops / SPEC_BF16_TFLOPS,
                        "kernel": "attn_bf16_kernel" if w.dtype == "bf16" else "attn_fp32_kernel (three-way bf16 split, tcgen05)",
