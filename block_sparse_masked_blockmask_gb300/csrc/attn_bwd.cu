@@ -466,11 +466,16 @@ constexpr int kSideDevices = 64;
 std::mutex g_side_mutex;
 BwdSide *g_side[kSideDevices] = {nullptr};
 
-BwdSide *bwd_side() {
+// The side stream of the current device, created on first use; while
+// `stream` is being captured, only one that already exists (creating
+// streams and events is not among the calls a capture may record).
+BwdSide *bwd_side(cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kSideDevices) return nullptr;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return nullptr;
     std::lock_guard<std::mutex> lock(g_side_mutex);
-    if (!g_side[dev]) {
+    if (!g_side[dev] && cap == cudaStreamCaptureStatusNone) {
         BwdSide *b = new BwdSide();
         if (cudaStreamCreateWithFlags(&b->s2, cudaStreamNonBlocking) != cudaSuccess ||
             cudaEventCreateWithFlags(&b->fork, cudaEventDisableTiming) != cudaSuccess ||
@@ -482,11 +487,16 @@ BwdSide *bwd_side() {
 }
 
 // dK/dV on `stream`, dQ on the side stream between a fork after the work
-// already on `stream` (delta) and a join back into `stream`.
+// already on `stream` (delta) and a join back into `stream`; both on
+// `stream`, one after the other, when there is no side stream.
 template <class DkDv, class Dq>
 cudaError_t launch_dkdv_dq(cudaStream_t stream, DkDv &&dkdv, Dq &&dq) {
-    BwdSide *side = bwd_side();
-    if (!side) return cudaErrorInitializationError;
+    BwdSide *side = bwd_side(stream);
+    if (!side) {
+        cudaGetLastError();  // a failed capture-status query leaves nothing to report
+        const cudaError_t e = dkdv(stream);
+        return e != cudaSuccess ? e : dq(stream);
+    }
     std::lock_guard<std::mutex> lock(side->enqueue);
     cudaError_t e;
     if ((e = cudaEventRecord(side->fork, stream)) != cudaSuccess ||

@@ -387,11 +387,13 @@ FLEX_API int flex_block_mask_transpose(const flex_block_mask *bm, flex_block_mas
  * flex_attention_fwd, FLEX_ERR_SHAPE when
  * bq does not match bm, and FLEX_ERR_UNSUPPORTED for bf16 with Q_LEN >
  * 262144.  Asynchronous on `stream`: dq is computed on a library stream
- * (created once per device) that forks from `stream` after the work already
- * queued there and joins it again, so that its kernel fills the SMs the
- * dk/dv kernel leaves idle; the call stays ordered on `stream` like any
- * other, also under stream capture.  Calls from several host threads on one
- * device enqueue one at a time.
+ * (created by the first call on a device that is not made during a stream
+ * capture) that forks from `stream` after the work already queued there and
+ * joins it again, so that its kernel fills the SMs the dk/dv kernel leaves
+ * idle; without that stream dq follows dk and dv on `stream`.  Either way
+ * the call stays ordered on `stream` like any other, also under stream
+ * capture.  Calls from several host threads on one device enqueue one at a
+ * time.
  */
 FLEX_API int flex_attention_bwd(const flex_tensor *q, const flex_tensor *k, const flex_tensor *v, const void *out,
                                 const float *lse, const void *dout, const flex_block_mask *bm,

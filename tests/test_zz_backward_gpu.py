@@ -165,6 +165,32 @@ def test_backward_fp32_long_q_side(D):
     _compare([got[0][:, :, :Sc], got[1], got[2]], ref, "fp32", f"long q side D{D}")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_backward_under_graph_capture(dtype):
+    # flex_attention_bwd recorded into a CUDA graph (dq on the library's side
+    # stream, forked from and joined into the captured stream) and replayed
+    # gives the eager call's gradients bit for bit
+    B, H, S, D = 1, 2, 512, 64
+    q, k, v, g = _draw(B, H, S, S, D, 40, dtype)
+    dq_, dk_, dv_, dg = (device_tensor(x, dtype) for x in (q, k, v, g))
+    bm = gpu_block_mask(W.MASK_CAUSAL, B, H, S, S, 0, 0, None)
+    bq = fa.flex_block_mask_transpose(bm)
+    out, lse = fa.flex_attention_fwd(dq_, dk_, dv_, bm, W.SCORE_ALIBI, 0.0, 0.125)
+    eager = [x.clone() for x in fa.flex_attention_bwd(dq_, dk_, dv_, out, lse, dg, bm, bq, W.SCORE_ALIBI, 0.0, 0.125)]
+    torch.cuda.synchronize()
+    grads = [torch.full_like(x, float("nan")) for x in eager]
+    delta = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fa.flex_attention_bwd(dq_, dk_, dv_, out, lse, dg, bm, bq, W.SCORE_ALIBI, 0.0, 0.125,
+                              dq=grads[0], dk=grads[1], dv=grads[2], delta=delta)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert fa.flex_device_status() == fa.FLEX_OK
+    for name, a, e in zip(("dq", "dk", "dv"), grads, eager):
+        assert torch.equal(a, e), f"{dtype} {name}: replay differs from the eager call"
+
+
 def test_backward_at_scale():
     # the headline shape's sequence length (causal + ALiBi, S = 16384, two
     # heads): dq on sampled rows against the oracle (a row's dq needs only
