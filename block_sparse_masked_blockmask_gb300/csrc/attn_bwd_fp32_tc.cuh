@@ -1044,110 +1044,57 @@ __global__ void __launch_bounds__(16 * 32, 1) dq128_kernel(AttnProblem p, BwdF32
 }
 
 // dK and dV at D = 128: two CTAs per 128-row kv block, so that each holds
-// one accumulator of all 128 columns and only the products it needs.
+// one accumulator of all 128 columns and only the products it needs; both
+// walk the q side in chunks of 64 rows.
 //   role 0 (dK): S^T = K Q^T (K parts resident in shared memory), dP^T = V
 //     dO^T (V parts the A operand from tensor memory), dS^T elementwise and
-//     dK += dS^T Q, over the q side in chunks of 32 rows;
+//     dK += dS^T Q.  One ring stage (the resident K leaves room for no
+//     second); three 64-column TMEM slots: S^T of every chunk in slot X,
+//     dP^T in Y and Z by turns, so that dP^T of the next chunk is issued
+//     while the elementwise warps work on this one (its dO half frees as
+//     soon as this chunk's dP^T is done).  The dS^T parts go over dP^T and
+//     the first half of each 32-column half of S^T.
 //   role 1 (dV): S^T = K Q^T (K parts the A operand from tensor memory), P^T
-//     elementwise and dV += P^T dO, in chunks of 64 q rows; it needs neither
-//     dP^T nor delta.
+//     elementwise and dV += P^T dO, through a two-stage ring; it needs
+//     neither dP^T nor delta.  Two buffers of S^T (64) | P3 (32), P1 and P2
+//     over S^T.
 // Tensor memory (512 columns): A parts (V or K: 3 x 64) | accumulator (128) |
-// two buffers: role 0 S^T (32) | dP^T (32), the dS^T parts over dP^T and the
-// first half of S^T; role 1 S^T (64) | P3 (32), P1 and P2 over S^T.
-// The row values of a chunk (lse, delta) travel with the half of its ring
-// stage that is freed last: the Q half in role 0 (read by dK), the dO half
-// in role 1 (read by dV); the other half is freed as soon as its one MMA
-// group has read it.
+// 192 columns of slots or buffers.  The row values of a chunk (lse, delta)
+// travel with the half of its ring stage that is freed last: the Q half in
+// role 0 (read by dK), the dO half in role 1 (read by dV).
 namespace d128kv {
 constexpr int D = 128;
+constexpr int kQr = 64;                          // q rows per chunk
 constexpr uint32_t kA = 0, kAcc = 192;
-constexpr uint32_t kKPart = 128 * D * 2;  // 32 KB: one part of role 0's resident K (two 64-wide atoms)
-constexpr uint32_t kKAtom = 128 * 128;    // 128 rows x 64 bf16
+constexpr uint32_t kKPart = 128 * D * 2;         // 32 KB: one part of role 0's resident K (two 64-wide atoms)
+constexpr uint32_t kKAtom = 128 * 128;           // 128 rows x 64 bf16
+constexpr uint32_t kCPart = kQr * D * 2;         // 16 KB: one part of a 64-row Q or dO chunk
+constexpr uint32_t kCAtom = kQr * 128;           // 64 rows x 64 bf16
+constexpr uint32_t kStQ = 0, kStDo = 3 * kCPart, kStRows = 6 * kCPart;  // rows: role 0 lse[64], delta[64]; role 1 lse[64]
+constexpr uint32_t kStBytes = 6 * kCPart + 1024;
 template <int ROLE>
 struct Role;
 template <>
 struct Role<0> {
-    static constexpr int kQr = 32;                                 // q rows per chunk
-    static constexpr uint32_t kCPart = kQr * D * 2, kCAtom = kQr * 128;
-    static constexpr uint32_t kSt0 = 3 * kKPart;                   // after the resident K
-    static constexpr uint32_t kStQ = 0, kStDo = 3 * kCPart, kStRows = 6 * kCPart;  // rows: lse[32], delta[32]
-    static constexpr uint32_t kStBytes = 6 * kCPart + 1024;
-    static constexpr uint32_t kBufCols = 64;
-    static constexpr int kRowGrp = 0, kRowVals = 64;
+    static constexpr uint32_t kSt0 = 3 * kKPart;  // after the resident K
+    static constexpr int kStages = 1, kRowGrp = 0, kRowVals = 128;
 };
 template <>
 struct Role<1> {
-    static constexpr int kQr = 64;
-    static constexpr uint32_t kCPart = kQr * D * 2, kCAtom = kQr * 128;
     static constexpr uint32_t kSt0 = 0;
-    static constexpr uint32_t kStQ = 0, kStDo = 3 * kCPart, kStRows = 6 * kCPart;  // rows: lse[64]
-    static constexpr uint32_t kStBytes = 6 * kCPart + 1024;
-    static constexpr uint32_t kBufCols = 96;
-    static constexpr int kRowGrp = 1, kRowVals = 64;
+    static constexpr int kStages = 2, kRowGrp = 1, kRowVals = 64;
 };
-template <int ROLE>
-__host__ __device__ constexpr uint32_t buf_col(int b) { return 320u + Role<ROLE>::kBufCols * (uint32_t)b; }
-constexpr uint32_t kMiscOff = 3 * kKPart + 2 * Role<0>::kStBytes;
-static_assert(kMiscOff == 2 * Role<1>::kStBytes, "both roles place Misc at one offset");
+// role 0: slot X holds S^T, dP^T alternates between Y and Z
+constexpr uint32_t kSlotX = 320;
+__host__ __device__ constexpr uint32_t dp_slot(int j) { return 384u + 64u * (uint32_t)(j & 1); }
+// role 1: S^T (64) | P3 (32) buffers
+__host__ __device__ constexpr uint32_t s_buf(int b) { return 320u + 96u * (uint32_t)b; }
+constexpr uint32_t kMiscOff = 2 * kStBytes;
+static_assert(Role<0>::kSt0 + kStBytes <= kMiscOff, "role 0's shared memory");
 constexpr size_t kSmemBytes = kMiscOff + sizeof(Misc) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-static_assert(buf_col<0>(2) <= kTmemCols && buf_col<1>(2) == kTmemCols, "tensor memory");
-static_assert(Role<0>::kStBytes % 1024 == 0 && Role<1>::kStBytes % 1024 == 0 && (3 * kKPart) % 1024 == 0,
-              "ring alignment");
-
-// 32 rows r0 .. r0 + 31 of a [.., len, 128] float32 tensor into registers
-// (zeros past len), then split into a 32-row tile (atoms of 32 rows x 128
-// bytes).  Thread lt (0..127) takes units i = lt + 128 u: row i / 16, 8
-// floats at column 8 (i % 16).
-struct Rows32 {
-    float4 x[8];
-};
-__device__ __forceinline__ void load32(Rows32 &g, const float *src, int64_t rs, int r0, int len, int lt) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int i = lt + 128 * u, r = i / 16, c = i % 16;
-        const bool in = r0 + r < len;
-        const float4 *p = reinterpret_cast<const float4 *>(src + (int64_t)(in ? r0 + r : 0) * rs) + 2 * c;
-        g.x[2 * u] = in ? __ldg(p) : make_float4(0.f, 0.f, 0.f, 0.f);
-        g.x[2 * u + 1] = in ? __ldg(p + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-}
-__device__ __forceinline__ void store32(uint8_t *dst, const Rows32 &g, int lt) {
-    constexpr uint32_t kPart = Role<0>::kCPart;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int i = lt + 128 * u, r = i / 16, c = i % 16;
-        uint4 p1, p2, p3;
-        split3(g.x[2 * u].x, g.x[2 * u].y, p1.x, p2.x, p3.x);
-        split3(g.x[2 * u].z, g.x[2 * u].w, p1.y, p2.y, p3.y);
-        split3(g.x[2 * u + 1].x, g.x[2 * u + 1].y, p1.z, p2.z, p3.z);
-        split3(g.x[2 * u + 1].z, g.x[2 * u + 1].w, p1.w, p2.w, p3.w);
-        const uint32_t off = sw128_chunk(r, c, Role<0>::kCAtom);
-        *reinterpret_cast<uint4 *>(dst + off) = p1;
-        *reinterpret_cast<uint4 *>(dst + kPart + off) = p2;
-        *reinterpret_cast<uint4 *>(dst + 2 * kPart + off) = p3;
-    }
-}
-// The rows of a chunk into registers, then into the ring (role 0: 32 rows,
-// role 1: 64 rows, both with atoms of the chunk's rows x 128 bytes).
-template <int ROLE>
-struct Chunk {
-    Rows32 g;
-    __device__ __forceinline__ void load(const float *src, int64_t rs, int r0, int len, int lt) {
-        load32(g, src, rs, r0, len, lt);
-    }
-    __device__ __forceinline__ void store(uint8_t *dst, int lt) const { store32(dst, g, lt); }
-};
-template <>
-struct Chunk<1> {
-    d128::Rows64 g;
-    __device__ __forceinline__ void load(const float *src, int64_t rs, int r0, int len, int lt) {
-        d128::load64(g, src, rs, r0, len, lt);
-    }
-    __device__ __forceinline__ void store(uint8_t *dst, int lt) const {
-        d128::store64(dst, Role<1>::kCPart, Role<1>::kCAtom, 0, g, lt);
-    }
-};
+static_assert(dp_slot(1) + 64 == kTmemCols && s_buf(1) + 96 == kTmemCols, "tensor memory");
+static_assert(Role<0>::kSt0 % 1024 == 0 && kStBytes % 1024 == 0, "ring alignment");
 }  // namespace d128kv
 
 template <int SCORE, int ROLE>
@@ -1159,10 +1106,13 @@ __device__ __forceinline__ void dkdv128_role(const AttnProblem &p, const BwdF32T
     const int kv0 = kvb * kBlock;
     const uint32_t tmem = ms.tmem_base;
     volatile int *abort_flag = &ms.abort;
-    constexpr int kPerTile = kBlock / R::kQr;
+    constexpr int kPerTile = kBlock / c::kQr;
     const int nchunk = kPerTile * ms.ntiles;
-    auto chunk_q0 = [&](int j) { return (int)(ms.list[j / kPerTile] & 0xFFFFu) * kBlock + (j % kPerTile) * R::kQr; };
-    auto stage = [&](int s) { return smem + R::kSt0 + s * R::kStBytes; };
+    auto chunk_q0 = [&](int j) { return (int)(ms.list[j / kPerTile] & 0xFFFFu) * kBlock + (j % kPerTile) * c::kQr; };
+    // ring stage of chunk j and the parity of its n-th use
+    auto stage_of = [](int j) { return R::kStages == 1 ? 0 : (j & 1); };
+    auto use_of = [](int j) { return R::kStages == 1 ? j : (j >> 1); };
+    auto stage = [&](int s) { return smem + R::kSt0 + s * c::kStBytes; };
     const int qi = q_index(warp), di = do_index(warp);
 
     if (qi >= 0 || di >= 0) {
@@ -1188,23 +1138,25 @@ __device__ __forceinline__ void dkdv128_role(const AttnProblem &p, const BwdF32T
         const bool rows = grp == R::kRowGrp && lt < R::kRowVals;
         bool ok = true;
         for (int j = 0; j < nchunk; ++j) {
-            const int s = j & 1;
+            const int s = stage_of(j);
             const int q0 = chunk_q0(j);
-            c::Chunk<ROLE> g;
-            g.load(base, rs, q0, p.q_len, lt);
-            // role 0: lse of rows 0-31, then delta; role 1: lse of rows 0-63
+            // this chunk's rows (and its row values) into registers, then the slot
+            d128::Rows64 g;
+            d128::load64(g, base, rs, q0, p.q_len, lt);
+            // role 0: lse of rows 0-63, then their delta; role 1: lse of rows 0-63
             float rowv = 0.f;
             if (rows) {
-                const bool is_lse = ROLE == 1 || lt < 32;
-                const int q = q0 + (is_lse ? lt : lt - 32);
+                const bool is_lse = lt < 64;
+                const int q = q0 + (is_lse ? lt : lt - 64);
                 rowv = q < p.q_len ? (is_lse ? lse_g[q] : delta_g[q]) : (is_lse ? -INFINITY : 0.f);
             }
-            if (j >= 2 && !f32_warp_wait(&ms.st_empty[s][grp], (uint32_t)((j >> 1) - 1) & 1u, abort_flag)) {
+            if (j >= R::kStages &&
+                !f32_warp_wait(&ms.st_empty[s][grp], (uint32_t)(use_of(j) - 1) & 1u, abort_flag)) {
                 ok = false;
                 break;
             }
-            g.store(stage(s) + (grp == 0 ? R::kStQ : R::kStDo), lt);
-            if (rows) reinterpret_cast<float *>(stage(s) + R::kStRows)[lt] = rowv;
+            d128::store64(stage(s) + (grp == 0 ? c::kStQ : c::kStDo), c::kCPart, c::kCAtom, 0, g, lt);
+            if (rows) reinterpret_cast<float *>(stage(s) + c::kStRows)[lt] = rowv;
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ms.st_full[s][grp]);
@@ -1214,44 +1166,31 @@ __device__ __forceinline__ void dkdv128_role(const AttnProblem &p, const BwdF32T
         // ----------------------------------------------------------------- MMA
         if (lane == 0 && nchunk > 0) {
             constexpr uint32_t kHi = smem_desc_hi_sw128(1024);
-            constexpr uint32_t idesc_kmaj = idesc_bf16_f32(128, R::kQr, 0, 0);  // S^T, dP^T: N = chunk rows
+            constexpr uint32_t idesc_kmaj = idesc_bf16_f32(128, c::kQr, 0, 0);  // S^T, dP^T: N = 64 q rows
             constexpr uint32_t idesc_mn = idesc_bf16_f32(128, c::D, 0, 1);      // dK, dV: N = 128, B MN-major
             auto pa = [](int t) { return t == 2 || t == 4 ? 1 : t == 5 ? 2 : 0; };
             auto pbp = [](int t) { return t == 1 || t == 4 ? 1 : t == 3 ? 2 : 0; };
-            // The K steps stay rolled loops: unrolled, the issue code of the
-            // MMAs no longer fits the instruction cache beside the other roles'
-            // (measured: the issue rate and the elementwise warps both slowed).
-            // K-major B of a chunk (rows = q), part pt, K step k of 16 head dims
-            auto kstep = [](int pt, int k) {
-                return (pt * R::kCPart + (k / 4) * R::kCAtom + (k % 4) * 32) >> 4;
-            };
-            // role 0: dP^T(j) = V dO^T, free the dO half, then S^T(j) = K Q^T
-            // role 1: S^T(j) = K Q^T, free the Q half
-            auto issue_s = [&](int j) -> bool {
-                const int s = j & 1;
-                const uint32_t st = smem_u32(stage(s));
-                const uint32_t qd = smem_desc_lo(st + R::kStQ, 16);
-                if (ROLE == 0) {
-                    const uint32_t gd = smem_desc_lo(st + R::kStDo, 16);
-                    if (!mbar_wait(&ms.st_full[s][1], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
-                    tc_fence_after_sync();
-#pragma unroll 1
-                    for (int k = 0; k < c::D / 16; ++k)
-#pragma unroll
-                        for (int t = 0; t < 6; ++t)
-                            mma_ts_lo<kHi>(tmem + c::buf_col<ROLE>(s) + 32, tmem + c::kA + 64 * pa(t) + 8 * k,
-                                           gd + kstep(pbp(t), k), idesc_kmaj, (k > 0 || t > 0) ? 1u : 0u);
-                    mma_commit(&ms.st_empty[s][1]);
-                }
-                if (!mbar_wait(&ms.st_full[s][0], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+            // The K-step loops that issue MMAs stay rolled loops: unrolled,
+            // the issue code no longer fits the instruction cache beside the
+            // other roles' (measured: the issue rate and the elementwise warps
+            // both slowed).  K-major B of a chunk (rows = q), part pt, K step
+            // k of 16 head dims:
+            auto kstep = [](int pt, int k) { return (pt * c::kCPart + (k / 4) * c::kCAtom + (k % 4) * 32) >> 4; };
+            // S^T(j) = K Q^T into `dcol`: role 0 with K parts in shared
+            // memory (SS), role 1 with K parts in TMEM (TS); frees nothing
+            // (role 1 frees the Q half after it)
+            auto issue_s = [&](int j, uint32_t dcol) -> bool {
+                const int s = stage_of(j);
+                if (!mbar_wait(&ms.st_full[s][0], (uint32_t)use_of(j) & 1u, abort_flag)) return false;
                 tc_fence_after_sync();
+                const uint32_t qd = smem_desc_lo(smem_u32(stage(s)) + c::kStQ, 16);
                 if (ROLE == 0) {
                     const uint32_t kd = smem_desc_lo(smem_u32(smem), 16);
 #pragma unroll 1
                     for (int k = 0; k < c::D / 16; ++k)
 #pragma unroll
                         for (int t = 0; t < 6; ++t)
-                            mma_ss_lo<kHi, kHi>(tmem + c::buf_col<ROLE>(s),
+                            mma_ss_lo<kHi, kHi>(tmem + dcol,
                                                 kd + ((pa(t) * c::kKPart + (k / 4) * c::kKAtom + (k % 4) * 32) >> 4),
                                                 qd + kstep(pbp(t), k), idesc_kmaj, (k > 0 || t > 0) ? 1u : 0u);
                 } else {
@@ -1259,35 +1198,48 @@ __device__ __forceinline__ void dkdv128_role(const AttnProblem &p, const BwdF32T
                     for (int k = 0; k < c::D / 16; ++k)
 #pragma unroll
                         for (int t = 0; t < 6; ++t)
-                            mma_ts_lo<kHi>(tmem + c::buf_col<ROLE>(s), tmem + c::kA + 64 * pa(t) + 8 * k,
-                                           qd + kstep(pbp(t), k), idesc_kmaj, (k > 0 || t > 0) ? 1u : 0u);
+                            mma_ts_lo<kHi>(tmem + dcol, tmem + c::kA + 64 * pa(t) + 8 * k, qd + kstep(pbp(t), k),
+                                           idesc_kmaj, (k > 0 || t > 0) ? 1u : 0u);
                     mma_commit(&ms.st_empty[s][0]);
                 }
-                mma_commit(&ms.s_full[s]);
+                mma_commit(&ms.s_full[ROLE == 0 ? 0 : s]);
+                return true;
+            };
+            // role 0: dP^T(j) = V dO^T into its slot, then the dO half is free
+            auto issue_dp = [&](int j) -> bool {
+                if (!mbar_wait(&ms.st_full[0][1], (uint32_t)j & 1u, abort_flag)) return false;
+                tc_fence_after_sync();
+                const uint32_t gd = smem_desc_lo(smem_u32(stage(0)) + c::kStDo, 16);
+#pragma unroll 1
+                for (int k = 0; k < c::D / 16; ++k)
+#pragma unroll
+                    for (int t = 0; t < 6; ++t)
+                        mma_ts_lo<kHi>(tmem + c::dp_slot(j), tmem + c::kA + 64 * pa(t) + 8 * k, gd + kstep(pbp(t), k),
+                                       idesc_kmaj, (k > 0 || t > 0) ? 1u : 0u);
+                mma_commit(&ms.st_empty[0][1]);
                 return true;
             };
             // role 0: dK += dS^T Q; role 1: dV += P^T dO (B MN-major: two
             // 64-wide slabs one atom apart, K steps of 16 q rows = 2048 bytes)
             auto issue_acc = [&](int j) -> bool {
-                const int s = j & 1;
-                if (!mbar_wait(&ms.p_full[s], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
-                if (ROLE == 1 && !mbar_wait(&ms.st_full[s][1], (uint32_t)(j >> 1) & 1u, abort_flag)) return false;
+                const int s = stage_of(j);
+                const int pb = ROLE == 0 ? 0 : s;
+                if (!mbar_wait(&ms.p_full[pb], (uint32_t)use_of(j) & 1u, abort_flag)) return false;
+                if (ROLE == 1 && !mbar_wait(&ms.st_full[s][1], (uint32_t)use_of(j) & 1u, abort_flag)) return false;
                 tc_fence_after_sync();
-                const uint32_t bm =
-                    smem_desc_lo(smem_u32(stage(s)) + (ROLE == 0 ? R::kStQ : R::kStDo), R::kCAtom);
-                const uint32_t bc = c::buf_col<ROLE>(s);
+                const uint32_t bm = smem_desc_lo(smem_u32(stage(s)) + (ROLE == 0 ? c::kStQ : c::kStDo), c::kCAtom);
 #pragma unroll 1
-                for (int k = 0; k < R::kQr / 16; ++k)
+                for (int k = 0; k < c::kQr / 16; ++k)
 #pragma unroll
                     for (int t = 0; t < 6; ++t) {
-                        const int ap = pa(t);
-                        // role 0: dS1, dS2 over dP^T, dS3 over S^T; role 1: P1, P2
-                        // over S^T columns 32 (k / 2) .., P3 in the spare columns
+                        const uint32_t ap = (uint32_t)pa(t), h32 = 32u * (uint32_t)(k / 2), o8 = 8u * (uint32_t)(k % 2);
+                        // role 0: dS1, dS2 over dP^T, dS3 over the S^T slot;
+                        // role 1: P1, P2 over S^T, P3 in the spare columns
                         const uint32_t col =
-                            ROLE == 0 ? (ap < 2 ? bc + 32u + 16u * ap + 8u * k : bc + 8u * k)
-                                      : (ap < 2 ? bc + 32u * (k / 2) + 16u * ap + 8u * (k % 2)
-                                                : bc + 64u + 16u * (k / 2) + 8u * (k % 2));
-                        mma_ts_lo<kHi>(tmem + c::kAcc, tmem + col, bm + ((pbp(t) * R::kCPart + k * 2048) >> 4),
+                            ROLE == 0 ? (ap < 2 ? c::dp_slot(j) + h32 + 16u * ap + o8 : c::kSlotX + h32 + o8)
+                                      : (ap < 2 ? c::s_buf(s) + h32 + 16u * ap + o8
+                                                : c::s_buf(s) + 64u + 16u * (uint32_t)(k / 2) + o8);
+                        mma_ts_lo<kHi>(tmem + c::kAcc, tmem + col, bm + ((pbp(t) * c::kCPart + k * 2048) >> 4),
                                        idesc_mn, (j > 0 || k > 0 || t > 0) ? 1u : 0u);
                     }
                 mma_commit(&ms.st_empty[s][ROLE == 0 ? 0 : 1]);
@@ -1295,9 +1247,20 @@ __device__ __forceinline__ void dkdv128_role(const AttnProblem &p, const BwdF32T
             };
             bool ok = mbar_wait(&ms.kv_ready, 0, abort_flag);
             if (ok) tc_fence_after_sync();
-            for (int j = 0; ok && j < min(nchunk, 2); ++j) ok = issue_s(j);
-            // S^T(j + 2) reuses the buffer acc(j) read: MMAs of one thread run in order
-            for (int j = 0; ok && j < nchunk; ++j) ok = issue_acc(j) && (j + 2 >= nchunk || issue_s(j + 2));
+            if (ROLE == 0) {
+                // dP^T(0), S^T(0); then per chunk dP^T(j + 1) (its slot was
+                // last read by dK(j - 1), issued earlier), dK(j), S^T(j + 1)
+                // over the slot dK(j) read: MMAs of one thread run in order
+                ok = ok && issue_dp(0) && issue_s(0, c::kSlotX);
+                for (int j = 0; ok && j < nchunk; ++j)
+                    ok = (j + 1 >= nchunk || issue_dp(j + 1)) && issue_acc(j) &&
+                         (j + 1 >= nchunk || issue_s(j + 1, c::kSlotX));
+            } else {
+                for (int j = 0; ok && j < min(nchunk, 2); ++j) ok = issue_s(j, c::s_buf(j & 1));
+                // S^T(j + 2) reuses the buffer dV(j) read: MMAs of one thread run in order
+                for (int j = 0; ok && j < nchunk; ++j)
+                    ok = issue_acc(j) && (j + 2 >= nchunk || issue_s(j + 2, c::s_buf(j & 1)));
+            }
             if (ok) mma_commit(&ms.acc_full);
             if (!ok) fail(ms, p.status);
             mma_commit(&ms.drain);  // every MMA issued above completes before TMEM is freed
@@ -1340,43 +1303,48 @@ __device__ __forceinline__ void dkdv128_role(const AttnProblem &p, const BwdF32T
             if (lane == 0) mbar_arrive(&ms.kv_ready);
         }
         for (int j = 0; j < nchunk; ++j) {
-            const int s = j & 1;
+            const int s = stage_of(j);
             const bool full = (ms.list[j / kPerTile] >> 16) & 1u;
             const int q0 = chunk_q0(j);
-            if (!f32_warp_wait(&ms.s_full[s], (uint32_t)(j >> 1) & 1u, abort_flag) ||
-                !f32_warp_wait(&ms.st_full[s][R::kRowGrp], (uint32_t)(j >> 1) & 1u, abort_flag)) {
+            // S^T (and in role 0 dP^T, issued before it) are in TMEM; the row
+            // values (written by the producers) are read after their own barrier
+            if (!f32_warp_wait(&ms.s_full[ROLE == 0 ? 0 : s], (uint32_t)use_of(j) & 1u, abort_flag) ||
+                !f32_warp_wait(&ms.st_full[s][R::kRowGrp], (uint32_t)use_of(j) & 1u, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after_sync();
-            const float *rows_s = reinterpret_cast<const float *>(stage(s) + R::kStRows);
-            const uint32_t bc = c::buf_col<ROLE>(s);
-            if (ROLE == 0) {
-                uint32_t sr[32], dr[32];
-                f32_ld32(trow + bc, sr);
-                f32_ld32(trow + bc + 32, dr);
-                float dsv[32];
-#pragma unroll
-                for (int cc = 0; cc < 32; ++cc) {
-                    const int q = q0 + cc;
-                    const float lse = rows_s[cc];
-                    const bool keep = lse != -INFINITY && (full || (kv < p.kv_len && mask_mod(p.mask, b, q, kv)));
-                    float grad;
-                    const float x = score_t<SCORE>(p.score_param, __uint_as_float(sr[cc]) * scale, slope, q, kv, grad);
-                    const float pr = keep ? ex2_approx(fmaf(x, kLog2e, -lse * kLog2e)) : 0.f;
-                    dsv[cc] = keep ? scale * pr * (__uint_as_float(dr[cc]) - rows_s[32 + cc]) * grad : 0.f;
-                }
-                uint32_t w1[16], w2[16], w3[16];
-#pragma unroll
-                for (int cc = 0; cc < 16; ++cc) split3(dsv[2 * cc], dsv[2 * cc + 1], w1[cc], w2[cc], w3[cc]);
-                tmem_st16(trow + bc + 32, w1);  // over dP^T and S^T, all read above
-                tmem_st16(trow + bc + 48, w2);
-                tmem_st16(trow + bc, w3);
-            } else {
+            const float *rows_s = reinterpret_cast<const float *>(stage(s) + c::kStRows);
 #pragma unroll 1
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t sr[32];
-                    f32_ld32(trow + bc + 32 * half, sr);
+            for (int half = 0; half < 2; ++half) {
+                const uint32_t scol = ROLE == 0 ? c::kSlotX + 32u * half : c::s_buf(s) + 32u * half;
+                uint32_t sr[32];
+                f32_ld32(trow + scol, sr);
+                if (ROLE == 0) {
+                    const uint32_t dcol = c::dp_slot(j) + 32u * half;
+                    uint32_t dr[32];
+                    f32_ld32(trow + dcol, dr);
+                    float dsv[32];
+#pragma unroll
+                    for (int cc = 0; cc < 32; ++cc) {
+                        const int q = q0 + 32 * half + cc;
+                        const float lse = rows_s[32 * half + cc];
+                        const bool keep = lse != -INFINITY && (full || (kv < p.kv_len && mask_mod(p.mask, b, q, kv)));
+                        float grad;
+                        const float x =
+                            score_t<SCORE>(p.score_param, __uint_as_float(sr[cc]) * scale, slope, q, kv, grad);
+                        const float pr = keep ? ex2_approx(fmaf(x, kLog2e, -lse * kLog2e)) : 0.f;
+                        dsv[cc] = keep ? scale * pr * (__uint_as_float(dr[cc]) - rows_s[64 + 32 * half + cc]) * grad
+                                       : 0.f;
+                    }
+                    uint32_t w1[16], w2[16], w3[16];
+#pragma unroll
+                    for (int cc = 0; cc < 16; ++cc) split3(dsv[2 * cc], dsv[2 * cc + 1], w1[cc], w2[cc], w3[cc]);
+                    // over this half's dP^T and S^T columns, all read above
+                    tmem_st16(trow + dcol, w1);
+                    tmem_st16(trow + dcol + 16, w2);
+                    tmem_st16(trow + scol, w3);
+                } else {
                     float pv[32];
 #pragma unroll
                     for (int cc = 0; cc < 32; ++cc) {
@@ -1392,15 +1360,15 @@ __device__ __forceinline__ void dkdv128_role(const AttnProblem &p, const BwdF32T
 #pragma unroll
                     for (int cc = 0; cc < 16; ++cc) split3(pv[2 * cc], pv[2 * cc + 1], w1[cc], w2[cc], w3[cc]);
                     // over S^T columns 32 half .. 32 half + 31, all read above
-                    tmem_st16(trow + bc + 32 * half, w1);
-                    tmem_st16(trow + bc + 32 * half + 16, w2);
-                    tmem_st16(trow + bc + 64 + 16 * half, w3);
+                    tmem_st16(trow + scol, w1);
+                    tmem_st16(trow + scol + 16, w2);
+                    tmem_st16(trow + c::s_buf(s) + 64 + 16 * half, w3);
                 }
             }
             tmem_wait_st();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ms.p_full[s]);
+            if (lane == 0) mbar_arrive(&ms.p_full[ROLE == 0 ? 0 : s]);
         }
         // ------------------------------------------------------------ epilogue
         const bool have = ok && nchunk > 0;
