@@ -1,10 +1,12 @@
 // Backward pass of the block-sparse attention (the flex_attention_backward op
 // of "[Inductor][Flex Attention] Add Subtiling Option for Alpha Scaling",
 // PyTorch PR #167356, test diffs: it takes q, k, v, the forward's out and lse,
-// and the output gradient, and returns dq, dk, dv).  fp32 inputs run on the
-// CUDA cores with fp32 arithmetic (the kernels below); bf16 inputs take delta
-// from the kernel below and dq, dk, dv from the tensor-core kernels of
-// attn_bwd_tc.cuh.
+// and the output gradient, and returns dq, dk, dv).  Both dtypes take delta
+// from the kernel below; bf16 inputs take dq, dk, dv from the tensor-core
+// kernels of attn_bwd_tc.cuh, fp32 inputs from those of attn_bwd_fp32_tc.cuh
+// (three-way bf16 split), except dk and dv of q sides longer than
+// kBwdF32TcMaxQTiles tiles, which take the register-tiled CUDA-core kernels
+// below.  The dq kernel runs on a side stream beside the dk/dv kernel.
 //
 // With t = scale q.k, s = score_mod(t) where mask_mod holds, P = exp(s - lse):
 //   delta_i = dO_i . out_i
@@ -17,7 +19,7 @@
 // forward does.  P is recomputed from the saved lse in both, so nothing is
 // accumulated across CTAs.  A fourth kernel transposes the kv-side lists.
 //
-// The fp32 dK/dV and dQ kernels are register-tiled on the CUDA cores: a CTA
+// The CUDA-core fp32 dK/dV and dQ kernels are register-tiled: a CTA
 // of 256 threads holds its 64 owned rows of two tensors in shared memory
 // and walks the other side in steps of 64 rows (two tiles of 64 x D).  Per
 // step a thread computes a 4 x 4 patch of the two 64 x 64 products over D
